@@ -1,0 +1,238 @@
+/*
+ * ns.h -- C ABI of a single-GPU (GB300, sm_103a) continuous-batching transformer decode step
+ * over a paged KV cache.
+ *
+ * What the step computes (per request row, independently): embedding gather; per layer a
+ * pre-norm decoder block -- RMSNorm, QKV projection, RoPE, paged KV-cache write, paged
+ * grouped-query decode attention, O projection + residual, RMSNorm, SwiGLU FFN + residual;
+ * then a final RMSNorm and the LM head to fp32 logits.  Sources, by page and section:
+ *   - "GPU waiting, not working" (nanoserve notes), the table under "What I changed because
+ *     of it": RoPE cos/sin once per step, fused RMSNorm, grouped-query attention without the
+ *     expanded K/V copy, one pinned host-to-device copy of step metadata, token-to-slot
+ *     mapping, a fused paged-attention kernel; "Where this leaves nanoserve": capture the
+ *     decode step as CUDA graphs once and replay them.
+ *   - "NanoFlow: LLM Serving Is Compute Bound, and Your GPU Is Half Idle": "Four resource
+ *     classes" (dense KQV/O/Up/Gate/Down, memory-bound decode attention), "Nano-batching:
+ *     manufacturing independence" (split the dense batch, co-run nano-ops of different
+ *     resource classes), "The part that is harder than it looks" (thread-block budgets per
+ *     nano-op), closing paragraph (CUDA events order nano-ops).
+ *   - "Speeding up model cold start", "Bounding the CUDA graph capture": capture graphs only
+ *     for the batch sizes actually used.
+ *
+ * Conventions for every call:
+ *   - Every call returns ns_status; nothing aborts the process.  Host-side validation fails
+ *     before anything is launched or changed.  CUDA runtime failures map to NS_ERR_CUDA and
+ *     ns_last_error_message() gives the text.
+ *   - "device" pointers are CUDA device memory of the current device; "host" pointers are
+ *     ordinary (pageable or pinned) host memory.  The library never frees caller memory.
+ *   - Work is enqueued on the caller's `stream` (a cudaStream_t; NULL = legacy default) and
+ *     the call returns after enqueueing.
+ *   - A handle is not thread safe: one thread at a time per handle.
+ *   - Kernels check indices they read from metadata (block ids, slots, lengths).  A failed
+ *     check, or a wait inside a kernel that runs past its time limit, skips the access and
+ *     records a code that ns_get_device_error() returns; kernels never trap.
+ */
+#ifndef NS_DECODE_STEP_H
+#define NS_DECODE_STEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ns_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  NS_OK = 0,
+  NS_ERR_INVALID_ARG = 1,     /* argument out of range or inconsistent; nothing launched */
+  NS_ERR_OUT_OF_MEMORY = 2,   /* device or pinned allocation failed */
+  NS_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed */
+  NS_ERR_UNSUPPORTED = 4,     /* shape or dtype this build does not implement */
+  NS_ERR_NOT_INITIALIZED = 5, /* e.g. ns_decode_step before ns_kv_alloc */
+  NS_ERR_DEVICE_CHECK = 6,    /* a kernel recorded a failed bounds check or a timed-out wait */
+  NS_ERR_OUT_OF_BLOCKS = 7    /* the KV block pool has too few free blocks */
+} ns_status;
+
+typedef enum { NS_F16 = 0, NS_BF16 = 1 } ns_dtype;
+
+/* Device error codes recorded by kernels (ns_get_device_error). */
+enum {
+  NS_DEV_OK = 0,
+  NS_DEV_BAD_BLOCK = 1,    /* block id outside the pool */
+  NS_DEV_BAD_SLOT = 2,     /* slot outside the pool */
+  NS_DEV_BAD_LENGTH = 3,   /* seq_len outside [1, max_blocks_per_seq * block_size] */
+  NS_DEV_WAIT_TIMEOUT = 4, /* an mbarrier wait exceeded its time limit (the kernel returned) */
+  NS_DEV_BAD_TOKEN = 5     /* token id outside the vocabulary */
+};
+
+typedef struct ns_ctx* ns_handle;
+
+/* Model configuration.  Dims: hidden H, n_layers L, n_q_heads Hq, n_kv_heads Hkv (Hq % Hkv
+ * == 0, G = Hq / Hkv <= 8), head_dim d in {64, 128}, ffn F, vocab V.  This build requires
+ * H, Hq*d, Hkv*d, 2F, V multiples of 128 and H, Hq*d, F multiples of 64.
+ * rope_theta: RoPE base; pairs (i, i + d/2), inverse frequency theta^(-2i/d).
+ * rms_eps: RMSNorm epsilon, y = x / sqrt(mean(x^2) + eps) * gamma.
+ * max_batch: largest batch ns_decode_step accepts (rows; <= 4096).
+ * max_blocks_per_seq: width of the block table rows passed to ns_decode_step.
+ * use_graphs: 1 = capture the step as a CUDA graph per batch size on first use and replay
+ * it; 0 = launch the kernels eagerly every step (a debugging path). */
+typedef struct {
+  int hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rms_eps;
+  double rope_theta;
+  int dtype; /* ns_dtype: storage type of weights, activations and the KV cache */
+  int tie_embeddings;
+  int max_batch, max_blocks_per_seq, use_graphs;
+} ns_model_cfg;
+
+/* One layer's weights (host or device pointers, storage dtype).  Linear weights are row-major
+ * [out_features][in_features] (y = x W^T): wq [Hq*d][H], wk/wv [Hkv*d][H], wo [H][Hq*d],
+ * w_gate/w_up [F][H], w_down [H][F]; attn_norm/ffn_norm are the RMSNorm gains [H]. */
+typedef struct {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+} ns_layer_weights;
+
+/* embed [V][H]; final_norm [H]; lm_head [V][H] or NULL when tie_embeddings (head = embed). */
+typedef struct {
+  const void *embed, *final_norm, *lm_head;
+  const ns_layer_weights* layers; /* [n_layers] */
+} ns_weights;
+
+/* Create a handle on the current device.  Copies and re-lays-out the weights into
+ * library-owned device memory (QKV concatenated, gate/up interleaved in 64-row groups), so
+ * the caller may free its copies on return.  Creates the streams, events and TMA descriptors
+ * the step uses.  Errors: INVALID_ARG (bad dims/pointers), UNSUPPORTED (shape this build
+ * does not implement), OUT_OF_MEMORY, CUDA. */
+ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out);
+
+/* Free everything the handle owns (device memory, graphs, streams).  NULL is ignored. */
+void ns_destroy(ns_handle h);
+
+/* Allocate the per-layer paged K and V pools: num_blocks blocks of block_size (16) token
+ * slots.  Layout per layer and per K/V: [num_blocks][Hkv][block_size][d], storage dtype, so
+ * each (block, kv head) tile is contiguous.  Initialises the host free list 0..num_blocks-1
+ * (first-in first-out reuse).  A second call returns INVALID_ARG. */
+ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size);
+
+/* Device addresses of layer `layer`'s K and V pools (for preloading synthetic context). */
+ns_status ns_kv_layer_ptrs(ns_handle h, int layer, void** k_pool, void** v_pool);
+
+/* Host slot mapper ("mapping tokens to cache slots", nanoserve notes).  For each row b in
+ * order: p = positions[b]; when p % block_size == 0 a block is popped from the free list into
+ * block_tables[b][p / block_size]; slot_mapping[b] = block_tables[b][p/bs] * bs + p % bs.
+ * block_tables: host, [batch][max_blocks_per_seq] int32, updated in place.  slot_mapping: host,
+ * [batch] int64, written.  Fails with OUT_OF_BLOCKS / INVALID_ARG before changing anything. */
+ns_status ns_kv_prepare_step(ns_handle h, int batch, const int32_t* positions,
+                             int32_t* block_tables, int64_t* slot_mapping);
+
+/* Host-only block pool (no GPU needed): the free list and slot mapper that a handle's KV cache
+ * uses, usable on its own.  Same policy as ns_kv_prepare_step / ns_kv_reserve / ns_kv_release:
+ * the free list starts 0..num_blocks-1, blocks are taken from the front and returned to the
+ * back.  max_blocks_per_seq is the block-table row width prepare_step writes into. */
+typedef struct ns_block_pool* ns_pool;
+ns_status ns_pool_create(int num_blocks, int block_size, int max_blocks_per_seq, ns_pool* out);
+void ns_pool_destroy(ns_pool p);
+ns_status ns_pool_prepare_step(ns_pool p, int batch, const int32_t* positions,
+                               int32_t* block_tables, int64_t* slot_mapping);
+ns_status ns_pool_reserve(ns_pool p, int n, int32_t* out_ids);
+ns_status ns_pool_release(ns_pool p, const int32_t* block_ids, int n);
+ns_status ns_pool_free_count(ns_pool p, int* n_free);
+
+/* Host validation of one step's metadata, exactly as ns_decode_step performs it before
+ * anything is launched: 1 <= batch <= max_batch; token ids in [0, vocab); positions >= 0;
+ * seq_lens == positions + 1 <= max_blocks_per_seq * block_size; the first
+ * ceil(seq_len / block_size) table entries in [0, num_blocks); slot_mapping[b] ==
+ * block_tables[b][p / bs] * bs + p % bs.  Returns NS_OK or NS_ERR_INVALID_ARG. */
+ns_status ns_check_step_metadata(int num_blocks, int block_size, int max_blocks_per_seq,
+                                 int vocab, int max_batch, int batch, const int32_t* token_ids,
+                                 const int32_t* positions, const int32_t* block_tables,
+                                 const int32_t* seq_lens, const int64_t* slot_mapping);
+
+/* Reserve n blocks from the free list (host ids written to out_ids[n]); OUT_OF_BLOCKS if short. */
+ns_status ns_kv_reserve(ns_handle h, int n, int32_t* out_ids);
+
+/* Return blocks to the back of the free list (a request leaving).  INVALID_ARG on an id
+ * outside the pool. */
+ns_status ns_kv_release(ns_handle h, const int32_t* block_ids, int n);
+
+/* Number of free blocks. */
+ns_status ns_kv_free_count(ns_handle h, int* n_free);
+
+/* Nano-batching (NanoFlow page, "Nano-batching: manufacturing independence"): split each
+ * step's rows into n_split (1..4) consecutive nano-batches of the given sizes (host array;
+ * NULL = even split rounded to multiples of 128 where possible).  Nano-batch i runs on stream
+ * i % 2; its attention waits on the QKV projection of every earlier nano-batch of the same
+ * layer (prefill rows of one chunk may span nano-batches); everything else in a nano-batch
+ * depends only on its own rows, so results are bitwise identical to the unsplit step.
+ * attn_cta_budget > 0 caps the attention grid (thread blocks) of each nano-op, <= 0 = one
+ * wave.  Sizes must sum to the batch of the following ns_decode_step calls. */
+ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_cta_budget);
+
+/* One decode step for `batch` rows.  Host metadata (validated, packed into one pinned buffer
+ * and uploaded with a single host-to-device copy on `stream`):
+ *   token_ids [batch] int32 in [0, V); positions [batch] int32 >= 0;
+ *   block_tables [batch][max_blocks_per_seq] int32 (entries for blocks 0..ceil(seq_len/bs)-1
+ *   must be valid pool ids; the rest are ignored); seq_lens [batch] int32 == positions + 1
+ *   (cached tokens including this step's token); slot_mapping [batch] int64, must equal
+ *   block_tables[b][p/bs]*bs + p%bs.
+ * logits_out: device, [batch][V] fp32, written.  Writes this step's K/V into the pools.
+ * With use_graphs the first call for a batch size captures a graph (not during a caller's
+ * stream capture); later calls replay it.  Returns NOT_INITIALIZED before ns_kv_alloc. */
+ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
+                         const int32_t* positions, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int64_t* slot_mapping,
+                         float* logits_out, ns_stream_t stream);
+
+/* Paged grouped-query decode attention alone (nanoserve notes: the fused paged-attention
+ * kernel; grouped-query attention without the expanded K/V copy).  All pointers device:
+ *   q [batch][n_q_heads][head_dim]; k_pool, v_pool [num_blocks][n_kv_heads][block_size]
+ *   [head_dim]; block_tables [batch][max_blocks_per_seq] int32; seq_lens [batch] int32 in
+ *   [1, max_blocks_per_seq*block_size]; out [batch][n_q_heads][head_dim] (same dtype as q).
+ * For q head h the kv head is h / (n_q_heads / n_kv_heads); o = softmax(q.K^T * scale) V over
+ * tokens t < seq_len.  Long contexts are split into fixed 256-token chunks merged by
+ * log-sum-exp; the split depends only on seq_len, so results do not depend on the batch.
+ * Scratch (partials and counters) is allocated by the library on first use per device and
+ * kept until exit.  num_blocks bounds the block ids the kernel accepts.  Supports head_dim
+ * 64/128, G <= 8 (G in 1,2,4,7,8), block_size 16.  Not to be called during stream capture
+ * the first time on a device (it may allocate). */
+ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                         int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                         ns_stream_t stream);
+
+/* Dense projection through the tcgen05 GEMM used by the step (NanoFlow page: the dense
+ * class KQV/O/Up/Gate/Down): y[m][n] = sum_k x[m][k] * w[n][k], fp32 out.  w [n][k], x [m][k]
+ * device, storage dtype; y device fp32 [m][n].  n % 128 == 0, k % 64 == 0, 1 <= m <= 4096.
+ * Uses library-allocated split-K scratch (allocated on first use per device). */
+ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k, int dtype,
+                    ns_stream_t stream);
+
+/* Greedy next token per row: index of the largest logit, ties to the lowest index.
+ * logits device [batch][vocab] fp32; out_ids device [batch] int32. */
+ns_status ns_greedy_argmax(const float* logits, int batch, int vocab, int32_t* out_ids,
+                           ns_stream_t stream);
+
+/* Read and clear the device error word of the handle (NULL handle = the word used by the
+ * handle-free calls on the current device).  Synchronises the device. */
+ns_status ns_get_device_error(ns_handle h, int* code);
+
+/* Step statistics: kernels launched per step and per graph, graph count, last capture ms. */
+typedef struct {
+  int kernels_per_step;     /* kernel launches in one step (eager) / kernel nodes (graph) */
+  int graphs_cached;        /* captured batch sizes */
+  double last_capture_ms;   /* host time of the last capture + instantiate */
+  long long steps;          /* ns_decode_step calls that succeeded */
+} ns_step_info;
+ns_status ns_get_step_info(ns_handle h, ns_step_info* out);
+
+/* Human-readable name of a status; thread-local text of the last failure. */
+const char* ns_status_str(ns_status s);
+const char* ns_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NS_DECODE_STEP_H */

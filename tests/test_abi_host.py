@@ -1,0 +1,131 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol include/ns.h declares,
+its host block pool reproduces the allocator model bit for bit, and host validation rejects
+bad step metadata before anything is launched."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.kvcache import AllocatorError, BlockAllocator
+from transformer_decode_step_ns_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_lib.LIB_PATH):
+        from transformer_decode_step_ns_gb300 import _build
+        _build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ns.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ns_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SYMBOLS)
+
+
+def test_status_strings(L):
+    assert L.ns_status_str(0) == b"NS_OK"
+    assert L.ns_status_str(7) == b"NS_ERR_OUT_OF_BLOCKS"
+
+
+def test_block_pool_matches_the_allocator_model_bit_for_bit(L):
+    rng = np.random.default_rng(11)
+    nb, bs, mb, B = 40, 16, 12, 6
+    pool = _lib.BlockPool(nb, bs, mb)
+    model = BlockAllocator(nb, bs)
+    t_lib = np.zeros((B, mb), dtype=np.int32)
+    t_mod = np.zeros((B, mb), dtype=np.int32)
+    ctx = np.zeros(B, dtype=np.int64)
+    for step in range(300):
+        # a request leaves now and then; its slot restarts at position 0
+        if rng.random() < 0.1:
+            b = int(rng.integers(B))
+            n = (int(ctx[b]) + bs - 1) // bs
+            ids = t_lib[b, :n].copy()
+            np.testing.assert_array_equal(ids, t_mod[b, :n])
+            pool.release(ids)
+            model.release(ids.tolist())
+            ctx[b] = 0
+            t_lib[b] = 0
+            t_mod[b] = 0
+        pos = ctx.astype(np.int32)
+        try:
+            s_mod = model.prepare_step(t_mod, pos)
+            err_mod = None
+        except AllocatorError as e:
+            err_mod = e
+        if err_mod is None:
+            s_lib = pool.prepare_step(pos, t_lib)
+            np.testing.assert_array_equal(s_lib, s_mod)
+            np.testing.assert_array_equal(t_lib, t_mod)
+            ctx += 1
+            ctx[ctx >= mb * bs] = 0  # wrap long requests (release-free restart in the test)
+        else:
+            with pytest.raises(_lib.NSError):
+                pool.prepare_step(pos, t_lib)
+            np.testing.assert_array_equal(t_lib, t_mod)
+        assert pool.free_count() == model.free_count()
+
+
+def test_block_pool_errors(L):
+    pool = _lib.BlockPool(2, 16, 4)
+    tab = np.zeros((3, 4), dtype=np.int32)
+    with pytest.raises(_lib.NSError) as e:
+        pool.prepare_step(np.array([0, 0, 0]), tab)
+    assert e.value.status == 7 and pool.free_count() == 2 and not tab.any()
+    with pytest.raises(_lib.NSError) as e:
+        pool.prepare_step(np.array([64]), np.zeros((1, 4), dtype=np.int32))
+    assert e.value.status == 1
+    with pytest.raises(_lib.NSError):
+        pool.release([5])
+    assert pool.reserve(2).tolist() == [0, 1]
+    with pytest.raises(_lib.NSError):
+        pool.reserve(1)
+
+
+def _meta(B=3, bs=16, mb=4, nb=20, vocab=50):
+    db = synth.decode_batch(7, "m", [3, 17, 40], vocab, bs, num_blocks=nb, max_blocks_per_seq=mb)
+    return db, dict(num_blocks=nb, block_size=bs, max_blocks_per_seq=mb, vocab=vocab, max_batch=8)
+
+
+def _chk(kw, db, **over):
+    a = dict(token_ids=db.token_ids.copy(), positions=db.positions.copy(),
+             block_tables=db.block_tables.copy(), seq_lens=db.seq_lens.copy(),
+             slot_mapping=db.slot_mapping.copy())
+    a.update(over)
+    return _lib.check_step_metadata(kw["num_blocks"], kw["block_size"], kw["max_blocks_per_seq"],
+                                    kw["vocab"], kw["max_batch"], **a)
+
+
+def test_step_metadata_validation(L):
+    db, kw = _meta()
+    assert _chk(kw, db) == 0
+    bad_tok = db.token_ids.copy(); bad_tok[1] = 50
+    assert _chk(kw, db, token_ids=bad_tok) == 1
+    bad_len = db.seq_lens.copy(); bad_len[0] += 1
+    assert _chk(kw, db, seq_lens=bad_len) == 1
+    bad_tab = db.block_tables.copy(); bad_tab[2, 1] = 20
+    assert _chk(kw, db, block_tables=bad_tab) == 1
+    bad_tab = db.block_tables.copy(); bad_tab[2, 3] = -5   # beyond seq_len: ignored
+    assert _chk(kw, db, block_tables=bad_tab) == 0
+    bad_slot = db.slot_mapping.copy(); bad_slot[0] += 1
+    assert _chk(kw, db, slot_mapping=bad_slot) == 1
+    kw2 = dict(kw); kw2["max_batch"] = 2
+    assert _chk(kw2, db) == 1
+    kw3 = dict(kw); kw3["max_blocks_per_seq"] = 4
+    long_pos = db.positions.copy(); long_pos[2] = 64
+    long_len = db.seq_lens.copy(); long_len[2] = 65
+    assert _chk(kw3, db, positions=long_pos, seq_lens=long_len) == 1

@@ -1,0 +1,122 @@
+"""GPU parity of the individual kernels against the oracle, through the C ABI.
+
+Tolerances: the decode-step requirement is per-tensor relative L2 <= 1e-2 for fp16/bf16
+math; the projections (fp32 accumulation of exact 16-bit products) are held to 1e-4; where the
+result is a copy of an input (single cached token) or must not depend on the rest of the
+batch / the physical block order, the comparison is bitwise.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import (attention_case, from_dev, oracle_attention, rel_l2, run_attention,
+                     storage_f64, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n_q,n_kv,d,dtype,lens", [
+    (32, 8, 128, "bf16", [1, 15, 16, 17, 255, 256, 257, 700]),
+    (14, 2, 64, "f16", [129, 1, 600, 1040]),
+    (64, 8, 128, "bf16", [3, 513, 1024]),
+    (8, 8, 128, "f16", [40, 300]),
+    (16, 8, 64, "bf16", [77, 1]),
+])
+def test_attention_matches_oracle(cuda_lib, n_q, n_kv, d, dtype, lens):
+    q, kp, vp, tab, sl, nb = attention_case(3, lens, n_q, n_kv, d, dtype)
+    got = storage_f64(run_attention(q, kp, vp, tab, sl, n_q, n_kv, d, dtype, nb), dtype)
+    ref = oracle_attention(q, kp, vp, tab, sl, d, dtype)
+    for b in range(len(lens)):
+        assert rel_l2(got[b], ref[b]) < 1e-2, b
+    assert np.abs(got - ref).max() < 3e-2
+
+
+def test_attention_single_cached_token_returns_v_exactly(cuda_lib):
+    q, kp, vp, tab, sl, nb = attention_case(4, [1, 1, 1], 32, 8, 128, "bf16")
+    got = run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb)
+    for b in range(3):
+        for h in range(32):
+            np.testing.assert_array_equal(got[b, h], vp[tab[b, 0], h // 4, 0])
+
+
+def test_attention_block_permutation_and_batch_independence_bitwise(cuda_lib):
+    lens = [300, 17, 1200, 64]
+    q, kp, vp, tab, sl, nb = attention_case(5, lens, 32, 8, 128, "bf16")
+    base = run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb)
+    perm = np.random.default_rng(0).permutation(nb)
+    kp2 = np.empty_like(kp)
+    vp2 = np.empty_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    tab2 = np.where(tab >= 0, perm[tab], tab).astype(np.int32)
+    out2 = run_attention(q, kp2, vp2, tab2, sl, 32, 8, 128, "bf16", nb)
+    np.testing.assert_array_equal(out2, base)
+    for b in range(len(lens)):
+        one = run_attention(q[b:b + 1], kp, vp, tab[b:b + 1], sl[b:b + 1], 32, 8, 128, "bf16", nb)
+        np.testing.assert_array_equal(one[0], base[b])
+
+
+def test_attention_rejects_unsupported_shapes(cuda_lib):
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    x = torch.zeros(16, dtype=torch.int16, device="cuda")
+    t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.NSError) as e:
+        _lib.attn_decode(x, x, x, t, t, x, 12, 4, 96, 16, 1, 1, 0.1, "bf16")  # d = 96
+    assert e.value.status == 4
+    with pytest.raises(_lib.NSError) as e:
+        _lib.attn_decode(x, x, x, t, t, x, 12, 5, 128, 16, 1, 1, 0.1, "bf16")  # Hq % Hkv
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("m,n,k,dtype", [
+    (1, 128, 64, "bf16"), (16, 256, 128, "f16"), (33, 1152, 896, "f16"),
+    (7, 896, 4864, "bf16"), (32, 9728, 896, "f16"), (256, 384, 512, "bf16"),
+    (300, 256, 1024, "bf16"), (1000, 512, 256, "f16"), (2048, 1024, 2048, "bf16"),
+])
+def test_linear_matches_fp64(cuda_lib, m, n, k, dtype):
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    w = synth.normal(9, f"w{m}{n}{k}", (n, k), dtype, std=0.05)
+    x = synth.normal(9, f"x{m}{n}{k}", (m, k), dtype)
+    y = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    _lib.linear(to_dev(w), to_dev(x), y, m, n, k, dtype)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    ref = storage_f64(x, dtype) @ storage_f64(w, dtype).T
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) < 1e-4
+    assert _lib.device_error() == 0
+
+
+def test_linear_rows_do_not_depend_on_the_batch(cuda_lib):
+    """Row independence (NanoFlow: rows of the activation matrix are independent), bitwise."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    n, k = 1152, 896
+    w = to_dev(synth.normal(10, "w", (n, k), "f16", std=0.05))
+    x = synth.normal(10, "x", (40, k), "f16")
+    full = torch.empty((40, n), dtype=torch.float32, device="cuda")
+    _lib.linear(w, to_dev(x), full, 40, n, k, "f16")
+    for lo, hi in ((0, 1), (3, 19), (19, 40)):
+        part = torch.empty((hi - lo, n), dtype=torch.float32, device="cuda")
+        _lib.linear(w, to_dev(x[lo:hi]), part, hi - lo, n, k, "f16")
+        torch.cuda.synchronize()
+        assert torch.equal(part, full[lo:hi])
+
+
+def test_greedy_argmax_ties_to_lowest(cuda_lib):
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    logits = torch.randn(5, 151936, device="cuda")
+    logits[2, 7] = 50.0
+    logits[2, 90000] = 50.0
+    logits[4, :] = 1.0
+    out = torch.empty(5, dtype=torch.int32, device="cuda")
+    _lib.greedy_argmax(logits, out)
+    ref = torch.argmax(logits, dim=-1).to(torch.int32)
+    ref[2] = 7
+    ref[4] = 0
+    assert torch.equal(out, ref)

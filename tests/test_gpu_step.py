@@ -1,0 +1,202 @@
+"""GPU parity of the whole decode step (ns_decode_step) against the oracle, plus the step's
+bitwise properties: graph replay equals eager launch, nano-batched equals unsplit, and only
+this step's slots of the KV cache change."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import from_dev, rel_l2, storage_f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _tiny(dtype="bf16", tie=True, n_layers=2):
+    return synth.ModelShape(hidden=256, n_layers=n_layers, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                            ffn=384, vocab=512, rms_eps=1e-6, rope_theta=1e4, dtype=dtype,
+                            tie_embeddings=tie)
+
+
+class Harness:
+    """One model on the device and the same model + cache in the oracle."""
+
+    def __init__(self, shape, seed, ctx, bs=16, extra_blocks=4, max_batch=None, mb=None,
+                 use_graphs=True, gamma_std=0.1, weights=None, kv_std=1.0):
+        from transformer_decode_step_ns_gb300 import _lib
+        self.shape, self.bs = shape, bs
+        self.w = weights if weights is not None else synth.model_weights(shape, seed, gamma_std=gamma_std)
+        need = sum(math.ceil((c + 1) / bs) for c in ctx)
+        self.num_blocks = need + extra_blocks
+        mb = mb or max(math.ceil((c + 1) / bs) for c in ctx) + 1
+        self.batch = synth.decode_batch(seed, "batch", list(ctx), shape.vocab, bs,
+                                        num_blocks=self.num_blocks, max_blocks_per_seq=mb)
+        self.mb = mb
+        self.kp = [synth.kv_pool(seed, f"k{l}", self.num_blocks, shape.n_kv_heads, bs,
+                                 shape.head_dim, shape.dtype, kv_std) for l in range(shape.n_layers)]
+        self.vp = [synth.kv_pool(seed, f"v{l}", self.num_blocks, shape.n_kv_heads, bs,
+                                 shape.head_dim, shape.dtype, kv_std) for l in range(shape.n_layers)]
+        self.dev = _lib.DecodeStep(shape, self.w, max_batch or len(ctx), mb, use_graphs=use_graphs)
+        self.dev.kv_alloc(self.num_blocks, bs)
+        self.upload_pools()
+
+    def upload_pools(self):
+        from transformer_decode_step_ns_gb300 import _lib
+        for l in range(self.shape.n_layers):
+            k, v = self.dev.kv_layer_ptrs(l)
+            _lib.memcpy(k, self.kp[l].ctypes.data, self.kp[l].nbytes)
+            _lib.memcpy(v, self.vp[l].ctypes.data, self.vp[l].nbytes)
+
+    def download_pools(self):
+        from transformer_decode_step_ns_gb300 import _lib
+        ks, vs = [], []
+        for l in range(self.shape.n_layers):
+            k, v = self.dev.kv_layer_ptrs(l)
+            kk = np.empty_like(self.kp[l])
+            vv = np.empty_like(self.vp[l])
+            _lib.memcpy(kk.ctypes.data, k, kk.nbytes)
+            _lib.memcpy(vv.ctypes.data, v, vv.nbytes)
+            ks.append(kk)
+            vs.append(vv)
+        return ks, vs
+
+    def run_gpu(self, rows=None):
+        import torch
+        b = self.batch
+        sl = slice(None) if rows is None else rows
+        B = len(b.token_ids[sl])
+        logits = torch.full((B, self.shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
+        self.dev.step(b.token_ids[sl], b.positions[sl], b.block_tables[sl], b.seq_lens[sl],
+                      b.slot_mapping[sl], logits)
+        torch.cuda.synchronize()
+        assert self.dev.device_error() == 0
+        return logits.cpu().numpy().astype(np.float64)
+
+    def run_oracle(self):
+        b = self.batch
+        model = oracle.OracleModel.from_weights(self.shape, self.w)
+        kp = [a.copy() for a in self.kp]
+        vp = [a.copy() for a in self.vp]
+        logits = oracle.decode_step(model, kp, vp, b.token_ids, b.positions, b.block_tables,
+                                    b.seq_lens, b.slot_mapping, self.bs)
+        return logits, kp, vp
+
+
+def _check_step(h: Harness):
+    got = h.run_gpu()
+    ref, kp_ref, vp_ref = h.run_oracle()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) < 1e-2
+    assert np.abs(got - ref).max() < 5e-2
+    ks, vs = h.download_pools()
+    dt = h.shape.dtype
+    for l in range(h.shape.n_layers):
+        for s in h.batch.slot_mapping:
+            blk, off = int(s) // h.bs, int(s) % h.bs
+            assert rel_l2(storage_f64(ks[l][blk, :, off], dt), storage_f64(kp_ref[l][blk, :, off], dt)) < 1e-2
+            assert rel_l2(storage_f64(vs[l][blk, :, off], dt), storage_f64(vp_ref[l][blk, :, off], dt)) < 1e-2
+    return got, ref
+
+
+@pytest.mark.parametrize("dtype,tie", [("bf16", True), ("f16", False)])
+def test_tiny_step_matches_oracle(cuda_lib, dtype, tie):
+    h = Harness(_tiny(dtype, tie), 31, [0, 5, 16, 300])
+    _check_step(h)
+
+
+def test_qwen_shape_two_layers_batch1(cuda_lib):
+    """Two-layer Qwen2.5-0.5B-shaped decoder, batch 1: 128 cached tokens whose blocks are a
+    random permutation of physical blocks 0-7; this step's token takes block 8."""
+    shape = synth.qwen05b_shape(n_layers=2)
+    seed = synth.config_seed(0)
+    w = synth.model_weights(shape, seed)
+    h = Harness.__new__(Harness)
+    from transformer_decode_step_ns_gb300 import _lib
+    h.shape, h.bs, h.w = shape, 16, w
+    perm = synth.permutation(seed, "cfg0.blocks", 8)
+    tab = np.zeros((1, 9), dtype=np.int32)
+    tab[0, :8] = perm
+    tab[0, 8] = 8
+    tok = synth.uniform_int(seed, "cfg0.token", 1, 0, shape.vocab - 1).astype(np.int32)
+    h.batch = synth.DecodeBatch(token_ids=tok, positions=np.array([128], dtype=np.int32),
+                                seq_lens=np.array([129], dtype=np.int32), block_tables=tab,
+                                slot_mapping=np.array([8 * 16], dtype=np.int64), num_blocks=9,
+                                block_size=16)
+    h.num_blocks, h.mb = 9, 9
+    h.kp = [synth.kv_pool(seed, f"k{l}", 9, 2, 16, 64, "f16") for l in range(2)]
+    h.vp = [synth.kv_pool(seed, f"v{l}", 9, 2, 16, 64, "f16") for l in range(2)]
+    h.dev = _lib.DecodeStep(shape, w, 1, 9, use_graphs=True)
+    h.dev.kv_alloc(9, 16)
+    h.upload_pools()
+    got, ref = _check_step(h)
+    assert int(np.argmax(got[0])) == int(np.argmax(ref[0])) or \
+        abs(ref[0].max() - ref[0][int(np.argmax(got[0]))]) < 5e-2
+
+
+def test_graph_replay_equals_eager_bitwise(cuda_lib):
+    shape = _tiny("bf16")
+    a = Harness(shape, 41, [3, 40, 200], use_graphs=True)
+    b = Harness(shape, 41, [3, 40, 200], use_graphs=False)
+    ga = a.run_gpu()
+    gb = b.run_gpu()
+    np.testing.assert_array_equal(ga, gb)
+    # a second replay of the captured graph on fresh caches gives the same answer
+    a.upload_pools()
+    np.testing.assert_array_equal(a.run_gpu(), ga)
+    assert a.dev.info().graphs_cached == 1
+
+
+def test_nano_batches_equal_the_whole_batch_bitwise(cuda_lib):
+    shape = _tiny("bf16")
+    ctx = [3, 40, 200, 17, 1, 600]
+    whole = Harness(shape, 51, ctx)
+    g_whole = whole.run_gpu()
+    split = Harness(shape, 51, ctx)
+    split.dev.set_nanobatch([2, 4])
+    g_split = split.run_gpu()
+    np.testing.assert_array_equal(g_split, g_whole)
+    split3 = Harness(shape, 51, ctx, use_graphs=False)
+    split3.dev.set_nanobatch([1, 3, 2], attn_cta_budget=3)
+    np.testing.assert_array_equal(split3.run_gpu(), g_whole)
+
+
+def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):
+    shape = _tiny("f16")
+    ctx = [9, 33, 129]
+    h = Harness(shape, 61, ctx, max_batch=3)
+    full = h.run_gpu()
+    for b in range(3):
+        h.upload_pools()
+        one = h.run_gpu(rows=slice(b, b + 1))
+        np.testing.assert_array_equal(one[0], full[b])
+
+
+def test_only_this_steps_slots_change(cuda_lib):
+    shape = _tiny("bf16")
+    h = Harness(shape, 71, [5, 31, 32, 100])
+    before_k = [a.copy() for a in h.kp]
+    h.run_gpu()
+    ks, vs = h.download_pools()
+    written = {(int(s) // 16, int(s) % 16) for s in h.batch.slot_mapping}
+    for l in range(shape.n_layers):
+        diff = np.argwhere((ks[l] != before_k[l]).any(axis=(1, 3)))
+        assert {(int(b), int(o)) for b, o in diff} <= written
+        diffv = np.argwhere((vs[l] != h.vp[l]).any(axis=(1, 3)))
+        assert {(int(b), int(o)) for b, o in diffv} <= written
+
+
+def test_decode_step_rejects_bad_metadata_before_launch(cuda_lib):
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    h = Harness(_tiny("bf16"), 81, [4, 20])
+    b = h.batch
+    logits = torch.zeros((2, 512), device="cuda")
+    bad = b.slot_mapping.copy()
+    bad[1] += 1
+    with pytest.raises(_lib.NSError) as e:
+        h.dev.step(b.token_ids, b.positions, b.block_tables, b.seq_lens, bad, logits)
+    assert e.value.status == 1
+    h.dev.set_nanobatch([1, 2])
+    with pytest.raises(_lib.NSError):
+        h.dev.step(b.token_ids, b.positions, b.block_tables, b.seq_lens, b.slot_mapping, logits)

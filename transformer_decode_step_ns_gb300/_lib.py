@@ -1,0 +1,372 @@
+"""ctypes binding of libns.so: argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels.  PyTorch appears here only
+as device-memory and stream plumbing (``data_ptr()``, ``cuda_stream``).  When the library is
+missing or cannot load, every call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libns.so")
+
+NS_F16 = 0
+NS_BF16 = 1
+DTYPES = {"f16": NS_F16, "bf16": NS_BF16}
+
+STATUS = {
+    0: "NS_OK", 1: "NS_ERR_INVALID_ARG", 2: "NS_ERR_OUT_OF_MEMORY", 3: "NS_ERR_CUDA",
+    4: "NS_ERR_UNSUPPORTED", 5: "NS_ERR_NOT_INITIALIZED", 6: "NS_ERR_DEVICE_CHECK",
+    7: "NS_ERR_OUT_OF_BLOCKS",
+}
+
+# exported symbols declared in include/ns.h
+SYMBOLS = (
+    "ns_create", "ns_destroy", "ns_kv_alloc", "ns_kv_layer_ptrs", "ns_kv_prepare_step",
+    "ns_kv_reserve", "ns_kv_release", "ns_kv_free_count", "ns_set_nanobatch", "ns_decode_step",
+    "ns_attn_decode", "ns_linear", "ns_greedy_argmax", "ns_get_device_error",
+    "ns_get_step_info", "ns_status_str", "ns_last_error_message", "ns_pool_create",
+    "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
+    "ns_pool_free_count", "ns_check_step_metadata",
+)
+
+
+class NSError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class ModelCfg(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_layers", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_double), ("dtype", ctypes.c_int),
+                ("tie_embeddings", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int), ("use_graphs", ctypes.c_int)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class StepInfo(ctypes.Structure):
+    _fields_ = [("kernels_per_step", ctypes.c_int), ("graphs_cached", ctypes.c_int),
+                ("last_capture_ms", ctypes.c_double), ("steps", ctypes.c_longlong)]
+
+
+_lib = None
+_cudart = None
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+F = ctypes.c_float
+
+
+def lib() -> ctypes.CDLL:
+    """Load libns.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "ns_create": ([ctypes.POINTER(ModelCfg), ctypes.POINTER(Weights), ctypes.POINTER(P)], I),
+            "ns_destroy": ([P], None),
+            "ns_kv_alloc": ([P, I, I], I),
+            "ns_kv_layer_ptrs": ([P, I, ctypes.POINTER(P), ctypes.POINTER(P)], I),
+            "ns_kv_prepare_step": ([P, I, P, P, P], I),
+            "ns_kv_reserve": ([P, I, P], I),
+            "ns_kv_release": ([P, P, I], I),
+            "ns_kv_free_count": ([P, ctypes.POINTER(I)], I),
+            "ns_set_nanobatch": ([P, I, P, I], I),
+            "ns_decode_step": ([P, I, P, P, P, P, P, P, P], I),
+            "ns_attn_decode": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P], I),
+            "ns_linear": ([P, P, P, I, I, I, I, P], I),
+            "ns_greedy_argmax": ([P, I, I, P, P], I),
+            "ns_get_device_error": ([P, ctypes.POINTER(I)], I),
+            "ns_get_step_info": ([P, ctypes.POINTER(StepInfo)], I),
+            "ns_status_str": ([I], ctypes.c_char_p),
+            "ns_pool_create": ([I, I, I, ctypes.POINTER(P)], I),
+            "ns_pool_destroy": ([P], None),
+            "ns_pool_prepare_step": ([P, I, P, P, P], I),
+            "ns_pool_reserve": ([P, I, P], I),
+            "ns_pool_release": ([P, P, I], I),
+            "ns_pool_free_count": ([P, ctypes.POINTER(I)], I),
+            "ns_check_step_metadata": ([I, I, I, I, I, I, P, P, P, P, P], I),
+            "ns_last_error_message": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def check(status: int) -> None:
+    if status != 0:
+        raise NSError(status, lib().ns_last_error_message().decode())
+
+
+def cudart() -> ctypes.CDLL:
+    """The CUDA runtime libns.so links against (for plain memcpy plumbing in harnesses)."""
+    global _cudart
+    if _cudart is None:
+        lib()
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                _cudart = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if _cudart is None:
+            raise RuntimeError("libcudart not found")
+        _cudart.cudaMemcpy.argtypes = [P, P, ctypes.c_size_t, I]
+        _cudart.cudaMemcpy.restype = I
+    return _cudart
+
+
+def memcpy(dst: int, src: int, nbytes: int) -> None:
+    """cudaMemcpy with cudaMemcpyDefault (direction from the pointers)."""
+    r = cudart().cudaMemcpy(P(dst), P(src), ctypes.c_size_t(nbytes), 4)
+    if r != 0:
+        raise RuntimeError(f"cudaMemcpy failed ({r})")
+
+
+def _ptr(a) -> Optional[int]:
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("host arrays must be C-contiguous")
+        return a.ctypes.data
+    if hasattr(a, "data_ptr"):
+        if not a.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return a.data_ptr()
+    raise TypeError(type(a))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class DecodeStep:
+    """A model handle: ns_create / ns_kv_alloc / ns_decode_step and friends.
+
+    ``weights`` is a dict shaped like ``synth.model_weights`` (host numpy arrays or device
+    tensors, storage dtype); the library copies them.
+    """
+
+    def __init__(self, shape, weights, max_batch: int, max_blocks_per_seq: int,
+                 use_graphs: bool = True):
+        L = lib()
+        self.shape = shape
+        self.max_batch = max_batch
+        self.mb = max_blocks_per_seq
+        cfg = ModelCfg(shape.hidden, shape.n_layers, shape.n_q_heads, shape.n_kv_heads,
+                       shape.head_dim, shape.ffn, shape.vocab, float(shape.rms_eps),
+                       float(shape.rope_theta), DTYPES[shape.dtype],
+                       1 if shape.tie_embeddings else 0, max_batch, max_blocks_per_seq,
+                       1 if use_graphs else 0)
+        keep = []
+        layers = (LayerWeights * shape.n_layers)()
+        for l, lw in enumerate(weights["layers"]):
+            for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
+                a = lw[k]
+                if isinstance(a, np.ndarray):
+                    a = np.ascontiguousarray(a)
+                keep.append(a)
+                setattr(layers[l], k, _ptr(a))
+        emb = np.ascontiguousarray(weights["embed"]) if isinstance(weights["embed"], np.ndarray) else weights["embed"]
+        fin = np.ascontiguousarray(weights["final_norm"]) if isinstance(weights["final_norm"], np.ndarray) else weights["final_norm"]
+        head = weights.get("lm_head")
+        keep += [emb, fin, head]
+        w = Weights(_ptr(emb), _ptr(fin), _ptr(head), layers)
+        h = P()
+        check(L.ns_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)))
+        self.h = h
+        self.num_blocks = 0
+        self.block_size = 0
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            lib().ns_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def kv_alloc(self, num_blocks: int, block_size: int = 16) -> None:
+        check(lib().ns_kv_alloc(self.h, num_blocks, block_size))
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def kv_layer_ptrs(self, layer: int):
+        k, v = P(), P()
+        check(lib().ns_kv_layer_ptrs(self.h, layer, ctypes.byref(k), ctypes.byref(v)))
+        return k.value, v.value
+
+    def kv_pool_bytes(self) -> int:
+        s = self.shape
+        return self.num_blocks * s.n_kv_heads * self.block_size * s.head_dim * 2
+
+    def prepare_step(self, positions: np.ndarray, block_tables: np.ndarray) -> np.ndarray:
+        pos = np.ascontiguousarray(positions, dtype=np.int32)
+        assert block_tables.dtype == np.int32 and block_tables.flags["C_CONTIGUOUS"]
+        slots = np.zeros(pos.shape[0], dtype=np.int64)
+        check(lib().ns_kv_prepare_step(self.h, pos.shape[0], _ptr(pos), _ptr(block_tables),
+                                       _ptr(slots)))
+        return slots
+
+    def reserve(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib().ns_kv_reserve(self.h, n, _ptr(out)))
+        return out[:n]
+
+    def release(self, ids: Sequence[int]) -> None:
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().ns_kv_release(self.h, _ptr(a) if a.size else None, a.size))
+
+    def free_count(self) -> int:
+        n = I()
+        check(lib().ns_kv_free_count(self.h, ctypes.byref(n)))
+        return n.value
+
+    def set_nanobatch(self, sizes: Optional[Sequence[int]] = None, attn_cta_budget: int = 0):
+        if not sizes or len(sizes) == 1:
+            check(lib().ns_set_nanobatch(self.h, 1, None, attn_cta_budget))
+            return
+        a = np.ascontiguousarray(sizes, dtype=np.int32)
+        check(lib().ns_set_nanobatch(self.h, a.size, _ptr(a), attn_cta_budget))
+
+    def step(self, token_ids, positions, block_tables, seq_lens, slot_mapping, logits,
+             stream=None) -> None:
+        """One decode step; host metadata arrays, ``logits`` a device fp32 [B, V] buffer."""
+        tok = np.ascontiguousarray(token_ids, dtype=np.int32)
+        pos = np.ascontiguousarray(positions, dtype=np.int32)
+        tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        if tab.ndim != 2 or tab.shape[1] != self.mb:
+            raise ValueError(f"block_tables must be [batch, {self.mb}]")
+        check(lib().ns_decode_step(self.h, tok.shape[0], _ptr(tok), _ptr(pos), _ptr(tab),
+                                   _ptr(sl), _ptr(slot), _ptr(logits), _stream(stream)))
+
+    def device_error(self) -> int:
+        c = I()
+        check(lib().ns_get_device_error(self.h, ctypes.byref(c)))
+        return c.value
+
+    def info(self) -> StepInfo:
+        s = StepInfo()
+        check(lib().ns_get_step_info(self.h, ctypes.byref(s)))
+        return s
+
+
+def attn_decode(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
+                n_kv_heads: int, head_dim: int, block_size: int, max_blocks_per_seq: int,
+                num_blocks: int, scale: float, dtype: str, stream=None) -> None:
+    batch = int(seq_lens.shape[0])
+    check(lib().ns_attn_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                               _ptr(seq_lens), _ptr(out), batch, n_q_heads, n_kv_heads,
+                               head_dim, block_size, max_blocks_per_seq, num_blocks,
+                               float(scale), DTYPES[dtype], _stream(stream)))
+
+
+def linear(w, x, y, m: int, n: int, k: int, dtype: str, stream=None) -> None:
+    check(lib().ns_linear(_ptr(w), _ptr(x), _ptr(y), m, n, k, DTYPES[dtype], _stream(stream)))
+
+
+def greedy_argmax(logits, out_ids, stream=None) -> None:
+    b, v = int(logits.shape[0]), int(logits.shape[1])
+    check(lib().ns_greedy_argmax(_ptr(logits), b, v, _ptr(out_ids), _stream(stream)))
+
+
+def device_error() -> int:
+    c = I()
+    check(lib().ns_get_device_error(None, ctypes.byref(c)))
+    return c.value
+
+
+class BlockPool:
+    """Host-only block pool (ns_pool_*): the allocator and slot mapper, no GPU needed."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        h = P()
+        check(lib().ns_pool_create(num_blocks, block_size, max_blocks_per_seq, ctypes.byref(h)))
+        self.h = h
+        self.mb = max_blocks_per_seq
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().ns_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prepare_step(self, positions, block_tables) -> np.ndarray:
+        pos = np.ascontiguousarray(positions, dtype=np.int32)
+        assert block_tables.dtype == np.int32 and block_tables.flags["C_CONTIGUOUS"]
+        slots = np.zeros(max(pos.shape[0], 1), dtype=np.int64)
+        check(lib().ns_pool_prepare_step(self.h, pos.shape[0], _ptr(pos), _ptr(block_tables),
+                                         _ptr(slots)))
+        return slots[: pos.shape[0]]
+
+    def reserve(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib().ns_pool_reserve(self.h, n, _ptr(out)))
+        return out[:n]
+
+    def release(self, ids) -> None:
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().ns_pool_release(self.h, _ptr(a) if a.size else None, a.size))
+
+    def free_count(self) -> int:
+        n = I()
+        check(lib().ns_pool_free_count(self.h, ctypes.byref(n)))
+        return n.value
+
+
+def check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab, max_batch,
+                        token_ids, positions, block_tables, seq_lens, slot_mapping) -> int:
+    """Run the library's host validation; returns the ns_status code (0 = valid)."""
+    tok = np.ascontiguousarray(token_ids, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return lib().ns_check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab,
+                                        max_batch, tok.shape[0], _ptr(tok), _ptr(pos),
+                                        _ptr(tab), _ptr(sl), _ptr(slot))

@@ -1,0 +1,408 @@
+// Dense projections of the decode step on the 5th-generation tensor cores (tcgen05 / TMEM).
+//
+// "NanoFlow: LLM Serving Is Compute Bound ..." ("Four resource classes"): the KQV, O, Up/Gate
+// and Down projections are the dense class -- compute bound once batched, weight-read bound at
+// small batch ("The roofline flips": AI_decode ~ 2B).  One kernel serves both regimes:
+//
+//   D[128 features x BN tokens] = W_tile[128 x K] . X_tile[BN x K]^T   (UMMA M=128, N=BN)
+//
+// The weight is the UMMA "A" operand (so the batch is the N dimension, 16..256 tokens), both
+// operands K-major, staged by TMA with 128-byte swizzle into an mbarrier ring; one thread
+// issues tcgen05.mma into a TMEM accumulator; four warps read TMEM back for the epilogue.
+// Split-K over CTAs (chosen from the weight's shape only, never from the batch) gives small
+// matrices enough CTAs to stream HBM; the last-arriving CTA of a tile sums the partial tiles in
+// split order (deterministic, no spin) and runs the fused epilogue:
+//   EPI_QKV    RMSNorm scale, RoPE on q/k, q store, k/v store into the paged cache slots
+//              (nanoserve notes: RoPE once per step, slot mapping);
+//   EPI_RESID  residual add, next RMSNorm's input x*gamma and per-tile sum of squares
+//              (the "fused RMSNorm" of the nanoserve notes, folded into the producer);
+//   EPI_SWIGLU silu(gate) * up on interleaved gate/up rows;
+//   EPI_F32    fp32 output (LM head logits), optional RMSNorm scale.
+// Weights are read before griddepcontrol.wait, so with programmatic dependent launch a GEMM
+// streams its weights while the previous kernel of the step finishes.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ns_internal.h"
+#include "ns_ptx.cuh"
+
+namespace ns {
+
+namespace {
+
+template <typename T>
+struct Cvt;
+template <>
+struct Cvt<__half> {
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <>
+struct Cvt<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) {
+    return __float2bfloat16_rn(x);
+  }
+};
+
+constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
+constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void set_err(int* err, int code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+}  // namespace
+
+template <typename T>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int BN = p.BN;
+  const uint32_t b_bytes = static_cast<uint32_t>(BN) * kGemmTileK * 2;
+  const uint32_t stage_bytes = kABytes + b_bytes;
+  uint8_t* ctrl = smem + static_cast<size_t>(p.nstage) * stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + p.nstage;
+  uint64_t* accum = empty + p.nstage;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* last_flag = abort_flag + 1;
+  int* issued = last_flag + 1;
+  float* rs_s = reinterpret_cast<float*>(ctrl + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x;
+  const int split = blockIdx.y;
+  const int tile_m = blockIdx.z;
+  const int tile_id = tile_m * gridDim.x + tile_n;
+  const int n0 = tile_n * kGemmTileN;
+  const int nkb_total = p.K / kGemmTileK;
+  const int kb0 = split * p.kb_per_split;
+  const int nkb = min(p.kb_per_split, nkb_total - kb0);
+  const int tok0 = p.row0 + tile_m * BN;
+  const int m_valid = min(BN, p.M - tile_m * BN);
+  const uint32_t ncols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
+
+  auto stageA = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes; };
+  auto stageB = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kABytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.nstage; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *issued = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mapA);
+    prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Dependents may be scheduled once every CTA holds its TMEM (so none of them can starve us).
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && nkb > 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const int pre = min(p.nstage, nkb);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        tma_load_2d_hint(stageA(i), &mapA, &full[i], (kb0 + i) * kGemmTileK, n0, pol_w);
+      }
+      griddep_wait();  // activations come from the previous kernel of the step
+      for (int i = 0; i < pre; ++i) tma_load_2d(stageB(i), &mapB, &full[i], (kb0 + i) * kGemmTileK, tok0);
+      int i = pre;
+      for (; i < nkb; ++i) {
+        const int s = i % p.nstage;
+        const uint32_t ph = static_cast<uint32_t>((i / p.nstage) - 1) & 1u;
+        if (!mbar_wait(&empty[s], ph, abort_flag)) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_2d_hint(stageA(s), &mapA, &full[s], (kb0 + i) * kGemmTileK, n0, pol_w);
+        tma_load_2d(stageB(s), &mapB, &full[s], (kb0 + i) * kGemmTileK, tok0);
+      }
+      *issued = i;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % p.nstage;
+        if (!mbar_wait(&full[s], static_cast<uint32_t>(i / p.nstage) & 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(stageA(s));
+        const uint32_t b_addr = smem_u32(stageB(s));
+#pragma unroll
+        for (int k = 0; k < kGemmTileK / 16; ++k) {
+          umma_f16(tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32),
+                   p.idesc, (i | k) != 0 ? 1u : 0u);
+        }
+        umma_commit(&empty[s]);
+      }
+      umma_commit(accum);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (4 warps)
+    const int q = warp & 3;             // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;      // output feature within the tile
+    const int et = threadIdx.x - 64;    // 0..127
+    const int ew = warp - 2;            // 0..3
+    bool ok = mbar_wait(accum, 0, abort_flag);
+    griddep_wait();
+    tc_fence_after();
+    if (!ok) {
+      *abort_flag = 1;
+      set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+    }
+    float* tile = reinterpret_cast<float*>(smem);  // [BN][128] fp32, reuses the stage ring
+    const int nchunk = (m_valid + 15) >> 4;
+    if (ok && !*abort_flag) {
+      for (int c = 0; c < nchunk; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), r);
+        tmem_ld_wait();
+        if (p.splits == 1) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) tile[(c * 16 + i) * kGemmTileN + row] = __uint_as_float(r[i]);
+        } else {
+          float* w = p.ws + (static_cast<size_t>(tile_id) * p.splits + split) * BN * kGemmTileN +
+                     static_cast<size_t>(c * 16) * kGemmTileN;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i * kGemmTileN + row] = __uint_as_float(r[i]);
+        }
+      }
+    }
+    bool run = ok && !*abort_flag;
+    if (run && p.splits > 1) {
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (et == 0) {
+        const int old = atomicAdd(&p.counters[tile_id], 1);
+        const int last = (old == p.splits - 1) ? 1 : 0;
+        if (last) p.counters[tile_id] = 0;  // ready for the next launch that uses this slot
+        *last_flag = last;
+      }
+      named_barrier_sync(1, 128);
+      run = *last_flag != 0;
+      if (run) {
+        __threadfence();
+        const float* w0 = p.ws + static_cast<size_t>(tile_id) * p.splits * BN * kGemmTileN;
+        for (int j = 0; j < m_valid; ++j) {
+          float acc = 0.f;
+          for (int s = 0; s < p.splits; ++s)
+            acc += __ldcg(w0 + (static_cast<size_t>(s) * BN + j) * kGemmTileN + et);
+          tile[j * kGemmTileN + et] = acc;
+        }
+      }
+    }
+    if (run) {
+      const EpiArgs& e = p.e;
+      const bool scaled = e.sumsq_in != nullptr;
+      if (scaled) {
+        for (int j = et; j < m_valid; j += 128) {
+          float ss = 0.f;
+          for (int t = 0; t < e.sumsq_tiles; ++t) ss += e.sumsq_in[static_cast<size_t>(t) * e.sumsq_ld + tok0 + j];
+          rs_s[j] = rsqrtf(ss / static_cast<float>(e.norm_dim) + e.eps);
+        }
+      }
+      named_barrier_sync(1, 128);
+      if (p.epi == EPI_F32) {
+        float* out = e.out_f32;
+        if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
+        for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
+          const int j = idx >> 7, r = idx & 127;
+          float v = tile[idx];
+          if (scaled) v *= rs_s[j];
+          out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
+        }
+      } else if (p.epi == EPI_QKV) {
+        const int d = e.head_dim, half = d >> 1;
+        T* qo = reinterpret_cast<T*>(e.q_out);
+        T* kp = reinterpret_cast<T*>(e.k_pool);
+        T* vp = reinterpret_cast<T*>(e.v_pool);
+        if (n0 < e.q_dim + e.kv_dim) {
+          for (int idx = et; idx < m_valid * 64; idx += 128) {
+            const int j = idx >> 6, pr = idx & 63;
+            const int hl = pr / half, i = pr - hl * half;
+            const int r_lo = hl * d + i, r_hi = r_lo + half;
+            const int tok = tok0 + j;
+            const float sc = scaled ? rs_s[j] : 1.f;
+            const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
+            const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
+            const float c = e.rope_cos[static_cast<size_t>(tok) * half + i];
+            const float sn = e.rope_sin[static_cast<size_t>(tok) * half + i];
+            const float y_lo = x_lo * c - x_hi * sn;
+            const float y_hi = x_hi * c + x_lo * sn;
+            if (n0 < e.q_dim) {
+              T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
+              dst[r_lo] = Cvt<T>::from_f(y_lo);
+              dst[r_hi] = Cvt<T>::from_f(y_hi);
+            } else {
+              const int col = n0 - e.q_dim + r_lo;
+              const int kvh = col / d;
+              const long long slot = e.slot_mapping[tok];
+              if (slot < 0 || slot >= e.pool_slots) {
+                set_err(p.err, NS_DEV_BAD_SLOT);
+                continue;
+              }
+              const size_t base =
+                  ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                   static_cast<size_t>(slot % e.block_size)) * d;
+              kp[base + i] = Cvt<T>::from_f(y_lo);
+              kp[base + i + half] = Cvt<T>::from_f(y_hi);
+            }
+          }
+        } else {
+          for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
+            const int j = idx >> 7, r = idx & 127;
+            const int tok = tok0 + j;
+            const int col = n0 - e.q_dim - e.kv_dim + r;
+            const int kvh = col / d, dim = col - kvh * d;
+            const long long slot = e.slot_mapping[tok];
+            if (slot < 0 || slot >= e.pool_slots) {
+              set_err(p.err, NS_DEV_BAD_SLOT);
+              continue;
+            }
+            const float v = tile[idx] * (scaled ? rs_s[j] : 1.f);
+            const size_t base =
+                ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                 static_cast<size_t>(slot % e.block_size)) * d;
+            vp[base + dim] = Cvt<T>::from_f(v);
+          }
+        }
+        fence_proxy_async_global();
+      } else if (p.epi == EPI_RESID) {
+        T* xo = reinterpret_cast<T*>(e.xn_out);
+        for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
+          const int j = idx >> 7, r = idx & 127;
+          const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
+          const float rn = e.resid[gi] + tile[idx];
+          e.resid[gi] = rn;
+          xo[gi] = Cvt<T>::from_f(rn * e.gamma_next[n0 + r]);
+          tile[idx] = rn * rn;
+        }
+        named_barrier_sync(1, 128);
+        for (int j = ew; j < m_valid; j += 4) {
+          const float* tr = tile + j * kGemmTileN;
+          float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (lane == 0) e.sumsq_out[static_cast<size_t>(tile_n) * e.sumsq_ld + tok0 + j] = s;
+        }
+        fence_proxy_async_global();
+      } else if (p.epi == EPI_SWIGLU) {
+        T* ao = reinterpret_cast<T*>(e.act_out);
+        const int f0 = tile_n * 64;
+        for (int idx = et; idx < m_valid * 64; idx += 128) {
+          const int j = idx >> 6, c = idx & 63;
+          const float sc = scaled ? rs_s[j] : 1.f;
+          const float g = tile[j * kGemmTileN + c] * sc;
+          const float u = tile[j * kGemmTileN + 64 + c] * sc;
+          const float a = g / (1.f + expf(-g)) * u;
+          ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
+        }
+        fence_proxy_async_global();
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // Let this CTA's own copies in flight land before its shared memory is released.
+    const int n_issued = *issued;
+    for (int i = max(0, n_issued - p.nstage); i < n_issued; ++i) {
+      (void)mbar_wait(&full[i % p.nstage], static_cast<uint32_t>(i / p.nstage) & 1u, nullptr);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+size_t gemm_smem_bytes(int BN, int nstage) {
+  return 1024 + static_cast<size_t>(nstage) * (kABytes + static_cast<size_t>(BN) * kGemmTileK * 2) +
+         kCtrlBytes;
+}
+
+int gemm_pick_stages(int BN) {
+  const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
+  const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
+  int n = static_cast<int>(budget / stage);
+  if (n > 8) n = 8;
+  if (n < 4) n = 4;  // the epilogue tile reuses at least 4 stages ([BN][128] fp32)
+  return n;
+}
+
+uint32_t gemm_idesc(int dtype, int BN) {
+  const uint32_t ab = dtype == NS_BF16 ? 1u : 0u;
+  return (1u << 4)                                   // D format: fp32
+         | (ab << 7) | (ab << 10)                    // A, B format: f16 / bf16
+         | (static_cast<uint32_t>(BN >> 3) << 17)    // N >> 3
+         | (static_cast<uint32_t>(kGemmTileN >> 4) << 24);  // M >> 4
+}
+
+namespace {
+template <typename T>
+cudaError_t launch_gemm_t(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                          cudaStream_t s, bool pdl) {
+  static int configured_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = gemm_smem_bytes(p.BN, p.nstage);
+  if (dev < 31 && !(configured_mask & (1 << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured_mask |= 1 << dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.N / kGemmTileN, p.splits, (p.M + p.BN - 1) / p.BN);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<T>, *mapA, *mapB, p);
+}
+}  // namespace
+
+cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                        int dtype, cudaStream_t s, bool pdl) {
+  if (dtype == NS_BF16) return launch_gemm_t<__nv_bfloat16>(mapA, mapB, p, s, pdl);
+  return launch_gemm_t<__half>(mapA, mapB, p, s, pdl);
+}
+
+}  // namespace ns

@@ -1,0 +1,147 @@
+// Per-step token kernels: embedding gather fused with the RoPE table and the first RMSNorm's
+// inputs, and the greedy argmax over the logits.
+//
+// "GPU waiting, not working" (nanoserve notes), change table: the RoPE cos/sin are built once
+// per step (positions are shared by every layer) -- here in the same launch as the embedding
+// gather, which also writes the first layer's RMSNorm input (x * gamma) and the per-128-column
+// sums of squares that the QKV projection's epilogue turns into the norm scale.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ns_internal.h"
+#include "ns_ptx.cuh"
+
+namespace ns {
+
+namespace {
+
+template <typename T>
+struct EV;
+template <>
+struct EV<__half> {
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <>
+struct EV<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+}  // namespace
+
+// grid = batch rows, block = 128 threads (one thread per column of each 128-column tile).
+template <typename T>
+__global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
+  __shared__ float warp_sums[4];
+  const int row = p.row0 + blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Token ids and positions are step metadata, complete before the step: read them early.
+  int tok = p.token_ids[row];
+  const int pos = p.positions[row];
+  if (tid == 0) griddep_launch_dependents();
+  griddep_wait();  // the residual/xn rows may still be read by the previous step's tail
+  if (tok < 0 || tok >= p.vocab) {
+    if (tid == 0) atomicCAS(p.err, 0, NS_DEV_BAD_TOKEN);
+    tok = 0;
+  }
+  const T* e = reinterpret_cast<const T*>(p.embed) + static_cast<size_t>(tok) * p.hidden;
+  T* xn = reinterpret_cast<T*>(p.xn) + static_cast<size_t>(row) * p.hidden;
+  float* resid = p.resid + static_cast<size_t>(row) * p.hidden;
+  for (int t = 0; t < p.hidden / 128; ++t) {
+    const int i = t * 128 + tid;
+    const float v = EV<T>::to_f(e[i]);
+    resid[i] = v;
+    xn[i] = EV<T>::from_f(v * p.gamma[i]);
+    float s = v * v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) warp_sums[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+      p.sumsq[static_cast<size_t>(t) * p.sumsq_ld + row] =
+          (warp_sums[0] + warp_sums[1]) + (warp_sums[2] + warp_sums[3]);
+    }
+    __syncthreads();
+  }
+  // RoPE table for this row: inv_freq_i = theta^(-2i/d), angle = pos * inv_freq_i, in fp64.
+  const int half = p.head_dim / 2;
+  for (int i = tid; i < half; i += 128) {
+    const double inv = pow(p.theta, -2.0 * static_cast<double>(i) / static_cast<double>(p.head_dim));
+    const double ang = static_cast<double>(pos) * inv;
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    p.rope_cos[static_cast<size_t>(row) * half + i] = static_cast<float>(cs);
+    p.rope_sin[static_cast<size_t>(row) * half + i] = static_cast<float>(sn);
+  }
+  fence_proxy_async_global();  // xn is read through TMA by the next kernel
+}
+
+// Greedy argmax over one row per block; ties go to the lowest index.
+__global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int vocab,
+                                                      int32_t* out) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float* r = logits + static_cast<size_t>(blockIdx.x) * vocab;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+    const float v = r[i];
+    if (v > best || (v == best && i < bi)) {
+      best = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sv[warp] = best;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    best = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;
+  }
+}
+
+cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.batch, 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (dtype == NS_BF16) return cudaLaunchKernelEx(&cfg, embed_rope_kernel<__nv_bfloat16>, p);
+  return cudaLaunchKernelEx(&cfg, embed_rope_kernel<__half>, p);
+}
+
+cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
+                          cudaStream_t s) {
+  argmax_kernel<<<batch, 1024, 0, s>>>(logits, vocab, out);
+  return cudaGetLastError();
+}
+
+}  // namespace ns

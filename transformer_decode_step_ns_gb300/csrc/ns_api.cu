@@ -1,0 +1,1097 @@
+// Host runtime behind the C ABI in ns.h: weight re-layout, KV pools and the block allocator,
+// the single packed metadata upload per step, the per-batch-size CUDA-graph cache, and the
+// two-stream nano-batch schedule.
+//
+// Sources, by page and section:
+//  * "GPU waiting, not working" (nanoserve notes), change table: one pinned host-to-device copy
+//    of the step metadata instead of six small ones; mapping tokens to cache slots; RoPE once
+//    per step; "Where this leaves nanoserve": capture the decode step once as CUDA graphs and
+//    replay them.
+//  * "Speeding up model cold start", "Bounding the CUDA graph capture": capture only the batch
+//    sizes actually used (graphs are captured lazily, per batch size on first use).
+//  * "NanoFlow ...", "Nano-batching: manufacturing independence": split the dense batch into
+//    nano-batches whose nano-ops co-run; "The part that is harder than it looks": thread-block
+//    budgets per nano-op; closing paragraph: CUDA events order the nano-ops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <deque>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "ns.h"
+#include "ns_internal.h"
+
+using namespace ns;
+
+namespace {
+
+thread_local std::string g_msg;
+
+ns_status fail(ns_status s, const std::string& m) {
+  g_msg = m;
+  return s;
+}
+
+#define NS_CUDA(expr)                                                                       \
+  do {                                                                                      \
+    cudaError_t e_ = (expr);                                                                \
+    if (e_ != cudaSuccess)                                                                  \
+      return fail(e_ == cudaErrorMemoryAllocation ? NS_ERR_OUT_OF_MEMORY : NS_ERR_CUDA,     \
+                  std::string(#expr) + ": " + cudaGetErrorString(e_));                     \
+  } while (0)
+
+#define NS_TRY(expr)                 \
+  do {                               \
+    ns_status s_ = (expr);           \
+    if (s_ != NS_OK) return s_;      \
+  } while (0)
+
+// ------------------------------------------------------------------------------ TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows][cols] 16-bit matrix; box = 64 columns (128 B, one swizzle row) x box_rows.
+ns_status make_tmap(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(NS_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dtype == NS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NS_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
+  return NS_OK;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Token tile for m rows: balanced tiles of at most 256, multiple of 16.
+int pick_bn(int m) {
+  const int tiles = (m + kMaxBN - 1) / kMaxBN;
+  int bn = round_up((m + tiles - 1) / tiles, 16);
+  return std::max(16, std::min(kMaxBN, bn));
+}
+
+// Split-K from the weight's shape only (never the batch): enough CTAs to cover the SMs,
+// at least two k-blocks per split.
+void choose_splits(int N, int K, int sms, int* splits, int* kb_per) {
+  const int tiles = N / kGemmTileN, nkb = K / kGemmTileK;
+  int s = std::max(1, sms / std::max(1, tiles));
+  s = std::min(s, std::max(1, nkb / 2));
+  *kb_per = (nkb + s - 1) / s;
+  *splits = (nkb + *kb_per - 1) / *kb_per;
+}
+
+size_t gemm_ws_bytes(int N, int splits, int rows) {
+  if (splits <= 1) return 0;
+  const int mt = (rows + kMaxBN - 1) / kMaxBN;
+  const size_t cap_rows = static_cast<size_t>(mt) * pick_bn(rows);
+  return static_cast<size_t>(N / kGemmTileN) * splits * cap_rows * kGemmTileN * sizeof(float);
+}
+
+int gemm_counter_count(int N, int rows) {
+  return (N / kGemmTileN) * ((rows + kMaxBN - 1) / kMaxBN) + 1;
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// fp16 / bf16 bit patterns to float (IEEE 754 binary16 decode; bf16 is the top half of fp32).
+float half_bits_to_float(uint16_t h) {
+  const uint32_t sign = (h >> 15) & 1u, exp = (h >> 10) & 0x1Fu, man = h & 0x3FFu;
+  float v;
+  if (exp == 0) v = std::ldexp(static_cast<float>(man), -24);
+  else if (exp == 31) v = man ? NAN : INFINITY;
+  else v = std::ldexp(static_cast<float>(man | 0x400u), static_cast<int>(exp) - 25);
+  return sign ? -v : v;
+}
+float bf16_bits_to_float(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// ------------------------------------------------------------------------------ per-device scratch
+// Used by the handle-free calls (ns_attn_decode, ns_linear).  Grown on demand, kept until exit.
+
+struct DevScratch {
+  void* buf = nullptr;
+  size_t bytes = 0;
+  int* counters = nullptr;
+  size_t n_counters = 0;
+  int* err = nullptr;
+};
+std::mutex g_scratch_mu;
+DevScratch g_scratch[64];
+
+ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
+  int dev = 0;
+  NS_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(NS_ERR_UNSUPPORTED, "device index");
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  DevScratch& s = g_scratch[dev];
+  if (s.err == nullptr) {
+    NS_CUDA(cudaMalloc(&s.err, sizeof(int)));
+    NS_CUDA(cudaMemset(s.err, 0, sizeof(int)));
+  }
+  if (s.bytes < bytes) {
+    if (s.buf) cudaFree(s.buf);
+    s.buf = nullptr;
+    s.bytes = 0;
+    NS_CUDA(cudaMalloc(&s.buf, bytes));
+    s.bytes = bytes;
+  }
+  if (s.n_counters < n_counters) {
+    if (s.counters) cudaFree(s.counters);
+    s.counters = nullptr;
+    s.n_counters = 0;
+    NS_CUDA(cudaMalloc(&s.counters, n_counters * sizeof(int)));
+    NS_CUDA(cudaMemset(s.counters, 0, n_counters * sizeof(int)));
+    s.n_counters = n_counters;
+  }
+  *out = &s;
+  return NS_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------ block pool
+
+struct ns_block_pool {
+  int num_blocks = 0, block_size = 0, mb = 0;
+  std::deque<int> free_list;
+};
+
+namespace {
+
+ns_status pool_prepare(ns_block_pool* p, int batch, const int32_t* positions, int32_t* block_tables,
+                       int64_t* slot_mapping) {
+  if (positions == nullptr || block_tables == nullptr || slot_mapping == nullptr || batch < 0)
+    return fail(NS_ERR_INVALID_ARG, "argument");
+  const int bs = p->block_size, mb = p->mb;
+  size_t need = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int pos = positions[b];
+    if (pos < 0 || pos / bs >= mb) return fail(NS_ERR_INVALID_ARG, "position beyond the block table");
+    if (pos % bs == 0) ++need;
+  }
+  if (need > p->free_list.size()) return fail(NS_ERR_OUT_OF_BLOCKS, "out of KV blocks");
+  for (int b = 0; b < batch; ++b) {
+    const int pos = positions[b];
+    int32_t* row = block_tables + static_cast<size_t>(b) * mb;
+    if (pos % bs == 0) {
+      row[pos / bs] = p->free_list.front();
+      p->free_list.pop_front();
+    }
+    slot_mapping[b] = static_cast<int64_t>(row[pos / bs]) * bs + pos % bs;
+  }
+  return NS_OK;
+}
+
+ns_status pool_reserve(ns_block_pool* p, int n, int32_t* out_ids) {
+  if ((n > 0 && out_ids == nullptr) || n < 0) return fail(NS_ERR_INVALID_ARG, "argument");
+  if (static_cast<size_t>(n) > p->free_list.size()) return fail(NS_ERR_OUT_OF_BLOCKS, "out of KV blocks");
+  for (int i = 0; i < n; ++i) {
+    out_ids[i] = p->free_list.front();
+    p->free_list.pop_front();
+  }
+  return NS_OK;
+}
+
+ns_status pool_release(ns_block_pool* p, const int32_t* ids, int n) {
+  if ((n > 0 && ids == nullptr) || n < 0) return fail(NS_ERR_INVALID_ARG, "argument");
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= p->num_blocks) return fail(NS_ERR_INVALID_ARG, "block id out of range");
+  for (int i = 0; i < n; ++i) p->free_list.push_back(ids[i]);
+  return NS_OK;
+}
+
+ns_status check_meta(int num_blocks, int bs, int mb, int vocab, int max_batch, int batch,
+                     const int32_t* token_ids, const int32_t* positions, const int32_t* block_tables,
+                     const int32_t* seq_lens, const int64_t* slot_mapping) {
+  if (batch < 1 || batch > max_batch) return fail(NS_ERR_INVALID_ARG, "batch out of range");
+  if (!token_ids || !positions || !block_tables || !seq_lens || !slot_mapping)
+    return fail(NS_ERR_INVALID_ARG, "null argument");
+  for (int b = 0; b < batch; ++b) {
+    const int tok = token_ids[b], p = positions[b], L = seq_lens[b];
+    if (tok < 0 || tok >= vocab) return fail(NS_ERR_INVALID_ARG, "token id out of range");
+    if (p < 0 || L != p + 1) return fail(NS_ERR_INVALID_ARG, "seq_lens must equal positions + 1");
+    if (L > mb * bs) return fail(NS_ERR_INVALID_ARG, "seq_len beyond max_blocks_per_seq * block_size");
+    const int32_t* row = block_tables + static_cast<size_t>(b) * mb;
+    const int nblk = (L + bs - 1) / bs;
+    for (int i = 0; i < nblk; ++i)
+      if (row[i] < 0 || row[i] >= num_blocks) return fail(NS_ERR_INVALID_ARG, "block id out of range");
+    if (slot_mapping[b] != static_cast<int64_t>(row[p / bs]) * bs + p % bs)
+      return fail(NS_ERR_INVALID_ARG, "slot_mapping disagrees with block_tables");
+  }
+  return NS_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------ the handle
+
+struct Proj {
+  void* w = nullptr;
+  bool owned = true;
+  int N = 0, K = 0, splits = 1, kb_per = 1;
+  CUtensorMap mapA;
+};
+
+struct LayerDev {
+  Proj qkv, o, gu, down;
+  float* attn_norm = nullptr;
+  float* ffn_norm = nullptr;
+};
+
+struct NanoSlot {
+  float* gemm_ws = nullptr;
+  int* gemm_counters = nullptr;
+};
+
+struct ns_ctx {
+  ns_model_cfg cfg;
+  int dev = 0, sms = 1, dtype = 0;
+  int R = 0;  // activation rows (max_batch)
+  std::vector<LayerDev> layers;
+  Proj lm;
+  void* embed = nullptr;
+  float* final_norm = nullptr;
+  // activations
+  float* resid = nullptr;
+  void* xn = nullptr;
+  float* sumsq = nullptr;
+  void* q = nullptr;
+  void* o = nullptr;
+  void* act = nullptr;
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  std::map<std::tuple<const void*, int>, CUtensorMap> bmaps;
+  // KV cache
+  int num_blocks = 0, block_size = 0, max_chunks = 1;
+  void* pools = nullptr;
+  std::vector<void*> kpool, vpool;
+  ns_block_pool pool;
+  int* attn_counters = nullptr;
+  float* attn_partials = nullptr;
+  // metadata
+  size_t meta_cap = 0;
+  uint8_t* meta_host = nullptr;
+  uint8_t* meta_dev = nullptr;
+  cudaEvent_t meta_done = nullptr;
+  bool meta_pending = false;
+  // nano-batching
+  int n_split = 1;
+  std::vector<int> split_sizes;
+  int attn_budget = 0;
+  NanoSlot slots[4];
+  cudaStream_t side = nullptr, cap = nullptr;
+  std::vector<cudaEvent_t> events;
+  // graphs
+  std::map<std::vector<int>, cudaGraphExec_t> graphs;
+  int* err = nullptr;
+  ns_step_info info{};
+  int kernels_last = 0;
+};
+
+namespace {
+
+struct MetaLayout {
+  size_t tok, pos, seq, slot, tab, logits, total;
+};
+
+MetaLayout meta_layout(int B, int MB) {
+  MetaLayout m;
+  size_t o = 0;
+  m.tok = o; o += static_cast<size_t>(B) * 4;
+  m.pos = o; o += static_cast<size_t>(B) * 4;
+  m.seq = o; o += static_cast<size_t>(B) * 4;
+  o = (o + 15) & ~size_t(15);
+  m.slot = o; o += static_cast<size_t>(B) * 8;
+  m.tab = o; o += static_cast<size_t>(B) * MB * 4;
+  o = (o + 15) & ~size_t(15);
+  m.logits = o; o += 16;
+  m.total = o;
+  return m;
+}
+
+ns_status get_bmap(ns_ctx* h, const void* buf, int cols, int BN, const CUtensorMap** out) {
+  auto key = std::make_tuple(buf, BN);
+  auto it = h->bmaps.find(key);
+  if (it == h->bmaps.end()) {
+    CUtensorMap m;
+    NS_TRY(make_tmap(&m, buf, h->dtype, static_cast<uint64_t>(h->R), static_cast<uint64_t>(cols),
+                     static_cast<uint32_t>(BN)));
+    it = h->bmaps.emplace(key, m).first;
+  }
+  *out = &it->second;
+  return NS_OK;
+}
+
+ns_status init_proj(ns_ctx* h, Proj& p, int N, int K) {
+  p.N = N;
+  p.K = K;
+  choose_splits(N, K, h->sms, &p.splits, &p.kb_per);
+  return make_tmap(&p.mapA, p.w, h->dtype, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                   kGemmTileN);
+}
+
+ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
+  const int H = h->cfg.hidden;
+  std::vector<uint16_t> raw(H);
+  NS_CUDA(cudaMemcpy(raw.data(), src, H * 2, cudaMemcpyDefault));
+  std::vector<float> f(H);
+  for (int i = 0; i < H; ++i)
+    f[i] = h->dtype == NS_BF16 ? bf16_bits_to_float(raw[i]) : half_bits_to_float(raw[i]);
+  NS_CUDA(cudaMalloc(dst, H * sizeof(float)));
+  NS_CUDA(cudaMemcpy(*dst, f.data(), H * sizeof(float), cudaMemcpyHostToDevice));
+  return NS_OK;
+}
+
+ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
+                      int epi, const EpiArgs& e, NanoSlot& slot, cudaStream_t s) {
+  GemmParams p{};
+  p.M = m;
+  p.row0 = row0;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.BN = pick_bn(m);
+  p.splits = pr.splits;
+  p.kb_per_split = pr.kb_per;
+  p.nstage = gemm_pick_stages(p.BN);
+  p.epi = epi;
+  p.idesc = gemm_idesc(h->dtype, p.BN);
+  p.ws = slot.gemm_ws;
+  p.counters = slot.gemm_counters;
+  p.err = h->err;
+  p.e = e;
+  const CUtensorMap* mb = nullptr;
+  NS_TRY(get_bmap(h, x, x_cols, p.BN, &mb));
+  NS_CUDA(launch_gemm(&pr.mapA, mb, p, h->dtype, s, true));
+  h->kernels_last++;
+  return NS_OK;
+}
+
+// Enqueue one step for `B` rows on `s0` (and the side stream when nano-batched).
+ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
+  const ns_model_cfg& c = h->cfg;
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, F = c.ffn;
+  const int qd = Hq * d, kvd = Hkv * d;
+  const MetaLayout ml = meta_layout(B, c.max_blocks_per_seq);
+  const int* m_tok = reinterpret_cast<const int*>(h->meta_dev + ml.tok);
+  const int* m_pos = reinterpret_cast<const int*>(h->meta_dev + ml.pos);
+  const int* m_seq = reinterpret_cast<const int*>(h->meta_dev + ml.seq);
+  const long long* m_slot = reinterpret_cast<const long long*>(h->meta_dev + ml.slot);
+  const int* m_tab = reinterpret_cast<const int*>(h->meta_dev + ml.tab);
+  const unsigned long long* m_logits = reinterpret_cast<const unsigned long long*>(h->meta_dev + ml.logits);
+  h->kernels_last = 0;
+
+  // nano-batches: (row0, rows)
+  std::vector<std::pair<int, int>> nb;
+  if (h->n_split <= 1) {
+    nb.push_back({0, B});
+  } else {
+    int r = 0;
+    for (int i = 0; i < h->n_split; ++i) {
+      nb.push_back({r, h->split_sizes[i]});
+      r += h->split_sizes[i];
+    }
+  }
+  const int n = static_cast<int>(nb.size());
+  cudaStream_t st[2] = {s0, h->side};
+  // events: fork, join, and per (layer, nano-batch) QKV completion
+  const size_t need_ev = 2 + static_cast<size_t>(c.n_layers) * n;
+  while (h->events.size() < need_ev) {
+    cudaEvent_t ev;
+    NS_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    h->events.push_back(ev);
+  }
+  if (n > 1) {
+    NS_CUDA(cudaEventRecord(h->events[0], s0));
+    NS_CUDA(cudaStreamWaitEvent(h->side, h->events[0], 0));
+  }
+  const int G = Hq / Hkv;
+  const float scale_log2 = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)) * 1.4426950408889634);
+
+  EpiArgs norm{};  // common fused-RMSNorm inputs
+  norm.sumsq_in = h->sumsq;
+  norm.sumsq_tiles = H / kGemmTileN;
+  norm.sumsq_ld = h->R;
+  norm.norm_dim = H;
+  norm.eps = c.rms_eps;
+
+  for (int i = 0; i < n; ++i) {
+    EmbedParams ep{};
+    ep.embed = h->embed;
+    ep.token_ids = m_tok;
+    ep.positions = m_pos;
+    ep.vocab = c.vocab;
+    ep.hidden = H;
+    ep.gamma = h->layers[0].attn_norm;
+    ep.resid = h->resid;
+    ep.xn = h->xn;
+    ep.sumsq = h->sumsq;
+    ep.sumsq_ld = h->R;
+    ep.rope_cos = h->rope_cos;
+    ep.rope_sin = h->rope_sin;
+    ep.head_dim = d;
+    ep.theta = c.rope_theta;
+    ep.batch = nb[i].second;
+    ep.row0 = nb[i].first;
+    ep.err = h->err;
+    NS_CUDA(launch_embed(ep, h->dtype, st[i % 2], true));
+    h->kernels_last++;
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerDev& L = h->layers[l];
+    for (int i = 0; i < n; ++i) {
+      EpiArgs e = norm;
+      e.q_out = h->q;
+      e.k_pool = h->kpool[l];
+      e.v_pool = h->vpool[l];
+      e.slot_mapping = m_slot;
+      e.rope_cos = h->rope_cos;
+      e.rope_sin = h->rope_sin;
+      e.q_dim = qd;
+      e.kv_dim = kvd;
+      e.head_dim = d;
+      e.n_kv_heads = Hkv;
+      e.block_size = h->block_size;
+      e.pool_slots = static_cast<long long>(h->num_blocks) * h->block_size;
+      NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e, h->slots[i],
+                         st[i % 2]));
+      if (n > 1) NS_CUDA(cudaEventRecord(h->events[2 + static_cast<size_t>(l) * n + i], st[i % 2]));
+    }
+    for (int i = 0; i < n; ++i) {
+      cudaStream_t s = st[i % 2];
+      for (int j = 0; j < i; ++j)
+        if ((j % 2) != (i % 2)) NS_CUDA(cudaStreamWaitEvent(s, h->events[2 + static_cast<size_t>(l) * n + j], 0));
+      AttnParams ap{};
+      ap.q = h->q;
+      ap.q_row_stride = qd;
+      ap.k_pool = h->kpool[l];
+      ap.v_pool = h->vpool[l];
+      ap.block_tables = m_tab;
+      ap.mb = c.max_blocks_per_seq;
+      ap.seq_lens = m_seq;
+      ap.out = h->o;
+      ap.out_row_stride = qd;
+      ap.batch = nb[i].second;
+      ap.row0 = nb[i].first;
+      ap.n_kv_heads = Hkv;
+      ap.num_blocks = h->num_blocks;
+      ap.block_size = h->block_size;
+      ap.scale_log2 = scale_log2;
+      ap.max_chunks = h->max_chunks;
+      ap.partials = h->attn_partials;
+      ap.counters = h->attn_counters;
+      ap.err = h->err;
+      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
+      if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
+      NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+      h->kernels_last++;
+
+      EpiArgs eo{};
+      eo.resid = h->resid;
+      eo.xn_out = h->xn;
+      eo.gamma_next = L.ffn_norm;
+      eo.sumsq_out = h->sumsq;
+      eo.sumsq_ld = h->R;
+      eo.resid_dim = H;
+      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, h->slots[i], s));
+
+      EpiArgs eg = norm;
+      eg.act_out = h->act;
+      eg.ffn = F;
+      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, h->slots[i], s));
+
+      EpiArgs ed{};
+      ed.resid = h->resid;
+      ed.xn_out = h->xn;
+      ed.gamma_next = (l + 1 < c.n_layers) ? h->layers[l + 1].attn_norm : h->final_norm;
+      ed.sumsq_out = h->sumsq;
+      ed.sumsq_ld = h->R;
+      ed.resid_dim = H;
+      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, h->slots[i], s));
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    EpiArgs el = norm;
+    el.out_ptr_slot = m_logits;
+    el.ldo = c.vocab;
+    NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el, h->slots[i],
+                       st[i % 2]));
+  }
+  if (n > 1) {
+    NS_CUDA(cudaEventRecord(h->events[1], h->side));
+    NS_CUDA(cudaStreamWaitEvent(s0, h->events[1], 0));
+  }
+  return NS_OK;
+}
+
+std::vector<int> graph_key(const ns_ctx* h, int B) {
+  std::vector<int> k{B, h->n_split, h->attn_budget};
+  for (int v : h->split_sizes) k.push_back(v);
+  return k;
+}
+
+ns_status get_graph(ns_ctx* h, int B, cudaGraphExec_t* out) {
+  auto key = graph_key(h, B);
+  auto it = h->graphs.find(key);
+  if (it != h->graphs.end()) {
+    *out = it->second;
+    return NS_OK;
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  NS_CUDA(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+  ns_status st = enqueue_step(h, B, h->cap);
+  cudaGraph_t g = nullptr;
+  cudaError_t ce = cudaStreamEndCapture(h->cap, &g);
+  if (st != NS_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (ce != cudaSuccess) return fail(NS_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(ce));
+  cudaGraphExec_t ex = nullptr;
+  ce = cudaGraphInstantiate(&ex, g, 0);
+  size_t n_nodes = 0;
+  cudaGraphGetNodes(g, nullptr, &n_nodes);
+  std::vector<cudaGraphNode_t> nodes(n_nodes);
+  int kernels = 0;
+  if (n_nodes) {
+    cudaGraphGetNodes(g, nodes.data(), &n_nodes);
+    for (auto nd : nodes) {
+      cudaGraphNodeType t;
+      if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
+    }
+  }
+  cudaGraphDestroy(g);
+  if (ce != cudaSuccess) return fail(NS_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ce));
+  h->graphs.emplace(key, ex);
+  h->info.graphs_cached = static_cast<int>(h->graphs.size());
+  h->info.kernels_per_step = kernels;
+  h->info.last_capture_ms =
+      std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  *out = ex;
+  return NS_OK;
+}
+
+void free_proj(Proj& p) {
+  if (p.owned && p.w) cudaFree(p.w);
+  p.w = nullptr;
+}
+
+ns_status alloc_slots(ns_ctx* h) {
+  size_t ws = 0;
+  int cnt = 1;
+  auto acc = [&](const Proj& p) {
+    ws = std::max(ws, gemm_ws_bytes(p.N, p.splits, h->R));
+    cnt = std::max(cnt, gemm_counter_count(p.N, h->R));
+  };
+  for (auto& L : h->layers) {
+    acc(L.qkv);
+    acc(L.o);
+    acc(L.gu);
+    acc(L.down);
+  }
+  acc(h->lm);
+  for (auto& s : h->slots) {
+    if (ws) NS_CUDA(cudaMalloc(&s.gemm_ws, ws));
+    NS_CUDA(cudaMalloc(&s.gemm_counters, cnt * sizeof(int)));
+    NS_CUDA(cudaMemset(s.gemm_counters, 0, cnt * sizeof(int)));
+  }
+  return NS_OK;
+}
+
+}  // namespace
+
+// ================================================================================== C ABI
+
+extern "C" {
+
+const char* ns_status_str(ns_status s) {
+  switch (s) {
+    case NS_OK: return "NS_OK";
+    case NS_ERR_INVALID_ARG: return "NS_ERR_INVALID_ARG";
+    case NS_ERR_OUT_OF_MEMORY: return "NS_ERR_OUT_OF_MEMORY";
+    case NS_ERR_CUDA: return "NS_ERR_CUDA";
+    case NS_ERR_UNSUPPORTED: return "NS_ERR_UNSUPPORTED";
+    case NS_ERR_NOT_INITIALIZED: return "NS_ERR_NOT_INITIALIZED";
+    case NS_ERR_DEVICE_CHECK: return "NS_ERR_DEVICE_CHECK";
+    case NS_ERR_OUT_OF_BLOCKS: return "NS_ERR_OUT_OF_BLOCKS";
+  }
+  return "NS_ERR_UNKNOWN";
+}
+
+const char* ns_last_error_message(void) { return g_msg.c_str(); }
+
+void ns_destroy(ns_handle h) {
+  if (h == nullptr) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->dev);
+  cudaDeviceSynchronize();
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& L : h->layers) {
+    free_proj(L.qkv);
+    free_proj(L.o);
+    free_proj(L.gu);
+    free_proj(L.down);
+    cudaFree(L.attn_norm);
+    cudaFree(L.ffn_norm);
+  }
+  free_proj(h->lm);
+  cudaFree(h->embed);
+  cudaFree(h->final_norm);
+  cudaFree(h->resid);
+  cudaFree(h->xn);
+  cudaFree(h->sumsq);
+  cudaFree(h->q);
+  cudaFree(h->o);
+  cudaFree(h->act);
+  cudaFree(h->rope_cos);
+  cudaFree(h->rope_sin);
+  cudaFree(h->pools);
+  cudaFree(h->attn_counters);
+  cudaFree(h->attn_partials);
+  for (auto& s : h->slots) {
+    cudaFree(s.gemm_ws);
+    cudaFree(s.gemm_counters);
+  }
+  cudaFreeHost(h->meta_host);
+  cudaFree(h->meta_dev);
+  cudaFree(h->err);
+  if (h->meta_done) cudaEventDestroy(h->meta_done);
+  for (auto ev : h->events) cudaEventDestroy(ev);
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->cap) cudaStreamDestroy(h->cap);
+  delete h;
+  cudaSetDevice(prev);
+}
+
+ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out) {
+  if (cfg == nullptr || w == nullptr || out == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  const ns_model_cfg& c = *cfg;
+  if (c.hidden <= 0 || c.n_layers <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 ||
+      c.ffn <= 0 || c.vocab <= 0 || c.max_batch <= 0 || c.max_blocks_per_seq <= 0 ||
+      c.n_q_heads % c.n_kv_heads != 0 || !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.0))
+    return fail(NS_ERR_INVALID_ARG, "model dims");
+  if (c.dtype != NS_F16 && c.dtype != NS_BF16) return fail(NS_ERR_INVALID_ARG, "dtype");
+  if (c.max_batch > kMaxRows) return fail(NS_ERR_UNSUPPORTED, "max_batch above 4096");
+  const int H = c.hidden, d = c.head_dim, qd = c.n_q_heads * d, kvd = c.n_kv_heads * d, F = c.ffn;
+  const int G = c.n_q_heads / c.n_kv_heads;
+  if (H % 128 || qd % 128 || kvd % 128 || (2 * F) % 128 || c.vocab % 128 || F % 64 ||
+      !attn_supported(d, G, 16))
+    return fail(NS_ERR_UNSUPPORTED, "shape not implemented (see ns.h)");
+  if (w->embed == nullptr || w->final_norm == nullptr || w->layers == nullptr ||
+      (!c.tie_embeddings && w->lm_head == nullptr))
+    return fail(NS_ERR_INVALID_ARG, "weight pointers");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const ns_layer_weights& lw = w->layers[l];
+    if (!lw.attn_norm || !lw.wq || !lw.wk || !lw.wv || !lw.wo || !lw.ffn_norm || !lw.w_gate ||
+        !lw.w_up || !lw.w_down)
+      return fail(NS_ERR_INVALID_ARG, "layer weight pointers");
+  }
+  ns_ctx* h = new ns_ctx();
+  h->cfg = c;
+  h->dtype = c.dtype;
+  h->R = c.max_batch;
+  cudaGetDevice(&h->dev);
+  h->sms = device_sms();
+  auto bail = [&](ns_status s) {
+    std::string keep = g_msg;
+    ns_destroy(h);
+    g_msg = keep;
+    return s;
+  };
+#define CK(expr)                       \
+  do {                                 \
+    ns_status s__ = (expr);            \
+    if (s__ != NS_OK) return bail(s__); \
+  } while (0)
+  auto cuda = [&](cudaError_t e, const char* what) -> ns_status {
+    if (e == cudaSuccess) return NS_OK;
+    return fail(e == cudaErrorMemoryAllocation ? NS_ERR_OUT_OF_MEMORY : NS_ERR_CUDA,
+                std::string(what) + ": " + cudaGetErrorString(e));
+  };
+  const size_t e2 = 2;
+  h->layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const ns_layer_weights& lw = w->layers[l];
+    LayerDev& L = h->layers[l];
+    // QKV concatenated: rows q | k | v
+    CK(cuda(cudaMalloc(&L.qkv.w, static_cast<size_t>(qd + 2 * kvd) * H * e2), "malloc qkv"));
+    uint8_t* q8 = static_cast<uint8_t*>(L.qkv.w);
+    CK(cuda(cudaMemcpy(q8, lw.wq, static_cast<size_t>(qd) * H * e2, cudaMemcpyDefault), "copy wq"));
+    CK(cuda(cudaMemcpy(q8 + static_cast<size_t>(qd) * H * e2, lw.wk, static_cast<size_t>(kvd) * H * e2,
+                       cudaMemcpyDefault), "copy wk"));
+    CK(cuda(cudaMemcpy(q8 + static_cast<size_t>(qd + kvd) * H * e2, lw.wv,
+                       static_cast<size_t>(kvd) * H * e2, cudaMemcpyDefault), "copy wv"));
+    CK(init_proj(h, L.qkv, qd + 2 * kvd, H));
+    CK(cuda(cudaMalloc(&L.o.w, static_cast<size_t>(H) * qd * e2), "malloc wo"));
+    CK(cuda(cudaMemcpy(L.o.w, lw.wo, static_cast<size_t>(H) * qd * e2, cudaMemcpyDefault), "copy wo"));
+    CK(init_proj(h, L.o, H, qd));
+    // gate/up interleaved in 64-row groups: [gate 64j..64j+63 ; up 64j..64j+63] per 128 rows
+    CK(cuda(cudaMalloc(&L.gu.w, static_cast<size_t>(2 * F) * H * e2), "malloc gate/up"));
+    const size_t grp = static_cast<size_t>(64) * H * e2;
+    CK(cuda(cudaMemcpy2D(L.gu.w, 2 * grp, lw.w_gate, grp, grp, F / 64, cudaMemcpyDefault), "copy gate"));
+    CK(cuda(cudaMemcpy2D(static_cast<uint8_t*>(L.gu.w) + grp, 2 * grp, lw.w_up, grp, grp, F / 64,
+                         cudaMemcpyDefault), "copy up"));
+    CK(init_proj(h, L.gu, 2 * F, H));
+    CK(cuda(cudaMalloc(&L.down.w, static_cast<size_t>(H) * F * e2), "malloc down"));
+    CK(cuda(cudaMemcpy(L.down.w, lw.w_down, static_cast<size_t>(H) * F * e2, cudaMemcpyDefault), "copy down"));
+    CK(init_proj(h, L.down, H, F));
+    CK(copy_gain(h, lw.attn_norm, &L.attn_norm));
+    CK(copy_gain(h, lw.ffn_norm, &L.ffn_norm));
+  }
+  CK(cuda(cudaMalloc(&h->embed, static_cast<size_t>(c.vocab) * H * e2), "malloc embed"));
+  CK(cuda(cudaMemcpy(h->embed, w->embed, static_cast<size_t>(c.vocab) * H * e2, cudaMemcpyDefault), "copy embed"));
+  CK(copy_gain(h, w->final_norm, &h->final_norm));
+  if (c.tie_embeddings) {
+    h->lm.w = h->embed;
+    h->lm.owned = false;
+  } else {
+    CK(cuda(cudaMalloc(&h->lm.w, static_cast<size_t>(c.vocab) * H * e2), "malloc lm_head"));
+    CK(cuda(cudaMemcpy(h->lm.w, w->lm_head, static_cast<size_t>(c.vocab) * H * e2, cudaMemcpyDefault),
+            "copy lm_head"));
+  }
+  CK(init_proj(h, h->lm, c.vocab, H));
+  // activations
+  const size_t R = h->R;
+  CK(cuda(cudaMalloc(&h->resid, R * H * 4), "malloc resid"));
+  CK(cuda(cudaMalloc(&h->xn, R * H * e2), "malloc xn"));
+  CK(cuda(cudaMalloc(&h->sumsq, R * (H / 128) * 4), "malloc sumsq"));
+  CK(cuda(cudaMalloc(&h->q, R * qd * e2), "malloc q"));
+  CK(cuda(cudaMalloc(&h->o, R * qd * e2), "malloc o"));
+  CK(cuda(cudaMalloc(&h->act, R * F * e2), "malloc act"));
+  CK(cuda(cudaMalloc(&h->rope_cos, R * (d / 2) * 4), "malloc rope"));
+  CK(cuda(cudaMalloc(&h->rope_sin, R * (d / 2) * 4), "malloc rope"));
+  CK(cuda(cudaMemset(h->xn, 0, R * H * e2), "memset"));
+  CK(cuda(cudaMemset(h->o, 0, R * qd * e2), "memset"));
+  CK(cuda(cudaMemset(h->act, 0, R * F * e2), "memset"));
+  CK(alloc_slots(h));
+  // metadata: pinned host staging + device copy, sized for max_batch
+  h->meta_cap = meta_layout(h->R, c.max_blocks_per_seq).total;
+  CK(cuda(cudaMallocHost(&h->meta_host, h->meta_cap), "pinned metadata"));
+  CK(cuda(cudaMalloc(&h->meta_dev, h->meta_cap), "metadata"));
+  CK(cuda(cudaEventCreateWithFlags(&h->meta_done, cudaEventDisableTiming), "event"));
+  CK(cuda(cudaMalloc(&h->err, sizeof(int)), "err"));
+  CK(cuda(cudaMemset(h->err, 0, sizeof(int)), "err"));
+  CK(cuda(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking), "stream"));
+  CK(cuda(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking), "stream"));
+  CK(cuda(cudaDeviceSynchronize(), "create sync"));
+#undef CK
+  *out = h;
+  return NS_OK;
+}
+
+ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (h->pools != nullptr) return fail(NS_ERR_INVALID_ARG, "KV pools already allocated");
+  if (num_blocks <= 0 || block_size != 16)
+    return fail(num_blocks <= 0 ? NS_ERR_INVALID_ARG : NS_ERR_UNSUPPORTED, "num_blocks > 0, block_size 16");
+  const ns_model_cfg& c = h->cfg;
+  const size_t pool = static_cast<size_t>(num_blocks) * c.n_kv_heads * block_size * c.head_dim * 2;
+  NS_CUDA(cudaSetDevice(h->dev));
+  NS_CUDA(cudaMalloc(&h->pools, pool * 2 * c.n_layers));
+  h->kpool.resize(c.n_layers);
+  h->vpool.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    h->kpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l));
+    h->vpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l) + 1);
+  }
+  h->num_blocks = num_blocks;
+  h->block_size = block_size;
+  h->max_chunks = (c.max_blocks_per_seq * block_size + kAttnChunkTokens - 1) / kAttnChunkTokens;
+  const int G = c.n_q_heads / c.n_kv_heads;
+  const size_t rows_heads = static_cast<size_t>(h->R) * c.n_kv_heads;
+  NS_CUDA(cudaMalloc(&h->attn_counters, rows_heads * sizeof(int)));
+  NS_CUDA(cudaMemset(h->attn_counters, 0, rows_heads * sizeof(int)));
+  NS_CUDA(cudaMalloc(&h->attn_partials,
+                     rows_heads * h->max_chunks * G * (c.head_dim + 2) * sizeof(float)));
+  h->pool.num_blocks = num_blocks;
+  h->pool.block_size = block_size;
+  h->pool.mb = c.max_blocks_per_seq;
+  h->pool.free_list.clear();
+  for (int i = 0; i < num_blocks; ++i) h->pool.free_list.push_back(i);
+  return NS_OK;
+}
+
+ns_status ns_kv_layer_ptrs(ns_handle h, int layer, void** k_pool, void** v_pool) {
+  if (h == nullptr || k_pool == nullptr || v_pool == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  if (layer < 0 || layer >= h->cfg.n_layers) return fail(NS_ERR_INVALID_ARG, "layer");
+  *k_pool = h->kpool[layer];
+  *v_pool = h->vpool[layer];
+  return NS_OK;
+}
+
+ns_status ns_kv_prepare_step(ns_handle h, int batch, const int32_t* positions, int32_t* block_tables,
+                             int64_t* slot_mapping) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  return pool_prepare(&h->pool, batch, positions, block_tables, slot_mapping);
+}
+
+ns_status ns_kv_reserve(ns_handle h, int n, int32_t* out_ids) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  return pool_reserve(&h->pool, n, out_ids);
+}
+
+ns_status ns_kv_release(ns_handle h, const int32_t* block_ids, int n) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  return pool_release(&h->pool, block_ids, n);
+}
+
+ns_status ns_kv_free_count(ns_handle h, int* n_free) {
+  if (h == nullptr || n_free == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  *n_free = static_cast<int>(h->pool.free_list.size());
+  return NS_OK;
+}
+
+ns_status ns_pool_create(int num_blocks, int block_size, int max_blocks_per_seq, ns_pool* out) {
+  if (out == nullptr || num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
+    return fail(NS_ERR_INVALID_ARG, "pool arguments");
+  ns_block_pool* p = new ns_block_pool();
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->mb = max_blocks_per_seq;
+  for (int i = 0; i < num_blocks; ++i) p->free_list.push_back(i);
+  *out = p;
+  return NS_OK;
+}
+
+void ns_pool_destroy(ns_pool p) { delete p; }
+
+ns_status ns_pool_prepare_step(ns_pool p, int batch, const int32_t* positions, int32_t* block_tables,
+                               int64_t* slot_mapping) {
+  if (p == nullptr) return fail(NS_ERR_INVALID_ARG, "null pool");
+  return pool_prepare(p, batch, positions, block_tables, slot_mapping);
+}
+
+ns_status ns_pool_reserve(ns_pool p, int n, int32_t* out_ids) {
+  if (p == nullptr) return fail(NS_ERR_INVALID_ARG, "null pool");
+  return pool_reserve(p, n, out_ids);
+}
+
+ns_status ns_pool_release(ns_pool p, const int32_t* block_ids, int n) {
+  if (p == nullptr) return fail(NS_ERR_INVALID_ARG, "null pool");
+  return pool_release(p, block_ids, n);
+}
+
+ns_status ns_pool_free_count(ns_pool p, int* n_free) {
+  if (p == nullptr || n_free == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  *n_free = static_cast<int>(p->free_list.size());
+  return NS_OK;
+}
+
+ns_status ns_check_step_metadata(int num_blocks, int block_size, int max_blocks_per_seq, int vocab,
+                                 int max_batch, int batch, const int32_t* token_ids,
+                                 const int32_t* positions, const int32_t* block_tables,
+                                 const int32_t* seq_lens, const int64_t* slot_mapping) {
+  if (num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 1 || vocab < 1)
+    return fail(NS_ERR_INVALID_ARG, "pool arguments");
+  return check_meta(num_blocks, block_size, max_blocks_per_seq, vocab, max_batch, batch, token_ids,
+                    positions, block_tables, seq_lens, slot_mapping);
+}
+
+ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_cta_budget) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (n_split < 1 || n_split > 4) return fail(NS_ERR_INVALID_ARG, "n_split must be 1..4");
+  std::vector<int> s;
+  if (n_split > 1) {
+    if (sizes == nullptr) return fail(NS_ERR_INVALID_ARG, "sizes required for n_split > 1");
+    for (int i = 0; i < n_split; ++i) {
+      if (sizes[i] <= 0) return fail(NS_ERR_INVALID_ARG, "nano-batch sizes must be positive");
+      s.push_back(sizes[i]);
+    }
+  }
+  h->n_split = n_split;
+  h->split_sizes = s;
+  h->attn_budget = attn_cta_budget > 0 ? attn_cta_budget : 0;
+  return NS_OK;
+}
+
+ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const int32_t* positions,
+                         const int32_t* block_tables, const int32_t* seq_lens,
+                         const int64_t* slot_mapping, float* logits_out, ns_stream_t stream) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  const ns_model_cfg& c = h->cfg;
+  if (logits_out == nullptr) return fail(NS_ERR_INVALID_ARG, "null logits_out");
+  const int bs = h->block_size, mb = c.max_blocks_per_seq;
+  NS_TRY(check_meta(h->num_blocks, bs, mb, c.vocab, c.max_batch, batch, token_ids, positions,
+                    block_tables, seq_lens, slot_mapping));
+  if (h->n_split > 1) {
+    int sum = 0;
+    for (int v : h->split_sizes) sum += v;
+    if (sum != batch) return fail(NS_ERR_INVALID_ARG, "nano-batch sizes do not sum to the batch");
+  }
+  NS_CUDA(cudaSetDevice(h->dev));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one packed metadata buffer, one host-to-device copy
+  if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
+  const MetaLayout ml = meta_layout(batch, mb);
+  uint8_t* mh = h->meta_host;
+  std::memcpy(mh + ml.tok, token_ids, batch * 4);
+  std::memcpy(mh + ml.pos, positions, batch * 4);
+  std::memcpy(mh + ml.seq, seq_lens, batch * 4);
+  std::memcpy(mh + ml.slot, slot_mapping, batch * 8);
+  std::memcpy(mh + ml.tab, block_tables, static_cast<size_t>(batch) * mb * 4);
+  const unsigned long long lp = reinterpret_cast<unsigned long long>(logits_out);
+  std::memcpy(mh + ml.logits, &lp, 8);
+  NS_CUDA(cudaMemcpyAsync(h->meta_dev, mh, ml.total, cudaMemcpyHostToDevice, s));
+  NS_CUDA(cudaEventRecord(h->meta_done, s));
+  h->meta_pending = true;
+  if (c.use_graphs) {
+    cudaGraphExec_t ex = nullptr;
+    NS_TRY(get_graph(h, batch, &ex));
+    NS_CUDA(cudaGraphLaunch(ex, s));
+  } else {
+    NS_TRY(enqueue_step(h, batch, s));
+    h->info.kernels_per_step = h->kernels_last;
+  }
+  h->info.steps++;
+  return NS_OK;
+}
+
+ns_status ns_get_step_info(ns_handle h, ns_step_info* out) {
+  if (h == nullptr || out == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  *out = h->info;
+  return NS_OK;
+}
+
+ns_status ns_get_device_error(ns_handle h, int* code) {
+  if (code == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  int* word = nullptr;
+  if (h != nullptr) {
+    NS_CUDA(cudaSetDevice(h->dev));
+    word = h->err;
+  } else {
+    DevScratch* sc = nullptr;
+    NS_TRY(scratch_get(0, 0, &sc));
+    word = sc->err;
+  }
+  NS_CUDA(cudaDeviceSynchronize());
+  NS_CUDA(cudaMemcpy(code, word, sizeof(int), cudaMemcpyDeviceToHost));
+  NS_CUDA(cudaMemset(word, 0, sizeof(int)));
+  return NS_OK;
+}
+
+ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                         const int32_t* seq_lens, void* out, int batch, int n_q_heads, int n_kv_heads,
+                         int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                         int dtype, ns_stream_t stream) {
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return fail(NS_ERR_INVALID_ARG, "null argument");
+  if (batch < 1 || batch > kMaxRows || n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads ||
+      max_blocks_per_seq < 1 || num_blocks < 1 || !(scale > 0.f) || (dtype != NS_F16 && dtype != NS_BF16))
+    return fail(NS_ERR_INVALID_ARG, "attention arguments");
+  const int G = n_q_heads / n_kv_heads;
+  if (!attn_supported(head_dim, G, block_size)) return fail(NS_ERR_UNSUPPORTED, "attention shape");
+  const int max_chunks = (max_blocks_per_seq * block_size + kAttnChunkTokens - 1) / kAttnChunkTokens;
+  const size_t rows_heads = static_cast<size_t>(batch) * n_kv_heads;
+  DevScratch* sc = nullptr;
+  NS_TRY(scratch_get(rows_heads * max_chunks * G * (head_dim + 2) * sizeof(float), rows_heads, &sc));
+  AttnParams ap{};
+  ap.q = q;
+  ap.q_row_stride = static_cast<long long>(n_q_heads) * head_dim;
+  ap.k_pool = k_pool;
+  ap.v_pool = v_pool;
+  ap.block_tables = block_tables;
+  ap.mb = max_blocks_per_seq;
+  ap.seq_lens = seq_lens;
+  ap.out = out;
+  ap.out_row_stride = static_cast<long long>(n_q_heads) * head_dim;
+  ap.batch = batch;
+  ap.row0 = 0;
+  ap.n_kv_heads = n_kv_heads;
+  ap.num_blocks = num_blocks;
+  ap.block_size = block_size;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.max_chunks = max_chunks;
+  ap.partials = static_cast<float*>(sc->buf);
+  ap.counters = sc->counters;
+  ap.err = sc->err;
+  const int cap = attn_max_grid(dtype, head_dim, G, batch);
+  const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
+  const int grid = static_cast<int>(std::min<long long>(cap, units));
+  NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));
+  return NS_OK;
+}
+
+ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k, int dtype, ns_stream_t stream) {
+  if (!w || !x || !y) return fail(NS_ERR_INVALID_ARG, "null argument");
+  if (m < 1 || m > kMaxRows || n < 128 || k < 64 || (dtype != NS_F16 && dtype != NS_BF16))
+    return fail(NS_ERR_INVALID_ARG, "linear arguments");
+  if (n % 128 || k % 64) return fail(NS_ERR_UNSUPPORTED, "n % 128 and k % 64 must be 0");
+  Proj pr;
+  pr.w = const_cast<void*>(w);
+  pr.owned = false;
+  pr.N = n;
+  pr.K = k;
+  choose_splits(n, k, device_sms(), &pr.splits, &pr.kb_per);
+  NS_TRY(make_tmap(&pr.mapA, w, dtype, static_cast<uint64_t>(n), static_cast<uint64_t>(k), kGemmTileN));
+  GemmParams p{};
+  p.M = m;
+  p.row0 = 0;
+  p.N = n;
+  p.K = k;
+  p.BN = pick_bn(m);
+  p.splits = pr.splits;
+  p.kb_per_split = pr.kb_per;
+  p.nstage = gemm_pick_stages(p.BN);
+  p.epi = EPI_F32;
+  p.idesc = gemm_idesc(dtype, p.BN);
+  DevScratch* sc = nullptr;
+  NS_TRY(scratch_get(gemm_ws_bytes(n, pr.splits, m) + 256, gemm_counter_count(n, m), &sc));
+  p.ws = static_cast<float*>(sc->buf);
+  p.counters = sc->counters;
+  p.err = sc->err;
+  p.e.out_f32 = y;
+  p.e.ldo = n;
+  CUtensorMap mb;
+  NS_TRY(make_tmap(&mb, x, dtype, static_cast<uint64_t>(m), static_cast<uint64_t>(k), static_cast<uint32_t>(p.BN)));
+  NS_CUDA(launch_gemm(&pr.mapA, &mb, p, dtype, reinterpret_cast<cudaStream_t>(stream), false));
+  return NS_OK;
+}
+
+ns_status ns_greedy_argmax(const float* logits, int batch, int vocab, int32_t* out_ids, ns_stream_t stream) {
+  if (!logits || !out_ids || batch < 1 || vocab < 1) return fail(NS_ERR_INVALID_ARG, "argmax arguments");
+  NS_CUDA(launch_argmax(logits, batch, vocab, out_ids, reinterpret_cast<cudaStream_t>(stream)));
+  return NS_OK;
+}
+
+}  // extern "C"

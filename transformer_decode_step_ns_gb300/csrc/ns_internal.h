@@ -1,0 +1,123 @@
+// Internal interfaces between the host runtime (ns_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ns.h"
+
+namespace ns {
+
+constexpr int kGemmTileN = 128;   // output features per CTA (UMMA M)
+constexpr int kGemmTileK = 64;    // K per pipeline stage (one 128-byte swizzle row)
+constexpr int kGemmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kMaxBN = 256;       // token tile (UMMA N) upper bound
+constexpr int kAttnChunkTokens = 256;  // static split-K chunk of the decode attention
+constexpr int kMaxRows = 4096;
+
+enum EpiMode : int {
+  EPI_F32 = 0,     // y = acc (* rs) -> fp32 [tok][ldo]
+  EPI_QKV = 1,     // rs scale, RoPE on q/k, q -> q_out, k/v -> paged pools at slot_mapping
+  EPI_RESID = 2,   // resid += acc; xn = resid * gamma_next; per-tile sum of squares
+  EPI_SWIGLU = 3,  // rows [0,64) gate, [64,128) up: act = silu(rs g) * (rs u)
+};
+
+struct EpiArgs {
+  // fused RMSNorm scale: rs[tok] = rsqrt(sum_t sumsq_in[t * sumsq_ld + tok] / norm_dim + eps)
+  const float* sumsq_in;
+  int sumsq_tiles, sumsq_ld, norm_dim;
+  float eps;
+  // EPI_F32
+  float* out_f32;
+  long long ldo;
+  const unsigned long long* out_ptr_slot;  // when set, the output base is read from here
+  // EPI_QKV
+  void* q_out;
+  void* k_pool;
+  void* v_pool;
+  const long long* slot_mapping;
+  const float* rope_cos;
+  const float* rope_sin;
+  int q_dim, kv_dim, head_dim, n_kv_heads, block_size;
+  long long pool_slots;
+  // EPI_RESID
+  float* resid;
+  void* xn_out;
+  const float* gamma_next;
+  float* sumsq_out;
+  int resid_dim;
+  // EPI_SWIGLU
+  void* act_out;
+  int ffn;
+};
+
+struct GemmParams {
+  int M;        // rows (tokens) in this launch
+  int row0;     // first row in the activation / output buffers
+  int N, K;     // output features, reduction length
+  int BN;       // token tile, multiple of 16, 16..256
+  int splits;   // split-K count
+  int kb_per_split;
+  int nstage;
+  int epi;
+  uint32_t idesc;
+  float* ws;       // split-K partial tiles
+  int* counters;   // per output tile arrival counters (zero between launches)
+  int* err;
+  EpiArgs e;
+};
+
+struct AttnParams {
+  const void* q;
+  long long q_row_stride;  // elements between rows of q
+  const void* k_pool;
+  const void* v_pool;
+  const int* block_tables;
+  int mb;                  // block-table row width
+  const int* seq_lens;
+  void* out;
+  long long out_row_stride;
+  int batch, row0, n_kv_heads, num_blocks, block_size;
+  float scale_log2;        // softmax scale * log2(e)
+  int max_chunks;          // ceil(mb * block_size / chunk): partial slots per (row, kv head)
+  float* partials;         // [rows][n_kv_heads][max_chunks][G][head_dim + 2]
+  int* counters;           // [rows][n_kv_heads], zero between launches
+  int* err;
+};
+
+struct EmbedParams {
+  const void* embed;
+  const int* token_ids;
+  const int* positions;
+  int vocab, hidden;
+  const float* gamma;  // first layer's attention-norm gain (fp32)
+  float* resid;
+  void* xn;
+  float* sumsq;
+  int sumsq_ld;
+  float* rope_cos;
+  float* rope_sin;
+  int head_dim;
+  double theta;
+  int batch, row0;
+  int* err;
+};
+
+// Kernel launchers (return the launch error; `pdl` adds programmatic stream serialisation).
+size_t gemm_smem_bytes(int BN, int nstage);
+int gemm_pick_stages(int BN);
+uint32_t gemm_idesc(int dtype, int BN);
+cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                        int dtype, cudaStream_t s, bool pdl);
+
+bool attn_supported(int head_dim, int group, int block_size);
+int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
+cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
+                        cudaStream_t s, bool pdl);
+
+cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
+cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
+                          cudaStream_t s);
+
+}  // namespace ns
