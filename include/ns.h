@@ -228,6 +228,20 @@ typedef struct {
 } ns_step_info;
 ns_status ns_get_step_info(ns_handle h, ns_step_info* out);
 
+/* Per-kernel timing of eager steps (for roofline accounting).  While on, ns_decode_step
+ * launches the kernels eagerly (graphs are bypassed) with a CUDA event pair around each launch
+ * on the stream the kernel runs on.  Kinds: 0 embedding + RoPE table, 1 QKV projection,
+ * 2 attention, 3 O projection, 4 gate/up projection, 5 down projection, 6 LM head.
+ * ns_get_kernel_timing synchronises, returns launches and summed milliseconds per kind since
+ * the last read, and clears them. */
+#define NS_KERNEL_KINDS 8
+typedef struct {
+  int launches[NS_KERNEL_KINDS];
+  double total_ms[NS_KERNEL_KINDS];
+} ns_kernel_timing;
+ns_status ns_set_kernel_timing(ns_handle h, int on);
+ns_status ns_get_kernel_timing(ns_handle h, ns_kernel_timing* out);
+
 /* Human-readable name of a status; thread-local text of the last failure. */
 const char* ns_status_str(ns_status s);
 const char* ns_last_error_message(void);

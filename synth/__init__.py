@@ -332,3 +332,103 @@ def ctx_log_uniform(seed: int, name: str, batch: int, lo: int, hi: int) -> np.nd
 
 
 __all__: List[str] = [n for n in dir() if not n.startswith("_")]
+
+
+# --------------------------------------------------------------------------------------------
+# Device-side draws (same generator, for pools and weights too large to draw on the host)
+# --------------------------------------------------------------------------------------------
+
+_FILL_LIB = None
+
+
+def _fill_lib():
+    global _FILL_LIB
+    if _FILL_LIB is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth.so")
+        if not os.path.exists(path):
+            build_fill()
+        L = ctypes.CDLL(path)
+        L.synth_fill_normal.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_ulonglong,
+                                        ctypes.c_ulonglong, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_int, ctypes.c_void_p]
+        L.synth_fill_normal.restype = ctypes.c_int
+        _FILL_LIB = L
+    return _FILL_LIB
+
+
+def build_fill(force: bool = False) -> str:
+    """Compile synth/csrc/fill.cu into synth/libsynth.so (sm_103a)."""
+    import os
+    import shutil
+    import subprocess
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "csrc", "fill.cu")
+    out = os.path.join(here, "libsynth.so")
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared", "-Xcompiler",
+           "-fPIC", "-cudart", "shared", "-o", out, src]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for fill.cu:\n{r.stderr}")
+    return out
+
+
+def fill_normal_device(ptr: int, count: int, seed: int, name: str, dtype: str, std: float = 1.0,
+                       mean: float = 0.0, offset: int = 0, stream: int = 0) -> None:
+    """Write ``count`` draws of stream ``name`` (elements offset .. offset+count-1) at device
+    address ``ptr`` in storage dtype: the same values ``normal()`` returns on the host."""
+    r = _fill_lib().synth_fill_normal(ptr, count, stream_key(seed, name), offset, float(mean),
+                                      float(std), 1 if dtype == BF16 else 0, stream or None)
+    if r != 0:
+        raise RuntimeError(f"synth_fill_normal failed ({r})")
+
+
+def normal_device(seed: int, name: str, shape: Sequence[int], dtype: str, std: float = 1.0,
+                  mean: float = 0.0):
+    """A torch CUDA tensor (float16 / bfloat16) holding ``normal(seed, name, shape, ...)``."""
+    import torch
+    t = torch.empty(tuple(shape), dtype=torch.float16 if dtype == F16 else torch.bfloat16,
+                    device="cuda")
+    fill_normal_device(t.data_ptr(), t.numel(), seed, name, dtype, std, mean,
+                       stream=torch.cuda.current_stream().cuda_stream)
+    return t
+
+
+def model_weights_device(shape: ModelShape, seed: int, std: float = 0.02,
+                         gamma_std: float = 0.0) -> Dict[str, object]:
+    """``model_weights`` drawn on the GPU (same values), as torch CUDA tensors."""
+    import torch
+    tdt = torch.float16 if shape.dtype == F16 else torch.bfloat16
+    h = shape.hidden
+
+    def gain(name):
+        if gamma_std == 0.0:
+            return torch.ones(h, dtype=tdt, device="cuda")
+        return normal_device(seed, name, (h,), shape.dtype, std=gamma_std, mean=1.0)
+
+    layers = []
+    for l in range(shape.n_layers):
+        p = f"layer{l}."
+        layers.append({
+            "attn_norm": gain(p + "attn_norm"),
+            "wq": normal_device(seed, p + "wq", (shape.q_dim, h), shape.dtype, std),
+            "wk": normal_device(seed, p + "wk", (shape.kv_dim, h), shape.dtype, std),
+            "wv": normal_device(seed, p + "wv", (shape.kv_dim, h), shape.dtype, std),
+            "wo": normal_device(seed, p + "wo", (h, shape.q_dim), shape.dtype, std),
+            "ffn_norm": gain(p + "ffn_norm"),
+            "w_gate": normal_device(seed, p + "w_gate", (shape.ffn, h), shape.dtype, std),
+            "w_up": normal_device(seed, p + "w_up", (shape.ffn, h), shape.dtype, std),
+            "w_down": normal_device(seed, p + "w_down", (h, shape.ffn), shape.dtype, std),
+        })
+    return {
+        "embed": normal_device(seed, "embed", (shape.vocab, h), shape.dtype, std),
+        "final_norm": gain("final_norm"),
+        "lm_head": None if shape.tie_embeddings else normal_device(seed, "lm_head",
+                                                                   (shape.vocab, h),
+                                                                   shape.dtype, std),
+        "layers": layers,
+    }

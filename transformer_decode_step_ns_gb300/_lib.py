@@ -32,7 +32,8 @@ SYMBOLS = (
     "ns_attn_decode", "ns_linear", "ns_greedy_argmax", "ns_get_device_error",
     "ns_get_step_info", "ns_status_str", "ns_last_error_message", "ns_pool_create",
     "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
-    "ns_pool_free_count", "ns_check_step_metadata",
+    "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
+    "ns_get_kernel_timing",
 )
 
 
@@ -59,6 +60,13 @@ class LayerWeights(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
                 ("lm_head", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerWeights))]
+
+
+KERNEL_KINDS = ("embed_rope", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
+
+
+class KernelTiming(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int * 8), ("total_ms", ctypes.c_double * 8)]
 
 
 class StepInfo(ctypes.Structure):
@@ -106,6 +114,8 @@ def lib() -> ctypes.CDLL:
             "ns_pool_free_count": ([P, ctypes.POINTER(I)], I),
             "ns_check_step_metadata": ([I, I, I, I, I, I, P, P, P, P, P], I),
             "ns_last_error_message": ([], ctypes.c_char_p),
+            "ns_set_kernel_timing": ([P, I], I),
+            "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -284,6 +294,15 @@ class DecodeStep:
         c = I()
         check(lib().ns_get_device_error(self.h, ctypes.byref(c)))
         return c.value
+
+    def set_kernel_timing(self, on: bool) -> None:
+        check(lib().ns_set_kernel_timing(self.h, 1 if on else 0))
+
+    def kernel_timing(self) -> dict:
+        t = KernelTiming()
+        check(lib().ns_get_kernel_timing(self.h, ctypes.byref(t)))
+        return {KERNEL_KINDS[i]: (t.launches[i], t.total_ms[i]) for i in range(8)
+                if t.launches[i] > 0}
 
     def info(self) -> StepInfo:
         s = StepInfo()

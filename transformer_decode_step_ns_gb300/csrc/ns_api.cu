@@ -322,6 +322,14 @@ struct ns_ctx {
   int* err = nullptr;
   ns_step_info info{};
   int kernels_last = 0;
+  // per-kernel timing (eager only)
+  bool timing = false;
+  struct TimedLaunch {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<TimedLaunch> timed;
+  ns_kernel_timing timing_acc{};
 };
 
 namespace {
@@ -344,6 +352,27 @@ MetaLayout meta_layout(int B, int MB) {
   m.total = o;
   return m;
 }
+
+enum KernelKind { K_EMBED = 0, K_QKV = 1, K_ATTN = 2, K_O = 3, K_GU = 4, K_DOWN = 5, K_LM = 6 };
+
+// Event pair around one launch when per-kernel timing is on.
+struct TimeScope {
+  ns_ctx* h;
+  cudaStream_t s;
+  int kind;
+  cudaEvent_t a = nullptr, b = nullptr;
+  TimeScope(ns_ctx* h_, cudaStream_t s_, int kind_) : h(h_), s(s_), kind(kind_) {
+    if (!h->timing) return;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    cudaEventRecord(a, s);
+  }
+  ~TimeScope() {
+    if (!h->timing) return;
+    cudaEventRecord(b, s);
+    h->timed.push_back({kind, a, b});
+  }
+};
 
 ns_status get_bmap(ns_ctx* h, const void* buf, int cols, int BN, const CUtensorMap** out) {
   auto key = std::make_tuple(buf, BN);
@@ -379,7 +408,7 @@ ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
 }
 
 ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
-                      int epi, const EpiArgs& e, NanoSlot& slot, cudaStream_t s) {
+                      int epi, const EpiArgs& e, NanoSlot& slot, cudaStream_t s, int kind) {
   GemmParams p{};
   p.M = m;
   p.row0 = row0;
@@ -397,6 +426,7 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   p.e = e;
   const CUtensorMap* mb = nullptr;
   NS_TRY(get_bmap(h, x, x_cols, p.BN, &mb));
+  TimeScope ts(h, s, kind);
   NS_CUDA(launch_gemm(&pr.mapA, mb, p, h->dtype, s, true));
   h->kernels_last++;
   return NS_OK;
@@ -469,7 +499,10 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     ep.batch = nb[i].second;
     ep.row0 = nb[i].first;
     ep.err = h->err;
-    NS_CUDA(launch_embed(ep, h->dtype, st[i % 2], true));
+    {
+      TimeScope ts(h, st[i % 2], K_EMBED);
+      NS_CUDA(launch_embed(ep, h->dtype, st[i % 2], true));
+    }
     h->kernels_last++;
   }
   for (int l = 0; l < c.n_layers; ++l) {
@@ -489,7 +522,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.block_size = h->block_size;
       e.pool_slots = static_cast<long long>(h->num_blocks) * h->block_size;
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e, h->slots[i],
-                         st[i % 2]));
+                         st[i % 2], K_QKV));
       if (n > 1) NS_CUDA(cudaEventRecord(h->events[2 + static_cast<size_t>(l) * n + i], st[i % 2]));
     }
     for (int i = 0; i < n; ++i) {
@@ -518,7 +551,10 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.err = h->err;
       int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
       if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
-      NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+      {
+        TimeScope ts(h, s, K_ATTN);
+        NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+      }
       h->kernels_last++;
 
       EpiArgs eo{};
@@ -528,12 +564,12 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       eo.sumsq_out = h->sumsq;
       eo.sumsq_ld = h->R;
       eo.resid_dim = H;
-      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, h->slots[i], s));
+      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, h->slots[i], s, K_O));
 
       EpiArgs eg = norm;
       eg.act_out = h->act;
       eg.ffn = F;
-      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, h->slots[i], s));
+      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, h->slots[i], s, K_GU));
 
       EpiArgs ed{};
       ed.resid = h->resid;
@@ -542,7 +578,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ed.sumsq_out = h->sumsq;
       ed.sumsq_ld = h->R;
       ed.resid_dim = H;
-      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, h->slots[i], s));
+      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, h->slots[i], s, K_DOWN));
     }
   }
   for (int i = 0; i < n; ++i) {
@@ -550,7 +586,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     el.out_ptr_slot = m_logits;
     el.ldo = c.vocab;
     NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el, h->slots[i],
-                       st[i % 2]));
+                       st[i % 2], K_LM));
   }
   if (n > 1) {
     NS_CUDA(cudaEventRecord(h->events[1], h->side));
@@ -976,7 +1012,7 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   NS_CUDA(cudaMemcpyAsync(h->meta_dev, mh, ml.total, cudaMemcpyHostToDevice, s));
   NS_CUDA(cudaEventRecord(h->meta_done, s));
   h->meta_pending = true;
-  if (c.use_graphs) {
+  if (c.use_graphs && !h->timing) {
     cudaGraphExec_t ex = nullptr;
     NS_TRY(get_graph(h, batch, &ex));
     NS_CUDA(cudaGraphLaunch(ex, s));
@@ -985,6 +1021,31 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
     h->info.kernels_per_step = h->kernels_last;
   }
   h->info.steps++;
+  return NS_OK;
+}
+
+ns_status ns_set_kernel_timing(ns_handle h, int on) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  h->timing = on != 0;
+  return NS_OK;
+}
+
+ns_status ns_get_kernel_timing(ns_handle h, ns_kernel_timing* out) {
+  if (h == nullptr || out == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  NS_CUDA(cudaSetDevice(h->dev));
+  NS_CUDA(cudaDeviceSynchronize());
+  for (auto& t : h->timed) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess && t.kind >= 0 && t.kind < NS_KERNEL_KINDS) {
+      h->timing_acc.launches[t.kind]++;
+      h->timing_acc.total_ms[t.kind] += ms;
+    }
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  h->timed.clear();
+  *out = h->timing_acc;
+  h->timing_acc = ns_kernel_timing{};
   return NS_OK;
 }
 
