@@ -203,6 +203,26 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
                          int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                          ns_stream_t stream);
 
+/* ns_attn_decode without any device allocation, for callers that cannot allocate: code
+ * running inside an allocator or memory-pool callback, a plugin whose host process owns every
+ * device allocation, or a process that must keep its device footprint fixed after start-up.
+ * The source pages have no counterpart of this call; it exists for such callers only.
+ * Same arguments and result as ns_attn_decode, plus dev_err: an optional device int (NULL = none)
+ * where a failed bounds check inside the kernel is recorded.  The split-K scratch (partials and
+ * counters) lives in a fixed buffer inside the library image: 32 MiB of partials and 65,536
+ * counters, held by every GPU that loads the library until the process exits.  Requests needing
+ * more -- batch * n_kv_heads * ceil(max_blocks_per_seq * block_size / 256) *
+ * (n_q_heads / n_kv_heads) * (head_dim + 2) * 4 bytes, or batch * n_kv_heads counters -- return
+ * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the buffer and each call leaves
+ * its contents behind: calls whose kernels overlap on the GPU race; order them on one stream. */
+ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                                 int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq, int num_blocks,
+                                 float scale, int dtype, int* dev_err, ns_stream_t stream);
+
 /* Dense projection through the tcgen05 GEMM used by the step (NanoFlow page: the dense
  * class KQV/O/Up/Gate/Down): y[m][n] = sum_k x[m][k] * w[n][k], fp32 out.  w [n][k], x [m][k]
  * device, storage dtype; y device fp32 [m][n].  n % 128 == 0, k % 64 == 0, 1 <= m <= 4096.

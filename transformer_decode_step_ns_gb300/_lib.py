@@ -33,7 +33,7 @@ SYMBOLS = (
     "ns_get_step_info", "ns_status_str", "ns_last_error_message", "ns_pool_create",
     "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
     "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
-    "ns_get_kernel_timing",
+    "ns_get_kernel_timing", "ns_attn_decode_noalloc",
 )
 
 
@@ -102,6 +102,7 @@ def lib() -> ctypes.CDLL:
             "ns_decode_step": ([P, I, P, P, P, P, P, P, P], I),
             "ns_attn_decode": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P], I),
             "ns_linear": ([P, P, P, I, I, I, I, P], I),
+            "ns_attn_decode_noalloc": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P], I),
             "ns_greedy_argmax": ([P, I, I, P, P], I),
             "ns_get_device_error": ([P, ctypes.POINTER(I)], I),
             "ns_get_step_info": ([P, ctypes.POINTER(StepInfo)], I),
@@ -318,6 +319,19 @@ def attn_decode(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
                                _ptr(seq_lens), _ptr(out), batch, n_q_heads, n_kv_heads,
                                head_dim, block_size, max_blocks_per_seq, num_blocks,
                                float(scale), DTYPES[dtype], _stream(stream)))
+
+
+def attn_decode_noalloc(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
+                        n_kv_heads: int, head_dim: int, block_size: int,
+                        max_blocks_per_seq: int, num_blocks: int, scale: float, dtype: str,
+                        dev_err=None, stream=None) -> None:
+    """The allocation-free attention call (fixed in-library scratch; see include/ns.h)."""
+    batch = int(seq_lens.shape[0])
+    check(lib().ns_attn_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                       _ptr(seq_lens), _ptr(out), batch, n_q_heads, n_kv_heads,
+                                       head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                       float(scale), DTYPES[dtype], _ptr(dev_err),
+                                       _stream(stream)))
 
 
 def linear(w, x, y, m: int, n: int, k: int, dtype: str, stream=None) -> None:

@@ -185,6 +185,8 @@ ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
 
 }  // namespace
 
+void ns::set_last_error(const char* msg) { g_msg = msg ? msg : ""; }
+
 // ------------------------------------------------------------------------------ block pool
 
 struct ns_block_pool {

@@ -116,6 +116,9 @@ int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full w
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
                         cudaStream_t s, bool pdl);
 
+// Record the text ns_last_error_message() returns on this thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
                           cudaStream_t s);
