@@ -191,10 +191,12 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
  *   [head_dim]; block_tables [batch][max_blocks_per_seq] int32; seq_lens [batch] int32 in
  *   [1, max_blocks_per_seq*block_size]; out [batch][n_q_heads][head_dim] (same dtype as q).
  * For q head h the kv head is h / (n_q_heads / n_kv_heads); o = softmax(q.K^T * scale) V over
- * tokens t < seq_len.  Long contexts are split into fixed 256-token chunks merged by
- * log-sum-exp; the split depends only on seq_len, so results do not depend on the batch.
- * Scratch (partials and counters) is allocated by the library on first use per device and
- * kept until exit.  num_blocks bounds the block ids the kernel accepts.  Supports head_dim
+ * tokens t < seq_len.  The split depends only on seq_len, so results do not depend on the
+ * batch.  num_blocks * n_kv_heads * block_size must be below 2^31.
+ * Rows of length L split into chunks of 128 * ceil(L / 2048) tokens (at most 16), merged by
+ * log-sum-exp.  Scratch (partials and counters) is allocated by the library on first use per
+ * device and kept until exit.  Slots past seq_len in a row's last block are never used, even
+ * if they hold non-finite values.  num_blocks bounds the block ids the kernel accepts.  Supports head_dim
  * 64/128, G <= 8 (G in 1,2,4,7,8), block_size 16.  Not to be called during stream capture
  * the first time on a device (it may allocate). */
 ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
@@ -211,7 +213,7 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
  * where a failed bounds check inside the kernel is recorded.  The split-K scratch (partials and
  * counters) lives in a fixed buffer inside the library image: 32 MiB of partials and 65,536
  * counters, held by every GPU that loads the library until the process exits.  Requests needing
- * more -- batch * n_kv_heads * ceil(max_blocks_per_seq * block_size / 256) *
+ * more -- batch * n_kv_heads * min(16, ceil(max_blocks_per_seq * block_size / 128)) *
  * (n_q_heads / n_kv_heads) * (head_dim + 2) * 4 bytes, or batch * n_kv_heads counters -- return
  * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the
  * buffer's device address (cudaGetSymbolAddress) with that device current; make that first

@@ -1,21 +1,28 @@
-// Paged grouped-query decode attention with fixed-chunk split-K and an in-kernel merge.
+// Paged grouped-query decode attention: warp-independent units, TMA-staged K/V tiles,
+// tensor-core (mma.sync m16n8k16) QK^T and PV, split-K over fixed chunks with an in-kernel merge.
 //
-// "GPU waiting, not working" (nanoserve notes), change table: grouped-query attention must
-// not materialise the G-times expanded copy of K and V, and a fused paged-attention kernel
-// replaced about ten ops per layer.  "NanoFlow ..." ("Four resource classes"): decode
-// attention is the memory-bound class, so the kernel is built to stream K/V at HBM speed:
+// "GPU waiting, not working" (nanoserve notes), change table: grouped-query attention must not
+// materialise the G-times expanded copy of K and V, and one fused paged-attention kernel
+// replaces about ten ops per layer.  "NanoFlow ..." ("Four resource classes"): decode attention
+// is the memory-bound class, so the kernel is built to stream K/V at HBM speed:
 //
-// * Work unit = (request b, kv head g, chunk of 256 tokens).  The chunking depends only on
-//   seq_len, so a row's result never depends on the rest of the batch (nano-batch identity).
-// * Persistent CTAs walk units round-robin.  One producer thread streams each (block, kv head)
-//   K tile and V tile (block_size x d contiguous, 4 KiB at d=128 bf16) with cp.async.bulk into
-//   an mbarrier ring; the producer runs ahead across unit boundaries.
-// * Consumers: each K/V tile is read once from shared memory for all G query heads of its
-//   group (no expansion).  QK: TPT threads per token, q held in registers, shuffle reduction;
-//   online softmax in the log2 domain; PV: threads own dim pairs, token slices merged at the
-//   end of the unit.
-// * Chunks of one (b, g) are merged by the last-arriving CTA (atomic counter, no spin) in
-//   chunk order with the log-sum-exp rule, so the result is deterministic.
+// * Work unit = (request b, kv head g, chunk).  A row of length L splits into chunks of
+//   128 * ceil(L / 2048) tokens (at most 16 chunks); the chunking is a function of L alone, so a
+//   row's result never depends on the rest of the batch.
+// * Every warp walks its own units (round-robin over all warps of the grid) with a private ring
+//   of TMA tensor copies: one 16 x d K tile and one V tile per cache block, 128-byte swizzled so
+//   the ldmatrix reads below are bank-conflict free.  The warp refills a stage as soon as it has
+//   consumed it and runs ahead across unit boundaries.  A unit's block ids are copied to shared
+//   memory (cp.async) one unit ahead, and its q one unit ahead into registers, so the stream
+//   never waits on a block-table or q read.
+// * The G <= 8 query heads of the group form the rows of one 16-row mma.sync tile:
+//     S^T[head][token]  = q[head][:] . K[token][:]          (A = q in registers, B = K tile)
+//     O^T[dim][head]   += V^T[dim][token] . P^T[token][head] (A = V tile via ldmatrix.trans)
+//   The accumulator layout of the first product is exactly the B-operand layout of the second,
+//   so P never leaves registers.  Each K/V element is read once from shared memory for all G
+//   heads: no expansion.  Online softmax in the log2 domain, per head, in registers.
+// * Chunks of one (b, g) are merged by the last-arriving warp (atomic counter, no spin) in chunk
+//   order with the log-sum-exp rule: deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -27,25 +34,70 @@ namespace ns {
 namespace {
 
 template <typename T>
-struct AV;  // vector helpers for the storage type
+struct MV;
 template <>
-struct AV<__half> {
-  static __device__ __forceinline__ float2 to2(uint32_t u) {
-    return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu))),
-                       __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))));
+struct MV<__half> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
   static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
-  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 };
 template <>
-struct AV<__nv_bfloat16> {
-  static __device__ __forceinline__ float2 to2(uint32_t u) {
-    // bf16 is the upper half of an fp32: widening is a shift
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+struct MV<__nv_bfloat16> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
   static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
-  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 };
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_err(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
@@ -55,80 +107,63 @@ __device__ __forceinline__ void set_err(int* err, int code) {
 
 template <int D, int G>
 struct AttnShape {
-  static constexpr int BS = 16;
-  static constexpr int TPT = (G * D / 64 > 8) ? 16 : 8;  // QK threads per token (q regs <= 64)
-  static constexpr int DPT = D / TPT;                               // dims per QK thread
-  static constexpr int NC = BS * TPT;                               // consumer threads
-  static constexpr int NWC = NC / 32;
-  static constexpr int NT = NC + 32;                                // + producer warp
-  static constexpr int DP = D / 2;                                  // PV dim pairs
-  static constexpr int TS = NC / DP;                                // PV token slices
-  static constexpr int TPS = BS / TS;                               // tokens per slice
-  static constexpr int TILE = BS * D * 2;                           // bytes per K or V tile
-  static constexpr int NSTAGE = (D == 128) ? 8 : 16;
-  static constexpr int CHUNK_BLOCKS = kAttnChunkTokens / BS;
-  static_assert(NC % 32 == 0 && TS * DP == NC && BS % TS == 0, "thread mapping");
-  static_assert(DPT % 8 == 0, "16-byte K loads");
-  // shared memory layout (bytes, from a 128-byte aligned base)
-  static constexpr int OFF_RING = 0;
-  static constexpr int OFF_BAR = OFF_RING + NSTAGE * 2 * TILE;
-  static constexpr int OFF_S = OFF_BAR + 2 * NSTAGE * 8;
-  static constexpr int OFF_P = OFF_S + G * BS * 4;
-  static constexpr int OFF_ML = OFF_P + BS * 8 * 4;          // m[8], l[8], alpha[8]
-  static constexpr int OFF_FLAG = OFF_ML + 3 * 8 * 4;         // abort, last, total
-  static constexpr int OFF_RED = OFF_FLAG + 16;
-  static constexpr int OFF_PRE = OFF_RED + TS * G * D * 4;    // prefix over rows [batch + 1]
-  static size_t smem_bytes(int batch) {
-    return 128 + OFF_PRE + static_cast<size_t>(batch + 1) * 4;
+  static constexpr int NW = 4;                 // independent warps per CTA
+  static constexpr int NT = NW * 32;
+  static constexpr int BS = 16;                // tokens per cache block
+  static constexpr int NH = D / 64;            // 128-byte column halves of a tile
+  static constexpr int TILE = BS * D * 2;      // bytes of one K or V tile
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int NST = (D == 128) ? 3 : 6;
+  static constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
+  static constexpr int RING = NST * STAGE;     // bytes per warp
+  static constexpr int OFF_BAR = NW * RING;
+  static constexpr int OFF_FLAG = OFF_BAR + NW * NST * 8;
+  static constexpr int OFF_IDS = OFF_FLAG + 16;  // per warp, 2 slots x ids_cap block ids
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(G >= 1 && G <= 8, "group");
+  // then chunk prefix [batch + 1], lengths [batch], scan scratch [NT]
+  static size_t smem_bytes(int batch, int ids_cap) {
+    return 1024 + OFF_IDS + static_cast<size_t>(NW) * 2 * ids_cap * 4 +
+           static_cast<size_t>(2 * batch + 1 + NT) * 4;
   }
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(AttnShape<D, G>::NT)
-    attn_decode_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   using S = AttnShape<D, G>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
-  uint64_t* empty = full + S::NSTAGE;
-  float* s_sc = reinterpret_cast<float*>(smem + S::OFF_S);    // [G][BS] scores (log2 domain)
-  float* s_p = reinterpret_cast<float*>(smem + S::OFF_P);     // [BS][8] probabilities
-  float* s_m = reinterpret_cast<float*>(smem + S::OFF_ML);
-  float* s_l = s_m + 8;
-  float* s_a = s_m + 16;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int* abort_flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
-  int* last_flag = abort_flag + 1;
-  int* s_stop = abort_flag + 2;
-  float* red = reinterpret_cast<float*>(smem + S::OFF_RED);   // [TS][G][D]
-  int* pre = reinterpret_cast<int*>(smem + S::OFF_PRE);        // chunk prefix over rows
+  int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);  // [NW][2][ids_cap]
+  int* pre = ids_all + S::NW * 2 * p.ids_cap;                 // chunk prefix over rows [batch + 1]
+  int* lens = pre + p.batch + 1;                              // validated seq_lens [batch]
+  int* tot = lens + p.batch;                                  // per-thread scan scratch [NT]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = p.n_kv_heads, batch = p.batch;
+  uint8_t* ring = smem + warp * S::RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR) + warp * S::NST;
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int Hkv = p.n_kv_heads;
-  const int batch = p.batch;
-
-  if (tid == 0) {
-    for (int s = 0; s < S::NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], S::NWC);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
+  if (lane == 0) {
+    for (int s = 0; s < S::NST; ++s) mbar_init(&full[s], 1);
   }
-  // Chunk prefix over the rows (metadata is final before the step starts, so this overlaps the
-  // previous kernel under programmatic dependent launch).
+  if (tid == 0) *abort_flag = 0;
+  // Chunk prefix over the rows.  seq_lens are step metadata, final before the step starts, so
+  // under programmatic dependent launch this overlaps the previous kernel.
   {
     const int per = (batch + S::NT - 1) / S::NT;
     const int lo = tid * per, hi = min(batch, lo + per);
     int run = 0;
     for (int b = lo; b < hi; ++b) {
       const int L = p.seq_lens[p.row0 + b];
-      const int ok = (L >= 1 && L <= p.mb * p.block_size);
-      run += ok ? (L + kAttnChunkTokens - 1) / kAttnChunkTokens : 0;
+      const bool ok = L >= 1 && L <= p.mb * p.block_size;
+      if (!ok) set_err(p.err, NS_DEV_BAD_LENGTH);
+      lens[b] = ok ? L : 0;
+      run += ok ? attn_num_chunks(L) : 0;
     }
-    // exclusive scan of per-thread totals through shared memory (reuses the red buffer)
-    int* tot = reinterpret_cast<int*>(red);
     tot[tid] = run;
+    fence_mbar_init();
     __syncthreads();
     if (tid == 0) {
       int acc = 0;
@@ -143,10 +178,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT)
     int acc = tot[tid];
     for (int b = lo; b < hi; ++b) {
       pre[b] = acc;
-      const int L = p.seq_lens[p.row0 + b];
-      const int ok = (L >= 1 && L <= p.mb * p.block_size);
-      if (!ok) set_err(p.err, NS_DEV_BAD_LENGTH);
-      acc += ok ? (L + kAttnChunkTokens - 1) / kAttnChunkTokens : 0;
+      acc += attn_num_chunks(lens[b]);
     }
     __syncthreads();
   }
@@ -154,274 +186,294 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT)
   if (tid == 0) griddep_launch_dependents();
   griddep_wait();  // q and this step's K/V come from the previous kernel
 
-  auto decode_unit = [&](int u, int& b, int& g, int& chunk, int& L) {
+  struct Unit {
+    int b, g, chunk, L, t0, t1, nblk, nchunks;
+  };
+  auto decode = [&](int u) {
+    Unit x;
     const int cg = u / Hkv;
-    g = u - cg * Hkv;
+    x.g = u - cg * Hkv;
     int lo = 0, hi = batch - 1;  // largest b with pre[b] <= cg
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (pre[mid] <= cg) lo = mid; else hi = mid - 1;
     }
-    b = lo;
-    chunk = cg - pre[b];
-    L = p.seq_lens[p.row0 + b];
+    x.b = lo;
+    x.chunk = cg - pre[lo];
+    x.L = lens[lo];
+    const int ct = attn_chunk_tokens(x.L);
+    x.t0 = x.chunk * ct;
+    x.t1 = min(x.L, x.t0 + ct);
+    x.nblk = (x.t1 - x.t0 + S::BS - 1) / S::BS;
+    x.nchunks = attn_num_chunks(x.L);
+    return x;
   };
 
-  const T* kpool = reinterpret_cast<const T*>(p.k_pool);
-  const T* vpool = reinterpret_cast<const T*>(p.v_pool);
+  const int gw = blockIdx.x * S::NW + warp, TW = gridDim.x * S::NW;
 
-  if (warp == S::NWC) {
-    // ---------------------------------------------------------------- producer
+  // ---- producer cursor (warp-uniform): the warp's stream of (unit, block) in consumption order
+  int* ids = ids_all + warp * 2 * p.ids_cap;
+  auto prefetch_ids = [&](int unit, int slot) {
+    if (unit < total) {
+      const Unit x = decode(unit);
+      const int* src = p.block_tables + static_cast<size_t>(p.row0 + x.b) * p.mb + x.t0 / S::BS;
+      for (int j = lane; j < x.nblk; j += 32) cp_async_4(ids + slot * p.ids_cap + j, src + j);
+    }
+    cp_async_commit();
+  };
+  int pu = gw, pi = 0, ps = 0, issued = 0;
+  Unit pun{};
+  auto enter = [&]() {  // the producer starts unit pu (slot ps): its ids were prefetched
+    cp_async_wait_all();
+    __syncwarp();
+    if (pu < total) pun = decode(pu);
+    prefetch_ids(pu + TW, ps ^ 1);
+  };
+  prefetch_ids(pu, 0);
+  enter();
+  auto issue = [&](int stage) {  // warp-collective; lane 0 issues the copies
+    if (pu >= total) return;
+    int blk = ids[ps * p.ids_cap + pi];
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (lane == 0) set_err(p.err, NS_DEV_BAD_BLOCK);
+      blk = 0;  // keep the pipeline consistent; the error word flags the result
+    }
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int it = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < total && !stop; u += gridDim.x) {
-        int b, g, chunk, L;
-        decode_unit(u, b, g, chunk, L);
-        const int blk0 = chunk * S::CHUNK_BLOCKS;
-        const int t_end = min(L, (chunk + 1) * kAttnChunkTokens);
-        const int nblk = (t_end - chunk * kAttnChunkTokens + S::BS - 1) / S::BS;
-        const int* row_tab = p.block_tables + static_cast<size_t>(p.row0 + b) * p.mb;
-        for (int i = 0; i < nblk; ++i, ++it) {
-          const int s = it % S::NSTAGE;
-          if (it >= S::NSTAGE) {
-            if (!mbar_wait(&empty[s], static_cast<uint32_t>((it / S::NSTAGE) - 1) & 1u, abort_flag)) {
-              *abort_flag = 1;
-              set_err(p.err, NS_DEV_WAIT_TIMEOUT);
-              stop = true;
-              break;
-            }
-          }
-          int blk = row_tab[blk0 + i];
-          if (blk < 0 || blk >= p.num_blocks) {
-            set_err(p.err, NS_DEV_BAD_BLOCK);
-            blk = 0;  // keep the pipeline consistent; the row's output is flagged invalid
-          }
-          const size_t off = (static_cast<size_t>(blk) * Hkv + g) * S::BS * D;
-          uint8_t* dst = smem + S::OFF_RING + static_cast<size_t>(s) * 2 * S::TILE;
-          mbar_arrive_expect_tx(&full[s], 2 * S::TILE);
-          bulk_g2s_hint(dst, kpool + off, S::TILE, &full[s], pol);
-          bulk_g2s_hint(dst + S::TILE, vpool + off, S::TILE, &full[s], pol);
-        }
-      }
-      // drain: let copies in flight land before exit
-      __threadfence_block();
-      const int first = max(0, it - S::NSTAGE);
-      for (int i = first; i < it; ++i) {
-        (void)mbar_wait(&full[i % S::NSTAGE], static_cast<uint32_t>(i / S::NSTAGE) & 1u,
-                        nullptr);
+      uint8_t* dst = ring + stage * S::STAGE;
+      const int y = (blk * Hkv + pun.g) * S::BS;
+      mbar_arrive_expect_tx(&full[stage], S::STAGE);
+#pragma unroll
+      for (int h = 0; h < S::NH; ++h) {
+        tma_load_2d(dst + h * 2048, &kmap, &full[stage], h * 64, y);
+        tma_load_2d(dst + S::TILE + h * 2048, &vmap, &full[stage], h * 64, y);
       }
     }
-    return;
-  }
-
-  // ------------------------------------------------------------------ consumers
-  const int ct = tid;                 // 0..NC-1
-  const int qt = ct / S::TPT;         // QK token
-  const int qp = ct % S::TPT;         // QK part
-  const int ts = ct / S::DP;          // PV token slice
-  const int dp = ct % S::DP;          // PV dim pair
-  int it = 0;
-  for (int u = blockIdx.x; u < total; u += gridDim.x) {
-    int b, g, chunk, L;
-    decode_unit(u, b, g, chunk, L);
-    const int t_begin = chunk * kAttnChunkTokens;
-    const int t_end = min(L, t_begin + kAttnChunkTokens);
-    const int nblk = (t_end - t_begin + S::BS - 1) / S::BS;
-    const int nchunks = (L + kAttnChunkTokens - 1) / kAttnChunkTokens;
-    const size_t row = static_cast<size_t>(p.row0 + b);
-
-    float qr[G][S::DPT];
-    {
-      const T* qsrc = reinterpret_cast<const T*>(p.q) + row * p.q_row_stride +
-                      static_cast<size_t>(g) * G * D + qp * S::DPT;
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-        for (int v = 0; v < S::DPT / 8; ++v) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(qsrc + gg * D + v * 8);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = AV<T>::to2(w[k]);
-            qr[gg][v * 8 + 2 * k] = f.x * p.scale_log2;
-            qr[gg][v * 8 + 2 * k + 1] = f.y * p.scale_log2;
-          }
-        }
-      }
+    ++issued;
+    if (++pi >= pun.nblk) {
+      pi = 0;
+      pu += TW;
+      ps ^= 1;
+      enter();
     }
-    if (ct < G) {
-      s_m[ct] = -INFINITY;
-      s_l[ct] = 0.f;
-    }
-    float acc[G][2];
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0.f;
+  };
+  for (int s = 0; s < S::NST; ++s) issue(s);
 
-    bool failed = false;
-    for (int i = 0; i < nblk; ++i, ++it) {
-      const int s = it % S::NSTAGE;
-      const bool got = mbar_wait(&full[s], static_cast<uint32_t>(it / S::NSTAGE) & 1u, abort_flag);
-      if (!got) {
+  const int gq = lane >> 2, tq = lane & 3;
+  // ldmatrix lane address: token row and 16-byte chunk offset within the 4 matrices
+  const int lm_tok = (lane & 7) + ((lane >> 4) << 3);
+  const int lm_chunk = (lane >> 3) & 1;
+  T* out = reinterpret_cast<T*>(p.out);
+
+  // q of the group as the A operand (rows = heads, G of 16 used; k = dims), loaded one unit
+  // ahead so the loads overlap the previous unit's blocks.
+  uint32_t qn[S::KS][2];
+  auto load_q = [&](int unit) {
+    if (unit >= total || gq >= G) {
+#pragma unroll
+      for (int ks = 0; ks < S::KS; ++ks) qn[ks][0] = qn[ks][1] = 0u;
+      return;
+    }
+    const Unit x = decode(unit);
+    const T* qrow = reinterpret_cast<const T*>(p.q) + static_cast<size_t>(p.row0 + x.b) * p.q_row_stride +
+                    static_cast<size_t>(x.g * G + gq) * D;
+#pragma unroll
+    for (int ks = 0; ks < S::KS; ++ks) {
+      qn[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq);
+      qn[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq);
+    }
+  };
+  load_q(gw);
+
+  int ci = 0;
+  bool failed = false;
+  for (int u = gw; u < total && !failed; u += TW) {
+    const Unit x = decode(u);
+    const size_t row = static_cast<size_t>(p.row0 + x.b);
+    uint32_t qa[S::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < S::KS; ++ks) {
+      qa[ks][0] = qn[ks][0];
+      qa[ks][1] = qn[ks][1];
+    }
+    load_q(u + TW);
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[S::KS][4];
+#pragma unroll
+    for (int mt = 0; mt < S::KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+    for (int i = 0; i < x.nblk; ++i, ++ci) {
+      const int s = ci % S::NST;
+      if (!mbar_wait(&full[s], static_cast<uint32_t>(ci / S::NST) & 1u, abort_flag)) {
         *abort_flag = 1;
         set_err(p.err, NS_DEV_WAIT_TIMEOUT);
-      }
-      const uint8_t* kt = smem + S::OFF_RING + static_cast<size_t>(s) * 2 * S::TILE;
-      const uint8_t* vt = kt + S::TILE;
-      const int tok_base = t_begin + i * S::BS;
-      // ---- QK: scores for token qt of this block, all G heads
-      {
-        float kf[S::DPT];
-        const T* krow = reinterpret_cast<const T*>(kt) + qt * D + qp * S::DPT;
-#pragma unroll
-        for (int v = 0; v < S::DPT / 8; ++v) {
-          uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-          if (got) raw = *reinterpret_cast<const uint4*>(krow + v * 8);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = AV<T>::to2(w[k]);
-            kf[v * 8 + 2 * k] = f.x;
-            kf[v * 8 + 2 * k + 1] = f.y;
-          }
-        }
-        const bool valid = tok_base + qt < t_end;
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          float sdot = 0.f;
-#pragma unroll
-          for (int k = 0; k < S::DPT; ++k) sdot = fmaf(qr[gg][k], kf[k], sdot);
-#pragma unroll
-          for (int o = S::TPT / 2; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
-          if (qp == 0) s_sc[gg * S::BS + qt] = valid ? sdot : -INFINITY;
-        }
-      }
-      named_barrier_sync(1, S::NC);
-      // ---- online softmax: thread (gg, t) for ct < 16 G; every consumer lane takes part in
-      // the shuffles (16-lane groups), only active lanes write.
-      {
-        const bool act = ct < S::BS * G;
-        const int gg = act ? ct / S::BS : 0, t = ct % S::BS;
-        const float sc = act ? s_sc[gg * S::BS + t] : 0.f;
-        float mx = sc;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float m_old = s_m[gg];
-        const float m_new = fmaxf(m_old, mx);
-        const float pr = exp2f(sc - m_new);
-        float sum = pr;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (ct == 0) s_stop[0] = *abort_flag;
-        if (act) {
-          s_p[t * 8 + gg] = pr;
-          if (t == 0) {
-            const float a = exp2f(m_old - m_new);
-            s_a[gg] = a;
-            s_l[gg] = s_l[gg] * a + sum;
-            s_m[gg] = m_new;
-          }
-        }
-      }
-      named_barrier_sync(1, S::NC);
-      if (s_stop[0]) {
         failed = true;
-        break;
       }
-      // ---- PV: dim pair dp, tokens of slice ts
-      {
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          const float a = s_a[gg];
-          acc[gg][0] *= a;
-          acc[gg][1] *= a;
+      failed = __any_sync(0xffffffffu, failed);
+      if (failed) break;
+      const uint8_t* kt = ring + s * S::STAGE;
+      const uint8_t* vt = kt + S::TILE;
+      const int n_valid = min(S::BS, x.t1 - (x.t0 + i * S::BS));
+      const bool zeroed = n_valid < S::BS;
+      if (zeroed) {
+        // stale slots past seq_len: zero their V rows so 0 * (anything) stays 0
+        uint4* v4 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(vt));
+        for (int c = lane; c < S::BS * S::NH * 8; c += 32) {
+          const int h = c / (S::BS * 8), r = (c / 8) % S::BS;
+          if (r >= n_valid) v4[h * 128 + r * 8 + (c & 7)] = make_uint4(0u, 0u, 0u, 0u);
         }
-        const uint32_t* vw = reinterpret_cast<const uint32_t*>(vt);
-#pragma unroll
-        for (int tt = 0; tt < S::TPS; ++tt) {
-          const int t = ts * S::TPS + tt;
-          if (tok_base + t < t_end) {
-            const float2 v = AV<T>::to2(vw[t * S::DP + dp]);
-            const float* pp = s_p + t * 8;
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-              const float pr = pp[gg];
-              acc[gg][0] = fmaf(pr, v.x, acc[gg][0]);
-              acc[gg][1] = fmaf(pr, v.y, acc[gg][1]);
-            }
-          }
-        }
+        __syncwarp();
       }
+      const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+      // ---- S^T = q K^T: two n-tiles of 8 tokens; even / odd k-steps accumulate separately,
+      // which halves the dependent MMA chain
+      float sacc[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < S::KS; ++ks) {
+        const int chunk16 = 2 * ks + lm_chunk;           // 16-byte chunk = 8 dims
+        const int h = chunk16 >> 3, cc = chunk16 & 7;
+        const uint32_t addr = kbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
+        uint32_t kb[4];
+        ldsm_x4(addr, kb);
+        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+        MV<T>::mma(sacc[(ks & 1) * 2 + 0], a, kb[0], kb[1]);
+        MV<T>::mma(sacc[(ks & 1) * 2 + 1], a, kb[2], kb[3]);
+      }
+      // ---- online softmax for head gq over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
+      float sc[4] = {sacc[0][0] + sacc[2][0], sacc[0][1] + sacc[2][1], sacc[1][0] + sacc[3][0],
+                     sacc[1][1] + sacc[3][1]};
+      const int tk[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sc[k] = tk[k] < n_valid ? sc[k] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sc[k]);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = exp2f(m_run - m_new);
+      float pr[4], psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pr[k] = exp2f(sc[k] - m_new);
+        psum += pr[k];
+      }
+      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      // ---- O^T += V^T P^T  (P^T in the B-operand layout straight from the S^T accumulator)
+      const uint32_t pb0 = MV<T>::pack(pr[0], pr[1]);
+      const uint32_t pb1 = MV<T>::pack(pr[2], pr[3]);
+      const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * tq);      // head 2tq
+      const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);  // head 2tq + 1
+#pragma unroll
+      for (int mt = 0; mt < S::KS; ++mt) {
+        acc[mt][0] *= a_e;
+        acc[mt][1] *= a_o;
+        acc[mt][2] *= a_e;
+        acc[mt][3] *= a_o;
+        const int chunk16 = 2 * mt + lm_chunk;
+        const int h = chunk16 >> 3, cc = chunk16 & 7;
+        const uint32_t addr = vbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
+        uint32_t va[4];
+        ldsm_x4_t(addr, va);
+        MV<T>::mma(acc[mt], va, pb0, pb1);
+      }
+      // ---- the stage is consumed: refill it with the next block of this warp's stream
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // generic-proxy zero writes must be ordered before the TMA overwrite of this stage
+      if (zeroed && lane == 0) fence_proxy_async_smem();
+      issue(s);
     }
     if (failed) break;
 
-    // ---- merge token slices; write the output or this chunk's partial
+    // ---- unit result: heads 2tq and 2tq + 1 of this lane's accumulator columns
+    const float l_e = __shfl_sync(0xffffffffu, l_run, 8 * tq);
+    const float l_o = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4);
+    const int h_e = 2 * tq, h_o = 2 * tq + 1;
+    if (x.nchunks == 1) {
+      T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      red[(ts * G + gg) * D + 2 * dp] = acc[gg][0];
-      red[(ts * G + gg) * D + 2 * dp + 1] = acc[gg][1];
-    }
-    named_barrier_sync(1, S::NC);
-    T* out = reinterpret_cast<T*>(p.out);
-    if (nchunks == 1) {
-      for (int idx = ct; idx < G * D; idx += S::NC) {
-        const int gg = idx / D, dd = idx - gg * D;
-        float o = 0.f;
-#pragma unroll
-        for (int k = 0; k < S::TS; ++k) o += red[(k * G + gg) * D + dd];
-        out[row * p.out_row_stride + static_cast<size_t>(g * G + gg) * D + dd] =
-            AV<T>::from_f(o / s_l[gg]);
+      for (int mt = 0; mt < S::KS; ++mt) {
+        const int d0 = mt * 16 + gq;
+        if (h_e < G) {
+          orow[h_e * D + d0] = MV<T>::from_f(acc[mt][0] / l_e);
+          orow[h_e * D + d0 + 8] = MV<T>::from_f(acc[mt][2] / l_e);
+        }
+        if (h_o < G) {
+          orow[h_o * D + d0] = MV<T>::from_f(acc[mt][1] / l_o);
+          orow[h_o * D + d0 + 8] = MV<T>::from_f(acc[mt][3] / l_o);
+        }
       }
     } else {
-      float* part = p.partials +
-                    ((row * Hkv + g) * static_cast<size_t>(p.max_chunks) + chunk) * G * (D + 2);
-      for (int idx = ct; idx < G * D; idx += S::NC) {
-        const int gg = idx / D, dd = idx - gg * D;
-        float o = 0.f;
+      const size_t slot0 = (row * Hkv + x.g) * static_cast<size_t>(p.max_chunks);
+      float* part = p.partials + (slot0 + x.chunk) * G * (D + 2);
 #pragma unroll
-        for (int k = 0; k < S::TS; ++k) o += red[(k * G + gg) * D + dd];
-        part[gg * (D + 2) + dd] = o;
+      for (int mt = 0; mt < S::KS; ++mt) {
+        const int d0 = mt * 16 + gq;
+        if (h_e < G) {
+          part[h_e * (D + 2) + d0] = acc[mt][0];
+          part[h_e * (D + 2) + d0 + 8] = acc[mt][2];
+        }
+        if (h_o < G) {
+          part[h_o * (D + 2) + d0] = acc[mt][1];
+          part[h_o * (D + 2) + d0 + 8] = acc[mt][3];
+        }
       }
-      if (ct < G) {
-        part[ct * (D + 2) + D] = s_m[ct];
-        part[ct * (D + 2) + D + 1] = s_l[ct];
+      if (tq == 0 && gq < G) {
+        part[gq * (D + 2) + D] = m_run;
+        part[gq * (D + 2) + D + 1] = l_run;
       }
       __threadfence();
-      named_barrier_sync(1, S::NC);
-      if (ct == 0) {
-        int* cnt = p.counters + row * Hkv + g;
-        const int old = atomicAdd(cnt, 1);
-        const int last = (old == nchunks - 1) ? 1 : 0;
-        if (last) *cnt = 0;
-        *last_flag = last;
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        int* cnt = p.counters + row * Hkv + x.g;
+        last = (atomicAdd(cnt, 1) == x.nchunks - 1) ? 1 : 0;
+        if (last) *cnt = 0;  // ready for the next launch
       }
-      named_barrier_sync(1, S::NC);
-      if (*last_flag) {
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
         __threadfence();
-        const float* p0 = p.partials + (row * Hkv + g) * static_cast<size_t>(p.max_chunks) * G * (D + 2);
-        for (int idx = ct; idx < G * D; idx += S::NC) {
-          const int gg = idx / D, dd = idx - gg * D;
-          float mmax = -INFINITY;
-          for (int c = 0; c < nchunks; ++c) {
-            const float* pc = p0 + static_cast<size_t>(c) * G * (D + 2) + gg * (D + 2);
-            mmax = fmaxf(mmax, __ldcg(pc + D));
+        const float* p0 = p.partials + slot0 * G * (D + 2);
+        T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
+        for (int hh = 0; hh < G; ++hh) {
+          // lane c < nchunks holds chunk c's (m, l); weights 2^(m_c - M), summed in chunk order
+          float mc = -INFINITY, lc = 0.f;
+          if (lane < x.nchunks) {
+            mc = __ldcg(p0 + (static_cast<size_t>(lane) * G + hh) * (D + 2) + D);
+            lc = __ldcg(p0 + (static_cast<size_t>(lane) * G + hh) * (D + 2) + D + 1);
           }
-          float lsum = 0.f, o = 0.f;
-          for (int c = 0; c < nchunks; ++c) {
-            const float* pc = p0 + static_cast<size_t>(c) * G * (D + 2) + gg * (D + 2);
-            const float w = exp2f(__ldcg(pc + D) - mmax);
-            lsum = fmaf(__ldcg(pc + D + 1), w, lsum);
-            o = fmaf(__ldcg(pc + dd), w, o);
+          float M = mc;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          const float w = lane < x.nchunks ? exp2f(mc - M) : 0.f;
+          float Lsum = 0.f;
+          for (int c = 0; c < x.nchunks; ++c)
+            Lsum = fmaf(__shfl_sync(0xffffffffu, lc, c), __shfl_sync(0xffffffffu, w, c), Lsum);
+          for (int dd = lane; dd < D; dd += 32) {
+            float o = 0.f;
+            for (int c = 0; c < x.nchunks; ++c) {
+              const float wc = __shfl_sync(0xffffffffu, w, c);
+              o = fmaf(__ldcg(p0 + (static_cast<size_t>(c) * G + hh) * (D + 2) + dd), wc, o);
+            }
+            orow[hh * D + dd] = MV<T>::from_f(o / Lsum);
           }
-          out[row * p.out_row_stride + static_cast<size_t>(g * G + gg) * D + dd] =
-              AV<T>::from_f(o / lsum);
         }
       }
     }
-    named_barrier_sync(1, S::NC);  // red / s_m / s_l are reused by the next unit
+  }
+  // On the normal path every issued copy was consumed.  After a timed-out wait, copies this
+  // warp issued but did not consume must land before the CTA releases its shared memory.
+  __syncwarp();
+  cp_async_wait_all();
+  if (failed && lane == 0) {
+    for (int c = ci; c < issued; ++c) {
+      (void)mbar_wait(&full[c % S::NST], static_cast<uint32_t>(c / S::NST) & 1u, nullptr);
+    }
   }
 }
 
@@ -430,7 +482,8 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT)
 namespace {
 
 template <typename T, int D, int G>
-cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_attn_t(const AttnParams& p, const CUtensorMap* km, const CUtensorMap* vm,
+                          int grid, cudaStream_t s, bool pdl) {
   using S = AttnShape<D, G>;
   static int configured_mask = 0;
   int dev = 0;
@@ -444,30 +497,31 @@ cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pd
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(S::NT, 1, 1);
-  cfg.dynamicSmemBytes = S::smem_bytes(p.batch);
+  cfg.dynamicSmemBytes = S::smem_bytes(p.batch, p.ids_cap);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G>, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G>, *km, *vm, p);
 }
 
 template <typename T, int D>
-cudaError_t dispatch_g(const AttnParams& p, int group, int grid, cudaStream_t s, bool pdl) {
+cudaError_t dispatch_g(const AttnParams& p, const CUtensorMap* km, const CUtensorMap* vm,
+                       int group, int grid, cudaStream_t s, bool pdl) {
   switch (group) {
-    case 1: return launch_attn_t<T, D, 1>(p, grid, s, pdl);
-    case 2: return launch_attn_t<T, D, 2>(p, grid, s, pdl);
-    case 4: return launch_attn_t<T, D, 4>(p, grid, s, pdl);
-    case 7: return launch_attn_t<T, D, 7>(p, grid, s, pdl);
-    case 8: return launch_attn_t<T, D, 8>(p, grid, s, pdl);
+    case 1: return launch_attn_t<T, D, 1>(p, km, vm, grid, s, pdl);
+    case 2: return launch_attn_t<T, D, 2>(p, km, vm, grid, s, pdl);
+    case 4: return launch_attn_t<T, D, 4>(p, km, vm, grid, s, pdl);
+    case 7: return launch_attn_t<T, D, 7>(p, km, vm, grid, s, pdl);
+    case 8: return launch_attn_t<T, D, 8>(p, km, vm, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, int D, int G>
-int max_grid_t(int batch) {
+int max_grid_t(int batch, int ids_cap) {
   using S = AttnShape<D, G>;
   int dev = 0, sms = 1, per_sm = 0;
   cudaGetDevice(&dev);
@@ -475,20 +529,20 @@ int max_grid_t(int batch) {
   cudaFuncSetAttribute(attn_decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        227 * 1024);
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<T, D, G>, S::NT,
-                                                    S::smem_bytes(batch)) != cudaSuccess ||
+                                                    S::smem_bytes(batch, ids_cap)) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   return sms * per_sm;
 }
 
 template <typename T, int D>
-int max_grid_g(int group, int batch) {
+int max_grid_g(int group, int batch, int ids_cap) {
   switch (group) {
-    case 1: return max_grid_t<T, D, 1>(batch);
-    case 2: return max_grid_t<T, D, 2>(batch);
-    case 4: return max_grid_t<T, D, 4>(batch);
-    case 7: return max_grid_t<T, D, 7>(batch);
-    default: return max_grid_t<T, D, 8>(batch);
+    case 1: return max_grid_t<T, D, 1>(batch, ids_cap);
+    case 2: return max_grid_t<T, D, 2>(batch, ids_cap);
+    case 4: return max_grid_t<T, D, 4>(batch, ids_cap);
+    case 7: return max_grid_t<T, D, 7>(batch, ids_cap);
+    default: return max_grid_t<T, D, 8>(batch, ids_cap);
   }
 }
 
@@ -500,22 +554,23 @@ bool attn_supported(int head_dim, int group, int block_size) {
   return group == 1 || group == 2 || group == 4 || group == 7 || group == 8;
 }
 
-int attn_max_grid(int dtype, int head_dim, int group, int batch) {
+int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap) {
   if (dtype == NS_BF16)
-    return head_dim == 64 ? max_grid_g<__nv_bfloat16, 64>(group, batch)
-                          : max_grid_g<__nv_bfloat16, 128>(group, batch);
-  return head_dim == 64 ? max_grid_g<__half, 64>(group, batch) : max_grid_g<__half, 128>(group, batch);
+    return head_dim == 64 ? max_grid_g<__nv_bfloat16, 64>(group, batch, ids_cap)
+                          : max_grid_g<__nv_bfloat16, 128>(group, batch, ids_cap);
+  return head_dim == 64 ? max_grid_g<__half, 64>(group, batch, ids_cap)
+                        : max_grid_g<__half, 128>(group, batch, ids_cap);
 }
 
-cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
-                        cudaStream_t s, bool pdl) {
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                        int dtype, int head_dim, int group, int grid, cudaStream_t s, bool pdl) {
   if (grid < 1) grid = 1;
   if (dtype == NS_BF16) {
-    return head_dim == 64 ? dispatch_g<__nv_bfloat16, 64>(p, group, grid, s, pdl)
-                          : dispatch_g<__nv_bfloat16, 128>(p, group, grid, s, pdl);
+    return head_dim == 64 ? dispatch_g<__nv_bfloat16, 64>(p, kmap, vmap, group, grid, s, pdl)
+                          : dispatch_g<__nv_bfloat16, 128>(p, kmap, vmap, group, grid, s, pdl);
   }
-  return head_dim == 64 ? dispatch_g<__half, 64>(p, group, grid, s, pdl)
-                        : dispatch_g<__half, 128>(p, group, grid, s, pdl);
+  return head_dim == 64 ? dispatch_g<__half, 64>(p, kmap, vmap, group, grid, s, pdl)
+                        : dispatch_g<__half, 128>(p, kmap, vmap, group, grid, s, pdl);
 }
 
 }  // namespace ns

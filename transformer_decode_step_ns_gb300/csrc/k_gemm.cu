@@ -10,8 +10,9 @@
 // operands K-major, staged by TMA with 128-byte swizzle into an mbarrier ring; one thread
 // issues tcgen05.mma into a TMEM accumulator; four warps read TMEM back for the epilogue.
 // Split-K over CTAs (chosen from the weight's shape only, never from the batch) gives small
-// matrices enough CTAs to stream HBM; the last-arriving CTA of a tile sums the partial tiles in
-// split order (deterministic, no spin) and runs the fused epilogue:
+// matrices enough CTAs to stream HBM.  The split CTAs of a tile form one thread-block cluster
+// and reduce through distributed shared memory in rank order (deterministic, no global
+// workspace, no atomics); each cluster CTA then runs the fused epilogue for its share of tokens:
 //   EPI_QKV    RMSNorm scale, RoPE on q/k, q store, k/v store into the paged cache slots
 //              (nanoserve notes: RoPE once per step, slot mapping);
 //   EPI_RESID  residual add, next RMSNorm's input x*gamma and per-tile sum of squares
@@ -57,7 +58,7 @@ __device__ __forceinline__ void set_err(int* err, int code) {
 }  // namespace
 
 template <typename T>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -167,64 +168,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ epilogue (4 warps)
+    // ------------------------------------------------------------------ epilogue stage 1
+    // TMEM -> shared tile [BN][128] fp32 (reuses the stage ring: every MMA has completed)
     const int q = warp & 3;             // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;      // output feature within the tile
-    const int et = threadIdx.x - 64;    // 0..127
-    const int ew = warp - 2;            // 0..3
-    bool ok = mbar_wait(accum, 0, abort_flag);
-    griddep_wait();
+    const bool ok = mbar_wait(accum, 0, abort_flag);
     tc_fence_after();
     if (!ok) {
       *abort_flag = 1;
       set_err(p.err, NS_DEV_WAIT_TIMEOUT);
     }
-    float* tile = reinterpret_cast<float*>(smem);  // [BN][128] fp32, reuses the stage ring
+    float* tile = reinterpret_cast<float*>(smem);
     const int nchunk = (m_valid + 15) >> 4;
     if (ok && !*abort_flag) {
       for (int c = 0; c < nchunk; ++c) {
         uint32_t r[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), r);
         tmem_ld_wait();
-        if (p.splits == 1) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) tile[(c * 16 + i) * kGemmTileN + row] = __uint_as_float(r[i]);
-        } else {
-          float* w = p.ws + (static_cast<size_t>(tile_id) * p.splits + split) * BN * kGemmTileN +
-                     static_cast<size_t>(c * 16) * kGemmTileN;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i * kGemmTileN + row] = __uint_as_float(r[i]);
-        }
+        for (int i = 0; i < 16; ++i) tile[(c * 16 + i) * kGemmTileN + row] = __uint_as_float(r[i]);
       }
     }
-    bool run = ok && !*abort_flag;
-    if (run && p.splits > 1) {
-      __threadfence();
-      named_barrier_sync(1, 128);
-      if (et == 0) {
-        const int old = atomicAdd(&p.counters[tile_id], 1);
-        const int last = (old == p.splits - 1) ? 1 : 0;
-        if (last) p.counters[tile_id] = 0;  // ready for the next launch that uses this slot
-        *last_flag = last;
-      }
-      named_barrier_sync(1, 128);
-      run = *last_flag != 0;
-      if (run) {
-        __threadfence();
-        const float* w0 = p.ws + static_cast<size_t>(tile_id) * p.splits * BN * kGemmTileN;
-        for (int j = 0; j < m_valid; ++j) {
-          float acc = 0.f;
-          for (int s = 0; s < p.splits; ++s)
-            acc += __ldcg(w0 + (static_cast<size_t>(s) * BN + j) * kGemmTileN + et);
-          tile[j * kGemmTileN + et] = acc;
-        }
+  }
+
+  // ------------------------------------------------------------------ split-K reduction
+  // The split CTAs of one output tile form a thread-block cluster.  CTA `rank` owns tokens
+  // j = rank, rank + S, ...; it sums their partial rows over every CTA of the cluster through
+  // distributed shared memory, in rank order (deterministic), then runs the epilogue for them.
+  __syncthreads();
+  const int S = p.splits;
+  const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  if (S > 1) cluster_sync();
+  const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;
+  float* tile = reinterpret_cast<float*>(smem);
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;  // 0..127: feature within the tile
+    const int ew = warp - 2;
+    griddep_wait();  // outputs may still be read by the previous kernel of the step
+    const bool run = !*abort_flag;
+    if (run && S > 1) {
+      const uint32_t base = smem_u32(tile);
+      for (int jj = 0; jj < n_own; ++jj) {
+        const int j = rank + S * jj;
+        const uint32_t off = base + static_cast<uint32_t>((j * kGemmTileN + et) * 4);
+        float v[kMaxSplits];
+#pragma unroll
+        for (int r = 0; r < kMaxSplits; ++r)
+          v[r] = r < S ? ld_shared_cluster_f32(map_shared_rank(off, r)) : 0.f;
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxSplits; ++r)
+          if (r < S) acc += v[r];
+        tile[j * kGemmTileN + et] = acc;
       }
     }
     if (run) {
       const EpiArgs& e = p.e;
       const bool scaled = e.sumsq_in != nullptr;
       if (scaled) {
-        for (int j = et; j < m_valid; j += 128) {
+        for (int jj = et; jj < n_own; jj += 128) {
+          const int j = rank + S * jj;
           float ss = 0.f;
           for (int t = 0; t < e.sumsq_tiles; ++t) ss += e.sumsq_in[static_cast<size_t>(t) * e.sumsq_ld + tok0 + j];
           rs_s[j] = rsqrtf(ss / static_cast<float>(e.norm_dim) + e.eps);
@@ -234,9 +237,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (p.epi == EPI_F32) {
         float* out = e.out_f32;
         if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
-        for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
-          const int j = idx >> 7, r = idx & 127;
-          float v = tile[idx];
+        for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
+          const int j = rank + S * (idx >> 7), r = idx & 127;
+          float v = tile[j * kGemmTileN + r];
           if (scaled) v *= rs_s[j];
           out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
         }
@@ -246,8 +249,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         T* kp = reinterpret_cast<T*>(e.k_pool);
         T* vp = reinterpret_cast<T*>(e.v_pool);
         if (n0 < e.q_dim + e.kv_dim) {
-          for (int idx = et; idx < m_valid * 64; idx += 128) {
-            const int j = idx >> 6, pr = idx & 63;
+          for (int idx = et; idx < n_own * 64; idx += 128) {
+            const int j = rank + S * (idx >> 6), pr = idx & 63;
             const int hl = pr / half, i = pr - hl * half;
             const int r_lo = hl * d + i, r_hi = r_lo + half;
             const int tok = tok0 + j;
@@ -278,8 +281,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         } else {
-          for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
-            const int j = idx >> 7, r = idx & 127;
+          for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
+            const int j = rank + S * (idx >> 7), r = idx & 127;
             const int tok = tok0 + j;
             const int col = n0 - e.q_dim - e.kv_dim + r;
             const int kvh = col / d, dim = col - kvh * d;
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               set_err(p.err, NS_DEV_BAD_SLOT);
               continue;
             }
-            const float v = tile[idx] * (scaled ? rs_s[j] : 1.f);
+            const float v = tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f);
             const size_t base =
                 ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
                  static_cast<size_t>(slot % e.block_size)) * d;
@@ -298,16 +301,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_proxy_async_global();
       } else if (p.epi == EPI_RESID) {
         T* xo = reinterpret_cast<T*>(e.xn_out);
-        for (int idx = et; idx < m_valid * kGemmTileN; idx += 128) {
-          const int j = idx >> 7, r = idx & 127;
+        for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
+          const int j = rank + S * (idx >> 7), r = idx & 127;
           const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
-          const float rn = e.resid[gi] + tile[idx];
+          const float rn = e.resid[gi] + tile[j * kGemmTileN + r];
           e.resid[gi] = rn;
           xo[gi] = Cvt<T>::from_f(rn * e.gamma_next[n0 + r]);
-          tile[idx] = rn * rn;
+          tile[j * kGemmTileN + r] = rn * rn;
         }
         named_barrier_sync(1, 128);
-        for (int j = ew; j < m_valid; j += 4) {
+        for (int jj = ew; jj < n_own; jj += 4) {
+          const int j = rank + S * jj;
           const float* tr = tile + j * kGemmTileN;
           float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
 #pragma unroll
@@ -318,8 +322,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if (p.epi == EPI_SWIGLU) {
         T* ao = reinterpret_cast<T*>(e.act_out);
         const int f0 = tile_n * 64;
-        for (int idx = et; idx < m_valid * 64; idx += 128) {
-          const int j = idx >> 6, c = idx & 63;
+        for (int idx = et; idx < n_own * 64; idx += 128) {
+          const int j = rank + S * (idx >> 6), c = idx & 63;
           const float sc = scaled ? rs_s[j] : 1.f;
           const float g = tile[j * kGemmTileN + c] * sc;
           const float u = tile[j * kGemmTileN + 64 + c] * sc;
@@ -330,6 +334,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   }
+  // no CTA of the cluster may exit while another still reads its tile
+  if (S > 1) cluster_sync();
 
   // ------------------------------------------------------------------ teardown
   __syncthreads();
@@ -355,6 +361,7 @@ size_t gemm_smem_bytes(int BN, int nstage) {
 }
 
 int gemm_pick_stages(int BN) {
+  if (BN <= 64) return 4;  // <= 97 KiB: two CTAs per SM, one's epilogue overlaps the other's loads
   const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
   int n = static_cast<int>(budget / stage);
@@ -390,11 +397,22 @@ cudaError_t launch_gemm_t(const CUtensorMap* mapA, const CUtensorMap* mapB, cons
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (p.splits > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = p.splits;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, gemm_kernel<T>, *mapA, *mapB, p);
 }
 }  // namespace

@@ -97,25 +97,15 @@ int pick_bn(int m) {
   return std::max(16, std::min(kMaxBN, bn));
 }
 
-// Split-K from the weight's shape only (never the batch): enough CTAs to cover the SMs,
-// at least two k-blocks per split.
+// Split-K from the weight's shape only (never the batch): about two CTAs per SM, at least two
+// k-blocks per split, at most one portable cluster (8 CTAs) per output tile.
 void choose_splits(int N, int K, int sms, int* splits, int* kb_per) {
   const int tiles = N / kGemmTileN, nkb = K / kGemmTileK;
-  int s = std::max(1, sms / std::max(1, tiles));
+  int s = std::max(1, 2 * sms / std::max(1, tiles));
   s = std::min(s, std::max(1, nkb / 2));
+  s = std::min(s, kMaxSplits);
   *kb_per = (nkb + s - 1) / s;
   *splits = (nkb + *kb_per - 1) / *kb_per;
-}
-
-size_t gemm_ws_bytes(int N, int splits, int rows) {
-  if (splits <= 1) return 0;
-  const int mt = (rows + kMaxBN - 1) / kMaxBN;
-  const size_t cap_rows = static_cast<size_t>(mt) * pick_bn(rows);
-  return static_cast<size_t>(N / kGemmTileN) * splits * cap_rows * kGemmTileN * sizeof(float);
-}
-
-int gemm_counter_count(int N, int rows) {
-  return (N / kGemmTileN) * ((rows + kMaxBN - 1) / kMaxBN) + 1;
 }
 
 int device_sms() {
@@ -186,6 +176,14 @@ ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
 }  // namespace
 
 void ns::set_last_error(const char* msg) { g_msg = msg ? msg : ""; }
+
+ns_status ns::make_pool_tmap(CUtensorMap* m, const void* pool, int dtype, long long rows,
+                             int head_dim, int block_size) {
+  if (rows <= 0 || rows >= (1ll << 31))
+    return fail(NS_ERR_UNSUPPORTED, "pool rows (blocks * kv heads * block_size) must fit in int32");
+  return make_tmap(m, pool, dtype, static_cast<uint64_t>(rows), static_cast<uint64_t>(head_dim),
+                   static_cast<uint32_t>(block_size));
+}
 
 // ------------------------------------------------------------------------------ block pool
 
@@ -276,10 +274,6 @@ struct LayerDev {
   float* ffn_norm = nullptr;
 };
 
-struct NanoSlot {
-  float* gemm_ws = nullptr;
-  int* gemm_counters = nullptr;
-};
 
 struct ns_ctx {
   ns_model_cfg cfg;
@@ -298,11 +292,13 @@ struct ns_ctx {
   void* act = nullptr;
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
+  double* inv_freq = nullptr;
   std::map<std::tuple<const void*, int>, CUtensorMap> bmaps;
   // KV cache
   int num_blocks = 0, block_size = 0, max_chunks = 1;
   void* pools = nullptr;
   std::vector<void*> kpool, vpool;
+  std::vector<CUtensorMap> kmaps, vmaps;  // 2-D views [blocks * Hkv * bs][d] for TMA tiles
   ns_block_pool pool;
   int* attn_counters = nullptr;
   float* attn_partials = nullptr;
@@ -316,7 +312,6 @@ struct ns_ctx {
   int n_split = 1;
   std::vector<int> split_sizes;
   int attn_budget = 0;
-  NanoSlot slots[4];
   cudaStream_t side = nullptr, cap = nullptr;
   std::vector<cudaEvent_t> events;
   // graphs
@@ -410,7 +405,7 @@ ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
 }
 
 ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
-                      int epi, const EpiArgs& e, NanoSlot& slot, cudaStream_t s, int kind) {
+                      int epi, const EpiArgs& e, cudaStream_t s, int kind) {
   GemmParams p{};
   p.M = m;
   p.row0 = row0;
@@ -422,8 +417,6 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   p.nstage = gemm_pick_stages(p.BN);
   p.epi = epi;
   p.idesc = gemm_idesc(h->dtype, p.BN);
-  p.ws = slot.gemm_ws;
-  p.counters = slot.gemm_counters;
   p.err = h->err;
   p.e = e;
   const CUtensorMap* mb = nullptr;
@@ -497,7 +490,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     ep.rope_cos = h->rope_cos;
     ep.rope_sin = h->rope_sin;
     ep.head_dim = d;
-    ep.theta = c.rope_theta;
+    ep.inv_freq = h->inv_freq;
     ep.batch = nb[i].second;
     ep.row0 = nb[i].first;
     ep.err = h->err;
@@ -523,7 +516,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.n_kv_heads = Hkv;
       e.block_size = h->block_size;
       e.pool_slots = static_cast<long long>(h->num_blocks) * h->block_size;
-      NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e, h->slots[i],
+      NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
                          st[i % 2], K_QKV));
       if (n > 1) NS_CUDA(cudaEventRecord(h->events[2 + static_cast<size_t>(l) * n + i], st[i % 2]));
     }
@@ -548,14 +541,16 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.block_size = h->block_size;
       ap.scale_log2 = scale_log2;
       ap.max_chunks = h->max_chunks;
+      ap.ids_cap = attn_chunk_tokens(c.max_blocks_per_seq * h->block_size) / h->block_size;
       ap.partials = h->attn_partials;
       ap.counters = h->attn_counters;
       ap.err = h->err;
-      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
+      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second, ap.ids_cap),
+                          nb[i].second * Hkv * h->max_chunks);
       if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
       {
         TimeScope ts(h, s, K_ATTN);
-        NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+        NS_CUDA(launch_attn(ap, &h->kmaps[l], &h->vmaps[l], h->dtype, d, G, grid, s, true));
       }
       h->kernels_last++;
 
@@ -566,12 +561,12 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       eo.sumsq_out = h->sumsq;
       eo.sumsq_ld = h->R;
       eo.resid_dim = H;
-      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, h->slots[i], s, K_O));
+      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O));
 
       EpiArgs eg = norm;
       eg.act_out = h->act;
       eg.ffn = F;
-      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, h->slots[i], s, K_GU));
+      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, s, K_GU));
 
       EpiArgs ed{};
       ed.resid = h->resid;
@@ -580,14 +575,14 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ed.sumsq_out = h->sumsq;
       ed.sumsq_ld = h->R;
       ed.resid_dim = H;
-      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, h->slots[i], s, K_DOWN));
+      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN));
     }
   }
   for (int i = 0; i < n; ++i) {
     EpiArgs el = norm;
     el.out_ptr_slot = m_logits;
     el.ldo = c.vocab;
-    NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el, h->slots[i],
+    NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el,
                        st[i % 2], K_LM));
   }
   if (n > 1) {
@@ -649,28 +644,6 @@ void free_proj(Proj& p) {
   p.w = nullptr;
 }
 
-ns_status alloc_slots(ns_ctx* h) {
-  size_t ws = 0;
-  int cnt = 1;
-  auto acc = [&](const Proj& p) {
-    ws = std::max(ws, gemm_ws_bytes(p.N, p.splits, h->R));
-    cnt = std::max(cnt, gemm_counter_count(p.N, h->R));
-  };
-  for (auto& L : h->layers) {
-    acc(L.qkv);
-    acc(L.o);
-    acc(L.gu);
-    acc(L.down);
-  }
-  acc(h->lm);
-  for (auto& s : h->slots) {
-    if (ws) NS_CUDA(cudaMalloc(&s.gemm_ws, ws));
-    NS_CUDA(cudaMalloc(&s.gemm_counters, cnt * sizeof(int)));
-    NS_CUDA(cudaMemset(s.gemm_counters, 0, cnt * sizeof(int)));
-  }
-  return NS_OK;
-}
-
 }  // namespace
 
 // ================================================================================== C ABI
@@ -719,13 +692,10 @@ void ns_destroy(ns_handle h) {
   cudaFree(h->act);
   cudaFree(h->rope_cos);
   cudaFree(h->rope_sin);
+  cudaFree(h->inv_freq);
   cudaFree(h->pools);
   cudaFree(h->attn_counters);
   cudaFree(h->attn_partials);
-  for (auto& s : h->slots) {
-    cudaFree(s.gemm_ws);
-    cudaFree(s.gemm_counters);
-  }
   cudaFreeHost(h->meta_host);
   cudaFree(h->meta_dev);
   cudaFree(h->err);
@@ -835,10 +805,17 @@ ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out
   CK(cuda(cudaMalloc(&h->act, R * F * e2), "malloc act"));
   CK(cuda(cudaMalloc(&h->rope_cos, R * (d / 2) * 4), "malloc rope"));
   CK(cuda(cudaMalloc(&h->rope_sin, R * (d / 2) * 4), "malloc rope"));
+  {
+    // RoPE inverse frequencies theta^(-2i/d), computed once on the host in fp64
+    std::vector<double> inv(d / 2);
+    for (int i = 0; i < d / 2; ++i) inv[i] = std::pow(c.rope_theta, -2.0 * i / static_cast<double>(d));
+    CK(cuda(cudaMalloc(&h->inv_freq, inv.size() * sizeof(double)), "malloc inv_freq"));
+    CK(cuda(cudaMemcpy(h->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice),
+            "copy inv_freq"));
+  }
   CK(cuda(cudaMemset(h->xn, 0, R * H * e2), "memset"));
   CK(cuda(cudaMemset(h->o, 0, R * qd * e2), "memset"));
   CK(cuda(cudaMemset(h->act, 0, R * F * e2), "memset"));
-  CK(alloc_slots(h));
   // metadata: pinned host staging + device copy, sized for max_batch
   h->meta_cap = meta_layout(h->R, c.max_blocks_per_seq).total;
   CK(cuda(cudaMallocHost(&h->meta_host, h->meta_cap), "pinned metadata"));
@@ -862,16 +839,25 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   const ns_model_cfg& c = h->cfg;
   const size_t pool = static_cast<size_t>(num_blocks) * c.n_kv_heads * block_size * c.head_dim * 2;
   NS_CUDA(cudaSetDevice(h->dev));
+  const long long pool_rows = static_cast<long long>(num_blocks) * c.n_kv_heads * block_size;
+  if (pool_rows >= (1ll << 31))
+    return fail(NS_ERR_UNSUPPORTED, "pool rows (blocks * kv heads * block_size) must fit in int32");
   NS_CUDA(cudaMalloc(&h->pools, pool * 2 * c.n_layers));
+  // never-written slots read as zeros (finite), never as stale garbage
+  NS_CUDA(cudaMemset(h->pools, 0, pool * 2 * c.n_layers));
   h->kpool.resize(c.n_layers);
   h->vpool.resize(c.n_layers);
+  h->kmaps.resize(c.n_layers);
+  h->vmaps.resize(c.n_layers);
   for (int l = 0; l < c.n_layers; ++l) {
     h->kpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l));
     h->vpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l) + 1);
+    NS_TRY(make_pool_tmap(&h->kmaps[l], h->kpool[l], h->dtype, pool_rows, c.head_dim, block_size));
+    NS_TRY(make_pool_tmap(&h->vmaps[l], h->vpool[l], h->dtype, pool_rows, c.head_dim, block_size));
   }
   h->num_blocks = num_blocks;
   h->block_size = block_size;
-  h->max_chunks = (c.max_blocks_per_seq * block_size + kAttnChunkTokens - 1) / kAttnChunkTokens;
+  h->max_chunks = attn_max_chunks(c.max_blocks_per_seq * block_size);
   const int G = c.n_q_heads / c.n_kv_heads;
   const size_t rows_heads = static_cast<size_t>(h->R) * c.n_kv_heads;
   NS_CUDA(cudaMalloc(&h->attn_counters, rows_heads * sizeof(int)));
@@ -1084,8 +1070,12 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
     return fail(NS_ERR_INVALID_ARG, "attention arguments");
   const int G = n_q_heads / n_kv_heads;
   if (!attn_supported(head_dim, G, block_size)) return fail(NS_ERR_UNSUPPORTED, "attention shape");
-  const int max_chunks = (max_blocks_per_seq * block_size + kAttnChunkTokens - 1) / kAttnChunkTokens;
+  const int max_chunks = attn_max_chunks(max_blocks_per_seq * block_size);
   const size_t rows_heads = static_cast<size_t>(batch) * n_kv_heads;
+  const long long pool_rows = static_cast<long long>(num_blocks) * n_kv_heads * block_size;
+  CUtensorMap kmap, vmap;
+  NS_TRY(make_pool_tmap(&kmap, k_pool, dtype, pool_rows, head_dim, block_size));
+  NS_TRY(make_pool_tmap(&vmap, v_pool, dtype, pool_rows, head_dim, block_size));
   DevScratch* sc = nullptr;
   NS_TRY(scratch_get(rows_heads * max_chunks * G * (head_dim + 2) * sizeof(float), rows_heads, &sc));
   AttnParams ap{};
@@ -1105,13 +1095,15 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
   ap.block_size = block_size;
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.max_chunks = max_chunks;
+  ap.ids_cap = attn_chunk_tokens(max_blocks_per_seq * block_size) / block_size;
   ap.partials = static_cast<float*>(sc->buf);
   ap.counters = sc->counters;
   ap.err = sc->err;
-  const int cap = attn_max_grid(dtype, head_dim, G, batch);
+  const int cap = attn_max_grid(dtype, head_dim, G, batch, ap.ids_cap);
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid = static_cast<int>(std::min<long long>(cap, units));
-  NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));
+  NS_CUDA(launch_attn(ap, &kmap, &vmap, dtype, head_dim, G, grid,
+                      reinterpret_cast<cudaStream_t>(stream), false));
   return NS_OK;
 }
 
@@ -1139,9 +1131,7 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   p.epi = EPI_F32;
   p.idesc = gemm_idesc(dtype, p.BN);
   DevScratch* sc = nullptr;
-  NS_TRY(scratch_get(gemm_ws_bytes(n, pr.splits, m) + 256, gemm_counter_count(n, m), &sc));
-  p.ws = static_cast<float*>(sc->buf);
-  p.counters = sc->counters;
+  NS_TRY(scratch_get(0, 0, &sc));
   p.err = sc->err;
   p.e.out_f32 = y;
   p.e.ldo = n;

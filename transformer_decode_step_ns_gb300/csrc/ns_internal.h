@@ -13,7 +13,9 @@ constexpr int kGemmTileN = 128;   // output features per CTA (UMMA M)
 constexpr int kGemmTileK = 64;    // K per pipeline stage (one 128-byte swizzle row)
 constexpr int kGemmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kMaxBN = 256;       // token tile (UMMA N) upper bound
-constexpr int kAttnChunkTokens = 256;  // static split-K chunk of the decode attention
+constexpr int kMaxSplits = 8;     // split-K CTAs per tile = portable cluster size
+constexpr int kAttnChunkBase = 128;  // decode-attention chunk: 128 * ceil(seq_len / 2048) tokens
+constexpr int kAttnMaxChunks = 16;   // so a row never splits into more than 16 chunks
 constexpr int kMaxRows = 4096;
 
 enum EpiMode : int {
@@ -57,13 +59,11 @@ struct GemmParams {
   int row0;     // first row in the activation / output buffers
   int N, K;     // output features, reduction length
   int BN;       // token tile, multiple of 16, 16..256
-  int splits;   // split-K count
+  int splits;   // split-K count = cluster size along grid y (<= kMaxSplits)
   int kb_per_split;
   int nstage;
   int epi;
   uint32_t idesc;
-  float* ws;       // split-K partial tiles
-  int* counters;   // per output tile arrival counters (zero between launches)
   int* err;
   EpiArgs e;
 };
@@ -80,7 +80,8 @@ struct AttnParams {
   long long out_row_stride;
   int batch, row0, n_kv_heads, num_blocks, block_size;
   float scale_log2;        // softmax scale * log2(e)
-  int max_chunks;          // ceil(mb * block_size / chunk): partial slots per (row, kv head)
+  int max_chunks;          // partial slots per (row, kv head): attn_max_chunks(mb * block_size)
+  int ids_cap;             // blocks of the longest chunk: attn_chunk_tokens(mb * bs) / bs
   float* partials;         // [rows][n_kv_heads][max_chunks][G][head_dim + 2]
   int* counters;           // [rows][n_kv_heads], zero between launches
   int* err;
@@ -99,7 +100,7 @@ struct EmbedParams {
   float* rope_cos;
   float* rope_sin;
   int head_dim;
-  double theta;
+  const double* inv_freq;  // [head_dim / 2] theta^(-2i/d), fp64
   int batch, row0;
   int* err;
 };
@@ -112,9 +113,24 @@ cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const 
                         int dtype, cudaStream_t s, bool pdl);
 
 bool attn_supported(int head_dim, int group, int block_size);
-int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
-cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
-                        cudaStream_t s, bool pdl);
+int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap);  // one wave
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                        int dtype, int head_dim, int group, int grid, cudaStream_t s, bool pdl);
+// Chunking of a row of length L (a function of L alone): chunks of 128 * ceil(L / 2048) tokens,
+// so at most 16 chunks per row.  attn_max_chunks bounds the chunk count of any L <= L_max.
+__host__ __device__ inline int attn_chunk_tokens(int L) {
+  return kAttnChunkBase * (L > 2048 ? (L + 2047) / 2048 : 1);
+}
+__host__ __device__ inline int attn_num_chunks(int L) {
+  return L <= 0 ? 0 : (L + attn_chunk_tokens(L) - 1) / attn_chunk_tokens(L);
+}
+__host__ __device__ inline int attn_max_chunks(int L_max) {
+  const int c = (L_max + kAttnChunkBase - 1) / kAttnChunkBase;
+  return c < kAttnMaxChunks ? c : kAttnMaxChunks;
+}
+// 2-D TMA view [rows][d] of a paged K or V pool, box 64 x block_size (128-byte swizzle).
+ns_status make_pool_tmap(CUtensorMap* m, const void* pool, int dtype, long long rows, int head_dim,
+                         int block_size);
 
 // Record the text ns_last_error_message() returns on this thread.
 void set_last_error(const char* msg);
