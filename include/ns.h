@@ -75,7 +75,7 @@ typedef struct ns_ctx* ns_handle;
  * rope_theta: RoPE base; pairs (i, i + d/2), inverse frequency theta^(-2i/d).
  * rms_eps: RMSNorm epsilon, y = x / sqrt(mean(x^2) + eps) * gamma.
  * max_batch: largest batch ns_decode_step accepts (rows; <= 4096).
- * max_blocks_per_seq: width of the block table rows passed to ns_decode_step.
+ * max_blocks_per_seq: width of the block table rows passed to ns_decode_step (<= 4096).
  * use_graphs: 1 = capture the step as a CUDA graph per batch size on first use and replay
  * it; 0 = launch the kernels eagerly every step (a debugging path). */
 typedef struct {
@@ -192,7 +192,8 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
  *   [1, max_blocks_per_seq*block_size]; out [batch][n_q_heads][head_dim] (same dtype as q).
  * For q head h the kv head is h / (n_q_heads / n_kv_heads); o = softmax(q.K^T * scale) V over
  * tokens t < seq_len.  The split depends only on seq_len, so results do not depend on the
- * batch.  num_blocks * n_kv_heads * block_size must be below 2^31.
+ * batch.  num_blocks * n_kv_heads * block_size must be below 2^31 and max_blocks_per_seq *
+ * block_size at most 65536.
  * Rows of length L split into chunks of 128 * ceil(L / 2048) tokens (at most 16), merged by
  * log-sum-exp.  Scratch (partials and counters) is allocated by the library on first use per
  * device and kept until exit.  Slots past seq_len in a row's last block are never used, even
@@ -213,8 +214,9 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
  * where a failed bounds check inside the kernel is recorded.  The split-K scratch (partials and
  * counters) lives in a fixed buffer inside the library image: 32 MiB of partials and 65,536
  * counters, held by every GPU that loads the library until the process exits.  Requests needing
- * more -- batch * n_kv_heads * min(16, ceil(max_blocks_per_seq * block_size / 128)) *
- * (n_q_heads / n_kv_heads) * (head_dim + 2) * 4 bytes, or batch * n_kv_heads counters -- return
+ * more -- batch * n_kv_heads slots of min(16, ceil(max_blocks_per_seq * block_size / 128)) *
+ * (n_q_heads / n_kv_heads) * (head_dim + 2) floats each (rounded up to 16 bytes), or
+ * batch * n_kv_heads counters -- return
  * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the
  * buffer's device address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture.  All calls on a device share the buffer and each call leaves

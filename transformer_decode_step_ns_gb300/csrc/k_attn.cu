@@ -1,4 +1,4 @@
-// Paged grouped-query decode attention: warp-independent units, TMA-staged K/V tiles,
+// Paged grouped-query decode attention: warp-independent units, cp.async-staged K/V tiles,
 // tensor-core (mma.sync m16n8k16) QK^T and PV, split-K over fixed chunks with an in-kernel merge.
 //
 // "GPU waiting, not working" (nanoserve notes), change table: grouped-query attention must not
@@ -10,11 +10,13 @@
 //   128 * ceil(L / 2048) tokens (at most 16 chunks); the chunking is a function of L alone, so a
 //   row's result never depends on the rest of the batch.
 // * Every warp walks its own units (round-robin over all warps of the grid) with a private ring
-//   of TMA tensor copies: one 16 x d K tile and one V tile per cache block, 128-byte swizzled so
-//   the ldmatrix reads below are bank-conflict free.  The warp refills a stage as soon as it has
-//   consumed it and runs ahead across unit boundaries.  A unit's block ids are copied to shared
-//   memory (cp.async) one unit ahead, and its q one unit ahead into registers, so the stream
-//   never waits on a block-table or q read.
+//   of stages; each stage holds one 16 x d K tile and one V tile of a cache block, copied with
+//   16-byte cp.async by all 32 lanes (each tile is one contiguous run, so every warp request is a
+//   coalesced 512-byte read) into an XOR-swizzled layout that keeps the ldmatrix reads below
+//   bank-conflict free.  Small per-block copies go through the load/store path rather than the
+//   TMA engine, whose per-request cost limits throughput at 2-4 KiB tiles.  The warp refills a
+//   stage as soon as it has consumed it and runs ahead across unit boundaries; q of the next unit
+//   is loaded one unit ahead into registers.
 // * The G <= 8 query heads of the group form the rows of one 16-row mma.sync tile:
 //     S^T[head][token]  = q[head][:] . K[token][:]          (A = q in registers, B = K tile)
 //     O^T[dim][head]   += V^T[dim][token] . P^T[token][head] (A = V tile via ldmatrix.trans)
@@ -82,8 +84,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "memory");
 }
 
-__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+// 16-byte global -> shared copy bypassing L1, with an L2 eviction-priority hint.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* gsrc, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_dst),
+               "l"(gsrc), "l"(policy)
                : "memory");
 }
 
@@ -91,12 +95,9 @@ __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void set_err(int* err, int code) {
@@ -116,39 +117,31 @@ struct AttnShape {
   static constexpr int NST = (D == 128) ? 3 : 6;
   static constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
   static constexpr int RING = NST * STAGE;     // bytes per warp
-  static constexpr int OFF_BAR = NW * RING;
-  static constexpr int OFF_FLAG = OFF_BAR + NW * NST * 8;
-  static constexpr int OFF_IDS = OFF_FLAG + 16;  // per warp, 2 slots x ids_cap block ids
+  static constexpr int CPL = 2 * BS * D / 8 / 32;  // 16-byte copies per lane per stage
+  static constexpr int OFF_MRG = NW * RING;    // per warp, [2][8][16] floats of merge scratch
+  static constexpr int OFF_IDS = OFF_MRG + NW * 256 * 4;  // per warp, ids of the producer unit
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G >= 1 && G <= 8, "group");
   // then chunk prefix [batch + 1], lengths [batch], scan scratch [NT]
   static size_t smem_bytes(int batch, int ids_cap) {
-    return 1024 + OFF_IDS + static_cast<size_t>(NW) * 2 * ids_cap * 4 +
+    return 1024 + OFF_IDS + static_cast<size_t>(NW) * ids_cap * 4 +
            static_cast<size_t>(2 * batch + 1 + NT) * 4;
   }
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
-    attn_decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+__global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(const AttnParams p) {
   using S = AttnShape<D, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* abort_flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
-  int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);  // [NW][2][ids_cap]
-  int* pre = ids_all + S::NW * 2 * p.ids_cap;                 // chunk prefix over rows [batch + 1]
+  float* merge_all = reinterpret_cast<float*>(smem + S::OFF_MRG);  // [NW][2][8][16]
+  int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);  // [NW][ids_cap]
+  int* pre = ids_all + S::NW * p.ids_cap;                     // chunk prefix over rows [batch + 1]
   int* lens = pre + p.batch + 1;                              // validated seq_lens [batch]
   int* tot = lens + p.batch;                                  // per-thread scan scratch [NT]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads, batch = p.batch;
   uint8_t* ring = smem + warp * S::RING;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR) + warp * S::NST;
-
-  if (lane == 0) {
-    for (int s = 0; s < S::NST; ++s) mbar_init(&full[s], 1);
-  }
-  if (tid == 0) *abort_flag = 0;
   // Chunk prefix over the rows.  seq_lens are step metadata, final before the step starts, so
   // under programmatic dependent launch this overlaps the previous kernel.
   {
@@ -163,7 +156,6 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
       run += ok ? attn_num_chunks(L) : 0;
     }
     tot[tid] = run;
-    fence_mbar_init();
     __syncthreads();
     if (tid == 0) {
       int acc = 0;
@@ -211,50 +203,72 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
 
   const int gw = blockIdx.x * S::NW + warp, TW = gridDim.x * S::NW;
 
-  // ---- producer cursor (warp-uniform): the warp's stream of (unit, block) in consumption order
-  int* ids = ids_all + warp * 2 * p.ids_cap;
-  auto prefetch_ids = [&](int unit, int slot) {
-    if (unit < total) {
-      const Unit x = decode(unit);
-      const int* src = p.block_tables + static_cast<size_t>(p.row0 + x.b) * p.mb + x.t0 / S::BS;
-      for (int j = lane; j < x.nblk; j += 32) cp_async_4(ids + slot * p.ids_cap + j, src + j);
-    }
-    cp_async_commit();
-  };
-  int pu = gw, pi = 0, ps = 0, issued = 0;
-  Unit pun{};
-  auto enter = [&]() {  // the producer starts unit pu (slot ps): its ids were prefetched
-    cp_async_wait_all();
-    __syncwarp();
-    if (pu < total) pun = decode(pu);
-    prefetch_ids(pu + TW, ps ^ 1);
-  };
-  prefetch_ids(pu, 0);
-  enter();
-  auto issue = [&](int stage) {  // warp-collective; lane 0 issues the copies
-    if (pu >= total) return;
-    int blk = ids[ps * p.ids_cap + pi];
-    if (blk < 0 || blk >= p.num_blocks) {
-      if (lane == 0) set_err(p.err, NS_DEV_BAD_BLOCK);
-      blk = 0;  // keep the pipeline consistent; the error word flags the result
-    }
-    if (lane == 0) {
-      uint8_t* dst = ring + stage * S::STAGE;
-      const int y = (blk * Hkv + pun.g) * S::BS;
-      mbar_arrive_expect_tx(&full[stage], S::STAGE);
+  // ---- producer cursor (warp-uniform): the warp's stream of (unit, block) in consumption
+  // order.  The block ids of the next unit are loaded into registers (lane j holds ids j,
+  // j + 32, ...) when the producer enters the current one, and stored to shared memory when it
+  // reaches the next, so the stream never waits on a block-table read.  Every stage is one
+  // cp.async group, so "oldest stage landed" is wait_group(NST - 1).
+  int* ids = ids_all + warp * p.ids_cap;
+  const uint64_t pol = policy_evict_first();  // K/V are streamed once
+  const T* kpool = reinterpret_cast<const T*>(p.k_pool);
+  const T* vpool = reinterpret_cast<const T*>(p.v_pool);
+  int pu = gw, pi = 0;
+  Unit pun{}, nun{};
+  int nid[kAttnIdRegs];
+  auto load_ids = [&](int unit) {  // registers <- block ids of `unit` (non-blocking loads)
+    nun = decode(unit);
+    const int* src = p.block_tables + static_cast<size_t>(p.row0 + nun.b) * p.mb + nun.t0 / S::BS;
 #pragma unroll
-      for (int h = 0; h < S::NH; ++h) {
-        tma_load_2d(dst + h * 2048, &kmap, &full[stage], h * 64, y);
-        tma_load_2d(dst + S::TILE + h * 2048, &vmap, &full[stage], h * 64, y);
+    for (int k = 0; k < kAttnIdRegs; ++k) {
+      const int j = lane + 32 * k;
+      nid[k] = j < nun.nblk ? src[j] : 0;
+    }
+  };
+  auto enter = [&]() {  // the producer starts unit pu; its ids are in the registers
+    __syncwarp();
+    if (pu < total) {
+      pun = nun;
+#pragma unroll
+      for (int k = 0; k < kAttnIdRegs; ++k) {
+        const int j = lane + 32 * k;
+        if (j < pun.nblk) {
+          int blk = nid[k];
+          if (blk < 0 || blk >= p.num_blocks) {
+            set_err(p.err, NS_DEV_BAD_BLOCK);
+            blk = 0;  // keep the pipeline consistent; the error word flags the result
+          }
+          ids[j] = blk;
+        }
+      }
+      if (pu + TW < total) load_ids(pu + TW);
+    }
+    __syncwarp();
+  };
+  if (pu < total) load_ids(pu);
+  enter();
+  auto issue = [&](int stage) {  // warp-collective: one cp.async group per call
+    if (pu < total) {
+      const size_t tile_off = (static_cast<size_t>(ids[pi]) * Hkv + pun.g) * S::BS * D;
+      const uint8_t* ksrc = reinterpret_cast<const uint8_t*>(kpool + tile_off);
+      const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(vpool + tile_off);
+      const uint32_t dst = smem_u32(ring + stage * S::STAGE);
+#pragma unroll
+      for (int k = 0; k < S::CPL; ++k) {
+        const int c = lane + 32 * k;                  // chunk over [K | V] x 16 rows x D/8
+        const int kv = c / (S::BS * D / 8);           // 0 = K, 1 = V
+        const int ci16 = c - kv * (S::BS * D / 8);
+        const int t = ci16 / (D / 8), c16 = ci16 % (D / 8);
+        const int h = c16 >> 3, cc = c16 & 7;
+        const uint32_t d_off = kv * S::TILE + h * 2048 + t * 128 + ((cc ^ (t & 7)) << 4);
+        cp_async_16(dst + d_off, (kv ? vsrc : ksrc) + ci16 * 16, pol);
+      }
+      if (++pi >= pun.nblk) {
+        pi = 0;
+        pu += TW;
+        enter();
       }
     }
-    ++issued;
-    if (++pi >= pun.nblk) {
-      pi = 0;
-      pu += TW;
-      ps ^= 1;
-      enter();
-    }
+    cp_async_commit();
   };
   for (int s = 0; s < S::NST; ++s) issue(s);
 
@@ -285,8 +299,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
   load_q(gw);
 
   int ci = 0;
-  bool failed = false;
-  for (int u = gw; u < total && !failed; u += TW) {
+  for (int u = gw; u < total; u += TW) {
     const Unit x = decode(u);
     const size_t row = static_cast<size_t>(p.row0 + x.b);
     uint32_t qa[S::KS][2];
@@ -303,18 +316,12 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
 
     for (int i = 0; i < x.nblk; ++i, ++ci) {
       const int s = ci % S::NST;
-      if (!mbar_wait(&full[s], static_cast<uint32_t>(ci / S::NST) & 1u, abort_flag)) {
-        *abort_flag = 1;
-        set_err(p.err, NS_DEV_WAIT_TIMEOUT);
-        failed = true;
-      }
-      failed = __any_sync(0xffffffffu, failed);
-      if (failed) break;
+      cp_async_wait_group<S::NST - 1>();  // this lane's copies of the oldest stage landed
+      __syncwarp();                       // ... and every other lane's
       const uint8_t* kt = ring + s * S::STAGE;
       const uint8_t* vt = kt + S::TILE;
       const int n_valid = min(S::BS, x.t1 - (x.t0 + i * S::BS));
-      const bool zeroed = n_valid < S::BS;
-      if (zeroed) {
+      if (n_valid < S::BS) {
         // stale slots past seq_len: zero their V rows so 0 * (anything) stays 0
         uint4* v4 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(vt));
         for (int c = lane; c < S::BS * S::NH * 8; c += 32) {
@@ -384,11 +391,8 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
       }
       // ---- the stage is consumed: refill it with the next block of this warp's stream
       __syncwarp();
-      // generic-proxy zero writes must be ordered before the TMA overwrite of this stage
-      if (zeroed && lane == 0) fence_proxy_async_smem();
       issue(s);
     }
-    if (failed) break;
 
     // ---- unit result: heads 2tq and 2tq + 1 of this lane's accumulator columns
     const float l_e = __shfl_sync(0xffffffffu, l_run, 8 * tq);
@@ -409,24 +413,24 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
         }
       }
     } else {
-      const size_t slot0 = (row * Hkv + x.g) * static_cast<size_t>(p.max_chunks);
-      float* part = p.partials + (slot0 + x.chunk) * G * (D + 2);
+      // partial slot of (row, kv head): acc [max_chunks][G][D], then (m, l) [max_chunks][G][2]
+      float* pacc = p.partials + (row * Hkv + x.g) * attn_slot_floats(p.max_chunks, G, D);
+      float* pml = pacc + static_cast<size_t>(p.max_chunks) * G * D;
+      float* part = pacc + static_cast<size_t>(x.chunk) * G * D;
 #pragma unroll
       for (int mt = 0; mt < S::KS; ++mt) {
         const int d0 = mt * 16 + gq;
         if (h_e < G) {
-          part[h_e * (D + 2) + d0] = acc[mt][0];
-          part[h_e * (D + 2) + d0 + 8] = acc[mt][2];
+          part[h_e * D + d0] = acc[mt][0];
+          part[h_e * D + d0 + 8] = acc[mt][2];
         }
         if (h_o < G) {
-          part[h_o * (D + 2) + d0] = acc[mt][1];
-          part[h_o * (D + 2) + d0 + 8] = acc[mt][3];
+          part[h_o * D + d0] = acc[mt][1];
+          part[h_o * D + d0 + 8] = acc[mt][3];
         }
       }
-      if (tq == 0 && gq < G) {
-        part[gq * (D + 2) + D] = m_run;
-        part[gq * (D + 2) + D + 1] = l_run;
-      }
+      if (tq == 0 && gq < G)
+        reinterpret_cast<float2*>(pml)[x.chunk * G + gq] = make_float2(m_run, l_run);
       __threadfence();
       __syncwarp();
       int last = 0;
@@ -437,44 +441,74 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
+        // Merge the chunks: weight_c = 2^(m_c - M) / sum_c' l_c' 2^(m_c' - M), summed in chunk
+        // order.  One round trip for every (m, l), then one per head for the accumulators.
         __threadfence();
-        const float* p0 = p.partials + slot0 * G * (D + 2);
-        T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
-        for (int hh = 0; hh < G; ++hh) {
-          // lane c < nchunks holds chunk c's (m, l); weights 2^(m_c - M), summed in chunk order
-          float mc = -INFINITY, lc = 0.f;
-          if (lane < x.nchunks) {
-            mc = __ldcg(p0 + (static_cast<size_t>(lane) * G + hh) * (D + 2) + D);
-            lc = __ldcg(p0 + (static_cast<size_t>(lane) * G + hh) * (D + 2) + D + 1);
-          }
-          float M = mc;
+        float* mw = merge_all + warp * 256;  // [2][8 heads][16 chunks]
+        const int nml = x.nchunks * G;       // <= 128
+        float2 ml[4];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          const float w = lane < x.nchunks ? exp2f(mc - M) : 0.f;
-          float Lsum = 0.f;
-          for (int c = 0; c < x.nchunks; ++c)
-            Lsum = fmaf(__shfl_sync(0xffffffffu, lc, c), __shfl_sync(0xffffffffu, w, c), Lsum);
-          for (int dd = lane; dd < D; dd += 32) {
-            float o = 0.f;
-            for (int c = 0; c < x.nchunks; ++c) {
-              const float wc = __shfl_sync(0xffffffffu, w, c);
-              o = fmaf(__ldcg(p0 + (static_cast<size_t>(c) * G + hh) * (D + 2) + dd), wc, o);
-            }
-            orow[hh * D + dd] = MV<T>::from_f(o / Lsum);
+        for (int k = 0; k < 4; ++k) {
+          const int i = lane + 32 * k;
+          ml[k] = i < nml ? __ldcg(reinterpret_cast<const float2*>(pml) + i) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = lane + 32 * k;
+          if (i < nml) {
+            const int c = i / G, hh = i - c * G;
+            mw[hh * 16 + c] = ml[k].x;
+            mw[128 + hh * 16 + c] = ml[k].y;
           }
         }
+        __syncwarp();
+        if (lane < G) {
+          float M = -INFINITY;
+          for (int c = 0; c < x.nchunks; ++c) M = fmaxf(M, mw[lane * 16 + c]);
+          float Lsum = 0.f;
+          for (int c = 0; c < x.nchunks; ++c) Lsum = fmaf(mw[128 + lane * 16 + c], exp2f(mw[lane * 16 + c] - M), Lsum);
+          const float inv = 1.f / Lsum;
+          for (int c = 0; c < x.nchunks; ++c) mw[lane * 16 + c] = exp2f(mw[lane * 16 + c] - M) * inv;
+        }
+        __syncwarp();
+        T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
+        constexpr int VW = D / 32;  // dims per lane: 4 (d = 128) or 2 (d = 64)
+        for (int hh = 0; hh < G; ++hh) {
+          float o[VW];
+#pragma unroll
+          for (int e = 0; e < VW; ++e) o[e] = 0.f;
+          for (int cb = 0; cb < x.nchunks; cb += 8) {  // 8 chunks' loads in flight at a time
+            float v[8][VW];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              if (cb + c < x.nchunks) {
+                const float* src = pacc + (static_cast<size_t>(cb + c) * G + hh) * D + VW * lane;
+                if constexpr (VW == 4) {
+                  const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+                  v[c][0] = t.x; v[c][1] = t.y; v[c][2] = t.z; v[c][3] = t.w;
+                } else {
+                  const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+                  v[c][0] = t.x; v[c][1] = t.y;
+                }
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              if (cb + c < x.nchunks) {
+                const float w = mw[hh * 16 + cb + c];
+#pragma unroll
+                for (int e = 0; e < VW; ++e) o[e] = fmaf(v[c][e], w, o[e]);
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < VW; ++e) orow[hh * D + VW * lane + e] = MV<T>::from_f(o[e]);
+        }
+        __syncwarp();
       }
     }
   }
-  // On the normal path every issued copy was consumed.  After a timed-out wait, copies this
-  // warp issued but did not consume must land before the CTA releases its shared memory.
-  __syncwarp();
-  cp_async_wait_all();
-  if (failed && lane == 0) {
-    for (int c = ci; c < issued; ++c) {
-      (void)mbar_wait(&full[c % S::NST], static_cast<uint32_t>(c / S::NST) & 1u, nullptr);
-    }
-  }
+  cp_async_wait_group<0>();  // every copy this warp issued was consumed; drain regardless
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -482,8 +516,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2)
 namespace {
 
 template <typename T, int D, int G>
-cudaError_t launch_attn_t(const AttnParams& p, const CUtensorMap* km, const CUtensorMap* vm,
-                          int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pdl) {
   using S = AttnShape<D, G>;
   static int configured_mask = 0;
   int dev = 0;
@@ -504,18 +537,17 @@ cudaError_t launch_attn_t(const AttnParams& p, const CUtensorMap* km, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G>, *km, *vm, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G>, p);
 }
 
 template <typename T, int D>
-cudaError_t dispatch_g(const AttnParams& p, const CUtensorMap* km, const CUtensorMap* vm,
-                       int group, int grid, cudaStream_t s, bool pdl) {
+cudaError_t dispatch_g(const AttnParams& p, int group, int grid, cudaStream_t s, bool pdl) {
   switch (group) {
-    case 1: return launch_attn_t<T, D, 1>(p, km, vm, grid, s, pdl);
-    case 2: return launch_attn_t<T, D, 2>(p, km, vm, grid, s, pdl);
-    case 4: return launch_attn_t<T, D, 4>(p, km, vm, grid, s, pdl);
-    case 7: return launch_attn_t<T, D, 7>(p, km, vm, grid, s, pdl);
-    case 8: return launch_attn_t<T, D, 8>(p, km, vm, grid, s, pdl);
+    case 1: return launch_attn_t<T, D, 1>(p, grid, s, pdl);
+    case 2: return launch_attn_t<T, D, 2>(p, grid, s, pdl);
+    case 4: return launch_attn_t<T, D, 4>(p, grid, s, pdl);
+    case 7: return launch_attn_t<T, D, 7>(p, grid, s, pdl);
+    case 8: return launch_attn_t<T, D, 8>(p, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -562,15 +594,15 @@ int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap) {
                         : max_grid_g<__half, 128>(group, batch, ids_cap);
 }
 
-cudaError_t launch_attn(const AttnParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                        int dtype, int head_dim, int group, int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
+                        cudaStream_t s, bool pdl) {
   if (grid < 1) grid = 1;
   if (dtype == NS_BF16) {
-    return head_dim == 64 ? dispatch_g<__nv_bfloat16, 64>(p, kmap, vmap, group, grid, s, pdl)
-                          : dispatch_g<__nv_bfloat16, 128>(p, kmap, vmap, group, grid, s, pdl);
+    return head_dim == 64 ? dispatch_g<__nv_bfloat16, 64>(p, group, grid, s, pdl)
+                          : dispatch_g<__nv_bfloat16, 128>(p, group, grid, s, pdl);
   }
-  return head_dim == 64 ? dispatch_g<__half, 64>(p, kmap, vmap, group, grid, s, pdl)
-                        : dispatch_g<__half, 128>(p, kmap, vmap, group, grid, s, pdl);
+  return head_dim == 64 ? dispatch_g<__half, 64>(p, group, grid, s, pdl)
+                        : dispatch_g<__half, 128>(p, group, grid, s, pdl);
 }
 
 }  // namespace ns

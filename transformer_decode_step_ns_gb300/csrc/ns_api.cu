@@ -177,13 +177,6 @@ ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
 
 void ns::set_last_error(const char* msg) { g_msg = msg ? msg : ""; }
 
-ns_status ns::make_pool_tmap(CUtensorMap* m, const void* pool, int dtype, long long rows,
-                             int head_dim, int block_size) {
-  if (rows <= 0 || rows >= (1ll << 31))
-    return fail(NS_ERR_UNSUPPORTED, "pool rows (blocks * kv heads * block_size) must fit in int32");
-  return make_tmap(m, pool, dtype, static_cast<uint64_t>(rows), static_cast<uint64_t>(head_dim),
-                   static_cast<uint32_t>(block_size));
-}
 
 // ------------------------------------------------------------------------------ block pool
 
@@ -298,7 +291,6 @@ struct ns_ctx {
   int num_blocks = 0, block_size = 0, max_chunks = 1;
   void* pools = nullptr;
   std::vector<void*> kpool, vpool;
-  std::vector<CUtensorMap> kmaps, vmaps;  // 2-D views [blocks * Hkv * bs][d] for TMA tiles
   ns_block_pool pool;
   int* attn_counters = nullptr;
   float* attn_partials = nullptr;
@@ -550,7 +542,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
       {
         TimeScope ts(h, s, K_ATTN);
-        NS_CUDA(launch_attn(ap, &h->kmaps[l], &h->vmaps[l], h->dtype, d, G, grid, s, true));
+        NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
       }
       h->kernels_last++;
 
@@ -717,6 +709,7 @@ ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out
     return fail(NS_ERR_INVALID_ARG, "model dims");
   if (c.dtype != NS_F16 && c.dtype != NS_BF16) return fail(NS_ERR_INVALID_ARG, "dtype");
   if (c.max_batch > kMaxRows) return fail(NS_ERR_UNSUPPORTED, "max_batch above 4096");
+  if (c.max_blocks_per_seq > 4096) return fail(NS_ERR_UNSUPPORTED, "max_blocks_per_seq above 4096");
   const int H = c.hidden, d = c.head_dim, qd = c.n_q_heads * d, kvd = c.n_kv_heads * d, F = c.ffn;
   const int G = c.n_q_heads / c.n_kv_heads;
   if (H % 128 || qd % 128 || kvd % 128 || (2 * F) % 128 || c.vocab % 128 || F % 64 ||
@@ -847,13 +840,9 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   NS_CUDA(cudaMemset(h->pools, 0, pool * 2 * c.n_layers));
   h->kpool.resize(c.n_layers);
   h->vpool.resize(c.n_layers);
-  h->kmaps.resize(c.n_layers);
-  h->vmaps.resize(c.n_layers);
   for (int l = 0; l < c.n_layers; ++l) {
     h->kpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l));
     h->vpool[l] = static_cast<uint8_t*>(h->pools) + pool * (2 * static_cast<size_t>(l) + 1);
-    NS_TRY(make_pool_tmap(&h->kmaps[l], h->kpool[l], h->dtype, pool_rows, c.head_dim, block_size));
-    NS_TRY(make_pool_tmap(&h->vmaps[l], h->vpool[l], h->dtype, pool_rows, c.head_dim, block_size));
   }
   h->num_blocks = num_blocks;
   h->block_size = block_size;
@@ -863,7 +852,7 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   NS_CUDA(cudaMalloc(&h->attn_counters, rows_heads * sizeof(int)));
   NS_CUDA(cudaMemset(h->attn_counters, 0, rows_heads * sizeof(int)));
   NS_CUDA(cudaMalloc(&h->attn_partials,
-                     rows_heads * h->max_chunks * G * (c.head_dim + 2) * sizeof(float)));
+                     rows_heads * attn_slot_floats(h->max_chunks, G, c.head_dim) * sizeof(float)));
   h->pool.num_blocks = num_blocks;
   h->pool.block_size = block_size;
   h->pool.mb = c.max_blocks_per_seq;
@@ -1070,14 +1059,14 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
     return fail(NS_ERR_INVALID_ARG, "attention arguments");
   const int G = n_q_heads / n_kv_heads;
   if (!attn_supported(head_dim, G, block_size)) return fail(NS_ERR_UNSUPPORTED, "attention shape");
+  if (max_blocks_per_seq * block_size > 65536)
+    return fail(NS_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size above 65536");
   const int max_chunks = attn_max_chunks(max_blocks_per_seq * block_size);
   const size_t rows_heads = static_cast<size_t>(batch) * n_kv_heads;
-  const long long pool_rows = static_cast<long long>(num_blocks) * n_kv_heads * block_size;
-  CUtensorMap kmap, vmap;
-  NS_TRY(make_pool_tmap(&kmap, k_pool, dtype, pool_rows, head_dim, block_size));
-  NS_TRY(make_pool_tmap(&vmap, v_pool, dtype, pool_rows, head_dim, block_size));
+  if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1ll << 31))
+    return fail(NS_ERR_UNSUPPORTED, "num_blocks * n_kv_heads * block_size must fit in int32");
   DevScratch* sc = nullptr;
-  NS_TRY(scratch_get(rows_heads * max_chunks * G * (head_dim + 2) * sizeof(float), rows_heads, &sc));
+  NS_TRY(scratch_get(rows_heads * attn_slot_floats(max_chunks, G, head_dim) * sizeof(float), rows_heads, &sc));
   AttnParams ap{};
   ap.q = q;
   ap.q_row_stride = static_cast<long long>(n_q_heads) * head_dim;
@@ -1102,8 +1091,7 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
   const int cap = attn_max_grid(dtype, head_dim, G, batch, ap.ids_cap);
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid = static_cast<int>(std::min<long long>(cap, units));
-  NS_CUDA(launch_attn(ap, &kmap, &vmap, dtype, head_dim, G, grid,
-                      reinterpret_cast<cudaStream_t>(stream), false));
+  NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));
   return NS_OK;
 }
 

@@ -16,6 +16,7 @@ constexpr int kMaxBN = 256;       // token tile (UMMA N) upper bound
 constexpr int kMaxSplits = 8;     // split-K CTAs per tile = portable cluster size
 constexpr int kAttnChunkBase = 128;  // decode-attention chunk: 128 * ceil(seq_len / 2048) tokens
 constexpr int kAttnMaxChunks = 16;   // so a row never splits into more than 16 chunks
+constexpr int kAttnIdRegs = 8;       // block ids per lane prefetched: chunks of <= 256 blocks
 constexpr int kMaxRows = 4096;
 
 enum EpiMode : int {
@@ -82,7 +83,8 @@ struct AttnParams {
   float scale_log2;        // softmax scale * log2(e)
   int max_chunks;          // partial slots per (row, kv head): attn_max_chunks(mb * block_size)
   int ids_cap;             // blocks of the longest chunk: attn_chunk_tokens(mb * bs) / bs
-  float* partials;         // [rows][n_kv_heads][max_chunks][G][head_dim + 2]
+  float* partials;         // per (row, kv head), attn_slot_floats apart (16-byte aligned):
+                           // [max_chunks][G][head_dim] accumulators, then [max_chunks][G][2] (m, l)
   int* counters;           // [rows][n_kv_heads], zero between launches
   int* err;
 };
@@ -114,8 +116,8 @@ cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const 
 
 bool attn_supported(int head_dim, int group, int block_size);
 int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap);  // one wave
-cudaError_t launch_attn(const AttnParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                        int dtype, int head_dim, int group, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
+                        cudaStream_t s, bool pdl);
 // Chunking of a row of length L (a function of L alone): chunks of 128 * ceil(L / 2048) tokens,
 // so at most 16 chunks per row.  attn_max_chunks bounds the chunk count of any L <= L_max.
 __host__ __device__ inline int attn_chunk_tokens(int L) {
@@ -124,13 +126,15 @@ __host__ __device__ inline int attn_chunk_tokens(int L) {
 __host__ __device__ inline int attn_num_chunks(int L) {
   return L <= 0 ? 0 : (L + attn_chunk_tokens(L) - 1) / attn_chunk_tokens(L);
 }
+// Floats of one (row, kv head) partial slot, rounded up so every slot starts 16-byte aligned.
+__host__ __device__ inline size_t attn_slot_floats(int max_chunks, int group, int head_dim) {
+  return (static_cast<size_t>(max_chunks) * group * (head_dim + 2) + 3) & ~static_cast<size_t>(3);
+}
 __host__ __device__ inline int attn_max_chunks(int L_max) {
   const int c = (L_max + kAttnChunkBase - 1) / kAttnChunkBase;
   return c < kAttnMaxChunks ? c : kAttnMaxChunks;
 }
-// 2-D TMA view [rows][d] of a paged K or V pool, box 64 x block_size (128-byte swizzle).
-ns_status make_pool_tmap(CUtensorMap* m, const void* pool, int dtype, long long rows, int head_dim,
-                         int block_size);
+
 
 // Record the text ns_last_error_message() returns on this thread.
 void set_last_error(const char* msg);

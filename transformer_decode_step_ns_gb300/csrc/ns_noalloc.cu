@@ -80,9 +80,13 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
     set_last_error("ns_attn_decode_noalloc: attention shape not supported");
     return NS_ERR_UNSUPPORTED;
   }
+  if (max_blocks_per_seq * block_size > 65536) {
+    set_last_error("ns_attn_decode_noalloc: max_blocks_per_seq * block_size above 65536");
+    return NS_ERR_UNSUPPORTED;
+  }
   const int max_chunks = attn_max_chunks(max_blocks_per_seq * block_size);
   const size_t rows_heads = static_cast<size_t>(batch) * n_kv_heads;
-  const size_t partial_bytes = rows_heads * max_chunks * G * (head_dim + 2) * sizeof(float);
+  const size_t partial_bytes = rows_heads * attn_slot_floats(max_chunks, G, head_dim) * sizeof(float);
   if (partial_bytes > kNoAllocPartialBytes || rows_heads > kNoAllocCounters) {
     set_last_error(("ns_attn_decode_noalloc: request needs " + std::to_string(partial_bytes) +
                     " bytes of partials and " + std::to_string(rows_heads) +
@@ -91,13 +95,12 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
                     " counters (reduce batch, kv heads or max_blocks_per_seq)").c_str());
     return NS_ERR_INVALID_ARG;
   }
-  CUtensorMap kmap, vmap;
-  const long long pool_rows = static_cast<long long>(num_blocks) * n_kv_heads * block_size;
-  ns_status st = make_pool_tmap(&kmap, k_pool, dtype, pool_rows, head_dim, block_size);
-  if (st == NS_OK) st = make_pool_tmap(&vmap, v_pool, dtype, pool_rows, head_dim, block_size);
-  if (st != NS_OK) return st;
+  if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1ll << 31)) {
+    set_last_error("ns_attn_decode_noalloc: num_blocks * n_kv_heads * block_size must fit in int32");
+    return NS_ERR_UNSUPPORTED;
+  }
   unsigned char* base = nullptr;
-  st = scratch_address(&base);
+  ns_status st = scratch_address(&base);
   if (st != NS_OK) return st;
   int* counters = reinterpret_cast<int*>(base + kNoAllocPartialBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -131,7 +134,7 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid =
       static_cast<int>(std::min<long long>(attn_max_grid(dtype, head_dim, G, batch, ap.ids_cap), units));
-  e = launch_attn(ap, &kmap, &vmap, dtype, head_dim, G, grid, s, false);
+  e = launch_attn(ap, dtype, head_dim, G, grid, s, false);
   if (e != cudaSuccess) {
     set_last_error((std::string("ns_attn_decode_noalloc: launch: ") + cudaGetErrorString(e)).c_str());
     return NS_ERR_CUDA;
