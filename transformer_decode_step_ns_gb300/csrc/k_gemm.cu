@@ -207,20 +207,30 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     griddep_wait();  // outputs may still be read by the previous kernel of the step
     const bool run = !*abort_flag;
     if (run && S > 1) {
+      // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads are
+      // issued before they are summed (in rank order)
       const uint32_t base = smem_u32(tile);
-      for (int jj = 0; jj < n_own; ++jj) {
+      const int fg = et & 31, slot = et >> 5;
+      for (int jj = slot; jj < n_own; jj += 4) {
         const int j = rank + S * jj;
-        const uint32_t off = base + static_cast<uint32_t>((j * kGemmTileN + et) * 4);
-        float v[kMaxSplits];
+        const uint32_t off = base + static_cast<uint32_t>((j * kGemmTileN + 4 * fg) * 4);
+        float4 v[kMaxSplits];
 #pragma unroll
         for (int r = 0; r < kMaxSplits; ++r)
-          v[r] = r < S ? ld_shared_cluster_f32(map_shared_rank(off, r)) : 0.f;
-        float acc = 0.f;
+          if (r < S) v[r] = ld_shared_cluster_f32x4(map_shared_rank(off, r));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int r = 0; r < kMaxSplits; ++r)
-          if (r < S) acc += v[r];
-        tile[j * kGemmTileN + et] = acc;
+        for (int r = 0; r < kMaxSplits; ++r) {
+          if (r < S) {
+            acc.x += v[r].x;
+            acc.y += v[r].y;
+            acc.z += v[r].z;
+            acc.w += v[r].w;
+          }
+        }
+        *reinterpret_cast<float4*>(&tile[j * kGemmTileN + 4 * fg]) = acc;
       }
+      named_barrier_sync(1, 128);
     }
     if (run) {
       const EpiArgs& e = p.e;

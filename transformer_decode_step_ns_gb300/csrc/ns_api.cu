@@ -97,11 +97,12 @@ int pick_bn(int m) {
   return std::max(16, std::min(kMaxBN, bn));
 }
 
-// Split-K from the weight's shape only (never the batch): about two CTAs per SM, at least two
-// k-blocks per split, at most one portable cluster (8 CTAs) per output tile.
+// Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
+// cluster of a launch is resident at once; at least two k-blocks per split; at most one
+// portable cluster (8 CTAs) per output tile.
 void choose_splits(int N, int K, int sms, int* splits, int* kb_per) {
   const int tiles = N / kGemmTileN, nkb = K / kGemmTileK;
-  int s = std::max(1, 2 * sms / std::max(1, tiles));
+  int s = std::max(1, sms / std::max(1, tiles));
   s = std::min(s, std::max(1, nkb / 2));
   s = std::min(s, kMaxSplits);
   *kb_per = (nkb + s - 1) / s;
