@@ -194,8 +194,8 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
  * tokens t < seq_len.  The split depends only on seq_len, so results do not depend on the
  * batch.  num_blocks * n_kv_heads * block_size must be below 2^31 and max_blocks_per_seq *
  * block_size at most 65536.
- * Rows of length L split into chunks of 128 * ceil(L / 2048) tokens (at most 16), merged by
- * log-sum-exp.  Scratch (partials and counters) is allocated by the library on first use per
+ * Rows split into superchunks of at most 1024 tokens (ceil(ceil(L / 16) / 64) of them), merged
+ * by log-sum-exp.  Scratch (partials and counters) is allocated by the library on first use per
  * device and kept until exit.  Slots past seq_len in a row's last block are never used, even
  * if they hold non-finite values.  num_blocks bounds the block ids the kernel accepts.  Supports head_dim
  * 64/128, G <= 8 (G in 1,2,4,7,8), block_size 16.  Not to be called during stream capture
@@ -214,7 +214,7 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
  * where a failed bounds check inside the kernel is recorded.  The split-K scratch (partials and
  * counters) lives in a fixed buffer inside the library image: 32 MiB of partials and 65,536
  * counters, held by every GPU that loads the library until the process exits.  Requests needing
- * more -- batch * n_kv_heads slots of min(16, ceil(max_blocks_per_seq * block_size / 128)) *
+ * more -- batch * n_kv_heads slots of ceil(max_blocks_per_seq / 64) *
  * (n_q_heads / n_kv_heads) * (head_dim + 2) floats each (rounded up to 16 bytes), or
  * batch * n_kv_heads counters -- return
  * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the

@@ -6,25 +6,26 @@
 // replaces about ten ops per layer.  "NanoFlow ..." ("Four resource classes"): decode attention
 // is the memory-bound class, so the kernel is built to stream K/V at HBM speed:
 //
-// * Work unit = (request b, kv head g, chunk).  A row of length L splits into chunks of
-//   128 * ceil(L / 2048) tokens (at most 16 chunks); the chunking is a function of L alone, so a
-//   row's result never depends on the rest of the batch.
-// * Every warp walks its own units (round-robin over all warps of the grid) with a private ring
-//   of stages; each stage holds one 16 x d K tile and one V tile of a cache block, copied with
+// * Work unit = (request b, kv head g, superchunk).  A row's blocks split into superchunks of at
+//   most 64 blocks (1024 tokens); the split is a function of the row's length alone, so a row's
+//   result never depends on the rest of the batch.  A CTA takes a unit; its 4 warps take
+//   contiguous quarters of the superchunk and merge through shared memory.
+// * Every warp streams its blocks (running ahead into its share of the CTA's next unit) through
+//   a private ring of stages; each stage holds one 16 x d K tile and one V tile, copied with
 //   16-byte cp.async by all 32 lanes (each tile is one contiguous run, so every warp request is a
 //   coalesced 512-byte read) into an XOR-swizzled layout that keeps the ldmatrix reads below
 //   bank-conflict free.  Small per-block copies go through the load/store path rather than the
 //   TMA engine, whose per-request cost limits throughput at 2-4 KiB tiles.  The warp refills a
-//   stage as soon as it has consumed it and runs ahead across unit boundaries; q of the next unit
-//   is loaded one unit ahead into registers.
+//   stage as soon as it has consumed it.
 // * The G <= 8 query heads of the group form the rows of one 16-row mma.sync tile:
 //     S^T[head][token]  = q[head][:] . K[token][:]          (A = q in registers, B = K tile)
 //     O^T[dim][head]   += V^T[dim][token] . P^T[token][head] (A = V tile via ldmatrix.trans)
 //   The accumulator layout of the first product is exactly the B-operand layout of the second,
 //   so P never leaves registers.  Each K/V element is read once from shared memory for all G
 //   heads: no expansion.  Online softmax in the log2 domain, per head, in registers.
-// * Chunks of one (b, g) are merged by the last-arriving warp (atomic counter, no spin) in chunk
-//   order with the log-sum-exp rule: deterministic.
+// * The 4 warps' shares are combined in warp order; superchunks of one (b, g) are combined by the
+//   CTA that finishes last (atomic counter, no spin) in superchunk order with the log-sum-exp rule:
+//   deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -108,7 +109,7 @@ __device__ __forceinline__ void set_err(int* err, int code) {
 
 template <int D, int G>
 struct AttnShape {
-  static constexpr int NW = 4;                 // independent warps per CTA
+  static constexpr int NW = 4;                 // warps per CTA; they split one superchunk
   static constexpr int NT = NW * 32;
   static constexpr int BS = 16;                // tokens per cache block
   static constexpr int NH = D / 64;            // 128-byte column halves of a tile
@@ -118,14 +119,15 @@ struct AttnShape {
   static constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
   static constexpr int RING = NST * STAGE;     // bytes per warp
   static constexpr int CPL = 2 * BS * D / 8 / 32;  // 16-byte copies per lane per stage
-  static constexpr int OFF_MRG = NW * RING;    // per warp, [2][8][16] floats of merge scratch
-  static constexpr int OFF_IDS = OFF_MRG + NW * 256 * 4;  // per warp, ids of the producer unit
+  // CTA merge area: per warp acc [G][D] and (m, l) [G]; then merge weights [G][kAttnMaxChunks]
+  static constexpr int OFF_MRG = NW * RING;
+  static constexpr int MRG_FLOATS = NW * G * D + NW * G * 2 + 2 * G * kAttnMaxChunks + 4;  // + flag
+  static constexpr int OFF_IDS = OFF_MRG + ((MRG_FLOATS * 4 + 15) & ~15);  // [NW][16] block ids
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G >= 1 && G <= 8, "group");
-  // then chunk prefix [batch + 1], lengths [batch], scan scratch [NT]
-  static size_t smem_bytes(int batch, int ids_cap) {
-    return 1024 + OFF_IDS + static_cast<size_t>(NW) * ids_cap * 4 +
-           static_cast<size_t>(2 * batch + 1 + NT) * 4;
+  // then superchunk prefix [batch + 1], lengths [batch], scan scratch [NT]
+  static size_t smem_bytes(int batch) {
+    return 1024 + OFF_IDS + NW * kAttnWarpBlocks * 4 + static_cast<size_t>(2 * batch + 1 + NT) * 4;
   }
 };
 
@@ -134,16 +136,18 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
   using S = AttnShape<D, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* merge_all = reinterpret_cast<float*>(smem + S::OFF_MRG);  // [NW][2][8][16]
-  int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);  // [NW][ids_cap]
-  int* pre = ids_all + S::NW * p.ids_cap;                     // chunk prefix over rows [batch + 1]
-  int* lens = pre + p.batch + 1;                              // validated seq_lens [batch]
-  int* tot = lens + p.batch;                                  // per-thread scan scratch [NT]
+  float* m_acc = reinterpret_cast<float*>(smem + S::OFF_MRG);   // [NW][G][D]
+  float* m_ml = m_acc + S::NW * G * D;                           // [NW][G][2]
+  float* m_w = m_ml + S::NW * G * 2;                             // [2][G][kAttnMaxChunks]
+  int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);      // [NW][kAttnWarpBlocks]
+  int* pre = ids_all + S::NW * kAttnWarpBlocks;                  // superchunk prefix [batch + 1]
+  int* lens = pre + p.batch + 1;                                 // validated seq_lens [batch]
+  int* tot = lens + p.batch;                                     // per-thread scan scratch [NT]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads, batch = p.batch;
   uint8_t* ring = smem + warp * S::RING;
-  // Chunk prefix over the rows.  seq_lens are step metadata, final before the step starts, so
-  // under programmatic dependent launch this overlaps the previous kernel.
+  // Superchunk prefix over the rows.  seq_lens are step metadata, final before the step starts,
+  // so under programmatic dependent launch this overlaps the previous kernel.
   {
     const int per = (batch + S::NT - 1) / S::NT;
     const int lo = tid * per, hi = min(batch, lo + per);
@@ -176,10 +180,10 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
   }
   const int total = pre[batch] * Hkv;
   if (tid == 0) griddep_launch_dependents();
-  griddep_wait();  // q and this step's K/V come from the previous kernel
 
+  // A unit is (row b, kv head g, superchunk sc); this warp's share is blocks [w0, w1) of it.
   struct Unit {
-    int b, g, chunk, L, t0, t1, nblk, nchunks;
+    int b, g, sc, L, blk0, nchunks, w0, w1;
   };
   auto decode = [&](int u) {
     Unit x;
@@ -191,61 +195,53 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
       if (pre[mid] <= cg) lo = mid; else hi = mid - 1;
     }
     x.b = lo;
-    x.chunk = cg - pre[lo];
+    x.sc = cg - pre[lo];
     x.L = lens[lo];
-    const int ct = attn_chunk_tokens(x.L);
-    x.t0 = x.chunk * ct;
-    x.t1 = min(x.L, x.t0 + ct);
-    x.nblk = (x.t1 - x.t0 + S::BS - 1) / S::BS;
     x.nchunks = attn_num_chunks(x.L);
+    const int cb = attn_chunk_blocks(x.L);
+    x.blk0 = x.sc * cb;
+    const int nb = min(cb, (x.L + S::BS - 1) / S::BS - x.blk0);
+    x.w0 = x.blk0 + (nb * warp) / S::NW;
+    x.w1 = x.blk0 + (nb * (warp + 1)) / S::NW;
     return x;
   };
 
-  const int gw = blockIdx.x * S::NW + warp, TW = gridDim.x * S::NW;
-
-  // ---- producer cursor (warp-uniform): the warp's stream of (unit, block) in consumption
-  // order.  The block ids of the next unit are loaded into registers (lane j holds ids j,
-  // j + 32, ...) when the producer enters the current one, and stored to shared memory when it
-  // reaches the next, so the stream never waits on a block-table read.  Every stage is one
-  // cp.async group, so "oldest stage landed" is wait_group(NST - 1).
-  int* ids = ids_all + warp * p.ids_cap;
+  // ---- producer cursor (warp-uniform): this warp's stream of blocks over its units, in
+  // consumption order.  The block ids of the next unit are loaded into a register when the
+  // producer enters the current one and stored to shared memory when it gets there, so the
+  // stream never waits on a block-table read.  Every stage is one cp.async group, so "oldest
+  // stage landed" is wait_group(NST - 1).
+  int* ids = ids_all + warp * kAttnWarpBlocks;
   const uint64_t pol = policy_evict_first();  // K/V are streamed once
   const T* kpool = reinterpret_cast<const T*>(p.k_pool);
   const T* vpool = reinterpret_cast<const T*>(p.v_pool);
-  int pu = gw, pi = 0;
+  int pu = blockIdx.x, pi = 0;
   Unit pun{}, nun{};
-  int nid[kAttnIdRegs];
-  auto load_ids = [&](int unit) {  // registers <- block ids of `unit` (non-blocking loads)
+  int nid = 0;
+  auto load_ids = [&](int unit) {  // register <- this warp's block ids of `unit` (non-blocking)
     nun = decode(unit);
-    const int* src = p.block_tables + static_cast<size_t>(p.row0 + nun.b) * p.mb + nun.t0 / S::BS;
-#pragma unroll
-    for (int k = 0; k < kAttnIdRegs; ++k) {
-      const int j = lane + 32 * k;
-      nid[k] = j < nun.nblk ? src[j] : 0;
-    }
+    const int* src = p.block_tables + static_cast<size_t>(p.row0 + nun.b) * p.mb;
+    nid = lane < nun.w1 - nun.w0 ? src[nun.w0 + lane] : 0;
   };
-  auto enter = [&]() {  // the producer starts unit pu; its ids are in the registers
-    __syncwarp();
-    if (pu < total) {
+  auto enter = [&]() {  // the producer moves to unit pu; skip units where this warp has no blocks
+    for (;;) {
+      __syncwarp();
+      if (pu >= total) break;
       pun = nun;
-#pragma unroll
-      for (int k = 0; k < kAttnIdRegs; ++k) {
-        const int j = lane + 32 * k;
-        if (j < pun.nblk) {
-          int blk = nid[k];
-          if (blk < 0 || blk >= p.num_blocks) {
-            set_err(p.err, NS_DEV_BAD_BLOCK);
-            blk = 0;  // keep the pipeline consistent; the error word flags the result
-          }
-          ids[j] = blk;
+      if (lane < pun.w1 - pun.w0) {
+        int blk = nid;
+        if (blk < 0 || blk >= p.num_blocks) {
+          set_err(p.err, NS_DEV_BAD_BLOCK);
+          blk = 0;  // keep the pipeline consistent; the error word flags the result
         }
+        ids[lane] = blk;
       }
-      if (pu + TW < total) load_ids(pu + TW);
+      if (pu + static_cast<int>(gridDim.x) < total) load_ids(pu + gridDim.x);
+      __syncwarp();
+      if (pun.w1 > pun.w0) break;
+      pu += gridDim.x;
     }
-    __syncwarp();
   };
-  if (pu < total) load_ids(pu);
-  enter();
   auto issue = [&](int stage) {  // warp-collective: one cp.async group per call
     if (pu < total) {
       const size_t tile_off = (static_cast<size_t>(ids[pi]) * Hkv + pun.g) * S::BS * D;
@@ -262,251 +258,240 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
         const uint32_t d_off = kv * S::TILE + h * 2048 + t * 128 + ((cc ^ (t & 7)) << 4);
         cp_async_16(dst + d_off, (kv ? vsrc : ksrc) + ci16 * 16, pol);
       }
-      if (++pi >= pun.nblk) {
+      if (++pi >= pun.w1 - pun.w0) {
         pi = 0;
-        pu += TW;
+        pu += gridDim.x;
         enter();
       }
     }
     cp_async_commit();
   };
-  for (int s = 0; s < S::NST; ++s) issue(s);
+  if (pu < total) load_ids(pu);
+  enter();
+  // Blocks without a token of this step may be fetched before the previous kernel (which writes
+  // this step's K/V and q) has finished: only the last block of a row holds this step's token.
+  int s0 = 0;
+  while (s0 < S::NST && pu < total && pun.w0 + pi != (pun.L - 1) / S::BS) issue(s0++);
+  griddep_wait();
+  for (int s = s0; s < S::NST; ++s) issue(s);
 
   const int gq = lane >> 2, tq = lane & 3;
   // ldmatrix lane address: token row and 16-byte chunk offset within the 4 matrices
   const int lm_tok = (lane & 7) + ((lane >> 4) << 3);
   const int lm_chunk = (lane >> 3) & 1;
   T* out = reinterpret_cast<T*>(p.out);
-
-  // q of the group as the A operand (rows = heads, G of 16 used; k = dims), loaded one unit
-  // ahead so the loads overlap the previous unit's blocks.
-  uint32_t qn[S::KS][2];
-  auto load_q = [&](int unit) {
-    if (unit >= total || gq >= G) {
-#pragma unroll
-      for (int ks = 0; ks < S::KS; ++ks) qn[ks][0] = qn[ks][1] = 0u;
-      return;
-    }
-    const Unit x = decode(unit);
-    const T* qrow = reinterpret_cast<const T*>(p.q) + static_cast<size_t>(p.row0 + x.b) * p.q_row_stride +
-                    static_cast<size_t>(x.g * G + gq) * D;
-#pragma unroll
-    for (int ks = 0; ks < S::KS; ++ks) {
-      qn[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq);
-      qn[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq);
-    }
-  };
-  load_q(gw);
+  const int h_e = 2 * tq, h_o = 2 * tq + 1;
 
   int ci = 0;
-  for (int u = gw; u < total; u += TW) {
+  for (int u = blockIdx.x; u < total; u += gridDim.x) {
     const Unit x = decode(u);
     const size_t row = static_cast<size_t>(p.row0 + x.b);
-    uint32_t qa[S::KS][2];
-#pragma unroll
-    for (int ks = 0; ks < S::KS; ++ks) {
-      qa[ks][0] = qn[ks][0];
-      qa[ks][1] = qn[ks][1];
-    }
-    load_q(u + TW);
     float m_run = -INFINITY, l_run = 0.f;
     float acc[S::KS][4];
 #pragma unroll
     for (int mt = 0; mt < S::KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-    for (int i = 0; i < x.nblk; ++i, ++ci) {
-      const int s = ci % S::NST;
-      cp_async_wait_group<S::NST - 1>();  // this lane's copies of the oldest stage landed
-      __syncwarp();                       // ... and every other lane's
-      const uint8_t* kt = ring + s * S::STAGE;
-      const uint8_t* vt = kt + S::TILE;
-      const int n_valid = min(S::BS, x.t1 - (x.t0 + i * S::BS));
-      if (n_valid < S::BS) {
-        // stale slots past seq_len: zero their V rows so 0 * (anything) stays 0
-        uint4* v4 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(vt));
-        for (int c = lane; c < S::BS * S::NH * 8; c += 32) {
-          const int h = c / (S::BS * 8), r = (c / 8) % S::BS;
-          if (r >= n_valid) v4[h * 128 + r * 8 + (c & 7)] = make_uint4(0u, 0u, 0u, 0u);
+    if (x.w1 > x.w0) {
+      // q of the group as the A operand: rows = heads (G of 16 used), k = dims
+      uint32_t qa[S::KS][2];
+      {
+        const T* qrow = reinterpret_cast<const T*>(p.q) + row * p.q_row_stride +
+                        static_cast<size_t>(x.g * G + (gq < G ? gq : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < S::KS; ++ks) {
+          qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq) : 0u;
+          qa[ks][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq) : 0u;
         }
+      }
+      for (int i = x.w0; i < x.w1; ++i, ++ci) {
+        const int s = ci % S::NST;
+        cp_async_wait_group<S::NST - 1>();  // this lane's copies of the oldest stage landed
+        __syncwarp();                       // ... and every other lane's
+        const uint8_t* kt = ring + s * S::STAGE;
+        const uint8_t* vt = kt + S::TILE;
+        const int n_valid = min(S::BS, x.L - i * S::BS);
+        if (n_valid < S::BS) {
+          // stale slots past seq_len: zero their V rows so 0 * (anything) stays 0
+          uint4* v4 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(vt));
+          for (int c = lane; c < S::BS * S::NH * 8; c += 32) {
+            const int h = c / (S::BS * 8), r = (c / 8) % S::BS;
+            if (r >= n_valid) v4[h * 128 + r * 8 + (c & 7)] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+        // ---- S^T = q K^T: two n-tiles of 8 tokens; even / odd k-steps accumulate separately,
+        // which halves the dependent MMA chain
+        float sacc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < S::KS; ++ks) {
+          const int chunk16 = 2 * ks + lm_chunk;           // 16-byte chunk = 8 dims
+          const int h = chunk16 >> 3, cc = chunk16 & 7;
+          const uint32_t addr = kbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
+          uint32_t kb[4];
+          ldsm_x4(addr, kb);
+          const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+          MV<T>::mma(sacc[(ks & 1) * 2 + 0], a, kb[0], kb[1]);
+          MV<T>::mma(sacc[(ks & 1) * 2 + 1], a, kb[2], kb[3]);
+        }
+        // ---- online softmax for head gq over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
+        float sc[4] = {sacc[0][0] + sacc[2][0], sacc[0][1] + sacc[2][1], sacc[1][0] + sacc[3][0],
+                       sacc[1][1] + sacc[3][1]};
+        const int tk[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          sc[k] = tk[k] < n_valid ? sc[k] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sc[k]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        float pr[4], psum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          pr[k] = exp2f(sc[k] - m_new);
+          psum += pr[k];
+        }
+        psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        // ---- O^T += V^T P^T  (P^T in the B-operand layout straight from the S^T accumulator)
+        const uint32_t pb0 = MV<T>::pack(pr[0], pr[1]);
+        const uint32_t pb1 = MV<T>::pack(pr[2], pr[3]);
+        const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * tq);      // head 2tq
+        const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);  // head 2tq + 1
+#pragma unroll
+        for (int mt = 0; mt < S::KS; ++mt) {
+          acc[mt][0] *= a_e;
+          acc[mt][1] *= a_o;
+          acc[mt][2] *= a_e;
+          acc[mt][3] *= a_o;
+          const int chunk16 = 2 * mt + lm_chunk;
+          const int h = chunk16 >> 3, cc = chunk16 & 7;
+          const uint32_t addr = vbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
+          uint32_t va[4];
+          ldsm_x4_t(addr, va);
+          MV<T>::mma(acc[mt], va, pb0, pb1);
+        }
+        // ---- the stage is consumed: refill it with the next block of this warp's stream
         __syncwarp();
+        issue(s);
       }
-      const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-      // ---- S^T = q K^T: two n-tiles of 8 tokens; even / odd k-steps accumulate separately,
-      // which halves the dependent MMA chain
-      float sacc[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < S::KS; ++ks) {
-        const int chunk16 = 2 * ks + lm_chunk;           // 16-byte chunk = 8 dims
-        const int h = chunk16 >> 3, cc = chunk16 & 7;
-        const uint32_t addr = kbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
-        uint32_t kb[4];
-        ldsm_x4(addr, kb);
-        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-        MV<T>::mma(sacc[(ks & 1) * 2 + 0], a, kb[0], kb[1]);
-        MV<T>::mma(sacc[(ks & 1) * 2 + 1], a, kb[2], kb[3]);
-      }
-      // ---- online softmax for head gq over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
-      float sc[4] = {sacc[0][0] + sacc[2][0], sacc[0][1] + sacc[2][1], sacc[1][0] + sacc[3][0],
-                     sacc[1][1] + sacc[3][1]};
-      const int tk[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sc[k] = tk[k] < n_valid ? sc[k] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sc[k]);
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = exp2f(m_run - m_new);
-      float pr[4], psum = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pr[k] = exp2f(sc[k] - m_new);
-        psum += pr[k];
-      }
-      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      // ---- O^T += V^T P^T  (P^T in the B-operand layout straight from the S^T accumulator)
-      const uint32_t pb0 = MV<T>::pack(pr[0], pr[1]);
-      const uint32_t pb1 = MV<T>::pack(pr[2], pr[3]);
-      const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * tq);      // head 2tq
-      const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);  // head 2tq + 1
-#pragma unroll
-      for (int mt = 0; mt < S::KS; ++mt) {
-        acc[mt][0] *= a_e;
-        acc[mt][1] *= a_o;
-        acc[mt][2] *= a_e;
-        acc[mt][3] *= a_o;
-        const int chunk16 = 2 * mt + lm_chunk;
-        const int h = chunk16 >> 3, cc = chunk16 & 7;
-        const uint32_t addr = vbase + h * 2048 + lm_tok * 128 + ((cc ^ (lm_tok & 7)) << 4);
-        uint32_t va[4];
-        ldsm_x4_t(addr, va);
-        MV<T>::mma(acc[mt], va, pb0, pb1);
-      }
-      // ---- the stage is consumed: refill it with the next block of this warp's stream
-      __syncwarp();
-      issue(s);
     }
 
-    // ---- unit result: heads 2tq and 2tq + 1 of this lane's accumulator columns
-    const float l_e = __shfl_sync(0xffffffffu, l_run, 8 * tq);
-    const float l_o = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4);
-    const int h_e = 2 * tq, h_o = 2 * tq + 1;
-    if (x.nchunks == 1) {
-      T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
+    // ---- merge the 4 warps' shares of the superchunk through shared memory, in warp order
+    {
+      float* wacc = m_acc + warp * G * D;
 #pragma unroll
       for (int mt = 0; mt < S::KS; ++mt) {
         const int d0 = mt * 16 + gq;
         if (h_e < G) {
-          orow[h_e * D + d0] = MV<T>::from_f(acc[mt][0] / l_e);
-          orow[h_e * D + d0 + 8] = MV<T>::from_f(acc[mt][2] / l_e);
+          wacc[h_e * D + d0] = acc[mt][0];
+          wacc[h_e * D + d0 + 8] = acc[mt][2];
         }
         if (h_o < G) {
-          orow[h_o * D + d0] = MV<T>::from_f(acc[mt][1] / l_o);
-          orow[h_o * D + d0 + 8] = MV<T>::from_f(acc[mt][3] / l_o);
+          wacc[h_o * D + d0] = acc[mt][1];
+          wacc[h_o * D + d0 + 8] = acc[mt][3];
         }
       }
-    } else {
-      // partial slot of (row, kv head): acc [max_chunks][G][D], then (m, l) [max_chunks][G][2]
-      float* pacc = p.partials + (row * Hkv + x.g) * attn_slot_floats(p.max_chunks, G, D);
-      float* pml = pacc + static_cast<size_t>(p.max_chunks) * G * D;
-      float* part = pacc + static_cast<size_t>(x.chunk) * G * D;
+      if (tq == 0 && gq < G) {
+        m_ml[(warp * G + gq) * 2] = m_run;
+        m_ml[(warp * G + gq) * 2 + 1] = l_run;
+      }
+    }
+    named_barrier_sync(1, S::NT);
+    // combined (m, l) of the superchunk per head, and each warp's weight 2^(m_w - M)
+    float* pacc = p.partials + (row * Hkv + x.g) * attn_slot_floats(p.max_chunks, G, D);
+    float* pml = pacc + static_cast<size_t>(p.max_chunks) * G * D;
+    for (int e = tid; e < G * D; e += S::NT) {
+      const int hh = e / D;
+      float M = -INFINITY;
 #pragma unroll
-      for (int mt = 0; mt < S::KS; ++mt) {
-        const int d0 = mt * 16 + gq;
-        if (h_e < G) {
-          part[h_e * D + d0] = acc[mt][0];
-          part[h_e * D + d0 + 8] = acc[mt][2];
-        }
-        if (h_o < G) {
-          part[h_o * D + d0] = acc[mt][1];
-          part[h_o * D + d0 + 8] = acc[mt][3];
-        }
+      for (int w = 0; w < S::NW; ++w) M = fmaxf(M, m_ml[(w * G + hh) * 2]);
+      float o = 0.f, Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < S::NW; ++w) {
+        const float wt = M == -INFINITY ? 0.f : exp2f(m_ml[(w * G + hh) * 2] - M);
+        o = fmaf(m_acc[(w * G) * D + e], wt, o);
+        Ls = fmaf(m_ml[(w * G + hh) * 2 + 1], wt, Ls);
       }
-      if (tq == 0 && gq < G)
-        reinterpret_cast<float2*>(pml)[x.chunk * G + gq] = make_float2(m_run, l_run);
+      if (x.nchunks == 1) {
+        out[row * p.out_row_stride + static_cast<size_t>(x.g) * G * D + e] = MV<T>::from_f(o / Ls);
+      } else {
+        pacc[static_cast<size_t>(x.sc) * G * D + e] = o;
+        if ((e % D) == 0) reinterpret_cast<float2*>(pml)[x.sc * G + hh] = make_float2(M, Ls);
+      }
+    }
+    if (x.nchunks > 1) {
+      // superchunks of one (row, kv head) are merged by the CTA that finishes last
       __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
+      named_barrier_sync(1, S::NT);
+      int* last_flag = reinterpret_cast<int*>(m_w + 2 * G * kAttnMaxChunks);
+      if (tid == 0) {
         int* cnt = p.counters + row * Hkv + x.g;
-        last = (atomicAdd(cnt, 1) == x.nchunks - 1) ? 1 : 0;
+        const int last = (atomicAdd(cnt, 1) == x.nchunks - 1) ? 1 : 0;
         if (last) *cnt = 0;  // ready for the next launch
+        last_flag[0] = last;
       }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        // Merge the chunks: weight_c = 2^(m_c - M) / sum_c' l_c' 2^(m_c' - M), summed in chunk
-        // order.  One round trip for every (m, l), then one per head for the accumulators.
+      named_barrier_sync(1, S::NT);
+      if (last_flag[0]) {
         __threadfence();
-        float* mw = merge_all + warp * 256;  // [2][8 heads][16 chunks]
-        const int nml = x.nchunks * G;       // <= 128
-        float2 ml[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = lane + 32 * k;
-          ml[k] = i < nml ? __ldcg(reinterpret_cast<const float2*>(pml) + i) : make_float2(0.f, 0.f);
+        // weight_c = 2^(m_c - M) / sum_c' l_c' 2^(m_c' - M), summed in superchunk order
+        float* wm = m_w;                          // [G][kAttnMaxChunks]: m, then the weight
+        float* wl = m_w + G * kAttnMaxChunks;     // [G][kAttnMaxChunks]: l
+        for (int i = tid; i < x.nchunks * G; i += S::NT) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(pml) + i);
+          const int c = i / G, hh = i - c * G;
+          wm[hh * kAttnMaxChunks + c] = v.x;
+          wl[hh * kAttnMaxChunks + c] = v.y;
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = lane + 32 * k;
-          if (i < nml) {
-            const int c = i / G, hh = i - c * G;
-            mw[hh * 16 + c] = ml[k].x;
-            mw[128 + hh * 16 + c] = ml[k].y;
-          }
-        }
-        __syncwarp();
-        if (lane < G) {
+        named_barrier_sync(1, S::NT);
+        if (tid < G) {
           float M = -INFINITY;
-          for (int c = 0; c < x.nchunks; ++c) M = fmaxf(M, mw[lane * 16 + c]);
-          float Lsum = 0.f;
-          for (int c = 0; c < x.nchunks; ++c) Lsum = fmaf(mw[128 + lane * 16 + c], exp2f(mw[lane * 16 + c] - M), Lsum);
-          const float inv = 1.f / Lsum;
-          for (int c = 0; c < x.nchunks; ++c) mw[lane * 16 + c] = exp2f(mw[lane * 16 + c] - M) * inv;
+          for (int c = 0; c < x.nchunks; ++c) M = fmaxf(M, wm[tid * kAttnMaxChunks + c]);
+          float Ls = 0.f;
+          for (int c = 0; c < x.nchunks; ++c)
+            Ls = fmaf(wl[tid * kAttnMaxChunks + c], exp2f(wm[tid * kAttnMaxChunks + c] - M), Ls);
+          const float inv = 1.f / Ls;
+          for (int c = 0; c < x.nchunks; ++c)
+            wm[tid * kAttnMaxChunks + c] = exp2f(wm[tid * kAttnMaxChunks + c] - M) * inv;
         }
-        __syncwarp();
+        named_barrier_sync(1, S::NT);
         T* orow = out + row * p.out_row_stride + static_cast<size_t>(x.g) * G * D;
-        constexpr int VW = D / 32;  // dims per lane: 4 (d = 128) or 2 (d = 64)
-        for (int hh = 0; hh < G; ++hh) {
-          float o[VW];
+        constexpr int NC4 = G * D / 4;
+        for (int col = tid; col < NC4; col += S::NT) {
+          const int hh = col / (D / 4), dq = col - hh * (D / 4);
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cb = 0; cb < x.nchunks; cb += 8) {  // 8 superchunks' loads in flight at a time
+            float4 v[8];
 #pragma unroll
-          for (int e = 0; e < VW; ++e) o[e] = 0.f;
-          for (int cb = 0; cb < x.nchunks; cb += 8) {  // 8 chunks' loads in flight at a time
-            float v[8][VW];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              if (cb + c < x.nchunks) {
-                const float* src = pacc + (static_cast<size_t>(cb + c) * G + hh) * D + VW * lane;
-                if constexpr (VW == 4) {
-                  const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-                  v[c][0] = t.x; v[c][1] = t.y; v[c][2] = t.z; v[c][3] = t.w;
-                } else {
-                  const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-                  v[c][0] = t.x; v[c][1] = t.y;
-                }
-              }
-            }
+            for (int c = 0; c < 8; ++c)
+              if (cb + c < x.nchunks)
+                v[c] = __ldcg(reinterpret_cast<const float4*>(pacc + (static_cast<size_t>(cb + c) * G + hh) * D) + dq);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               if (cb + c < x.nchunks) {
-                const float w = mw[hh * 16 + cb + c];
-#pragma unroll
-                for (int e = 0; e < VW; ++e) o[e] = fmaf(v[c][e], w, o[e]);
+                const float w = wm[hh * kAttnMaxChunks + cb + c];
+                o.x = fmaf(v[c].x, w, o.x);
+                o.y = fmaf(v[c].y, w, o.y);
+                o.z = fmaf(v[c].z, w, o.z);
+                o.w = fmaf(v[c].w, w, o.w);
               }
             }
           }
-#pragma unroll
-          for (int e = 0; e < VW; ++e) orow[hh * D + VW * lane + e] = MV<T>::from_f(o[e]);
+          T* dst = orow + hh * D + 4 * dq;
+          dst[0] = MV<T>::from_f(o.x);
+          dst[1] = MV<T>::from_f(o.y);
+          dst[2] = MV<T>::from_f(o.z);
+          dst[3] = MV<T>::from_f(o.w);
         }
-        __syncwarp();
       }
     }
+    named_barrier_sync(1, S::NT);  // the merge area is reused by the next unit
   }
   cp_async_wait_group<0>();  // every copy this warp issued was consumed; drain regardless
 }
@@ -530,7 +515,7 @@ cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pd
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(S::NT, 1, 1);
-  cfg.dynamicSmemBytes = S::smem_bytes(p.batch, p.ids_cap);
+  cfg.dynamicSmemBytes = S::smem_bytes(p.batch);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -553,7 +538,7 @@ cudaError_t dispatch_g(const AttnParams& p, int group, int grid, cudaStream_t s,
 }
 
 template <typename T, int D, int G>
-int max_grid_t(int batch, int ids_cap) {
+int max_grid_t(int batch) {
   using S = AttnShape<D, G>;
   int dev = 0, sms = 1, per_sm = 0;
   cudaGetDevice(&dev);
@@ -561,20 +546,20 @@ int max_grid_t(int batch, int ids_cap) {
   cudaFuncSetAttribute(attn_decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        227 * 1024);
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<T, D, G>, S::NT,
-                                                    S::smem_bytes(batch, ids_cap)) != cudaSuccess ||
+                                                    S::smem_bytes(batch)) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   return sms * per_sm;
 }
 
 template <typename T, int D>
-int max_grid_g(int group, int batch, int ids_cap) {
+int max_grid_g(int group, int batch) {
   switch (group) {
-    case 1: return max_grid_t<T, D, 1>(batch, ids_cap);
-    case 2: return max_grid_t<T, D, 2>(batch, ids_cap);
-    case 4: return max_grid_t<T, D, 4>(batch, ids_cap);
-    case 7: return max_grid_t<T, D, 7>(batch, ids_cap);
-    default: return max_grid_t<T, D, 8>(batch, ids_cap);
+    case 1: return max_grid_t<T, D, 1>(batch);
+    case 2: return max_grid_t<T, D, 2>(batch);
+    case 4: return max_grid_t<T, D, 4>(batch);
+    case 7: return max_grid_t<T, D, 7>(batch);
+    default: return max_grid_t<T, D, 8>(batch);
   }
 }
 
@@ -586,12 +571,11 @@ bool attn_supported(int head_dim, int group, int block_size) {
   return group == 1 || group == 2 || group == 4 || group == 7 || group == 8;
 }
 
-int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap) {
+int attn_max_grid(int dtype, int head_dim, int group, int batch) {
   if (dtype == NS_BF16)
-    return head_dim == 64 ? max_grid_g<__nv_bfloat16, 64>(group, batch, ids_cap)
-                          : max_grid_g<__nv_bfloat16, 128>(group, batch, ids_cap);
-  return head_dim == 64 ? max_grid_g<__half, 64>(group, batch, ids_cap)
-                        : max_grid_g<__half, 128>(group, batch, ids_cap);
+    return head_dim == 64 ? max_grid_g<__nv_bfloat16, 64>(group, batch)
+                          : max_grid_g<__nv_bfloat16, 128>(group, batch);
+  return head_dim == 64 ? max_grid_g<__half, 64>(group, batch) : max_grid_g<__half, 128>(group, batch);
 }
 
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,

@@ -534,12 +534,10 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.block_size = h->block_size;
       ap.scale_log2 = scale_log2;
       ap.max_chunks = h->max_chunks;
-      ap.ids_cap = attn_chunk_tokens(c.max_blocks_per_seq * h->block_size) / h->block_size;
       ap.partials = h->attn_partials;
       ap.counters = h->attn_counters;
       ap.err = h->err;
-      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second, ap.ids_cap),
-                          nb[i].second * Hkv * h->max_chunks);
+      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
       if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
       {
         TimeScope ts(h, s, K_ATTN);
@@ -1085,11 +1083,10 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
   ap.block_size = block_size;
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.max_chunks = max_chunks;
-  ap.ids_cap = attn_chunk_tokens(max_blocks_per_seq * block_size) / block_size;
   ap.partials = static_cast<float*>(sc->buf);
   ap.counters = sc->counters;
   ap.err = sc->err;
-  const int cap = attn_max_grid(dtype, head_dim, G, batch, ap.ids_cap);
+  const int cap = attn_max_grid(dtype, head_dim, G, batch);
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid = static_cast<int>(std::min<long long>(cap, units));
   NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));

@@ -14,9 +14,9 @@ constexpr int kGemmTileK = 64;    // K per pipeline stage (one 128-byte swizzle 
 constexpr int kGemmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kMaxBN = 256;       // token tile (UMMA N) upper bound
 constexpr int kMaxSplits = 8;     // split-K CTAs per tile = portable cluster size
-constexpr int kAttnChunkBase = 128;  // decode-attention chunk: 128 * ceil(seq_len / 2048) tokens
-constexpr int kAttnMaxChunks = 16;   // so a row never splits into more than 16 chunks
-constexpr int kAttnIdRegs = 8;       // block ids per lane prefetched: chunks of <= 256 blocks
+constexpr int kAttnSuperBlocks = 64;  // decode attention: rows split into superchunks of <= 64 blocks
+constexpr int kAttnMaxChunks = 64;    // superchunks per row (seq_len <= 65536 with 16-token blocks)
+constexpr int kAttnWarpBlocks = 16;   // blocks one warp handles per superchunk (64 / 4 warps)
 constexpr int kMaxRows = 4096;
 
 enum EpiMode : int {
@@ -82,7 +82,6 @@ struct AttnParams {
   int batch, row0, n_kv_heads, num_blocks, block_size;
   float scale_log2;        // softmax scale * log2(e)
   int max_chunks;          // partial slots per (row, kv head): attn_max_chunks(mb * block_size)
-  int ids_cap;             // blocks of the longest chunk: attn_chunk_tokens(mb * bs) / bs
   float* partials;         // per (row, kv head), attn_slot_floats apart (16-byte aligned):
                            // [max_chunks][G][head_dim] accumulators, then [max_chunks][G][2] (m, l)
   int* counters;           // [rows][n_kv_heads], zero between launches
@@ -115,24 +114,26 @@ cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const 
                         int dtype, cudaStream_t s, bool pdl);
 
 bool attn_supported(int head_dim, int group, int block_size);
-int attn_max_grid(int dtype, int head_dim, int group, int batch, int ids_cap);  // one wave
+int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
                         cudaStream_t s, bool pdl);
-// Chunking of a row of length L (a function of L alone): chunks of 128 * ceil(L / 2048) tokens,
-// so at most 16 chunks per row.  attn_max_chunks bounds the chunk count of any L <= L_max.
-__host__ __device__ inline int attn_chunk_tokens(int L) {
-  return kAttnChunkBase * (L > 2048 ? (L + 2047) / 2048 : 1);
-}
+// Split of a row of length L (a function of L alone, 16-token blocks): ceil(L / 16) blocks in
+// ceil(blocks / 64) superchunks of ceil(blocks / superchunks) blocks; a CTA's 4 warps share one
+// superchunk.  attn_max_chunks bounds the superchunk count of any L <= L_max.
 __host__ __device__ inline int attn_num_chunks(int L) {
-  return L <= 0 ? 0 : (L + attn_chunk_tokens(L) - 1) / attn_chunk_tokens(L);
+  return L <= 0 ? 0 : ((L + 15) / 16 + kAttnSuperBlocks - 1) / kAttnSuperBlocks;
+}
+__host__ __device__ inline int attn_chunk_blocks(int L) {
+  const int nb = (L + 15) / 16, n = attn_num_chunks(L);
+  return n == 0 ? 0 : (nb + n - 1) / n;
 }
 // Floats of one (row, kv head) partial slot, rounded up so every slot starts 16-byte aligned.
 __host__ __device__ inline size_t attn_slot_floats(int max_chunks, int group, int head_dim) {
   return (static_cast<size_t>(max_chunks) * group * (head_dim + 2) + 3) & ~static_cast<size_t>(3);
 }
 __host__ __device__ inline int attn_max_chunks(int L_max) {
-  const int c = (L_max + kAttnChunkBase - 1) / kAttnChunkBase;
-  return c < kAttnMaxChunks ? c : kAttnMaxChunks;
+  const int c = attn_num_chunks(L_max);
+  return c < 1 ? 1 : (c < kAttnMaxChunks ? c : kAttnMaxChunks);
 }
 
 

@@ -127,13 +127,12 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
   ap.block_size = block_size;
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.max_chunks = max_chunks;
-  ap.ids_cap = attn_chunk_tokens(max_blocks_per_seq * block_size) / block_size;
   ap.partials = reinterpret_cast<float*>(base);
   ap.counters = counters;
   ap.err = dev_err;
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid =
-      static_cast<int>(std::min<long long>(attn_max_grid(dtype, head_dim, G, batch, ap.ids_cap), units));
+      static_cast<int>(std::min<long long>(attn_max_grid(dtype, head_dim, G, batch), units));
   e = launch_attn(ap, dtype, head_dim, G, grid, s, false);
   if (e != cudaSuccess) {
     set_last_error((std::string("ns_attn_decode_noalloc: launch: ") + cudaGetErrorString(e)).c_str());
