@@ -65,15 +65,17 @@ def load_peaks():
 # ---------------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 50 ms; the report keeps the samples taken inside the window
+    marked by mark_start() / mark_stop() (host wall clock), else the ones nearest to it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self):
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -81,38 +83,66 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50", "-i", str(self._device_index())],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    @staticmethod
+    def _device_index():
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[local].strip() if local < len(ids) else str(local)
+
+    def has_samples(self) -> bool:
+        return self.path is not None and os.path.getsize(self.path) > 0
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        import datetime
+        samples = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+        os.unlink(self.path)
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [x for x in samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        where = "inside the timed region"
+        if not inside:
+            # the region was shorter than the sampling period: the nearest samples either side
+            mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None else samples[-1][0]
+            inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
+            where = "nearest the timed region (shorter than the 50 ms period)"
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for x in inside:
+            for n, v in zip(names, x[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return {"sm_mhz": float(np.median([x[1] for x in inside])),
+                "sm_max_mhz": float(max(x[2] for x in inside)),
+                "samples": len(inside), "where": where, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------------- workload
@@ -242,70 +272,373 @@ def blas_threads():
 
 # ---------------------------------------------------------------------------------- attention
 
-def attention_workload(steps: int, warmup: int, batch: int = 256):
-    """Paged decode attention alone; returns GB/s and per-launch ms."""
-    import torch
-    from transformer_decode_step_ns_gb300 import _lib
-    seed = synth.config_seed(2)
-    n_q, n_kv, d, bs, nb = 32, 8, 128, 16, 160_000
-    ctx = synth.ctx_log_uniform(seed, "cfg2.ctx", batch, 512, 8192)
-    need = [int(math.ceil(c / bs)) for c in ctx]
-    mb = 512
-    perm = synth.permutation(seed, "cfg2.pool", nb)
-    tab = np.zeros((batch, mb), dtype=np.int32)
-    c = 0
-    for b in range(batch):
-        tab[b, : need[b]] = perm[c: c + need[b]]
-        c += need[b]
-    kp = torch.empty((nb, n_kv, bs, d), dtype=torch.bfloat16, device="cuda")
-    vp = torch.empty_like(kp)
-    stream = torch.cuda.current_stream().cuda_stream
-    synth.fill_normal_device(kp.data_ptr(), kp.numel(), seed, "cfg2.k", "bf16", stream=stream)
-    synth.fill_normal_device(vp.data_ptr(), vp.numel(), seed, "cfg2.v", "bf16", stream=stream)
-    q = synth.normal_device(seed, "cfg2.q", (batch, n_q, d), "bf16")
-    out = torch.empty_like(q)
-    dt = torch.from_numpy(tab).cuda()
-    dl = torch.from_numpy(ctx.astype(np.int32)).cuda()
-    scale = 1.0 / math.sqrt(d)
+class AttentionWorkload:
+    """Paged decode attention alone: 32 Q / 8 KV heads, head_dim 128, bf16, block size 16,
+    contexts log-uniform in [512, 8192], block tables drawn from a shuffled pool.
 
-    def launch():
-        _lib.attn_decode(q, kp, vp, dt, dl, out, n_q, n_kv, d, bs, mb, nb, scale, "bf16")
+    Contexts are drawn for `max_batch` rows by index, so batch B uses the first B of them and
+    batch 256 is the same input at any `max_batch`."""
 
-    for _ in range(max(warmup, 3)):
-        launch()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(steps, 10)
-    e0.record()
-    for _ in range(n):
-        launch()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    nbytes = rl.attention_bytes(ctx, n_kv, d, 2)
-    err = _lib.device_error()
-    del kp, vp
-    torch.cuda.empty_cache()
-    return {"workload": "paged GQA decode attention, batch 256, 32Q/8KV, d128, bf16, "
-                        "ctx log-uniform[512,8192], 160k-block pool",
-            "gbs": nbytes / (ms * 1e-3) / 1e9, "ms_per_launch": ms, "bytes_per_launch": nbytes,
-            "launches": n, "device_error": err}
+    n_q, n_kv, d, bs, mb = 32, 8, 128, 16, 512
+
+    def __init__(self, max_batch: int = 512, pool_blocks: int = 160_000):
+        import torch
+        seed = synth.config_seed(2)
+        self.ctx = synth.ctx_log_uniform(seed, "cfg2.ctx", max_batch, 512, 8192)
+        need = [int(math.ceil(c / self.bs)) for c in self.ctx]
+        nb = max(pool_blocks, sum(need) + 1)
+        self.nb = nb
+        perm = synth.permutation(seed, "cfg2.pool", nb)
+        tab = np.zeros((max_batch, self.mb), dtype=np.int32)
+        c = 0
+        for b in range(max_batch):
+            tab[b, : need[b]] = perm[c: c + need[b]]
+            c += need[b]
+        self.kp = torch.empty((nb, self.n_kv, self.bs, self.d), dtype=torch.bfloat16,
+                              device="cuda")
+        self.vp = torch.empty_like(self.kp)
+        stream = torch.cuda.current_stream().cuda_stream
+        synth.fill_normal_device(self.kp.data_ptr(), self.kp.numel(), seed, "cfg2.k", "bf16",
+                                 stream=stream)
+        synth.fill_normal_device(self.vp.data_ptr(), self.vp.numel(), seed, "cfg2.v", "bf16",
+                                 stream=stream)
+        self.q = synth.normal_device(seed, "cfg2.q", (max_batch, self.n_q, self.d), "bf16")
+        self.out = torch.empty_like(self.q)
+        self.tab = torch.from_numpy(tab).cuda()
+        self.lens = torch.from_numpy(self.ctx.astype(np.int32)).cuda()
+        # a buffer larger than L2 (129 MB): writing it between launches evicts the K/V
+        self.flush_buf = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+
+    def launch(self, B):
+        from transformer_decode_step_ns_gb300 import _lib
+        _lib.attn_decode(self.q[:B], self.kp, self.vp, self.tab[:B], self.lens[:B],
+                         self.out[:B], self.n_q, self.n_kv, self.d, self.bs, self.mb, self.nb,
+                         1.0 / math.sqrt(self.d), "bf16")
+
+    def nbytes(self, B):
+        return rl.attention_bytes(self.ctx[:B], self.n_kv, self.d, 2)
+
+    def back_to_back(self, B, n, warmup):
+        """Mean launch time of n launches in a row (only valid when the K/V exceed L2)."""
+        import torch
+        for _ in range(max(warmup, 3)):
+            self.launch(B)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            self.launch(B)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def flushed(self, B, n, warmup):
+        """Mean launch time with L2 flushed before every launch (event pair per launch)."""
+        import torch
+        for _ in range(max(warmup, 3)):
+            self.launch(B)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            self.flush_buf.zero_()
+            a.record()
+            self.launch(B)
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n
+
+    def report(self, B, steps, warmup, hbm):
+        ms = self.back_to_back(B, max(steps, 10), warmup)
+        nbytes = self.nbytes(B)
+        return {"workload": f"paged GQA decode attention, batch {B}, 32Q/8KV, d128, bf16, "
+                            f"ctx log-uniform[512,8192], {self.nb}-block pool",
+                "gbs": nbytes / (ms * 1e-3) / 1e9, "ms_per_launch": ms,
+                "bytes_per_launch": nbytes, "launches": max(steps, 10),
+                "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                "l2": "K/V read per launch larger than L2, launches back to back"}
+
+    def sweep(self, batches, hbm, n=10):
+        rows = []
+        for B in batches:
+            ms = self.flushed(B, n, 3)
+            nbytes = self.nbytes(B)
+            rows.append({"batch": B, "us": round(ms * 1e3, 2), "bytes": nbytes,
+                         "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                         "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)})
+        return rows
+
+
+SWEEP_BATCHES = [1, 2, 4, 8, 16, 32, 64, 128, 256, 512]
+
+
+# ---------------------------------------------------------------------------------- nano-batches
+
+class NanoLayerWorkload:
+    """One LLaMA-2-70B-shaped layer (hidden 8192, 64 Q / 8 KV heads, head_dim 128, SwiGLU 28672,
+    bf16, seeded N(0, 0.02) weights) over a dense batch of 2048 rows: 1024 decode requests with
+    contexts uniform in [256, 2048], then one 1024-token prefill chunk as pseudo-requests
+    (positions 0..1023 over one shared block table, each row attending to its prefix).  The
+    step stops after the layer (no LM head).  Run unsplit and as 2, 3 and 4 nano-batches."""
+
+    VARIANTS = [("1", None, 0), ("2", [1024, 1024], 0), ("2 uneven", [768, 1280], 0),
+                ("3", [640, 640, 768], 0), ("4", [512, 512, 512, 512], 0),
+                ("2, attention budget 76 CTAs", [1024, 1024], 76),
+                ("4, attention budget 76 CTAs", [512, 512, 512, 512], 76)]
+
+    def __init__(self):
+        import dataclasses
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        seed = synth.config_seed(3)
+        # the vocabulary only feeds the embedding gather: tie it so no head is allocated
+        self.shape = dataclasses.replace(synth.llama2_70b_layer_shape(), tie_embeddings=True)
+        sh = self.shape
+        self.bs = bs = 16
+        n_dec, n_pre = 1024, 1024
+        self.B = B = n_dec + n_pre
+        self.w = synth.model_weights_device(sh, seed)
+        ctx_dec = synth.ctx_uniform(seed, "cfg3.ctx", n_dec, 256, 2048).astype(np.int64)
+        pos = np.concatenate([ctx_dec, np.arange(n_pre, dtype=np.int64)])
+        self.mb = mb = int(math.ceil((ctx_dec.max() + 1) / bs))
+        need_dec = [int(math.ceil((c + 1) / bs)) for c in ctx_dec]
+        chunk_blocks = int(math.ceil(n_pre / bs))
+        self.num_blocks = sum(need_dec) + chunk_blocks + 16
+        self.dev = _lib.DecodeStep(sh, self.w, B, mb, use_graphs=True)
+        self.dev.kv_alloc(self.num_blocks, bs)
+        ids = self.dev.reserve(self.num_blocks)
+        self.dev.release(ids[synth.permutation(seed, "cfg3.pool", self.num_blocks)])
+        tab = np.zeros((B, mb), dtype=np.int32)
+        for b in range(n_dec):
+            tab[b, :need_dec[b]] = self.dev.reserve(need_dec[b])
+        tab[n_dec:, :chunk_blocks] = self.dev.reserve(chunk_blocks)[None, :]
+        stream = torch.cuda.current_stream().cuda_stream
+        k, v = self.dev.kv_layer_ptrs(0)
+        n = self.dev.kv_pool_bytes() // 2
+        synth.fill_normal_device(k, n, seed, "cfg3.k0", "bf16", stream=stream)
+        synth.fill_normal_device(v, n, seed, "cfg3.v0", "bf16", stream=stream)
+        torch.cuda.synchronize()
+        blk = tab[np.arange(B), pos // bs].astype(np.int64)
+        self.meta = (synth.uniform_int(seed, "cfg3.tokens", B, 0, sh.vocab - 1).astype(np.int32),
+                     pos.astype(np.int32), tab, (pos + 1).astype(np.int32), blk * bs + pos % bs)
+        self.ctx_dec, self.n_pre = ctx_dec, n_pre
+
+    def work(self):
+        """Algorithmic FLOPs and bytes of the layer step (chunk K/V counted once)."""
+        sh = self.shape
+        h, f, d = sh.hidden, sh.ffn, sh.head_dim
+        qd, kvd = sh.n_q_heads * d, sh.n_kv_heads * d
+        lin = h * qd + 2 * h * kvd + qd * h + 3 * h * f
+        seq = self.meta[3].astype(np.float64)
+        flops = 2.0 * self.B * lin + 4.0 * qd * seq.sum()
+        weights = (lin + 2 * h) * 2
+        kv = (float((self.ctx_dec + 1).sum()) + self.n_pre) * 2 * kvd * 2
+        kv_write = self.B * 2 * kvd * 2
+        return flops, weights + kv + kv_write
+
+    def time_variant(self, sizes, budget, steps, warmup):
+        import torch
+        self.dev.set_nanobatch(sizes, attn_cta_budget=budget)
+        for _ in range(max(warmup, 3)):
+            self.dev.step(*self.meta, None)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            self.dev.step(*self.meta, None)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def serial_kernels(self):
+        """Per-kind kernel time of the unsplit step, launched eagerly with an event pair each."""
+        self.dev.set_nanobatch(None)
+        self.dev.set_kernel_timing(True)
+        self.dev.step(*self.meta, None)
+        self.dev.kernel_timing()
+        for _ in range(3):
+            self.dev.step(*self.meta, None)
+        kt = self.dev.kernel_timing()
+        self.dev.set_kernel_timing(False)
+        return {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]}
+
+    def report(self, steps, warmup, peaks):
+        from transformer_decode_step_ns_gb300 import _lib
+        flops, nbytes = self.work()
+        tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
+        hbm = float(peaks["hbm_gbs"]) * 1e9
+        t_roof = rl.step_roofline_time(flops, nbytes, tflops, hbm)
+        rows = []
+        for label, sizes, budget in self.VARIANTS:
+            ms = self.time_variant(sizes, budget, steps, warmup)
+            rows.append({"split": label, "sizes": sizes or [self.B], "attn_cta_budget": budget,
+                         "us": round(ms * 1e3, 1),
+                         "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                         "frac_of_roofline": round(t_roof / (ms * 1e-3), 4)})
+        serial = self.serial_kernels()
+        return {"workload": "LLaMA-2-70B-shaped layer, bf16, 1024 decode rows (ctx U[256,2048]) "
+                            "+ 1024-token prefill chunk, graph replay, no LM head",
+                "flops": flops, "bytes": nbytes, "roofline_us": round(t_roof * 1e6, 1),
+                "bound": "tensor" if flops / tflops >= nbytes / hbm else "hbm",
+                "variants": rows, "serial_kernel_us": serial,
+                "device_error": _lib.device_error()}
+
+
+# ---------------------------------------------------------------------------------- continuous run
+
+class ContinuousWorkload:
+    """Continuous-batching decode of a 32-layer LLaMA-3-8B-shaped model (hidden 4096, 32 Q / 8
+    KV heads, head_dim 128, SwiGLU 14336, vocab 128256, untied head, bf16, seeded N(0, 0.02)
+    weights) at a constant batch of 256 requests.
+
+    Every request starts with a context uniform in [512, 4096] (its K/V preloaded N(0, 1)) and
+    decodes a length uniform in [100, 1000]; when it finishes it leaves (its blocks return to
+    the pool) and a new request joins in its row.  Each step: join/leave bookkeeping and the
+    host slot mapper, one ns_decode_step (graph replay), greedy argmax on the GPU and the ids
+    read back to the host as the next tokens."""
+
+    B, bs, ctx_lo, ctx_hi, dec_lo, dec_hi = 256, 16, 512, 4096, 100, 1000
+
+    def __init__(self, max_joins: int = 100_000):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        self.seed = seed = synth.config_seed(4)
+        self.shape = sh = synth.llama3_8b_shape(32)
+        B, bs = self.B, self.bs
+        self.mb = mb = int(math.ceil((self.ctx_hi + self.dec_hi + 1) / bs))
+        self.num_blocks = B * mb
+        t0 = time.time()
+        self.w = synth.model_weights_device(sh, seed)
+        self.dev = _lib.DecodeStep(sh, self.w, B, mb, use_graphs=True)
+        self.w = None  # the library holds its own copy
+        torch.cuda.empty_cache()
+        self.dev.kv_alloc(self.num_blocks, bs)
+        ids = self.dev.reserve(self.num_blocks)
+        self.dev.release(ids[synth.permutation(seed, "cfg4.pool", self.num_blocks)])
+        stream = torch.cuda.current_stream().cuda_stream
+        n = self.dev.kv_pool_bytes() // 2
+        for l in range(sh.n_layers):
+            k, v = self.dev.kv_layer_ptrs(l)
+            synth.fill_normal_device(k, n, seed, f"cfg4.k{l}", "bf16", stream=stream)
+            synth.fill_normal_device(v, n, seed, f"cfg4.v{l}", "bf16", stream=stream)
+        torch.cuda.synchronize()
+        # per-join draws, indexed by join number
+        self.j_ctx = synth.ctx_uniform(seed, "cfg4.join.ctx", max_joins, self.ctx_lo, self.ctx_hi)
+        self.j_len = synth.uniform_int(seed, "cfg4.join.len", max_joins, self.dec_lo, self.dec_hi)
+        self.joins = 0
+        self.tables = np.zeros((B, mb), dtype=np.int32)
+        self.pos = np.zeros(B, dtype=np.int32)
+        self.left = np.zeros(B, dtype=np.int64)
+        for b in range(B):
+            self.join(b)
+        self.tokens = synth.uniform_int(seed, "cfg4.tokens", B, 0, sh.vocab - 1).astype(np.int32)
+        self.logits = torch.empty((B, sh.vocab), dtype=torch.float32, device="cuda")
+        self.setup_s = time.time() - t0
+
+    def join(self, b):
+        c = int(self.j_ctx[self.joins])
+        self.left[b] = int(self.j_len[self.joins])
+        self.joins += 1
+        n = int(math.ceil(c / self.bs))
+        self.tables[b] = 0
+        self.tables[b, :n] = self.dev.reserve(n)
+        self.pos[b] = c
+
+    def leave(self, b):
+        n = int(math.ceil(self.pos[b] / self.bs))
+        self.dev.release(self.tables[b, :n].copy())
+
+    def run(self, steps, peaks, nano=None):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        self.dev.set_nanobatch(nano)
+        ids_dev = torch.empty(self.B, dtype=torch.int32, device="cuda")
+        ids_host = torch.empty(self.B, dtype=torch.int32).pin_memory()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        t_roof = 0.0
+        tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
+        hbm = float(peaks["hbm_gbs"]) * 1e9
+        leaves = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            slots = self.dev.prepare_step(self.pos, self.tables)
+            seq = self.pos + 1
+            work = rl.decode_step_work(self.shape, seq)
+            t_roof += rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm)
+            ev[i][0].record()
+            self.dev.step(self.tokens, self.pos, self.tables, seq, slots, self.logits)
+            ev[i][1].record()
+            _lib.greedy_argmax(self.logits, ids_dev)
+            ids_host.copy_(ids_dev, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            self.tokens = ids_host.numpy().copy()
+            self.pos += 1
+            self.left -= 1
+            for b in np.nonzero(self.left == 0)[0]:
+                self.leave(int(b))
+                self.join(int(b))
+                leaves += 1
+        wall = time.perf_counter() - t0
+        dev_ms = np.array([a.elapsed_time(b) for a, b in ev])
+        return {"steps": steps, "nano_split": nano or [self.B], "leaves_and_joins": leaves,
+                "device_ms_per_step_mean": float(dev_ms.mean()),
+                "device_ms_per_step_median": float(np.median(dev_ms)),
+                "tokens_per_s_device": self.B * steps / (dev_ms.sum() * 1e-3),
+                "tokens_per_s_e2e": self.B * steps / wall,
+                "roofline_ms_per_step_mean": t_roof / steps * 1e3,
+                "frac_of_roofline": t_roof / (dev_ms.sum() * 1e-3),
+                "graphs_cached": self.dev.info().graphs_cached,
+                "device_error": self.dev.device_error()}
+
+    def report(self, steps, peaks):
+        # a short comparison of the nano-batch splits, then the full run with the faster one
+        trial = {}
+        for nano in (None, [128, 128]):
+            trial[str(nano or [self.B])] = self.run(20, peaks, nano)["device_ms_per_step_median"]
+        best = None if trial[str([self.B])] <= trial[str([128, 128])] else [128, 128]
+        r = self.run(steps, peaks, best)
+        r["split_trial_ms_per_step"] = trial
+        r["workload"] = ("LLaMA-3-8B-shaped 32L bf16, batch 256, ctx U[512,4096], decode lengths "
+                         "U[100,1000] with leave/join, greedy argmax fed back, graph replay")
+        r["setup_s"] = round(self.setup_s, 1)
+        return r
 
 
 # ---------------------------------------------------------------------------------- main arms
 
+KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_gemm.cu",
+                 "o_proj": "k_gemm.cu", "gate_up": "k_gemm.cu", "down": "k_gemm.cu",
+                 "lm_head": "k_gemm.cu"}
+
+
+def kernel_source_hash(kind):
+    """sha256 (first 16 hex digits) of the kernel's source file and the shared headers."""
+    import hashlib
+    base = kind.split("_cfg")[0]
+    csrc = os.path.join(ROOT, "transformer_decode_step_ns_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCE.get(base, "k_gemm.cu"), "ns_ptx.cuh", "ns_internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(kind):
-    """Per-launch DRAM bytes from the committed ncu summary, when it matches this kernel."""
+    """Per-launch DRAM bytes from the committed ncu summary, when it was taken on this kernel
+    source (else None: the counters are stale)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
     for line in open(p):
         parts = line.split()
-        if len(parts) >= 2 and parts[0] == kind:
+        if len(parts) >= 3 and parts[0] == kind:
             try:
-                return float(parts[1])
+                nbytes = float(parts[1])
             except ValueError:
                 return None
+            return nbytes if parts[2] == kernel_source_hash(kind) else None
     return None
 
 
@@ -324,7 +657,8 @@ def run_ours(args, rank, world):
 
     # warm-up (captures the graph on the first step)
     for _ in range(W):
-        wl.step(wl.next_meta())
+        warm_meta = wl.next_meta()
+        wl.step(warm_meta)
     torch.cuda.synchronize()
     metas = [wl.next_meta() for _ in range(K)]
     if world > 1:
@@ -332,12 +666,20 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     clocks = ClockSampler()
     clocks.start()
+    # keep the GPU busy (untimed replays of the last warm-up step) until sampling is live
+    t_wait = time.time()
+    while not clocks.has_samples() and time.time() - t_wait < 5.0:
+        for _ in range(20):
+            wl.step(warm_meta)
+        torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
     e0.record()
     for m in metas:
         wl.step(m)
     e1.record()
     torch.cuda.synchronize()
+    clocks.mark_stop()
     ms_total = e0.elapsed_time(e1)
     clk = clocks.stop()
     if world > 1:
@@ -402,8 +744,26 @@ def run_ours(args, rank, world):
 
     attn = None
     if not args.skip_attention and rank == 0:
-        attn = attention_workload(max(10, min(K, 50)), W)
-        attn["frac_of_hbm"] = attn["gbs"] / hbm
+        aw = AttentionWorkload(max_batch=max(SWEEP_BATCHES))
+        attn = aw.report(256, max(10, min(K, 50)), W, hbm)
+        attn["sweep_l2_flushed"] = aw.sweep(SWEEP_BATCHES, hbm)
+        attn["device_error"] = _lib.device_error()
+        del aw
+        torch.cuda.empty_cache()
+
+    nano = None
+    if not args.skip_nanobatch and rank == 0:
+        nw = NanoLayerWorkload()
+        nano = nw.report(20, 3, peaks)
+        del nw
+        torch.cuda.empty_cache()
+
+    cont = None
+    if not args.skip_continuous and rank == 0 and args.continuous_steps > 0:
+        cw = ContinuousWorkload()
+        cont = cw.report(args.continuous_steps, peaks)
+        del cw
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -411,11 +771,14 @@ def run_ours(args, rank, world):
         hw, hk, hv = host_copy_of(wl)
         model = oracle.OracleModel.from_weights(wl.shape, hw)
         rows = np.arange(min(args.cpu_rows, wl.B))
-        secs = oracle_sample(model, hk, hv, metas[0], rows, wl.bs)
-        cpu = {"value": len(rows) / secs, "unit": "tokens/s", "cores": blas_threads(),
+        secs, reps = 0.0, 0
+        while reps < 1 or (secs < args.cpu_seconds and reps < 200):
+            secs += oracle_sample(model, hk, hv, metas[reps % len(metas)], rows, wl.bs)
+            reps += 1
+        cpu = {"value": len(rows) * reps / secs, "unit": "tokens/s", "cores": blas_threads(),
                "kind": "oracle",
-               "sample": f"{len(rows)} of the {wl.B} requests through one full step (24 layers + "
-                         f"LM head, fp64 numpy), {secs:.1f} s"}
+               "sample": f"{reps} decode steps of {len(rows)} of the {wl.B} requests (24 layers "
+                         f"+ LM head each, fp64 numpy), {secs:.1f} s of CPU work"}
 
     if rank != 0:
         return
@@ -433,6 +796,8 @@ def run_ours(args, rank, world):
         "roofline": roof,
         "step_roofline": step_roof,
         "attention": attn,
+        "nanobatch_layer": nano,
+        "continuous": cont,
         "cpu_baseline": cpu,
         "clocks": clk,
         "gpu_launches": info.kernels_per_step * K,
@@ -441,6 +806,60 @@ def run_ours(args, rank, world):
         "device_error": dev_err,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_attention_only(args, rank, world):
+    """Paged decode attention alone at one batch size (the attention workload's own line)."""
+    import torch
+    import __graft_entry__ as ge
+    from transformer_decode_step_ns_gb300 import _lib
+    ge.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    B = args.attn_batch
+    aw = AttentionWorkload(max_batch=B, pool_blocks=args.attn_pool_blocks)
+    r = aw.report(B, args.steps, args.warmup, hbm)
+    if rank != 0:
+        return
+    line = {"metric": "paged-attn HBM GB/s", "value": r["gbs"], "unit": "GB/s",
+            "n_gpus": world, "steps": max(args.steps, 10), "warmup": args.warmup,
+            "ms_per_step": r["ms_per_launch"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": r["workload"], "l2": r["l2"]},
+            "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": hbm, "unit": "GB/s",
+                         "frac": r["frac_of_hbm"], "traffic": read_traffic(f"attention_cfg2_b{B}"),
+                         "peak_source": src},
+            "device_error": _lib.device_error()}
+    print(json.dumps(line), flush=True)
+
+
+def run_extra_only(args, rank, world):
+    """One of the extra workloads alone, as its own JSON line (--nanobatch-only,
+    --continuous-only)."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    peaks, src = load_peaks()
+    if args.nanobatch_only:
+        nw = NanoLayerWorkload()
+        r = nw.report(max(args.steps, 1), args.warmup, peaks)
+        best = min(r["variants"], key=lambda v: v["us"])
+        line = {"metric": "70B-layer step time, dense batch 2048 (1024 decode + 1024 prefill)",
+                "value": best["us"], "unit": "us", "higher_is_better": False,
+                "n_gpus": world, "steps": max(args.steps, 1), "warmup": args.warmup,
+                "dtype": "bf16", "data": "synthetic", "config": {"workload": r["workload"]},
+                "nanobatch_layer": r}
+    else:
+        cw = ContinuousWorkload()
+        r = cw.report(args.continuous_steps, peaks)
+        line = {"metric": "decode output tokens/s, continuous batching", "unit": "tokens/s",
+                "value": r["tokens_per_s_device"], "higher_is_better": True,
+                "n_gpus": world, "steps": r["steps"], "warmup": 20, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": r["workload"]}, "continuous": r}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -496,8 +915,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-attention", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-nanobatch", action="store_true")
+    ap.add_argument("--skip-continuous", action="store_true")
+    ap.add_argument("--continuous-steps", type=int, default=2000)
+    ap.add_argument("--nanobatch-only", action="store_true",
+                    help="time the 70B-layer nano-batch workload alone")
+    ap.add_argument("--continuous-only", action="store_true",
+                    help="run the continuous-batching LLaMA-3-8B workload alone")
     ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="minimum CPU time of the oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--attention-only", action="store_true",
+                    help="time the paged attention workload alone at --attn-batch")
+    ap.add_argument("--attn-batch", type=int, default=256)
+    ap.add_argument("--attn-pool-blocks", type=int, default=160_000)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -510,6 +942,10 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.attention_only:
+            run_attention_only(args, rank, world)
+        elif args.nanobatch_only or args.continuous_only:
+            run_extra_only(args, rank, world)
         else:
             run_ours(args, rank, world)
     finally:

@@ -177,7 +177,9 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
  *   must be valid pool ids; the rest are ignored); seq_lens [batch] int32 == positions + 1
  *   (cached tokens including this step's token); slot_mapping [batch] int64, must equal
  *   block_tables[b][p/bs]*bs + p%bs.
- * logits_out: device, [batch][V] fp32, written.  Writes this step's K/V into the pools.
+ * logits_out: device, [batch][V] fp32, written; NULL stops the step after the last layer
+ * (no final norm, no LM head), for callers that only advance the KV cache or time the layers
+ * alone.  Writes this step's K/V into the pools.
  * With use_graphs the first call for a batch size captures a graph (not during a caller's
  * stream capture); later calls replay it.  Returns NOT_INITIALIZED before ns_kv_alloc. */
 ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,

@@ -23,7 +23,8 @@ class Harness:
     """One model on the device and the same model + cache in the oracle."""
 
     def __init__(self, shape, seed, ctx, bs=16, extra_blocks=4, max_batch=None, mb=None,
-                 use_graphs=True, gamma_std=0.1, weights=None, kv_std=1.0):
+                 use_graphs=True, gamma_std=0.1, weights=None, kv_std=1.0,
+                 shared_table_rows=None):
         from transformer_decode_step_ns_gb300 import _lib
         self.shape, self.bs = shape, bs
         self.w = weights if weights is not None else synth.model_weights(shape, seed, gamma_std=gamma_std)
@@ -31,7 +32,8 @@ class Harness:
         self.num_blocks = need + extra_blocks
         mb = mb or max(math.ceil((c + 1) / bs) for c in ctx) + 1
         self.batch = synth.decode_batch(seed, "batch", list(ctx), shape.vocab, bs,
-                                        num_blocks=self.num_blocks, max_blocks_per_seq=mb)
+                                        num_blocks=self.num_blocks, max_blocks_per_seq=mb,
+                                        shared_table_rows=shared_table_rows)
         self.mb = mb
         self.kp = [synth.kv_pool(seed, f"k{l}", self.num_blocks, shape.n_kv_heads, bs,
                                  shape.head_dim, shape.dtype, kv_std) for l in range(shape.n_layers)]
@@ -61,17 +63,20 @@ class Harness:
             vs.append(vv)
         return ks, vs
 
-    def run_gpu(self, rows=None):
+    def run_gpu(self, rows=None, with_logits=True):
         import torch
         b = self.batch
         sl = slice(None) if rows is None else rows
         B = len(b.token_ids[sl])
-        logits = torch.full((B, self.shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
+        logits = None
+        if with_logits:
+            logits = torch.full((B, self.shape.vocab), float("nan"), dtype=torch.float32,
+                                device="cuda")
         self.dev.step(b.token_ids[sl], b.positions[sl], b.block_tables[sl], b.seq_lens[sl],
                       b.slot_mapping[sl], logits)
         torch.cuda.synchronize()
         assert self.dev.device_error() == 0
-        return logits.cpu().numpy().astype(np.float64)
+        return logits.cpu().numpy().astype(np.float64) if with_logits else None
 
     def run_oracle(self):
         b = self.batch
@@ -134,6 +139,17 @@ def test_qwen_shape_two_layers_batch1(cuda_lib):
         abs(ref[0].max() - ref[0][int(np.argmax(got[0]))]) < 5e-2
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(8, 2), (8, 1)])
+def test_head_dim_128_over_several_token_tiles(cuda_lib, n_q, n_kv):
+    """head_dim 128 with 4 and 8 q heads per kv head (the LLaMA shapes), and 300 rows so every
+    projection runs two token tiles (a ragged 160-row tile pair)."""
+    shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=n_q, n_kv_heads=n_kv, head_dim=128,
+                             ffn=768, vocab=640, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
+                             tie_embeddings=False)
+    ctx = list(synth.uniform_int(81, "ctx300", 300, 0, 70))
+    _check_step(Harness(shape, 81 + n_kv, ctx))
+
+
 def test_graph_replay_equals_eager_bitwise(cuda_lib):
     shape = _tiny("bf16")
     a = Harness(shape, 41, [3, 40, 200], use_graphs=True)
@@ -159,6 +175,33 @@ def test_nano_batches_equal_the_whole_batch_bitwise(cuda_lib):
     split3 = Harness(shape, 51, ctx, use_graphs=False)
     split3.dev.set_nanobatch([1, 3, 2], attn_cta_budget=3)
     np.testing.assert_array_equal(split3.run_gpu(), g_whole)
+
+
+def test_prefill_chunk_rows_spanning_nano_batches(cuda_lib):
+    """A prefill chunk as pseudo-requests (positions 0..C-1 over one shared block table) next
+    to decode rows: matches the oracle, and every nano-batch split -- the chunk cut across
+    nano-batches on both streams -- gives the unsplit result bitwise."""
+    shape = _tiny("bf16")
+    dec = [5, 70, 33]
+    C = 40
+    ctx = dec + list(range(C))
+    last = len(ctx) - 1
+    shared = list(range(len(dec))) + [last] * C
+    h = Harness(shape, 71, ctx, shared_table_rows=shared)
+    got, _ = _check_step(h)
+    ks0, vs0 = h.download_pools()
+    for sizes in ([16, 27], [10, 16, 17], [11, 11, 11, 10]):
+        h.upload_pools()
+        h.dev.set_nanobatch(sizes)
+        np.testing.assert_array_equal(h.run_gpu(), got)
+    # without an LM head the step writes the same KV cache bitwise
+    h.upload_pools()
+    h.dev.set_nanobatch([16, 27])
+    h.run_gpu(with_logits=False)
+    ks, vs = h.download_pools()
+    for l in range(shape.n_layers):
+        np.testing.assert_array_equal(ks[l], ks0[l])
+        np.testing.assert_array_equal(vs[l], vs0[l])
 
 
 def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):

@@ -280,7 +280,8 @@ class DecodeStep:
 
     def step(self, token_ids, positions, block_tables, seq_lens, slot_mapping, logits,
              stream=None) -> None:
-        """One decode step; host metadata arrays, ``logits`` a device fp32 [B, V] buffer."""
+        """One decode step; host metadata arrays, ``logits`` a device fp32 [B, V] buffer
+        (None: stop after the last layer, no LM head)."""
         tok = np.ascontiguousarray(token_ids, dtype=np.int32)
         pos = np.ascontiguousarray(positions, dtype=np.int32)
         tab = np.ascontiguousarray(block_tables, dtype=np.int32)

@@ -269,9 +269,12 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
   if (pu < total) load_ids(pu);
   enter();
   // Blocks without a token of this step may be fetched before the previous kernel (which writes
-  // this step's K/V and q) has finished: only the last block of a row holds this step's token.
+  // this step's K/V and q) has finished.  In a decode-only batch only the last block of a row
+  // holds this step's token; rows of a prefill chunk read blocks other rows write now, and the
+  // host then clears early_ok.
+  const bool early = p.early_ok == nullptr || *p.early_ok != 0;
   int s0 = 0;
-  while (s0 < S::NST && pu < total && pun.w0 + pi != (pun.L - 1) / S::BS) issue(s0++);
+  while (early && s0 < S::NST && pu < total && pun.w0 + pi != (pun.L - 1) / S::BS) issue(s0++);
   griddep_wait();
   for (int s = s0; s < S::NST; ++s) issue(s);
 

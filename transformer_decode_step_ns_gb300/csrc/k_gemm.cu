@@ -78,10 +78,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tile_n = blockIdx.x;
+  // Token tiles vary fastest in launch order, so the CTAs that share a weight tile run
+  // together and all but the first read it from L2.
+  const int tile_m = blockIdx.x;
   const int split = blockIdx.y;
-  const int tile_m = blockIdx.z;
-  const int tile_id = tile_m * gridDim.x + tile_n;
+  const int tile_n = blockIdx.z;
   const int n0 = tile_n * kGemmTileN;
   const int nkb_total = p.K / kGemmTileK;
   const int kb0 = split * p.kb_per_split;
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && nkb > 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // a weight tile read by one CTA only is streamed; one shared by several token tiles stays
+      const uint64_t pol_w = gridDim.x > 1 ? policy_evict_normal() : policy_evict_first();
       const int pre = min(p.nstage, nkb);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], stage_bytes);
@@ -403,7 +405,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* mapA, const CUtensorMap* mapB, cons
     configured_mask |= 1 << dev;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.N / kGemmTileN, p.splits, (p.M + p.BN - 1) / p.BN);
+  cfg.gridDim = dim3((p.M + p.BN - 1) / p.BN, p.splits, p.N / kGemmTileN);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -305,6 +305,8 @@ struct ns_ctx {
   int n_split = 1;
   std::vector<int> split_sizes;
   int attn_budget = 0;
+  bool with_lm = true;  // false: the step stops after the last layer (logits_out == NULL)
+  std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
   cudaStream_t side = nullptr, cap = nullptr;
   std::vector<cudaEvent_t> events;
   // graphs
@@ -325,7 +327,7 @@ struct ns_ctx {
 namespace {
 
 struct MetaLayout {
-  size_t tok, pos, seq, slot, tab, logits, total;
+  size_t tok, pos, seq, slot, tab, logits, flags, total;
 };
 
 MetaLayout meta_layout(int B, int MB) {
@@ -338,7 +340,8 @@ MetaLayout meta_layout(int B, int MB) {
   m.slot = o; o += static_cast<size_t>(B) * 8;
   m.tab = o; o += static_cast<size_t>(B) * MB * 4;
   o = (o + 15) & ~size_t(15);
-  m.logits = o; o += 16;
+  m.logits = o; o += 8;
+  m.flags = o; o += 8;  // int early_ok (see AttnParams), 4 bytes of padding
   m.total = o;
   return m;
 }
@@ -537,6 +540,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.partials = h->attn_partials;
       ap.counters = h->attn_counters;
       ap.err = h->err;
+      ap.early_ok = reinterpret_cast<const int*>(h->meta_dev + ml.flags);
       int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
       if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
       {
@@ -569,7 +573,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN));
     }
   }
-  for (int i = 0; i < n; ++i) {
+  for (int i = 0; i < n && h->with_lm; ++i) {
     EpiArgs el = norm;
     el.out_ptr_slot = m_logits;
     el.ldo = c.vocab;
@@ -583,8 +587,31 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   return NS_OK;
 }
 
+// True when no row reads, at a block other than its last, a block that this step writes (the
+// block of some row's slot).  Decode-only batches satisfy it; rows of a prefill chunk sharing
+// one block table do not.  The metadata has passed check_meta.
+bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int32_t* seq_lens,
+                    const int64_t* slot_mapping) {
+  const int bs = h->block_size, mb = h->cfg.max_blocks_per_seq;
+  std::vector<uint8_t>& dirty = h->dirty_blocks;
+  if (dirty.size() != static_cast<size_t>(h->num_blocks)) dirty.assign(h->num_blocks, 0);
+  for (int b = 0; b < batch; ++b) dirty[slot_mapping[b] / bs] = 1;
+  bool ok = true;
+  for (int b = 0; b < batch && ok; ++b) {
+    const int nbk = (seq_lens[b] + bs - 1) / bs;
+    const int32_t* row = block_tables + static_cast<size_t>(b) * mb;
+    for (int j = 0; j + 1 < nbk; ++j)
+      if (dirty[row[j]]) {
+        ok = false;
+        break;
+      }
+  }
+  for (int b = 0; b < batch; ++b) dirty[slot_mapping[b] / bs] = 0;
+  return ok;
+}
+
 std::vector<int> graph_key(const ns_ctx* h, int B) {
-  std::vector<int> k{B, h->n_split, h->attn_budget};
+  std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0};
   for (int v : h->split_sizes) k.push_back(v);
   return k;
 }
@@ -712,7 +739,7 @@ ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out
   const int H = c.hidden, d = c.head_dim, qd = c.n_q_heads * d, kvd = c.n_kv_heads * d, F = c.ffn;
   const int G = c.n_q_heads / c.n_kv_heads;
   if (H % 128 || qd % 128 || kvd % 128 || (2 * F) % 128 || c.vocab % 128 || F % 64 ||
-      !attn_supported(d, G, 16))
+      !attn_supported(d, G, 16) || c.vocab / kGemmTileN > 65535 || (2 * F) / kGemmTileN > 65535)
     return fail(NS_ERR_UNSUPPORTED, "shape not implemented (see ns.h)");
   if (w->embed == nullptr || w->final_norm == nullptr || w->layers == nullptr ||
       (!c.tie_embeddings && w->lm_head == nullptr))
@@ -963,7 +990,6 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
   if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
   const ns_model_cfg& c = h->cfg;
-  if (logits_out == nullptr) return fail(NS_ERR_INVALID_ARG, "null logits_out");
   const int bs = h->block_size, mb = c.max_blocks_per_seq;
   NS_TRY(check_meta(h->num_blocks, bs, mb, c.vocab, c.max_batch, batch, token_ids, positions,
                     block_tables, seq_lens, slot_mapping));
@@ -985,9 +1011,13 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   std::memcpy(mh + ml.tab, block_tables, static_cast<size_t>(batch) * mb * 4);
   const unsigned long long lp = reinterpret_cast<unsigned long long>(logits_out);
   std::memcpy(mh + ml.logits, &lp, 8);
+  const int early_ok = early_fetch_ok(h, batch, block_tables, seq_lens, slot_mapping) ? 1 : 0;
+  std::memset(mh + ml.flags, 0, 8);
+  std::memcpy(mh + ml.flags, &early_ok, 4);
   NS_CUDA(cudaMemcpyAsync(h->meta_dev, mh, ml.total, cudaMemcpyHostToDevice, s));
   NS_CUDA(cudaEventRecord(h->meta_done, s));
   h->meta_pending = true;
+  h->with_lm = logits_out != nullptr;
   if (c.use_graphs && !h->timing) {
     cudaGraphExec_t ex = nullptr;
     NS_TRY(get_graph(h, batch, &ex));
@@ -1098,6 +1128,7 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   if (m < 1 || m > kMaxRows || n < 128 || k < 64 || (dtype != NS_F16 && dtype != NS_BF16))
     return fail(NS_ERR_INVALID_ARG, "linear arguments");
   if (n % 128 || k % 64) return fail(NS_ERR_UNSUPPORTED, "n % 128 and k % 64 must be 0");
+  if (n / kGemmTileN > 65535) return fail(NS_ERR_UNSUPPORTED, "n above 65535 * 128");
   Proj pr;
   pr.w = const_cast<void*>(w);
   pr.owned = false;

@@ -86,6 +86,10 @@ struct AttnParams {
                            // [max_chunks][G][head_dim] accumulators, then [max_chunks][G][2] (m, l)
   int* counters;           // [rows][n_kv_heads], zero between launches
   int* err;
+  // Device word, read before the dependency wait: nonzero when no block a row reads, other than
+  // its last, receives a token in this step, so those blocks may be fetched while the previous
+  // kernel (which writes this step's K/V) still runs.  nullptr = always (K/V are inputs).
+  const int* early_ok;
 };
 
 struct EmbedParams {
