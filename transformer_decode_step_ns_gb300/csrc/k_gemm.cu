@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "ns_internal.h"
 #include "ns_ptx.cuh"
 
@@ -46,6 +48,7 @@ struct Cvt<__nv_bfloat16> {
 
 constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
 constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
+constexpr int kPf = 4;  // epilogue iterations per thread whose inputs are loaded early
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -114,6 +117,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const int S = p.splits;
+  const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;  // owned tokens
+  // epilogue prefetch registers (first kPf iterations of each epilogue thread)
+  float pf_a[kPf] = {}, pf_b[kPf] = {};
+  long long pf_s[kPf] = {};
   const uint32_t tmem = *tmem_slot;
   // Dependents may be scheduled once every CTA holds its TMEM (so none of them can starve us).
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -170,7 +179,82 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ epilogue stage 1
+    // ------------------------------------------------------------------ epilogue warps
+    // Everything the epilogue reads besides the accumulator is loaded while the main loop
+    // runs: the RMSNorm scale of each owned token, and (for the first kPf iterations of each
+    // thread) the RoPE cos/sin and cache slots or the residual values.  Loads are issued
+    // before any of their results is used, so they cost one memory round trip.
+    const EpiArgs& e = p.e;
+    const int et = threadIdx.x - 64;  // 0..127
+    const int ew = warp - 2;
+    const bool qk_cols = n0 < e.q_dim + e.kv_dim;
+    // inputs fixed before the step starts (metadata, weights)
+    if (p.epi == EPI_QKV) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int idx = et + 128 * u;
+        if (qk_cols) {
+          if (idx < n_own * 64 && n0 >= e.q_dim) pf_s[u] = e.slot_mapping[tok0 + rank + S * (idx >> 6)];
+        } else if (idx < n_own * kGemmTileN) {
+          pf_s[u] = e.slot_mapping[tok0 + rank + S * (idx >> 7)];
+        }
+      }
+    } else if (p.epi == EPI_RESID) {
+      pf_b[0] = e.gamma_next[n0 + et];
+    }
+    griddep_wait();  // the previous kernel wrote the rest and may still read our outputs
+    if (p.epi == EPI_QKV && qk_cols) {
+      const int half = e.head_dim >> 1;
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int idx = et + 128 * u;
+        if (idx < n_own * 64) {
+          const size_t o = static_cast<size_t>(tok0 + rank + S * (idx >> 6)) * half + (idx & 63) % half;
+          pf_a[u] = e.rope_cos[o];
+          pf_b[u] = e.rope_sin[o];
+        }
+      }
+    } else if (p.epi == EPI_RESID) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int idx = et + 128 * u;
+        if (idx < n_own * kGemmTileN)
+          pf_a[u] = e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et];
+      }
+    }
+    if (e.sumsq_in != nullptr) {
+      // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps): one warp per token,
+      // lanes over the partials, a fixed shuffle tree (the order depends on H only)
+      const int n_tiles = e.sumsq_tiles;
+      const size_t ld = static_cast<size_t>(e.sumsq_ld);
+      for (int jj0 = ew; jj0 < n_own; jj0 += 16) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int jj = jj0 + 4 * u;
+          const float* sp = e.sumsq_in + tok0 + rank + S * jj;
+          v[u] = 0.f;
+          if (jj < n_own) {
+            if (n_tiles <= 64) {
+              const float x0 = lane < n_tiles ? sp[lane * ld] : 0.f;
+              const float x1 = lane + 32 < n_tiles ? sp[(lane + 32) * ld] : 0.f;
+              v[u] = x0 + x1;
+            } else {
+              for (int t = lane; t < n_tiles; t += 32) v[u] += sp[t * ld];
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float x = v[u];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          const int jj = jj0 + 4 * u;
+          if (lane == 0 && jj < n_own)
+            rs_s[rank + S * jj] = rsqrtf(x / static_cast<float>(e.norm_dim) + e.eps);
+        }
+      }
+    }
     // TMEM -> shared tile [BN][128] fp32 (reuses the stage ring: every MMA has completed)
     const int q = warp & 3;             // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;      // output feature within the tile
@@ -197,16 +281,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   // The split CTAs of one output tile form a thread-block cluster.  CTA `rank` owns tokens
   // j = rank, rank + S, ...; it sums their partial rows over every CTA of the cluster through
   // distributed shared memory, in rank order (deterministic), then runs the epilogue for them.
+  // Two cluster barrier phases: "every tile is complete" before the reduction, and "every
+  // peer has finished reading" before a CTA leaves; the second is arrived at as soon as a
+  // thread is done with remote reads and waited for only at the end.
   __syncthreads();
-  const int S = p.splits;
-  const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  if (S > 1) cluster_sync();
-  const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;
+  if (S > 1) {
+    cluster_sync();
+    if (warp < 2) cluster_arrive();  // these warps read no peer memory
+  }
   float* tile = reinterpret_cast<float*>(smem);
   if (warp >= 2) {
     const int et = threadIdx.x - 64;  // 0..127: feature within the tile
     const int ew = warp - 2;
-    griddep_wait();  // outputs may still be read by the previous kernel of the step
     const bool run = !*abort_flag;
     if (run && S > 1) {
       // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads are
@@ -232,20 +318,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
         *reinterpret_cast<float4*>(&tile[j * kGemmTileN + 4 * fg]) = acc;
       }
-      named_barrier_sync(1, 128);
     }
+    named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
+    if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
     if (run) {
       const EpiArgs& e = p.e;
       const bool scaled = e.sumsq_in != nullptr;
-      if (scaled) {
-        for (int jj = et; jj < n_own; jj += 128) {
-          const int j = rank + S * jj;
-          float ss = 0.f;
-          for (int t = 0; t < e.sumsq_tiles; ++t) ss += e.sumsq_in[static_cast<size_t>(t) * e.sumsq_ld + tok0 + j];
-          rs_s[j] = rsqrtf(ss / static_cast<float>(e.norm_dim) + e.eps);
-        }
-      }
-      named_barrier_sync(1, 128);
       if (p.epi == EPI_F32) {
         float* out = e.out_f32;
         if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
@@ -260,8 +338,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         T* qo = reinterpret_cast<T*>(e.q_out);
         T* kp = reinterpret_cast<T*>(e.k_pool);
         T* vp = reinterpret_cast<T*>(e.v_pool);
+        auto kv_base = [&](long long slot, int kvh) {
+          return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                  static_cast<size_t>(slot % e.block_size)) * d;
+        };
         if (n0 < e.q_dim + e.kv_dim) {
-          for (int idx = et; idx < n_own * 64; idx += 128) {
+          // q and k columns: RoPE pairs (i, i + d/2) of each head
+          auto qk = [&](int idx, float c, float sn, long long slot) {
             const int j = rank + S * (idx >> 6), pr = idx & 63;
             const int hl = pr / half, i = pr - hl * half;
             const int r_lo = hl * d + i, r_hi = r_lo + half;
@@ -269,8 +352,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             const float sc = scaled ? rs_s[j] : 1.f;
             const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
             const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
-            const float c = e.rope_cos[static_cast<size_t>(tok) * half + i];
-            const float sn = e.rope_sin[static_cast<size_t>(tok) * half + i];
             const float y_lo = x_lo * c - x_hi * sn;
             const float y_hi = x_hi * c + x_lo * sn;
             if (n0 < e.q_dim) {
@@ -278,49 +359,67 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
               dst[r_lo] = Cvt<T>::from_f(y_lo);
               dst[r_hi] = Cvt<T>::from_f(y_hi);
             } else {
-              const int col = n0 - e.q_dim + r_lo;
-              const int kvh = col / d;
-              const long long slot = e.slot_mapping[tok];
               if (slot < 0 || slot >= e.pool_slots) {
                 set_err(p.err, NS_DEV_BAD_SLOT);
-                continue;
+                return;
               }
-              const size_t base =
-                  ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
-                   static_cast<size_t>(slot % e.block_size)) * d;
+              const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
               kp[base + i] = Cvt<T>::from_f(y_lo);
               kp[base + i + half] = Cvt<T>::from_f(y_hi);
             }
+          };
+#pragma unroll
+          for (int u = 0; u < kPf; ++u) {
+            const int idx = et + 128 * u;
+            if (idx < n_own * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
+          }
+          for (int idx = et + 128 * kPf; idx < n_own * 64; idx += 128) {
+            const int j = rank + S * (idx >> 6), i = (idx & 63) % half;
+            const int tok = tok0 + j;
+            qk(idx, e.rope_cos[static_cast<size_t>(tok) * half + i],
+               e.rope_sin[static_cast<size_t>(tok) * half + i],
+               n0 >= e.q_dim ? e.slot_mapping[tok] : 0);
           }
         } else {
-          for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
+          // v columns
+          auto vv = [&](int idx, long long slot) {
             const int j = rank + S * (idx >> 7), r = idx & 127;
-            const int tok = tok0 + j;
             const int col = n0 - e.q_dim - e.kv_dim + r;
             const int kvh = col / d, dim = col - kvh * d;
-            const long long slot = e.slot_mapping[tok];
             if (slot < 0 || slot >= e.pool_slots) {
               set_err(p.err, NS_DEV_BAD_SLOT);
-              continue;
+              return;
             }
             const float v = tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f);
-            const size_t base =
-                ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
-                 static_cast<size_t>(slot % e.block_size)) * d;
-            vp[base + dim] = Cvt<T>::from_f(v);
+            vp[kv_base(slot, kvh) + dim] = Cvt<T>::from_f(v);
+          };
+#pragma unroll
+          for (int u = 0; u < kPf; ++u) {
+            const int idx = et + 128 * u;
+            if (idx < n_own * kGemmTileN) vv(idx, pf_s[u]);
           }
+          for (int idx = et + 128 * kPf; idx < n_own * kGemmTileN; idx += 128)
+            vv(idx, e.slot_mapping[tok0 + rank + S * (idx >> 7)]);
         }
         fence_proxy_async_global();
       } else if (p.epi == EPI_RESID) {
         T* xo = reinterpret_cast<T*>(e.xn_out);
-        for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
+        const float gam = pf_b[0];
+        auto rs_row = [&](int idx, float old) {
           const int j = rank + S * (idx >> 7), r = idx & 127;
           const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
-          const float rn = e.resid[gi] + tile[j * kGemmTileN + r];
+          const float rn = old + tile[j * kGemmTileN + r];
           e.resid[gi] = rn;
-          xo[gi] = Cvt<T>::from_f(rn * e.gamma_next[n0 + r]);
+          xo[gi] = Cvt<T>::from_f(rn * gam);
           tile[j * kGemmTileN + r] = rn * rn;
+        };
+#pragma unroll
+        for (int u = 0; u < kPf; ++u) {
+          const int idx = et + 128 * u;
+          if (idx < n_own * kGemmTileN) rs_row(idx, pf_a[u]);
         }
+        for (int idx = et + 128 * kPf; idx < n_own * kGemmTileN; idx += 128)
+          rs_row(idx, e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et]);
         named_barrier_sync(1, 128);
         for (int jj = ew; jj < n_own; jj += 4) {
           const int j = rank + S * jj;
@@ -346,10 +445,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       }
     }
   }
-  // no CTA of the cluster may exit while another still reads its tile
-  if (S > 1) cluster_sync();
 
   // ------------------------------------------------------------------ teardown
+  // no CTA of the cluster may leave while a peer still reads its tile
+  if (S > 1) cluster_wait();
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
     // Let this CTA's own copies in flight land before its shared memory is released.
@@ -372,14 +471,23 @@ size_t gemm_smem_bytes(int BN, int nstage) {
          kCtrlBytes;
 }
 
-int gemm_pick_stages(int BN) {
-  if (BN <= 64) return 4;  // <= 97 KiB: two CTAs per SM, one's epilogue overlaps the other's loads
-  const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
+int gemm_pick_stages(int BN, int kb_per_split) {
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
+  // the epilogue tile [BN][128] fp32 reuses the stage ring
+  const int tile_min = static_cast<int>((static_cast<size_t>(BN) * kGemmTileN * 4 + stage - 1) / stage);
+  if (BN <= 64) {
+    // Decode batches: enough stages to prefetch the whole k-range of the CTA where it fits in
+    // half an SM's shared memory, so the next kernel's CTAs can be resident (and stream their
+    // own weights) while this one runs.
+    const size_t half_sm = 113 * 1024 - 1024 - kCtrlBytes;
+    int n = static_cast<int>(half_sm / stage);
+    n = std::min(n, std::max(kb_per_split, 2));
+    return std::max(n, std::max(tile_min, 2));
+  }
+  const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
   int n = static_cast<int>(budget / stage);
   if (n > 8) n = 8;
-  if (n < 4) n = 4;  // the epilogue tile reuses at least 4 stages ([BN][128] fp32)
-  return n;
+  return std::max(n, std::max(tile_min, 4));
 }
 
 uint32_t gemm_idesc(int dtype, int BN) {

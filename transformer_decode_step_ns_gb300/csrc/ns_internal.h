@@ -112,7 +112,7 @@ struct EmbedParams {
 
 // Kernel launchers (return the launch error; `pdl` adds programmatic stream serialisation).
 size_t gemm_smem_bytes(int BN, int nstage);
-int gemm_pick_stages(int BN);
+int gemm_pick_stages(int BN, int kb_per_split);
 uint32_t gemm_idesc(int dtype, int BN);
 cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                         int dtype, cudaStream_t s, bool pdl);
