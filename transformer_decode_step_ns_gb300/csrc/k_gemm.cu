@@ -48,7 +48,7 @@ struct Cvt<__nv_bfloat16> {
 
 constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
 constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
-constexpr int kPf = 4;  // epilogue iterations per thread whose inputs are loaded early
+constexpr int kPf = 8;  // epilogue iterations per thread whose inputs are loaded early
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           for (int idx = et + 128 * kPf; idx < n_own * kGemmTileN; idx += 128)
             vv(idx, e.slot_mapping[tok0 + rank + S * (idx >> 7)]);
         }
-        fence_proxy_async_global();
+        // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
       } else if (p.epi == EPI_RESID) {
         T* xo = reinterpret_cast<T*>(e.xn_out);
         const float gam = pf_b[0];
