@@ -600,6 +600,15 @@ class ContinuousWorkload:
         best = None if trial[str([self.B])] <= trial[str([128, 128])] else [128, 128]
         r = self.run(steps, peaks, best)
         r["split_trial_ms_per_step"] = trial
+        # per-kind kernel time of eager steps (an event pair around each launch)
+        self.dev.set_kernel_timing(True)
+        self.run(2, peaks, best)
+        self.dev.kernel_timing()
+        self.run(3, peaks, best)
+        kt = self.dev.kernel_timing()
+        self.dev.set_kernel_timing(False)
+        r["eager_kernel_us"] = {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]}
+        r["eager_kernel_launches_per_step"] = {k: v[0] // 3 for k, v in kt.items() if v[0]}
         r["workload"] = ("LLaMA-3-8B-shaped 32L bf16, batch 256, ctx U[512,4096], decode lengths "
                          "U[100,1000] with leave/join, greedy argmax fed back, graph replay")
         r["setup_s"] = round(self.setup_s, 1)

@@ -115,7 +115,8 @@ struct AttnShape {
   static constexpr int NH = D / 64;            // 128-byte column halves of a tile
   static constexpr int TILE = BS * D * 2;      // bytes of one K or V tile
   static constexpr int STAGE = 2 * TILE;
-  static constexpr int NST = (D == 128) ? 3 : 6;
+  // stages per warp: G = 8 keeps the ring at two stages so two CTAs fit on an SM
+  static constexpr int NST = (D == 128) ? (G == 8 ? 2 : 3) : 6;
   static constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
   static constexpr int RING = NST * STAGE;     // bytes per warp
   static constexpr int CPL = 2 * BS * D / 8 / 32;  // 16-byte copies per lane per stage

@@ -373,12 +373,26 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             const int idx = et + 128 * u;
             if (idx < n_own * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
           }
-          for (int idx = et + 128 * kPf; idx < n_own * 64; idx += 128) {
-            const int j = rank + S * (idx >> 6), i = (idx & 63) % half;
-            const int tok = tok0 + j;
-            qk(idx, e.rope_cos[static_cast<size_t>(tok) * half + i],
-               e.rope_sin[static_cast<size_t>(tok) * half + i],
-               n0 >= e.q_dim ? e.slot_mapping[tok] : 0);
+          // wide tiles: the rest in chunks of kPf, each chunk's loads issued before its stores
+          for (int b0 = et + 128 * kPf; b0 < n_own * 64; b0 += 128 * kPf) {
+            float ca[kPf], cb[kPf];
+            long long cs[kPf];
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < n_own * 64) {
+                const int tok = tok0 + rank + S * (idx >> 6);
+                const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
+                ca[u] = e.rope_cos[o];
+                cb[u] = e.rope_sin[o];
+                cs[u] = n0 >= e.q_dim ? e.slot_mapping[tok] : 0;
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < n_own * 64) qk(idx, ca[u], cb[u], cs[u]);
+            }
           }
         } else {
           // v columns
@@ -398,8 +412,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             const int idx = et + 128 * u;
             if (idx < n_own * kGemmTileN) vv(idx, pf_s[u]);
           }
-          for (int idx = et + 128 * kPf; idx < n_own * kGemmTileN; idx += 128)
-            vv(idx, e.slot_mapping[tok0 + rank + S * (idx >> 7)]);
+          for (int b0 = et + 128 * kPf; b0 < n_own * kGemmTileN; b0 += 128 * kPf) {
+            long long cs[kPf];
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < n_own * kGemmTileN) cs[u] = e.slot_mapping[tok0 + rank + S * (idx >> 7)];
+            }
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < n_own * kGemmTileN) vv(idx, cs[u]);
+            }
+          }
         }
         // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
       } else if (p.epi == EPI_RESID) {
@@ -418,8 +443,20 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           const int idx = et + 128 * u;
           if (idx < n_own * kGemmTileN) rs_row(idx, pf_a[u]);
         }
-        for (int idx = et + 128 * kPf; idx < n_own * kGemmTileN; idx += 128)
-          rs_row(idx, e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et]);
+        for (int b0 = et + 128 * kPf; b0 < n_own * kGemmTileN; b0 += 128 * kPf) {
+          float cr[kPf];
+#pragma unroll
+          for (int u = 0; u < kPf; ++u) {
+            const int idx = b0 + 128 * u;
+            if (idx < n_own * kGemmTileN)
+              cr[u] = e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et];
+          }
+#pragma unroll
+          for (int u = 0; u < kPf; ++u) {
+            const int idx = b0 + 128 * u;
+            if (idx < n_own * kGemmTileN) rs_row(idx, cr[u]);
+          }
+        }
         named_barrier_sync(1, 128);
         for (int jj = ew; jj < n_own; jj += 4) {
           const int j = rank + S * jj;
@@ -438,7 +475,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           const float sc = scaled ? rs_s[j] : 1.f;
           const float g = tile[j * kGemmTileN + c] * sc;
           const float u = tile[j * kGemmTileN + 64 + c] * sc;
-          const float a = g / (1.f + expf(-g)) * u;
+          const float a = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
           ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
         }
         fence_proxy_async_global();
