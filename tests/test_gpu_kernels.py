@@ -75,6 +75,8 @@ def test_attention_rejects_unsupported_shapes(cuda_lib):
     (1, 128, 64, "bf16"), (16, 256, 128, "f16"), (33, 1152, 896, "f16"),
     (7, 896, 4864, "bf16"), (32, 9728, 896, "f16"), (256, 384, 512, "bf16"),
     (300, 256, 1024, "bf16"), (1000, 512, 256, "f16"), (2048, 1024, 2048, "bf16"),
+    # >= 152 output tiles: one split, tiles of 160 and 256 tokens staged in two passes
+    (300, 19456, 256, "bf16"), (256, 19456, 512, "f16"),
 ])
 def test_linear_matches_fp64(cuda_lib, m, n, k, dtype):
     import torch

@@ -8,7 +8,7 @@
 //
 // * Work unit = (request b, kv head g, superchunk).  A row's blocks split into superchunks of at
 //   most 64 blocks (1024 tokens); the split is a function of the row's length alone, so a row's
-//   result never depends on the rest of the batch.  A CTA takes a unit; its 4 warps take
+//   result never depends on the rest of the batch.  A CTA takes a unit; its warps (8 at head_dim 64, else 4) take
 //   contiguous quarters of the superchunk and merge through shared memory.
 // * Every warp streams its blocks (running ahead into its share of the CTA's next unit) through
 //   a private ring of stages; each stage holds one 16 x d K tile and one V tile, copied with
@@ -23,7 +23,7 @@
 //   The accumulator layout of the first product is exactly the B-operand layout of the second,
 //   so P never leaves registers.  Each K/V element is read once from shared memory for all G
 //   heads: no expansion.  Online softmax in the log2 domain, per head, in registers.
-// * The 4 warps' shares are combined in warp order; superchunks of one (b, g) are combined by the
+// * The warps' shares are combined in warp order; superchunks of one (b, g) are combined by the
 //   CTA that finishes last (atomic counter, no spin) in superchunk order with the log-sum-exp rule:
 //   deterministic.
 #include <cuda_bf16.h>
@@ -109,14 +109,16 @@ __device__ __forceinline__ void set_err(int* err, int code) {
 
 template <int D, int G>
 struct AttnShape {
-  static constexpr int NW = 4;                 // warps per CTA; they split one superchunk
+  // warps per CTA; they split one superchunk (8 at head_dim 64, whose blocks are cheap to
+  // stream but long to walk one by one)
+  static constexpr int NW = D == 64 ? 8 : 4;
   static constexpr int NT = NW * 32;
   static constexpr int BS = 16;                // tokens per cache block
   static constexpr int NH = D / 64;            // 128-byte column halves of a tile
   static constexpr int TILE = BS * D * 2;      // bytes of one K or V tile
   static constexpr int STAGE = 2 * TILE;
   // stages per warp: G = 8 keeps the ring at two stages so two CTAs fit on an SM
-  static constexpr int NST = (D == 128) ? (G == 8 ? 2 : 3) : 6;
+  static constexpr int NST = (D == 128) ? (G == 8 ? 2 : 3) : 4;
   static constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
   static constexpr int RING = NST * STAGE;     // bytes per warp
   static constexpr int CPL = 2 * BS * D / 8 / 32;  // 16-byte copies per lane per stage
@@ -133,7 +135,8 @@ struct AttnShape {
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 ? 1 : 2)
+    attn_decode_kernel(const AttnParams p) {
   using S = AttnShape<D, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, 2) attn_decode_kernel(con
       }
     }
 
-    // ---- merge the 4 warps' shares of the superchunk through shared memory, in warp order
+    // ---- merge the warps' shares of the superchunk through shared memory, in warp order
     {
       float* wacc = m_acc + warp * G * D;
 #pragma unroll

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   const int S = p.splits;
   const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;  // owned tokens
+  const bool two_pass = gemm_two_pass(BN, S);
   // epilogue prefetch registers (first kPf iterations of each epilogue thread)
   float pf_a[kPf] = {}, pf_b[kPf] = {};
   long long pf_s[kPf] = {};
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
     float* tile = reinterpret_cast<float*>(smem);
     const int nchunk = (m_valid + 15) >> 4;
-    if (ok && !*abort_flag) {
+    if (ok && !*abort_flag && !two_pass) {
       for (int c = 0; c < nchunk; ++c) {
         uint32_t r[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), r);
@@ -324,161 +325,192 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     if (run) {
       const EpiArgs& e = p.e;
       const bool scaled = e.sumsq_in != nullptr;
-      if (p.epi == EPI_F32) {
-        float* out = e.out_f32;
-        if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
-        for (int idx = et; idx < n_own * kGemmTileN; idx += 128) {
-          const int j = rank + S * (idx >> 7), r = idx & 127;
-          float v = tile[j * kGemmTileN + r];
-          if (scaled) v *= rs_s[j];
-          out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
+      float* const tbase = reinterpret_cast<float*>(smem);
+      // A single-split tile wider than kPassRows tokens is staged and finished kPassRows
+      // tokens at a time (its shared-memory tile is then half the size).
+      const int npass = two_pass ? (m_valid + kPassRows - 1) / kPassRows : 1;
+      for (int pass = 0; pass < npass; ++pass) {
+        const int jlo = pass * kPassRows;  // first owned-token index of this pass
+        const int jn = two_pass ? min(kPassRows, m_valid - jlo) : n_own;  // owned tokens in it
+        if (two_pass) {
+          if (pass > 0) named_barrier_sync(1, 128);  // the previous pass is done with the tile
+          const int q = warp & 3, frow = q * 32 + lane;
+          for (int c = 0; c < (jn + 15) >> 4; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(jlo + c * 16), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tbase[(c * 16 + i) * kGemmTileN + frow] = __uint_as_float(r[i]);
+          }
+          named_barrier_sync(1, 128);
         }
-      } else if (p.epi == EPI_QKV) {
-        const int d = e.head_dim, half = d >> 1;
-        T* qo = reinterpret_cast<T*>(e.q_out);
-        T* kp = reinterpret_cast<T*>(e.k_pool);
-        T* vp = reinterpret_cast<T*>(e.v_pool);
-        auto kv_base = [&](long long slot, int kvh) {
-          return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
-                  static_cast<size_t>(slot % e.block_size)) * d;
-        };
-        if (n0 < e.q_dim + e.kv_dim) {
-          // q and k columns: RoPE pairs (i, i + d/2) of each head
-          auto qk = [&](int idx, float c, float sn, long long slot) {
-            const int j = rank + S * (idx >> 6), pr = idx & 63;
-            const int hl = pr / half, i = pr - hl * half;
-            const int r_lo = hl * d + i, r_hi = r_lo + half;
-            const int tok = tok0 + j;
-            const float sc = scaled ? rs_s[j] : 1.f;
-            const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
-            const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
-            const float y_lo = x_lo * c - x_hi * sn;
-            const float y_hi = x_hi * c + x_lo * sn;
-            if (n0 < e.q_dim) {
-              T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
-              dst[r_lo] = Cvt<T>::from_f(y_lo);
-              dst[r_hi] = Cvt<T>::from_f(y_hi);
-            } else {
+        // tile[j * 128 + r] addresses the staged row of token j of this pass
+        float* tile = tbase - static_cast<ptrdiff_t>(jlo) * kGemmTileN;
+        const bool use_pf = pass == 0;  // the prefetched registers hold pass 0's first chunk
+        const int start = use_pf ? et + 128 * kPf : et;
+        auto tok_of = [&](int k) { return rank + S * (jlo + k); };  // k-th owned token of the pass
+        if (p.epi == EPI_F32) {
+          float* out = e.out_f32;
+          if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
+          for (int idx = et; idx < jn * kGemmTileN; idx += 128) {
+            const int j = tok_of(idx >> 7), r = idx & 127;
+            float v = tile[j * kGemmTileN + r];
+            if (scaled) v *= rs_s[j];
+            out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
+          }
+        } else if (p.epi == EPI_QKV) {
+          const int d = e.head_dim, half = d >> 1;
+          T* qo = reinterpret_cast<T*>(e.q_out);
+          T* kp = reinterpret_cast<T*>(e.k_pool);
+          T* vp = reinterpret_cast<T*>(e.v_pool);
+          auto kv_base = [&](long long slot, int kvh) {
+            return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                    static_cast<size_t>(slot % e.block_size)) * d;
+          };
+          if (n0 < e.q_dim + e.kv_dim) {
+            // q and k columns: RoPE pairs (i, i + d/2) of each head
+            auto qk = [&](int idx, float c, float sn, long long slot) {
+              const int j = tok_of(idx >> 6), pr = idx & 63;
+              const int hl = pr / half, i = pr - hl * half;
+              const int r_lo = hl * d + i, r_hi = r_lo + half;
+              const int tok = tok0 + j;
+              const float sc = scaled ? rs_s[j] : 1.f;
+              const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
+              const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
+              const float y_lo = x_lo * c - x_hi * sn;
+              const float y_hi = x_hi * c + x_lo * sn;
+              if (n0 < e.q_dim) {
+                T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
+                dst[r_lo] = Cvt<T>::from_f(y_lo);
+                dst[r_hi] = Cvt<T>::from_f(y_hi);
+              } else {
+                if (slot < 0 || slot >= e.pool_slots) {
+                  set_err(p.err, NS_DEV_BAD_SLOT);
+                  return;
+                }
+                const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
+                kp[base + i] = Cvt<T>::from_f(y_lo);
+                kp[base + i + half] = Cvt<T>::from_f(y_hi);
+              }
+            };
+            if (use_pf) {
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = et + 128 * u;
+                if (idx < jn * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
+              }
+            }
+            // the rest in chunks of kPf, each chunk's loads issued before its stores
+            for (int b0 = start; b0 < jn * 64; b0 += 128 * kPf) {
+              float ca[kPf], cb[kPf];
+              long long cs[kPf];
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * 64) {
+                  const int tok = tok0 + tok_of(idx >> 6);
+                  const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
+                  ca[u] = e.rope_cos[o];
+                  cb[u] = e.rope_sin[o];
+                  cs[u] = n0 >= e.q_dim ? e.slot_mapping[tok] : 0;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * 64) qk(idx, ca[u], cb[u], cs[u]);
+              }
+            }
+          } else {
+            // v columns
+            auto vv = [&](int idx, long long slot) {
+              const int j = tok_of(idx >> 7), r = idx & 127;
+              const int col = n0 - e.q_dim - e.kv_dim + r;
+              const int kvh = col / d, dim = col - kvh * d;
               if (slot < 0 || slot >= e.pool_slots) {
                 set_err(p.err, NS_DEV_BAD_SLOT);
                 return;
               }
-              const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
-              kp[base + i] = Cvt<T>::from_f(y_lo);
-              kp[base + i + half] = Cvt<T>::from_f(y_hi);
-            }
-          };
+              const float v = tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f);
+              vp[kv_base(slot, kvh) + dim] = Cvt<T>::from_f(v);
+            };
+            if (use_pf) {
 #pragma unroll
-          for (int u = 0; u < kPf; ++u) {
-            const int idx = et + 128 * u;
-            if (idx < n_own * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
-          }
-          // wide tiles: the rest in chunks of kPf, each chunk's loads issued before its stores
-          for (int b0 = et + 128 * kPf; b0 < n_own * 64; b0 += 128 * kPf) {
-            float ca[kPf], cb[kPf];
-            long long cs[kPf];
-#pragma unroll
-            for (int u = 0; u < kPf; ++u) {
-              const int idx = b0 + 128 * u;
-              if (idx < n_own * 64) {
-                const int tok = tok0 + rank + S * (idx >> 6);
-                const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
-                ca[u] = e.rope_cos[o];
-                cb[u] = e.rope_sin[o];
-                cs[u] = n0 >= e.q_dim ? e.slot_mapping[tok] : 0;
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = et + 128 * u;
+                if (idx < jn * kGemmTileN) vv(idx, pf_s[u]);
               }
             }
+            for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
+              long long cs[kPf];
 #pragma unroll
-            for (int u = 0; u < kPf; ++u) {
-              const int idx = b0 + 128 * u;
-              if (idx < n_own * 64) qk(idx, ca[u], cb[u], cs[u]);
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * kGemmTileN) cs[u] = e.slot_mapping[tok0 + tok_of(idx >> 7)];
+              }
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * kGemmTileN) vv(idx, cs[u]);
+              }
             }
           }
-        } else {
-          // v columns
-          auto vv = [&](int idx, long long slot) {
-            const int j = rank + S * (idx >> 7), r = idx & 127;
-            const int col = n0 - e.q_dim - e.kv_dim + r;
-            const int kvh = col / d, dim = col - kvh * d;
-            if (slot < 0 || slot >= e.pool_slots) {
-              set_err(p.err, NS_DEV_BAD_SLOT);
-              return;
-            }
-            const float v = tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f);
-            vp[kv_base(slot, kvh) + dim] = Cvt<T>::from_f(v);
+          // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
+        } else if (p.epi == EPI_RESID) {
+          T* xo = reinterpret_cast<T*>(e.xn_out);
+          const float gam = pf_b[0];
+          auto rs_row = [&](int idx, float old) {
+            const int j = tok_of(idx >> 7), r = idx & 127;
+            const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
+            const float rn = old + tile[j * kGemmTileN + r];
+            e.resid[gi] = rn;
+            xo[gi] = Cvt<T>::from_f(rn * gam);
+            tile[j * kGemmTileN + r] = rn * rn;
           };
+          if (use_pf) {
 #pragma unroll
-          for (int u = 0; u < kPf; ++u) {
-            const int idx = et + 128 * u;
-            if (idx < n_own * kGemmTileN) vv(idx, pf_s[u]);
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = et + 128 * u;
+              if (idx < jn * kGemmTileN) rs_row(idx, pf_a[u]);
+            }
           }
-          for (int b0 = et + 128 * kPf; b0 < n_own * kGemmTileN; b0 += 128 * kPf) {
-            long long cs[kPf];
+          for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
+            float cr[kPf];
 #pragma unroll
             for (int u = 0; u < kPf; ++u) {
               const int idx = b0 + 128 * u;
-              if (idx < n_own * kGemmTileN) cs[u] = e.slot_mapping[tok0 + rank + S * (idx >> 7)];
+              if (idx < jn * kGemmTileN)
+                cr[u] = e.resid[static_cast<size_t>(tok0 + tok_of(idx >> 7)) * e.resid_dim + n0 + et];
             }
 #pragma unroll
             for (int u = 0; u < kPf; ++u) {
               const int idx = b0 + 128 * u;
-              if (idx < n_own * kGemmTileN) vv(idx, cs[u]);
+              if (idx < jn * kGemmTileN) rs_row(idx, cr[u]);
             }
           }
-        }
-        // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
-      } else if (p.epi == EPI_RESID) {
-        T* xo = reinterpret_cast<T*>(e.xn_out);
-        const float gam = pf_b[0];
-        auto rs_row = [&](int idx, float old) {
-          const int j = rank + S * (idx >> 7), r = idx & 127;
-          const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
-          const float rn = old + tile[j * kGemmTileN + r];
-          e.resid[gi] = rn;
-          xo[gi] = Cvt<T>::from_f(rn * gam);
-          tile[j * kGemmTileN + r] = rn * rn;
-        };
+          named_barrier_sync(1, 128);
+          for (int k = ew; k < jn; k += 4) {
+            const int j = tok_of(k);
+            const float* tr = tile + j * kGemmTileN;
+            float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
 #pragma unroll
-        for (int u = 0; u < kPf; ++u) {
-          const int idx = et + 128 * u;
-          if (idx < n_own * kGemmTileN) rs_row(idx, pf_a[u]);
-        }
-        for (int b0 = et + 128 * kPf; b0 < n_own * kGemmTileN; b0 += 128 * kPf) {
-          float cr[kPf];
-#pragma unroll
-          for (int u = 0; u < kPf; ++u) {
-            const int idx = b0 + 128 * u;
-            if (idx < n_own * kGemmTileN)
-              cr[u] = e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et];
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) e.sumsq_out[static_cast<size_t>(tile_n) * e.sumsq_ld + tok0 + j] = s;
           }
-#pragma unroll
-          for (int u = 0; u < kPf; ++u) {
-            const int idx = b0 + 128 * u;
-            if (idx < n_own * kGemmTileN) rs_row(idx, cr[u]);
+          fence_proxy_async_global();
+        } else if (p.epi == EPI_SWIGLU) {
+          T* ao = reinterpret_cast<T*>(e.act_out);
+          const int f0 = tile_n * 64;
+          for (int idx = et; idx < jn * 64; idx += 128) {
+            const int j = tok_of(idx >> 6), c = idx & 63;
+            const float sc = scaled ? rs_s[j] : 1.f;
+            const float g = tile[j * kGemmTileN + c] * sc;
+            const float u = tile[j * kGemmTileN + 64 + c] * sc;
+            const float a = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
+            ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
           }
+          fence_proxy_async_global();
         }
-        named_barrier_sync(1, 128);
-        for (int jj = ew; jj < n_own; jj += 4) {
-          const int j = rank + S * jj;
-          const float* tr = tile + j * kGemmTileN;
-          float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lane == 0) e.sumsq_out[static_cast<size_t>(tile_n) * e.sumsq_ld + tok0 + j] = s;
-        }
-        fence_proxy_async_global();
-      } else if (p.epi == EPI_SWIGLU) {
-        T* ao = reinterpret_cast<T*>(e.act_out);
-        const int f0 = tile_n * 64;
-        for (int idx = et; idx < n_own * 64; idx += 128) {
-          const int j = rank + S * (idx >> 6), c = idx & 63;
-          const float sc = scaled ? rs_s[j] : 1.f;
-          const float g = tile[j * kGemmTileN + c] * sc;
-          const float u = tile[j * kGemmTileN + 64 + c] * sc;
-          const float a = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
-          ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
-        }
-        fence_proxy_async_global();
       }
     }
   }
@@ -508,14 +540,16 @@ size_t gemm_smem_bytes(int BN, int nstage) {
          kCtrlBytes;
 }
 
-int gemm_pick_stages(int BN, int kb_per_split) {
+int gemm_pick_stages(int BN, int kb_per_split, int splits) {
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
-  // the epilogue tile [BN][128] fp32 reuses the stage ring
-  const int tile_min = static_cast<int>((static_cast<size_t>(BN) * kGemmTileN * 4 + stage - 1) / stage);
-  if (BN <= 64) {
-    // Decode batches: enough stages to prefetch the whole k-range of the CTA where it fits in
-    // half an SM's shared memory, so the next kernel's CTAs can be resident (and stream their
-    // own weights) while this one runs.
+  // the epilogue tile [rows][128] fp32 reuses the stage ring
+  const size_t tile_rows = gemm_two_pass(BN, splits) ? kPassRows : BN;
+  const int tile_min = static_cast<int>((tile_rows * kGemmTileN * 4 + stage - 1) / stage);
+  if (BN <= 64 || gemm_two_pass(BN, splits)) {
+    // Enough stages to prefetch the CTA's k-range where it fits in half an SM's shared memory:
+    // for decode batches the next kernel's CTAs can then be resident (streaming their own
+    // weights) while this one runs; for wide single-split tiles two CTAs share an SM, one's
+    // epilogue overlapping the other's main loop.
     const size_t half_sm = 113 * 1024 - 1024 - kCtrlBytes;
     int n = static_cast<int>(half_sm / stage);
     n = std::min(n, std::max(kb_per_split, 2));
