@@ -8,8 +8,9 @@
 //
 // * Work unit = (request b, kv head g, superchunk).  A row's blocks split into superchunks of at
 //   most 64 blocks (1024 tokens); the split is a function of the row's length alone, so a row's
-//   result never depends on the rest of the batch.  A CTA takes a unit; its warps (8 at head_dim 64, else 4) take
-//   contiguous quarters of the superchunk and merge through shared memory.
+//   result never depends on the rest of the batch.  A CTA takes a unit; its warps (8 at
+//   head_dim 64, else 4) take contiguous shares of the superchunk and merge through shared
+//   memory.
 // * Every warp streams its blocks (running ahead into its share of the CTA's next unit) through
 //   a private ring of stages; each stage holds one 16 x d K tile and one V tile, copied with
 //   16-byte cp.async by all 32 lanes (each tile is one contiguous run, so every warp request is a
