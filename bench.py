@@ -651,6 +651,22 @@ def read_traffic(kind):
     return None
 
 
+def replica_aggregate(ms_local: float, units_local: int, world: int):
+    """Whole-job figures of independent replicas (the step does not shard): the slowest rank's
+    time and the units every rank processed.  One collective per measurement, outside the
+    timed region; the data path has none."""
+    if world <= 1:
+        return ms_local, units_local
+    import torch
+    import torch.distributed as dist
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
 def run_ours(args, rank, world):
     import torch
     import __graft_entry__ as ge
@@ -691,20 +707,19 @@ def run_ours(args, rank, world):
     clocks.mark_stop()
     ms_total = e0.elapsed_time(e1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, units = replica_aggregate(ms_total, wl.B * K, world)
     dev_err = wl.dev.device_error()
     info = wl.dev.info()
     ms_step = ms_total / K
-    value = wl.B * K * world / (ms_total * 1e-3)
+    value = units / (ms_total * 1e-3)
 
     # e2e: greedy decode loop through the public API, ids read back every step
     ids_dev = torch.empty(wl.B, dtype=torch.int32, device="cuda")
     ids_host = torch.empty(wl.B, dtype=torch.int32).pin_memory()
     toks = wl.tokens.copy()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         wl.step(wl.next_meta(toks))
@@ -712,8 +727,8 @@ def run_ours(args, rank, world):
         ids_host.copy_(ids_dev, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         toks = ids_host.numpy().copy()
-    e2e_s = time.perf_counter() - t0
-    e2e_value = wl.B * e2e_steps * world / e2e_s
+    e2e_ms, e2e_units = replica_aggregate((time.perf_counter() - t0) * 1e3, wl.B * e2e_steps, world)
+    e2e_value = e2e_units / (e2e_ms * 1e-3)
 
     # per-kernel timing in eager steps (same kernels, same data)
     wl.dev.set_kernel_timing(True)
