@@ -48,7 +48,7 @@ struct Cvt<__nv_bfloat16> {
 
 constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
 constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
-constexpr int kPf = 8;  // epilogue iterations per thread whose inputs are loaded early
+constexpr int kPf = 6;  // epilogue iterations per thread whose inputs are loaded early
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   const int S = p.splits;
   const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;  // owned tokens
-  const bool two_pass = gemm_two_pass(BN, S);
+  const bool two_pass = gemm_two_pass(BN);
   // epilogue prefetch registers (first kPf iterations of each epilogue thread)
   float pf_a[kPf] = {}, pf_b[kPf] = {};
   long long pf_s[kPf] = {};
@@ -282,27 +282,38 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   // The split CTAs of one output tile form a thread-block cluster.  CTA `rank` owns tokens
   // j = rank, rank + S, ...; it sums their partial rows over every CTA of the cluster through
   // distributed shared memory, in rank order (deterministic), then runs the epilogue for them.
-  // Two cluster barrier phases: "every tile is complete" before the reduction, and "every
-  // peer has finished reading" before a CTA leaves; the second is arrived at as soon as a
-  // thread is done with remote reads and waited for only at the end.
+  // Cluster barrier phases, per staged pass: "every tile is complete" before the reduction and
+  // "every peer has finished reading" before the tile is overwritten or the CTA leaves; the
+  // second is arrived at as soon as a thread is done with remote reads and waited for late.
+  // A tile wider than kPassRows tokens is staged kPassRows tokens at a time (its shared-memory
+  // tile is then half the size, so two CTAs fit on an SM).
+  const int npass = two_pass ? (m_valid + kPassRows - 1) / kPassRows : 1;
   __syncthreads();
-  if (S > 1) {
+  if (S > 1 && !two_pass) {
     cluster_sync();
     if (warp < 2) cluster_arrive();  // these warps read no peer memory
   }
-  float* tile = reinterpret_cast<float*>(smem);
+  if (S > 1 && two_pass && warp < 2) {
+    for (int pass = 0; pass < npass; ++pass) {  // the same phases as the epilogue warps
+      if (pass > 0) cluster_wait();
+      cluster_sync();
+      cluster_arrive();
+    }
+  }
   if (warp >= 2) {
     const int et = threadIdx.x - 64;  // 0..127: feature within the tile
     const int ew = warp - 2;
     const bool run = !*abort_flag;
-    if (run && S > 1) {
-      // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads are
-      // issued before they are summed (in rank order)
-      const uint32_t base = smem_u32(tile);
+    float* const tbase = reinterpret_cast<float*>(smem);
+    // owned tokens j = rank + S * k with lo <= j < hi (rows j - lo of the staged tile)
+    auto reduce = [&](int k_lo, int k_hi, int lo) {
+      // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads
+      // are issued before they are summed (in rank order)
+      const uint32_t base = smem_u32(tbase);
       const int fg = et & 31, slot = et >> 5;
-      for (int jj = slot; jj < n_own; jj += 4) {
-        const int j = rank + S * jj;
-        const uint32_t off = base + static_cast<uint32_t>((j * kGemmTileN + 4 * fg) * 4);
+      for (int k = k_lo + slot; k < k_hi; k += 4) {
+        const int row = rank + S * k - lo;
+        const uint32_t off = base + static_cast<uint32_t>((row * kGemmTileN + 4 * fg) * 4);
         float4 v[kMaxSplits];
 #pragma unroll
         for (int r = 0; r < kMaxSplits; ++r)
@@ -317,38 +328,52 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             acc.w += v[r].w;
           }
         }
-        *reinterpret_cast<float4*>(&tile[j * kGemmTileN + 4 * fg]) = acc;
+        *reinterpret_cast<float4*>(&tbase[row * kGemmTileN + 4 * fg]) = acc;
       }
+    };
+    if (!two_pass) {
+      if (run && S > 1) reduce(0, n_own, 0);
+      named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
+      if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
     }
-    named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
-    if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
-    if (run) {
-      const EpiArgs& e = p.e;
-      const bool scaled = e.sumsq_in != nullptr;
-      float* const tbase = reinterpret_cast<float*>(smem);
-      // A single-split tile wider than kPassRows tokens is staged and finished kPassRows
-      // tokens at a time (its shared-memory tile is then half the size).
-      const int npass = two_pass ? (m_valid + kPassRows - 1) / kPassRows : 1;
-      for (int pass = 0; pass < npass; ++pass) {
-        const int jlo = pass * kPassRows;  // first owned-token index of this pass
-        const int jn = two_pass ? min(kPassRows, m_valid - jlo) : n_own;  // owned tokens in it
-        if (two_pass) {
-          if (pass > 0) named_barrier_sync(1, 128);  // the previous pass is done with the tile
-          const int q = warp & 3, frow = q * 32 + lane;
-          for (int c = 0; c < (jn + 15) >> 4; ++c) {
+    const EpiArgs& e = p.e;
+    const bool scaled = e.sumsq_in != nullptr;
+    for (int pass = 0; pass < npass; ++pass) {
+      // token rows [lo, hi) of the CTA's tile; owned tokens k_lo <= k < k_hi among them
+      const int lo = two_pass ? pass * kPassRows : 0;
+      const int hi = two_pass ? min(lo + kPassRows, m_valid) : m_valid;
+      const int k_lo = two_pass ? max(0, (lo - rank + S - 1) / S) : 0;
+      const int k_hi = two_pass ? max(k_lo, (hi - rank + S - 1) / S) : n_own;
+      const int jn = k_hi - k_lo;
+      if (two_pass) {
+        if (pass > 0) {
+          named_barrier_sync(1, 128);  // this CTA is done with the previous pass's tile
+          if (S > 1) cluster_wait();   // ... and so are its peers
+        }
+        const int q = warp & 3, frow = q * 32 + lane;
+        if (run) {
+          for (int c = 0; c < (hi - lo + 15) >> 4; ++c) {
             uint32_t r[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(jlo + c * 16), r);
+            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(lo + c * 16), r);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) tbase[(c * 16 + i) * kGemmTileN + frow] = __uint_as_float(r[i]);
           }
-          named_barrier_sync(1, 128);
         }
+        named_barrier_sync(1, 128);
+        if (S > 1) {
+          cluster_sync();
+          if (run) reduce(k_lo, k_hi, lo);
+          named_barrier_sync(1, 128);
+          cluster_arrive();
+        }
+      }
+      if (run) {
         // tile[j * 128 + r] addresses the staged row of token j of this pass
-        float* tile = tbase - static_cast<ptrdiff_t>(jlo) * kGemmTileN;
+        float* tile = tbase - static_cast<ptrdiff_t>(lo) * kGemmTileN;
         const bool use_pf = pass == 0;  // the prefetched registers hold pass 0's first chunk
         const int start = use_pf ? et + 128 * kPf : et;
-        auto tok_of = [&](int k) { return rank + S * (jlo + k); };  // k-th owned token of the pass
+        auto tok_of = [&](int k) { return rank + S * (k_lo + k); };  // k-th owned token of the pass
         if (p.epi == EPI_F32) {
           float* out = e.out_f32;
           if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
@@ -540,25 +565,27 @@ size_t gemm_smem_bytes(int BN, int nstage) {
          kCtrlBytes;
 }
 
-int gemm_pick_stages(int BN, int kb_per_split, int splits) {
+int gemm_pick_stages(int BN, int kb_per_split, int ctas, int sms) {
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
   // the epilogue tile [rows][128] fp32 reuses the stage ring
-  const size_t tile_rows = gemm_two_pass(BN, splits) ? kPassRows : BN;
+  const size_t tile_rows = gemm_two_pass(BN) ? kPassRows : BN;
   const int tile_min = static_cast<int>((tile_rows * kGemmTileN * 4 + stage - 1) / stage);
-  if (BN <= 64 || gemm_two_pass(BN, splits)) {
-    // Enough stages to prefetch the CTA's k-range where it fits in half an SM's shared memory:
-    // for decode batches the next kernel's CTAs can then be resident (streaming their own
-    // weights) while this one runs; for wide single-split tiles two CTAs share an SM, one's
-    // epilogue overlapping the other's main loop.
-    const size_t half_sm = 113 * 1024 - 1024 - kCtrlBytes;
+  const size_t half_sm = 113 * 1024 - 1024 - kCtrlBytes;
+  // Wide tiles run two CTAs per SM (one's epilogue overlapping the other's main loop) unless
+  // the grid is small enough to sit comfortably at one per SM: a grid needing 90 % or more of
+  // the SMs at one CTA each did not fit in one wave once its clusters were placed.
+  if (BN <= 64 || (gemm_two_pass(BN) && ctas * 10 >= sms * 9)) {
+    // Half an SM: for decode batches the next kernel's CTAs can be resident (streaming their
+    // own weights) while this one runs.  As many stages as the CTA's k-range needs.
     int n = static_cast<int>(half_sm / stage);
     n = std::min(n, std::max(kb_per_split, 2));
     return std::max(n, std::max(tile_min, 2));
   }
+  // one CTA per SM: a deep ring keeps enough weight bytes in flight
   const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
   int n = static_cast<int>(budget / stage);
   if (n > 8) n = 8;
-  return std::max(n, std::max(tile_min, 4));
+  return std::max(n, std::max(tile_min, gemm_two_pass(BN) ? 2 : 4));
 }
 
 uint32_t gemm_idesc(int dtype, int BN) {

@@ -410,7 +410,8 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   p.BN = pick_bn(m);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, p.splits);
+  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split,
+                              ((m + p.BN - 1) / p.BN) * p.splits * (p.N / kGemmTileN), h->sms);
   p.epi = epi;
   p.idesc = gemm_idesc(h->dtype, p.BN);
   p.err = h->err;
@@ -1144,7 +1145,8 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   p.BN = pick_bn(m);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, p.splits);
+  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split,
+                              ((m + p.BN - 1) / p.BN) * p.splits * (p.N / kGemmTileN), device_sms());
   p.epi = EPI_F32;
   p.idesc = gemm_idesc(dtype, p.BN);
   DevScratch* sc = nullptr;

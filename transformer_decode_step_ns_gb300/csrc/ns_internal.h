@@ -111,12 +111,13 @@ struct EmbedParams {
 };
 
 // Kernel launchers (return the launch error; `pdl` adds programmatic stream serialisation).
-// A single-split GEMM tile wider than kPassRows tokens stages its accumulator in shared memory
+// A GEMM tile wider than kPassRows tokens stages its accumulator in shared memory
 // kPassRows tokens at a time, so its stage ring may be two stages (two CTAs per SM).
 constexpr int kPassRows = 128;
-__host__ __device__ inline bool gemm_two_pass(int BN, int splits) { return splits == 1 && BN > kPassRows; }
+__host__ __device__ inline bool gemm_two_pass(int BN) { return BN > kPassRows; }
 size_t gemm_smem_bytes(int BN, int nstage);
-int gemm_pick_stages(int BN, int kb_per_split, int splits);
+// Stage-ring depth for a launch of `ctas` CTAs (the depth never changes results).
+int gemm_pick_stages(int BN, int kb_per_split, int ctas, int sms);
 uint32_t gemm_idesc(int dtype, int BN);
 cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                         int dtype, cudaStream_t s, bool pdl);
