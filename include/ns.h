@@ -187,6 +187,17 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
                          const int32_t* seq_lens, const int64_t* slot_mapping,
                          float* logits_out, ns_stream_t stream);
 
+/* Token ids from device memory (NanoFlow page, "Runtime details that keep the pipeline fed":
+ * the next iteration's batch is formed before the current one finishes, so an end-of-sequence
+ * token is seen one iteration late and no synchronisation sits on the critical path).  When device_token_ids is non-NULL, every later
+ * ns_decode_step reads row b's token from device_token_ids[b] (int32, device memory of at least
+ * max_batch entries, owned by the caller) instead of its token_ids argument, which may then be
+ * NULL and is not validated; a token outside [0, V) sets NS_DEV_BAD_TOKEN and row b uses token
+ * 0.  Writes to the buffer must be ordered before the step on its stream (for example
+ * ns_greedy_argmax of the previous step's logits on the same stream).  NULL restores the host
+ * token ids.  A graph is captured per source pointer. */
+ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids);
+
 /* Paged grouped-query decode attention alone (nanoserve notes: the fused paged-attention
  * kernel; grouped-query attention without the expanded K/V copy).  All pointers device:
  *   q [batch][n_q_heads][head_dim]; k_pool, v_pool [num_blocks][n_kv_heads][block_size]

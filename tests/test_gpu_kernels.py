@@ -122,3 +122,26 @@ def test_greedy_argmax_ties_to_lowest(cuda_lib):
     ref[2] = 7
     ref[4] = 0
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("vocab", [1, 5, 1001, 128256])
+def test_greedy_argmax_slices_and_nan(cuda_lib, vocab):
+    """The row is split over several CTAs: ragged and empty slices, a maximum in the last
+    slice, ties across slices, and NaN (never chosen; an all-NaN row gives 0)."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    g = torch.Generator(device="cpu").manual_seed(vocab)
+    logits = torch.randn(6, vocab, generator=g).cuda()
+    logits[1, :] = float("nan")
+    logits[1, vocab // 2] = -3.0
+    logits[2, vocab - 1] = 100.0
+    logits[3, :] = float("nan")
+    logits[4, :] = 2.0
+    out = torch.empty(6, dtype=torch.int32, device="cuda")
+    _lib.greedy_argmax(logits, out)
+    ref = torch.argmax(logits, dim=-1).to(torch.int32)
+    ref[1] = vocab // 2
+    ref[2] = vocab - 1
+    ref[3] = 0
+    ref[4] = 0
+    assert torch.equal(out.cpu(), ref.cpu())

@@ -204,6 +204,37 @@ def test_prefill_chunk_rows_spanning_nano_batches(cuda_lib):
         np.testing.assert_array_equal(vs[l], vs0[l])
 
 
+def test_device_token_source_equals_host_tokens_bitwise(cuda_lib):
+    """Three greedy steps with the tokens read back to the host and passed in, against the
+    same steps reading the previous argmax from device memory: the same logits bitwise."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    shape = _tiny("bf16")
+    ctx = [3, 40, 200]  # positions ctx .. ctx + 2 stay inside the rows' allocated blocks
+    ha = Harness(shape, 91, ctx)
+    hb = Harness(shape, 91, ctx)
+    bt = ha.batch
+    B = len(ctx)
+    ids_dev = to_dev(bt.token_ids.copy())
+    hb.dev.set_token_source(ids_dev)
+    la = torch.empty((B, shape.vocab), dtype=torch.float32, device="cuda")
+    lb = torch.empty_like(la)
+    out_a = torch.empty(B, dtype=torch.int32, device="cuda")
+    tok_a = bt.token_ids.copy()
+    for s in range(3):
+        pos = (bt.positions + s).astype(np.int32)
+        slots = bt.block_tables[np.arange(B), pos // 16].astype(np.int64) * 16 + pos % 16
+        ha.dev.step(tok_a, pos, bt.block_tables, pos + 1, slots, la)
+        _lib.greedy_argmax(la, out_a)
+        tok_a = from_dev(out_a)
+        hb.dev.step(None, pos, bt.block_tables, pos + 1, slots, lb)
+        _lib.greedy_argmax(lb, ids_dev)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(from_dev(la), from_dev(lb))
+        np.testing.assert_array_equal(tok_a, from_dev(ids_dev))
+    assert ha.dev.device_error() == 0 and hb.dev.device_error() == 0
+
+
 def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):
     shape = _tiny("f16")
     ctx = [9, 33, 129]

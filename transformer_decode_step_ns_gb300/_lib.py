@@ -33,7 +33,7 @@ SYMBOLS = (
     "ns_get_step_info", "ns_status_str", "ns_last_error_message", "ns_pool_create",
     "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
     "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
-    "ns_get_kernel_timing", "ns_attn_decode_noalloc",
+    "ns_get_kernel_timing", "ns_attn_decode_noalloc", "ns_set_token_source",
 )
 
 
@@ -116,6 +116,7 @@ def lib() -> ctypes.CDLL:
             "ns_check_step_metadata": ([I, I, I, I, I, I, P, P, P, P, P], I),
             "ns_last_error_message": ([], ctypes.c_char_p),
             "ns_set_kernel_timing": ([P, I], I),
+            "ns_set_token_source": ([P, P], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
@@ -281,21 +282,27 @@ class DecodeStep:
     def step(self, token_ids, positions, block_tables, seq_lens, slot_mapping, logits,
              stream=None) -> None:
         """One decode step; host metadata arrays, ``logits`` a device fp32 [B, V] buffer
-        (None: stop after the last layer, no LM head)."""
-        tok = np.ascontiguousarray(token_ids, dtype=np.int32)
+        (None: stop after the last layer, no LM head).  ``token_ids`` may be None after
+        ``set_token_source``."""
         pos = np.ascontiguousarray(positions, dtype=np.int32)
+        tok = None if token_ids is None else np.ascontiguousarray(token_ids, dtype=np.int32)
         tab = np.ascontiguousarray(block_tables, dtype=np.int32)
         sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
         slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
         if tab.ndim != 2 or tab.shape[1] != self.mb:
             raise ValueError(f"block_tables must be [batch, {self.mb}]")
-        check(lib().ns_decode_step(self.h, tok.shape[0], _ptr(tok), _ptr(pos), _ptr(tab),
+        check(lib().ns_decode_step(self.h, pos.shape[0], _ptr(tok), _ptr(pos), _ptr(tab),
                                    _ptr(sl), _ptr(slot), _ptr(logits), _stream(stream)))
 
     def device_error(self) -> int:
         c = I()
         check(lib().ns_get_device_error(self.h, ctypes.byref(c)))
         return c.value
+
+    def set_token_source(self, device_ids=None) -> None:
+        """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,
+        from the host arrays passed to ``step``."""
+        check(lib().ns_set_token_source(self.h, _ptr(device_ids)))
 
     def set_kernel_timing(self, on: bool) -> None:
         check(lib().ns_set_kernel_timing(self.h, 1 if on else 0))

@@ -81,30 +81,35 @@ __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
   fence_proxy_async_global();  // xn is read through TMA by the next kernel
 }
 
-// Greedy argmax over one row per block; ties go to the lowest index.
+// Greedy argmax; ties go to the lowest index, NaN never wins (an all-NaN row gives 0).  A
+// cluster of kArgmaxSplit CTAs takes one row, each CTA a contiguous slice; rank 0 combines the
+// slices' results through distributed shared memory (the comparison is a total order, so the
+// result does not depend on the split).
+constexpr int kArgmaxSplit = 8;
+
+__device__ __forceinline__ void argmax_merge(float& best, int& bi, float ov, int oi) {
+  if (ov > best || (ov == best && oi < bi)) {
+    best = ov;
+    bi = oi;
+  }
+}
+
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int vocab,
                                                       int32_t* out) {
   __shared__ float sv[32];
   __shared__ int si[32];
-  const float* r = logits + static_cast<size_t>(blockIdx.x) * vocab;
+  const int row = blockIdx.y;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int per = (vocab + kArgmaxSplit - 1) / kArgmaxSplit;
+  const int lo = rank * per, hi = min(vocab, lo + per);
+  const float* r = logits + static_cast<size_t>(row) * vocab;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
-    const float v = r[i];
-    if (v > best || (v == best && i < bi)) {
-      best = v;
-      bi = i;
-    }
-  }
+#pragma unroll 4
+  for (int i = lo + static_cast<int>(threadIdx.x); i < hi; i += blockDim.x) argmax_merge(best, bi, r[i], i);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
-      best = ov;
-      bi = oi;
-    }
-  }
+  for (int o = 16; o > 0; o >>= 1)
+    argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
     sv[warp] = best;
@@ -116,16 +121,27 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int v
     best = lane < nw ? sv[lane] : -INFINITY;
     bi = lane < nw ? si[lane] : 0x7fffffff;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > best || (ov == best && oi < bi)) {
-        best = ov;
-        bi = oi;
-      }
+    for (int o = 16; o > 0; o >>= 1)
+      argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+    if (lane == 0) {
+      sv[0] = best;  // this slice's result, read by rank 0
+      si[0] = bi;
     }
-    if (lane == 0) out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;
   }
+  cluster_sync();
+  if (rank == 0 && warp == 0) {
+    best = -INFINITY;
+    bi = 0x7fffffff;
+    if (lane < kArgmaxSplit) {
+      best = ld_shared_cluster_f32(map_shared_rank(smem_u32(&sv[0]), lane));
+      bi = static_cast<int>(ld_shared_cluster_u32(map_shared_rank(smem_u32(&si[0]), lane)));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1)
+      argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+    if (lane == 0) out[row] = bi == 0x7fffffff ? 0 : bi;
+  }
+  cluster_sync();  // every slice stays resident until rank 0 has read it
 }
 
 cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl) {
@@ -144,8 +160,18 @@ cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool p
 
 cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
                           cudaStream_t s) {
-  argmax_kernel<<<batch, 1024, 0, s>>>(logits, vocab, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kArgmaxSplit, batch, 1);
+  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kArgmaxSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, vocab, out);
 }
 
 }  // namespace ns

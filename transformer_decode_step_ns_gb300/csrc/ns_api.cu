@@ -232,13 +232,14 @@ ns_status pool_release(ns_block_pool* p, const int32_t* ids, int n) {
 
 ns_status check_meta(int num_blocks, int bs, int mb, int vocab, int max_batch, int batch,
                      const int32_t* token_ids, const int32_t* positions, const int32_t* block_tables,
-                     const int32_t* seq_lens, const int64_t* slot_mapping) {
+                     const int32_t* seq_lens, const int64_t* slot_mapping, bool tokens_on_host = true) {
   if (batch < 1 || batch > max_batch) return fail(NS_ERR_INVALID_ARG, "batch out of range");
-  if (!token_ids || !positions || !block_tables || !seq_lens || !slot_mapping)
+  if ((tokens_on_host && !token_ids) || !positions || !block_tables || !seq_lens || !slot_mapping)
     return fail(NS_ERR_INVALID_ARG, "null argument");
   for (int b = 0; b < batch; ++b) {
-    const int tok = token_ids[b], p = positions[b], L = seq_lens[b];
-    if (tok < 0 || tok >= vocab) return fail(NS_ERR_INVALID_ARG, "token id out of range");
+    const int p = positions[b], L = seq_lens[b];
+    if (tokens_on_host && (token_ids[b] < 0 || token_ids[b] >= vocab))
+      return fail(NS_ERR_INVALID_ARG, "token id out of range");
     if (p < 0 || L != p + 1) return fail(NS_ERR_INVALID_ARG, "seq_lens must equal positions + 1");
     if (L > mb * bs) return fail(NS_ERR_INVALID_ARG, "seq_len beyond max_blocks_per_seq * block_size");
     const int32_t* row = block_tables + static_cast<size_t>(b) * mb;
@@ -306,6 +307,7 @@ struct ns_ctx {
   std::vector<int> split_sizes;
   int attn_budget = 0;
   bool with_lm = true;  // false: the step stops after the last layer (logits_out == NULL)
+  const int32_t* tok_src = nullptr;  // device token ids (ns_set_token_source) or null: metadata
   std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
   cudaStream_t side = nullptr, cap = nullptr;
   std::vector<cudaEvent_t> events;
@@ -475,7 +477,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   for (int i = 0; i < n; ++i) {
     EmbedParams ep{};
     ep.embed = h->embed;
-    ep.token_ids = m_tok;
+    ep.token_ids = h->tok_src != nullptr ? h->tok_src : m_tok;
     ep.positions = m_pos;
     ep.vocab = c.vocab;
     ep.hidden = H;
@@ -612,7 +614,9 @@ bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int
 }
 
 std::vector<int> graph_key(const ns_ctx* h, int B) {
-  std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0};
+  const uint64_t src = reinterpret_cast<uint64_t>(h->tok_src);
+  std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0,
+                     static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32)};
   for (int v : h->split_sizes) k.push_back(v);
   return k;
 }
@@ -992,8 +996,9 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
   const ns_model_cfg& c = h->cfg;
   const int bs = h->block_size, mb = c.max_blocks_per_seq;
+  const bool host_tokens = h->tok_src == nullptr;
   NS_TRY(check_meta(h->num_blocks, bs, mb, c.vocab, c.max_batch, batch, token_ids, positions,
-                    block_tables, seq_lens, slot_mapping));
+                    block_tables, seq_lens, slot_mapping, host_tokens));
   if (h->n_split > 1) {
     int sum = 0;
     for (int v : h->split_sizes) sum += v;
@@ -1005,7 +1010,10 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
   const MetaLayout ml = meta_layout(batch, mb);
   uint8_t* mh = h->meta_host;
-  std::memcpy(mh + ml.tok, token_ids, batch * 4);
+  if (host_tokens)
+    std::memcpy(mh + ml.tok, token_ids, batch * 4);
+  else
+    std::memset(mh + ml.tok, 0, batch * 4);
   std::memcpy(mh + ml.pos, positions, batch * 4);
   std::memcpy(mh + ml.seq, seq_lens, batch * 4);
   std::memcpy(mh + ml.slot, slot_mapping, batch * 8);
@@ -1028,6 +1036,12 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
     h->info.kernels_per_step = h->kernels_last;
   }
   h->info.steps++;
+  return NS_OK;
+}
+
+ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  h->tok_src = device_token_ids;
   return NS_OK;
 }
 
