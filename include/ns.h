@@ -112,7 +112,8 @@ void ns_destroy(ns_handle h);
 
 /* Allocate the per-layer paged K and V pools: num_blocks blocks of block_size (16) token
  * slots.  Layout per layer and per K/V: [num_blocks][Hkv][block_size][d], storage dtype, so
- * each (block, kv head) tile is contiguous.  Initialises the host free list 0..num_blocks-1
+ * each (block, kv head) tile is contiguous; one more block follows each pool, reserved for the
+ * padding rows of bucketed graphs (ns_set_graph_buckets).  Initialises the host free list 0..num_blocks-1
  * (first-in first-out reuse).  A second call returns INVALID_ARG. */
 ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size);
 
@@ -186,6 +187,14 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
                          const int32_t* positions, const int32_t* block_tables,
                          const int32_t* seq_lens, const int64_t* slot_mapping,
                          float* logits_out, ns_stream_t stream);
+
+/* Graph buckets ("Bounding the CUDA graph capture", model cold-start page: capture graphs for
+ * a bounded set of batch sizes and pad).  With n > 0 ascending sizes (each <= max_batch), a
+ * graph-replayed step of `batch` rows uses the graph of the smallest size >= batch; the rows
+ * up to that size are padding (token 0 at position 0 in a block past the caller's pool, no
+ * logits written), so one captured graph serves every batch up to its size.  Batches above the
+ * largest size, eager steps and nano-batched steps use their exact size.  n = 0 clears. */
+ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes);
 
 /* Token ids from device memory (NanoFlow page, "Runtime details that keep the pipeline fed":
  * the next iteration's batch is formed before the current one finishes, so an end-of-sequence

@@ -235,6 +235,37 @@ def test_device_token_source_equals_host_tokens_bitwise(cuda_lib):
     assert ha.dev.device_error() == 0 and hb.dev.device_error() == 0
 
 
+def test_graph_buckets_pad_batches_and_match_exact_graphs(cuda_lib):
+    """With buckets {4, 8} a batch of 3 or 6 replays the graph of 4 or 8 with padding rows: the
+    real rows' logits equal those of exact-size graphs bitwise, the padding rows write no
+    logits (the rows after the caller's buffer keep their sentinel) and only the real rows'
+    slots of the caller's pool change."""
+    import torch
+    shape = _tiny("bf16")
+    ctx = [3, 40, 200, 17, 1, 600, 33, 9]
+    exact = Harness(shape, 101, ctx)
+    bucket = Harness(shape, 101, ctx)
+    bucket.dev.set_graph_buckets([4, 8])
+    bt = bucket.batch
+    for n in (3, 6, 8, 4):
+        exact.upload_pools()
+        bucket.upload_pools()
+        ref = exact.run_gpu(rows=slice(0, n))
+        big = torch.full((8 + 2, shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
+        bucket.dev.step(bt.token_ids[:n], bt.positions[:n], bt.block_tables[:n], bt.seq_lens[:n],
+                        bt.slot_mapping[:n], big[:n])
+        torch.cuda.synchronize()
+        assert bucket.dev.device_error() == 0
+        got = big.cpu().numpy()
+        np.testing.assert_array_equal(got[:n].astype(np.float64), ref)
+        assert np.isnan(got[n:]).all()
+        ks, vs = bucket.download_pools()
+        for l in range(shape.n_layers):
+            changed = np.nonzero((ks[l] != bucket.kp[l]).any(axis=(1, 2, 3)))[0]
+            assert set(changed.tolist()) <= {int(s) // 16 for s in bt.slot_mapping[:n]}
+    assert bucket.dev.info().graphs_cached == 2
+
+
 def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):
     shape = _tiny("f16")
     ctx = [9, 33, 129]

@@ -34,6 +34,7 @@ SYMBOLS = (
     "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
     "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
     "ns_get_kernel_timing", "ns_attn_decode_noalloc", "ns_set_token_source",
+    "ns_set_graph_buckets",
 )
 
 
@@ -117,6 +118,7 @@ def lib() -> ctypes.CDLL:
             "ns_last_error_message": ([], ctypes.c_char_p),
             "ns_set_kernel_timing": ([P, I], I),
             "ns_set_token_source": ([P, P], I),
+            "ns_set_graph_buckets": ([P, I, P], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
@@ -298,6 +300,11 @@ class DecodeStep:
         c = I()
         check(lib().ns_get_device_error(self.h, ctypes.byref(c)))
         return c.value
+
+    def set_graph_buckets(self, sizes: Optional[Sequence[int]] = None) -> None:
+        """Replay graphs captured for these batch sizes only, padding smaller batches."""
+        a = np.ascontiguousarray(sizes or [], dtype=np.int32)
+        check(lib().ns_set_graph_buckets(self.h, a.size, _ptr(a) if a.size else None))
 
     def set_token_source(self, device_ids=None) -> None:
         """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,

@@ -377,8 +377,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         if (p.epi == EPI_F32) {
           float* out = e.out_f32;
           if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
+          // padding rows of a bucketed graph have no output row
+          const int n_rows = e.rows_valid != nullptr ? *e.rows_valid - tok0 : m_valid;
           for (int idx = et; idx < jn * kGemmTileN; idx += 128) {
             const int j = tok_of(idx >> 7), r = idx & 127;
+            if (j >= n_rows) continue;
             float v = tile[j * kGemmTileN + r];
             if (scaled) v *= rs_s[j];
             out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;

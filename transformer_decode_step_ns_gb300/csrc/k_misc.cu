@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
   const int row = p.row0 + blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Token ids and positions are step metadata, complete before the step: read them early.
-  int tok = p.token_ids[row];
+  int tok = (p.rows_valid != nullptr && row >= *p.rows_valid) ? 0 : p.token_ids[row];
   const int pos = p.positions[row];
   if (tid == 0) griddep_launch_dependents();
   griddep_wait();  // the residual/xn rows may still be read by the previous step's tail

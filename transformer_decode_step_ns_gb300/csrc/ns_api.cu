@@ -306,6 +306,7 @@ struct ns_ctx {
   int n_split = 1;
   std::vector<int> split_sizes;
   int attn_budget = 0;
+  std::vector<int> buckets;  // graph batch sizes (ns_set_graph_buckets), ascending
   bool with_lm = true;  // false: the step stops after the last layer (logits_out == NULL)
   const int32_t* tok_src = nullptr;  // device token ids (ns_set_token_source) or null: metadata
   std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
@@ -343,7 +344,7 @@ MetaLayout meta_layout(int B, int MB) {
   m.tab = o; o += static_cast<size_t>(B) * MB * 4;
   o = (o + 15) & ~size_t(15);
   m.logits = o; o += 8;
-  m.flags = o; o += 8;  // int early_ok (see AttnParams), 4 bytes of padding
+  m.flags = o; o += 8;  // int early_ok (see AttnParams), int rows_valid (real rows)
   m.total = o;
   return m;
 }
@@ -438,6 +439,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   const long long* m_slot = reinterpret_cast<const long long*>(h->meta_dev + ml.slot);
   const int* m_tab = reinterpret_cast<const int*>(h->meta_dev + ml.tab);
   const unsigned long long* m_logits = reinterpret_cast<const unsigned long long*>(h->meta_dev + ml.logits);
+  const int* m_rows_valid = reinterpret_cast<const int*>(h->meta_dev + ml.flags) + 1;
   h->kernels_last = 0;
 
   // nano-batches: (row0, rows)
@@ -478,6 +480,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     EmbedParams ep{};
     ep.embed = h->embed;
     ep.token_ids = h->tok_src != nullptr ? h->tok_src : m_tok;
+    ep.rows_valid = m_rows_valid;
     ep.positions = m_pos;
     ep.vocab = c.vocab;
     ep.hidden = H;
@@ -514,7 +517,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.head_dim = d;
       e.n_kv_heads = Hkv;
       e.block_size = h->block_size;
-      e.pool_slots = static_cast<long long>(h->num_blocks) * h->block_size;
+      e.pool_slots = static_cast<long long>(h->num_blocks + 1) * h->block_size;  // + padding block
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
                          st[i % 2], K_QKV));
       if (n > 1) NS_CUDA(cudaEventRecord(h->events[2 + static_cast<size_t>(l) * n + i], st[i % 2]));
@@ -536,7 +539,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.batch = nb[i].second;
       ap.row0 = nb[i].first;
       ap.n_kv_heads = Hkv;
-      ap.num_blocks = h->num_blocks;
+      ap.num_blocks = h->num_blocks + 1;  // + padding block
       ap.block_size = h->block_size;
       ap.scale_log2 = scale_log2;
       ap.max_chunks = h->max_chunks;
@@ -579,6 +582,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   for (int i = 0; i < n && h->with_lm; ++i) {
     EpiArgs el = norm;
     el.out_ptr_slot = m_logits;
+    el.rows_valid = m_rows_valid;
     el.ldo = c.vocab;
     NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el,
                        st[i % 2], K_LM));
@@ -861,9 +865,10 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   if (num_blocks <= 0 || block_size != 16)
     return fail(num_blocks <= 0 ? NS_ERR_INVALID_ARG : NS_ERR_UNSUPPORTED, "num_blocks > 0, block_size 16");
   const ns_model_cfg& c = h->cfg;
-  const size_t pool = static_cast<size_t>(num_blocks) * c.n_kv_heads * block_size * c.head_dim * 2;
+  // one block past the caller's pool takes the rows that pad a batch up to a graph bucket
+  const size_t pool = static_cast<size_t>(num_blocks + 1) * c.n_kv_heads * block_size * c.head_dim * 2;
   NS_CUDA(cudaSetDevice(h->dev));
-  const long long pool_rows = static_cast<long long>(num_blocks) * c.n_kv_heads * block_size;
+  const long long pool_rows = static_cast<long long>(num_blocks + 1) * c.n_kv_heads * block_size;
   if (pool_rows >= (1ll << 31))
     return fail(NS_ERR_UNSUPPORTED, "pool rows (blocks * kv heads * block_size) must fit in int32");
   NS_CUDA(cudaMalloc(&h->pools, pool * 2 * c.n_layers));
@@ -1008,7 +1013,16 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // one packed metadata buffer, one host-to-device copy
   if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
-  const MetaLayout ml = meta_layout(batch, mb);
+  // graph batch: the smallest bucket that holds the rows; padding rows fill the rest
+  const bool graphed = c.use_graphs && !h->timing;
+  int Bg = batch;
+  if (graphed && h->n_split <= 1)
+    for (int v : h->buckets)
+      if (v >= batch) {
+        Bg = v;
+        break;
+      }
+  const MetaLayout ml = meta_layout(Bg, mb);
   uint8_t* mh = h->meta_host;
   if (host_tokens)
     std::memcpy(mh + ml.tok, token_ids, batch * 4);
@@ -1018,24 +1032,48 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   std::memcpy(mh + ml.seq, seq_lens, batch * 4);
   std::memcpy(mh + ml.slot, slot_mapping, batch * 8);
   std::memcpy(mh + ml.tab, block_tables, static_cast<size_t>(batch) * mb * 4);
+  // padding rows: token 0 at position 0 in the padding block (past the caller's pool)
+  const int pad_block = h->num_blocks;
+  for (int b = batch; b < Bg; ++b) {
+    const int32_t zero = 0, one = 1;
+    const int64_t slot = static_cast<int64_t>(pad_block) * bs;
+    std::memcpy(mh + ml.tok + b * 4, &zero, 4);
+    std::memcpy(mh + ml.pos + b * 4, &zero, 4);
+    std::memcpy(mh + ml.seq + b * 4, &one, 4);
+    std::memcpy(mh + ml.slot + b * 8, &slot, 8);
+    int32_t* row = reinterpret_cast<int32_t*>(mh + ml.tab) + static_cast<size_t>(b) * mb;
+    std::memset(row, 0, static_cast<size_t>(mb) * 4);
+    row[0] = pad_block;
+  }
   const unsigned long long lp = reinterpret_cast<unsigned long long>(logits_out);
   std::memcpy(mh + ml.logits, &lp, 8);
-  const int early_ok = early_fetch_ok(h, batch, block_tables, seq_lens, slot_mapping) ? 1 : 0;
-  std::memset(mh + ml.flags, 0, 8);
-  std::memcpy(mh + ml.flags, &early_ok, 4);
+  const int flags[2] = {early_fetch_ok(h, batch, block_tables, seq_lens, slot_mapping) ? 1 : 0,
+                        batch};
+  std::memcpy(mh + ml.flags, flags, 8);
   NS_CUDA(cudaMemcpyAsync(h->meta_dev, mh, ml.total, cudaMemcpyHostToDevice, s));
   NS_CUDA(cudaEventRecord(h->meta_done, s));
   h->meta_pending = true;
   h->with_lm = logits_out != nullptr;
-  if (c.use_graphs && !h->timing) {
+  if (graphed) {
     cudaGraphExec_t ex = nullptr;
-    NS_TRY(get_graph(h, batch, &ex));
+    NS_TRY(get_graph(h, Bg, &ex));
     NS_CUDA(cudaGraphLaunch(ex, s));
   } else {
     NS_TRY(enqueue_step(h, batch, s));
     h->info.kernels_per_step = h->kernels_last;
   }
   h->info.steps++;
+  return NS_OK;
+}
+
+ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (n < 0 || n > 64 || (n > 0 && sizes == nullptr)) return fail(NS_ERR_INVALID_ARG, "bucket count");
+  std::vector<int> v(sizes, sizes + n);
+  for (int i = 0; i < n; ++i)
+    if (v[i] < 1 || v[i] > h->cfg.max_batch || (i > 0 && v[i] <= v[i - 1]))
+      return fail(NS_ERR_INVALID_ARG, "bucket sizes must ascend within [1, max_batch]");
+  h->buckets = v;
   return NS_OK;
 }
 

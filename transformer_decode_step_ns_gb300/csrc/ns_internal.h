@@ -35,6 +35,7 @@ struct EpiArgs {
   float* out_f32;
   long long ldo;
   const unsigned long long* out_ptr_slot;  // when set, the output base is read from here
+  const int* rows_valid;                   // when set, rows at or past *rows_valid are padding
   // EPI_QKV
   void* q_out;
   void* k_pool;
@@ -107,6 +108,7 @@ struct EmbedParams {
   int head_dim;
   const double* inv_freq;  // [head_dim / 2] theta^(-2i/d), fp64
   int batch, row0;
+  const int* rows_valid;  // when set, rows at or past *rows_valid are padding (token 0)
   int* err;
 };
 
