@@ -451,16 +451,18 @@ class NanoLayerWorkload:
         return e0.elapsed_time(e1) / steps
 
     def serial_kernels(self):
-        """Per-kind kernel time of the unsplit step, launched eagerly with an event pair each."""
+        """Per-kind kernel time per step (µs) of the unsplit step, launched eagerly with an event
+        pair around each launch (attention: the decode rows' and the chunk's kernels)."""
         self.dev.set_nanobatch(None)
         self.dev.set_kernel_timing(True)
         self.dev.step(*self.meta, None)
         self.dev.kernel_timing()
-        for _ in range(3):
+        steps = 3
+        for _ in range(steps):
             self.dev.step(*self.meta, None)
         kt = self.dev.kernel_timing()
         self.dev.set_kernel_timing(False)
-        return {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]}
+        return {k: round(v[1] / steps * 1e3, 1) for k, v in kt.items() if v[0]}
 
     def report(self, steps, warmup, peaks):
         from transformer_decode_step_ns_gb300 import _lib

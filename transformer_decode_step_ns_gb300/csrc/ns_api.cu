@@ -307,6 +307,8 @@ struct ns_ctx {
   std::vector<int> split_sizes;
   int attn_budget = 0;
   std::vector<int> buckets;  // graph batch sizes (ns_set_graph_buckets), ascending
+  int chunk_first = 0;       // rows [chunk_first, batch) of the current step form a prefill
+                             // chunk (chunk_first == the step's row count: none)
   bool with_lm = true;  // false: the step stops after the last layer (logits_out == NULL)
   const int32_t* tok_src = nullptr;  // device token ids (ns_set_token_source) or null: metadata
   std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
@@ -547,13 +549,39 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.counters = h->attn_counters;
       ap.err = h->err;
       ap.early_ok = reinterpret_cast<const int*>(h->meta_dev + ml.flags);
-      int grid = std::min(attn_max_grid(h->dtype, d, G, nb[i].second), nb[i].second * Hkv * h->max_chunks);
-      if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
-      {
+      // decode rows of the nano-batch, then the prefill-chunk rows it holds (the chunk is last)
+      const int r_lo = nb[i].first, r_hi = nb[i].first + nb[i].second;
+      const int d_hi = std::min(r_hi, std::max(r_lo, h->chunk_first));
+      if (d_hi > r_lo) {
+        ap.batch = d_hi - r_lo;
+        int grid = std::min(attn_max_grid(h->dtype, d, G, ap.batch), ap.batch * Hkv * h->max_chunks);
+        if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
         TimeScope ts(h, s, K_ATTN);
         NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+        h->kernels_last++;
       }
-      h->kernels_last++;
+      if (r_hi > d_hi) {
+        PrefillParams pp{};
+        pp.q = h->q;
+        pp.q_row_stride = qd;
+        pp.k_pool = h->kpool[l];
+        pp.v_pool = h->vpool[l];
+        pp.block_tables = m_tab;
+        pp.mb = c.max_blocks_per_seq;
+        pp.table_row = B - 1;
+        pp.positions = m_pos;
+        pp.out = h->o;
+        pp.out_row_stride = qd;
+        pp.row0 = d_hi;
+        pp.chunk = r_hi - d_hi;
+        pp.n_kv_heads = Hkv;
+        pp.num_blocks = h->num_blocks + 1;
+        pp.scale_log2 = scale_log2;
+        pp.err = h->err;
+        TimeScope ts(h, s, K_ATTN);
+        NS_CUDA(launch_prefill(pp, h->dtype, d, G, s, true));
+        h->kernels_last++;
+      }
 
       EpiArgs eo{};
       eo.resid = h->resid;
@@ -620,7 +648,8 @@ bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int
 std::vector<int> graph_key(const ns_ctx* h, int B) {
   const uint64_t src = reinterpret_cast<uint64_t>(h->tok_src);
   std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0,
-                     static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32)};
+                     static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
+                     h->chunk_first};
   for (int v : h->split_sizes) k.push_back(v);
   return k;
 }
@@ -1022,6 +1051,22 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
         Bg = v;
         break;
       }
+  // A trailing run of at least kPrefillMinRows rows at consecutive positions that read the same
+  // blocks as the run's last row is a prefill chunk: its attention runs as one causal kernel.
+  int chunk_first = Bg;  // none (the graph batch, so padded steps share their bucket's graph)
+  if (Bg == batch) {
+    const int32_t* tl = block_tables + static_cast<size_t>(batch - 1) * mb;
+    int f = batch - 1;
+    while (f > 0) {
+      const int b = f - 1;
+      if (positions[b] != positions[f] - 1) break;
+      const int need = (seq_lens[b] + bs - 1) / bs;
+      if (std::memcmp(block_tables + static_cast<size_t>(b) * mb, tl, static_cast<size_t>(need) * 4) != 0) break;
+      f = b;
+    }
+    if (batch - f >= kPrefillMinRows) chunk_first = f;
+  }
+  h->chunk_first = chunk_first;
   const MetaLayout ml = meta_layout(Bg, mb);
   uint8_t* mh = h->meta_host;
   if (host_tokens)

@@ -93,6 +93,28 @@ struct AttnParams {
   const int* early_ok;
 };
 
+// Causal attention of a prefill chunk: rows row0 .. row0 + chunk - 1 of the batch are queries at
+// consecutive positions (positions[row0] first) over the block table of row table_row.
+struct PrefillParams {
+  const void* q;
+  long long q_row_stride;
+  const void* k_pool;
+  const void* v_pool;
+  const int* block_tables;
+  int mb;
+  int table_row;        // the chunk row whose table covers every position of the chunk
+  const int* positions;
+  void* out;
+  long long out_row_stride;
+  int row0, chunk, n_kv_heads, num_blocks;
+  float scale_log2;
+  int* err;
+};
+
+// A run of at least this many rows at consecutive positions over one block table at the end of
+// a step is attended as a prefill chunk.
+constexpr int kPrefillMinRows = 16;
+
 struct EmbedParams {
   const void* embed;
   const int* token_ids;
@@ -126,6 +148,8 @@ cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const 
 
 bool attn_supported(int head_dim, int group, int block_size);
 int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
+cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, int group,
+                           cudaStream_t s, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
                         cudaStream_t s, bool pdl);
 // Split of a row of length L (a function of L alone, 16-token blocks): ceil(L / 16) blocks in
