@@ -266,6 +266,30 @@ def test_graph_buckets_pad_batches_and_match_exact_graphs(cuda_lib):
     assert bucket.dev.info().graphs_cached == 2
 
 
+@pytest.mark.parametrize("chunk,p0", [(15, 0), (16, 0), (33, 20)])
+def test_prefill_chunk_threshold_and_offset(cuda_lib, chunk, p0):
+    """A trailing run of 15 rows stays on the decode kernel, 16 or more go to the prefill-chunk
+    kernel (a chunk that continues a prompt at position p0 > 0 reads its cached prefix too);
+    both match the oracle."""
+    shape = _tiny("bf16")
+    dec = [7, 90]
+    ctx = dec + list(range(p0, p0 + chunk))
+    last = len(ctx) - 1
+    shared = list(range(len(dec))) + [last] * chunk
+    _check_step(Harness(shape, 111 + chunk, ctx, shared_table_rows=shared))
+
+
+def test_graph_bucket_arguments_are_validated(cuda_lib):
+    from transformer_decode_step_ns_gb300 import _lib
+    h = Harness(_tiny("bf16"), 121, [3, 5])
+    for bad in ([4, 2], [0, 2], [2, 3]):
+        with pytest.raises(_lib.NSError) as e:
+            h.dev.set_graph_buckets(bad)
+        assert e.value.status == 1
+    h.dev.set_graph_buckets([1, 2])
+    h.dev.set_graph_buckets(None)
+
+
 def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):
     shape = _tiny("f16")
     ctx = [9, 33, 129]
