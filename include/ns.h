@@ -180,9 +180,13 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
  *   block_tables[b][p/bs]*bs + p%bs.
  * logits_out: device, [batch][V] fp32, written; NULL stops the step after the last layer
  * (no final norm, no LM head), for callers that only advance the KV cache or time the layers
- * alone.  Writes this step's K/V into the pools.
- * With use_graphs the first call for a batch size captures a graph (not during a caller's
- * stream capture); later calls replay it.  Returns NOT_INITIALIZED before ns_kv_alloc. */
+ * alone.  Writes this step's K/V into the pools; every row's K/V is written before any row
+ * attends, so rows of one prompt chunk (consecutive positions over one block table) see each
+ * other causally.  A trailing run of at least 16 such rows whose tables agree with the run's
+ * last row is attended by one causal prefill-chunk kernel; other rows by the decode kernel.
+ * With use_graphs the first call for a batch size (or graph bucket) captures a graph (not
+ * during a caller's stream capture); later calls replay it.  Returns NOT_INITIALIZED before
+ * ns_kv_alloc. */
 ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
                          const int32_t* positions, const int32_t* block_tables,
                          const int32_t* seq_lens, const int64_t* slot_mapping,
