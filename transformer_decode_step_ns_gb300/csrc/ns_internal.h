@@ -16,7 +16,8 @@ constexpr int kMaxBN = 256;       // token tile (UMMA N) upper bound
 constexpr int kMaxSplits = 8;     // split-K CTAs per tile = portable cluster size
 constexpr int kAttnSuperBlocks = 64;  // decode attention: rows split into superchunks of <= 64 blocks
 constexpr int kAttnMaxChunks = 64;    // superchunks per row (seq_len <= 65536 with 16-token blocks)
-constexpr int kAttnWarpBlocks = 16;   // blocks one warp handles per superchunk (64 / 4 warps)
+constexpr int kAttnWarpBlocks = 16;   // block ids one warp holds per superchunk (64 / 4 warps at
+                                      // most; 8 at head_dim 64)
 constexpr int kMaxRows = 4096;
 
 enum EpiMode : int {
@@ -153,7 +154,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, int 
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
                         cudaStream_t s, bool pdl);
 // Split of a row of length L (a function of L alone, 16-token blocks): ceil(L / 16) blocks in
-// ceil(blocks / 64) superchunks of ceil(blocks / superchunks) blocks; a CTA's 4 warps share one
+// ceil(blocks / 64) superchunks of ceil(blocks / superchunks) blocks; a CTA's warps share one
 // superchunk.  attn_max_chunks bounds the superchunk count of any L <= L_max.
 __host__ __device__ inline int attn_num_chunks(int L) {
   return L <= 0 ? 0 : ((L + 15) / 16 + kAttnSuperBlocks - 1) / kAttnSuperBlocks;
