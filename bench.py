@@ -625,14 +625,19 @@ KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_
 
 
 def kernel_source_hash(kind):
-    """sha256 (first 16 hex digits) of the kernel's source file and the shared headers."""
+    """sha256 (first 16 hex digits) of the kernel's source file and the shared headers, with
+    comments and whitespace removed (an edit of comments does not change the kernel)."""
     import hashlib
+    import re
     base = kind.split("_cfg")[0]
     csrc = os.path.join(ROOT, "transformer_decode_step_ns_gb300", "csrc")
     h = hashlib.sha256()
     for f in (KERNEL_SOURCE.get(base, "k_gemm.cu"), "ns_ptx.cuh", "ns_internal.h"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
     return h.hexdigest()[:16]
 
 
