@@ -594,6 +594,51 @@ class ContinuousWorkload:
                 "graphs_cached": self.dev.info().graphs_cached,
                 "device_error": self.dev.device_error()}
 
+    def offload(self, steps, peaks, nano):
+        """KV offload: steps with every step's new K/V mirrored to pinned host memory (each
+        layer's rows copied while its attention and FFN run) against the same steps without;
+        then the longest request saved to the host and reloaded into its blocks (contiguous
+        transfer + device scatter), against plain copies of the same bytes."""
+        import torch
+        sh = self.shape
+        row = 2 * sh.n_kv_heads * sh.head_dim
+        mirror = torch.empty((sh.n_layers, self.B, row), dtype=torch.int16).pin_memory()
+        self.dev.set_kv_offload(mirror)
+        on = self.run(steps, peaks, nano)
+        self.dev.set_kv_offload(None)
+        off = self.run(steps, peaks, nano)
+        b = int(np.argmax(self.pos))
+        n = int(self.pos[b])
+        tab = self.tables[b, :int(math.ceil(n / self.bs))].copy()
+        host = torch.empty((sh.n_layers, n, row), dtype=torch.int16).pin_memory()
+        dev_buf = torch.empty_like(host, device="cuda")
+        nbytes = host.numel() * 2
+
+        def timed(fn, reps=5):
+            fn()
+            torch.cuda.synchronize()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            z.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(z) / reps
+
+        save_ms = timed(lambda: self.dev.kv_save(host, n, 0, tab))
+        reload_ms = timed(lambda: self.dev.kv_reload(host, n, 0, tab))  # same bits, same blocks
+        d2h_ms = timed(lambda: host.copy_(dev_buf, non_blocking=True))
+        h2d_ms = timed(lambda: dev_buf.copy_(host, non_blocking=True))
+        return {"mirror_bytes_per_step": sh.n_layers * self.B * row * 2,
+                "ms_per_step_mirror_on": round(on["device_ms_per_step_median"], 3),
+                "ms_per_step_mirror_off": round(off["device_ms_per_step_median"], 3),
+                "request_tokens": n, "request_bytes": nbytes,
+                "save_ms": round(save_ms, 3), "reload_ms": round(reload_ms, 3),
+                "plain_d2h_ms": round(d2h_ms, 3), "plain_h2d_ms": round(h2d_ms, 3),
+                "reload_gbs": round(nbytes / reload_ms * 1e-6, 1),
+                "plain_h2d_gbs": round(nbytes / h2d_ms * 1e-6, 1),
+                "device_error": self.dev.device_error()}
+
     def report(self, steps, peaks):
         # a short comparison of the nano-batch splits, then the full run with the faster one
         trial = {}
@@ -611,6 +656,7 @@ class ContinuousWorkload:
         self.dev.set_kernel_timing(False)
         r["eager_kernel_us"] = {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]}
         r["eager_kernel_launches_per_step"] = {k: v[0] // 3 for k, v in kt.items() if v[0]}
+        r["kv_offload"] = self.offload(30, peaks, best)
         r["workload"] = ("LLaMA-3-8B-shaped 32L bf16, batch 256, ctx U[512,4096], decode lengths "
                          "U[100,1000] with leave/join, greedy argmax fed back, graph replay")
         r["setup_s"] = round(self.setup_s, 1)

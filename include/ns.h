@@ -211,6 +211,42 @@ ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes);
  * token ids.  A graph is captured per source pointer. */
 ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids);
 
+/* KV offload (NanoFlow page, "Runtime details that keep the pipeline fed": K/V go to the host
+ * right after the QKV projection produces them, while they are still contiguous, and the copy
+ * overlaps the FFN).  With host_dst non-NULL, every later ns_decode_step also writes the K (after
+ * RoPE) and V that it stores for row b of layer l into row (l, b) of host_dst, laid out
+ * [n_layers][max_batch][2][n_kv_heads * head_dim] in the model dtype (K first, then V; the same
+ * bits as the cache).  The QKV epilogue stages the rows in a device buffer of that layout and a
+ * copy stream moves each layer's rows to host_dst as soon as that layer's QKV finishes, while its
+ * attention and FFN run; the step's work on its stream completes only after every copy has.
+ * Rows batch .. max_batch-1 are unspecified (graph padding rows land there).  host_dst must be
+ * pinned host memory (cudaMallocHost or cudaHostRegister, else NS_ERR_INVALID_ARG) of at least
+ * bytes = n_layers * max_batch * 2 * n_kv_heads * head_dim * 2 bytes, owned by the caller; each
+ * step overwrites it, so copy a step's rows out before the next step's work starts.  A graph is
+ * captured per destination.  NULL stops the mirroring. */
+ns_status ns_set_kv_offload(ns_handle h, void* host_dst, size_t bytes);
+
+/* KV reload (same page: reloaded K/V land in one contiguous device buffer and only then are
+ * scattered into the fragmented pages, instead of scattering across the host link).
+ * host_src holds the K/V of n_tokens tokens of one request at positions first_pos ..
+ * first_pos + n_tokens - 1, laid out [n_layers][n_tokens][2][n_kv_heads * head_dim] in the model
+ * dtype (the ns_set_kv_offload row layout, one row per token).  They are copied to a contiguous
+ * device buffer held by the handle, then scattered to slot block_table[p / 16] * 16 + p % 16 of
+ * every layer's pools (block_table: host int32 of n_table >= (first_pos + n_tokens - 1) / 16 + 1
+ * ids in [0, num_blocks), else NS_ERR_INVALID_ARG).  Asynchronous on `stream`; host_src must stay
+ * valid until the copy has run when it is pinned (pageable memory is copied before the call
+ * returns).  Calls on one handle share the transfer buffer: order them on one stream, and
+ * before any step that reads the blocks.  The buffer grows to the largest request seen (the
+ * growth synchronises the device).  Returns NOT_INITIALIZED before ns_kv_alloc. */
+ns_status ns_kv_reload(ns_handle h, const void* host_src, int n_tokens, int first_pos,
+                       const int32_t* block_table, int n_table, ns_stream_t stream);
+
+/* The inverse of ns_kv_reload, for a request whose K/V were not mirrored: the tokens' K/V are
+ * gathered from the pages into the contiguous device buffer, then copied to host_dst in the same
+ * [n_layers][n_tokens][2][n_kv_heads * head_dim] layout.  Same arguments, ordering and errors. */
+ns_status ns_kv_save(ns_handle h, void* host_dst, int n_tokens, int first_pos,
+                     const int32_t* block_table, int n_table, ns_stream_t stream);
+
 /* Paged grouped-query decode attention alone (nanoserve notes: the fused paged-attention
  * kernel; grouped-query attention without the expanded K/V copy).  All pointers device:
  *   q [batch][n_q_heads][head_dim]; k_pool, v_pool [num_blocks][n_kv_heads][block_size]

@@ -22,4 +22,4 @@ from .decode import (  # noqa: F401
     greedy_argmax, paged_attention, param_bytes, rms_norm, rope_apply, rope_tables,
     round_storage, silu, slot_of, softmax, swiglu,
 )
-from .kvcache import BlockAllocator  # noqa: F401
+from .kvcache import BlockAllocator, kv_rows, kv_scatter, request_slots  # noqa: F401

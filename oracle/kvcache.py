@@ -71,3 +71,46 @@ class BlockAllocator:
                 block_tables[b, p // bs] = self.free.popleft()
             slots[b] = int(block_tables[b, p // bs]) * bs + p % bs
         return slots
+
+
+# ------------------------------------------------------------------------------------------
+# KV offload rows ("NanoFlow: ..." page, "Runtime details that keep the pipeline fed": K/V
+# leave for the host as contiguous vectors right after the KQV projection; on reload they land
+# contiguously on the device and are then scattered into the fragmented pages).  The row
+# layout is this library's reading (the page gives none): row (layer l, token t) is the K of
+# every kv head of that token, heads in order, then its V, in the cache's storage type.
+# ------------------------------------------------------------------------------------------
+
+def kv_rows(k_pools: List[np.ndarray], v_pools: List[np.ndarray], slots: Iterable[int]) -> np.ndarray:
+    """[n_layers][n][2 * Hkv * d] rows of the tokens at ``slots`` from per-layer pools shaped
+    [num_blocks, Hkv, bs, d], copied element for element (no arithmetic)."""
+    slots = [int(s) for s in slots]
+    L = len(k_pools)
+    _, hkv, bs, d = k_pools[0].shape
+    out = np.empty((L, len(slots), 2 * hkv * d), dtype=k_pools[0].dtype)
+    for l in range(L):
+        for t, s in enumerate(slots):
+            blk, off = s // bs, s % bs
+            for h in range(hkv):
+                out[l, t, h * d:(h + 1) * d] = k_pools[l][blk, h, off, :]
+                out[l, t, (hkv + h) * d:(hkv + h + 1) * d] = v_pools[l][blk, h, off, :]
+    return out
+
+
+def kv_scatter(k_pools: List[np.ndarray], v_pools: List[np.ndarray], rows: np.ndarray,
+               slots: Iterable[int]) -> None:
+    """Inverse of ``kv_rows``: write row (l, t) into every layer's pools at slots[t], in place."""
+    slots = [int(s) for s in slots]
+    _, hkv, bs, d = k_pools[0].shape
+    for l in range(len(k_pools)):
+        for t, s in enumerate(slots):
+            blk, off = s // bs, s % bs
+            for h in range(hkv):
+                k_pools[l][blk, h, off, :] = rows[l, t, h * d:(h + 1) * d]
+                v_pools[l][blk, h, off, :] = rows[l, t, (hkv + h) * d:(hkv + h + 1) * d]
+
+
+def request_slots(block_table_row: np.ndarray, first_pos: int, n_tokens: int, block_size: int) -> np.ndarray:
+    """Slots of positions first_pos .. first_pos + n_tokens - 1 through one block-table row."""
+    return np.array([int(block_table_row[p // block_size]) * block_size + p % block_size
+                     for p in range(first_pos, first_pos + n_tokens)], dtype=np.int64)

@@ -66,6 +66,47 @@ def test_allocator_model_never_hands_out_a_block_twice():
 # ------------------------------------------------------------------ roofline arithmetic
 
 
+def test_kv_rows_layout_closed_form():
+    """Every pool element holds its own flat index, so the row element at (l, t, c) must be the
+    index of (block, head, offset, dim) that the row layout names: K heads first, then V."""
+    L, nb, hkv, bs, d = 2, 5, 3, 4, 8
+    base = np.arange(nb * hkv * bs * d, dtype=np.float64).reshape(nb, hkv, bs, d)
+    kp = [base + 1e6 * l for l in range(L)]
+    vp = [base + 1e6 * l + 5e5 for l in range(L)]
+    slots = [17, 0, 9, 19]
+    rows = oracle.kv_rows(kp, vp, slots)
+    assert rows.shape == (L, len(slots), 2 * hkv * d)
+    for l in range(L):
+        for t, s in enumerate(slots):
+            blk, off = divmod(s, bs)
+            for c in range(2 * hkv * d):
+                kv, col = divmod(c, hkv * d)
+                h, i = divmod(col, d)
+                want = ((blk * hkv + h) * bs + off) * d + i + 1e6 * l + 5e5 * kv
+                assert rows[l, t, c] == want
+
+
+def test_kv_scatter_inverts_kv_rows_and_touches_only_its_slots():
+    rng = np.random.default_rng(7)
+    L, nb, hkv, bs, d = 3, 6, 2, 4, 16
+    slots = rng.permutation(nb * bs)[:9]
+    rows = rng.standard_normal((L, len(slots), 2 * hkv * d))
+    kp = [np.zeros((nb, hkv, bs, d)) for _ in range(L)]
+    vp = [np.zeros((nb, hkv, bs, d)) for _ in range(L)]
+    oracle.kv_scatter(kp, vp, rows, slots)
+    np.testing.assert_array_equal(oracle.kv_rows(kp, vp, slots), rows)
+    for l in range(L):
+        # each slot's 2 * hkv * d elements, and nothing else, became nonzero
+        assert np.count_nonzero(kp[l]) + np.count_nonzero(vp[l]) == len(slots) * 2 * hkv * d
+
+
+def test_request_slots_by_hand():
+    # table [5, 2, 9], block size 4, positions 3..8: block 5 offset 3, block 2 offsets 0..3,
+    # block 9 offset 0
+    got = oracle.request_slots(np.array([5, 2, 9]), 3, 6, 4)
+    np.testing.assert_array_equal(got, [23, 8, 9, 10, 11, 36])
+
+
 def test_bandwidth_floor_matches_nanoserve():
     g = GOLDEN["nanoserve_bandwidth_floor_ms"]
     nbytes = g["bytes_mib"] * 2 ** 20

@@ -34,7 +34,7 @@ SYMBOLS = (
     "ns_pool_destroy", "ns_pool_prepare_step", "ns_pool_reserve", "ns_pool_release",
     "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
     "ns_get_kernel_timing", "ns_attn_decode_noalloc", "ns_set_token_source",
-    "ns_set_graph_buckets",
+    "ns_set_graph_buckets", "ns_set_kv_offload", "ns_kv_reload", "ns_kv_save",
 )
 
 
@@ -119,6 +119,9 @@ def lib() -> ctypes.CDLL:
             "ns_set_kernel_timing": ([P, I], I),
             "ns_set_token_source": ([P, P], I),
             "ns_set_graph_buckets": ([P, I, P], I),
+            "ns_set_kv_offload": ([P, P, ctypes.c_size_t], I),
+            "ns_kv_reload": ([P, P, I, I, P, I, P], I),
+            "ns_kv_save": ([P, P, I, I, P, I, P], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
@@ -310,6 +313,36 @@ class DecodeStep:
         """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,
         from the host arrays passed to ``step``."""
         check(lib().ns_set_token_source(self.h, _ptr(device_ids)))
+
+    def kv_row_elems(self) -> int:
+        """Elements of one (layer, token) K/V row of the offload layout: K then V."""
+        return 2 * self.shape.n_kv_heads * self.shape.head_dim
+
+    def set_kv_offload(self, host_buf=None) -> None:
+        """Mirror each step's new K/V into ``host_buf``, pinned host memory of
+        [n_layers][max_batch][kv_row_elems] storage-dtype elements (e.g. a pinned torch tensor),
+        or stop with None."""
+        if host_buf is None:
+            check(lib().ns_set_kv_offload(self.h, None, 0))
+            return
+        nbytes = host_buf.numel() * host_buf.element_size() if hasattr(host_buf, "numel") else host_buf.nbytes
+        check(lib().ns_set_kv_offload(self.h, _ptr(host_buf), nbytes))
+
+    def _kv_transfer(self, fn, buf, n_tokens: int, first_pos: int, block_table, stream) -> None:
+        tab = np.ascontiguousarray(block_table, dtype=np.int32)
+        nbytes = buf.numel() * buf.element_size() if hasattr(buf, "numel") else buf.nbytes
+        if nbytes < self.shape.n_layers * n_tokens * self.kv_row_elems() * 2:
+            raise ValueError("buffer smaller than [n_layers][n_tokens][kv_row_elems]")
+        check(fn(self.h, _ptr(buf), n_tokens, first_pos, _ptr(tab), tab.size, _stream(stream)))
+
+    def kv_reload(self, host_src, n_tokens: int, first_pos: int, block_table, stream=None) -> None:
+        """Scatter [n_layers][n_tokens][kv_row_elems] host K/V rows of positions first_pos..
+        into the pages of ``block_table``."""
+        self._kv_transfer(lib().ns_kv_reload, host_src, n_tokens, first_pos, block_table, stream)
+
+    def kv_save(self, host_dst, n_tokens: int, first_pos: int, block_table, stream=None) -> None:
+        """Gather the K/V of positions first_pos.. of ``block_table`` into host rows."""
+        self._kv_transfer(lib().ns_kv_save, host_dst, n_tokens, first_pos, block_table, stream)
 
     def set_kernel_timing(self, on: bool) -> None:
         check(lib().ns_set_kernel_timing(self.h, 1 if on else 0))

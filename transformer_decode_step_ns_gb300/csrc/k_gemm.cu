@@ -417,8 +417,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                   return;
                 }
                 const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
-                kp[base + i] = Cvt<T>::from_f(y_lo);
-                kp[base + i + half] = Cvt<T>::from_f(y_hi);
+                const T k_lo = Cvt<T>::from_f(y_lo), k_hi = Cvt<T>::from_f(y_hi);
+                kp[base + i] = k_lo;
+                kp[base + i + half] = k_hi;
+                if (e.kv_stage != nullptr) {
+                  T* st = reinterpret_cast<T*>(e.kv_stage) + static_cast<size_t>(tok) * 2 * e.kv_dim +
+                          (n0 - e.q_dim);
+                  st[r_lo] = k_lo;
+                  st[r_hi] = k_hi;
+                }
               }
             };
             if (use_pf) {
@@ -459,8 +466,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 set_err(p.err, NS_DEV_BAD_SLOT);
                 return;
               }
-              const float v = tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f);
-              vp[kv_base(slot, kvh) + dim] = Cvt<T>::from_f(v);
+              const T v = Cvt<T>::from_f(tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f));
+              vp[kv_base(slot, kvh) + dim] = v;
+              if (e.kv_stage != nullptr)
+                reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok0 + j) * 2 * e.kv_dim + e.kv_dim + col] = v;
             };
             if (use_pf) {
 #pragma unroll

@@ -144,6 +144,48 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int v
   cluster_sync();  // every slice stays resident until rank 0 has read it
 }
 
+// KV offload and reload (NanoFlow, "Runtime details that keep the pipeline fed"): K/V travel to
+// and from the host as contiguous rows, and only on the device are they scattered into (or
+// gathered from) the fragmented pages.  A thread moves 16 bytes: 8 elements of one head of one
+// token, consecutive threads consecutive 16-byte pieces of a row, so both sides are coalesced
+// (a head's d elements are contiguous in a page).  Grid-stride over every piece.
+__global__ void __launch_bounds__(256) kv_copy_kernel(const KvCopyParams p) {
+  const int kvd = p.n_kv_heads * p.head_dim;
+  const int per_row = kvd / 4;  // 16-byte pieces of a (layer, token) row of 2 * kvd elements
+  const long long total = static_cast<long long>(p.n_layers) * p.n * per_row;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += stride) {
+    const long long r = u / per_row;
+    const int c = static_cast<int>(u - r * per_row) * 8;  // element within the row
+    const int l = static_cast<int>(r / p.n), t = static_cast<int>(r - static_cast<long long>(l) * p.n);
+    const int kv = c >= kvd ? 1 : 0, col = c - kv * kvd;
+    const int kvh = col / p.head_dim, dim = col - kvh * p.head_dim;
+    const long long slot = p.slots[t];
+    if (slot < 0 || slot >= p.pool_slots) {
+      if (dim == 0) atomicCAS(p.err, 0, NS_DEV_BAD_SLOT);
+      continue;
+    }
+    const size_t page = ((static_cast<size_t>(slot / p.block_size) * p.n_kv_heads + kvh) * p.block_size +
+                         static_cast<size_t>(slot % p.block_size)) * p.head_dim + dim;
+    uint4* pool = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.pools) +
+                                           p.pool_bytes * (2 * static_cast<size_t>(l) + kv) + page * 2);
+    uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.buf) +
+                                          (static_cast<size_t>(r) * 2 * kvd + c) * 2);
+    if (p.to_pool) *pool = *row;
+    else *row = *pool;
+  }
+}
+
+cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s) {
+  const long long pieces = static_cast<long long>(p.n_layers) * p.n * (p.n_kv_heads * p.head_dim / 4);
+  if (pieces <= 0) return cudaSuccess;
+  // up to eight 256-thread CTAs per SM, a whole number of waves when the copy is large
+  const long long need = (pieces + 255) / 256;
+  const int grid = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
+  kv_copy_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.batch, 1, 1);

@@ -314,6 +314,16 @@ struct ns_ctx {
   std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
   cudaStream_t side = nullptr, cap = nullptr;
   std::vector<cudaEvent_t> events;
+  // KV offload: each step's new K/V rows, staged on the device by the QKV epilogues and copied
+  // on `copy` to the caller's pinned mirror [n_layers][R][2][kv_dim] (ns_set_kv_offload)
+  void* kv_host = nullptr;
+  void* kv_stage = nullptr;
+  cudaStream_t copy = nullptr;
+  // contiguous device buffer and slots of ns_kv_reload / ns_kv_save (grown on demand)
+  void* kv_xfer = nullptr;
+  size_t kv_xfer_cap = 0;
+  long long* kv_slots = nullptr;
+  size_t kv_slots_cap = 0;
   // graphs
   std::map<std::vector<int>, cudaGraphExec_t> graphs;
   int* err = nullptr;
@@ -457,8 +467,11 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   }
   const int n = static_cast<int>(nb.size());
   cudaStream_t st[2] = {s0, h->side};
-  // events: fork, join, and per (layer, nano-batch) QKV completion
-  const size_t need_ev = 2 + static_cast<size_t>(c.n_layers) * n;
+  // events: fork, side-stream join, copy-stream join, and per (layer, nano-batch) QKV completion
+  const bool mirror = h->kv_host != nullptr;
+  const size_t kv_row_bytes = static_cast<size_t>(2) * kvd * 2;
+  auto ev_qkv = [&](int l, int i) { return h->events[3 + static_cast<size_t>(l) * n + i]; };
+  const size_t need_ev = 3 + static_cast<size_t>(c.n_layers) * n;
   while (h->events.size() < need_ev) {
     cudaEvent_t ev;
     NS_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
@@ -520,14 +533,25 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.n_kv_heads = Hkv;
       e.block_size = h->block_size;
       e.pool_slots = static_cast<long long>(h->num_blocks + 1) * h->block_size;  // + padding block
+      e.kv_stage = mirror ? static_cast<uint8_t*>(h->kv_stage) + static_cast<size_t>(l) * h->R * kv_row_bytes
+                          : nullptr;
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
                          st[i % 2], K_QKV));
-      if (n > 1) NS_CUDA(cudaEventRecord(h->events[2 + static_cast<size_t>(l) * n + i], st[i % 2]));
+      if (n > 1 || mirror) NS_CUDA(cudaEventRecord(ev_qkv(l, i), st[i % 2]));
+      if (mirror) {
+        // the rows' K/V leave for the host while attention and the FFN of this layer run
+        NS_CUDA(cudaStreamWaitEvent(h->copy, ev_qkv(l, i), 0));
+        const size_t off = (static_cast<size_t>(l) * h->R + nb[i].first) * kv_row_bytes;
+        NS_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(h->kv_host) + off,
+                                static_cast<uint8_t*>(h->kv_stage) + off,
+                                static_cast<size_t>(nb[i].second) * kv_row_bytes, cudaMemcpyDeviceToHost,
+                                h->copy));
+      }
     }
     for (int i = 0; i < n; ++i) {
       cudaStream_t s = st[i % 2];
       for (int j = 0; j < i; ++j)
-        if ((j % 2) != (i % 2)) NS_CUDA(cudaStreamWaitEvent(s, h->events[2 + static_cast<size_t>(l) * n + j], 0));
+        if ((j % 2) != (i % 2)) NS_CUDA(cudaStreamWaitEvent(s, ev_qkv(l, j), 0));
       AttnParams ap{};
       ap.q = h->q;
       ap.q_row_stride = qd;
@@ -619,6 +643,10 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     NS_CUDA(cudaEventRecord(h->events[1], h->side));
     NS_CUDA(cudaStreamWaitEvent(s0, h->events[1], 0));
   }
+  if (mirror) {  // the step completes when its K/V are on the host
+    NS_CUDA(cudaEventRecord(h->events[2], h->copy));
+    NS_CUDA(cudaStreamWaitEvent(s0, h->events[2], 0));
+  }
   return NS_OK;
 }
 
@@ -647,9 +675,10 @@ bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int
 
 std::vector<int> graph_key(const ns_ctx* h, int B) {
   const uint64_t src = reinterpret_cast<uint64_t>(h->tok_src);
+  const uint64_t kvh = reinterpret_cast<uint64_t>(h->kv_host);
   std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0,
                      static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
-                     h->chunk_first};
+                     h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32)};
   for (int v : h->split_sizes) k.push_back(v);
   return k;
 }
@@ -759,6 +788,10 @@ void ns_destroy(ns_handle h) {
   for (auto ev : h->events) cudaEventDestroy(ev);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->cap) cudaStreamDestroy(h->cap);
+  if (h->copy) cudaStreamDestroy(h->copy);
+  cudaFree(h->kv_stage);
+  cudaFree(h->kv_xfer);
+  cudaFree(h->kv_slots);
   delete h;
   cudaSetDevice(prev);
 }
@@ -1125,6 +1158,117 @@ ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes) {
 ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids) {
   if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
   h->tok_src = device_token_ids;
+  return NS_OK;
+}
+
+ns_status ns_set_kv_offload(ns_handle h, void* host_dst, size_t bytes) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (host_dst == nullptr) {
+    h->kv_host = nullptr;
+    return NS_OK;
+  }
+  const ns_model_cfg& c = h->cfg;
+  const size_t need = static_cast<size_t>(c.n_layers) * h->R * 2 * c.n_kv_heads * c.head_dim * 2;
+  if (bytes < need) return fail(NS_ERR_INVALID_ARG, "host buffer smaller than n_layers * max_batch * 2 * kv_dim elements");
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host_dst) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(NS_ERR_INVALID_ARG, "host_dst must be pinned host memory (cudaMallocHost / cudaHostRegister)");
+  }
+  NS_CUDA(cudaSetDevice(h->dev));
+  if (h->kv_stage == nullptr) {
+    NS_CUDA(cudaMalloc(&h->kv_stage, need));
+    NS_CUDA(cudaMemset(h->kv_stage, 0, need));
+  }
+  if (h->copy == nullptr) NS_CUDA(cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking));
+  h->kv_host = host_dst;
+  return NS_OK;
+}
+
+namespace {
+
+// Slots of tokens first_pos .. first_pos + n - 1 of one request, uploaded to the handle's slot
+// buffer on `s`, and the contiguous transfer buffer grown to `bytes`.
+ns_status kv_transfer_setup(ns_ctx* h, int n_tokens, int first_pos, const int32_t* block_table, int n_table,
+                            size_t bytes, cudaStream_t s) {
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  if (n_tokens < 1 || first_pos < 0 || block_table == nullptr || n_table < 1)
+    return fail(NS_ERR_INVALID_ARG, "n_tokens >= 1, first_pos >= 0, a block table");
+  const int bs = h->block_size;
+  const long long last = static_cast<long long>(first_pos) + n_tokens - 1;
+  if (last / bs >= n_table) return fail(NS_ERR_INVALID_ARG, "block table shorter than the token range");
+  std::vector<long long> slots(n_tokens);
+  for (int t = 0; t < n_tokens; ++t) {
+    const long long pos = static_cast<long long>(first_pos) + t;
+    const int b = block_table[pos / bs];
+    if (b < 0 || b >= h->num_blocks) return fail(NS_ERR_INVALID_ARG, "block id out of range");
+    slots[t] = static_cast<long long>(b) * bs + pos % bs;
+  }
+  NS_CUDA(cudaSetDevice(h->dev));
+  if (h->kv_xfer_cap < bytes || h->kv_slots_cap < slots.size() * sizeof(long long)) {
+    NS_CUDA(cudaDeviceSynchronize());  // earlier transfers may still use the old buffers
+    if (h->kv_xfer_cap < bytes) {
+      cudaFree(h->kv_xfer);
+      h->kv_xfer = nullptr;
+      h->kv_xfer_cap = 0;
+      NS_CUDA(cudaMalloc(&h->kv_xfer, bytes));
+      h->kv_xfer_cap = bytes;
+    }
+    if (h->kv_slots_cap < slots.size() * sizeof(long long)) {
+      cudaFree(h->kv_slots);
+      h->kv_slots = nullptr;
+      h->kv_slots_cap = 0;
+      NS_CUDA(cudaMalloc(&h->kv_slots, slots.size() * sizeof(long long)));
+      h->kv_slots_cap = slots.size() * sizeof(long long);
+    }
+  }
+  // pageable source: the call returns once the slots are staged, so `slots` may go
+  NS_CUDA(cudaMemcpyAsync(h->kv_slots, slots.data(), slots.size() * sizeof(long long),
+                          cudaMemcpyHostToDevice, s));
+  return NS_OK;
+}
+
+KvCopyParams kv_copy_params(ns_ctx* h, int n_tokens, int to_pool) {
+  const ns_model_cfg& c = h->cfg;
+  KvCopyParams p{};
+  p.pools = h->pools;
+  p.pool_bytes = static_cast<size_t>(h->num_blocks + 1) * c.n_kv_heads * h->block_size * c.head_dim * 2;
+  p.buf = h->kv_xfer;
+  p.slots = h->kv_slots;
+  p.n = n_tokens;
+  p.n_layers = c.n_layers;
+  p.n_kv_heads = c.n_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = h->block_size;
+  p.pool_slots = static_cast<long long>(h->num_blocks) * h->block_size;
+  p.to_pool = to_pool;
+  p.err = h->err;
+  return p;
+}
+
+}  // namespace
+
+ns_status ns_kv_reload(ns_handle h, const void* host_src, int n_tokens, int first_pos, const int32_t* block_table,
+                       int n_table, ns_stream_t stream) {
+  if (h == nullptr || host_src == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  const ns_model_cfg& c = h->cfg;
+  const size_t bytes = static_cast<size_t>(c.n_layers) * n_tokens * 2 * c.n_kv_heads * c.head_dim * 2;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  NS_TRY(kv_transfer_setup(h, n_tokens, first_pos, block_table, n_table, bytes, s));
+  NS_CUDA(cudaMemcpyAsync(h->kv_xfer, host_src, bytes, cudaMemcpyHostToDevice, s));
+  NS_CUDA(launch_kv_copy(kv_copy_params(h, n_tokens, 1), h->sms, s));
+  return NS_OK;
+}
+
+ns_status ns_kv_save(ns_handle h, void* host_dst, int n_tokens, int first_pos, const int32_t* block_table,
+                     int n_table, ns_stream_t stream) {
+  if (h == nullptr || host_dst == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  const ns_model_cfg& c = h->cfg;
+  const size_t bytes = static_cast<size_t>(c.n_layers) * n_tokens * 2 * c.n_kv_heads * c.head_dim * 2;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  NS_TRY(kv_transfer_setup(h, n_tokens, first_pos, block_table, n_table, bytes, s));
+  NS_CUDA(launch_kv_copy(kv_copy_params(h, n_tokens, 0), h->sms, s));
+  NS_CUDA(cudaMemcpyAsync(host_dst, h->kv_xfer, bytes, cudaMemcpyDeviceToHost, s));
   return NS_OK;
 }
 

@@ -46,6 +46,7 @@ struct EpiArgs {
   const float* rope_sin;
   int q_dim, kv_dim, head_dim, n_kv_heads, block_size;
   long long pool_slots;
+  void* kv_stage;  // when set, row `tok` of [rows][2][kv_dim] also receives the K and V it writes
   // EPI_RESID
   float* resid;
   void* xn_out;
@@ -177,6 +178,20 @@ __host__ __device__ inline int attn_max_chunks(int L_max) {
 void set_last_error(const char* msg);
 
 cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
+
+// Copy between the paged pools and a contiguous buffer [n_layers][n][2][kv_dim] whose row
+// (layer, t) holds the K then V of the token at slot slots[t] (see ns_kv_reload / ns_kv_save).
+struct KvCopyParams {
+  void* pools;              // 2 * n_layers pools of pool_bytes: K of layer l at 2l, V at 2l + 1
+  size_t pool_bytes;
+  void* buf;                // contiguous rows, 16-byte aligned
+  const long long* slots;   // [n], device
+  int n, n_layers, n_kv_heads, head_dim, block_size;
+  long long pool_slots;     // slots at or past this are refused (error flag, no access)
+  int to_pool;              // 1: buf -> pages, 0: pages -> buf
+  int* err;
+};
+cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s);
 cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
                           cudaStream_t s);
 
