@@ -140,6 +140,76 @@ ns_status ns_pool_prepare_step(ns_pool p, int batch, const int32_t* positions,
 ns_status ns_pool_reserve(ns_pool p, int n, int32_t* out_ids);
 ns_status ns_pool_release(ns_pool p, const int32_t* block_ids, int n);
 ns_status ns_pool_free_count(ns_pool p, int* n_free);
+ns_status ns_pool_geometry(ns_pool p, int* num_blocks, int* block_size);
+
+/* The pool a handle's KV cache allocates from (after ns_kv_alloc), for the batch former below.
+ * Borrowed: it lives as long as the handle; never pass it to ns_pool_destroy. */
+ns_status ns_kv_get_pool(ns_handle h, ns_pool* out);
+
+/* Constant-dense-batch former (NanoFlow page, "Runtime details that keep the pipeline fed": the
+ * scheduler keeps the batch at the size the overlap schedule was tuned for by taking the
+ * unfinished decode requests first and topping up with prefill chunks cut at token
+ * granularity; requests that exceed their predicted peak memory go to the host and are
+ * reloaded later, never recomputed).  Host only; no GPU needed.  Each step:
+ *   ns_sched_next fills the metadata of ns_decode_step for at most dense_tokens rows:
+ *   1. while the decode rows of the first dense_tokens running requests need more new blocks
+ *      than are free, the last running request is preempted: a save move lists its cached
+ *      tokens (positions 0 .. prompt_len + generated - 2) and its blocks, the blocks return to
+ *      the pool, and it waits;
+ *   2. in a step that preempted nothing, waiting preempted requests resume, first in first out,
+ *      while the free blocks (after this step's decode blocks) hold the blocks of their cached
+ *      tokens and of their next position: a reload move lists the new blocks, and the request
+ *      runs again (last in the running order);
+ *   3. one decode row per running request, in running order (prompt completion order, resumed
+ *      requests appended), at most dense_tokens; a decode row's token is the request's last
+ *      sampled token at position prompt_len + generated - 1;
+ *   4. prompts in arrival order, each adding its next min(room, remaining) tokens as
+ *      consecutive positions over its own block table, cut to what the free blocks hold; a
+ *      prompt starts only when the free blocks cover its predicted peak -- the blocks of its
+ *      first prompt_len + min(max_new_tokens, predicted_new_tokens) - 1 positions
+ *      (predicted_new_tokens 0: max_new_tokens) -- plus what the requests holding blocks still
+ *      need to reach their predicted peaks and what the preempted ones need to resume; the fill
+ *      stops at the first prompt that gets no row.
+ *   Blocks are reserved as positions cross block boundaries, in row order.  seq_lens =
+ *   positions + 1; every chunk row carries its request's whole block table, so a prompt's rows
+ *   see one another causally within the step (ns_decode_step).  Arrays are host memory of
+ *   dense_tokens rows (block_tables [dense_tokens][max_blocks_per_seq]); row_request[b] is the
+ *   request of row b and row_samples[b] = 1 where the row yields a token (decode rows and a
+ *   prompt's last row).  *batch may be 0 (nothing to run).
+ *   ns_sched_moves lists the step's moves, saves first: the caller performs them in that order
+ *   on the step's stream before ns_decode_step (ns_kv_save of kind 0 into its own host store,
+ *   ns_kv_reload of kind 1 from it; a reload's blocks may be blocks a save of the same step
+ *   released, which stream order makes safe).
+ *   ns_sched_commit then takes the step's sampled tokens (sampled[b], read where
+ *   row_samples[b] = 1): a request whose prompt completed starts running, a request that
+ *   samples eos_token or reaches max_new_tokens finishes, its blocks return to the pool in
+ *   table order, and its id is written to finished_ids (capacity >= batch, or NULL).  A
+ *   second ns_sched_next before the commit returns INVALID_ARG.
+ * With predicted_new_tokens 0 every admitted request's peak is reserved, so nothing is ever
+ * preempted. */
+typedef struct ns_sched_st* ns_sched;
+ns_status ns_sched_create(ns_pool pool, int dense_tokens, int max_blocks_per_seq, int eos_token,
+                          int predicted_new_tokens, ns_sched* out);
+void ns_sched_destroy(ns_sched s);
+/* prompt: host, prompt_len >= 1 token ids (copied); prompt_len + max_new_tokens at most
+ * max_blocks_per_seq * block_size, and its blocks at most the pool's; ids are unique and
+ * non-negative. */
+ns_status ns_sched_add(ns_sched s, int request_id, const int32_t* prompt, int prompt_len,
+                       int max_new_tokens);
+ns_status ns_sched_next(ns_sched s, int32_t* token_ids, int32_t* positions, int32_t* block_tables,
+                        int32_t* seq_lens, int64_t* slot_mapping, int32_t* row_request,
+                        int32_t* row_samples, int* batch);
+/* The formed step's moves: *n = their count, the first min(*n, capacity) written (tables:
+ * [capacity][max_blocks_per_seq], the request's blocks in table order, zero-padded). */
+ns_status ns_sched_moves(ns_sched s, int32_t* kinds, int32_t* request_ids, int32_t* n_tokens,
+                         int32_t* tables, int capacity, int* n);
+ns_status ns_sched_commit(ns_sched s, const int32_t* sampled, int batch, int32_t* finished_ids,
+                          int* n_finished);
+/* Tokens generated so far by a request (running, preempted or finished): *n = their count, the
+ * first min(*n, capacity) copied to out. */
+ns_status ns_sched_tokens(ns_sched s, int request_id, int32_t* out, int capacity, int* n);
+/* Requests with prompt tokens left, running, preempted, finished. */
+ns_status ns_sched_counts(ns_sched s, int* waiting, int* running, int* preempted, int* finished);
 
 /* Host validation of one step's metadata, exactly as ns_decode_step performs it before
  * anything is launched: 1 <= batch <= max_batch; token ids in [0, vocab); positions >= 0;

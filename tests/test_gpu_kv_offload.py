@@ -144,3 +144,73 @@ def test_offload_and_reload_arguments_are_validated(cuda_lib):
         assert e.value.status == 1
     h.dev.kv_save(rows, 4, 0, [1])
     assert h.dev.device_error() == 0
+
+
+def test_dense_batch_former_with_preemption_matches_the_oracle(cuda_lib):
+    """Six prompts through the dense-batch former on a pool too small for their peaks
+    (predicted decode length 1): prompts are chunked to fill each step, running requests are
+    preempted (K/V saved to the host) and resumed (reloaded into other blocks).  Every
+    generated token's logits equal, within the logits tolerance, the oracle run over that
+    request alone (its prompt and generated tokens at positions 0 .. n-1)."""
+    import torch
+    import synth
+    from transformer_decode_step_ns_gb300 import _lib
+    from helpers import rel_l2
+    shape = _tiny("bf16")
+    bs, D, mb = 16, 24, 8
+    w = synth.model_weights(shape, 151, gamma_std=0.1)
+    dev = _lib.DecodeStep(shape, w, D, mb, use_graphs=False)
+    dev.kv_alloc(12, bs)
+    former = _lib.BatchFormer(dev.pool(), D, mb, eos_token=-1, predicted_new_tokens=1)
+    rng = np.random.default_rng(151)
+    prompts = {rid: rng.integers(0, shape.vocab, size=n).astype(np.int32)
+               for rid, n in enumerate([40, 7, 23, 16, 31, 5])}
+    for rid, p in prompts.items():
+        former.add(rid, p, 12)
+    store, got, saves, steps = {}, {rid: [] for rid in prompts}, 0, 0
+    ids = torch.empty(D, dtype=torch.int32, device="cuda")
+    while former.counts()[3] < len(prompts):
+        steps += 1
+        assert steps < 200
+        rows = former.next()
+        for kind, rid, n, table in former.moves():
+            if kind == 0:
+                store[rid] = np.zeros((shape.n_layers, n, dev.kv_row_elems()), dtype=np.uint16)
+                dev.kv_save(store[rid], n, 0, table)
+                saves += 1
+            else:
+                dev.kv_reload(store.pop(rid), n, 0, table)
+        B = len(rows["token_ids"])
+        assert B > 0
+        logits = torch.empty((B, shape.vocab), dtype=torch.float32, device="cuda")
+        dev.step(rows["token_ids"], rows["positions"], rows["block_tables"], rows["seq_lens"],
+                 rows["slot_mapping"], logits)
+        _lib.greedy_argmax(logits, ids[:B])
+        torch.cuda.synchronize()
+        assert dev.device_error() == 0
+        lg = logits.cpu().numpy().astype(np.float64)
+        for b in np.nonzero(rows["row_samples"])[0]:
+            got[int(rows["row_request"][b])].append(lg[b])
+        former.commit(ids[:B].cpu().numpy())
+    assert saves > 0  # the pool forced preemption
+    model = oracle.OracleModel.from_weights(shape, w)
+    for rid, prompt in prompts.items():
+        gen = former.tokens(rid)
+        assert len(gen) == 12
+        seq = np.concatenate([prompt, np.array(gen[:-1], dtype=np.int32)])
+        T = len(seq)
+        nblk = math.ceil(T / bs)
+        pool_shape = (nblk, shape.n_kv_heads, bs, shape.head_dim)
+        kp = [np.zeros(pool_shape, dtype=np.uint16) for _ in range(shape.n_layers)]
+        vp = [np.zeros(pool_shape, dtype=np.uint16) for _ in range(shape.n_layers)]
+        tab = np.tile(np.arange(mb, dtype=np.int32), (T, 1))
+        pos = np.arange(T, dtype=np.int32)
+        ref = oracle.decode_step(model, kp, vp, seq, pos, tab, pos + 1, pos.astype(np.int64), bs)
+        ref = ref[len(prompt) - 1:]
+        mine = np.stack(got[rid])
+        assert mine.shape == ref.shape
+        for i in range(len(ref)):
+            assert rel_l2(mine[i], ref[i]) < 1e-2, (rid, i, rel_l2(mine[i], ref[i]))
+            assert np.abs(mine[i] - ref[i]).max() < 5e-2, (rid, i)
+        # greedy: each generated token is the argmax of the logits that produced it
+        np.testing.assert_array_equal(np.argmax(mine, axis=1), gen)

@@ -1,0 +1,278 @@
+"""The constant-dense-batch former (NanoFlow page, "Runtime details that keep the pipeline fed"):
+the plain Python model is pinned by a worked example and by invariants over random runs; the
+library's C++ former must reproduce the model bit for bit."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle.kvcache import BlockAllocator
+from oracle.scheduler import DenseBatchFormer, SchedulerError
+
+KEYS = ("token_ids", "positions", "block_tables", "seq_lens", "slot_mapping", "row_request",
+        "row_samples")
+
+
+def _rows(st):
+    return {k: getattr(st, k) for k in KEYS}
+
+
+def test_worked_example_by_hand():
+    """Dense target 8, block size 4: prompt A (5 tokens, 3 new) and B (6 tokens, 2 new)."""
+    m = DenseBatchFormer(BlockAllocator(16, 4), dense_tokens=8, max_blocks_per_seq=4, eos_token=999)
+    A, B = 7, 3
+    m.add(A, [10, 11, 12, 13, 14], 3)
+    m.add(B, [20, 21, 22, 23, 24, 25], 2)
+    # step 1: A's whole prompt (blocks 0, 1), then 3 tokens of B (block 2)
+    s = m.next()
+    np.testing.assert_array_equal(s.token_ids, [10, 11, 12, 13, 14, 20, 21, 22])
+    np.testing.assert_array_equal(s.positions, [0, 1, 2, 3, 4, 0, 1, 2])
+    np.testing.assert_array_equal(s.slot_mapping, [0, 1, 2, 3, 4, 8, 9, 10])
+    np.testing.assert_array_equal(s.row_request, [A] * 5 + [B] * 3)
+    np.testing.assert_array_equal(s.row_samples, [0, 0, 0, 0, 1, 0, 0, 0])
+    np.testing.assert_array_equal(s.block_tables[0], [0, 1, 0, 0])
+    np.testing.assert_array_equal(s.block_tables[5], [2, 0, 0, 0])
+    assert m.commit([0, 0, 0, 0, 30, 0, 0, 0]) == []
+    # step 2: A decodes token 30 at position 5; B's last 3 prompt tokens (block 3 joins)
+    s = m.next()
+    np.testing.assert_array_equal(s.token_ids, [30, 23, 24, 25])
+    np.testing.assert_array_equal(s.positions, [5, 3, 4, 5])
+    np.testing.assert_array_equal(s.seq_lens, [6, 4, 5, 6])
+    np.testing.assert_array_equal(s.slot_mapping, [5, 11, 12, 13])
+    np.testing.assert_array_equal(s.row_samples, [1, 0, 0, 1])
+    assert m.commit([31, 0, 0, 40]) == []
+    # step 3: both decode; A reaches 3 new tokens, B 2: both finish, blocks return in order
+    s = m.next()
+    np.testing.assert_array_equal(s.token_ids, [31, 40])
+    np.testing.assert_array_equal(s.positions, [6, 6])
+    np.testing.assert_array_equal(s.slot_mapping, [6, 14])
+    assert m.commit([32, 41]) == [A, B]
+    assert m.tokens(A) == [30, 31, 32] and m.tokens(B) == [40, 41]
+    assert list(m.pool.free) == list(range(4, 16)) + [0, 1, 2, 3]
+    assert len(m.next().token_ids) == 0
+    assert m.counts() == (0, 0, 0, 2)
+
+
+def test_preemption_worked_example_by_hand():
+    """Pool of 4 blocks of 4, predicted decode length 1 (optimistic): A (4 prompt tokens) and
+    B (3) both decode 6 tokens.  B outgrows the pool at step 6, is saved and freed, and is
+    reloaded into other blocks once A finishes."""
+    m = DenseBatchFormer(BlockAllocator(4, 4), dense_tokens=4, max_blocks_per_seq=4,
+                         eos_token=999, predicted_new=1)
+    A, B = 1, 2
+    m.add(A, [10, 11, 12, 13], 6)
+    m.add(B, [20, 21, 22], 6)
+    s = m.next()                                   # A's prompt fills the batch (block 0)
+    np.testing.assert_array_equal(s.row_request, [A] * 4)
+    m.commit([0, 0, 0, 50])
+    s = m.next()                                   # A decodes at 4 (block 1); B admitted (block 2)
+    np.testing.assert_array_equal(s.positions, [4, 0, 1, 2])
+    np.testing.assert_array_equal(s.slot_mapping, [4, 8, 9, 10])
+    m.commit([51, 0, 0, 60])
+    for want_pos, want_slot in (([5, 3], [5, 11]), ([6, 4], [6, 12]), ([7, 5], [7, 13])):
+        s = m.next()                               # B's position 4 takes block 3, the last
+        np.testing.assert_array_equal(s.positions, want_pos)
+        np.testing.assert_array_equal(s.slot_mapping, want_slot)
+        assert m.moves == []
+        m.commit([52, 61])
+    s = m.next()                                   # A needs a block at 8: B (last) is preempted
+    assert [(v.kind, v.rid, v.n_tokens, v.table) for v in m.moves] == [(0, B, 6, [2, 3])]
+    np.testing.assert_array_equal(s.positions, [8])
+    np.testing.assert_array_equal(s.slot_mapping, [8])   # block 2, freed by B, reused
+    assert m.counts() == (0, 1, 1, 0)
+    assert m.commit([53]) == [A]                   # A's sixth token: finished, blocks 0, 1, 2 back
+    s = m.next()                                   # B resumes in blocks 3, 0 and decodes at 6
+    assert [(v.kind, v.rid, v.n_tokens, v.table) for v in m.moves] == [(1, B, 6, [3, 0])]
+    np.testing.assert_array_equal(s.positions, [6])
+    np.testing.assert_array_equal(s.slot_mapping, [2])
+    np.testing.assert_array_equal(s.token_ids, [61])
+    m.commit([62])
+    assert m.tokens(B) == [60, 61, 61, 61, 62] and m.counts() == (0, 1, 0, 1)
+
+
+def _random_run(form, rng, n_steps, vocab, eos, add_prob, max_prompt, max_new_hi):
+    """Drive a former (model or library) with seeded arrivals and sampled tokens; yield each
+    step's rows (or the error class) and finished ids."""
+    next_id = 0
+    for _ in range(n_steps):
+        while rng.random() < add_prob:
+            p = rng.integers(0, vocab, size=int(rng.integers(1, max_prompt + 1)))
+            try:
+                form.add(next_id, p, int(rng.integers(1, max_new_hi + 1)))
+                yield ("add", next_id)
+            except Exception as e:  # noqa: BLE001
+                yield ("add_err", type(e).__name__)
+            next_id += 1
+        try:
+            st = form.next()
+        except Exception as e:  # noqa: BLE001
+            yield ("next_err", type(e).__name__)
+            continue
+        rows = _rows(st) if not isinstance(st, dict) else st
+        yield ("formed", rows, form.moves())
+        n = len(rows["token_ids"])
+        sampled = rng.integers(0, vocab, size=n).astype(np.int32)
+        fin = form.commit(sampled)
+        yield ("step", rows, list(fin))
+
+
+class _ModelAdapter:
+    """The model behind the library class's interface."""
+
+    def __init__(self, m):
+        self.m = m
+
+    def add(self, rid, prompt, max_new):
+        try:
+            self.m.add(rid, prompt, max_new)
+        except SchedulerError as e:
+            raise RuntimeError(str(e))
+
+    def next(self):
+        try:
+            return _rows(self.m.next())
+        except SchedulerError as e:
+            raise RuntimeError(str(e))
+
+    def commit(self, sampled):
+        return self.m.commit(sampled)
+
+    def moves(self):
+        return [(v.kind, v.rid, v.n_tokens, np.array(v.table, np.int32)) for v in self.m.moves]
+
+
+CASES = [  # (dense, block size, pool blocks, blocks per seq, vocab, eos, add prob, max prompt,
+    #      max new, predicted new)
+    (8, 4, 64, 16, 50, 3, 0.5, 30, 6, 0),
+    (16, 16, 12, 8, 20, 0, 0.6, 100, 20, 0),     # tight pool, peaks reserved
+    (16, 16, 12, 8, 20, -1, 0.6, 100, 20, 2),    # tight pool, optimistic: preemption
+    (33, 16, 400, 32, 1000, 7, 0.9, 200, 40, 0),
+    (32, 4, 24, 32, 20, -1, 0.3, 60, 12, 3),     # preemption with chunked prompts
+    (64, 4, 40, 32, 30, 5, 0.08, 60, 8, 0),      # short batches: prompts run out
+    (1, 4, 8, 8, 10, 9, 0.3, 12, 4, 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_model_invariants_over_random_runs(case):
+    D, bs, nb, mb, vocab, eos, ap, mp, mn, pn = case
+    m = DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos, pn)
+    rng = np.random.default_rng(11)
+    placed = {}   # request -> prompt positions placed so far
+    saved = {}    # preempted request -> cached tokens it was saved with
+    for ev in _random_run(_ModelAdapter(m), rng, 300, vocab, eos, ap, mp, mn):
+        if ev[0] == "formed":
+            rows, moves = ev[1], ev[2]
+            # saves come before reloads; a reload restores exactly what was saved, into as many
+            # blocks as those tokens need; a request is saved at most once before it returns
+            kinds = [v[0] for v in moves]
+            assert kinds == sorted(kinds)
+            assert not (0 in kinds and 1 in kinds)  # no resumption in a preempting step
+            for kind, rid, n, table in moves:
+                assert len(table) == -(-n // bs)
+                if kind == 0:
+                    assert rid not in saved
+                    saved[rid] = n
+                else:
+                    assert saved.pop(rid) == n
+            if pn == 0:
+                assert moves == []  # peaks reserved: nothing is ever preempted
+            continue
+        if ev[0] != "step":
+            continue
+        rows, fin = ev[1], ev[2]
+        n = len(rows["token_ids"])
+        assert n <= D
+        pos, tab, req, smp = rows["positions"], rows["block_tables"], rows["row_request"], rows["row_samples"]
+        # slots follow the block table; no two rows share one
+        want = tab[np.arange(n), pos // bs].astype(np.int64) * bs + pos % bs
+        np.testing.assert_array_equal(rows["slot_mapping"], want)
+        assert len(set(rows["slot_mapping"].tolist())) == n
+        np.testing.assert_array_equal(rows["seq_lens"], pos + 1)
+        # decode rows (requests past their prompt) come first
+        is_dec = np.array([pos[b] >= len(m.req[int(req[b])].prompt) for b in range(n)], dtype=bool)
+        assert not np.any(is_dec[1:] & ~is_dec[:-1])
+        for b in range(n):
+            r = m.req[int(req[b])]
+            if not is_dec[b]:
+                # prompt rows: consecutive positions, each placed once, in order, right token
+                assert pos[b] == placed.get(r.rid, 0)
+                placed[r.rid] = pos[b] + 1
+                assert rows["token_ids"][b] == r.prompt[pos[b]]
+                assert smp[b] == (1 if pos[b] == len(r.prompt) - 1 else 0)
+            else:
+                assert smp[b] == 1
+        # finished requests: max_new reached or eos sampled, blocks returned
+        for rid in fin:
+            r = m.req[rid]
+            assert r.finished and r.table == []
+            assert len(r.gen) == r.max_new or r.gen[-1] == eos
+    # blocks of live requests are disjoint and, with the free list, cover the pool exactly
+    live = [b for r in m.req.values() for b in r.table]
+    assert sorted(live + list(m.pool.free)) == list(range(nb))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from transformer_decode_step_ns_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        pytest.skip("libns.so not built")
+    return _lib
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_library_former_matches_the_model_bit_for_bit(L, case):
+    D, bs, nb, mb, vocab, eos, ap, mp, mn, pn = case
+    model = _ModelAdapter(DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos, pn))
+    pool = L.BlockPool(nb, bs, mb)
+    lib_form = L.BatchFormer(pool, D, mb, eos, pn)
+    a = _random_run(model, np.random.default_rng(5), 300, vocab, eos, ap, mp, mn)
+    b = _random_run(lib_form, np.random.default_rng(5), 300, vocab, eos, ap, mp, mn)
+    steps = 0
+    for ea, eb in zip(a, b):
+        assert ea[0] == eb[0], (ea, eb)
+        if ea[0] == "formed":
+            for k in KEYS:
+                np.testing.assert_array_equal(ea[1][k], eb[1][k], err_msg=k)
+            assert len(ea[2]) == len(eb[2])
+            for va, vb in zip(ea[2], eb[2]):
+                assert va[:3] == vb[:3]
+                np.testing.assert_array_equal(va[3], vb[3])
+        elif ea[0] == "step":
+            steps += 1
+            for k in KEYS:
+                np.testing.assert_array_equal(ea[1][k], eb[1][k], err_msg=k)
+            assert ea[2] == eb[2]
+        elif ea[0] == "add":
+            assert ea[1] == eb[1]
+    assert steps > 0
+    assert pool.free_count() == model.m.pool.free_count()
+    ids = pool.reserve(pool.free_count())
+    np.testing.assert_array_equal(ids, list(model.m.pool.free))
+
+
+def test_library_former_errors(L):
+    pool = L.BlockPool(2, 4, 4)
+    f = L.BatchFormer(pool, 8, 4, 0)
+    for args in ((0, [], 1), (0, [1], 0), (0, [1] * 16, 1), (-1, [1], 1)):
+        with pytest.raises(L.NSError) as e:
+            f.add(*args)
+        assert e.value.status == 1
+    f.add(0, [1, 2, 3, 4, 5, 6, 7], 1)   # 2 blocks: the whole pool
+    f.add(1, [1, 2], 3)
+    with pytest.raises(L.NSError):
+        f.commit([0])                     # nothing formed yet
+    s = f.next()
+    assert len(s["token_ids"]) == 7       # B gets no row: the pool is empty
+    with pytest.raises(L.NSError):
+        f.next()                          # commit first
+    with pytest.raises(L.NSError):
+        f.commit([0] * 6)                 # wrong row count
+    assert f.commit([5] * 7) == [0]       # max_new 1: finished, blocks back
+    s = f.next()
+    np.testing.assert_array_equal(s["token_ids"], [1, 2])
+    f.commit([9, 9])
+    assert f.counts() == (0, 1, 0, 1) and f.tokens(1) == [9]
+    assert L.BatchFormer(pool, 1, 4, 0).counts() == (0, 0, 0, 0)
+    with pytest.raises(L.NSError):
+        L.BatchFormer(pool, 4, 4, 0, -1)

@@ -35,6 +35,9 @@ SYMBOLS = (
     "ns_pool_free_count", "ns_check_step_metadata", "ns_set_kernel_timing",
     "ns_get_kernel_timing", "ns_attn_decode_noalloc", "ns_set_token_source",
     "ns_set_graph_buckets", "ns_set_kv_offload", "ns_kv_reload", "ns_kv_save",
+    "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
+    "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
+    "ns_sched_counts",
 )
 
 
@@ -122,6 +125,16 @@ def lib() -> ctypes.CDLL:
             "ns_set_kv_offload": ([P, P, ctypes.c_size_t], I),
             "ns_kv_reload": ([P, P, I, I, P, I, P], I),
             "ns_kv_save": ([P, P, I, I, P, I, P], I),
+            "ns_pool_geometry": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "ns_kv_get_pool": ([P, ctypes.POINTER(P)], I),
+            "ns_sched_create": ([P, I, I, I, I, ctypes.POINTER(P)], I),
+            "ns_sched_moves": ([P, P, P, P, P, I, ctypes.POINTER(I)], I),
+            "ns_sched_destroy": ([P], None),
+            "ns_sched_add": ([P, I, P, I, I], I),
+            "ns_sched_next": ([P, P, P, P, P, P, P, P, ctypes.POINTER(I)], I),
+            "ns_sched_commit": ([P, P, I, P, ctypes.POINTER(I)], I),
+            "ns_sched_tokens": ([P, I, P, I, ctypes.POINTER(I)], I),
+            "ns_sched_counts": ([P] + [ctypes.POINTER(I)] * 4, I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
@@ -314,6 +327,12 @@ class DecodeStep:
         from the host arrays passed to ``step``."""
         check(lib().ns_set_token_source(self.h, _ptr(device_ids)))
 
+    def pool(self) -> int:
+        """The handle's block pool (borrowed), for ``BatchFormer``."""
+        out = P()
+        check(lib().ns_kv_get_pool(self.h, ctypes.byref(out)))
+        return out.value
+
     def kv_row_elems(self) -> int:
         """Elements of one (layer, token) K/V row of the offload layout: K then V."""
         return 2 * self.shape.n_kv_heads * self.shape.head_dim
@@ -451,3 +470,86 @@ def check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab, max_b
     return lib().ns_check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab,
                                         max_batch, tok.shape[0], _ptr(tok), _ptr(pos),
                                         _ptr(tab), _ptr(sl), _ptr(slot))
+
+
+class BatchFormer:
+    """Constant-dense-batch former (ns_sched_*): decode rows first, then prompt chunks up to
+    ``dense_tokens`` rows per step.  ``pool`` is a ``BlockPool`` or ``DecodeStep.pool()``."""
+
+    def __init__(self, pool, dense_tokens: int, max_blocks_per_seq: int, eos_token: int,
+                 predicted_new_tokens: int = 0):
+        self._pool = pool  # keeps a BlockPool alive
+        ph = pool.h if isinstance(pool, BlockPool) else P(pool)
+        h = P()
+        check(lib().ns_sched_create(ph, dense_tokens, max_blocks_per_seq, eos_token,
+                                    predicted_new_tokens, ctypes.byref(h)))
+        self.h, self.D, self.mb = h, dense_tokens, max_blocks_per_seq
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().ns_sched_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, request_id: int, prompt, max_new_tokens: int) -> None:
+        a = np.ascontiguousarray(prompt, dtype=np.int32)
+        check(lib().ns_sched_add(self.h, request_id, _ptr(a) if a.size else None, a.size, max_new_tokens))
+
+    def next(self) -> dict:
+        """The next step's rows: token_ids, positions, block_tables, seq_lens, slot_mapping,
+        row_request, row_samples (host arrays of the step's row count)."""
+        D, mb = self.D, self.mb
+        out = {"token_ids": np.zeros(D, np.int32), "positions": np.zeros(D, np.int32),
+               "block_tables": np.zeros((D, mb), np.int32), "seq_lens": np.zeros(D, np.int32),
+               "slot_mapping": np.zeros(D, np.int64), "row_request": np.zeros(D, np.int32),
+               "row_samples": np.zeros(D, np.int32)}
+        n = I()
+        check(lib().ns_sched_next(self.h, *(_ptr(out[k]) for k in (
+            "token_ids", "positions", "block_tables", "seq_lens", "slot_mapping", "row_request",
+            "row_samples")), ctypes.byref(n)))
+        return {k: v[:n.value] for k, v in out.items()}
+
+    def moves(self) -> list:
+        """The formed step's moves, saves first: (kind, request id, n_tokens, block ids);
+        kind 0 = save the cached tokens from those blocks, 1 = reload them into them."""
+        n = I()
+        check(lib().ns_sched_moves(self.h, None, None, None, None, 0, ctypes.byref(n)))
+        m = n.value
+        k, r, t = (np.zeros(max(m, 1), np.int32) for _ in range(3))
+        tab = np.zeros((max(m, 1), self.mb), np.int32)
+        check(lib().ns_sched_moves(self.h, _ptr(k), _ptr(r), _ptr(t), _ptr(tab), m, ctypes.byref(n)))
+        bs = self._block_size()
+        return [(int(k[i]), int(r[i]), int(t[i]), tab[i, :(int(t[i]) + bs - 1) // bs].copy())
+                for i in range(m)]
+
+    def _block_size(self) -> int:
+        nb, bs = I(), I()
+        ph = self._pool.h if isinstance(self._pool, BlockPool) else P(self._pool)
+        check(lib().ns_pool_geometry(ph, ctypes.byref(nb), ctypes.byref(bs)))
+        return bs.value
+
+    def commit(self, sampled) -> list:
+        a = np.ascontiguousarray(sampled, dtype=np.int32)
+        fin = np.zeros(max(a.size, 1), np.int32)
+        n = I()
+        check(lib().ns_sched_commit(self.h, _ptr(a) if a.size else None, a.size, _ptr(fin), ctypes.byref(n)))
+        return fin[:n.value].tolist()
+
+    def tokens(self, request_id: int) -> list:
+        n = I()
+        check(lib().ns_sched_tokens(self.h, request_id, None, 0, ctypes.byref(n)))
+        out = np.zeros(max(n.value, 1), np.int32)
+        check(lib().ns_sched_tokens(self.h, request_id, _ptr(out), n.value, ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+    def counts(self):
+        """(requests with prompt left, running, preempted, finished)."""
+        w, r, p, f = I(), I(), I(), I()
+        check(lib().ns_sched_counts(self.h, ctypes.byref(w), ctypes.byref(r), ctypes.byref(p),
+                                    ctypes.byref(f)))
+        return w.value, r.value, p.value, f.value

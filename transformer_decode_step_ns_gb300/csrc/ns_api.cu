@@ -1023,6 +1023,21 @@ ns_status ns_pool_release(ns_pool p, const int32_t* block_ids, int n) {
   return pool_release(p, block_ids, n);
 }
 
+ns_status ns_pool_geometry(ns_pool p, int* num_blocks, int* block_size) {
+  if (p == nullptr || num_blocks == nullptr || block_size == nullptr)
+    return fail(NS_ERR_INVALID_ARG, "null argument");
+  *num_blocks = p->num_blocks;
+  *block_size = p->block_size;
+  return NS_OK;
+}
+
+ns_status ns_kv_get_pool(ns_handle h, ns_pool* out) {
+  if (h == nullptr || out == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  *out = &h->pool;
+  return NS_OK;
+}
+
 ns_status ns_pool_free_count(ns_pool p, int* n_free) {
   if (p == nullptr || n_free == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
   *n_free = static_cast<int>(p->free_list.size());
