@@ -338,6 +338,16 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool,
                          int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                          ns_stream_t stream);
 
+/* ns_attn_decode on at most cta_budget CTAs (0: no cap): the thread-block cap that the NanoFlow
+ * page ("The part that is harder than it looks") sweeps from 8 to 128 when it profiles a
+ * memory-bound op co-running with a GEMM.  The CTAs loop over the work, so any cap >= 1
+ * computes the same result bitwise.  cta_budget < 0 returns INVALID_ARG. */
+ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                                int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int num_blocks,
+                                float scale, int dtype, int cta_budget, ns_stream_t stream);
+
 /* ns_attn_decode without any device allocation, for callers that cannot allocate: code
  * running inside an allocator or memory-pool callback, a plugin whose host process owns every
  * device allocation, or a process that must keep its device footprint fixed after start-up.
@@ -383,6 +393,29 @@ typedef struct {
   long long steps;          /* ns_decode_step calls that succeeded */
 } ns_step_info;
 ns_status ns_get_step_info(ns_handle h, ns_step_info* out);
+
+/* Capture report (model cold-start page, "Bounding the CUDA graph capture": capture costs
+ * start-up time, so capture only the batch sizes the workload uses, and measure it).  One
+ * entry per captured graph. */
+typedef struct {
+  int batch;            /* graph batch (bucket) size */
+  int n_split;          /* nano-batches */
+  int attn_cta_budget;  /* 0: none */
+  int with_lm;          /* the graph ends with the LM head */
+  int chunk_rows;       /* rows of the trailing prefill chunk (0: decode only) */
+  int kv_offload;       /* the graph mirrors K/V to the host */
+  int kernels;          /* kernel nodes */
+  double capture_ms;    /* host time of capture + instantiate */
+} ns_graph_info;
+/* *n = the number of graphs; the first min(*n, capacity) entries are written, in key order. */
+ns_status ns_get_graph_report(ns_handle h, ns_graph_info* out, int capacity, int* n);
+
+/* Capture the decode-only graphs of these batch sizes now (start-up), with or without the LM
+ * head, under the current nano-batch, token-source and offload settings, so that no step pays
+ * a capture later.  Sizes in [1, max_batch]; with nano-batches only their total.  Captures are
+ * not replayed (no device work is run).  INVALID_ARG when the handle does not use graphs,
+ * NOT_INITIALIZED before ns_kv_alloc. */
+ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with_lm);
 
 /* Per-kernel timing of eager steps (for roofline accounting).  While on, ns_decode_step
  * launches the kernels eagerly (graphs are bypassed) with a CUDA event pair around each launch

@@ -58,6 +58,26 @@ def test_attention_block_permutation_and_batch_independence_bitwise(cuda_lib):
         np.testing.assert_array_equal(one[0], base[b])
 
 
+def test_attention_cta_budget_is_bitwise_neutral(cuda_lib):
+    """Capping the attention at 1, 8 or 76 CTAs (the tuner's budgets) changes no bit."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    lens = [300, 17, 1200, 64, 2100, 5]
+    q, kp, vp, tab, sl, nb = attention_case(6, lens, 32, 8, 128, "bf16")
+    base = run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb)
+    dq, dk, dv, dt, dl = to_dev(q), to_dev(kp), to_dev(vp), to_dev(tab), to_dev(sl)
+    for budget in (1, 8, 76):
+        out = torch.zeros_like(dq)
+        _lib.attn_decode(dq, dk, dv, dt, dl, out, 32, 8, 128, 16, tab.shape[1], nb,
+                         1.0 / math.sqrt(128), "bf16", cta_budget=budget)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(from_dev(out), base)
+    with pytest.raises(_lib.NSError):
+        _lib.check(_lib.lib().ns_attn_decode_capped(
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dt.data_ptr(), dl.data_ptr(), dq.data_ptr(),
+            6, 32, 8, 128, 16, tab.shape[1], nb, 0.1, 1, -1, None))  # negative budget
+
+
 def test_attention_rejects_unsupported_shapes(cuda_lib):
     import torch
     from transformer_decode_step_ns_gb300 import _lib

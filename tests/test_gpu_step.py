@@ -279,6 +279,32 @@ def test_prefill_chunk_threshold_and_offset(cuda_lib, chunk, p0):
     _check_step(Harness(shape, 111 + chunk, ctx, shared_table_rows=shared))
 
 
+def test_startup_capture_and_capture_report(cuda_lib):
+    """Graphs captured at start-up for the buckets are the ones later steps replay (no new
+    capture); the report lists each with its kernel count and capture time."""
+    from transformer_decode_step_ns_gb300 import _lib
+    shape = _tiny("bf16")
+    ctx = [3, 40, 200, 17, 1, 600, 33, 9]
+    h = Harness(shape, 161, ctx)
+    h.dev.set_graph_buckets([4, 8])
+    h.dev.capture_graphs([4, 8])
+    rep = h.dev.graph_report()
+    assert sorted(r["batch"] for r in rep) == [4, 8]
+    for r in rep:
+        assert r["kernels"] == 2 + 5 * shape.n_layers and r["capture_ms"] > 0
+        assert r["with_lm"] == 1 and r["chunk_rows"] == 0 and r["n_split"] == 1
+    h.run_gpu(rows=slice(0, 3))
+    h.upload_pools()
+    h.run_gpu()
+    assert len(h.dev.graph_report()) == 2 and h.dev.info().graphs_cached == 2
+    for bad in ([0], [9]):
+        with pytest.raises(_lib.NSError):
+            h.dev.capture_graphs(bad)
+    eager = Harness(shape, 161, ctx, use_graphs=False)
+    with pytest.raises(_lib.NSError):
+        eager.dev.capture_graphs([4])
+
+
 def test_graph_bucket_arguments_are_validated(cuda_lib):
     from transformer_decode_step_ns_gb300 import _lib
     h = Harness(_tiny("bf16"), 121, [3, 5])

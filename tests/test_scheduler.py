@@ -276,3 +276,17 @@ def test_library_former_errors(L):
     assert L.BatchFormer(pool, 1, 4, 0).counts() == (0, 0, 0, 0)
     with pytest.raises(L.NSError):
         L.BatchFormer(pool, 4, 4, 0, -1)
+
+
+def test_tuner_candidate_splits():
+    from transformer_decode_step_ns_gb300 import tuner
+    c = tuner.candidate_splits(2048)
+    assert c[0] is None
+    assert all(sum(s) == 2048 and all(v % 128 == 0 for v in s) for s in c[1:])
+    two = [s for s in c[1:] if len(s) == 2]
+    assert len(two) == 15 and [768, 1280] in two and [1024, 1024] in two
+    assert sorted(s for s in c if s and len(s) == 3) == [[640, 640, 768], [640, 768, 640], [768, 640, 640]]
+    assert [s for s in c if s and len(s) == 4] == [[512] * 4]
+    # a batch that is not a multiple of 128: the last nano-batch takes the remainder
+    c = tuner.candidate_splits(1000)
+    assert all(sum(s) == 1000 for s in c[1:]) and [128, 872] in c

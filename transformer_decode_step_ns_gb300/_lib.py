@@ -37,7 +37,7 @@ SYMBOLS = (
     "ns_set_graph_buckets", "ns_set_kv_offload", "ns_kv_reload", "ns_kv_save",
     "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
-    "ns_sched_counts",
+    "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
 )
 
 
@@ -135,6 +135,9 @@ def lib() -> ctypes.CDLL:
             "ns_sched_commit": ([P, P, I, P, ctypes.POINTER(I)], I),
             "ns_sched_tokens": ([P, I, P, I, ctypes.POINTER(I)], I),
             "ns_sched_counts": ([P] + [ctypes.POINTER(I)] * 4, I),
+            "ns_capture_graphs": ([P, I, P, I], I),
+            "ns_attn_decode_capped": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P], I),
+            "ns_get_graph_report": ([P, P, I, ctypes.POINTER(I)], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
         }
         for name, (args, res) in sig.items():
@@ -203,6 +206,11 @@ def _stream(stream) -> Optional[int]:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+class GraphInfo(ctypes.Structure):
+    _fields_ = [("batch", I), ("n_split", I), ("attn_cta_budget", I), ("with_lm", I),
+                ("chunk_rows", I), ("kv_offload", I), ("kernels", I), ("capture_ms", ctypes.c_double)]
 
 
 class DecodeStep:
@@ -372,6 +380,20 @@ class DecodeStep:
         return {KERNEL_KINDS[i]: (t.launches[i], t.total_ms[i]) for i in range(8)
                 if t.launches[i] > 0}
 
+    def capture_graphs(self, sizes: Sequence[int], with_lm: bool = True) -> None:
+        """Capture the decode-only graphs of these batch sizes now (start-up)."""
+        a = np.ascontiguousarray(sizes, dtype=np.int32)
+        check(lib().ns_capture_graphs(self.h, a.size, _ptr(a) if a.size else None, 1 if with_lm else 0))
+
+    def graph_report(self) -> list:
+        """One dict per captured graph: batch, n_split, attn_cta_budget, with_lm, chunk_rows,
+        kv_offload, kernels, capture_ms."""
+        n = I()
+        check(lib().ns_get_graph_report(self.h, None, 0, ctypes.byref(n)))
+        arr = (GraphInfo * max(n.value, 1))()
+        check(lib().ns_get_graph_report(self.h, arr, n.value, ctypes.byref(n)))
+        return [{f: getattr(arr[i], f) for f, _ in GraphInfo._fields_} for i in range(n.value)]
+
     def info(self) -> StepInfo:
         s = StepInfo()
         check(lib().ns_get_step_info(self.h, ctypes.byref(s)))
@@ -380,12 +402,16 @@ class DecodeStep:
 
 def attn_decode(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
                 n_kv_heads: int, head_dim: int, block_size: int, max_blocks_per_seq: int,
-                num_blocks: int, scale: float, dtype: str, stream=None) -> None:
+                num_blocks: int, scale: float, dtype: str, stream=None, cta_budget: int = 0) -> None:
+    """Paged decode attention; ``cta_budget`` > 0 caps its CTAs (ns_attn_decode_capped)."""
     batch = int(seq_lens.shape[0])
-    check(lib().ns_attn_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
-                               _ptr(seq_lens), _ptr(out), batch, n_q_heads, n_kv_heads,
-                               head_dim, block_size, max_blocks_per_seq, num_blocks,
-                               float(scale), DTYPES[dtype], _stream(stream)))
+    args = (_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(out),
+            batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+            float(scale), DTYPES[dtype])
+    if cta_budget:
+        check(lib().ns_attn_decode_capped(*args, cta_budget, _stream(stream)))
+    else:
+        check(lib().ns_attn_decode(*args, _stream(stream)))
 
 
 def attn_decode_noalloc(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,

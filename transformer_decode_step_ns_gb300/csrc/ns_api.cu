@@ -325,7 +325,11 @@ struct ns_ctx {
   long long* kv_slots = nullptr;
   size_t kv_slots_cap = 0;
   // graphs
-  std::map<std::vector<int>, cudaGraphExec_t> graphs;
+  struct GraphEntry {
+    cudaGraphExec_t ex;
+    ns_graph_info info;
+  };
+  std::map<std::vector<int>, GraphEntry> graphs;
   int* err = nullptr;
   ns_step_info info{};
   int kernels_last = 0;
@@ -687,7 +691,7 @@ ns_status get_graph(ns_ctx* h, int B, cudaGraphExec_t* out) {
   auto key = graph_key(h, B);
   auto it = h->graphs.find(key);
   if (it != h->graphs.end()) {
-    *out = it->second;
+    *out = it->second.ex;
     return NS_OK;
   }
   const auto t0 = std::chrono::steady_clock::now();
@@ -715,11 +719,19 @@ ns_status get_graph(ns_ctx* h, int B, cudaGraphExec_t* out) {
   }
   cudaGraphDestroy(g);
   if (ce != cudaSuccess) return fail(NS_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ce));
-  h->graphs.emplace(key, ex);
+  ns_graph_info gi{};
+  gi.batch = B;
+  gi.n_split = h->n_split;
+  gi.attn_cta_budget = h->attn_budget;
+  gi.with_lm = h->with_lm ? 1 : 0;
+  gi.chunk_rows = h->chunk_first < B ? B - h->chunk_first : 0;
+  gi.kv_offload = h->kv_host != nullptr ? 1 : 0;
+  gi.kernels = kernels;
+  gi.capture_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  h->graphs.emplace(key, ns_ctx::GraphEntry{ex, gi});
   h->info.graphs_cached = static_cast<int>(h->graphs.size());
   h->info.kernels_per_step = kernels;
-  h->info.last_capture_ms =
-      std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  h->info.last_capture_ms = gi.capture_ms;
   *out = ex;
   return NS_OK;
 }
@@ -757,7 +769,7 @@ void ns_destroy(ns_handle h) {
   cudaGetDevice(&prev);
   cudaSetDevice(h->dev);
   cudaDeviceSynchronize();
-  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second.ex);
   for (auto& L : h->layers) {
     free_proj(L.qkv);
     free_proj(L.o);
@@ -1170,6 +1182,39 @@ ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes) {
   return NS_OK;
 }
 
+ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with_lm) {
+  if (h == nullptr || (n > 0 && batch_sizes == nullptr) || n < 0) return fail(NS_ERR_INVALID_ARG, "argument");
+  if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
+  if (!h->cfg.use_graphs) return fail(NS_ERR_INVALID_ARG, "the handle does not use graphs");
+  int split_sum = 0;
+  for (int v : h->split_sizes) split_sum += v;
+  for (int i = 0; i < n; ++i) {
+    const int B = batch_sizes[i];
+    if (B < 1 || B > h->R) return fail(NS_ERR_INVALID_ARG, "batch size outside [1, max_batch]");
+    if (h->n_split > 1 && B != split_sum)
+      return fail(NS_ERR_INVALID_ARG, "with nano-batches only their total batch is captured");
+  }
+  NS_CUDA(cudaSetDevice(h->dev));
+  for (int i = 0; i < n; ++i) {
+    h->with_lm = with_lm != 0;
+    h->chunk_first = batch_sizes[i];  // decode-only layout
+    cudaGraphExec_t ex = nullptr;
+    NS_TRY(get_graph(h, batch_sizes[i], &ex));
+  }
+  return NS_OK;
+}
+
+ns_status ns_get_graph_report(ns_handle h, ns_graph_info* out, int capacity, int* n) {
+  if (h == nullptr || n == nullptr || (capacity > 0 && out == nullptr)) return fail(NS_ERR_INVALID_ARG, "argument");
+  int i = 0;
+  for (const auto& kv : h->graphs) {
+    if (i < capacity) out[i] = kv.second.info;
+    ++i;
+  }
+  *n = i;
+  return NS_OK;
+}
+
 ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids) {
   if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
   h->tok_src = device_token_ids;
@@ -1339,6 +1384,15 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
                          const int32_t* seq_lens, void* out, int batch, int n_q_heads, int n_kv_heads,
                          int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
                          int dtype, ns_stream_t stream) {
+  return ns_attn_decode_capped(q, k_pool, v_pool, block_tables, seq_lens, out, batch, n_q_heads, n_kv_heads,
+                               head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, 0, stream);
+}
+
+ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                const int32_t* seq_lens, void* out, int batch, int n_q_heads, int n_kv_heads,
+                                int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                                int dtype, int cta_budget, ns_stream_t stream) {
+  if (cta_budget < 0) return fail(NS_ERR_INVALID_ARG, "cta_budget < 0");
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return fail(NS_ERR_INVALID_ARG, "null argument");
   if (batch < 1 || batch > kMaxRows || n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads ||
       max_blocks_per_seq < 1 || num_blocks < 1 || !(scale > 0.f) || (dtype != NS_F16 && dtype != NS_BF16))
@@ -1375,7 +1429,8 @@ ns_status ns_attn_decode(const void* q, const void* k_pool, const void* v_pool, 
   ap.err = sc->err;
   const int cap = attn_max_grid(dtype, head_dim, G, batch);
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
-  const int grid = static_cast<int>(std::min<long long>(cap, units));
+  int grid = static_cast<int>(std::min<long long>(cap, units));
+  if (cta_budget > 0) grid = std::min(grid, cta_budget);
   NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));
   return NS_OK;
 }
