@@ -711,6 +711,98 @@ class ContinuousWorkload:
         return r
 
 
+# ---------------------------------------------------------------------------------- serving run
+
+class ServingWorkload:
+    """Constant-dense-batch serving of the 32-layer LLaMA-3-8B-shaped model (bf16, seeded
+    N(0, 0.02) weights): 256 requests arrive at once with seeded prompts of lengths uniform in
+    [128, 1024] and decode lengths uniform in [64, 256].  The library's batch former (ns_sched)
+    forms every step at 512 tokens -- decode rows first, then prompt chunks at token granularity
+    -- admitting prompts against their full peak memory from a pool of 40 % of the requests'
+    summed peaks, so prompts and decodes interleave as requests finish.  Steps with prompt chunks
+    launch eagerly (their layouts vary); decode-only steps replay graphs padded to buckets of 64.
+    Greedy argmax on the GPU; ids read back each step."""
+
+    D, n_req, bs = 512, 256, 16
+
+    def __init__(self):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        self.seed = seed = synth.config_seed(4)
+        self.shape = sh = synth.llama3_8b_shape(32)
+        n, bs = self.n_req, self.bs
+        self.plen = synth.uniform_int(seed, "serve.plen", n, 128, 1024).astype(np.int64)
+        self.new = synth.uniform_int(seed, "serve.new", n, 64, 256).astype(np.int64)
+        self.mb = int(math.ceil((1024 + 256) / bs))
+        peaks = sum(int(math.ceil((p + m - 1) / bs)) for p, m in zip(self.plen, self.new))
+        self.num_blocks = int(0.4 * peaks)
+        t0 = time.time()
+        w = synth.model_weights_device(sh, seed)
+        self.dev = _lib.DecodeStep(sh, w, self.D, self.mb, use_graphs=True)
+        del w
+        torch.cuda.empty_cache()
+        self.dev.kv_alloc(self.num_blocks, bs)
+        self.dev.set_graph_chunks(False)
+        self.dev.set_graph_buckets(list(range(64, self.D + 1, 64)))
+        self.former = _lib.BatchFormer(self.dev.pool(), self.D, self.mb, eos_token=-1)
+        for i in range(n):
+            toks = synth.uniform_int(seed, f"serve.prompt{i}", int(self.plen[i]), 0, sh.vocab - 1)
+            self.former.add(i, toks.astype(np.int32), int(self.new[i]))
+        self.setup_s = time.time() - t0
+
+    def report(self):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        sh, D = self.shape, self.D
+        logits = torch.empty((D, sh.vocab), dtype=torch.float32, device="cuda")
+        ids_dev = torch.empty(D, dtype=torch.int32, device="cuda")
+        ids_host = torch.empty(D, dtype=torch.int32).pin_memory()
+        rows_per_step, kinds, dev_ms = [], [], []
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        while self.former.counts()[3] < self.n_req:
+            r = self.former.next()
+            B = len(r["token_ids"])
+            if B == 0:
+                raise RuntimeError("the former formed an empty step with requests unfinished")
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            self.dev.step(r["token_ids"], r["positions"], r["block_tables"], r["seq_lens"],
+                          r["slot_mapping"], logits[:B])
+            b.record()
+            _lib.greedy_argmax(logits[:B], ids_dev[:B])
+            ids_host[:B].copy_(ids_dev[:B], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            self.former.commit(ids_host[:B].numpy())
+            rows_per_step.append(B)
+            kinds.append("decode" if int(r["row_samples"].sum()) == B else "mixed")
+            dev_ms.append((a, b))
+        wall = time.perf_counter() - t0
+        dev_ms = np.array([a.elapsed_time(b) for a, b in dev_ms])
+        kinds = np.array(kinds)
+        rows = np.array(rows_per_step)
+        out_tok = int(self.new.sum())
+        all_tok = int(self.plen.sum() + self.new.sum() - self.n_req)  # rows fed: prompts + all but the last token
+        return {"workload": ("LLaMA-3-8B-shaped 32L bf16, 256 requests (prompts U[128,1024], decode "
+                             "U[64,256]), dense batch 512 tokens formed by ns_sched, pool 40% of "
+                             "summed peaks, mixed steps eager, decode-only steps graph-replayed"),
+                "steps": int(len(rows)), "wall_s": round(wall, 3),
+                "output_tokens": out_tok, "prompt_tokens": int(self.plen.sum()),
+                "output_tokens_per_s": round(out_tok / wall, 1),
+                "rows_per_s": round(all_tok / wall, 1),
+                "rows_per_step_mean": round(float(rows.mean()), 1),
+                "steps_at_dense_size": round(float((rows == D).mean()), 4),
+                "mixed_steps": int((kinds == "mixed").sum()),
+                "device_ms_per_step_mixed": round(float(dev_ms[kinds == "mixed"].mean()), 3)
+                if (kinds == "mixed").any() else None,
+                "device_ms_per_step_decode": round(float(dev_ms[kinds == "decode"].mean()), 3)
+                if (kinds == "decode").any() else None,
+                "device_busy_frac": round(float(dev_ms.sum() * 1e-3 / wall), 4),
+                "graphs_cached": self.dev.info().graphs_cached,
+                "num_blocks": self.num_blocks, "setup_s": round(self.setup_s, 1),
+                "device_error": self.dev.device_error()}
+
+
 # ---------------------------------------------------------------------------------- main arms
 
 KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_gemm.cu",
@@ -900,6 +992,13 @@ def run_ours(args, rank, world):
         del cw
         torch.cuda.empty_cache()
 
+    serve = None
+    if not args.skip_serving and rank == 0:
+        sw = ServingWorkload()
+        serve = sw.report()
+        del sw
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and not args.skip_cpu:
         import oracle
@@ -935,6 +1034,7 @@ def run_ours(args, rank, world):
         "attention": attn,
         "nanobatch_layer": nano,
         "continuous": cont,
+        "serving": serve,
         "cpu_baseline": cpu,
         "clocks": clk,
         "gpu_launches": info.kernels_per_step * K,
@@ -973,7 +1073,7 @@ def run_attention_only(args, rank, world):
 
 def run_extra_only(args, rank, world):
     """One of the extra workloads alone, as its own JSON line (--nanobatch-only,
-    --continuous-only)."""
+    --continuous-only, --serving-only)."""
     import torch
     import __graft_entry__ as ge
     ge.build()
@@ -987,6 +1087,12 @@ def run_extra_only(args, rank, world):
                 "n_gpus": world, "steps": max(args.steps, 1), "warmup": args.warmup,
                 "dtype": "bf16", "data": "synthetic", "config": {"workload": r["workload"]},
                 "nanobatch_layer": r}
+    elif args.serving_only:
+        r = ServingWorkload().report()
+        line = {"metric": "serving output tokens/s, constant dense batch", "unit": "tokens/s",
+                "value": r["output_tokens_per_s"], "higher_is_better": True,
+                "n_gpus": world, "steps": r["steps"], "warmup": 0, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": r["workload"]}, "serving": r}
     else:
         cw = ContinuousWorkload()
         r = cw.report(args.continuous_steps, peaks)
@@ -1054,6 +1160,9 @@ def main():
     ap.add_argument("--skip-nanobatch", action="store_true")
     ap.add_argument("--skip-continuous", action="store_true")
     ap.add_argument("--continuous-steps", type=int, default=2000)
+    ap.add_argument("--skip-serving", action="store_true")
+    ap.add_argument("--serving-only", action="store_true",
+                    help="run the batch-former serving workload alone")
     ap.add_argument("--nanobatch-only", action="store_true",
                     help="time the 70B-layer nano-batch workload alone")
     ap.add_argument("--continuous-only", action="store_true",
@@ -1080,7 +1189,7 @@ def main():
             run_reference(args, rank, world)
         elif args.attention_only:
             run_attention_only(args, rank, world)
-        elif args.nanobatch_only or args.continuous_only:
+        elif args.nanobatch_only or args.continuous_only or args.serving_only:
             run_extra_only(args, rank, world)
         else:
             run_ours(args, rank, world)

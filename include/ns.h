@@ -252,8 +252,10 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
  * (no final norm, no LM head), for callers that only advance the KV cache or time the layers
  * alone.  Writes this step's K/V into the pools; every row's K/V is written before any row
  * attends, so rows of one prompt chunk (consecutive positions over one block table) see each
- * other causally.  A trailing run of at least 16 such rows whose tables agree with the run's
- * last row is attended by one causal prefill-chunk kernel; other rows by the decode kernel.
+ * other causally.  Working back from the last row, each maximal run of at least 16 such rows
+ * whose tables agree with the run's last row is a prompt chunk attended by one causal
+ * prefill-chunk kernel (so a step may end with several chunks, one per prompt); the search
+ * stops at the first shorter run, and the rows before it use the decode kernel.
  * With use_graphs the first call for a batch size (or graph bucket) captures a graph (not
  * during a caller's stream capture); later calls replay it.  Returns NOT_INITIALIZED before
  * ns_kv_alloc. */
@@ -269,6 +271,11 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
  * logits written), so one captured graph serves every batch up to its size.  Batches above the
  * largest size, eager steps and nano-batched steps use their exact size.  n = 0 clears. */
 ns_status ns_set_graph_buckets(ns_handle h, int n, const int* sizes);
+
+/* Whether steps with prompt chunks (see ns_decode_step) replay graphs (capture != 0, the
+ * default) or launch eagerly (0).  A batch former's mixed steps rarely repeat a chunk layout, and
+ * every new layout is a new capture; with 0 only decode-only steps use (and capture) graphs. */
+ns_status ns_set_graph_chunks(ns_handle h, int capture);
 
 /* Token ids from device memory (NanoFlow page, "Runtime details that keep the pipeline fed":
  * the next iteration's batch is formed before the current one finishes, so an end-of-sequence

@@ -305,6 +305,27 @@ def test_startup_capture_and_capture_report(cuda_lib):
         eager.dev.capture_graphs([4])
 
 
+@pytest.mark.parametrize("tail", [25, 10])
+def test_two_prompt_chunks_in_one_step(cuda_lib, tail):
+    """Decode rows, then the rest of one prompt (positions 10..39), then the start of another
+    (positions 0..tail-1), as a batch former lays them out: with a 25-row tail both prompts run
+    as causal chunk kernels, with a 10-row tail (below the chunk threshold) the search stops and
+    every row uses the decode kernel.  Both match the oracle, and a nano-batch split cutting
+    through the first prompt gives the unsplit logits bitwise."""
+    shape = _tiny("bf16")
+    dec = [7, 90]
+    first = list(range(10, 40))
+    second = list(range(tail))
+    ctx = dec + first + second
+    ia, ib = len(dec) + len(first) - 1, len(ctx) - 1
+    shared = list(range(len(dec))) + [ia] * len(first) + [ib] * len(second)
+    h = Harness(shape, 171 + tail, ctx, shared_table_rows=shared)
+    got, _ = _check_step(h)
+    h.upload_pools()
+    h.dev.set_nanobatch([20, len(ctx) - 20])
+    np.testing.assert_array_equal(h.run_gpu(), got)
+
+
 def test_graph_bucket_arguments_are_validated(cuda_lib):
     from transformer_decode_step_ns_gb300 import _lib
     h = Harness(_tiny("bf16"), 121, [3, 5])

@@ -38,6 +38,7 @@ SYMBOLS = (
     "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
+    "ns_set_graph_chunks",
 )
 
 
@@ -136,6 +137,7 @@ def lib() -> ctypes.CDLL:
             "ns_sched_tokens": ([P, I, P, I, ctypes.POINTER(I)], I),
             "ns_sched_counts": ([P] + [ctypes.POINTER(I)] * 4, I),
             "ns_capture_graphs": ([P, I, P, I], I),
+            "ns_set_graph_chunks": ([P, I], I),
             "ns_attn_decode_capped": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P], I),
             "ns_get_graph_report": ([P, P, I, ctypes.POINTER(I)], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
@@ -329,6 +331,10 @@ class DecodeStep:
         """Replay graphs captured for these batch sizes only, padding smaller batches."""
         a = np.ascontiguousarray(sizes or [], dtype=np.int32)
         check(lib().ns_set_graph_buckets(self.h, a.size, _ptr(a) if a.size else None))
+
+    def set_graph_chunks(self, capture: bool) -> None:
+        """False: steps with prompt chunks launch eagerly; only decode-only steps use graphs."""
+        check(lib().ns_set_graph_chunks(self.h, 1 if capture else 0))
 
     def set_token_source(self, device_ids=None) -> None:
         """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,

@@ -307,8 +307,11 @@ struct ns_ctx {
   std::vector<int> split_sizes;
   int attn_budget = 0;
   std::vector<int> buckets;  // graph batch sizes (ns_set_graph_buckets), ascending
-  int chunk_first = 0;       // rows [chunk_first, batch) of the current step form a prefill
-                             // chunk (chunk_first == the step's row count: none)
+  bool graph_chunks = true;  // steps with prompt chunks replay graphs too (ns_set_graph_chunks)
+  int chunk_first = 0;       // rows [chunk_first, batch) of the current step form prefill
+                             // chunks (chunk_first == the step's row count: none)
+  std::vector<int> chunk_runs;  // first row of each chunk, ascending; a chunk ends where the
+                                // next begins (the last at the batch end)
   bool with_lm = true;  // false: the step stops after the last layer (logits_out == NULL)
   const int32_t* tok_src = nullptr;  // device token ids (ns_set_token_source) or null: metadata
   std::vector<uint8_t> dirty_blocks;  // scratch of early_fetch_ok, all zero between calls
@@ -577,7 +580,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.counters = h->attn_counters;
       ap.err = h->err;
       ap.early_ok = reinterpret_cast<const int*>(h->meta_dev + ml.flags);
-      // decode rows of the nano-batch, then the prefill-chunk rows it holds (the chunk is last)
+      // decode rows of the nano-batch, then the prefill-chunk rows it holds (chunks come last)
       const int r_lo = nb[i].first, r_hi = nb[i].first + nb[i].second;
       const int d_hi = std::min(r_hi, std::max(r_lo, h->chunk_first));
       if (d_hi > r_lo) {
@@ -588,7 +591,12 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
         NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
         h->kernels_last++;
       }
-      if (r_hi > d_hi) {
+      for (size_t ci = 0; ci < h->chunk_runs.size(); ++ci) {
+        // the part of chunk [c_lo, c_hi) inside this nano-batch
+        const int c_lo = h->chunk_runs[ci];
+        const int c_hi = ci + 1 < h->chunk_runs.size() ? h->chunk_runs[ci + 1] : B;
+        const int p_lo = std::max(c_lo, r_lo), p_hi = std::min(c_hi, r_hi);
+        if (p_hi <= p_lo) continue;
         PrefillParams pp{};
         pp.q = h->q;
         pp.q_row_stride = qd;
@@ -596,12 +604,12 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
         pp.v_pool = h->vpool[l];
         pp.block_tables = m_tab;
         pp.mb = c.max_blocks_per_seq;
-        pp.table_row = B - 1;
+        pp.table_row = c_hi - 1;
         pp.positions = m_pos;
         pp.out = h->o;
         pp.out_row_stride = qd;
-        pp.row0 = d_hi;
-        pp.chunk = r_hi - d_hi;
+        pp.row0 = p_lo;
+        pp.chunk = p_hi - p_lo;
         pp.n_kv_heads = Hkv;
         pp.num_blocks = h->num_blocks + 1;
         pp.scale_log2 = scale_log2;
@@ -682,7 +690,9 @@ std::vector<int> graph_key(const ns_ctx* h, int B) {
   const uint64_t kvh = reinterpret_cast<uint64_t>(h->kv_host);
   std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0,
                      static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
-                     h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32)};
+                     h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32),
+                     static_cast<int>(h->chunk_runs.size())};
+  for (int v : h->chunk_runs) k.push_back(v);
   for (int v : h->split_sizes) k.push_back(v);
   return k;
 }
@@ -1102,8 +1112,32 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // one packed metadata buffer, one host-to-device copy
   if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
-  // graph batch: the smallest bucket that holds the rows; padding rows fill the rest
-  const bool graphed = c.use_graphs && !h->timing;
+  // Prefill chunks: working back from the last row, each maximal run of at least kPrefillMinRows
+  // rows at consecutive positions that read the same blocks as the run's last row is one chunk,
+  // whose attention runs as one causal kernel; the first shorter run ends the search (the rows
+  // before it are decode rows).
+  std::vector<int> runs;
+  {
+    int end = batch;
+    while (end > 0) {
+      const int32_t* tl = block_tables + static_cast<size_t>(end - 1) * mb;
+      int f = end - 1;
+      while (f > 0) {
+        const int b = f - 1;
+        if (positions[b] != positions[f] - 1) break;
+        const int need = (seq_lens[b] + bs - 1) / bs;
+        if (std::memcmp(block_tables + static_cast<size_t>(b) * mb, tl, static_cast<size_t>(need) * 4) != 0) break;
+        f = b;
+      }
+      if (end - f < kPrefillMinRows) break;
+      runs.insert(runs.begin(), f);
+      end = f;
+    }
+  }
+  bool graphed = c.use_graphs && !h->timing;
+  if (graphed && !h->graph_chunks && !runs.empty()) graphed = false;  // layouts vary: eager
+  // graph batch: the smallest bucket that holds the rows; padding rows fill the rest, and a
+  // padded step has no chunk layout (its chunk rows, if any, use the decode kernel)
   int Bg = batch;
   if (graphed && h->n_split <= 1)
     for (int v : h->buckets)
@@ -1111,22 +1145,9 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
         Bg = v;
         break;
       }
-  // A trailing run of at least kPrefillMinRows rows at consecutive positions that read the same
-  // blocks as the run's last row is a prefill chunk: its attention runs as one causal kernel.
-  int chunk_first = Bg;  // none (the graph batch, so padded steps share their bucket's graph)
-  if (Bg == batch) {
-    const int32_t* tl = block_tables + static_cast<size_t>(batch - 1) * mb;
-    int f = batch - 1;
-    while (f > 0) {
-      const int b = f - 1;
-      if (positions[b] != positions[f] - 1) break;
-      const int need = (seq_lens[b] + bs - 1) / bs;
-      if (std::memcmp(block_tables + static_cast<size_t>(b) * mb, tl, static_cast<size_t>(need) * 4) != 0) break;
-      f = b;
-    }
-    if (batch - f >= kPrefillMinRows) chunk_first = f;
-  }
-  h->chunk_first = chunk_first;
+  if (Bg != batch) runs.clear();
+  h->chunk_runs = runs;
+  h->chunk_first = runs.empty() ? Bg : runs.front();  // Bg: none, so padded steps share a graph
   const MetaLayout ml = meta_layout(Bg, mb);
   uint8_t* mh = h->meta_host;
   if (host_tokens)
@@ -1198,6 +1219,7 @@ ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with
   for (int i = 0; i < n; ++i) {
     h->with_lm = with_lm != 0;
     h->chunk_first = batch_sizes[i];  // decode-only layout
+    h->chunk_runs.clear();
     cudaGraphExec_t ex = nullptr;
     NS_TRY(get_graph(h, batch_sizes[i], &ex));
   }
@@ -1212,6 +1234,12 @@ ns_status ns_get_graph_report(ns_handle h, ns_graph_info* out, int capacity, int
     ++i;
   }
   *n = i;
+  return NS_OK;
+}
+
+ns_status ns_set_graph_chunks(ns_handle h, int capture) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  h->graph_chunks = capture != 0;
   return NS_OK;
 }
 
