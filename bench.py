@@ -493,12 +493,26 @@ class NanoLayerWorkload:
                         f"of 1024 rows ({sh.ffn} x {sh.hidden})")
         return prof
 
-    def report(self, steps, warmup, peaks):
+    def report(self, steps, warmup, peaks, tune=True):
         from transformer_decode_step_ns_gb300 import _lib, tuner
         flops, nbytes = self.work()
         tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
         hbm = float(peaks["hbm_gbs"]) * 1e9
         t_roof = rl.step_roofline_time(flops, nbytes, tflops, hbm)
+        if not tune:  # the named splits only (a short command for profilers)
+            rows = []
+            for label, sizes in self.LABELS.items():
+                ms = self.time_variant(None if len(sizes) == 1 else sizes, 0, steps, warmup)
+                rows.append({"split": label, "sizes": sizes, "attn_cta_budget": 0,
+                             "us": round(ms * 1e3, 1),
+                             "frac_of_roofline": round(t_roof / (ms * 1e-3), 4)})
+            best = min(rows, key=lambda r: r["us"])
+            return {"workload": "LLaMA-2-70B-shaped layer, bf16, 1024 decode rows + 1024-token "
+                                "prefill chunk, graph replay, no LM head (named splits, untuned)",
+                    "roofline_us": round(t_roof * 1e6, 1), "variants": rows,
+                    "tuned": {"sizes": best["sizes"], "attn_cta_budget": 0, "us": best["us"],
+                              "frac_of_roofline": best["frac_of_roofline"]},
+                    "device_error": _lib.device_error()}
         prof = self.interference()
 
         def step(sizes, budget):
@@ -829,6 +843,73 @@ class ServingWorkload:
                 "device_error": self.dev.device_error()}
 
 
+# ---------------------------------------------------------------------------------- KV transfers
+
+class OffloadWorkload:
+    """KV save and reload of one 4096-token request with the LLaMA-3-8B KV geometry (32 layers,
+    8 KV heads, head_dim 128, bf16: 512 MiB of K/V rows), through a handle whose dense weights
+    are small (hidden 1024, 8 Q heads, FFN 1024, vocab 1024) since only the cache is touched.
+    The request's 256 blocks are a seeded permutation of a 1024-block pool.  Times, with CUDA
+    events: ns_kv_save (gather kernel + one D2H copy) and ns_kv_reload (one H2D copy + scatter
+    kernel) from pinned memory, and plain copies of the same bytes."""
+
+    n_tok, bs = 4096, 16
+
+    def __init__(self):
+        import dataclasses
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        seed = synth.config_seed(4)
+        sh = dataclasses.replace(synth.llama3_8b_shape(32), hidden=1024, n_q_heads=8, ffn=1024,
+                                 vocab=1024, tie_embeddings=True)
+        self.shape = sh
+        nblk = self.n_tok // self.bs
+        self.num_blocks = 4 * nblk
+        w = synth.model_weights_device(sh, seed)
+        self.dev = _lib.DecodeStep(sh, w, 1, nblk + 1, use_graphs=False)
+        del w
+        self.dev.kv_alloc(self.num_blocks, self.bs)
+        stream = torch.cuda.current_stream().cuda_stream
+        n = self.dev.kv_pool_bytes() // 2
+        for l in range(sh.n_layers):
+            k, v = self.dev.kv_layer_ptrs(l)
+            synth.fill_normal_device(k, n, seed, f"off.k{l}", "bf16", stream=stream)
+            synth.fill_normal_device(v, n, seed, f"off.v{l}", "bf16", stream=stream)
+        self.table = synth.permutation(seed, "off.table", self.num_blocks)[:nblk].astype(np.int32)
+        self.host = torch.empty((sh.n_layers, self.n_tok, self.dev.kv_row_elems()),
+                                dtype=torch.int16).pin_memory()
+        torch.cuda.synchronize()
+
+    def report(self, reps=5):
+        import torch
+        nbytes = self.host.numel() * 2
+        dev_buf = torch.empty_like(self.host, device="cuda")
+
+        def timed(fn):
+            fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        save = timed(lambda: self.dev.kv_save(self.host, self.n_tok, 0, self.table))
+        reload = timed(lambda: self.dev.kv_reload(self.host, self.n_tok, 0, self.table))
+        d2h = timed(lambda: self.host.copy_(dev_buf, non_blocking=True))
+        h2d = timed(lambda: dev_buf.copy_(self.host, non_blocking=True))
+        return {"workload": "KV save/reload of one 4096-token request, 32 layers x 8 KV heads x d128 "
+                            "bf16 (512 MiB of rows), 256 permuted blocks of a 1024-block pool, "
+                            "pinned host memory",
+                "bytes": nbytes, "save_ms": round(save, 3), "reload_ms": round(reload, 3),
+                "plain_d2h_ms": round(d2h, 3), "plain_h2d_ms": round(h2d, 3),
+                "save_gbs": round(nbytes / save * 1e-6, 1), "reload_gbs": round(nbytes / reload * 1e-6, 1),
+                "plain_h2d_gbs": round(nbytes / h2d * 1e-6, 1), "plain_d2h_gbs": round(nbytes / d2h * 1e-6, 1),
+                "device_error": self.dev.device_error()}
+
+
 # ---------------------------------------------------------------------------------- main arms
 
 KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_gemm.cu",
@@ -1099,7 +1180,7 @@ def run_attention_only(args, rank, world):
 
 def run_extra_only(args, rank, world):
     """One of the extra workloads alone, as its own JSON line (--nanobatch-only,
-    --continuous-only, --serving-only)."""
+    --continuous-only, --serving-only, --offload-only)."""
     import torch
     import __graft_entry__ as ge
     ge.build()
@@ -1107,12 +1188,18 @@ def run_extra_only(args, rank, world):
     peaks, src = load_peaks()
     if args.nanobatch_only:
         nw = NanoLayerWorkload()
-        r = nw.report(max(args.steps, 1), args.warmup, peaks)
+        r = nw.report(max(args.steps, 1), args.warmup, peaks, tune=not args.no_tune)
         line = {"metric": "70B-layer step time, dense batch 2048 (1024 decode + 1024 prefill)",
                 "value": r["tuned"]["us"], "unit": "us", "higher_is_better": False,
                 "n_gpus": world, "steps": max(args.steps, 1), "warmup": args.warmup,
                 "dtype": "bf16", "data": "synthetic", "config": {"workload": r["workload"]},
                 "nanobatch_layer": r}
+    elif args.offload_only:
+        r = OffloadWorkload().report()
+        line = {"metric": "KV reload GB/s (contiguous H2D + scatter into pages)", "unit": "GB/s",
+                "value": r["reload_gbs"], "higher_is_better": True, "n_gpus": world, "steps": 5,
+                "warmup": 1, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": r["workload"]}, "offload": r}
     elif args.serving_only:
         r = ServingWorkload().report()
         line = {"metric": "serving output tokens/s, constant dense batch", "unit": "tokens/s",
@@ -1189,6 +1276,10 @@ def main():
     ap.add_argument("--skip-continuous", action="store_true")
     ap.add_argument("--continuous-steps", type=int, default=2000)
     ap.add_argument("--skip-serving", action="store_true")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="with --nanobatch-only: time the named splits only, no tuner")
+    ap.add_argument("--offload-only", action="store_true",
+                    help="time KV save/reload of one request alone")
     ap.add_argument("--serving-only", action="store_true",
                     help="run the batch-former serving workload alone")
     ap.add_argument("--nanobatch-only", action="store_true",
@@ -1217,7 +1308,7 @@ def main():
             run_reference(args, rank, world)
         elif args.attention_only:
             run_attention_only(args, rank, world)
-        elif args.nanobatch_only or args.continuous_only or args.serving_only:
+        elif args.nanobatch_only or args.continuous_only or args.serving_only or args.offload_only:
             run_extra_only(args, rank, world)
         else:
             run_ours(args, rank, world)
