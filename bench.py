@@ -914,7 +914,7 @@ class OffloadWorkload:
 
 KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_gemm.cu",
                  "o_proj": "k_gemm.cu", "gate_up": "k_gemm.cu", "down": "k_gemm.cu",
-                 "lm_head": "k_gemm.cu"}
+                 "lm_head": "k_gemm.cu", "prefill": "k_prefill.cu", "kv_copy": "k_misc.cu"}
 
 
 def kernel_source_hash(kind):

@@ -146,18 +146,20 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int v
 
 // KV offload and reload (NanoFlow, "Runtime details that keep the pipeline fed"): K/V travel to
 // and from the host as contiguous rows, and only on the device are they scattered into (or
-// gathered from) the fragmented pages.  A thread moves 16 bytes: 8 elements of one head of one
-// token, consecutive threads consecutive 16-byte pieces of a row, so both sides are coalesced
-// (a head's d elements are contiguous in a page).  Grid-stride over every piece.
+// gathered from) the fragmented pages.  A thread moves one 16-byte piece per grid stride: 8
+// elements of one head of one token; consecutive threads take consecutive pieces of a row, so
+// both sides are coalesced (a head's d elements are contiguous in a page).  The index
+// arithmetic is 32-bit when the piece count allows.
+template <typename I>
 __global__ void __launch_bounds__(256) kv_copy_kernel(const KvCopyParams p) {
   const int kvd = p.n_kv_heads * p.head_dim;
-  const int per_row = kvd / 4;  // 16-byte pieces of a (layer, token) row of 2 * kvd elements
-  const long long total = static_cast<long long>(p.n_layers) * p.n * per_row;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += stride) {
-    const long long r = u / per_row;
+  const I per_row = kvd / 4;  // 16-byte pieces of a (layer, token) row of 2 * kvd elements
+  const I total = static_cast<I>(p.n_layers) * p.n * per_row;
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I u = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += stride) {
+    const I r = u / per_row;
     const int c = static_cast<int>(u - r * per_row) * 8;  // element within the row
-    const int l = static_cast<int>(r / p.n), t = static_cast<int>(r - static_cast<long long>(l) * p.n);
+    const I l = r / p.n, t = r - l * p.n;
     const int kv = c >= kvd ? 1 : 0, col = c - kv * kvd;
     const int kvh = col / p.head_dim, dim = col - kvh * p.head_dim;
     const long long slot = p.slots[t];
@@ -179,10 +181,20 @@ __global__ void __launch_bounds__(256) kv_copy_kernel(const KvCopyParams p) {
 cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s) {
   const long long pieces = static_cast<long long>(p.n_layers) * p.n * (p.n_kv_heads * p.head_dim / 4);
   if (pieces <= 0) return cudaSuccess;
-  // up to eight 256-thread CTAs per SM, a whole number of waves when the copy is large
+  const bool narrow = pieces + 2LL * 256 * 16 * sms < (1LL << 31);  // u + stride stays in int32
+  // one wave of resident CTAs (grid-stride beyond), fewer when the copy is small
+  static int per_sm[2] = {0, 0};
+  int& ps = per_sm[narrow ? 1 : 0];
+  if (ps == 0) {
+    cudaError_t e = narrow ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, kv_copy_kernel<int>, 256, 0)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, kv_copy_kernel<long long>, 256, 0);
+    if (e != cudaSuccess || ps < 1) ps = 1;
+  }
   const long long need = (pieces + 255) / 256;
-  const int grid = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
-  kv_copy_kernel<<<grid, 256, 0, s>>>(p);
+  const long long wave = static_cast<long long>(ps) * sms;
+  const int grid = static_cast<int>(need < wave ? need : wave);
+  if (narrow) kv_copy_kernel<int><<<grid, 256, 0, s>>>(p);
+  else kv_copy_kernel<long long><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
