@@ -25,6 +25,9 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "ns_internal.h"
 #include "ns_ptx.cuh"
@@ -577,27 +580,78 @@ size_t gemm_smem_bytes(int BN, int nstage) {
          kCtrlBytes;
 }
 
-int gemm_pick_stages(int BN, int kb_per_split, int ctas, int sms) {
+namespace {
+
+template <typename T>
+cudaError_t gemm_configure() {
+  static int configured_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 31 && !(configured_mask & (1 << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured_mask |= 1 << dev;
+  }
+  return cudaSuccess;
+}
+
+// How many clusters of `splits` CTAs with `smem` bytes of dynamic shared memory each the
+// current device holds at once (the occupancy API places clusters within GPCs); cached.
+int gemm_resident_clusters(int splits, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, splits, smem);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  if (gemm_configure<__half>() == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, splits, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<__half>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+}  // namespace
+
+int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits) {
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
   // the epilogue tile [rows][128] fp32 reuses the stage ring
   const size_t tile_rows = gemm_two_pass(BN) ? kPassRows : BN;
   const int tile_min = static_cast<int>((tile_rows * kGemmTileN * 4 + stage - 1) / stage);
   const size_t half_sm = 113 * 1024 - 1024 - kCtrlBytes;
-  // Wide tiles run two CTAs per SM (one's epilogue overlapping the other's main loop) unless
-  // the grid is small enough to sit comfortably at one per SM: a grid needing 90 % or more of
-  // the SMs at one CTA each did not fit in one wave once its clusters were placed.
-  if (BN <= 64 || (gemm_two_pass(BN) && ctas * 10 >= sms * 9)) {
-    // Half an SM: for decode batches the next kernel's CTAs can be resident (streaming their
-    // own weights) while this one runs.  As many stages as the CTA's k-range needs.
-    int n = static_cast<int>(half_sm / stage);
-    n = std::min(n, std::max(kb_per_split, 2));
-    return std::max(n, std::max(tile_min, 2));
-  }
   // one CTA per SM: a deep ring keeps enough weight bytes in flight
   const size_t budget = 227 * 1024 - 1024 - kCtrlBytes;
-  int n = static_cast<int>(budget / stage);
-  if (n > 8) n = 8;
-  return std::max(n, std::max(tile_min, gemm_two_pass(BN) ? 2 : 4));
+  const int deep = std::max(std::min(static_cast<int>(budget / stage), 8),
+                            std::max(tile_min, gemm_two_pass(BN) ? 2 : 4));
+  // Half an SM: two CTAs per SM, one's epilogue overlapping the other's main loop; for decode
+  // batches (narrow tiles) the next kernel's CTAs can be resident, streaming their own
+  // weights, while this one runs.  As many stages as the CTA's k-range needs.
+  const int half = std::max(std::min(static_cast<int>(half_sm / stage), std::max(kb_per_split, 2)),
+                            std::max(tile_min, 2));
+  if (BN <= 64) return half;
+  // A wide tile takes the deep ring when the whole grid is resident with it in one wave (the
+  // clusters placed as the hardware places them), else two per SM.
+  if (gemm_two_pass(BN)) return clusters <= gemm_resident_clusters(splits, gemm_smem_bytes(BN, deep)) ? deep : half;
+  return deep;
 }
 
 uint32_t gemm_idesc(int dtype, int BN) {
@@ -612,16 +666,9 @@ namespace {
 template <typename T>
 cudaError_t launch_gemm_t(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                           cudaStream_t s, bool pdl) {
-  static int configured_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
   const size_t smem = gemm_smem_bytes(p.BN, p.nstage);
-  if (dev < 31 && !(configured_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_mask |= 1 << dev;
-  }
+  cudaError_t e = gemm_configure<T>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.M + p.BN - 1) / p.BN, p.splits, p.N / kGemmTileN);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);

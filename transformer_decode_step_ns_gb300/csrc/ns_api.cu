@@ -432,8 +432,7 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   p.BN = pick_bn(m);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split,
-                              ((m + p.BN - 1) / p.BN) * p.splits * (p.N / kGemmTileN), h->sms);
+  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
   p.epi = epi;
   p.idesc = gemm_idesc(h->dtype, p.BN);
   p.err = h->err;
@@ -1484,8 +1483,7 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   p.BN = pick_bn(m);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split,
-                              ((m + p.BN - 1) / p.BN) * p.splits * (p.N / kGemmTileN), device_sms());
+  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
   p.epi = EPI_F32;
   p.idesc = gemm_idesc(dtype, p.BN);
   DevScratch* sc = nullptr;

@@ -142,8 +142,9 @@ struct EmbedParams {
 constexpr int kPassRows = 128;
 __host__ __device__ inline bool gemm_two_pass(int BN) { return BN > kPassRows; }
 size_t gemm_smem_bytes(int BN, int nstage);
-// Stage-ring depth for a launch of `ctas` CTAs (the depth never changes results).
-int gemm_pick_stages(int BN, int kb_per_split, int ctas, int sms);
+// Stage-ring depth for a launch of `clusters` clusters of `splits` CTAs (the depth never changes
+// results).
+int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits);
 uint32_t gemm_idesc(int dtype, int BN);
 cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                         int dtype, cudaStream_t s, bool pdl);
