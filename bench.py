@@ -1010,6 +1010,7 @@ def run_ours(args, rank, world):
     ms_total, units = replica_aggregate(ms_total, wl.B * K, world)
     dev_err = wl.dev.device_error()
     info = wl.dev.info()
+    graphs = wl.dev.graph_report()
     ms_step = ms_total / K
     value = units / (ms_total * 1e-3)
 
@@ -1147,6 +1148,8 @@ def run_ours(args, rank, world):
         "gpu_launches": info.kernels_per_step * K,
         "kernels_per_step": info.kernels_per_step,
         "graph_capture_ms": info.last_capture_ms,
+        "graphs": [{k: (round(v, 3) if isinstance(v, float) else v) for k, v in g.items()}
+                   for g in graphs],
         "device_error": dev_err,
     }
     print(json.dumps(line), flush=True)

@@ -208,8 +208,11 @@ ns_status ns_sched_commit(ns_sched s, const int32_t* sampled, int batch, int32_t
 /* Tokens generated so far by a request (running, preempted or finished): *n = their count, the
  * first min(*n, capacity) copied to out. */
 ns_status ns_sched_tokens(ns_sched s, int request_id, int32_t* out, int capacity, int* n);
-/* Requests with prompt tokens left, running, preempted, finished. */
+/* Requests with prompt tokens left, running, preempted, and finished ones not yet removed. */
 ns_status ns_sched_counts(ns_sched s, int* waiting, int* running, int* preempted, int* finished);
+/* Forget a finished request (its tokens and id); INVALID_ARG for an unknown or unfinished id.
+ * A long-running caller removes requests once it has read their tokens. */
+ns_status ns_sched_remove(ns_sched s, int request_id);
 
 /* Host validation of one step's metadata, exactly as ns_decode_step performs it before
  * anything is launched: 1 <= batch <= max_batch; token ids in [0, vocab); positions >= 0;

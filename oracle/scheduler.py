@@ -225,8 +225,14 @@ class DenseBatchFormer:
     def tokens(self, rid: int) -> List[int]:
         return list(self.req[rid].gen)
 
+    def remove(self, rid: int) -> None:
+        """Forget a finished request."""
+        if rid not in self.req or not self.req[rid].finished:
+            raise SchedulerError("unknown or unfinished request")
+        del self.req[rid]
+
     def counts(self):
-        """(requests with prompt left, running, preempted, finished)."""
+        """(requests with prompt left, running, preempted, finished and not removed)."""
         fin = sum(1 for r in self.req.values() if r.finished)
         return len(self.prefill), len(self.running), len(self.swapped), fin
 

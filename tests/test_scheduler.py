@@ -273,6 +273,12 @@ def test_library_former_errors(L):
     np.testing.assert_array_equal(s["token_ids"], [1, 2])
     f.commit([9, 9])
     assert f.counts() == (0, 1, 0, 1) and f.tokens(1) == [9]
+    with pytest.raises(L.NSError):
+        f.remove(1)                       # still running
+    f.remove(0)                           # finished: forgotten
+    assert f.counts() == (0, 1, 0, 0)
+    with pytest.raises(L.NSError):
+        f.tokens(0)
     assert L.BatchFormer(pool, 1, 4, 0).counts() == (0, 0, 0, 0)
     with pytest.raises(L.NSError):
         L.BatchFormer(pool, 4, 4, 0, -1)

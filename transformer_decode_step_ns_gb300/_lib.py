@@ -38,7 +38,7 @@ SYMBOLS = (
     "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
-    "ns_set_graph_chunks",
+    "ns_set_graph_chunks", "ns_sched_remove",
 )
 
 
@@ -138,6 +138,7 @@ def lib() -> ctypes.CDLL:
             "ns_sched_counts": ([P] + [ctypes.POINTER(I)] * 4, I),
             "ns_capture_graphs": ([P, I, P, I], I),
             "ns_set_graph_chunks": ([P, I], I),
+            "ns_sched_remove": ([P, I], I),
             "ns_attn_decode_capped": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P], I),
             "ns_get_graph_report": ([P, P, I, ctypes.POINTER(I)], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
@@ -579,8 +580,12 @@ class BatchFormer:
         check(lib().ns_sched_tokens(self.h, request_id, _ptr(out), n.value, ctypes.byref(n)))
         return out[:n.value].tolist()
 
+    def remove(self, request_id: int) -> None:
+        """Forget a finished request."""
+        check(lib().ns_sched_remove(self.h, request_id))
+
     def counts(self):
-        """(requests with prompt left, running, preempted, finished)."""
+        """(requests with prompt left, running, preempted, finished and not removed)."""
         w, r, p, f = I(), I(), I(), I()
         check(lib().ns_sched_counts(self.h, ctypes.byref(w), ctypes.byref(r), ctypes.byref(p),
                                     ctypes.byref(f)))

@@ -268,6 +268,15 @@ ns_status ns_sched_tokens(ns_sched s, int request_id, int32_t* out, int capacity
   return NS_OK;
 }
 
+ns_status ns_sched_remove(ns_sched s, int request_id) {
+  if (s == nullptr) return err(NS_ERR_INVALID_ARG, "null argument");
+  auto it = s->req.find(request_id);
+  if (it == s->req.end()) return err(NS_ERR_INVALID_ARG, "unknown request id");
+  if (!it->second.finished) return err(NS_ERR_INVALID_ARG, "request not finished");
+  s->req.erase(it);
+  return NS_OK;
+}
+
 ns_status ns_sched_counts(ns_sched s, int* waiting, int* running, int* preempted, int* finished) {
   if (s == nullptr || !waiting || !running || !preempted || !finished)
     return err(NS_ERR_INVALID_ARG, "null argument");
