@@ -100,8 +100,11 @@ __global__ void __launch_bounds__(32 * G) prefill_attn_kernel(const PrefillParam
   using S = PrefillShape<D>;
   __shared__ __align__(128) uint8_t ring[S::NST * S::STAGE];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.x * 16;  // first query of the tile (chunk-relative)
-  const int g = blockIdx.y;
+  // Grid (kv heads, query tiles), launched in that order: every head's longest tile first (the
+  // work of a tile grows with its position along the causal triangle), so the short ones fill
+  // the tail.  q0 is the tile's first query (chunk-relative).
+  const int q0 = (gridDim.y - 1 - blockIdx.y) * 16;
+  const int g = blockIdx.x;
   const int h = g * G + warp;      // this warp's q head
   const int Hkv = p.n_kv_heads;
   griddep_wait();  // q and the chunk's K/V come from the QKV projection of this step
@@ -269,7 +272,7 @@ namespace {
 template <typename T, int D, int G>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.chunk + 15) / 16, p.n_kv_heads, 1);
+  cfg.gridDim = dim3(p.n_kv_heads, (p.chunk + 15) / 16, 1);
   cfg.blockDim = dim3(32 * G, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
