@@ -28,7 +28,7 @@
 #include <vector>
 
 #include "ns.h"
-#include "ns_internal.h"
+#include "ns_host.h"
 
 using namespace ns;
 

@@ -1,0 +1,34 @@
+// Host-side interfaces of the kernel files, used by the runtime (ns_api.cu, ns_noalloc.cu,
+// ns_sched.cpp): launchers, launch-shape choices and the error-message setter.  Device code
+// does not depend on this file.
+#pragma once
+
+#include "ns_internal.h"
+
+namespace ns {
+
+// Kernel launchers return the launch error; `pdl` adds programmatic stream serialisation.
+size_t gemm_smem_bytes(int BN, int nstage);
+// Stage-ring depth for a launch of `clusters` clusters of `splits` CTAs (the depth never changes
+// results).
+int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits);
+uint32_t gemm_idesc(int dtype, int BN);
+cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                        int dtype, cudaStream_t s, bool pdl);
+
+bool attn_supported(int head_dim, int group, int block_size);
+int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
+cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, int group,
+                           cudaStream_t s, bool pdl);
+cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
+                        cudaStream_t s, bool pdl);
+
+cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
+cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
+                          cudaStream_t s);
+cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s);
+
+// Record the text ns_last_error_message() returns on this thread.
+void set_last_error(const char* msg);
+
+}  // namespace ns

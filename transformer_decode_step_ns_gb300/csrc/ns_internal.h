@@ -1,4 +1,5 @@
-// Internal interfaces between the host runtime (ns_api.cu) and the kernels.
+// Types and inline functions shared by the kernels and the host runtime (ns_api.cu): parameter
+// blocks, tile constants and the attention split.  Host-only declarations are in ns_host.h.
 #pragma once
 
 #include <cuda.h>
@@ -136,25 +137,11 @@ struct EmbedParams {
   int* err;
 };
 
-// Kernel launchers (return the launch error; `pdl` adds programmatic stream serialisation).
 // A GEMM tile wider than kPassRows tokens stages its accumulator in shared memory
 // kPassRows tokens at a time, so its stage ring may be two stages (two CTAs per SM).
 constexpr int kPassRows = 128;
 __host__ __device__ inline bool gemm_two_pass(int BN) { return BN > kPassRows; }
-size_t gemm_smem_bytes(int BN, int nstage);
-// Stage-ring depth for a launch of `clusters` clusters of `splits` CTAs (the depth never changes
-// results).
-int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits);
-uint32_t gemm_idesc(int dtype, int BN);
-cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
-                        int dtype, cudaStream_t s, bool pdl);
 
-bool attn_supported(int head_dim, int group, int block_size);
-int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
-cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, int group,
-                           cudaStream_t s, bool pdl);
-cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
-                        cudaStream_t s, bool pdl);
 // Split of a row of length L (a function of L alone, 16-token blocks): ceil(L / 16) blocks in
 // ceil(blocks / 64) superchunks of ceil(blocks / superchunks) blocks; a CTA's warps share one
 // superchunk.  attn_max_chunks bounds the superchunk count of any L <= L_max.
@@ -174,12 +161,6 @@ __host__ __device__ inline int attn_max_chunks(int L_max) {
   return c < 1 ? 1 : (c < kAttnMaxChunks ? c : kAttnMaxChunks);
 }
 
-
-// Record the text ns_last_error_message() returns on this thread.
-void set_last_error(const char* msg);
-
-cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
-
 // Copy between the paged pools and a contiguous buffer [n_layers][n][2][kv_dim] whose row
 // (layer, t) holds the K then V of the token at slot slots[t] (see ns_kv_reload / ns_kv_save).
 struct KvCopyParams {
@@ -192,8 +173,5 @@ struct KvCopyParams {
   int to_pool;              // 1: buf -> pages, 0: pages -> buf
   int* err;
 };
-cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s);
-cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
-                          cudaStream_t s);
 
 }  // namespace ns

@@ -19,7 +19,7 @@
 #include <string>
 
 #include "ns.h"
-#include "ns_internal.h"
+#include "ns_host.h"
 
 namespace {
 
