@@ -33,6 +33,18 @@ def test_attention_matches_oracle(cuda_lib, n_q, n_kv, d, dtype, lens):
     assert np.abs(got - ref).max() < 3e-2
 
 
+def test_attention_at_the_longest_supported_row(cuda_lib):
+    """Rows of 65,536 tokens (4096 blocks: the 64-superchunk cap), one past half of it, and 1,
+    next to each other; each matches the oracle."""
+    lens = [65536, 32769, 1]
+    q, kp, vp, tab, sl, nb = attention_case(13, lens, 32, 8, 128, "bf16", mb=4096)
+    got = storage_f64(run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb), "bf16")
+    ref = oracle_attention(q, kp, vp, tab, sl, 128, "bf16")
+    for b in range(len(lens)):
+        assert rel_l2(got[b], ref[b]) < 1e-2, b
+    assert np.abs(got - ref).max() < 3e-2
+
+
 def test_attention_single_cached_token_returns_v_exactly(cuda_lib):
     q, kp, vp, tab, sl, nb = attention_case(4, [1, 1, 1], 32, 8, 128, "bf16")
     got = run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb)

@@ -337,6 +337,25 @@ def test_graph_bucket_arguments_are_validated(cuda_lib):
     h.dev.set_graph_buckets(None)
 
 
+def test_step_at_the_largest_batch(cuda_lib):
+    """4096 rows (the largest batch a handle takes: 16 token tiles of 256 in every projection),
+    contexts 0..63 cycling; sampled rows match the oracle, which computes them alone."""
+    shape = _tiny("bf16")
+    ctx = [i % 64 for i in range(4096)]
+    h = Harness(shape, 181, ctx, max_batch=4096)
+    got = h.run_gpu()
+    assert np.isfinite(got).all()
+    rows = [0, 63, 1000, 2047, 4095]
+    b = h.batch
+    model = oracle.OracleModel.from_weights(h.shape, h.w)
+    kp = [k.copy() for k in h.kp]
+    vp = [v.copy() for v in h.vp]
+    ref = oracle.decode_step(model, kp, vp, b.token_ids[rows], b.positions[rows], b.block_tables[rows],
+                             b.seq_lens[rows], b.slot_mapping[rows], h.bs)
+    assert rel_l2(got[rows], ref) < 1e-2
+    assert np.abs(got[rows] - ref).max() < 5e-2
+
+
 def test_rows_alone_equal_rows_in_batch_bitwise(cuda_lib):
     shape = _tiny("f16")
     ctx = [9, 33, 129]
