@@ -918,8 +918,10 @@ KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_
 
 
 def kernel_source_hash(kind):
-    """sha256 (first 16 hex digits) of the kernel's source file and the shared headers, with
-    comments and whitespace removed (an edit of comments does not change the kernel)."""
+    """sha256 (first 16 hex digits) of the device code of the kernel's source file (the text
+    before its "host side" marker: launchers and launch-shape choices after it do not change
+    what the kernel does) and of the shared device headers, with comments and whitespace
+    removed (an edit of comments does not change the kernel)."""
     import hashlib
     import re
     base = kind.split("_cfg")[0]
@@ -928,6 +930,9 @@ def kernel_source_hash(kind):
     for f in (KERNEL_SOURCE.get(base, "k_gemm.cu"), "ns_ptx.cuh", "ns_internal.h"):
         with open(os.path.join(csrc, f)) as fh:
             src = fh.read()
+        cut = re.search(r"^// -+ host side$", src, flags=re.M)
+        if cut is not None:
+            src = src[:cut.start()]
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
         h.update(re.sub(r"\s+", "", src).encode())

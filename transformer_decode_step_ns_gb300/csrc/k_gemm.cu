@@ -648,10 +648,9 @@ int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits) {
   const int half = std::max(std::min(static_cast<int>(half_sm / stage), std::max(kb_per_split, 2)),
                             std::max(tile_min, 2));
   if (BN <= 64) return half;
-  // A wide tile takes the deep ring when the whole grid is resident with it in one wave (the
+  // A wider tile takes the deep ring when the whole grid is resident with it in one wave (the
   // clusters placed as the hardware places them), else two per SM.
-  if (gemm_two_pass(BN)) return clusters <= gemm_resident_clusters(splits, gemm_smem_bytes(BN, deep)) ? deep : half;
-  return deep;
+  return clusters <= gemm_resident_clusters(splits, gemm_smem_bytes(BN, deep)) ? deep : half;
 }
 
 uint32_t gemm_idesc(int dtype, int BN) {

@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(256) kv_copy_kernel(const KvCopyParams p) {
   }
 }
 
+// ------------------------------------------------------------------------------ host side
+
 cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s) {
   const long long pieces = static_cast<long long>(p.n_layers) * p.n * (p.n_kv_heads * p.head_dim / 4);
   if (pieces <= 0) return cudaSuccess;
