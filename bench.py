@@ -65,7 +65,7 @@ def load_peaks():
 # ---------------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 50 ms; the report keeps the samples taken inside the window
+    """nvidia-smi samples every 20 ms; the report keeps the samples taken inside the window
     marked by mark_start() / mark_stop() (host wall clock), else the ones nearest to it."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -83,7 +83,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-i", str(self._device_index())],
+                 "-lms", "20", "-i", str(self._device_index())],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -133,7 +133,7 @@ class ClockSampler:
             # the region was shorter than the sampling period: the nearest samples either side
             mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None else samples[-1][0]
             inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
-            where = "nearest the timed region (shorter than the 50 ms period)"
+            where = "nearest the timed region (shorter than the sampling period)"
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = set()
         for x in inside:
