@@ -96,11 +96,27 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // pays for (measured on 4096-wide projections at 256 rows: 22 k-blocks 46 -> 31 us, 16 k-blocks
 // 31 -> 27 us; with 56 or 64 k-blocks the 256-wide tile stays faster).  The tile never changes
 // a result.
-int pick_bn(int m, int kb_per_split) {
-  const int cap = (m > 128 && m <= 256 && kb_per_split <= 32) ? 128 : kMaxBN;
+int pick_bn_capped(int m, int cap) {
   const int tiles = (m + cap - 1) / cap;
   int bn = round_up((m + tiles - 1) / tiles, 16);
   return std::max(16, std::min(cap, bn));
+}
+
+// Above 256 rows a launch without split-K also compares the two widths by their waves of two
+// CTAs per SM, charging each CTA 64 + BN token-columns of work (a fixed cost plus its tile),
+// and takes the 128-token tile when that is at least 10 % less (the 4096 x 28672 gate/up
+// projection at 512 rows: 1.47 -> 2.95 waves, 160 -> 143 us).
+int pick_bn(int m, int kb_per_split, int splits, int n_tiles, int sms) {
+  if (m > 128 && m <= 256 && kb_per_split <= 32) return pick_bn_capped(m, 128);
+  const int wide = pick_bn_capped(m, kMaxBN);
+  if (m <= 256 || splits != 1) return wide;
+  const int narrow = pick_bn_capped(m, 128);
+  const long long slots = 2LL * sms;
+  auto cost = [&](int bn) {
+    const long long ctas = static_cast<long long>((m + bn - 1) / bn) * n_tiles;
+    return ((ctas + slots - 1) / slots) * (64 + bn);
+  };
+  return cost(narrow) * 10 <= cost(wide) * 9 ? narrow : wide;
 }
 
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
@@ -435,7 +451,7 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   p.row0 = row0;
   p.N = pr.N;
   p.K = pr.K;
-  p.BN = pick_bn(m, pr.kb_per);
+  p.BN = pick_bn(m, pr.kb_per, pr.splits, pr.N / kGemmTileN, h->sms);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
   p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
@@ -1486,7 +1502,7 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   p.row0 = 0;
   p.N = n;
   p.K = k;
-  p.BN = pick_bn(m, pr.kb_per);
+  p.BN = pick_bn(m, pr.kb_per, pr.splits, pr.N / kGemmTileN, device_sms());
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
   p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
