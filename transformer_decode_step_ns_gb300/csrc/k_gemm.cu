@@ -582,16 +582,19 @@ size_t gemm_smem_bytes(int BN, int nstage) {
 
 namespace {
 
+// Raise the kernel's dynamic shared-memory limit once per device (threads may race to do it;
+// setting the attribute twice is harmless).
 template <typename T>
 cudaError_t gemm_configure() {
-  static int configured_mask = 0;
+  static unsigned configured_mask = 0;  // accessed with atomic builtins
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 31 && !(configured_mask & (1 << dev))) {
+  const unsigned bit = dev < 31 ? 1u << dev : 0u;
+  if (bit == 0 || !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
-    configured_mask |= 1 << dev;
+    __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
   }
   return cudaSuccess;
 }

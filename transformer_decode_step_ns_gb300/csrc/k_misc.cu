@@ -184,14 +184,19 @@ cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s) {
   const long long pieces = static_cast<long long>(p.n_layers) * p.n * (p.n_kv_heads * p.head_dim / 4);
   if (pieces <= 0) return cudaSuccess;
   const bool narrow = pieces + 2LL * 256 * 16 * sms < (1LL << 31);  // u + stride stays in int32
-  // one wave of resident CTAs (grid-stride beyond), fewer when the copy is small
-  static int per_sm[2] = {0, 0};
-  int& ps = per_sm[narrow ? 1 : 0];
-  if (ps == 0) {
-    cudaError_t e = narrow ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, kv_copy_kernel<int>, 256, 0)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, kv_copy_kernel<long long>, 256, 0);
-    if (e != cudaSuccess || ps < 1) ps = 1;
-  }
+  // one wave of resident CTAs (grid-stride beyond), fewer when the copy is small; the
+  // occupancy of each instantiation is queried once (thread-safe static initialisation)
+  auto occupancy = [](auto kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    return n;
+  };
+  static const int per_sm_narrow = occupancy(kv_copy_kernel<int>);
+  static const int per_sm_wide = occupancy(kv_copy_kernel<long long>);
+  const int ps = narrow ? per_sm_narrow : per_sm_wide;
   const long long need = (pieces + 255) / 256;
   const long long wave = static_cast<long long>(ps) * sms;
   const int grid = static_cast<int>(need < wave ? need : wave);
