@@ -910,6 +910,60 @@ class OffloadWorkload:
                 "device_error": self.dev.device_error()}
 
 
+# ---------------------------------------------------------------------------------- projections alone
+
+class GemmWorkload:
+    """The LLaMA-3-8B projections alone through ns_linear (the step's GEMM kernel with a plain
+    fp32 epilogue) at `rows` rows: QKV 6144 x 4096, O 4096 x 4096, gate/up 28672 x 4096, down
+    4096 x 14336, bf16 weights N(0, 0.02) and activations N(0, 1) from the seed.  Each launch is
+    timed alone with CUDA events after a write of 256 MiB that flushes L2; the median of `reps`."""
+
+    SHAPES = {"qkv": (6144, 4096), "o": (4096, 4096), "gate_up": (28672, 4096), "down": (4096, 14336)}
+
+    def __init__(self, rows):
+        import torch
+        self.rows = rows
+        seed = synth.config_seed(4)
+        self.w = {k: synth.normal_device(seed, f"gemm.{k}", (n, kk), "bf16", std=0.02)
+                  for k, (n, kk) in self.SHAPES.items()}
+        self.x = {k: synth.normal_device(seed, f"gemm.x.{k}", (rows, kk), "bf16")
+                  for k, (n, kk) in self.SHAPES.items()}
+        self.y = {k: torch.empty((rows, n), dtype=torch.float32, device="cuda")
+                  for k, (n, kk) in self.SHAPES.items()}
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def report(self, peaks, reps=20):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        tflops = float(peaks.get("bf16_tflops", 1900)) * 1e12
+        hbm = float(peaks["hbm_gbs"]) * 1e9
+        out = {}
+        for k, (n, kk) in self.SHAPES.items():
+            m = self.rows
+            for _ in range(3):
+                _lib.linear(self.w[k], self.x[k], self.y[k], m, n, kk, "bf16")
+            ts = []
+            for _ in range(reps):
+                self.flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                _lib.linear(self.w[k], self.x[k], self.y[k], m, n, kk, "bf16")
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e-3)
+            t = float(np.median(ts))
+            flops = 2.0 * m * n * kk
+            nbytes = n * kk * 2 + m * kk * 2 + m * n * 4
+            roof = max(flops / tflops, nbytes / hbm)
+            out[k] = {"us": round(t * 1e6, 1), "tflops": round(flops / t / 1e12, 1),
+                      "gbs": round(nbytes / t / 1e9, 1), "roofline_us": round(roof * 1e6, 1),
+                      "bound": "tensor" if flops / tflops >= nbytes / hbm else "hbm",
+                      "frac_of_roofline": round(roof / t, 4)}
+        return {"workload": f"LLaMA-3-8B projections alone at {self.rows} rows, bf16, L2 flushed "
+                            "before each launch (peaks: burst bf16, HBM copy)",
+                "projections": out, "device_error": _lib.device_error()}
+
+
 # ---------------------------------------------------------------------------------- main arms
 
 KERNEL_SOURCE = {"embed_rope": "k_misc.cu", "attention": "k_attn.cu", "qkv": "k_gemm.cu",
@@ -1188,7 +1242,7 @@ def run_attention_only(args, rank, world):
 
 def run_extra_only(args, rank, world):
     """One of the extra workloads alone, as its own JSON line (--nanobatch-only,
-    --continuous-only, --serving-only, --offload-only)."""
+    --continuous-only, --serving-only, --offload-only, --gemm-only)."""
     import torch
     import __graft_entry__ as ge
     ge.build()
@@ -1202,6 +1256,15 @@ def run_extra_only(args, rank, world):
                 "n_gpus": world, "steps": max(args.steps, 1), "warmup": args.warmup,
                 "dtype": "bf16", "data": "synthetic", "config": {"workload": r["workload"]},
                 "nanobatch_layer": r}
+    elif args.gemm_only:
+        r = GemmWorkload(args.gemm_rows).report(peaks)
+        tot = sum(v["us"] for v in r["projections"].values())
+        roof = sum(v["roofline_us"] for v in r["projections"].values())
+        line = {"metric": "projection time per layer, LLaMA-3-8B shapes", "unit": "us",
+                "value": round(tot, 1), "higher_is_better": False, "n_gpus": world, "steps": 20,
+                "warmup": 3, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": r["workload"]}, "frac_of_roofline": round(roof / tot, 4),
+                "gemm": r}
     elif args.offload_only:
         r = OffloadWorkload().report()
         line = {"metric": "KV reload GB/s (contiguous H2D + scatter into pages)", "unit": "GB/s",
@@ -1288,6 +1351,9 @@ def main():
                     help="with --nanobatch-only: time the named splits only, no tuner")
     ap.add_argument("--offload-only", action="store_true",
                     help="time KV save/reload of one request alone")
+    ap.add_argument("--gemm-only", action="store_true",
+                    help="time the LLaMA-3-8B projections alone (--gemm-rows rows)")
+    ap.add_argument("--gemm-rows", type=int, default=256)
     ap.add_argument("--serving-only", action="store_true",
                     help="run the batch-former serving workload alone")
     ap.add_argument("--nanobatch-only", action="store_true",
@@ -1316,7 +1382,8 @@ def main():
             run_reference(args, rank, world)
         elif args.attention_only:
             run_attention_only(args, rank, world)
-        elif args.nanobatch_only or args.continuous_only or args.serving_only or args.offload_only:
+        elif (args.nanobatch_only or args.continuous_only or args.serving_only or args.offload_only
+              or args.gemm_only):
             run_extra_only(args, rank, world)
         else:
             run_ours(args, rank, world)
