@@ -1136,6 +1136,32 @@ def run_ours(args, rank, world):
                  "bound": "hbm" if work.total_bytes / (hbm * 1e9) >= work.flops / tflops
                  else "tensor"}
 
+    # the same model at batch 1 and 8 (and the headline's 32): graph-replayed step time
+    sweep = []
+    if rank == 0:
+        for B in (1, 8):
+            sw = DecodeWorkload(B, total_steps=70)
+            for _ in range(5):
+                sw.step(sw.next_meta())
+            sm = [sw.next_meta() for _ in range(50)]
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for m in sm:
+                sw.step(m)
+            s1.record()
+            torch.cuda.synchronize()
+            ms = s0.elapsed_time(s1) / len(sm)
+            wk = rl.decode_step_work(sw.shape, sm[-1][3])
+            tr = rl.step_roofline_time(wk.flops, wk.total_bytes, tflops, hbm * 1e9)
+            sweep.append({"batch": B, "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                          "roofline_us": round(tr * 1e6, 1), "frac_of_roofline": round(tr / (ms * 1e-3), 4)})
+            sw.dev.close()
+            del sw
+        sweep.append({"batch": wl.B, "ms_per_step": round(ms_step, 4), "tokens_per_s": round(value / world, 1),
+                      "roofline_us": round(t_roof * 1e6, 1), "frac_of_roofline": round(t_roof / (ms_step * 1e-3), 4)})
+        torch.cuda.empty_cache()
+
     attn = None
     if not args.skip_attention and rank == 0:
         aw = AttentionWorkload(max_batch=max(SWEEP_BATCHES))
@@ -1198,6 +1224,7 @@ def run_ours(args, rank, world):
                         "step late"},
         "roofline": roof,
         "step_roofline": step_roof,
+        "batch_sweep": sweep,
         "attention": attn,
         "nanobatch_layer": nano,
         "continuous": cont,
