@@ -296,3 +296,43 @@ def test_tuner_candidate_splits():
     # a batch that is not a multiple of 128: the last nano-batch takes the remainder
     c = tuner.candidate_splits(1000)
     assert all(sum(s) == 1000 for s in c[1:]) and [128, 872] in c
+
+
+def test_tuner_interference_row_arithmetic():
+    from transformer_decode_step_ns_gb300 import tuner
+    # attention best 100 us, capped solo 200, co-run 400; GEMM solo 50, co-run 80
+    r = tuner.interference_row(64, 100e-6, 200e-6, 50e-6, 400e-6, 80e-6, 8)
+    assert r["P_attn"] == 0.25 and r["P_attn_solo"] == 0.5
+    assert r["P_gemm"] == r["R_gemm"] == 0.625 and r["R_attn"] == 0.375
+    assert r["attn_us"] == 400.0 and r["gemm_us"] == 80.0 and r["n_gemm"] == 8
+
+
+def test_tuner_search_measures_every_split_then_budgets_and_picks_the_fastest():
+    """A synthetic step cost: two-way splits near 1280 + 768 are cheapest, and a CTA budget of
+    96 helps only the best splits; the profile keeps budgets with co-run P_attn >= 0.5."""
+    from transformer_decode_step_ns_gb300 import tuner
+    calls = []
+
+    def cost(sizes, budget):
+        base = 4.0 if sizes is None else 3.7 + 0.001 * abs(sizes[0] - 1280) + 0.05 * (len(sizes) - 2)
+        return base - (0.05 if budget == 96 else 0.0) + (0.01 if budget not in (0, 96) else 0.0)
+
+    def step(sizes, budget):
+        calls.append((None if sizes is None else tuple(sizes), budget))
+
+    def timer(fn, reps):
+        calls.clear()
+        fn()
+        (sizes, budget), = calls
+        return cost(None if sizes is None else list(sizes), budget)
+
+    profile = {"rows": [{"budget": b, "P_attn": 0.6 if b >= 96 else 0.3} for b in range(8, 129, 8)]}
+    out = tuner.search(step, 2048, profile=profile, timer=timer)
+    stage1 = [r for r in out["table"] if r["budget"] == 0]
+    assert len(stage1) == len(tuner.candidate_splits(2048))
+    assert out["budgets_kept"] == [96, 104, 112, 120, 128]
+    assert len(out["table"]) == len(stage1) + 3 * 5
+    assert out["best"]["sizes"] == [1280, 768] and out["best"]["budget"] == 96
+    # without a profile every budget is tried on the three fastest splits
+    out = tuner.search(step, 2048, timer=timer)
+    assert len(out["table"]) == len(stage1) + 3 * 16

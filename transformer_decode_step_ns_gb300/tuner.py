@@ -47,6 +47,19 @@ def _timed(fn: Callable[[], None], reps: int, warmup: int = 2) -> float:
     return a.elapsed_time(b) / reps
 
 
+def interference_row(budget: int, t_attn_best: float, t_attn_capped: float, t_gemm_solo: float,
+                     t_attn_corun: float, t_gemm_corun: float, n_gemm: int) -> Dict:
+    """One row of the R -> P table from per-launch times (seconds): P of each op relative to its
+    best solo run, R_gemm = P_gemm and R_attn = 1 - R_gemm (the page's inference of a share from
+    the throughput an op keeps)."""
+    p_g = t_gemm_solo / t_gemm_corun
+    return {"budget": budget, "attn_capped_solo_us": round(t_attn_capped * 1e6, 1),
+            "attn_us": round(t_attn_corun * 1e6, 1), "gemm_us": round(t_gemm_corun * 1e6, 1),
+            "n_gemm": n_gemm, "P_attn": round(t_attn_best / t_attn_corun, 3),
+            "P_attn_solo": round(t_attn_best / t_attn_capped, 3), "P_gemm": round(p_g, 3),
+            "R_gemm": round(p_g, 3), "R_attn": round(1.0 - p_g, 3)}
+
+
 def pair_profile(attn: Callable[[int, object], None], gemm: Callable[[object], None],
                  budgets: Sequence[int] = tuple(range(8, 129, 8)), reps: int = 6) -> Dict:
     """R -> P of decode attention against a GEMM.
@@ -90,11 +103,7 @@ def pair_profile(attn: Callable[[int, object], None], gemm: Callable[[object], N
         torch.cuda.synchronize()
         ta = aa.elapsed_time(ab) / reps
         tg = ga.elapsed_time(gb) / n_g
-        p_g = t_gemm / tg
-        rows.append({"budget": b, "attn_capped_solo_us": round(t_b * 1e3, 1),
-                     "attn_us": round(ta * 1e3, 1), "gemm_us": round(tg * 1e3, 1), "n_gemm": n_g,
-                     "P_attn": round(t_attn / ta, 3), "P_attn_solo": round(t_attn / t_b, 3),
-                     "P_gemm": round(p_g, 3), "R_gemm": round(p_g, 3), "R_attn": round(1.0 - p_g, 3)})
+        rows.append(interference_row(b, t_attn * 1e-3, t_b * 1e-3, t_gemm * 1e-3, ta * 1e-3, tg * 1e-3, n_g))
     return {"attn_solo_us": round(t_attn * 1e3, 1), "gemm_solo_us": round(t_gemm * 1e3, 1),
             "rows": rows}
 
@@ -127,18 +136,20 @@ def candidate_splits(batch: int, granularity: int = 128, max_nano: int = 4) -> L
 def search(step: Callable[[Optional[List[int]], int], None], batch: int,
            profile: Optional[Dict] = None, granularity: int = 128, max_nano: int = 4,
            budgets: Sequence[int] = tuple(range(8, 129, 8)), min_p: float = 0.5, top: int = 3,
-           reps: int = 5) -> Dict:
+           reps: int = 5, timer: Optional[Callable[[Callable[[], None], int], float]] = None) -> Dict:
     """Measure the candidate splits and attention budgets of one dense batch.
 
     ``step(sizes, budget)`` runs one step with that nano-batch split (None: unsplit) and
     attention CTA budget (0: none).  Budgets come from ``profile`` when given (those whose
-    co-run P_attn >= min_p, or the four best), else ``budgets``.  Returns {"best": {sizes, budget, ms}, "table":
-    [{sizes, budget, ms}, ...]} in measurement order.
+    co-run P_attn >= min_p, or the four best), else ``budgets``.  ``timer(fn, reps)`` returns
+    the ms per call of fn (default: CUDA events).  Returns {"best": {sizes, budget, ms},
+    "table": [{sizes, budget, ms}, ...], "budgets_kept"} in measurement order.
     """
     table = []
+    timer = timer or _timed
 
     def run(sizes, budget):
-        ms = _timed(lambda: step(sizes, budget), reps)
+        ms = timer(lambda: step(sizes, budget), reps)
         table.append({"sizes": sizes or [batch], "budget": budget, "ms": round(ms, 4)})
         return ms
 
