@@ -90,6 +90,28 @@ def test_attention_cta_budget_is_bitwise_neutral(cuda_lib):
             6, 32, 8, 128, 16, tab.shape[1], nb, 0.1, 1, -1, None))  # negative budget
 
 
+def test_attention_bounds_checks_record_errors_and_skip_the_access(cuda_lib):
+    """The kernel's own checks (each substitutes a safe value before any memory access, so no
+    fault is induced): a block id outside the pool records NS_DEV_BAD_BLOCK (1) and reads block 0
+    instead; a seq_len beyond the block table records NS_DEV_BAD_LENGTH (3) and skips the row.
+    The other rows' outputs are unchanged bitwise."""
+    from transformer_decode_step_ns_gb300 import _lib
+    q, kp, vp, tab, sl, nb = attention_case(21, [40, 300], 32, 8, 128, "bf16")
+    good = run_attention(q, kp, vp, tab, sl, 32, 8, 128, "bf16", nb)
+    assert _lib.device_error() == 0
+    bad_tab = tab.copy()
+    bad_tab[0, 1] = nb + 5
+    out = run_attention(q, kp, vp, bad_tab, sl, 32, 8, 128, "bf16", nb)
+    assert _lib.device_error() == 1
+    np.testing.assert_array_equal(out[1], good[1])
+    bad_sl = sl.copy()
+    bad_sl[1] = tab.shape[1] * 16 + 1
+    out = run_attention(q, kp, vp, tab, bad_sl, 32, 8, 128, "bf16", nb)
+    assert _lib.device_error() == 3
+    np.testing.assert_array_equal(out[0], good[0])
+    assert _lib.device_error() == 0  # reading the word cleared it
+
+
 def test_attention_rejects_unsupported_shapes(cuda_lib):
     import torch
     from transformer_decode_step_ns_gb300 import _lib

@@ -235,6 +235,32 @@ def test_device_token_source_equals_host_tokens_bitwise(cuda_lib):
     assert ha.dev.device_error() == 0 and hb.dev.device_error() == 0
 
 
+def test_device_token_outside_the_vocabulary_is_recorded_and_replaced(cuda_lib):
+    """A device token id outside [0, V) records NS_DEV_BAD_TOKEN (5) and the row embeds token 0:
+    the logits equal those of the same step with token 0 given on the host, bitwise."""
+    import torch
+    shape = _tiny("bf16")
+    ctx = [3, 40, 200]
+    ha = Harness(shape, 93, ctx)
+    hb = Harness(shape, 93, ctx)
+    bt = ha.batch
+    ids = bt.token_ids.copy()
+    ids[1] = shape.vocab + 7
+    ids_dev = to_dev(ids)
+    ha.dev.set_token_source(ids_dev)
+    la = torch.empty((3, shape.vocab), dtype=torch.float32, device="cuda")
+    lb = torch.empty_like(la)
+    ha.dev.step(None, bt.positions, bt.block_tables, bt.seq_lens, bt.slot_mapping, la)
+    torch.cuda.synchronize()
+    assert ha.dev.device_error() == 5
+    host_ids = bt.token_ids.copy()
+    host_ids[1] = 0
+    hb.dev.step(host_ids, bt.positions, bt.block_tables, bt.seq_lens, bt.slot_mapping, lb)
+    torch.cuda.synchronize()
+    assert hb.dev.device_error() == 0
+    np.testing.assert_array_equal(from_dev(la), from_dev(lb))
+
+
 def test_graph_buckets_pad_batches_and_match_exact_graphs(cuda_lib):
     """With buckets {4, 8} a batch of 3 or 6 replays the graph of 4 or 8 with padding rows: the
     real rows' logits equal those of exact-size graphs bitwise, the padding rows write no
