@@ -210,9 +210,23 @@ ns_status ns_sched_commit(ns_sched s, const int32_t* sampled, int batch, int32_t
 ns_status ns_sched_tokens(ns_sched s, int request_id, int32_t* out, int capacity, int* n);
 /* Requests with prompt tokens left, running, preempted, and finished ones not yet removed. */
 ns_status ns_sched_counts(ns_sched s, int* waiting, int* running, int* preempted, int* finished);
-/* Forget a finished request (its tokens and id); INVALID_ARG for an unknown or unfinished id.
- * A long-running caller removes requests once it has read their tokens. */
+/* Forget a finished request (its tokens and id); INVALID_ARG for an unknown or unfinished id, or
+ * while a formed row of it is not committed.  A long-running caller removes requests once it has
+ * read their tokens. */
 ns_status ns_sched_remove(ns_sched s, int request_id);
+/* Asynchronous formation (NanoFlow page, "Runtime details that keep the pipeline fed": the batch
+ * of iteration i + 1 is formed before iteration i finishes, so an end-of-sequence token is seen
+ * one iteration late).  With on != 0, ns_sched_next may be called once while one formed step is
+ * not committed yet; ns_sched_commit then commits the oldest.  A decode row whose token is not
+ * committed yet gets token id -(row + 1): the token sampled at that row of the previous step,
+ * which ns_decode_step reads from the device token source (ns_set_token_source; the previous
+ * step's greedy ids).  A request counts its formed rows toward max_new_tokens; one that samples
+ * eos_token keeps the row already formed for it in the next step (its token is ignored at that
+ * step's commit) and returns its blocks when no formed row of it is uncommitted.  Needs
+ * predicted_new_tokens = 0 (every peak reserved, so nothing is ever preempted) and no formed
+ * step pending, else INVALID_ARG.  A prompt joins the running order when its last row is formed,
+ * in either mode. */
+ns_status ns_sched_set_async(ns_sched s, int on);
 
 /* Host validation of one step's metadata, exactly as ns_decode_step performs it before
  * anything is launched: 1 <= batch <= max_batch; token ids in [0, vocab); positions >= 0;
@@ -246,7 +260,8 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
 
 /* One decode step for `batch` rows.  Host metadata (validated, packed into one pinned buffer
  * and uploaded with a single host-to-device copy on `stream`):
- *   token_ids [batch] int32 in [0, V); positions [batch] int32 >= 0;
+ *   token_ids [batch] int32 in [0, V) (with a device token source set, NULL or entries
+ *   -(r + 1) too: see ns_set_token_source); positions [batch] int32 >= 0;
  *   block_tables [batch][max_blocks_per_seq] int32 (entries for blocks 0..ceil(seq_len/bs)-1
  *   must be valid pool ids; the rest are ignored); seq_lens [batch] int32 == positions + 1
  *   (cached tokens including this step's token); slot_mapping [batch] int64, must equal
@@ -282,13 +297,16 @@ ns_status ns_set_graph_chunks(ns_handle h, int capture);
 
 /* Token ids from device memory (NanoFlow page, "Runtime details that keep the pipeline fed":
  * the next iteration's batch is formed before the current one finishes, so an end-of-sequence
- * token is seen one iteration late and no synchronisation sits on the critical path).  When device_token_ids is non-NULL, every later
- * ns_decode_step reads row b's token from device_token_ids[b] (int32, device memory of at least
- * max_batch entries, owned by the caller) instead of its token_ids argument, which may then be
- * NULL and is not validated; a token outside [0, V) sets NS_DEV_BAD_TOKEN and row b uses token
- * 0.  Writes to the buffer must be ordered before the step on its stream (for example
- * ns_greedy_argmax of the previous step's logits on the same stream).  NULL restores the host
- * token ids.  A graph is captured per source pointer. */
+ * token is seen one iteration late and no synchronisation sits on the critical path).  When
+ * device_token_ids is non-NULL (int32, device memory of at least max_batch entries, owned by
+ * the caller), every later ns_decode_step may take tokens from it: with token_ids NULL, row b
+ * reads device_token_ids[b]; with token_ids given, an entry -(r + 1) (1 <= r + 1 <= max_batch)
+ * makes row b read device_token_ids[r] and an entry in [0, V) is used as is (the form the batch
+ * former's asynchronous mode writes, ns_sched_set_async).  A device token outside [0, V) sets
+ * NS_DEV_BAD_TOKEN and the row uses token 0.  Writes to the buffer must be ordered before the
+ * step on its stream (for example ns_greedy_argmax of the previous step's logits on the same
+ * stream).  NULL restores host token ids only (negative ids are then INVALID_ARG).  A graph is
+ * captured per source pointer. */
 ns_status ns_set_token_source(ns_handle h, const int32_t* device_token_ids);
 
 /* KV offload (NanoFlow page, "Runtime details that keep the pipeline fed": K/V go to the host

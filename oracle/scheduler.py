@@ -40,6 +40,14 @@ reading (the page gives none):
   step's stream before the step.
 * A decode row's token is the request's last generated token at position
   prompt_len + generated - 1; seq_len = position + 1; slot = table[p // bs] * bs + p % bs.
+* Asynchronous formation (same passage: the batch of iteration i + 1 is formed before
+  iteration i finishes, so an end-of-sequence token is seen one iteration late).  With it on, one
+  formed step may be outstanding when the next is formed: a request whose previous row's token is
+  not committed yet decodes the token sampled at that row, written as token id -(row + 1); a
+  prompt joins the running order when its last row is formed (in either mode); a request counts
+  its formed rows toward max_new_tokens, and one that samples eos keeps the row already formed
+  for the next step, whose token is ignored, and returns its blocks once no formed row of it is
+  outstanding.  It requires every peak reserved (predicted_new = 0), so nothing is preempted.
 """
 from __future__ import annotations
 
@@ -66,6 +74,7 @@ class _Request:
     gen: List[int] = field(default_factory=list)
     table: List[int] = field(default_factory=list)
     finished: bool = False
+    inflight: List[tuple] = field(default_factory=list)   # (step, row) of formed sampling rows
 
 
 @dataclass
@@ -99,7 +108,16 @@ class DenseBatchFormer:
         self.running: List[int] = []    # request ids decoding, prompt-completion order
         self.swapped: deque = deque()   # preempted request ids, preemption order
         self.moves: List[Move] = []
-        self.pending: Optional[StepRows] = None
+        self.pending: deque = deque()   # (step number, StepRows) formed and not committed
+        self.async_mode = False
+        self.seq = 0
+
+    def set_async(self, on: bool) -> None:
+        if on and self.pred != 0:
+            raise SchedulerError("asynchronous formation needs every peak reserved")
+        if self.pending:
+            raise SchedulerError("commit the formed steps first")
+        self.async_mode = bool(on)
 
     def _blocks(self, n_pos: int) -> int:
         return -(-n_pos // self.pool.block_size)
@@ -121,14 +139,21 @@ class DenseBatchFormer:
     def _pos_next(self, rid: int) -> int:
         """Position of a running request's next row; its cached tokens are 0 .. this - 1."""
         r = self.req[rid]
-        return len(r.prompt) + len(r.gen) - 1
+        return len(r.prompt) + len(r.gen) + len(r.inflight) - 1
+
+    def _decoding(self) -> List[int]:
+        """The running requests that get a decode row: the first dense_tokens of those whose
+        formed rows have not reached max_new_tokens."""
+        out = [rid for rid in self.running
+               if len(self.req[rid].gen) + len(self.req[rid].inflight) < self.req[rid].max_new]
+        return out[:self.D]
 
     def _decode_need(self) -> int:
         bs = self.pool.block_size
-        return sum(1 for rid in self.running[:self.D] if self._pos_next(rid) % bs == 0)
+        return sum(1 for rid in self._decoding() if self._pos_next(rid) % bs == 0)
 
     def next(self) -> StepRows:
-        if self.pending is not None:
+        if len(self.pending) >= (2 if self.async_mode else 1):
             raise SchedulerError("commit the previous step first")
         bs = self.pool.block_size
         self.moves = []
@@ -153,12 +178,13 @@ class DenseBatchFormer:
             self.moves.append(Move(1, r.rid, n, list(r.table)))
             self.running.append(r.rid)
         rows = []  # (rid, token, pos, samples)
-        for rid in self.running[:self.D]:
+        for rid in self._decoding():
             r = self.req[rid]
             p = self._pos_next(rid)
             if p % bs == 0:
                 r.table.append(self.pool.alloc(1)[0])
-            rows.append((rid, r.gen[-1], p, 1))
+            tok = -(r.inflight[-1][1] + 1) if r.inflight else r.gen[-1]
+            rows.append((rid, tok, p, 1))
         room = self.D - len(rows)
         for rid in list(self.prefill):
             if room <= 0:
@@ -186,6 +212,15 @@ class DenseBatchFormer:
             r.done += c
             room -= c
         B = len(rows)
+        step = self.seq
+        self.seq += 1
+        for b, (rid, tok, p, smp) in enumerate(rows):
+            if smp:
+                r = self.req[rid]
+                if p == len(r.prompt) - 1:  # the prompt completes: the request runs from now
+                    self.prefill.remove(rid)
+                    self.running.append(rid)
+                r.inflight.append((step, b))
         tab = np.zeros((B, self.mb), dtype=np.int32)
         out = StepRows(np.zeros(B, np.int32), np.zeros(B, np.int32), tab, np.zeros(B, np.int32),
                        np.zeros(B, np.int64), np.zeros(B, np.int32), np.zeros(B, np.int32))
@@ -195,31 +230,31 @@ class DenseBatchFormer:
             tab[b, :len(t)] = t
             out.slot_mapping[b] = t[p // bs] * bs + p % bs
             out.row_request[b], out.row_samples[b] = rid, smp
-        self.pending = out
+        self.pending.append((step, out))
         return out
 
     def commit(self, sampled) -> List[int]:
-        """Sampled token of every row (read where row_samples = 1); returns the ids that
-        finished, in row order."""
-        if self.pending is None:
+        """Sampled token of every row of the oldest formed step (read where row_samples = 1);
+        returns the ids that finished, in row order."""
+        if not self.pending:
             raise SchedulerError("no step to commit")
-        st, self.pending = self.pending, None
+        step, st = self.pending.popleft()
         finished = []
         for b in range(len(st.token_ids)):
             if not st.row_samples[b]:
                 continue
             r = self.req[int(st.row_request[b])]
-            if not r.gen:  # the prompt completed in this step
-                self.prefill.remove(r.rid)
-                self.running.append(r.rid)
-            tok = int(sampled[b])
-            r.gen.append(tok)
-            if tok == self.eos or len(r.gen) == r.max_new:
-                r.finished = True
-                self.running.remove(r.rid)
+            r.inflight.remove((step, b))
+            if not r.finished:  # a row formed after the request's eos: its token is dropped
+                tok = int(sampled[b])
+                r.gen.append(tok)
+                if tok == self.eos or len(r.gen) == r.max_new:
+                    r.finished = True
+                    self.running.remove(r.rid)
+                    finished.append(r.rid)
+            if r.finished and not r.inflight and r.table:
                 self.pool.release(r.table)
                 r.table = []
-                finished.append(r.rid)
         return finished
 
     def tokens(self, rid: int) -> List[int]:
@@ -227,8 +262,8 @@ class DenseBatchFormer:
 
     def remove(self, rid: int) -> None:
         """Forget a finished request."""
-        if rid not in self.req or not self.req[rid].finished:
-            raise SchedulerError("unknown or unfinished request")
+        if rid not in self.req or not self.req[rid].finished or self.req[rid].inflight:
+            raise SchedulerError("unknown or unfinished request (or a formed row not committed)")
         del self.req[rid]
 
     def counts(self):

@@ -214,3 +214,53 @@ def test_dense_batch_former_with_preemption_matches_the_oracle(cuda_lib):
             assert np.abs(mine[i] - ref[i]).max() < 5e-2, (rid, i)
         # greedy: each generated token is the argmax of the logits that produced it
         np.testing.assert_array_equal(np.argmax(mine, axis=1), gen)
+
+
+def test_async_formation_generates_the_sync_tokens(cuda_lib):
+    """The batch former forming each step before the previous one is committed (decode rows
+    read their tokens from the previous step's device argmax) generates, greedily, exactly the
+    tokens of synchronous formation (the same steps, rows independent of one another)."""
+    import collections
+    import torch
+    import synth
+    from transformer_decode_step_ns_gb300 import _lib
+    shape = _tiny("bf16")
+    bs, D, mb = 16, 24, 8
+    w = synth.model_weights(shape, 157, gamma_std=0.1)
+    rng = np.random.default_rng(157)
+    prompts = {rid: rng.integers(0, shape.vocab, size=n).astype(np.int32)
+               for rid, n in enumerate([33, 5, 20, 17, 9, 26])}
+    out = {}
+    for async_mode in (False, True):
+        dev = _lib.DecodeStep(shape, w, D, mb, use_graphs=False)
+        dev.kv_alloc(64, bs)
+        ids = torch.zeros(D, dtype=torch.int32, device="cuda")
+        dev.set_token_source(ids)
+        former = _lib.BatchFormer(dev.pool(), D, mb, eos_token=-1)
+        former.set_async(async_mode)
+        for rid, p in prompts.items():
+            former.add(rid, p, 10)
+        logits = torch.empty((D, shape.vocab), dtype=torch.float32, device="cuda")
+        pending = collections.deque()
+        negative = 0
+        for _ in range(200):
+            r = former.next()
+            B = len(r["token_ids"])
+            negative += int((r["token_ids"] < 0).sum())
+            if B:
+                dev.step(r["token_ids"], r["positions"], r["block_tables"], r["seq_lens"],
+                         r["slot_mapping"], logits[:B])
+                _lib.greedy_argmax(logits[:B], ids[:B])
+            pending.append(ids[:B].cpu().numpy().copy())  # read before the next step's argmax
+            if len(pending) == (2 if async_mode else 1):
+                former.commit(pending.popleft())
+            if former.counts()[3] == len(prompts):
+                break
+        while pending:
+            former.commit(pending.popleft())
+        assert dev.device_error() == 0
+        assert (negative > 0) == async_mode
+        out[async_mode] = {rid: former.tokens(rid) for rid in prompts}
+        dev.close()
+    assert all(len(t) == 10 for t in out[False].values())
+    assert out[True] == out[False]

@@ -137,6 +137,9 @@ class _ModelAdapter:
     def commit(self, sampled):
         return self.m.commit(sampled)
 
+    def counts(self):
+        return self.m.counts()
+
     def moves(self):
         return [(v.kind, v.rid, v.n_tokens, np.array(v.table, np.int32)) for v in self.m.moves]
 
@@ -336,3 +339,94 @@ def test_tuner_search_measures_every_split_then_budgets_and_picks_the_fastest():
     # without a profile every budget is tried on the three fastest splits
     out = tuner.search(step, 2048, timer=timer)
     assert len(out["table"]) == len(stage1) + 3 * 16
+
+
+def test_async_formation_worked_example_by_hand():
+    """Asynchronous formation: step 1 is formed before step 0 is committed, so its decode rows
+    read their tokens from step 0's rows (-(row + 1)); B samples eos at step 0, which is seen
+    only when step 0 commits, after B's row in step 1 exists: that row's token is dropped and
+    B's blocks return at step 1's commit."""
+    m = DenseBatchFormer(BlockAllocator(16, 4), dense_tokens=8, max_blocks_per_seq=4, eos_token=9)
+    m.set_async(True)
+    A, B = 1, 2
+    m.add(A, [10, 11, 12], 3)
+    m.add(B, [20, 21, 22, 23, 24], 2)
+    s0 = m.next()
+    np.testing.assert_array_equal(s0.token_ids, [10, 11, 12, 20, 21, 22, 23, 24])
+    np.testing.assert_array_equal(s0.row_samples, [0, 0, 1, 0, 0, 0, 0, 1])
+    s1 = m.next()                                   # formed before step 0 commits
+    np.testing.assert_array_equal(s1.token_ids, [-3, -8])
+    np.testing.assert_array_equal(s1.positions, [3, 5])
+    with pytest.raises(SchedulerError):
+        m.next()                                    # at most one formed step outstanding
+    assert m.commit([0, 0, 50, 0, 0, 0, 0, 9]) == [B]   # B's eos, seen one step late
+    s2 = m.next()
+    np.testing.assert_array_equal(s2.token_ids, [-1])   # A only; its position 4 takes block 3
+    np.testing.assert_array_equal(s2.slot_mapping, [12])
+    assert m.commit([51, 77]) == []                 # B's extra token is dropped, blocks 1, 2 back
+    assert m.tokens(B) == [9]
+    assert m.commit([52]) == [A]
+    assert m.tokens(A) == [50, 51, 52]
+    assert list(m.pool.free) == list(range(4, 16)) + [1, 2, 0, 3]
+    with pytest.raises(SchedulerError):
+        DenseBatchFormer(BlockAllocator(4, 4), 4, 4, 0, predicted_new=3).set_async(True)
+
+
+def _pipelined(form, rng, n_req, vocab, eos, max_prompt, max_new_hi, sampler, async_mode):
+    """All requests arrive first; steps are formed and committed (one step late when
+    asynchronous) until every request finishes.  Yields formed rows and commit results."""
+    from collections import deque
+    for i in range(n_req):
+        form.add(i, rng.integers(0, vocab, size=int(rng.integers(1, max_prompt + 1))),
+                 int(rng.integers(1, max_new_hi + 1)))
+    pending = deque()
+    for _ in range(5000):
+        rows = form.next()
+        yield ("formed", rows)
+        pending.append(rows)
+        if len(pending) == (2 if async_mode else 1):
+            r = pending.popleft()
+            yield ("commit", form.commit(sampler(r)))
+        if form.counts()[3] == n_req:
+            break
+    while pending:
+        r = pending.popleft()
+        yield ("commit", form.commit(sampler(r)))
+
+
+def _sampler_for(vocab):
+    """The token a row samples depends only on its request and position."""
+    def sample(rows):
+        return np.array([(int(q) * 7919 + int(p) * 104729) % vocab
+                         for q, p in zip(rows["row_request"], rows["positions"])], dtype=np.int32)
+    return sample
+
+
+@pytest.mark.parametrize("case", [(16, 4, 200, 32, 30, 3, 20, 8), (33, 16, 400, 32, 100, 7, 60, 20)])
+def test_async_formation_generates_what_sync_formation_does(L, case):
+    """With a sampler that depends only on (request, position), asynchronous and synchronous
+    formation generate the same tokens for every request; the library equals the model row for
+    row in both modes."""
+    D, bs, nb, mb, vocab, eos, mp, mn = case
+    outs = {}
+    for async_mode in (False, True):
+        model = _ModelAdapter(DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos))
+        pool = L.BlockPool(nb, bs, mb)
+        lib_form = L.BatchFormer(pool, D, mb, eos)
+        if async_mode:
+            model.m.set_async(True)
+            lib_form.set_async(True)
+        n_req = 40
+        a = _pipelined(model, np.random.default_rng(17), n_req, vocab, eos, mp, mn, _sampler_for(vocab), async_mode)
+        b = _pipelined(lib_form, np.random.default_rng(17), n_req, vocab, eos, mp, mn, _sampler_for(vocab), async_mode)
+        for ea, eb in zip(a, b):
+            assert ea[0] == eb[0]
+            if ea[0] == "formed":
+                for k in KEYS:
+                    np.testing.assert_array_equal(ea[1][k], eb[1][k], err_msg=k)
+            else:
+                assert ea[1] == eb[1]
+        outs[async_mode] = {i: model.m.tokens(i) for i in range(n_req)}
+        assert all(lib_form.tokens(i) == outs[async_mode][i] for i in range(n_req))
+        assert model.m.counts()[3] == n_req and model.m.pool.free_count() == nb
+    assert outs[True] == outs[False]

@@ -38,7 +38,7 @@ SYMBOLS = (
     "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
-    "ns_set_graph_chunks", "ns_sched_remove",
+    "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async",
 )
 
 
@@ -139,6 +139,7 @@ def lib() -> ctypes.CDLL:
             "ns_capture_graphs": ([P, I, P, I], I),
             "ns_set_graph_chunks": ([P, I], I),
             "ns_sched_remove": ([P, I], I),
+            "ns_sched_set_async": ([P, I], I),
             "ns_attn_decode_capped": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P], I),
             "ns_get_graph_report": ([P, P, I, ctypes.POINTER(I)], I),
             "ns_get_kernel_timing": ([P, ctypes.POINTER(KernelTiming)], I),
@@ -583,6 +584,11 @@ class BatchFormer:
     def remove(self, request_id: int) -> None:
         """Forget a finished request."""
         check(lib().ns_sched_remove(self.h, request_id))
+
+    def set_async(self, on: bool) -> None:
+        """Form the next step before the previous one is committed (tokens not yet on the host
+        are written -(row + 1): the previous step's sampled token at that row)."""
+        check(lib().ns_sched_set_async(self.h, 1 if on else 0))
 
     def counts(self):
         """(requests with prompt left, running, preempted, finished and not removed)."""

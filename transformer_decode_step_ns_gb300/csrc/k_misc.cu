@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Token ids and positions are step metadata, complete before the step: read them early.
   int tok = (p.rows_valid != nullptr && row >= *p.rows_valid) ? 0 : p.token_ids[row];
+  // -(r + 1): the token sampled at row r of the previous step, in the device token source (its
+  // writer, the previous step's argmax, precedes this kernel without a programmatic edge)
+  if (tok < 0 && p.tok_src != nullptr) tok = p.tok_src[-tok - 1];
   const int pos = p.positions[row];
   if (tid == 0) griddep_launch_dependents();
   griddep_wait();  // the residual/xn rows may still be read by the previous step's tail

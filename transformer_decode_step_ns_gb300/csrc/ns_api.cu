@@ -254,13 +254,15 @@ ns_status pool_release(ns_block_pool* p, const int32_t* ids, int n) {
 
 ns_status check_meta(int num_blocks, int bs, int mb, int vocab, int max_batch, int batch,
                      const int32_t* token_ids, const int32_t* positions, const int32_t* block_tables,
-                     const int32_t* seq_lens, const int64_t* slot_mapping, bool tokens_on_host = true) {
+                     const int32_t* seq_lens, const int64_t* slot_mapping, int src_rows = 0) {
+  // src_rows > 0: a device token source of that many rows is set; token ids may then be NULL
+  // (row b reads source row b) or -(r + 1) (row b reads source row r < src_rows)
   if (batch < 1 || batch > max_batch) return fail(NS_ERR_INVALID_ARG, "batch out of range");
-  if ((tokens_on_host && !token_ids) || !positions || !block_tables || !seq_lens || !slot_mapping)
+  if ((src_rows == 0 && !token_ids) || !positions || !block_tables || !seq_lens || !slot_mapping)
     return fail(NS_ERR_INVALID_ARG, "null argument");
   for (int b = 0; b < batch; ++b) {
     const int p = positions[b], L = seq_lens[b];
-    if (tokens_on_host && (token_ids[b] < 0 || token_ids[b] >= vocab))
+    if (token_ids && (token_ids[b] >= vocab || token_ids[b] < -src_rows))
       return fail(NS_ERR_INVALID_ARG, "token id out of range");
     if (p < 0 || L != p + 1) return fail(NS_ERR_INVALID_ARG, "seq_lens must equal positions + 1");
     if (L > mb * bs) return fail(NS_ERR_INVALID_ARG, "seq_len beyond max_blocks_per_seq * block_size");
@@ -522,7 +524,8 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   for (int i = 0; i < n; ++i) {
     EmbedParams ep{};
     ep.embed = h->embed;
-    ep.token_ids = h->tok_src != nullptr ? h->tok_src : m_tok;
+    ep.token_ids = m_tok;
+    ep.tok_src = h->tok_src;
     ep.rows_valid = m_rows_valid;
     ep.positions = m_pos;
     ep.vocab = c.vocab;
@@ -1121,9 +1124,9 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   if (h->pools == nullptr) return fail(NS_ERR_NOT_INITIALIZED, "ns_kv_alloc first");
   const ns_model_cfg& c = h->cfg;
   const int bs = h->block_size, mb = c.max_blocks_per_seq;
-  const bool host_tokens = h->tok_src == nullptr;
+  const int src_rows = h->tok_src != nullptr ? h->R : 0;
   NS_TRY(check_meta(h->num_blocks, bs, mb, c.vocab, c.max_batch, batch, token_ids, positions,
-                    block_tables, seq_lens, slot_mapping, host_tokens));
+                    block_tables, seq_lens, slot_mapping, src_rows));
   if (h->n_split > 1) {
     int sum = 0;
     for (int v : h->split_sizes) sum += v;
@@ -1171,10 +1174,12 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   h->chunk_first = runs.empty() ? Bg : runs.front();  // Bg: none, so padded steps share a graph
   const MetaLayout ml = meta_layout(Bg, mb);
   uint8_t* mh = h->meta_host;
-  if (host_tokens)
+  if (token_ids != nullptr) {
     std::memcpy(mh + ml.tok, token_ids, batch * 4);
-  else
-    std::memset(mh + ml.tok, 0, batch * 4);
+  } else {  // every row reads its own row of the device token source
+    int32_t* t = reinterpret_cast<int32_t*>(mh + ml.tok);
+    for (int b = 0; b < batch; ++b) t[b] = -(b + 1);
+  }
   std::memcpy(mh + ml.pos, positions, batch * 4);
   std::memcpy(mh + ml.seq, seq_lens, batch * 4);
   std::memcpy(mh + ml.slot, slot_mapping, batch * 8);

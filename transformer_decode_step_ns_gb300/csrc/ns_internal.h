@@ -120,7 +120,8 @@ constexpr int kPrefillMinRows = 16;
 
 struct EmbedParams {
   const void* embed;
-  const int* token_ids;
+  const int* token_ids;   // step metadata; an id -(r + 1) names row r of tok_src
+  const int* tok_src;     // device token source (ns_set_token_source) or null
   const int* positions;
   int vocab, hidden;
   const float* gamma;  // first layer's attention-norm gain (fp32)

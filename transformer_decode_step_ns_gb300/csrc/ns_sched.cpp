@@ -41,6 +41,7 @@ struct Request {
   std::vector<int32_t> gen;
   std::vector<int32_t> table;
   bool finished = false;
+  std::deque<std::pair<long long, int>> inflight;  // (step, row) of formed sampling rows
 };
 
 struct Row {
@@ -66,16 +67,27 @@ struct ns_sched_st {
   std::deque<int> prefill;  // ids with prompt left, arrival order
   std::vector<int> running;  // ids decoding, prompt-completion order (resumed ones appended)
   std::deque<int> swapped;  // preempted ids, preemption order
-  bool pending = false;
-  std::vector<Row> rows;    // the formed, not yet committed step
+  bool async_mode = false;
+  long long seq = 0;                                        // next step number
+  std::deque<std::pair<long long, std::vector<Row>>> pending;  // formed, not committed
+  std::vector<Row> rows;    // the step being formed
   std::vector<Move> moves;  // saves and reloads the formed step needs first
 
   int blocks(long long n_pos) const { return static_cast<int>((n_pos + bs - 1) / bs); }
+  // running requests that get a decode row: the first D whose formed rows are below max_new
+  std::vector<int> decoding() {
+    std::vector<int> out;
+    for (int id : running) {
+      if (static_cast<int>(out.size()) >= D) break;
+      const Request& r = req[id];
+      if (static_cast<int>(r.gen.size() + r.inflight.size()) < r.max_new) out.push_back(id);
+    }
+    return out;
+  }
   int decode_need() {
     int need = 0;
-    const size_t n = std::min(running.size(), static_cast<size_t>(D));
-    for (size_t i = 0; i < n; ++i)
-      if (pos_next(req[running[i]]) % bs == 0) ++need;
+    for (int id : decoding())
+      if (pos_next(req[id]) % bs == 0) ++need;
     return need;
   }
 
@@ -85,7 +97,7 @@ struct ns_sched_st {
     return n;
   }
   int pos_next(const Request& r) const {
-    return static_cast<int>(r.prompt.size() + r.gen.size()) - 1;
+    return static_cast<int>(r.prompt.size() + r.gen.size() + r.inflight.size()) - 1;
   }
 };
 
@@ -138,7 +150,7 @@ ns_status ns_sched_next(ns_sched s, int32_t* token_ids, int32_t* positions, int3
   if (s == nullptr || !token_ids || !positions || !block_tables || !seq_lens || !slot_mapping ||
       !row_request || !row_samples || !batch)
     return err(NS_ERR_INVALID_ARG, "null argument");
-  if (s->pending) return err(NS_ERR_INVALID_ARG, "commit the previous step first");
+  if (s->pending.size() >= (s->async_mode ? 2u : 1u)) return err(NS_ERR_INVALID_ARG, "commit the previous step first");
   const int bs = s->bs;
   s->moves.clear();
   // preempt the last running request while the decode rows lack blocks
@@ -164,17 +176,18 @@ ns_status ns_sched_next(ns_sched s, int32_t* token_ids, int32_t* positions, int3
     s->moves.push_back({1, r.id, n, r.table});
     s->running.push_back(r.id);
   }
-  const size_t n_dec = std::min(s->running.size(), static_cast<size_t>(s->D));
   s->rows.clear();
-  for (size_t i = 0; i < n_dec; ++i) {
-    Request& r = s->req[s->running[i]];
+  for (int id : s->decoding()) {
+    Request& r = s->req[id];
     const int p = s->pos_next(r);
     if (p % bs == 0) {
       int32_t b = 0;
       ns_pool_reserve(s->pool, 1, &b);
       r.table.push_back(b);
     }
-    s->rows.push_back({r.id, r.gen.back(), p, 1});
+    // a token not committed yet is the one sampled at the request's row of the previous step
+    const int tok = r.inflight.empty() ? r.gen.back() : -(r.inflight.back().second + 1);
+    s->rows.push_back({r.id, tok, p, 1});
   }
   int room = s->D - static_cast<int>(s->rows.size());
   for (int id : s->prefill) {
@@ -209,6 +222,17 @@ ns_status ns_sched_next(ns_sched s, int32_t* token_ids, int32_t* positions, int3
     room -= c;
   }
   const int B = static_cast<int>(s->rows.size());
+  const long long step = s->seq++;
+  for (int b = 0; b < B; ++b) {
+    const Row& w = s->rows[b];
+    if (!w.samples) continue;
+    Request& r = s->req[w.id];
+    if (w.pos == static_cast<int>(r.prompt.size()) - 1) {  // the prompt completes: it runs from now
+      s->prefill.erase(std::find(s->prefill.begin(), s->prefill.end(), r.id));
+      s->running.push_back(r.id);
+    }
+    r.inflight.push_back({step, b});
+  }
   for (int b = 0; b < B; ++b) {
     const Row& w = s->rows[b];
     const std::vector<int32_t>& t = s->req[w.id].table;
@@ -223,7 +247,7 @@ ns_status ns_sched_next(ns_sched s, int32_t* token_ids, int32_t* positions, int3
     row_samples[b] = w.samples;
   }
   *batch = B;
-  s->pending = true;
+  s->pending.push_back({step, s->rows});
   return NS_OK;
 }
 
@@ -231,30 +255,42 @@ ns_status ns_sched_commit(ns_sched s, const int32_t* sampled, int batch, int32_t
                           int* n_finished) {
   if (s == nullptr || (batch > 0 && sampled == nullptr) || n_finished == nullptr)
     return err(NS_ERR_INVALID_ARG, "null argument");
-  if (!s->pending) return err(NS_ERR_INVALID_ARG, "no step to commit");
-  if (batch != static_cast<int>(s->rows.size())) return err(NS_ERR_INVALID_ARG, "batch differs from the formed step");
-  s->pending = false;
+  if (s->pending.empty()) return err(NS_ERR_INVALID_ARG, "no step to commit");
+  if (batch != static_cast<int>(s->pending.front().second.size()))
+    return err(NS_ERR_INVALID_ARG, "batch differs from the formed step");
+  const long long step = s->pending.front().first;
+  const std::vector<Row> rows = std::move(s->pending.front().second);
+  s->pending.pop_front();
   int nf = 0;
   for (int b = 0; b < batch; ++b) {
-    const Row& w = s->rows[b];
+    const Row& w = rows[b];
     if (!w.samples) continue;
     Request& r = s->req[w.id];
-    if (r.gen.empty()) {  // the prompt completed in this step
-      s->prefill.erase(std::find(s->prefill.begin(), s->prefill.end(), r.id));
-      s->running.push_back(r.id);
+    r.inflight.erase(std::find(r.inflight.begin(), r.inflight.end(), std::make_pair(step, b)));
+    if (!r.finished) {  // a row formed after the request's eos: its token is dropped
+      const int32_t tok = sampled[b];
+      r.gen.push_back(tok);
+      if (tok == s->eos || static_cast<int>(r.gen.size()) == r.max_new) {
+        r.finished = true;
+        s->running.erase(std::find(s->running.begin(), s->running.end(), r.id));
+        if (finished_ids != nullptr) finished_ids[nf] = r.id;
+        ++nf;
+      }
     }
-    const int32_t tok = sampled[b];
-    r.gen.push_back(tok);
-    if (tok == s->eos || static_cast<int>(r.gen.size()) == r.max_new) {
-      r.finished = true;
-      s->running.erase(std::find(s->running.begin(), s->running.end(), r.id));
-      if (!r.table.empty()) ns_pool_release(s->pool, r.table.data(), static_cast<int>(r.table.size()));
+    if (r.finished && r.inflight.empty() && !r.table.empty()) {
+      ns_pool_release(s->pool, r.table.data(), static_cast<int>(r.table.size()));
       r.table.clear();
-      if (finished_ids != nullptr) finished_ids[nf] = r.id;
-      ++nf;
     }
   }
   *n_finished = nf;
+  return NS_OK;
+}
+
+ns_status ns_sched_set_async(ns_sched s, int on) {
+  if (s == nullptr) return err(NS_ERR_INVALID_ARG, "null argument");
+  if (on && s->pred != 0) return err(NS_ERR_INVALID_ARG, "asynchronous formation needs every peak reserved");
+  if (!s->pending.empty()) return err(NS_ERR_INVALID_ARG, "commit the formed steps first");
+  s->async_mode = on != 0;
   return NS_OK;
 }
 
@@ -272,7 +308,8 @@ ns_status ns_sched_remove(ns_sched s, int request_id) {
   if (s == nullptr) return err(NS_ERR_INVALID_ARG, "null argument");
   auto it = s->req.find(request_id);
   if (it == s->req.end()) return err(NS_ERR_INVALID_ARG, "unknown request id");
-  if (!it->second.finished) return err(NS_ERR_INVALID_ARG, "request not finished");
+  if (!it->second.finished || !it->second.inflight.empty())
+    return err(NS_ERR_INVALID_ARG, "request not finished (or a formed row of it not committed)");
   s->req.erase(it);
   return NS_OK;
 }
