@@ -13,9 +13,11 @@ split-K, nano-batching and graph replay on the GPU side are exact re-orderings o
 
 Parity status: every function below is pinned by a ``-m "not gpu"`` test against something
 other than itself (closed forms, special cases that reduce to library routines, brute force,
-invariants, or numbers printed on the pages).  ``decode_step`` as a whole has no printed
-worked example on the pages; beyond the invariants and the independent PyTorch
-re-statement in ``tests/test_oracle_pins.py`` its whole-step values are "parity unpinned".
+invariants, or numbers printed on the pages).  The pages print no logits for any input, so
+``decode_step`` as a whole is pinned by closed forms instead (zero Wo/Wd: the tied head scores
+the input token; zero Wq: every head averages its kv head's V), by invariants (rows are
+independent; a prompt chunk equals its tokens decoded one step at a time, causally) and by
+an independent PyTorch statement over dense histories (``tests/test_oracle_pins.py``).
 """
 from .decode import (  # noqa: F401
     OracleModel, attention_weights, dense_attention, decode_step, from_storage, gqa_group,

@@ -350,6 +350,98 @@ def test_decode_rows_are_independent():
         np.testing.assert_allclose(one[0], full[b], rtol=1e-12, atol=1e-13)
 
 
+def test_uniform_attention_closed_form_through_the_whole_step():
+    """Wq = 0 makes every score 0, so each q head's attention output is the plain mean of its
+    kv head's V over the request's tokens t < seq_len, this step's own v included; with
+    Wd = 0 and unit gains the layer is x += Wo . concat_h mean(V[:, h // G]) and the tied head
+    gives rms(x) . E^T.  Written with np.mean over the dense histories (no softmax, no pool),
+    so a wrong head grouping, an off-by-one seq_len, a missing write of this step's v before
+    attending, or a rotation of v fails here."""
+    shape, w, batch, kp, vp, _, hv = _step_case("f16", True, gamma_std=0.0)
+    for lw in w["layers"]:
+        lw["wq"] = np.zeros_like(lw["wq"])
+        lw["w_down"] = np.zeros_like(lw["w_down"])
+    model = oracle.OracleModel.from_weights(shape, w)
+    logits = oracle.decode_step(model, kp, vp, batch.token_ids, batch.positions,
+                                batch.block_tables, batch.seq_lens, batch.slot_mapping, 4)
+    f64 = lambda a: synth.storage_to_f64(a, "f16")  # noqa: E731
+    E = f64(w["embed"])
+    hq, hkv, d, H = shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.hidden
+    G = hq // hkv
+    rms = lambda z: z / np.sqrt((z * z).mean(-1, keepdims=True) + shape.rms_eps)  # noqa: E731
+    x = E[batch.token_ids]
+    for l, lw in enumerate(w["layers"]):
+        v_new = rms(x) @ f64(lw["wv"]).T
+        v_new = torch.from_numpy(v_new).to(torch.float32).to(torch.float16).double().numpy()
+        o = np.zeros((batch.batch, hq * d))
+        for b in range(batch.batch):
+            V = np.concatenate([hv[l][b].numpy(), v_new[b].reshape(1, hkv, d)], 0)
+            for h in range(hq):
+                o[b, h * d:(h + 1) * d] = V[:, h // G, :].mean(0)
+        x = x + o @ f64(lw["wo"]).T
+    np.testing.assert_allclose(logits, rms(x) @ E.T, rtol=1e-9, atol=1e-11)
+
+
+def test_prompt_chunk_equals_feeding_its_tokens_one_step_at_a_time():
+    """A prompt chunk (rows of one request at consecutive positions over one block table, all
+    in one step) is the same computation as decoding those tokens one per step: each row sees
+    the cached tokens and the chunk's earlier rows, never its later ones (NanoFlow page,
+    "Runtime details that keep the pipeline fed": prompts enter the dense batch as chunks
+    next to decode rows).  Checked on logits and on the K/V left in the cache, with a decode
+    row of another request in the same step."""
+    bs, ctx0, n_chunk = 4, 5, 6
+    shape, w, batch, kp, vp, _, _ = _step_case("bf16", False, ctx=(ctx0, 9))
+    model = oracle.OracleModel.from_weights(shape, w)
+    rng = _rng(31)
+    chunk = rng.integers(0, shape.vocab, n_chunk).astype(np.int32)
+    table = batch.block_tables[0].copy()
+    assert (ctx0 + n_chunk + bs - 1) // bs <= len(table)
+    # give the chunk's later positions blocks of their own (free blocks of the pool)
+    used = set(batch.block_tables[:, :].ravel().tolist())
+    n_have = (ctx0 + 1 + bs - 1) // bs
+    free = [blk for blk in range(batch.num_blocks) if blk not in used]
+    for i in range(n_have, (ctx0 + n_chunk + bs - 1) // bs):
+        table[i] = free.pop()
+    pos = np.arange(ctx0, ctx0 + n_chunk, dtype=np.int32)
+    slots = np.array([table[p // bs] * bs + p % bs for p in pos], dtype=np.int64)
+
+    # one step: the decode row of request 1, then the chunk of request 0
+    kc = [a.copy() for a in kp]
+    vc = [a.copy() for a in vp]
+    tok = np.concatenate([batch.token_ids[1:2], chunk])
+    posn = np.concatenate([batch.positions[1:2], pos])
+    tabs = np.stack([batch.block_tables[1]] + [table] * n_chunk)
+    lens = posn + 1
+    sl = np.concatenate([batch.slot_mapping[1:2], slots])
+    together = oracle.decode_step(model, kc, vc, tok, posn, tabs, lens, sl, bs)
+
+    # the same tokens, one step each
+    ks = [a.copy() for a in kp]
+    vs = [a.copy() for a in vp]
+    one_by_one = []
+    for i in range(n_chunk):
+        one_by_one.append(oracle.decode_step(model, ks, vs, chunk[i:i + 1], pos[i:i + 1],
+                                             table[None], pos[i:i + 1] + 1, slots[i:i + 1],
+                                             bs)[0])
+    alone = oracle.decode_step(model, ks, vs, batch.token_ids[1:2], batch.positions[1:2],
+                               batch.block_tables[1:2], batch.seq_lens[1:2],
+                               batch.slot_mapping[1:2], bs)[0]
+    np.testing.assert_allclose(together[1:], np.stack(one_by_one), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(together[0], alone, rtol=1e-9, atol=1e-11)
+    for l in range(shape.n_layers):
+        for a, b in ((kc[l], ks[l]), (vc[l], vs[l])):
+            np.testing.assert_allclose(synth.storage_to_f64(a, "bf16"),
+                                       synth.storage_to_f64(b, "bf16"), rtol=2 ** -7, atol=0)
+    # and the chunk is causal: changing its last token changes no earlier row
+    chunk2 = chunk.copy()
+    chunk2[-1] = (chunk2[-1] + 1) % shape.vocab
+    tok2 = np.concatenate([batch.token_ids[1:2], chunk2])
+    other = oracle.decode_step(model, [a.copy() for a in kp], [a.copy() for a in vp], tok2,
+                               posn, tabs, lens, sl, bs)
+    np.testing.assert_array_equal(other[:-1], together[:-1])
+    assert np.abs(other[-1] - together[-1]).max() > 1e-3
+
+
 def test_qwen_shape_weight_bytes_match_the_printed_943_mib():
     g = json.load(open(os.path.join(GOLDEN, "pages_numbers.json")))["qwen05b_fp16_weights_mib"]
     mib = oracle.param_bytes(synth.qwen05b_shape()) / 2 ** 20
