@@ -180,11 +180,13 @@ ns_status ns_kv_get_pool(ns_handle h, ns_pool* out);
  *   on the step's stream before ns_decode_step (ns_kv_save of kind 0 into its own host store,
  *   ns_kv_reload of kind 1 from it; a reload's blocks may be blocks a save of the same step
  *   released, which stream order makes safe).
+ *   A prompt whose last row is formed joins the running order at once (its next decode row
+ *   comes in the following step).
  *   ns_sched_commit then takes the step's sampled tokens (sampled[b], read where
- *   row_samples[b] = 1): a request whose prompt completed starts running, a request that
- *   samples eos_token or reaches max_new_tokens finishes, its blocks return to the pool in
- *   table order, and its id is written to finished_ids (capacity >= batch, or NULL).  A
- *   second ns_sched_next before the commit returns INVALID_ARG.
+ *   row_samples[b] = 1; batch must equal the formed step's, else INVALID_ARG and nothing
+ *   changes): a request that samples eos_token or reaches max_new_tokens finishes, its blocks
+ *   return to the pool in table order, and its id is written to finished_ids (capacity >=
+ *   batch, or NULL).  A second ns_sched_next before the commit returns INVALID_ARG.
  * With predicted_new_tokens 0 every admitted request's peak is reserved, so nothing is ever
  * preempted. */
 typedef struct ns_sched_st* ns_sched;
@@ -329,9 +331,10 @@ ns_status ns_set_kv_offload(ns_handle h, void* host_dst, size_t bytes);
  * host_src holds the K/V of n_tokens tokens of one request at positions first_pos ..
  * first_pos + n_tokens - 1, laid out [n_layers][n_tokens][2][n_kv_heads * head_dim] in the model
  * dtype (the ns_set_kv_offload row layout, one row per token).  They are copied to a contiguous
- * device buffer held by the handle, then scattered to slot block_table[p / 16] * 16 + p % 16 of
- * every layer's pools (block_table: host int32 of n_table >= (first_pos + n_tokens - 1) / 16 + 1
- * ids in [0, num_blocks), else NS_ERR_INVALID_ARG).  Asynchronous on `stream`; host_src must stay
+ * device buffer held by the handle, then scattered to slot block_table[p / bs] * bs + p % bs of
+ * every layer's pools, bs the block_size given to ns_kv_alloc (block_table: host int32 of
+ * n_table >= (first_pos + n_tokens - 1) / bs + 1 ids in [0, num_blocks), else
+ * NS_ERR_INVALID_ARG).  Asynchronous on `stream`; host_src must stay
  * valid until the copy has run when it is pinned (pageable memory is copied before the call
  * returns).  Calls on one handle share the transfer buffer: order them on one stream, and
  * before any step that reads the blocks.  The buffer grows to the largest request seen (the
@@ -448,7 +451,8 @@ ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with
 /* Per-kernel timing of eager steps (for roofline accounting).  While on, ns_decode_step
  * launches the kernels eagerly (graphs are bypassed) with a CUDA event pair around each launch
  * on the stream the kernel runs on.  Kinds: 0 embedding + RoPE table, 1 QKV projection,
- * 2 attention, 3 O projection, 4 gate/up projection, 5 down projection, 6 LM head.
+ * 2 attention (decode rows and prompt-chunk kernels), 3 O projection, 4 gate/up projection,
+ * 5 down projection, 6 LM head; entry 7 is reserved and stays 0.
  * ns_get_kernel_timing synchronises, returns launches and summed milliseconds per kind since
  * the last read, and clears them. */
 #define NS_KERNEL_KINDS 8
