@@ -190,6 +190,10 @@ ns_status ns_kv_get_pool(ns_handle h, ns_pool* out);
  * With predicted_new_tokens 0 every admitted request's peak is reserved, so nothing is ever
  * preempted. */
 typedef struct ns_sched_st* ns_sched;
+/* pool is borrowed: it must outlive the former, and while the former runs only the former
+ * reserves and releases its blocks.  dense_tokens >= 1 (the target rows per step),
+ * max_blocks_per_seq >= 1 (the row width of the block tables it writes), eos_token (any
+ * value; one no token equals disables eos), predicted_new_tokens >= 0; else INVALID_ARG. */
 ns_status ns_sched_create(ns_pool pool, int dense_tokens, int max_blocks_per_seq, int eos_token,
                           int predicted_new_tokens, ns_sched* out);
 void ns_sched_destroy(ns_sched s);
