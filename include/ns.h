@@ -131,7 +131,8 @@ ns_status ns_kv_prepare_step(ns_handle h, int batch, const int32_t* positions,
 /* Host-only block pool (no GPU needed): the free list and slot mapper that a handle's KV cache
  * uses, usable on its own.  Same policy as ns_kv_prepare_step / ns_kv_reserve / ns_kv_release:
  * the free list starts 0..num_blocks-1, blocks are taken from the front and returned to the
- * back.  max_blocks_per_seq is the block-table row width prepare_step writes into. */
+ * back, and only blocks handed out can be returned (once).  max_blocks_per_seq is the
+ * block-table row width prepare_step writes into. */
 typedef struct ns_block_pool* ns_pool;
 ns_status ns_pool_create(int num_blocks, int block_size, int max_blocks_per_seq, ns_pool* out);
 void ns_pool_destroy(ns_pool p);
@@ -247,8 +248,10 @@ ns_status ns_check_step_metadata(int num_blocks, int block_size, int max_blocks_
 /* Reserve n blocks from the free list (host ids written to out_ids[n]); OUT_OF_BLOCKS if short. */
 ns_status ns_kv_reserve(ns_handle h, int n, int32_t* out_ids);
 
-/* Return blocks to the back of the free list (a request leaving).  INVALID_ARG on an id
- * outside the pool. */
+/* Return blocks to the back of the free list (a request leaving).  A block has one owner, so
+ * every id must be one that was handed out (reserve, prepare_step, the batch former) and not
+ * yet returned, and appear once in the call; INVALID_ARG otherwise (an id outside the pool, a
+ * free block, a repeated id), with nothing returned. */
 ns_status ns_kv_release(ns_handle h, const int32_t* block_ids, int n);
 
 /* Number of free blocks. */

@@ -15,6 +15,9 @@ own reading (the pages give none):
   first slot of a block (p % bs == 0) a block is taken and stored at table[b][p // bs]; the
   slot is table[b][p // bs] * bs + p % bs.  Running out of blocks or past the table width is an
   error, raised before anything is changed.
+* A block belongs to at most one request (a slot holds one token of one request), so
+  ``release`` accepts only blocks that were handed out and not yet returned, each once per
+  call; anything else is an error raised before anything is changed.
 """
 from __future__ import annotations
 
@@ -35,20 +38,29 @@ class BlockAllocator:
         self.num_blocks = num_blocks
         self.block_size = block_size
         self.free = deque(range(num_blocks))
+        self.held = set()
 
     def free_count(self) -> int:
         return len(self.free)
 
+    def _take(self) -> int:
+        i = self.free.popleft()
+        self.held.add(i)
+        return i
+
     def alloc(self, n: int) -> List[int]:
         if n < 0 or n > len(self.free):
             raise AllocatorError("out of blocks")
-        return [self.free.popleft() for _ in range(n)]
+        return [self._take() for _ in range(n)]
 
     def release(self, ids: Iterable[int]) -> None:
-        ids = list(ids)
+        ids = [int(i) for i in ids]
         for i in ids:
             if not 0 <= i < self.num_blocks:
                 raise AllocatorError("block id out of range")
+        if len(set(ids)) != len(ids) or not self.held.issuperset(ids):
+            raise AllocatorError("block not in use (already free, or twice in one release)")
+        self.held.difference_update(ids)
         self.free.extend(ids)
 
     def prepare_step(self, block_tables: np.ndarray, positions: np.ndarray) -> np.ndarray:
@@ -68,7 +80,7 @@ class BlockAllocator:
         for b in range(B):
             p = int(positions[b])
             if p % bs == 0:
-                block_tables[b, p // bs] = self.free.popleft()
+                block_tables[b, p // bs] = self._take()
             slots[b] = int(block_tables[b, p // bs]) * bs + p % bs
         return slots
 

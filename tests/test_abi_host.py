@@ -58,6 +58,11 @@ def test_block_pool_matches_the_allocator_model_bit_for_bit(L):
             np.testing.assert_array_equal(ids, t_mod[b, :n])
             pool.release(ids)
             model.release(ids.tolist())
+            if len(ids):  # returning them again is refused by both, with nothing changed
+                with pytest.raises(_lib.NSError):
+                    pool.release(ids[:1])
+                with pytest.raises(AllocatorError):
+                    model.release(ids[:1].tolist())
             ctx[b] = 0
             t_lib[b] = 0
             t_mod[b] = 0
@@ -94,6 +99,15 @@ def test_block_pool_errors(L):
     assert pool.reserve(2).tolist() == [0, 1]
     with pytest.raises(_lib.NSError):
         pool.reserve(1)
+    # a block has one owner: returning a free block, or one block twice in a call, is refused
+    # and leaves the free list as it was (the allocator model's rule)
+    pool.release([1])
+    for bad in ([1], [0, 0], [0, 1]):
+        with pytest.raises(_lib.NSError) as e:
+            pool.release(bad)
+        assert e.value.status == 1 and pool.free_count() == 1
+    pool.release([0])
+    assert pool.free_count() == 2 and pool.reserve(2).tolist() == [1, 0]
 
 
 def _meta(B=3, bs=16, mb=4, nb=20, vocab=50):
@@ -129,3 +143,18 @@ def test_step_metadata_validation(L):
     long_pos = db.positions.copy(); long_pos[2] = 64
     long_len = db.seq_lens.copy(); long_len[2] = 65
     assert _chk(kw3, db, positions=long_pos, seq_lens=long_len) == 1
+    # the largest int32 position (seq_len wrapped to the smallest int32) is rejected before
+    # p + 1 is formed or a table entry past the row is read
+    huge_pos = db.positions.copy(); huge_pos[1] = 2 ** 31 - 1
+    huge_len = db.seq_lens.copy(); huge_len[1] = -2 ** 31
+    assert _chk(kw, db, positions=huge_pos, seq_lens=huge_len) == 1
+    neg_pos = db.positions.copy(); neg_pos[0] = -1
+    zero_len = db.seq_lens.copy(); zero_len[0] = 0
+    assert _chk(kw, db, positions=neg_pos, seq_lens=zero_len) == 1
+    # the last slot of a full table is accepted
+    full_tab = db.block_tables.copy(); full_tab[2] = [3, 5, 7, 9]
+    last_pos = db.positions.copy(); last_pos[2] = 63
+    last_len = db.seq_lens.copy(); last_len[2] = 64
+    last_slot = db.slot_mapping.copy(); last_slot[2] = 9 * 16 + 15
+    assert _chk(kw, db, positions=last_pos, seq_lens=last_len, block_tables=full_tab,
+                slot_mapping=last_slot) == 0

@@ -46,6 +46,26 @@ def test_allocator_model_errors_leave_state_unchanged():
     assert a.free_count() == 2
 
 
+def test_allocator_model_rejects_returning_a_block_it_does_not_hold():
+    """A slot holds one token of one request, so a block returned twice (or never handed out)
+    would later go to two requests at once; the release is refused and nothing changes."""
+    a = BlockAllocator(4, 4)
+    got = a.alloc(2)
+    assert got == [0, 1]
+    for bad in ([2], [0, 0], [1, 3], [0, 1, 0]):
+        with pytest.raises(AllocatorError):
+            a.release(bad)
+        assert list(a.free) == [2, 3] and a.held == {0, 1}
+    a.release([1])
+    with pytest.raises(AllocatorError):
+        a.release([1])
+    assert list(a.free) == [2, 3, 1]
+    tables = np.zeros((1, 2), dtype=np.int32)
+    a.prepare_step(tables, np.array([0]))     # hands out block 2 through a table
+    a.release([int(tables[0, 0]), 0])
+    assert list(a.free) == [3, 1, 2, 0] and not a.held
+
+
 def test_allocator_model_never_hands_out_a_block_twice():
     rng = np.random.default_rng(0)
     a = BlockAllocator(64, 16)

@@ -206,6 +206,20 @@ void ns::set_last_error(const char* msg) { g_msg = msg ? msg : ""; }
 struct ns_block_pool {
   int num_blocks = 0, block_size = 0, mb = 0;
   std::deque<int> free_list;
+  std::vector<uint8_t> held;  // 1 while a block is handed out (a block has one owner)
+
+  void reset(int n) {
+    num_blocks = n;
+    free_list.clear();
+    for (int i = 0; i < n; ++i) free_list.push_back(i);
+    held.assign(static_cast<size_t>(n), 0);
+  }
+  int take() {
+    const int id = free_list.front();
+    free_list.pop_front();
+    held[static_cast<size_t>(id)] = 1;
+    return id;
+  }
 };
 
 namespace {
@@ -225,10 +239,7 @@ ns_status pool_prepare(ns_block_pool* p, int batch, const int32_t* positions, in
   for (int b = 0; b < batch; ++b) {
     const int pos = positions[b];
     int32_t* row = block_tables + static_cast<size_t>(b) * mb;
-    if (pos % bs == 0) {
-      row[pos / bs] = p->free_list.front();
-      p->free_list.pop_front();
-    }
+    if (pos % bs == 0) row[pos / bs] = p->take();
     slot_mapping[b] = static_cast<int64_t>(row[pos / bs]) * bs + pos % bs;
   }
   return NS_OK;
@@ -237,10 +248,7 @@ ns_status pool_prepare(ns_block_pool* p, int batch, const int32_t* positions, in
 ns_status pool_reserve(ns_block_pool* p, int n, int32_t* out_ids) {
   if ((n > 0 && out_ids == nullptr) || n < 0) return fail(NS_ERR_INVALID_ARG, "argument");
   if (static_cast<size_t>(n) > p->free_list.size()) return fail(NS_ERR_OUT_OF_BLOCKS, "out of KV blocks");
-  for (int i = 0; i < n; ++i) {
-    out_ids[i] = p->free_list.front();
-    p->free_list.pop_front();
-  }
+  for (int i = 0; i < n; ++i) out_ids[i] = p->take();
   return NS_OK;
 }
 
@@ -248,7 +256,19 @@ ns_status pool_release(ns_block_pool* p, const int32_t* ids, int n) {
   if ((n > 0 && ids == nullptr) || n < 0) return fail(NS_ERR_INVALID_ARG, "argument");
   for (int i = 0; i < n; ++i)
     if (ids[i] < 0 || ids[i] >= p->num_blocks) return fail(NS_ERR_INVALID_ARG, "block id out of range");
-  for (int i = 0; i < n; ++i) p->free_list.push_back(ids[i]);
+  // each id must be handed out and appear once: mark as seen (2), undo the marks on failure
+  for (int i = 0; i < n; ++i) {
+    uint8_t& h = p->held[static_cast<size_t>(ids[i])];
+    if (h != 1) {
+      for (int j = 0; j < i; ++j) p->held[static_cast<size_t>(ids[j])] = 1;
+      return fail(NS_ERR_INVALID_ARG, "block not in use (already free, or twice in one release)");
+    }
+    h = 2;
+  }
+  for (int i = 0; i < n; ++i) {
+    p->held[static_cast<size_t>(ids[i])] = 0;
+    p->free_list.push_back(ids[i]);
+  }
   return NS_OK;
 }
 
@@ -260,12 +280,14 @@ ns_status check_meta(int num_blocks, int bs, int mb, int vocab, int max_batch, i
   if (batch < 1 || batch > max_batch) return fail(NS_ERR_INVALID_ARG, "batch out of range");
   if ((src_rows == 0 && !token_ids) || !positions || !block_tables || !seq_lens || !slot_mapping)
     return fail(NS_ERR_INVALID_ARG, "null argument");
+  const long long cap = static_cast<long long>(mb) * bs;
   for (int b = 0; b < batch; ++b) {
     const int p = positions[b], L = seq_lens[b];
     if (token_ids && (token_ids[b] >= vocab || token_ids[b] < -src_rows))
       return fail(NS_ERR_INVALID_ARG, "token id out of range");
-    if (p < 0 || L != p + 1) return fail(NS_ERR_INVALID_ARG, "seq_lens must equal positions + 1");
-    if (L > mb * bs) return fail(NS_ERR_INVALID_ARG, "seq_len beyond max_blocks_per_seq * block_size");
+    // bound the position before p + 1 is formed (no overflow, no table read past the row)
+    if (p < 0 || p >= cap) return fail(NS_ERR_INVALID_ARG, "position outside [0, max_blocks_per_seq * block_size)");
+    if (L != p + 1) return fail(NS_ERR_INVALID_ARG, "seq_lens must equal positions + 1");
     const int32_t* row = block_tables + static_cast<size_t>(b) * mb;
     const int nblk = (L + bs - 1) / bs;
     for (int i = 0; i < nblk; ++i)
@@ -997,11 +1019,9 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   NS_CUDA(cudaMemset(h->attn_counters, 0, rows_heads * sizeof(int)));
   NS_CUDA(cudaMalloc(&h->attn_partials,
                      rows_heads * attn_slot_floats(h->max_chunks, G, c.head_dim) * sizeof(float)));
-  h->pool.num_blocks = num_blocks;
   h->pool.block_size = block_size;
   h->pool.mb = c.max_blocks_per_seq;
-  h->pool.free_list.clear();
-  for (int i = 0; i < num_blocks; ++i) h->pool.free_list.push_back(i);
+  h->pool.reset(num_blocks);
   return NS_OK;
 }
 
@@ -1043,10 +1063,9 @@ ns_status ns_pool_create(int num_blocks, int block_size, int max_blocks_per_seq,
   if (out == nullptr || num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
     return fail(NS_ERR_INVALID_ARG, "pool arguments");
   ns_block_pool* p = new ns_block_pool();
-  p->num_blocks = num_blocks;
   p->block_size = block_size;
   p->mb = max_blocks_per_seq;
-  for (int i = 0; i < num_blocks; ++i) p->free_list.push_back(i);
+  p->reset(num_blocks);
   *out = p;
   return NS_OK;
 }
