@@ -158,3 +158,33 @@ def test_step_metadata_validation(L):
     last_slot = db.slot_mapping.copy(); last_slot[2] = 9 * 16 + 15
     assert _chk(kw, db, positions=last_pos, seq_lens=last_len, block_tables=full_tab,
                 slot_mapping=last_slot) == 0
+
+
+def test_binding_refuses_host_memory_where_kernels_read_device_memory(L):
+    """A host buffer (numpy array or CPU tensor) passed where a kernel reads device memory, or
+    a device buffer of the wrong type, is refused by the binding with INVALID_ARG before
+    anything reaches the library."""
+    import torch
+    logits = torch.zeros((2, 5))
+    ids = torch.zeros(2, dtype=torch.int32)
+    for call in (lambda: _lib.greedy_argmax(logits, ids),
+                 lambda: _lib.linear(np.zeros((128, 64), np.uint16), np.zeros((1, 64), np.uint16),
+                                     torch.zeros((1, 128)), 1, 128, 64, "bf16"),
+                 lambda: _lib.attn_decode(torch.zeros(8), torch.zeros(8), torch.zeros(8),
+                                          np.zeros((1, 1), np.int32), np.ones(1, np.int32),
+                                          torch.zeros(8), 2, 1, 64, 16, 1, 1, 0.125, "bf16")):
+        with pytest.raises(_lib.NSError) as e:
+            call()
+        assert e.value.status == 1 and "device memory" in str(e.value)
+    # raw device addresses pass through untouched (the caller vouches for them); None stays None
+    assert _lib._dev(0x7F0000000000, "x") == 0x7F0000000000 and _lib._dev(None, "x") is None
+
+
+def test_binding_refuses_metadata_of_unequal_row_counts(L):
+    db, kw = _meta()
+    assert _chk(kw, db, seq_lens=db.seq_lens[:2]) == 1
+    assert _chk(kw, db, slot_mapping=db.slot_mapping[:1]) == 1
+    assert _chk(kw, db, block_tables=db.block_tables[:, :3]) == 1
+    with pytest.raises(_lib.NSError) as e:
+        _lib._same_rows(3, token_ids=np.zeros(3), seq_lens=np.zeros(2))
+    assert e.value.status == 1 and "seq_lens" in str(e.value)

@@ -182,6 +182,30 @@ def memcpy(dst: int, src: int, nbytes: int) -> None:
         raise RuntimeError(f"cudaMemcpy failed ({r})")
 
 
+def _dev(a, what: str, dtype: Optional[str] = None, min_numel: int = 0) -> Optional[int]:
+    """Address of an argument the library hands to its kernels: a contiguous CUDA tensor (of
+    torch dtype ``dtype`` and at least ``min_numel`` elements, where given) or a raw device
+    address (an int, the caller's responsibility).  Host memory or a short buffer would be
+    dereferenced on the device, so it is refused here, before anything is launched, with the
+    library's own INVALID_ARG status."""
+    if a is None or isinstance(a, int):
+        return a
+    if isinstance(a, np.ndarray) or not getattr(a, "is_cuda", False):
+        raise NSError(1, f"{what} must be device memory (a CUDA tensor or a device address)")
+    if dtype is not None and str(a.dtype) != "torch." + dtype:
+        raise NSError(1, f"{what} must be {dtype}, not {a.dtype}")
+    if a.numel() < min_numel:
+        raise NSError(1, f"{what} has {a.numel()} elements, needs at least {min_numel}")
+    return _ptr(a)
+
+
+def _same_rows(batch: int, **arrays) -> None:
+    """Host metadata arrays must all describe ``batch`` rows (the library reads that many)."""
+    for name, a in arrays.items():
+        if a is not None and (a.ndim < 1 or a.shape[0] != batch):
+            raise NSError(1, f"{name} has {a.shape[0] if a.ndim else 0} rows, the batch is {batch}")
+
+
 def _ptr(a) -> Optional[int]:
     if a is None:
         return None
@@ -321,8 +345,11 @@ class DecodeStep:
         slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
         if tab.ndim != 2 or tab.shape[1] != self.mb:
             raise ValueError(f"block_tables must be [batch, {self.mb}]")
-        check(lib().ns_decode_step(self.h, pos.shape[0], _ptr(tok), _ptr(pos), _ptr(tab),
-                                   _ptr(sl), _ptr(slot), _ptr(logits), _stream(stream)))
+        B = pos.shape[0] if pos.ndim == 1 else -1
+        _same_rows(B, token_ids=tok, block_tables=tab, seq_lens=sl, slot_mapping=slot)
+        out = _dev(logits, "logits", "float32", B * self.shape.vocab)
+        check(lib().ns_decode_step(self.h, B, _ptr(tok), _ptr(pos), _ptr(tab),
+                                   _ptr(sl), _ptr(slot), out, _stream(stream)))
 
     def device_error(self) -> int:
         c = I()
@@ -341,7 +368,7 @@ class DecodeStep:
     def set_token_source(self, device_ids=None) -> None:
         """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,
         from the host arrays passed to ``step``."""
-        check(lib().ns_set_token_source(self.h, _ptr(device_ids)))
+        check(lib().ns_set_token_source(self.h, _dev(device_ids, "device_ids", "int32")))
 
     def pool(self) -> int:
         """The handle's block pool (borrowed), for ``BatchFormer``."""
@@ -413,7 +440,8 @@ def attn_decode(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
                 num_blocks: int, scale: float, dtype: str, stream=None, cta_budget: int = 0) -> None:
     """Paged decode attention; ``cta_budget`` > 0 caps its CTAs (ns_attn_decode_capped)."""
     batch = int(seq_lens.shape[0])
-    args = (_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(out),
+    args = (_dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+            _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"), _dev(out, "out"),
             batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
             float(scale), DTYPES[dtype])
     if cta_budget:
@@ -428,20 +456,23 @@ def attn_decode_noalloc(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_head
                         dev_err=None, stream=None) -> None:
     """The allocation-free attention call (fixed in-library scratch; see include/ns.h)."""
     batch = int(seq_lens.shape[0])
-    check(lib().ns_attn_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
-                                       _ptr(seq_lens), _ptr(out), batch, n_q_heads, n_kv_heads,
-                                       head_dim, block_size, max_blocks_per_seq, num_blocks,
-                                       float(scale), DTYPES[dtype], _ptr(dev_err),
-                                       _stream(stream)))
+    check(lib().ns_attn_decode_noalloc(_dev(q, "q"), _dev(k_pool, "k_pool"),
+                                       _dev(v_pool, "v_pool"), _dev(block_tables, "block_tables"),
+                                       _dev(seq_lens, "seq_lens"), _dev(out, "out"), batch,
+                                       n_q_heads, n_kv_heads, head_dim, block_size,
+                                       max_blocks_per_seq, num_blocks, float(scale), DTYPES[dtype],
+                                       _dev(dev_err, "dev_err"), _stream(stream)))
 
 
 def linear(w, x, y, m: int, n: int, k: int, dtype: str, stream=None) -> None:
-    check(lib().ns_linear(_ptr(w), _ptr(x), _ptr(y), m, n, k, DTYPES[dtype], _stream(stream)))
+    check(lib().ns_linear(_dev(w, "w"), _dev(x, "x"), _dev(y, "y"), m, n, k, DTYPES[dtype],
+                          _stream(stream)))
 
 
 def greedy_argmax(logits, out_ids, stream=None) -> None:
     b, v = int(logits.shape[0]), int(logits.shape[1])
-    check(lib().ns_greedy_argmax(_ptr(logits), b, v, _ptr(out_ids), _stream(stream)))
+    check(lib().ns_greedy_argmax(_dev(logits, "logits", "float32"), b, v,
+                                 _dev(out_ids, "out_ids", "int32", b), _stream(stream)))
 
 
 def device_error() -> int:
@@ -501,6 +532,13 @@ def check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab, max_b
     tab = np.ascontiguousarray(block_tables, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    try:
+        _same_rows(pos.shape[0] if pos.ndim == 1 else -1, token_ids=tok, block_tables=tab,
+                   seq_lens=sl, slot_mapping=slot)
+    except NSError as e:
+        return e.status
+    if tab.ndim != 2 or tab.shape[1] != max_blocks_per_seq:
+        return 1
     return lib().ns_check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab,
                                         max_batch, tok.shape[0], _ptr(tok), _ptr(pos),
                                         _ptr(tab), _ptr(sl), _ptr(slot))
