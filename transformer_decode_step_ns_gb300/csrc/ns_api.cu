@@ -996,11 +996,12 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
     return fail(num_blocks <= 0 ? NS_ERR_INVALID_ARG : NS_ERR_UNSUPPORTED, "num_blocks > 0, block_size 16");
   const ns_model_cfg& c = h->cfg;
   // one block past the caller's pool takes the rows that pad a batch up to a graph bucket
-  const size_t pool = static_cast<size_t>(num_blocks + 1) * c.n_kv_heads * block_size * c.head_dim * 2;
-  NS_CUDA(cudaSetDevice(h->dev));
-  const long long pool_rows = static_cast<long long>(num_blocks + 1) * c.n_kv_heads * block_size;
+  const long long blocks = static_cast<long long>(num_blocks) + 1;
+  const long long pool_rows = blocks * c.n_kv_heads * block_size;
   if (pool_rows >= (1ll << 31))
     return fail(NS_ERR_UNSUPPORTED, "pool rows (blocks * kv heads * block_size) must fit in int32");
+  const size_t pool = static_cast<size_t>(pool_rows) * c.head_dim * 2;
+  NS_CUDA(cudaSetDevice(h->dev));
   NS_CUDA(cudaMalloc(&h->pools, pool * 2 * c.n_layers));
   // never-written slots read as zeros (finite), never as stale garbage
   NS_CUDA(cudaMemset(h->pools, 0, pool * 2 * c.n_layers));
