@@ -139,6 +139,11 @@ def test_step_metadata_validation(L):
     assert _chk(kw, db, slot_mapping=bad_slot) == 1
     kw2 = dict(kw); kw2["max_batch"] = 2
     assert _chk(kw2, db) == 1
+    # an empty step is refused (nothing to launch), as is a negative position
+    empty = dict(token_ids=db.token_ids[:0], positions=db.positions[:0],
+                 block_tables=db.block_tables[:0], seq_lens=db.seq_lens[:0],
+                 slot_mapping=db.slot_mapping[:0])
+    assert _chk(kw, db, **empty) == 1
     kw3 = dict(kw); kw3["max_blocks_per_seq"] = 4
     long_pos = db.positions.copy(); long_pos[2] = 64
     long_len = db.seq_lens.copy(); long_len[2] = 65

@@ -283,6 +283,11 @@ def test_library_former_errors(L):
     with pytest.raises(L.NSError):
         f.tokens(0)
     assert L.BatchFormer(pool, 1, 4, 0).counts() == (0, 0, 0, 0)
+    # with nothing to run, a step has no rows and commits nothing
+    idle = L.BatchFormer(L.BlockPool(4, 4, 4), 8, 4, 0)
+    s = idle.next()
+    assert all(len(s[k]) == 0 for k in ("token_ids", "positions", "seq_lens", "slot_mapping"))
+    assert idle.commit([]) == [] and idle.counts() == (0, 0, 0, 0)
     with pytest.raises(L.NSError):
         L.BatchFormer(pool, 4, 4, 0, -1)
 
