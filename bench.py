@@ -1051,6 +1051,19 @@ def replica_aggregate(ms_local: float, units_local: int, world: int):
     return float(t.item()), int(u.item())
 
 
+def repeat_check(ms_a: float, n_a: int, ms_b: float, n_b: int, limit: float = 0.15):
+    """The timed steps read as two back-to-back runs (first and second half): each run's ms per
+    step and whether they differ by more than ``limit`` of the faster one (clocks that had not
+    settled, or another tenant's load; such a number is re-measured).  None when a half is
+    empty."""
+    if n_a < 1 or n_b < 1:
+        return None
+    a, b = ms_a / n_a, ms_b / n_b
+    spread = abs(a - b) / max(min(a, b), 1e-12)
+    return {"ms_per_step_halves": [round(a, 4), round(b, 4)], "spread": round(spread, 4),
+            "limit": limit, "flagged": spread > limit}
+
+
 def run_ours(args, rank, world):
     import torch
     import __graft_entry__ as ge
@@ -1082,14 +1095,20 @@ def run_ours(args, rank, world):
             wl.step(warm_meta)
         torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_mid = torch.cuda.Event(enable_timing=True)
+    half = K // 2
     clocks.mark_start()
     e0.record()
-    for m in metas:
+    for i, m in enumerate(metas):
+        if i == half:
+            e_mid.record()
         wl.step(m)
     e1.record()
     torch.cuda.synchronize()
     clocks.mark_stop()
     ms_total = e0.elapsed_time(e1)
+    repeat = (repeat_check(e0.elapsed_time(e_mid), half, e_mid.elapsed_time(e1), K - half)
+              if half >= 1 else None)
     clk = clocks.stop()
     ms_total, units = replica_aggregate(ms_total, wl.B * K, world)
     dev_err = wl.dev.device_error()
@@ -1256,6 +1275,7 @@ def run_ours(args, rank, world):
         "serving": serve,
         "cpu_baseline": cpu,
         "clocks": clk,
+        "repeat": repeat,
         "gpu_launches": info.kernels_per_step * K,
         "kernels_per_step": info.kernels_per_step,
         "graph_capture_ms": info.last_capture_ms,
