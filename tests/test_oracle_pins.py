@@ -225,6 +225,42 @@ def test_storage_round_trip_matches_torch_rounding():
         np.testing.assert_array_equal(mine, ref)
 
 
+def test_storage_rounding_of_exact_midpoints_is_half_to_even():
+    """Values exactly halfway between two neighbours of the storage type (IEEE 754 round to
+    nearest, ties to even): the fp32 patterns whose dropped 16 bits are 0x8000 (bf16) and the
+    fp64 values halfway between fp16 neighbours, with even and odd kept last bits, of both
+    signs, and at the edge where the rounding carries into the exponent; checked against torch's
+    own conversion and the by-hand results."""
+    # bf16: kept part 0x3F80 (1.0, even) and 0x3F81 (odd), 0x3FFF (odd, carries to 0x4000)
+    pats = np.array([0x3F808000, 0x3F818000, 0x3FFF8000, 0xBF808000, 0xBF818000,
+                     0x3F808001, 0x3F807FFF], dtype=np.uint32)
+    x = pats.view(np.float32).astype(np.float64)
+    got = oracle.round_storage(x, "bf16")
+    np.testing.assert_array_equal(got, [0x3F80, 0x3F82, 0x4000, 0xBF80, 0xBF82, 0x3F81, 0x3F80])
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy()
+    np.testing.assert_array_equal(got, ref.view(np.uint16))
+    # fp16: 1 + 2^-11 lies halfway between 1 and 1 + 2^-10 (ties to 1, the even one);
+    # 1 + 3 * 2^-11 halfway between 1 + 2^-10 (odd) and 1 + 2^-9 (even)
+    x = np.array([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, -(1 + 2.0 ** -11), 2047.5 + 0.5])
+    got = oracle.from_storage(oracle.round_storage(x, "f16"), "f16")
+    np.testing.assert_array_equal(got, [1.0, 1 + 2.0 ** -9, -1.0, 2048.0])
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.float16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_greedy_argmax_breaks_ties_to_the_lowest_index():
+    """Brute force: the first index holding the row maximum, on rows with many exact ties."""
+    rng = _rng(17)
+    logits = rng.integers(-3, 3, size=(64, 37)).astype(np.float64)
+    logits[0] = 5.0                        # every entry ties
+    logits[1, [4, 30]] = 9.0               # two maxima
+    got = oracle.greedy_argmax(logits)
+    for r in range(logits.shape[0]):
+        first = next(i for i, v in enumerate(logits[r]) if v == max(logits[r]))
+        assert got[r] == first
+    assert got[0] == 0 and got[1] == 4
+
+
 # ------------------------------------------------------------------ whole step
 
 
