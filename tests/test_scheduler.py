@@ -90,6 +90,106 @@ def test_preemption_worked_example_by_hand():
     assert m.tokens(B) == [60, 61, 61, 61, 62] and m.counts() == (0, 1, 0, 1)
 
 
+def _moves(m):
+    return [(v.kind, v.rid, v.n_tokens, list(v.table)) for v in m.moves]
+
+
+def test_preempted_requests_resume_first_in_first_out_by_hand():
+    """Pool of 5 blocks of 4, predicted decode length 1.  Peaks: r0 (5 prompt tokens) 2 blocks,
+    r1 (3), r2 (4), r3 (3) one each.  Step 0 places r0's prompt (blocks 0, 1) and r1's (block 2);
+    step 1 decodes both and places r2's prompt (block 3) and two tokens of r3's (block 4).
+    Step 2: r1 and r2 both cross into a new block with none free, so r2 (last running) is saved;
+    step 4: r0 and r3 do the same, so r3 is saved too.  When r1 finishes, two blocks come back;
+    resuming needs the cached tokens' blocks plus the block of the next position (2 each), so
+    only one request fits: r2, saved first, resumes at step 5, and r3 only at step 7."""
+    m = DenseBatchFormer(BlockAllocator(5, 4), dense_tokens=8, max_blocks_per_seq=8,
+                         eos_token=999, predicted_new=1)
+    for i, (pl, mn) in enumerate([(5, 8), (3, 5), (4, 3), (3, 4)]):
+        m.add(i, list(range(100 * i, 100 * i + pl)), mn)
+    want = {  # step: (rows' requests, positions, slots, moves)
+        0: ([0, 0, 0, 0, 0, 1, 1, 1], [0, 1, 2, 3, 4, 0, 1, 2], [0, 1, 2, 3, 4, 8, 9, 10], []),
+        1: ([0, 1, 2, 2, 2, 2, 3, 3], [5, 3, 0, 1, 2, 3, 0, 1], [5, 11, 12, 13, 14, 15, 16, 17], []),
+        2: ([0, 1, 3], [6, 4, 2], [6, 12, 18], [(0, 2, 4, [3])]),
+        3: ([0, 1, 3], [7, 5, 3], [7, 13, 19], []),
+        4: ([0, 1], [8, 6], [16, 14], [(0, 3, 4, [4])]),
+        5: ([0, 2], [9, 4], [17, 12], [(1, 2, 4, [2])]),
+        6: ([0, 2], [10, 5], [18, 13], []),
+        7: ([0, 3], [11, 4], [19, 12], [(1, 3, 4, [2])]),
+        8: ([3], [5], [13], []),
+    }
+    for k in range(9):
+        s = m.next()
+        req, pos, slots, moves = want[k]
+        np.testing.assert_array_equal(s.row_request, req, err_msg=f"step {k}")
+        np.testing.assert_array_equal(s.positions, pos, err_msg=f"step {k}")
+        np.testing.assert_array_equal(s.slot_mapping, slots, err_msg=f"step {k}")
+        assert _moves(m) == moves, k
+        if k == 4:
+            assert list(m.swapped) == [2, 3]
+        m.commit(np.full(len(s.token_ids), 50 + k, np.int32))
+    assert m.counts() == (0, 0, 0, 4)
+    assert m.tokens(2) == [51, 55, 56] and m.tokens(3) == [52, 53, 57, 58]
+
+
+def test_no_resumption_in_a_step_that_preempts_by_hand():
+    """Pool of 4 blocks of 4, predicted decode length 1.  r0 (4 prompt tokens, 6 new) runs
+    alone until step 4, when r1 (4 prompt tokens) and r2 (1 token) arrive and take the last two
+    blocks.  At step 5 r0 and r1 both need a new block and none is free: r2 (last running) is
+    saved, which frees one block, still short, so r1 is saved too.  r2 would fit again at once,
+    but a step that preempts resumes nothing; both come back at step 6, r2 first (saved
+    first), once r0 has finished."""
+    m = DenseBatchFormer(BlockAllocator(4, 4), dense_tokens=8, max_blocks_per_seq=8,
+                         eos_token=999, predicted_new=1)
+    m.add(0, [0, 1, 2, 3], 6)
+    for k in range(4):
+        m.commit(np.full(len(m.next().token_ids), 50 + k, np.int32))
+    m.add(1, [100, 101, 102, 103], 3)
+    m.add(2, [200], 3)
+    s = m.next()
+    np.testing.assert_array_equal(s.row_request, [0, 1, 1, 1, 1, 2])
+    np.testing.assert_array_equal(s.slot_mapping, [7, 8, 9, 10, 11, 12])
+    m.commit(np.full(6, 54, np.int32))
+    s = m.next()
+    assert _moves(m) == [(0, 2, 1, [3]), (0, 1, 4, [2])]
+    np.testing.assert_array_equal(s.row_request, [0])
+    np.testing.assert_array_equal(s.slot_mapping, [12])   # r0 takes block 3, r2's old block
+    assert list(m.pool.free) == [2] and list(m.swapped) == [2, 1]
+    assert m.commit([55]) == [0]
+    s = m.next()
+    assert _moves(m) == [(1, 2, 1, [2]), (1, 1, 4, [0])]
+    np.testing.assert_array_equal(s.row_request, [2, 1])
+    np.testing.assert_array_equal(s.positions, [1, 4])
+    np.testing.assert_array_equal(s.slot_mapping, [9, 4])  # r1's position 4 takes block 1
+
+
+def test_prompts_wait_while_a_preempted_request_cannot_resume_by_hand():
+    """Pool of 6 blocks of 4, predicted decode length 1: A and S (8 prompt tokens each, 12 new)
+    fill the pool; at step 5 A needs a block and S is saved (10 tokens, blocks 3, 4, 5).  P
+    (2 prompt tokens, 1 new: a one-block peak) arrives at step 9, when one block is free after
+    A's decode block: P alone would fit, but S needs 3 blocks to resume, so P waits; when A
+    finishes, S resumes (blocks 5, 0, 1) and P starts in the same step."""
+    m = DenseBatchFormer(BlockAllocator(6, 4), dense_tokens=8, max_blocks_per_seq=8,
+                         eos_token=999, predicted_new=1)
+    A, S, P = 1, 2, 3
+    m.add(A, list(range(10, 18)), 12)
+    m.add(S, list(range(20, 28)), 12)
+    for k in range(13):
+        if k == 9:
+            m.add(P, [30, 31], 1)
+        s = m.next()
+        if k == 5:
+            assert _moves(m) == [(0, S, 10, [3, 4, 5])]
+        if 9 <= k <= 11:
+            np.testing.assert_array_equal(s.row_request, [A])   # P waits, one block free
+            assert m.counts() == (1, 1, 1, 0)
+        if k == 12:
+            assert _moves(m) == [(1, S, 10, [5, 0, 1])]
+            np.testing.assert_array_equal(s.row_request, [S, P, P])
+            np.testing.assert_array_equal(s.slot_mapping, [6, 8, 9])
+        m.commit(np.full(len(s.token_ids), 5, np.int32))
+    assert m.counts() == (0, 1, 0, 2)
+
+
 def _random_run(form, rng, n_steps, vocab, eos, add_prob, max_prompt, max_new_hi):
     """Drive a former (model or library) with seeded arrivals and sampled tokens; yield each
     step's rows (or the error class) and finished ids."""
@@ -407,20 +507,73 @@ def _sampler_for(vocab):
     return sample
 
 
-@pytest.mark.parametrize("case", [(16, 4, 200, 32, 30, 3, 20, 8), (33, 16, 400, 32, 100, 7, 60, 20)])
-def test_async_formation_generates_what_sync_formation_does(L, case):
+ASYNC_CASES = [(16, 4, 200, 32, 30, 3, 20, 8), (33, 16, 400, 32, 100, 7, 60, 20)]
+
+
+def _formed_blocks(rows, bs):
+    """(request, block) of every block the rows of one formed step read or write."""
+    out = set()
+    for b in range(len(rows["token_ids"])):
+        n = -(-int(rows["seq_lens"][b]) // bs)
+        for blk in rows["block_tables"][b, :n]:
+            out.add((int(rows["row_request"][b]), int(blk)))
+    return out
+
+
+@pytest.mark.parametrize("case", ASYNC_CASES)
+def test_async_formation_generates_what_sync_formation_does(case):
     """With a sampler that depends only on (request, position), asynchronous and synchronous
-    formation generate the same tokens for every request; the library equals the model row for
-    row in both modes."""
+    formation generate the same tokens for every request, and every block returns."""
     D, bs, nb, mb, vocab, eos, mp, mn = case
     outs = {}
     for async_mode in (False, True):
         model = _ModelAdapter(DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos))
+        model.m.set_async(async_mode)
+        n_req = 40
+        for _ in _pipelined(model, np.random.default_rng(17), n_req, vocab, eos, mp, mn,
+                            _sampler_for(vocab), async_mode):
+            pass
+        outs[async_mode] = {i: model.m.tokens(i) for i in range(n_req)}
+        assert model.m.counts()[3] == n_req and model.m.pool.free_count() == nb
+    assert outs[True] == outs[False]
+
+
+@pytest.mark.parametrize("case", ASYNC_CASES)
+def test_async_formation_keeps_the_blocks_of_formed_rows(case):
+    """While a formed step is not committed, every block its rows read or write stays out of
+    the free list and belongs to one request only, even after that request finished at the
+    previous step's commit (its blocks return only once no formed row of it is uncommitted)."""
+    D, bs, nb, mb, vocab, eos, mp, mn = case
+    m = DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos)
+    m.set_async(True)
+    model = _ModelAdapter(m)
+    pending = []
+    late_rows = 0
+    for ev in _pipelined(model, np.random.default_rng(23), 40, vocab, eos, mp, mn,
+                         _sampler_for(vocab), True):
+        if ev[0] == "formed":
+            pending.append(ev[1])
+        else:
+            pending.pop(0)
+        owned = set().union(*(_formed_blocks(r, bs) for r in pending)) if pending else set()
+        assert not {blk for _, blk in owned} & set(m.pool.free)
+        owner = {}
+        for rid, blk in owned:
+            assert owner.setdefault(blk, rid) == rid
+        late_rows += sum(1 for r in pending for q in r["row_request"] if m.req[int(q)].finished)
+    assert late_rows > 0  # the case does form rows for requests that already finished
+
+
+@pytest.mark.parametrize("case", ASYNC_CASES)
+def test_library_former_matches_the_model_in_both_formation_modes(L, case):
+    """The library equals the model row for row, synchronous and asynchronous."""
+    D, bs, nb, mb, vocab, eos, mp, mn = case
+    for async_mode in (False, True):
+        model = _ModelAdapter(DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos))
         pool = L.BlockPool(nb, bs, mb)
         lib_form = L.BatchFormer(pool, D, mb, eos)
-        if async_mode:
-            model.m.set_async(True)
-            lib_form.set_async(True)
+        model.m.set_async(async_mode)
+        lib_form.set_async(async_mode)
         n_req = 40
         a = _pipelined(model, np.random.default_rng(17), n_req, vocab, eos, mp, mn, _sampler_for(vocab), async_mode)
         b = _pipelined(lib_form, np.random.default_rng(17), n_req, vocab, eos, mp, mn, _sampler_for(vocab), async_mode)
@@ -431,7 +584,4 @@ def test_async_formation_generates_what_sync_formation_does(L, case):
                     np.testing.assert_array_equal(ea[1][k], eb[1][k], err_msg=k)
             else:
                 assert ea[1] == eb[1]
-        outs[async_mode] = {i: model.m.tokens(i) for i in range(n_req)}
-        assert all(lib_form.tokens(i) == outs[async_mode][i] for i in range(n_req))
-        assert model.m.counts()[3] == n_req and model.m.pool.free_count() == nb
-    assert outs[True] == outs[False]
+        assert all(lib_form.tokens(i) == model.m.tokens(i) for i in range(n_req))
