@@ -194,6 +194,36 @@ def test_step_work_counts_weights_once():
 # ------------------------------------------------------------------ input generator
 
 
+@pytest.mark.parametrize("dtype,tie", [("f16", True), ("bf16", False)])
+def test_step_weight_bytes_equal_the_arrays_a_step_reads(dtype, tie):
+    """Brute force: every layer array (projections and both norm gains), the final norm and
+    the head (the embedding when tied) of a generated model, byte for byte; the embedding table
+    of an untied model is only gathered, B rows, and counts under activations."""
+    shape = synth.tiny_shape(dtype=dtype, tie=tie, n_layers=3, hidden=64, n_q_heads=4,
+                             n_kv_heads=2, head_dim=16, ffn=96, vocab=80)
+    w = synth.model_weights(shape, 5)
+    arrays = [a for lw in w["layers"] for a in lw.values()]
+    arrays += [w["final_norm"], w["embed"] if tie else w["lm_head"]]
+    assert len(arrays) == 9 * 3 + 2
+    assert rl.decode_step_work(shape, [7, 1]).weight_bytes == sum(a.nbytes for a in arrays)
+
+
+def test_attention_bytes_equal_the_kv_rows_a_launch_gathers():
+    """Brute force: the bytes of the K and V rows gathered (``kv_rows``) for every cached token
+    of every request, against the per-launch figure the roofline divides by."""
+    rng = np.random.default_rng(3)
+    nb, hkv, bs, d = 40, 2, 4, 8
+    kp = rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)
+    vp = rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)
+    lens = [1, 4, 5, 17]
+    ids = iter(rng.permutation(nb).tolist())
+    total = 0
+    for n in lens:
+        table = np.array([next(ids) for _ in range(-(-n // bs))], dtype=np.int32)
+        total += oracle.kv_rows([kp], [vp], oracle.request_slots(table, 0, n, bs)).nbytes
+    assert rl.attention_bytes(lens, hkv, d, elt_bytes=2) == total
+
+
 def test_generator_is_counter_based_and_seeded():
     a = synth.normal(5, "x", (1000,), "bf16")
     b = synth.normal(5, "x", (400,), "bf16", offset=600)

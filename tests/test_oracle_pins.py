@@ -352,6 +352,18 @@ def test_decode_step_matches_independent_torch_statement(dtype, tie):
             np.testing.assert_array_equal(got, hk[l][b][-1].numpy())
 
 
+@pytest.mark.parametrize("dtype,tie", [("f16", True), ("bf16", False)])
+def test_step_flops_equal_torch_flop_count_of_the_independent_statement(dtype, tie):
+    """The roofline's FLOPs of a step (projections, attention QK and PV, LM head) equal what
+    PyTorch's own FLOP counter counts while running the independent statement of that step."""
+    from torch.utils.flop_counter import FlopCounterMode
+    from transformer_decode_step_ns_gb300 import roofline
+    shape, w, batch, _, _, hk, hv = _step_case(dtype, tie)
+    with FlopCounterMode(display=False) as fc:
+        _torch_step(shape, w, hk, hv, batch.token_ids, batch.positions)
+    assert fc.get_total_flops() == roofline.decode_step_work(shape, batch.seq_lens).flops
+
+
 def test_zero_layers_pass_the_embedding_through_to_a_tied_head():
     """With Wo = Wd = 0 the residual stream is the embedding row; a tied head then scores the
     input token itself highest, and the logits equal rs * E[tok] . E^T exactly."""
