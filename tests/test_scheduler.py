@@ -404,6 +404,10 @@ def test_tuner_candidate_splits():
     # a batch that is not a multiple of 128: the last nano-batch takes the remainder
     c = tuner.candidate_splits(1000)
     assert all(sum(s) == 1000 for s in c[1:]) and [128, 872] in c
+    # 7 units of 128 and 104 rows over: near-even thirds 3 + 2 + 2 units in every order, the
+    # last part taking the 104
+    assert sorted(s for s in c if s and len(s) == 3) == [[256, 256, 488], [256, 384, 360],
+                                                          [384, 256, 360]]
 
 
 def test_tuner_interference_row_arithmetic():
@@ -444,6 +448,14 @@ def test_tuner_search_measures_every_split_then_budgets_and_picks_the_fastest():
     # without a profile every budget is tried on the three fastest splits
     out = tuner.search(step, 2048, timer=timer)
     assert len(out["table"]) == len(stage1) + 3 * 16
+    # a budget exactly at min_p is kept; below it is not
+    edge = {"rows": [{"budget": 8, "P_attn": 0.5}, {"budget": 16, "P_attn": 0.49},
+                     {"budget": 24, "P_attn": 0.7}]}
+    assert tuner.search(step, 2048, profile=edge, timer=timer)["budgets_kept"] == [8, 24]
+    # fewer than two budgets clear min_p: the four with the highest co-run P_attn are tried
+    low = {"rows": [{"budget": b, "P_attn": p} for b, p in
+                    ((8, 0.1), (16, 0.45), (24, 0.2), (32, 0.3), (40, 0.05), (48, 0.4))]}
+    assert tuner.search(step, 2048, profile=low, timer=timer)["budgets_kept"] == [16, 48, 32, 24]
 
 
 def test_async_formation_worked_example_by_hand():
