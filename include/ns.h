@@ -49,7 +49,7 @@ typedef enum {
   NS_ERR_INVALID_ARG = 1,     /* argument out of range or inconsistent; nothing launched */
   NS_ERR_OUT_OF_MEMORY = 2,   /* device or pinned allocation failed */
   NS_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed */
-  NS_ERR_UNSUPPORTED = 4,     /* shape or dtype this build does not implement */
+  NS_ERR_UNSUPPORTED = 4,     /* shape or dtype this library does not implement */
   NS_ERR_NOT_INITIALIZED = 5, /* e.g. ns_decode_step before ns_kv_alloc */
   NS_ERR_DEVICE_CHECK = 6,    /* a kernel recorded a failed bounds check or a timed-out wait */
   NS_ERR_OUT_OF_BLOCKS = 7    /* the KV block pool has too few free blocks */
@@ -70,7 +70,7 @@ enum {
 typedef struct ns_ctx* ns_handle;
 
 /* Model configuration.  Dims: hidden H, n_layers L, n_q_heads Hq, n_kv_heads Hkv (Hq % Hkv
- * == 0, G = Hq / Hkv <= 8), head_dim d in {64, 128}, ffn F, vocab V.  This build requires
+ * == 0, G = Hq / Hkv <= 8), head_dim d in {64, 128}, ffn F, vocab V.  This library requires
  * H, Hq*d, Hkv*d, 2F, V multiples of 128 and H, Hq*d, F multiples of 64.
  * rope_theta: RoPE base; pairs (i, i + d/2), inverse frequency theta^(-2i/d).
  * rms_eps: RMSNorm epsilon, y = x / sqrt(mean(x^2) + eps) * gamma.
@@ -103,7 +103,7 @@ typedef struct {
 /* Create a handle on the current device.  Copies and re-lays-out the weights into
  * library-owned device memory (QKV concatenated, gate/up interleaved in 64-row groups), so
  * the caller may free its copies on return.  Creates the streams, events and TMA descriptors
- * the step uses.  Errors: INVALID_ARG (bad dims/pointers), UNSUPPORTED (shape this build
+ * the step uses.  Errors: INVALID_ARG (bad dims/pointers), UNSUPPORTED (shape this library
  * does not implement), OUT_OF_MEMORY, CUDA. */
 ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out);
 
