@@ -291,6 +291,17 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids,
                          const int32_t* seq_lens, const int64_t* slot_mapping,
                          float* logits_out, ns_stream_t stream);
 
+/* The prompt chunks ns_decode_step would find in a step (host only, no GPU): the first row of
+ * each, in row order.  Working back from the last row, each maximal run of at least 16 rows at
+ * consecutive positions whose first ceil(seq_len / block_size) block-table entries equal those
+ * of the run's last row is one chunk; the first shorter run ends the search.  Host arrays of
+ * `batch` rows (block_tables [batch][max_blocks_per_seq]); seq_lens in [1, max_blocks_per_seq
+ * * block_size] and positions >= 0, else INVALID_ARG.  *n = the number of chunks; the first
+ * min(*n, capacity) starts are written. */
+ns_status ns_find_prompt_chunks(int block_size, int max_blocks_per_seq, int batch,
+                                const int32_t* positions, const int32_t* block_tables,
+                                const int32_t* seq_lens, int32_t* starts, int capacity, int* n);
+
 /* Graph buckets ("Bounding the CUDA graph capture", model cold-start page: capture graphs for
  * a bounded set of batch sizes and pad).  With n > 0 ascending sizes (each <= max_batch), a
  * graph-replayed step of `batch` rows uses the graph of the smallest size >= batch; the rows

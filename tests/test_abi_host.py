@@ -193,3 +193,70 @@ def test_binding_refuses_metadata_of_unequal_row_counts(L):
     with pytest.raises(_lib.NSError) as e:
         _lib._same_rows(3, token_ids=np.zeros(3), seq_lens=np.zeros(2))
     assert e.value.status == 1 and "seq_lens" in str(e.value)
+
+
+def _chunk_rule(pos, tabs, sl, bs, min_rows=16):
+    """The documented rule, stated plainly: working back from the last row, grow a run while the
+    previous row sits one position earlier and reads the same leading blocks as the run's last
+    row; a run of at least min_rows rows is a chunk, a shorter one ends the search."""
+    starts, end = [], len(pos)
+    while end > 0:
+        f = end - 1
+        while f > 0:
+            need = -(-int(sl[f - 1]) // bs)
+            if pos[f - 1] != pos[f] - 1 or list(tabs[f - 1][:need]) != list(tabs[end - 1][:need]):
+                break
+            f -= 1
+        if end - f < min_rows:
+            break
+        starts.insert(0, f)
+        end = f
+    return starts
+
+
+def test_prompt_chunk_detection_by_hand_and_against_the_rule(L):
+    bs, mb = 16, 8
+    A = np.arange(0, 8, dtype=np.int32)
+    Bt = np.arange(8, 16, dtype=np.int32)
+    D = np.arange(16, 24, dtype=np.int32)
+
+    def find(rows):
+        pos = [p for p, _ in rows]
+        return _lib.find_prompt_chunks(bs, pos, np.stack([t for _, t in rows]), [p + 1 for p in pos])
+
+    dec = [(5, D), (9, D), (40, D)]
+    assert find(dec) == []                                             # decode rows only
+    assert find(dec + [(p, A) for p in range(16)]) == [3]              # exactly 16 rows: a chunk
+    assert find(dec + [(p, A) for p in range(15)]) == []               # 15 rows: not one
+    assert find(dec + [(p, A) for p in range(20)] + [(p, Bt) for p in range(30, 46)]) == [3, 23]
+    # the first shorter run ends the search: the 20-row run before the 5-row one is not found
+    assert find([(p, A) for p in range(20)] + [(p, D) for p in range(5)]
+                + [(p, Bt) for p in range(16)]) == [25]
+    # a position gap splits a run; so does a different block under the earlier row's tokens
+    assert find([(p, A) for p in range(16)] + [(p, A) for p in range(17, 33)]) == [0, 16]
+    other = A.copy()
+    other[0] = 99
+    assert find([(p, other) for p in range(16)] + [(p, A) for p in range(16, 32)]) == [0, 16]
+    # entries past a row's own blocks do not matter: only the blocks its tokens occupy compare
+    tail = A.copy()
+    tail[7] = 77
+    assert find([(p, tail) for p in range(16)] + [(p, A) for p in range(16, 24)]) == [0]
+    # random layouts against the stated rule
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        rows = []
+        for _ in range(int(rng.integers(1, 6))):
+            t = rng.permutation(64)[:mb].astype(np.int32)
+            n = int(rng.integers(1, 40))
+            p0 = int(rng.integers(0, mb * bs - n))
+            rows += [(p0 + k, t) for k in range(n)]
+        pos = [p for p, _ in rows]
+        tabs = np.stack([t for _, t in rows])
+        sl = [p + 1 for p in pos]
+        assert _lib.find_prompt_chunks(bs, pos, tabs, sl) == _chunk_rule(pos, tabs, sl, bs)
+    # bad lengths are refused before any table is read
+    with pytest.raises(_lib.NSError):
+        _lib.find_prompt_chunks(bs, [0], A[None], [0])
+    with pytest.raises(_lib.NSError):
+        _lib.find_prompt_chunks(bs, [127], A[None], [129])
+    assert _lib.find_prompt_chunks(bs, [], np.zeros((0, mb), np.int32), []) == []

@@ -38,7 +38,7 @@ SYMBOLS = (
     "ns_pool_geometry", "ns_kv_get_pool", "ns_sched_create", "ns_sched_destroy",
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
-    "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async",
+    "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async", "ns_find_prompt_chunks",
 )
 
 
@@ -119,6 +119,7 @@ def lib() -> ctypes.CDLL:
             "ns_pool_release": ([P, P, I], I),
             "ns_pool_free_count": ([P, ctypes.POINTER(I)], I),
             "ns_check_step_metadata": ([I, I, I, I, I, I, P, P, P, P, P], I),
+            "ns_find_prompt_chunks": ([I, I, I, P, P, P, P, I, ctypes.POINTER(I)], I),
             "ns_last_error_message": ([], ctypes.c_char_p),
             "ns_set_kernel_timing": ([P, I], I),
             "ns_set_token_source": ([P, P], I),
@@ -542,6 +543,22 @@ def check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab, max_b
     return lib().ns_check_step_metadata(num_blocks, block_size, max_blocks_per_seq, vocab,
                                         max_batch, tok.shape[0], _ptr(tok), _ptr(pos),
                                         _ptr(tab), _ptr(sl), _ptr(slot))
+
+
+def find_prompt_chunks(block_size: int, positions, block_tables, seq_lens) -> list:
+    """First rows of the prompt chunks ns_decode_step attends with the causal chunk kernel."""
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = pos.shape[0] if pos.ndim == 1 else -1
+    _same_rows(B, block_tables=tab, seq_lens=sl)
+    if tab.ndim != 2:
+        raise NSError(1, "block_tables must be [batch, max_blocks_per_seq]")
+    out = np.zeros(max(B, 1), dtype=np.int32)
+    n = I()
+    check(lib().ns_find_prompt_chunks(block_size, tab.shape[1], B, _ptr(pos), _ptr(tab), _ptr(sl),
+                                      _ptr(out), out.size, ctypes.byref(n)))
+    return out[:n.value].tolist()
 
 
 class BatchFormer:

@@ -298,6 +298,30 @@ ns_status check_meta(int num_blocks, int bs, int mb, int vocab, int max_batch, i
   return NS_OK;
 }
 
+// First rows of the prompt chunks of a step whose metadata passed check_meta: working back from
+// the last row, each maximal run of at least kPrefillMinRows rows at consecutive positions that
+// read the same blocks as the run's last row is one chunk; the first shorter run ends the search.
+std::vector<int> prompt_chunk_starts(int batch, const int32_t* positions, const int32_t* block_tables,
+                                     const int32_t* seq_lens, int mb, int bs) {
+  std::vector<int> runs;
+  int end = batch;
+  while (end > 0) {
+    const int32_t* tl = block_tables + static_cast<size_t>(end - 1) * mb;
+    int f = end - 1;
+    while (f > 0) {
+      const int b = f - 1;
+      if (positions[b] != positions[f] - 1) break;
+      const int need = (seq_lens[b] + bs - 1) / bs;
+      if (std::memcmp(block_tables + static_cast<size_t>(b) * mb, tl, static_cast<size_t>(need) * 4) != 0) break;
+      f = b;
+    }
+    if (end - f < kPrefillMinRows) break;
+    runs.insert(runs.begin(), f);
+    end = f;
+  }
+  return runs;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------------------ the handle
@@ -1120,6 +1144,25 @@ ns_status ns_check_step_metadata(int num_blocks, int block_size, int max_blocks_
                     positions, block_tables, seq_lens, slot_mapping);
 }
 
+ns_status ns_find_prompt_chunks(int block_size, int max_blocks_per_seq, int batch,
+                                const int32_t* positions, const int32_t* block_tables,
+                                const int32_t* seq_lens, int32_t* starts, int capacity, int* n) {
+  if (n == nullptr || (batch > 0 && (!positions || !block_tables || !seq_lens)) ||
+      (capacity > 0 && starts == nullptr))
+    return fail(NS_ERR_INVALID_ARG, "null argument");
+  if (block_size < 1 || max_blocks_per_seq < 1 || batch < 0 || capacity < 0)
+    return fail(NS_ERR_INVALID_ARG, "block_size, max_blocks_per_seq >= 1; batch, capacity >= 0");
+  const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > cap || positions[b] < 0)
+      return fail(NS_ERR_INVALID_ARG, "seq_len outside [1, max_blocks_per_seq * block_size] or a negative position");
+  const std::vector<int> runs =
+      prompt_chunk_starts(batch, positions, block_tables, seq_lens, max_blocks_per_seq, block_size);
+  *n = static_cast<int>(runs.size());
+  for (int i = 0; i < std::min(*n, capacity); ++i) starts[i] = runs[static_cast<size_t>(i)];
+  return NS_OK;
+}
+
 ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_cta_budget) {
   if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
   if (n_split < 1 || n_split > 4) return fail(NS_ERR_INVALID_ARG, "n_split must be 1..4");
@@ -1156,28 +1199,8 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // one packed metadata buffer, one host-to-device copy
   if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
-  // Prefill chunks: working back from the last row, each maximal run of at least kPrefillMinRows
-  // rows at consecutive positions that read the same blocks as the run's last row is one chunk,
-  // whose attention runs as one causal kernel; the first shorter run ends the search (the rows
-  // before it are decode rows).
-  std::vector<int> runs;
-  {
-    int end = batch;
-    while (end > 0) {
-      const int32_t* tl = block_tables + static_cast<size_t>(end - 1) * mb;
-      int f = end - 1;
-      while (f > 0) {
-        const int b = f - 1;
-        if (positions[b] != positions[f] - 1) break;
-        const int need = (seq_lens[b] + bs - 1) / bs;
-        if (std::memcmp(block_tables + static_cast<size_t>(b) * mb, tl, static_cast<size_t>(need) * 4) != 0) break;
-        f = b;
-      }
-      if (end - f < kPrefillMinRows) break;
-      runs.insert(runs.begin(), f);
-      end = f;
-    }
-  }
+  // prefill chunks, each attended by one causal kernel (the rows before them are decode rows)
+  std::vector<int> runs = prompt_chunk_starts(batch, positions, block_tables, seq_lens, mb, bs);
   bool graphed = c.use_graphs && !h->timing;
   if (graphed && !h->graph_chunks && !runs.empty()) graphed = false;  // layouts vary: eager
   // graph batch: the smallest bucket that holds the rows; padding rows fill the rest, and a
