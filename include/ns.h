@@ -198,7 +198,8 @@ typedef struct ns_sched_st* ns_sched;
 ns_status ns_sched_create(ns_pool pool, int dense_tokens, int max_blocks_per_seq, int eos_token,
                           int predicted_new_tokens, ns_sched* out);
 void ns_sched_destroy(ns_sched s);
-/* prompt: host, prompt_len >= 1 token ids (copied); prompt_len + max_new_tokens at most
+/* prompt: host, prompt_len >= 1 non-negative token ids (copied; negative ids are reserved for
+ * rows that read a device-sampled token); prompt_len + max_new_tokens at most
  * max_blocks_per_seq * block_size, and its blocks at most the pool's; ids are unique and
  * non-negative. */
 ns_status ns_sched_add(ns_sched s, int request_id, const int32_t* prompt, int prompt_len,

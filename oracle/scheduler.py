@@ -128,6 +128,8 @@ class DenseBatchFormer:
             raise SchedulerError("request id in use or negative")
         if not prompt or max_new < 1:
             raise SchedulerError("empty prompt or max_new_tokens < 1")
+        if min(prompt) < 0:
+            raise SchedulerError("negative prompt token id")
         if len(prompt) + max_new > self.mb * self.pool.block_size:
             raise SchedulerError("prompt + max_new_tokens beyond the block table")
         if self._blocks(len(prompt) + max_new - 1) > self.pool.num_blocks:

@@ -357,7 +357,7 @@ def test_library_former_matches_the_model_bit_for_bit(L, case):
 def test_library_former_errors(L):
     pool = L.BlockPool(2, 4, 4)
     f = L.BatchFormer(pool, 8, 4, 0)
-    for args in ((0, [], 1), (0, [1], 0), (0, [1] * 16, 1), (-1, [1], 1)):
+    for args in ((0, [], 1), (0, [1], 0), (0, [1] * 16, 1), (-1, [1], 1), (0, [4, -1], 1)):
         with pytest.raises(L.NSError) as e:
             f.add(*args)
         assert e.value.status == 1
@@ -597,3 +597,14 @@ def test_library_former_matches_the_model_in_both_formation_modes(L, case):
             else:
                 assert ea[1] == eb[1]
         assert all(lib_form.tokens(i) == model.m.tokens(i) for i in range(n_req))
+
+
+def test_model_refuses_negative_prompt_ids():
+    """A negative id in a formed row names a token sampled on the device in the previous step,
+    so a prompt may not contain one; the request is refused and nothing changes."""
+    m = DenseBatchFormer(BlockAllocator(4, 4), 4, 4, 0)
+    with pytest.raises(SchedulerError):
+        m.add(0, [3, -2], 1)
+    assert m.counts() == (0, 0, 0, 0)
+    m.add(0, [3, 0], 1)
+    assert m.counts() == (1, 0, 0, 0)

@@ -129,6 +129,9 @@ ns_status ns_sched_add(ns_sched s, int request_id, const int32_t* prompt, int pr
   if (s == nullptr || (prompt_len > 0 && prompt == nullptr)) return err(NS_ERR_INVALID_ARG, "null argument");
   if (request_id < 0 || s->req.count(request_id)) return err(NS_ERR_INVALID_ARG, "request id in use or negative");
   if (prompt_len < 1 || max_new_tokens < 1) return err(NS_ERR_INVALID_ARG, "empty prompt or max_new_tokens < 1");
+  // negative ids are how a formed row names a device-sampled token: never a prompt's
+  for (int i = 0; i < prompt_len; ++i)
+    if (prompt[i] < 0) return err(NS_ERR_INVALID_ARG, "negative prompt token id");
   if (static_cast<long long>(prompt_len) + max_new_tokens > static_cast<long long>(s->mb) * s->bs)
     return err(NS_ERR_INVALID_ARG, "prompt + max_new_tokens beyond the block table");
   if (s->blocks(static_cast<long long>(prompt_len) + max_new_tokens - 1) > s->nb)
