@@ -369,7 +369,9 @@ class DecodeStep:
     def set_token_source(self, device_ids=None) -> None:
         """Read token ids from a device int32 buffer (e.g. the previous argmax) or, with None,
         from the host arrays passed to ``step``."""
-        check(lib().ns_set_token_source(self.h, _dev(device_ids, "device_ids", "int32")))
+        # any row may name any entry (token id -(r + 1)), so the buffer holds max_batch ids
+        check(lib().ns_set_token_source(self.h, _dev(device_ids, "device_ids", "int32",
+                                                     self.max_batch)))
 
     def pool(self) -> int:
         """The handle's block pool (borrowed), for ``BatchFormer``."""
