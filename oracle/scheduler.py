@@ -17,10 +17,12 @@ reading (the page gives none):
   request's own block table); if the block pool cannot hold them all the chunk is cut to what
   fits, and the fill stops at the first prompt that gets nothing.
 * A row samples a token (``row_samples`` = 1) when it is a decode row or the last token of a
-  prompt.  After the step the caller commits the sampled tokens: a request whose prompt has just
-  completed starts running (at the end of the running order); a request finishes when it
-  samples ``eos_token`` or reaches ``max_new_tokens`` generated tokens, and its blocks return
-  to the pool in table order.
+  prompt.  A prompt whose last row is formed joins the end of the running order at once (its
+  first decode row comes in the next step).  After the step the caller commits the sampled
+  tokens: a request finishes when it samples ``eos_token`` or reaches ``max_new_tokens``
+  generated tokens, and its blocks return to the pool in table order.
+* Prompt token ids are non-negative: a negative id in a formed row names a token sampled on the
+  device (asynchronous formation, below).
 * Blocks are reserved from the pool as positions cross block boundaries, decode rows first
   (in row order), then the chunks (in row order).
 * Predicted peak memory (same passage: requests that outgrow their predicted peak are moved
@@ -28,7 +30,8 @@ reading (the page gives none):
   of its first prompt_len + min(max_new, predicted_new) - 1 positions (predicted_new = 0:
   max_new).  A prompt starts (gets its first row) only when the free blocks cover its predicted
   peak plus what the admitted requests (started prompts and running requests) still need to
-  reach theirs; started prompts always continue.
+  reach theirs and what the preempted requests need to resume (the blocks of their cached tokens
+  and next position); started prompts always continue.
 * When the first ``dense_tokens`` running requests need more new blocks than are free, the
   running request that started last is preempted (repeatedly): the caller saves its cached
   tokens (positions 0 .. prompt_len + generated - 2) from its blocks, the blocks return to the
