@@ -260,3 +260,58 @@ def test_prompt_chunk_detection_by_hand_and_against_the_rule(L):
     with pytest.raises(_lib.NSError):
         _lib.find_prompt_chunks(bs, [127], A[None], [129])
     assert _lib.find_prompt_chunks(bs, [], np.zeros((0, mb), np.int32), []) == []
+
+
+def test_block_pool_equals_the_model_on_arbitrary_call_sequences(L):
+    """Property test: any sequence of reserve / release (valid, repeated, foreign or out of
+    range ids) / prepare_step calls gives the library pool and the allocator model the same
+    outcome (result or refusal) and the same free list after every call."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    nb, bs, mb = 12, 4, 6
+    op = st.one_of(
+        st.tuples(st.just("reserve"), st.integers(0, 5)),
+        st.tuples(st.just("release"), st.lists(st.integers(-1, nb), max_size=4)),
+        st.tuples(st.just("release_held"), st.integers(0, 30)),
+        st.tuples(st.just("prepare"), st.lists(st.integers(0, mb * bs), min_size=1, max_size=3)),
+    )
+
+    @hyp.settings(max_examples=150, deadline=None)
+    @hyp.given(st.lists(op, max_size=40))
+    def run(ops):
+        pool, model = _lib.BlockPool(nb, bs, mb), BlockAllocator(nb, bs)
+        held = []
+        for kind, arg in ops:
+            if kind == "release_held":
+                arg = [held[arg % len(held)]] if held else []
+                kind = "release"
+            if kind == "reserve":
+                calls = (lambda: pool.reserve(arg).tolist(), lambda: model.alloc(arg))
+            elif kind == "release":
+                calls = (lambda: pool.release(np.array(arg, np.int32)), lambda: model.release(arg))
+            else:
+                t_lib = np.zeros((len(arg), mb), np.int32)
+                t_mod = np.zeros((len(arg), mb), np.int32)
+                pos = np.array(arg, np.int32)
+                calls = (lambda: pool.prepare_step(pos, t_lib).tolist(),
+                         lambda: model.prepare_step(t_mod, pos).tolist())
+            outcome = []
+            for fn, errs in zip(calls, (_lib.NSError, AllocatorError)):
+                try:
+                    outcome.append(("ok", fn()))
+                except errs:
+                    outcome.append(("refused", None))
+            assert outcome[0] == outcome[1], (kind, arg)
+            if outcome[0][0] == "ok":
+                if kind == "reserve":
+                    held += outcome[0][1]
+                elif kind == "release":
+                    for i in arg:
+                        held.remove(i)
+                else:  # rows starting a block took one
+                    held += [int(t_mod[r, p // bs]) for r, p in enumerate(arg) if p % bs == 0]
+            assert pool.free_count() == model.free_count() == nb - len(held)
+        rest = pool.reserve(pool.free_count()).tolist()
+        assert rest == list(model.free)
+
+    run()
