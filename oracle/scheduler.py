@@ -243,6 +243,8 @@ class DenseBatchFormer:
         returns the ids that finished, in row order."""
         if not self.pending:
             raise SchedulerError("no step to commit")
+        if len(sampled) != len(self.pending[0][1].token_ids):
+            raise SchedulerError("batch differs from the formed step")
         step, st = self.pending.popleft()
         finished = []
         for b in range(len(st.token_ids)):

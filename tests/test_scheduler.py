@@ -608,3 +608,69 @@ def test_model_refuses_negative_prompt_ids():
     assert m.counts() == (0, 0, 0, 0)
     m.add(0, [3, 0], 1)
     assert m.counts() == (1, 0, 0, 0)
+
+
+def test_library_former_equals_the_model_on_arbitrary_call_sequences(L):
+    """Property test: any interleaving of add (valid or not), next, commit (right or wrong row
+    count), remove and set_async gives the library and the model the same outcome -- the same
+    rows, moves, finished ids and tokens, or a refusal on both sides -- with every peak
+    reserved and with optimistic peaks."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    nb, bs, mb, D, eos = 10, 4, 6, 6, 7
+    op = st.one_of(
+        st.tuples(st.just("add"), st.integers(-1, 5), st.integers(0, 14), st.integers(0, 6)),
+        st.tuples(st.just("next"), st.just(0), st.just(0), st.just(0)),
+        st.tuples(st.just("commit"), st.integers(0, 2), st.integers(0, 9), st.just(0)),
+        st.tuples(st.just("remove"), st.integers(-1, 5), st.just(0), st.just(0)),
+        st.tuples(st.just("async"), st.integers(0, 1), st.just(0), st.just(0)),
+    )
+
+    @hyp.settings(max_examples=200, deadline=None)
+    @hyp.given(st.lists(op, max_size=60), st.sampled_from([0, 2]))
+    def run(ops, pred):
+        lib_f = L.BatchFormer(L.BlockPool(nb, bs, mb), D, mb, eos, pred)
+        mod = _ModelAdapter(DenseBatchFormer(BlockAllocator(nb, bs), D, mb, eos, pred))
+        formed = []  # row counts of the formed, uncommitted steps (oldest first)
+        for kind, a, b, c in ops:
+            if kind == "add":
+                calls = [lambda f: f.add(a, list(range(3, 3 + b)), c)] * 2
+            elif kind == "next":
+                calls = [lambda f: {k: v.tolist() for k, v in f.next().items()},
+                         lambda f: {k: v.tolist() for k, v in f.next().items()}]
+            elif kind == "commit":
+                n = (formed[0] if formed else 0) + (a - 1 if a != 1 else 0)  # 1: the right count
+                sampled = np.array([(b + 3 * r) % 10 for r in range(max(n, 0))], np.int32)
+                calls = [lambda f: f.commit(sampled)] * 2
+            elif kind == "remove":
+                calls = [lambda f: f.remove(a), lambda f: f.m.remove(a)]
+            else:
+                calls = [lambda f: f.set_async(bool(a)), lambda f: f.m.set_async(bool(a))]
+            out = []
+            for fn, f in zip(calls, (lib_f, mod)):
+                try:
+                    r = fn(f)
+                    out.append(("ok", r))
+                except (L.NSError, RuntimeError, SchedulerError):
+                    out.append(("refused", None))
+            if out[0][0] == "ok" and kind == "next":
+                assert out[0][1].keys() == {k: 0 for k in out[1][1]}.keys()
+                for k in out[0][1]:
+                    assert out[0][1][k] == out[1][1][k], k
+                assert [(m[0], m[1], m[2], list(m[3])) for m in lib_f.moves()] == \
+                       [(m[0], m[1], m[2], list(m[3])) for m in mod.moves()]
+                formed.append(len(out[0][1]["token_ids"]))
+            else:
+                assert out[0] == out[1], (kind, a, b, c, out)
+            if out[0][0] == "ok" and kind == "commit":
+                formed.pop(0)
+            assert lib_f.counts() == mod.counts()
+        for rid in range(6):
+            try:
+                t_lib = lib_f.tokens(rid)
+            except L.NSError:
+                t_lib = None
+            t_mod = mod.m.tokens(rid) if rid in mod.m.req else None
+            assert t_lib == t_mod
+
+    run()
