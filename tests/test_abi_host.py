@@ -276,7 +276,7 @@ def test_block_pool_equals_the_model_on_arbitrary_call_sequences(L):
         st.tuples(st.just("prepare"), st.lists(st.integers(0, mb * bs), min_size=1, max_size=3)),
     )
 
-    @hyp.settings(max_examples=150, deadline=None)
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True, database=None)
     @hyp.given(st.lists(op, max_size=40))
     def run(ops):
         pool, model = _lib.BlockPool(nb, bs, mb), BlockAllocator(nb, bs)
@@ -315,3 +315,47 @@ def test_block_pool_equals_the_model_on_arbitrary_call_sequences(L):
         assert rest == list(model.free)
 
     run()
+
+
+def test_step_metadata_validation_equals_the_stated_rules(L):
+    """Property test: on arbitrary (mostly invalid) metadata the library's host validation
+    accepts exactly what the documented rules accept: 1 <= batch <= max_batch, token ids in
+    [0, V), positions >= 0, seq_len = position + 1 <= max_blocks_per_seq * block_size, the
+    table entries under a row's tokens inside the pool, slot = table[p / bs] * bs + p % bs."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    nb, bs, mb, vocab, max_batch = 6, 4, 3, 20, 4
+
+    def rules(tok, pos, tab, sl, slot):
+        if not 1 <= len(pos) <= max_batch:
+            return 1
+        for b in range(len(pos)):
+            p, n = int(pos[b]), int(sl[b])
+            if not 0 <= tok[b] < vocab or p < 0 or n != p + 1 or n > mb * bs:
+                return 1
+            if any(not 0 <= tab[b][j] < nb for j in range(-(-n // bs))):
+                return 1
+            if slot[b] != int(tab[b][p // bs]) * bs + p % bs:
+                return 1
+        return 0
+
+    off = st.sampled_from([0, 0, 0, -1, 1])
+    row = st.tuples(st.integers(-2, vocab + 1), st.integers(-2, mb * bs + 1), off,
+                    st.lists(st.integers(-1, nb), min_size=mb, max_size=mb), off)
+    seen = {0: 0, 1: 0}
+
+    @hyp.settings(max_examples=400, deadline=None, derandomize=True, database=None)
+    @hyp.given(st.lists(row, min_size=0, max_size=max_batch + 1))
+    def run(rows):
+        tok = np.array([r[0] for r in rows], np.int32)
+        pos = np.array([r[1] for r in rows], np.int32)
+        sl = np.array([r[1] + 1 + r[2] for r in rows], np.int32)       # right or off by one
+        tab = np.array([r[3] for r in rows], np.int32).reshape(len(rows), mb)
+        slot = np.array([int(r[3][min(max(r[1], 0) // bs, mb - 1)]) * bs + max(r[1], 0) % bs + r[4]
+                         for r in rows], np.int64)                    # right or off by one
+        got = _lib.check_step_metadata(nb, bs, mb, vocab, max_batch, tok, pos, tab, sl, slot)
+        assert got == rules(tok, pos, tab, sl, slot)
+        seen[got] += 1
+
+    run()
+    assert seen[0] >= 20 and seen[1] >= 20, seen  # both outcomes well exercised
