@@ -411,8 +411,12 @@ ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v
  * batch * n_kv_heads counters -- return
  * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the
  * buffer's device address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls on a device share the buffer and each call leaves
- * its contents behind: calls whose kernels overlap on the GPU race; order them on one stream. */
+ * call before any stream capture.  The address is kept per device together with the id of the
+ * context it belongs to; after a device reset (a new primary context, the library image loaded
+ * again) the next call looks it up again, so it too should come before any capture.  All calls
+ * on a device share the buffer and each call leaves its contents behind (the counters are
+ * cleared on the call's stream before its kernel): calls whose kernels overlap on the GPU
+ * race; order them on one stream. */
 ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, const int32_t* seq_lens, void* out,
                                  int batch, int n_q_heads, int n_kv_heads, int head_dim,
@@ -481,6 +485,26 @@ typedef struct {
 } ns_kernel_timing;
 ns_status ns_set_kernel_timing(ns_handle h, int on);
 ns_status ns_get_kernel_timing(ns_handle h, ns_kernel_timing* out);
+
+/* Per-tensor view inside the step, for parity checks layer by layer (the nanoserve notes'
+ * change table fuses RMSNorm, RoPE and grouped-query attention inside each layer, so the
+ * layer's intermediate tensors are where a fused kernel's error would first show).  While a
+ * trace is set, ns_decode_step launches eagerly (graphs are bypassed) and, for layer `layer`,
+ * copies on the step's streams right after the kernel that produces each tensor:
+ *   q          [batch][n_q_heads * head_dim] storage dtype: q after the projection and RoPE;
+ *   attn       [batch][n_q_heads * head_dim] storage dtype: the attention output o;
+ *   resid_mid  [batch][hidden] fp32: the residual after the attention block, x + o Wo^T;
+ *   resid_out  [batch][hidden] fp32: the residual after the layer (after the FFN).
+ * (k and v are the cache slots the step writes: read them from ns_kv_layer_ptrs.)  Every
+ * pointer is a caller-owned device buffer of at least that size, or NULL to skip that tensor.
+ * layer < 0 or bufs == NULL turns the trace off; layer >= n_layers returns INVALID_ARG. */
+typedef struct {
+  void* q;
+  void* attn;
+  float* resid_mid;
+  float* resid_out;
+} ns_trace_bufs;
+ns_status ns_set_trace(ns_handle h, int layer, const ns_trace_bufs* bufs);
 
 /* Human-readable name of a status; thread-local text of the last failure. */
 const char* ns_status_str(ns_status s);

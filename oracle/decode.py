@@ -222,6 +222,11 @@ def decode_step(model: OracleModel, k_pools: List[np.ndarray], v_pools: List[np.
       x += o Wo^T; n = RMSNorm(x; ffn_norm); x += (silu(n Wg^T) * (n Wu^T)) Wd^T.
     Then logits = RMSNorm(x; final_norm) W_lm^T.  All rows' k/v are written before any row
     attends, so rows sharing a block table (a prefill chunk) see each other causally.
+
+    ``trace``, when given, receives per layer (lists indexed by layer, fp64, before any
+    storage rounding): "q" and "k" after RoPE [B, heads, d], "v", "attn" (o) [B, Hq, d],
+    "resid_attn" (x after the attention block) and "resid" (x after the layer) [B, H].
+    ``n_layers`` runs only the first layers before the final norm and head.
     """
     sh = model.shape
     dt = sh.dtype
@@ -246,6 +251,7 @@ def decode_step(model: OracleModel, k_pools: List[np.ndarray], v_pools: List[np.
         v_pools[l][blk, :, off, :] = round_storage(v, dt)
         o = paged_attention(q, k_pools[l], v_pools[l], block_tables, seq_lens, scale, dtype=dt)
         x = x + o.reshape(B, hq * d) @ w["wo"].T
+        x_attn = x
         n2 = rms_norm(x, w["ffn_norm"], sh.rms_eps)
         a = swiglu(n2 @ w["w_gate"].T, n2 @ w["w_up"].T)
         x = x + a @ w["w_down"].T
@@ -254,6 +260,7 @@ def decode_step(model: OracleModel, k_pools: List[np.ndarray], v_pools: List[np.
             trace.setdefault("k", []).append(k)
             trace.setdefault("v", []).append(v)
             trace.setdefault("attn", []).append(o)
+            trace.setdefault("resid_attn", []).append(x_attn.copy())
             trace.setdefault("resid", []).append(x.copy())
     nf = rms_norm(x, model.final_norm, sh.rms_eps)
     return nf @ model.lm_head.T

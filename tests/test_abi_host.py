@@ -185,6 +185,91 @@ def test_binding_refuses_host_memory_where_kernels_read_device_memory(L):
     assert _lib._dev(0x7F0000000000, "x") == 0x7F0000000000 and _lib._dev(None, "x") is None
 
 
+class _FakeCuda:
+    """Stands in for a CUDA tensor on a machine without a GPU.  The binding reads only these
+    attributes before it calls the library; every call below has one bad argument and must be
+    refused before the library is reached, so the address is never dereferenced."""
+    is_cuda = True
+
+    def __init__(self, n, dtype):
+        import torch
+        self.n, self.dtype = n, dtype
+        self._size = torch.empty(0, dtype=dtype).element_size()
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return self._size
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return 0x7F0000001000
+
+
+def test_binding_refuses_short_or_mistyped_attention_buffers(L):
+    """Each device buffer of the attention calls (ns_attn_decode, ns_attn_decode_noalloc) is
+    checked against what the kernel reads or writes: q and out [batch][Hq][d], the pools
+    [num_blocks][Hkv][bs][d] of 16-bit elements, block_tables int32 [batch][mb], seq_lens int32
+    [batch], dev_err int32 [1].  A short or mistyped one is refused with INVALID_ARG."""
+    import torch
+    B, hq, hkv, d, bs, mb, nb = 3, 8, 2, 64, 16, 5, 20
+    good = dict(q=(B * hq * d, torch.bfloat16), k_pool=(nb * hkv * bs * d, torch.bfloat16),
+                v_pool=(nb * hkv * bs * d, torch.int16), block_tables=(B * mb, torch.int32),
+                seq_lens=(B, torch.int32), out=(B * hq * d, torch.float16))
+    bad = {"q": [(B * hq * d - 1, torch.bfloat16), (B * hq * d, torch.float32)],
+           "k_pool": [(nb * hkv * bs * d - 1, torch.bfloat16), (nb * hkv * bs * d, torch.int32)],
+           "v_pool": [(nb * hkv * bs * d - 8, torch.bfloat16), (nb * hkv * bs * d, torch.uint8)],
+           "block_tables": [(B * mb - 1, torch.int32), (B * mb, torch.int64)],
+           "seq_lens": [(B, torch.int64)],
+           "out": [(B * hq * d - 1, torch.bfloat16), (B * hq * d, torch.float32)]}
+
+    def args(**over):
+        a = {k: _FakeCuda(*v) for k, v in good.items()}
+        a.update({k: _FakeCuda(*v) for k, v in over.items()})
+        if isinstance(a["seq_lens"], _FakeCuda):
+            a["seq_lens"].shape = (B,)
+        return a
+
+    refused = 0
+    for name, variants in bad.items():
+        for v in variants:
+            for noalloc in (False, True):
+                a = args(**{name: v})
+                fn = _lib.attn_decode_noalloc if noalloc else _lib.attn_decode
+                with pytest.raises(_lib.NSError) as e:
+                    fn(a["q"], a["k_pool"], a["v_pool"], a["block_tables"], a["seq_lens"],
+                       a["out"], hq, hkv, d, bs, mb, nb, 0.125, "bf16")
+                assert e.value.status == 1 and name in str(e.value), (name, v, str(e.value))
+                refused += 1
+    for err in ((0, torch.int32), (1, torch.int64)):
+        a = args()
+        with pytest.raises(_lib.NSError) as e:
+            _lib.attn_decode_noalloc(a["q"], a["k_pool"], a["v_pool"], a["block_tables"],
+                                     a["seq_lens"], a["out"], hq, hkv, d, bs, mb, nb, 0.125,
+                                     "bf16", dev_err=_FakeCuda(*err))
+        assert e.value.status == 1 and "dev_err" in str(e.value)
+        refused += 1
+    assert refused == 2 * 11 + 2
+
+
+def test_binding_refuses_short_or_mistyped_linear_buffers(L):
+    """ns_linear reads w [n][k] and x [m][k] (16-bit) and writes y [m][n] fp32."""
+    import torch
+    m, n, k = 4, 128, 64
+    good = dict(w=(n * k, torch.bfloat16), x=(m * k, torch.bfloat16), y=(m * n, torch.float32))
+    for name, v in (("w", (n * k - 1, torch.bfloat16)), ("w", (n * k, torch.float32)),
+                    ("x", (m * k - 1, torch.bfloat16)), ("y", (m * n - 1, torch.float32)),
+                    ("y", (m * n, torch.bfloat16))):
+        a = {kk: _FakeCuda(*vv) for kk, vv in good.items()}
+        a[name] = _FakeCuda(*v)
+        with pytest.raises(_lib.NSError) as e:
+            _lib.linear(a["w"], a["x"], a["y"], m, n, k, "bf16")
+        assert e.value.status == 1 and name in str(e.value)
+
+
 def test_binding_refuses_metadata_of_unequal_row_counts(L):
     db, kw = _meta()
     assert _chk(kw, db, seq_lens=db.seq_lens[:2]) == 1

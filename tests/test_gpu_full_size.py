@@ -217,3 +217,104 @@ def test_llama3_8b_32_layers_batch_256(cuda_lib):
     # logits by ~2-3 % (tests/test_tolerance_model.py), so the bound here is 5e-2 / 0.2
     _check_logits(got, ref, "llama3-8b b256", rel_tol=5e-2, abs_tol=0.2)
     dev.close()
+
+
+def _download_pool(ptr, nbytes, dtype):
+    """A whole device pool in the oracle's storage format (float16 values or bf16 bits)."""
+    from transformer_decode_step_ns_gb300 import _lib
+    out = np.empty(nbytes // 2, dtype=np.uint16)
+    _lib.memcpy(out.ctypes.data, ptr, nbytes)
+    return out.view(np.float16) if dtype == "f16" else out
+
+
+@pytest.mark.parametrize("depth", [1, 2, 4])
+def test_llama3_8b_shapes_at_truncated_depth_per_tensor(cuda_lib, depth):
+    """The LLaMA-3-8B shapes at the continuous run's full batch (256 rows, contexts uniform in
+    [512, 4096], block size 16, a 319-block table width, shuffled pool), truncated to `depth`
+    of its 32 layers, in the launch configurations the benchmark times (graph replay, unsplit
+    and as 128 + 128 nano-batches: bitwise equal).  Against the oracle on every row:
+      * logits, all 128,256 columns: relative L2 <= 1e-2; max abs <= 5e-2 scaled by the logits'
+        std over 0.6 (the bound is stated for logits of std ~0.6; this head's are ~1.3);
+      * every K/V slot the step writes, per layer: relative L2 <= 1e-2;
+      * per layer, q after RoPE, the attention output and the residuals after the attention
+        block and after the layer (ns_set_trace, eager launches): relative L2 <= 1e-2."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    seed = synth.config_seed(4)
+    sh = synth.llama3_8b_shape(depth)
+    B, bs, mb = 256, 16, 319
+    ctx = synth.ctx_uniform(seed, "cfg4.join.ctx", B, 512, 4096).astype(np.int64)
+    need = [math.ceil((int(c) + 1) / bs) for c in ctx]
+    nb = sum(need) + 8
+    w = synth.model_weights_device(sh, seed)
+    dev = _lib.DecodeStep(sh, w, B, mb, use_graphs=True)
+    dev.kv_alloc(nb, bs)
+    stream = torch.cuda.current_stream().cuda_stream
+    pool_bytes = dev.kv_pool_bytes()
+    for l in range(depth):
+        k, v = dev.kv_layer_ptrs(l)
+        synth.fill_normal_device(k, pool_bytes // 2, seed, f"cfg4.k{l}", "bf16", stream=stream)
+        synth.fill_normal_device(v, pool_bytes // 2, seed, f"cfg4.v{l}", "bf16", stream=stream)
+    ids = dev.reserve(nb)
+    dev.release(ids[synth.permutation(seed, "cfg4.pool", nb)])
+    tab = np.zeros((B, mb), dtype=np.int32)
+    for b in range(B):
+        tab[b, :math.ceil(int(ctx[b]) / bs)] = dev.reserve(math.ceil(int(ctx[b]) / bs))
+    pos = ctx.astype(np.int32)
+    slots = dev.prepare_step(pos, tab)
+    tok = synth.uniform_int(seed, "cfg4.tokens", B, 0, sh.vocab - 1).astype(np.int32)
+    meta = (tok, pos, tab, (pos + 1).astype(np.int32), slots)
+    torch.cuda.synchronize()
+    shp = (nb, sh.n_kv_heads, bs, sh.head_dim)
+    kp = [_download_pool(dev.kv_layer_ptrs(l)[0], pool_bytes, "bf16").reshape(shp) for l in range(depth)]
+    vp = [_download_pool(dev.kv_layer_ptrs(l)[1], pool_bytes, "bf16").reshape(shp) for l in range(depth)]
+    # the oracle on every row; the embedding rows it gathers are passed as a table of B rows
+    emb = _host(w["embed"])[tok.astype(np.int64)]
+    model = oracle.OracleModel(
+        shape=sh, embed=oracle.from_storage(emb, "bf16"),
+        final_norm=oracle.from_storage(_host(w["final_norm"]), "bf16"),
+        lm_head=oracle.from_storage(_host(w["lm_head"]), "bf16"),
+        layers=_LazyLayers(w["layers"], "bf16"))
+    tr = {}
+    ref = oracle.decode_step(model, kp, vp, np.arange(B, dtype=np.int32), pos, tab, meta[3],
+                             slots, bs, trace=tr)
+    logits = torch.empty((B, sh.vocab), dtype=torch.float32, device="cuda")
+    outs = []
+    for split in (None, [128, 128]):
+        dev.set_nanobatch(split)
+        dev.step(*meta, logits)
+        torch.cuda.synchronize()
+        assert dev.device_error() == 0
+        outs.append(logits.cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    got = outs[0].astype(np.float64)
+    abs_tol = 5e-2 * max(1.0, float(ref.std()) / 0.6)
+    _check_logits(got, ref, f"llama3-8b shapes, {depth} layers, logits", abs_tol=abs_tol)
+    blk, off = slots // bs, slots % bs
+    qd = sh.n_q_heads * sh.head_dim
+    q_t = torch.empty((B, qd), dtype=torch.bfloat16, device="cuda")
+    o_t = torch.empty_like(q_t)
+    rm = torch.empty((B, sh.hidden), dtype=torch.float32, device="cuda")
+    ro = torch.empty_like(rm)
+    dev.set_nanobatch(None)
+    for l in range(depth):
+        k_ptr, v_ptr = dev.kv_layer_ptrs(l)
+        kk = _download_pool(k_ptr, pool_bytes, "bf16").reshape(shp)
+        vv = _download_pool(v_ptr, pool_bytes, "bf16").reshape(shp)
+        for name, pool, want in (("k", kk, tr["k"][l]), ("v", vv, tr["v"][l])):
+            e = rel_l2(oracle.from_storage(pool[blk, :, off, :], "bf16"), want)
+            assert e < 1e-2, (depth, l, name, e)
+        dev.set_trace(l, q=q_t, attn=o_t, resid_mid=rm, resid_out=ro)
+        dev.step(*meta, logits)
+        torch.cuda.synchronize()
+        dev.set_trace(-1)
+        assert dev.device_error() == 0
+        np.testing.assert_array_equal(logits.cpu().numpy(), outs[0])  # eager = graph, bitwise
+        got_t = {"q": oracle.from_storage(_host(q_t), "bf16").reshape(B, sh.n_q_heads, -1),
+                 "attn": oracle.from_storage(_host(o_t), "bf16").reshape(B, sh.n_q_heads, -1),
+                 "resid_attn": rm.cpu().numpy().astype(np.float64),
+                 "resid": ro.cpu().numpy().astype(np.float64)}
+        for name, g in got_t.items():
+            e = rel_l2(g, tr[name][l])
+            assert e < 1e-2, (depth, l, name, e)
+    dev.close()

@@ -115,7 +115,7 @@ def test_attention_bounds_checks_record_errors_and_skip_the_access(cuda_lib):
 def test_attention_rejects_unsupported_shapes(cuda_lib):
     import torch
     from transformer_decode_step_ns_gb300 import _lib
-    x = torch.zeros(16, dtype=torch.int16, device="cuda")
+    x = torch.zeros(16384, dtype=torch.int16, device="cuda")  # as large as either call reads
     t = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(_lib.NSError) as e:
         _lib.attn_decode(x, x, x, t, t, x, 12, 4, 96, 16, 1, 1, 0.1, "bf16")  # d = 96

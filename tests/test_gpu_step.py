@@ -421,3 +421,83 @@ def test_decode_step_rejects_bad_metadata_before_launch(cuda_lib):
     h.dev.set_nanobatch([1, 2])
     with pytest.raises(_lib.NSError):
         h.dev.step(b.token_ids, b.positions, b.block_tables, b.seq_lens, b.slot_mapping, logits)
+
+
+def _trace_layer(h: Harness, layer: int):
+    """The GPU's q, attention output, residual after the attention block and after the layer
+    for ``layer`` (ns_set_trace), as fp64 host arrays, plus the step's logits."""
+    import torch
+    sh, B = h.shape, h.batch.batch
+    qd = sh.n_q_heads * sh.head_dim
+    R = h.dev.max_batch
+    q = torch.zeros((R, qd), dtype=torch.int16, device="cuda")
+    o = torch.zeros((R, qd), dtype=torch.int16, device="cuda")
+    rm = torch.zeros((R, sh.hidden), dtype=torch.float32, device="cuda")
+    ro = torch.zeros((R, sh.hidden), dtype=torch.float32, device="cuda")
+    h.dev.set_trace(layer, q=q, attn=o, resid_mid=rm, resid_out=ro)
+    logits = h.run_gpu()
+    h.dev.set_trace(-1)
+    dt = sh.dtype
+    return {"q": storage_f64(from_dev(q)[:B], dt).reshape(B, sh.n_q_heads, sh.head_dim),
+            "attn": storage_f64(from_dev(o)[:B], dt).reshape(B, sh.n_q_heads, sh.head_dim),
+            "resid_attn": rm[:B].cpu().numpy().astype(np.float64),
+            "resid": ro[:B].cpu().numpy().astype(np.float64)}, logits
+
+
+def _check_layers(h: Harness, split=None):
+    """Every layer's tensors against the oracle's trace, each within relative L2 1e-2 (the
+    stated per-tensor tolerance): q after RoPE, the k and v written to the cache, the attention
+    output, the residual after the attention block and after the layer; then the logits."""
+    b = h.batch
+    model = oracle.OracleModel.from_weights(h.shape, h.w)
+    kp = [a.copy() for a in h.kp]
+    vp = [a.copy() for a in h.vp]
+    tr = {}
+    ref = oracle.decode_step(model, kp, vp, b.token_ids, b.positions, b.block_tables, b.seq_lens,
+                             b.slot_mapping, h.bs, trace=tr)
+    h.dev.set_nanobatch(split)
+    dt = h.shape.dtype
+    blk = b.slot_mapping // h.bs
+    off = b.slot_mapping % h.bs
+    errs = {}
+    for l in range(h.shape.n_layers):
+        got, logits = _trace_layer(h, l)
+        for name in ("q", "attn", "resid_attn", "resid"):
+            e = rel_l2(got[name], tr[name][l])
+            errs[(l, name)] = e
+            assert e < 1e-2, (l, name, e)
+        ks, vs = h.download_pools()
+        for name, pool, want in (("k", ks[l], tr["k"][l]), ("v", vs[l], tr["v"][l])):
+            e = rel_l2(storage_f64(pool[blk, :, off, :], dt), want)
+            errs[(l, name)] = e
+            assert e < 1e-2, (l, name, e)
+        assert rel_l2(logits, ref) < 1e-2 and np.abs(logits - ref).max() < 5e-2
+    return errs
+
+
+@pytest.mark.parametrize("dtype,tie", [("bf16", True), ("f16", False)])
+def test_every_layer_tensor_matches_the_oracle(cuda_lib, dtype, tie):
+    """Per-tensor parity inside the step, layer by layer (an error in one layer that a later
+    layer damps would pass a logits-only check): a 4-layer model over ragged contexts that span
+    block and superchunk boundaries."""
+    shape = _tiny(dtype, tie, n_layers=4)
+    h = Harness(shape, 61, [0, 5, 16, 300, 1100, 64])
+    _check_layers(h)
+
+
+def test_traced_tensors_of_nano_batches_equal_the_whole_batch_bitwise(cuda_lib):
+    """The trace copies each nano-batch's rows on its own stream: the traced tensors of a split
+    step equal the unsplit ones bit for bit, and both match the oracle per tensor."""
+    shape = _tiny("bf16", n_layers=2)
+    h = Harness(shape, 62, [3, 40, 200, 17, 1, 600])
+    _check_layers(h, split=[2, 4])
+    for l in range(2):
+        h.dev.set_nanobatch(None)
+        whole, lw = _trace_layer(h, l)
+        h.dev.set_nanobatch([2, 4])
+        part, lp = _trace_layer(h, l)
+        np.testing.assert_array_equal(lw, lp)
+        for k in whole:
+            np.testing.assert_array_equal(whole[k], part[k])
+    with pytest.raises(Exception):
+        h.dev.set_trace(2, q=None)  # past the last layer

@@ -39,6 +39,7 @@ SYMBOLS = (
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
     "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async", "ns_find_prompt_chunks",
+    "ns_set_trace",
 )
 
 
@@ -72,6 +73,11 @@ KERNEL_KINDS = ("embed_rope", "qkv", "attention", "o_proj", "gate_up", "down", "
 
 class KernelTiming(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int * 8), ("total_ms", ctypes.c_double * 8)]
+
+
+class TraceBufs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("attn", ctypes.c_void_p), ("resid_mid", ctypes.c_void_p),
+                ("resid_out", ctypes.c_void_p)]
 
 
 class StepInfo(ctypes.Structure):
@@ -122,6 +128,7 @@ def lib() -> ctypes.CDLL:
             "ns_find_prompt_chunks": ([I, I, I, P, P, P, P, I, ctypes.POINTER(I)], I),
             "ns_last_error_message": ([], ctypes.c_char_p),
             "ns_set_kernel_timing": ([P, I], I),
+            "ns_set_trace": ([P, I, ctypes.POINTER(TraceBufs)], I),
             "ns_set_token_source": ([P, P], I),
             "ns_set_graph_buckets": ([P, I, P], I),
             "ns_set_kv_offload": ([P, P, ctypes.c_size_t], I),
@@ -183,18 +190,22 @@ def memcpy(dst: int, src: int, nbytes: int) -> None:
         raise RuntimeError(f"cudaMemcpy failed ({r})")
 
 
-def _dev(a, what: str, dtype: Optional[str] = None, min_numel: int = 0) -> Optional[int]:
+def _dev(a, what: str, dtype: Optional[str] = None, min_numel: int = 0,
+         itemsize: Optional[int] = None) -> Optional[int]:
     """Address of an argument the library hands to its kernels: a contiguous CUDA tensor (of
-    torch dtype ``dtype`` and at least ``min_numel`` elements, where given) or a raw device
-    address (an int, the caller's responsibility).  Host memory or a short buffer would be
-    dereferenced on the device, so it is refused here, before anything is launched, with the
-    library's own INVALID_ARG status."""
+    torch dtype ``dtype``, or of ``itemsize``-byte elements, and at least ``min_numel``
+    elements, where given) or a raw device address (an int, the caller's responsibility).  Host
+    memory, a buffer of the wrong element type or a short buffer would be dereferenced on the
+    device, so it is refused here, before anything is launched, with the library's own
+    INVALID_ARG status."""
     if a is None or isinstance(a, int):
         return a
     if isinstance(a, np.ndarray) or not getattr(a, "is_cuda", False):
         raise NSError(1, f"{what} must be device memory (a CUDA tensor or a device address)")
     if dtype is not None and str(a.dtype) != "torch." + dtype:
         raise NSError(1, f"{what} must be {dtype}, not {a.dtype}")
+    if itemsize is not None and a.element_size() != itemsize:
+        raise NSError(1, f"{what} must have {itemsize}-byte elements, not {a.element_size()}")
     if a.numel() < min_numel:
         raise NSError(1, f"{what} has {a.numel()} elements, needs at least {min_numel}")
     return _ptr(a)
@@ -409,6 +420,20 @@ class DecodeStep:
         """Gather the K/V of positions first_pos.. of ``block_table`` into host rows."""
         self._kv_transfer(lib().ns_kv_save, host_dst, n_tokens, first_pos, block_table, stream)
 
+    def set_trace(self, layer: int, q=None, attn=None, resid_mid=None, resid_out=None) -> None:
+        """Copy layer ``layer``'s q (after RoPE), attention output, residual after the attention
+        block and residual after the layer into these device buffers during the next eager
+        steps (graphs are bypassed); ``layer`` < 0 turns the trace off."""
+        if layer < 0:
+            check(lib().ns_set_trace(self.h, -1, None))
+            return
+        B, s = self.max_batch, self.shape
+        qd = s.n_q_heads * s.head_dim
+        tb = TraceBufs(_dev(q, "q", None, B * qd, 2), _dev(attn, "attn", None, B * qd, 2),
+                       _dev(resid_mid, "resid_mid", "float32", B * s.hidden),
+                       _dev(resid_out, "resid_out", "float32", B * s.hidden))
+        check(lib().ns_set_trace(self.h, layer, ctypes.byref(tb)))
+
     def set_kernel_timing(self, on: bool) -> None:
         check(lib().ns_set_kernel_timing(self.h, 1 if on else 0))
 
@@ -438,15 +463,29 @@ class DecodeStep:
         return s
 
 
+def _attn_args(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads, n_kv_heads,
+               head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype):
+    """The C arguments shared by the attention calls, each device buffer checked against the
+    sizes the kernel reads or writes: q and out [batch][n_q_heads][head_dim] and the pools
+    [num_blocks][n_kv_heads][block_size][head_dim] of 16-bit elements, block_tables int32
+    [batch][max_blocks_per_seq], seq_lens int32 [batch]."""
+    batch = int(seq_lens.shape[0])
+    rows = batch * n_q_heads * head_dim
+    pool = num_blocks * n_kv_heads * block_size * head_dim
+    return (_dev(q, "q", None, rows, 2), _dev(k_pool, "k_pool", None, pool, 2),
+            _dev(v_pool, "v_pool", None, pool, 2),
+            _dev(block_tables, "block_tables", "int32", batch * max_blocks_per_seq),
+            _dev(seq_lens, "seq_lens", "int32", batch), _dev(out, "out", None, rows, 2),
+            batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+            float(scale), DTYPES[dtype])
+
+
 def attn_decode(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads: int,
                 n_kv_heads: int, head_dim: int, block_size: int, max_blocks_per_seq: int,
                 num_blocks: int, scale: float, dtype: str, stream=None, cta_budget: int = 0) -> None:
     """Paged decode attention; ``cta_budget`` > 0 caps its CTAs (ns_attn_decode_capped)."""
-    batch = int(seq_lens.shape[0])
-    args = (_dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-            _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"), _dev(out, "out"),
-            batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
-            float(scale), DTYPES[dtype])
+    args = _attn_args(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads, n_kv_heads,
+                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype)
     if cta_budget:
         check(lib().ns_attn_decode_capped(*args, cta_budget, _stream(stream)))
     else:
@@ -458,17 +497,16 @@ def attn_decode_noalloc(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_head
                         max_blocks_per_seq: int, num_blocks: int, scale: float, dtype: str,
                         dev_err=None, stream=None) -> None:
     """The allocation-free attention call (fixed in-library scratch; see include/ns.h)."""
-    batch = int(seq_lens.shape[0])
-    check(lib().ns_attn_decode_noalloc(_dev(q, "q"), _dev(k_pool, "k_pool"),
-                                       _dev(v_pool, "v_pool"), _dev(block_tables, "block_tables"),
-                                       _dev(seq_lens, "seq_lens"), _dev(out, "out"), batch,
-                                       n_q_heads, n_kv_heads, head_dim, block_size,
-                                       max_blocks_per_seq, num_blocks, float(scale), DTYPES[dtype],
-                                       _dev(dev_err, "dev_err"), _stream(stream)))
+    args = _attn_args(q, k_pool, v_pool, block_tables, seq_lens, out, n_q_heads, n_kv_heads,
+                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype)
+    check(lib().ns_attn_decode_noalloc(*args, _dev(dev_err, "dev_err", "int32", 1),
+                                       _stream(stream)))
 
 
 def linear(w, x, y, m: int, n: int, k: int, dtype: str, stream=None) -> None:
-    check(lib().ns_linear(_dev(w, "w"), _dev(x, "x"), _dev(y, "y"), m, n, k, DTYPES[dtype],
+    """y[m][n] (fp32) = x[m][k] . w[n][k]^T on the projection kernel (16-bit w and x)."""
+    check(lib().ns_linear(_dev(w, "w", None, n * k, 2), _dev(x, "x", None, m * k, 2),
+                          _dev(y, "y", "float32", m * n), m, n, k, DTYPES[dtype],
                           _stream(stream)))
 
 

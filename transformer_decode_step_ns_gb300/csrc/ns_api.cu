@@ -408,6 +408,9 @@ struct ns_ctx {
   int kernels_last = 0;
   // per-kernel timing (eager only)
   bool timing = false;
+  // per-tensor trace of one layer (ns_set_trace; eager steps only)
+  int trace_layer = -1;
+  ns_trace_bufs trace{};
   struct TimedLaunch {
     int kind;
     cudaEvent_t a, b;
@@ -560,6 +563,16 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   const int G = Hq / Hkv;
   const float scale_log2 = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)) * 1.4426950408889634);
 
+  // rows [row0, row0 + rows) of a [R][row_bytes] activation buffer to a trace buffer
+  auto trace_copy = [&](int l, void* dst, const void* src, size_t row_bytes, int row0, int rows,
+                        cudaStream_t s) -> cudaError_t {
+    if (l != h->trace_layer || dst == nullptr) return cudaSuccess;
+    const size_t off = static_cast<size_t>(row0) * row_bytes;
+    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, static_cast<const uint8_t*>(src) + off,
+                           static_cast<size_t>(rows) * row_bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  const size_t q_row_bytes = static_cast<size_t>(qd) * 2, r_row_bytes = static_cast<size_t>(H) * 4;
+
   EpiArgs norm{};  // common fused-RMSNorm inputs
   norm.sumsq_in = h->sumsq;
   norm.sumsq_tiles = H / kGemmTileN;
@@ -614,6 +627,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
                           : nullptr;
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
                          st[i % 2], K_QKV));
+      NS_CUDA(trace_copy(l, h->trace.q, h->q, q_row_bytes, nb[i].first, nb[i].second, st[i % 2]));
       if (n > 1 || mirror) NS_CUDA(cudaEventRecord(ev_qkv(l, i), st[i % 2]));
       if (mirror) {
         // the rows' K/V leave for the host while attention and the FFN of this layer run
@@ -689,6 +703,8 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
         h->kernels_last++;
       }
 
+      NS_CUDA(trace_copy(l, h->trace.attn, h->o, q_row_bytes, r_lo, r_hi - r_lo, s));
+
       EpiArgs eo{};
       eo.resid = h->resid;
       eo.xn_out = h->xn;
@@ -697,6 +713,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       eo.sumsq_ld = h->R;
       eo.resid_dim = H;
       NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O));
+      NS_CUDA(trace_copy(l, h->trace.resid_mid, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
 
       EpiArgs eg = norm;
       eg.act_out = h->act;
@@ -711,6 +728,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ed.sumsq_ld = h->R;
       ed.resid_dim = H;
       NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN));
+      NS_CUDA(trace_copy(l, h->trace.resid_out, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
     }
   }
   for (int i = 0; i < n && h->with_lm; ++i) {
@@ -1201,7 +1219,7 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   if (h->meta_pending) NS_CUDA(cudaEventSynchronize(h->meta_done));
   // prefill chunks, each attended by one causal kernel (the rows before them are decode rows)
   std::vector<int> runs = prompt_chunk_starts(batch, positions, block_tables, seq_lens, mb, bs);
-  bool graphed = c.use_graphs && !h->timing;
+  bool graphed = c.use_graphs && !h->timing && h->trace_layer < 0;
   if (graphed && !h->graph_chunks && !runs.empty()) graphed = false;  // layouts vary: eager
   // graph batch: the smallest bucket that holds the rows; padding rows fill the rest, and a
   // padded step has no chunk layout (its chunk rows, if any, use the decode kernel)
@@ -1426,6 +1444,19 @@ ns_status ns_kv_save(ns_handle h, void* host_dst, int n_tokens, int first_pos, c
   NS_TRY(kv_transfer_setup(h, n_tokens, first_pos, block_table, n_table, bytes, s));
   NS_CUDA(launch_kv_copy(kv_copy_params(h, n_tokens, 0), h->sms, s));
   NS_CUDA(cudaMemcpyAsync(host_dst, h->kv_xfer, bytes, cudaMemcpyDeviceToHost, s));
+  return NS_OK;
+}
+
+ns_status ns_set_trace(ns_handle h, int layer, const ns_trace_bufs* bufs) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (layer >= h->cfg.n_layers) return fail(NS_ERR_INVALID_ARG, "trace layer past the last layer");
+  if (layer < 0 || bufs == nullptr) {
+    h->trace_layer = -1;
+    h->trace = ns_trace_bufs{};
+    return NS_OK;
+  }
+  h->trace_layer = layer;
+  h->trace = *bufs;
   return NS_OK;
 }
 

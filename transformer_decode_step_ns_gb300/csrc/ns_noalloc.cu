@@ -12,6 +12,8 @@
 // the attention kernel.  Its size is fixed at build time (kNoAllocScratchBytes); requests that
 // would need more are rejected.  Every call on a device shares the one buffer: two calls whose
 // kernels overlap in time on that GPU (different streams, no ordering between them) race on it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -31,9 +33,40 @@ constexpr size_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocCounters 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch per device (the symbol's host-side name is only a
-// stand-in; it must be translated once per device with that device current).
+// stand-in; it must be translated with that device current).  The address belongs to the
+// context the module was loaded into, so each entry also records that context's unique id:
+// after a device reset (or any teardown of the primary context) the module is loaded again,
+// perhaps elsewhere, the id changes, and the next call looks the address up again.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;
+  unsigned char* addr = nullptr;
+};
 std::mutex g_mu;
-unsigned char* g_addr[64] = {};
+ScratchSlot g_slot[64];
+
+// Unique id (cuCtxGetId) of the context current on this thread, or 0 when there is none or
+// the driver entry points are unavailable (then the address is looked up on every call).
+unsigned long long current_ctx_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (get_cur == nullptr || get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 ns_status scratch_address(unsigned char** out) {
   int dev = 0;
@@ -42,7 +75,9 @@ ns_status scratch_address(unsigned char** out) {
     return NS_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_addr[dev] == nullptr) {
+  ScratchSlot& slot = g_slot[dev];
+  const unsigned long long id = current_ctx_id();
+  if (slot.addr == nullptr || id == 0 || id != slot.ctx_id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -50,9 +85,10 @@ ns_status scratch_address(unsigned char** out) {
                           cudaGetErrorString(e)).c_str());
       return NS_ERR_CUDA;
     }
-    g_addr[dev] = static_cast<unsigned char*>(p);
+    slot.addr = static_cast<unsigned char*>(p);
+    slot.ctx_id = current_ctx_id();  // the lookup makes the primary context current if it was not
   }
-  *out = g_addr[dev];
+  *out = slot.addr;
   return NS_OK;
 }
 
