@@ -1,31 +1,47 @@
 #!/usr/bin/env python
 """Decode-step benchmark on GB300.
 
-Workload (one JSON line on rank 0): the 24-layer Qwen2.5-0.5B-shaped decoder (hidden 896,
-14 Q / 2 KV heads, head_dim 64, SwiGLU 4864, vocab 151936, tied head, fp16, seeded N(0, 0.02)
-weights), continuous-batching decode at batch 32 (``--batch``), per-request contexts uniform in
-[128, 1024], block size 16, physical blocks shuffled, the step captured as one CUDA graph and
-replayed.  A "step" is one full decode iteration for every row: packed metadata upload, all
-24 layers, the LM head to fp32 logits.
+Headline workload (one JSON line on rank 0): continuous-batching decode of a 32-layer
+LLaMA-3-8B-shaped decoder (hidden 4096, 32 Q / 8 KV heads, head_dim 128, SwiGLU 14336, vocab
+128256, untied head, bf16, seeded N(0, 0.02) weights) at a constant batch of 256 requests:
+contexts uniform in [512, 4096], decode lengths uniform in [100, 1000], finished requests leave
+and new ones join their rows, block size 16 over a shuffled pool, the step captured as a CUDA
+graph and replayed, greedy argmax fed back on the device.  A "step" is one full decode
+iteration for every row: packed metadata upload, all 32 layers, the LM head to fp32 logits, the
+greedy argmax.
 
 Reported:
-  value      output tokens/s over K device-timed steps (CUDA events on the stream; metadata
-             for each step prepared before the timed region, positions advancing every step).
-  e2e        the same through the public API as a greedy decode loop: every step uploads its
-             host metadata, runs, takes the argmax on the GPU and reads the token ids back to
-             the host, which feed the next step.
-  roofline   the dominant kernel (largest share of step time, measured with CUDA-event pairs
-             around each launch in eager steps) against the measured HBM copy bandwidth.
+  value      output tokens/s over K device-timed steps (CUDA events on the stream; the
+             metadata of every step, joins and leaves included, prepared before the region).
+  e2e        the continuous run (--continuous-steps, 2000 by default) through the public API,
+             host wall clock: every step the host slot mapper and bookkeeping, one metadata
+             upload, graph replay, argmax into the next step's token source, ids to the host.
+  roofline   the dominant kernel (paged decode attention: ~2/3 of the step) against the
+             measured HBM copy bandwidth, from CUDA-event pairs around each launch of eager
+             steps.
   step_roofline  the whole step against max(FLOPs / tensor peak, bytes / HBM bandwidth).
-  attention  the paged decode-attention kernel alone on its own workload (batch 256, 32 Q / 8
-             KV heads, head_dim 128, bf16, contexts log-uniform in [512, 8192], 160k-block pool):
-             algorithmic K/V bytes per launch / launch time.
-  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload.
+  cpu_baseline   the fp64 CPU oracle on a bounded sample of the same workload, on all host
+             cores and on one (inputs drawn on the host, in a child process).
+Extra objects: the 24-layer Qwen2.5-0.5B shape (batch 32 and batches 1, 8), the 2-layer Qwen
+shape at batch 1 with L2 flushed, paged attention alone (batch 256 and an L2-flushed batch
+sweep), the 70B-shaped layer's nano-batch tuning, the batch-former serving run and the KV
+offload.
 
-``--impl reference`` times the CPU oracle alone (the reference arm).  Under torchrun each rank
-runs an independent replica (no data-path collective; the step does not shard).
+``--impl reference`` times the CPU oracle alone (the reference arm) on the same workload.
+Under torchrun each rank runs an independent replica (no data-path collective; the step does
+not shard).
 """
 from __future__ import annotations
+
+import os as _os
+import sys as _sys
+
+if "--oracle-leg" in _sys.argv or ("--impl" in _sys.argv and "reference" in _sys.argv):
+    # the oracle's BLAS thread count is fixed when numpy loads: all host cores unless the
+    # caller chose (the oracle legs set it for their child processes)
+    _n = str(len(_os.sched_getaffinity(0)))
+    for _k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        _os.environ.setdefault(_k, _n)
 
 import argparse
 import json
@@ -45,7 +61,9 @@ import synth  # noqa: E402
 from transformer_decode_step_ns_gb300 import roofline as rl  # noqa: E402
 
 METRIC = "decode output tokens/s at 1 GB300 (+ % of step roofline); paged-attn HBM GB/s"
-WORKLOAD = "qwen2.5-0.5b-shape 24L fp16 decode, batch 32, ctx U[128,1024], bs16, graph replay"
+WORKLOAD = ("llama-3-8b-shape 32L bf16 continuous-batching decode, batch 256, ctx U[512,4096], "
+            "decode U[100,1000] with leave/join, bs16, graph replay, greedy argmax fed back")
+WORKLOAD_QWEN = "qwen2.5-0.5b-shape 24L fp16 decode, batch 32, ctx U[128,1024], bs16, graph replay"
 SEED = synth.config_seed(1)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -268,6 +286,122 @@ def blas_threads():
     except Exception:
         pass
     return os.cpu_count() or 1
+
+
+def cfg4_first_step_host():
+    """The continuous run's first step, built on the host alone with the allocator model: the
+    same tokens, positions, block tables (the run's shuffled free list, blocks handed out row by
+    row) and slots as ContinuousWorkload builds through the library's pool."""
+    import oracle
+    cw = ContinuousWorkload
+    seed = synth.config_seed(4)
+    sh = synth.llama3_8b_shape(32)
+    B, bs = cw.B, cw.bs
+    mb = cfg4_table_width(bs)
+    nb = B * mb
+    ctx = synth.ctx_uniform(seed, "cfg4.join.ctx", B, cw.ctx_lo, cw.ctx_hi)
+    alloc = oracle.BlockAllocator(nb, bs)
+    ids = np.array(alloc.alloc(nb))
+    alloc.release(ids[synth.permutation(seed, "cfg4.pool", nb)])
+    tab = np.zeros((B, mb), dtype=np.int32)
+    for b in range(B):
+        n = int(math.ceil(int(ctx[b]) / bs))
+        tab[b, :n] = alloc.alloc(n)
+    pos = ctx.astype(np.int32)
+    slots = alloc.prepare_step(tab, pos)
+    tok = synth.uniform_int(seed, "cfg4.tokens", B, 0, sh.vocab - 1).astype(np.int32)
+    return tok, pos, tab, pos + 1, slots
+
+
+class Cfg4OracleSample:
+    """Inputs of the oracle on the continuous LLaMA-3-8B workload, drawn on the host from the
+    seeded streams the GPU run uses (no GPU, no library): the first step of the batch of 256
+    (contexts, tokens, block tables handed out by the allocator model from the run's shuffled
+    free list) and, for the rows a sample takes, their cached K/V blocks.  The host draws layer
+    0's weights (218 M values) and the LM head (525 M); every layer of the oracle's model reuses
+    layer 0's weights and cache contents (drawing all 7 B weights on the host takes minutes), so
+    each sampled step does the arithmetic of the full 32-layer step plus the head."""
+
+    def __init__(self, workers):
+        import oracle
+        self.oracle = oracle
+        self.sh = sh = synth.llama3_8b_shape(32)
+        self.seed = seed = synth.config_seed(4)
+        self.tok, self.pos, self.tab, self.seq, self.slots = cfg4_first_step_host()
+        self.bs = bs = ContinuousWorkload.bs
+        h, f, qd, kvd = sh.hidden, sh.ffn, sh.q_dim, sh.kv_dim
+        shapes = {"wq": (qd, h), "wk": (kvd, h), "wv": (kvd, h), "wo": (h, qd),
+                  "w_gate": (f, h), "w_up": (f, h), "w_down": (h, f)}
+        t0 = time.perf_counter()
+        layer = {k: synth.normal_threads(seed, f"layer0.{k}", shp, "bf16", 0.02, threads=workers)
+                 for k, shp in shapes.items()}
+        head = synth.normal_threads(seed, "lm_head", (sh.vocab, h), "bf16", 0.02, threads=workers)
+        self.draw_s = time.perf_counter() - t0
+        wid = lambda a: oracle.from_storage(a, "bf16")  # noqa: E731
+        ones = wid(synth.to_storage(np.ones(h), "bf16"))
+        l0 = {k: wid(v) for k, v in layer.items()}
+        l0["attn_norm"], l0["ffn_norm"] = ones, ones
+        self.layers = [l0] * sh.n_layers
+        self.head = wid(head)
+        self.final_norm = ones
+        self.blk_elems = sh.n_kv_heads * bs * sh.head_dim
+
+    def inputs(self, rows):
+        """(model, k pools, v pools, token ids, positions, tables, seq_lens, slots) of `rows`,
+        their blocks renumbered into a compact pool; the embedding rows of their tokens."""
+        sh, bs, seed = self.sh, self.bs, self.seed
+        rows = np.asarray(rows)
+        used, index = [], {}
+        ctab = np.zeros((len(rows), self.tab.shape[1]), dtype=np.int32)
+        for i, r in enumerate(rows):
+            for j in range(int(math.ceil(int(self.seq[r]) / bs))):
+                b = int(self.tab[r, j])
+                if b not in index:
+                    index[b] = len(used)
+                    used.append(b)
+                ctab[i, j] = index[b]
+        shp = (len(used), sh.n_kv_heads, bs, sh.head_dim)
+        kp = np.stack([synth.normal_threads(seed, "cfg4.k0", (self.blk_elems,), "bf16",
+                                            offset=b * self.blk_elems) for b in used]).reshape(shp)
+        vp = np.stack([synth.normal_threads(seed, "cfg4.v0", (self.blk_elems,), "bf16",
+                                            offset=b * self.blk_elems) for b in used]).reshape(shp)
+        emb = np.stack([synth.normal(seed, "embed", (sh.hidden,), "bf16", std=0.02,
+                                     offset=int(self.tok[r]) * sh.hidden) for r in rows])
+        model = self.oracle.OracleModel(shape=sh, embed=self.oracle.from_storage(emb, "bf16"),
+                                        final_norm=self.final_norm, lm_head=self.head,
+                                        layers=self.layers)
+        cslots = np.array([index[int(s) // bs] * bs + int(s) % bs for s in self.slots[rows]],
+                          dtype=np.int64)
+        # the same compact pool serves every layer (layer 0's contents)
+        return (model, [kp] * sh.n_layers, [vp] * sh.n_layers, np.arange(len(rows), dtype=np.int32),
+                self.pos[rows], ctab, self.seq[rows], cslots)
+
+    def time_step(self, rows):
+        """Seconds of one oracle decode step over `rows` (inputs built outside the timing)."""
+        args = self.inputs(rows)
+        t0 = time.perf_counter()
+        self.oracle.decode_step(*args, self.bs)
+        return time.perf_counter() - t0
+
+    def describe(self, rows_per_step, steps):
+        return (f"{steps} decode steps of {rows_per_step} of the 256 requests (rows taken in turn), "
+                f"each a full 32-layer step + LM head in fp64 numpy; the 32 layers reuse layer 0's "
+                f"seeded weights and cache contents (drawn on the host in {self.draw_s:.0f} s)")
+
+
+def oracle_leg(args):
+    """The oracle on bounded samples of the headline workload, timed on the host cores this
+    process's BLAS was given; prints one JSON object."""
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", len(os.sched_getaffinity(0))))
+    smp = Cfg4OracleSample(workers=len(os.sched_getaffinity(0)))
+    R = max(1, args.ref_rows)
+    secs, n = 0.0, 0
+    while n < 1 or (secs < args.oracle_seconds and n < 200):
+        rows = (np.arange(R) + n * R) % ContinuousWorkload.B
+        secs += smp.time_step(rows)
+        n += 1
+    print(json.dumps({"value": R * n / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                      "seconds": secs, "steps": n, "sample": smp.describe(R, n)}), flush=True)
 
 
 # ---------------------------------------------------------------------------------- attention
@@ -558,8 +692,8 @@ class ContinuousWorkload:
     Every request starts with a context uniform in [512, 4096] (its K/V preloaded N(0, 1)) and
     decodes a length uniform in [100, 1000]; when it finishes it leaves (its blocks return to
     the pool) and a new request joins in its row.  Each step: join/leave bookkeeping and the
-    host slot mapper, one ns_decode_step (graph replay), greedy argmax on the GPU and the ids
-    read back to the host as the next tokens."""
+    host slot mapper, one ns_decode_step (graph replay), greedy argmax on the GPU whose ids are
+    the next step's tokens."""
 
     B, bs, ctx_lo, ctx_hi, dec_lo, dec_hi = 256, 16, 512, 4096, 100, 1000
 
@@ -569,7 +703,7 @@ class ContinuousWorkload:
         self.seed = seed = synth.config_seed(4)
         self.shape = sh = synth.llama3_8b_shape(32)
         B, bs = self.B, self.bs
-        self.mb = mb = int(math.ceil((self.ctx_hi + self.dec_hi + 1) / bs))
+        self.mb = mb = cfg4_table_width()
         self.num_blocks = B * mb
         t0 = time.time()
         self.w = synth.model_weights_device(sh, seed)
@@ -597,6 +731,9 @@ class ContinuousWorkload:
             self.join(b)
         self.tokens = synth.uniform_int(seed, "cfg4.tokens", B, 0, sh.vocab - 1).astype(np.int32)
         self.logits = torch.empty((B, sh.vocab), dtype=torch.float32, device="cuda")
+        # greedy ids of the last step: the next step's tokens (device token source)
+        self.ids_dev = torch.from_numpy(self.tokens.copy()).cuda()
+        self.nano = None
         self.setup_s = time.time() - t0
 
     def join(self, b):
@@ -612,51 +749,193 @@ class ContinuousWorkload:
         n = int(math.ceil(self.pos[b] / self.bs))
         self.dev.release(self.tables[b, :n].copy())
 
-    def run(self, steps, peaks, nano=None):
-        import torch
+    def next_meta(self):
+        """This step's metadata (the slot mapper takes a block where a row crosses into one)."""
+        slots = self.dev.prepare_step(self.pos, self.tables)
+        return (self.pos.copy(), self.tables.copy(), (self.pos + 1).astype(np.int32), slots)
+
+    def advance(self) -> int:
+        """After a step: every row moves one position on; finished requests leave and new ones
+        join their rows.  Returns the number of leave/join pairs."""
+        self.pos += 1
+        self.left -= 1
+        done = np.nonzero(self.left == 0)[0]
+        for b in done:
+            self.leave(int(b))
+            self.join(int(b))
+        return len(done)
+
+    def plan(self, n):
+        """Metadata of the next n steps, prepared ahead (the host bookkeeping does not depend on
+        the sampled tokens: requests leave at their drawn lengths)."""
+        metas, leaves = [], 0
+        for _ in range(n):
+            metas.append(self.next_meta())
+            leaves += self.advance()
+        return metas, leaves
+
+    def launch(self, meta):
+        """One step through the public API, tokens read on the device from the previous step's
+        greedy ids, and this step's greedy ids written back for the next."""
         from transformer_decode_step_ns_gb300 import _lib
+        self.dev.step(None, *meta, self.logits)
+        _lib.greedy_argmax(self.logits, self.ids_dev)
+
+    def set_nano(self, nano):
+        self.nano = nano
         self.dev.set_nanobatch(nano)
-        ids_dev = torch.empty(self.B, dtype=torch.int32, device="cuda")
-        ids_host = torch.empty(self.B, dtype=torch.int32).pin_memory()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        t_roof = 0.0
+        self.dev.set_token_source(self.ids_dev)
+
+    def roofline_time(self, metas, peaks):
         tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
         hbm = float(peaks["hbm_gbs"]) * 1e9
-        leaves = 0
+        t, nbytes, flops = 0.0, 0.0, 0.0
+        for m in metas:
+            work = rl.decode_step_work(self.shape, m[2])
+            t += rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm)
+            nbytes += work.total_bytes
+            flops += work.flops
+        return t, nbytes, flops
+
+    def headline(self, K, W, peaks, world):
+        """W warm-up steps, then exactly K steps timed with CUDA events on the stream (bracketed
+        by a barrier and synchronisation), metadata of every step prepared before the region,
+        nvidia-smi sampling the clocks during it.  An event at the midpoint reads the K steps
+        as two back-to-back runs."""
+        import torch
+        metas, leaves = self.plan(W + K)
+        for m in metas[:W]:
+            self.launch(m)
+        torch.cuda.synchronize()
+        timed = metas[W:]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler()
+        clocks.start()
+        # keep the GPU busy (untimed repeats of the last warm-up step) until sampling is live
+        t_wait = time.time()
+        while not clocks.has_samples() and time.time() - t_wait < 5.0:
+            for _ in range(5):
+                self.launch(metas[W - 1])
+            torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_mid = torch.cuda.Event(enable_timing=True)
+        half = K // 2
+        clocks.mark_start()
+        e0.record()
+        for i, m in enumerate(timed):
+            if i == half:
+                e_mid.record()
+            self.launch(m)
+        e1.record()
+        torch.cuda.synchronize()
+        clocks.mark_stop()
+        ms_total = e0.elapsed_time(e1)
+        repeat = (repeat_check(e0.elapsed_time(e_mid), half, e_mid.elapsed_time(e1), K - half)
+                  if half >= 1 else None)
+        t_roof, nbytes, flops = self.roofline_time(timed, peaks)
+        return {"ms_total": ms_total, "repeat": repeat, "clocks": clocks.stop(),
+                "roofline_s": t_roof, "bytes": nbytes, "flops": flops,
+                "leaves_and_joins": leaves, "meta_bytes": cfg4_meta_bytes(self.B, self.mb)}
+
+    def run_async(self, steps, peaks):
+        """The end-to-end loop through the public API, as a server runs it: every step packs and
+        uploads its host metadata (one pinned copy), replays the graph, takes the greedy argmax
+        into the device token source of the next step and copies the ids to pinned host memory;
+        the host reads them one step late (the end-of-sequence check of asynchronous batch
+        formation) while the next step runs.  Host wall clock over the whole run."""
+        import torch
+        host_ids = [torch.empty(self.B, dtype=torch.int32).pin_memory() for _ in range(2)]
+        evs = [torch.cuda.Event() for _ in range(2)]
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+        t_roof, leaves = 0.0, 0
+        tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
+        hbm = float(peaks["hbm_gbs"]) * 1e9
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(steps):
-            slots = self.dev.prepare_step(self.pos, self.tables)
-            seq = self.pos + 1
-            work = rl.decode_step_work(self.shape, seq)
+        for k in range(steps):
+            m = self.next_meta()
+            work = rl.decode_step_work(self.shape, m[2])
             t_roof += rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm)
-            ev[i][0].record()
-            self.dev.step(self.tokens, self.pos, self.tables, seq, slots, self.logits)
-            ev[i][1].record()
-            _lib.greedy_argmax(self.logits, ids_dev)
-            ids_host.copy_(ids_dev, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-            self.tokens = ids_host.numpy().copy()
-            self.pos += 1
-            self.left -= 1
-            for b in np.nonzero(self.left == 0)[0]:
-                self.leave(int(b))
-                self.join(int(b))
-                leaves += 1
+            dev_ev[k][0].record()
+            self.launch(m)
+            dev_ev[k][1].record()
+            host_ids[k % 2].copy_(self.ids_dev, non_blocking=True)
+            evs[k % 2].record()
+            if k > 0:
+                evs[(k - 1) % 2].synchronize()
+                self.tokens = host_ids[(k - 1) % 2].numpy().copy()
+            leaves += self.advance()
+        evs[(steps - 1) % 2].synchronize()
         wall = time.perf_counter() - t0
-        dev_ms = np.array([a.elapsed_time(b) for a, b in ev])
-        return {"steps": steps, "nano_split": nano or [self.B], "leaves_and_joins": leaves,
+        self.tokens = host_ids[(steps - 1) % 2].numpy().copy()
+        dev_ms = np.array([a.elapsed_time(b) for a, b in dev_ev])
+        return {"steps": steps, "nano_split": self.nano or [self.B], "leaves_and_joins": leaves,
+                "wall_s": wall, "tokens_per_s": self.B * steps / wall,
                 "device_ms_per_step_mean": float(dev_ms.mean()),
                 "device_ms_per_step_median": float(np.median(dev_ms)),
-                "tokens_per_s_device": self.B * steps / (dev_ms.sum() * 1e-3),
-                "tokens_per_s_e2e": self.B * steps / wall,
                 "roofline_ms_per_step_mean": t_roof / steps * 1e3,
-                "frac_of_roofline": t_roof / (dev_ms.sum() * 1e-3),
+                "frac_of_roofline_device": t_roof / (dev_ms.sum() * 1e-3),
                 "graphs_cached": self.dev.info().graphs_cached,
                 "device_error": self.dev.device_error()}
 
-    def offload(self, steps, peaks, nano):
+    def run(self, steps, peaks, nano=None):
+        """Steps one at a time, each waited for (the split trial and the eager kernel timing)."""
+        import torch
+        self.set_nano(nano)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        metas = []
+        for i in range(steps):
+            m = self.next_meta()
+            metas.append(m)
+            ev[i][0].record()
+            self.launch(m)
+            ev[i][1].record()
+            torch.cuda.current_stream().synchronize()
+            self.advance()
+        dev_ms = np.array([a.elapsed_time(b) for a, b in ev])
+        t_roof, _, _ = self.roofline_time(metas, peaks)
+        return {"steps": steps, "device_ms_per_step_median": float(np.median(dev_ms)),
+                "frac_of_roofline": t_roof / (dev_ms.sum() * 1e-3),
+                "attention_bytes": sum(rl.attention_bytes(m[2], self.shape.n_kv_heads,
+                                                          self.shape.head_dim)
+                                       + 4.0 * self.B * self.shape.q_dim for m in metas)
+                * self.shape.n_layers}
+
+    def pick_split(self, peaks):
+        """A short comparison of the unsplit step and two nano-batches of 128; the faster is
+        used for the rest of the run."""
+        trial = {}
+        for nano in (None, [128, 128]):
+            trial[str(nano or [self.B])] = self.run(20, peaks, nano)["device_ms_per_step_median"]
+        best = None if trial[str([self.B])] <= trial[str([128, 128])] else [128, 128]
+        self.set_nano(best)
+        return best, trial
+
+    def kernel_times(self, peaks):
+        """Per-kind kernel times of eager steps (an event pair around each launch, on the stream
+        the kernel runs on) and the attention kernel's achieved bandwidth: the algorithmic K/V
+        (+ q in, o out) bytes of the timed steps over the attention launches' summed time."""
+        self.dev.set_kernel_timing(True)
+        self.run(2, peaks, self.nano)
+        self.dev.kernel_timing()
+        r = self.run(3, peaks, self.nano)
+        kt = self.dev.kernel_timing()
+        self.dev.set_kernel_timing(False)
+        self.set_nano(self.nano)
+        total = sum(v[1] for v in kt.values())
+        n_attn, ms_attn = kt["attention"]
+        return {"kernel_us": {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]},
+                "launches_per_step": {k: v[0] // 3 for k, v in kt.items() if v[0]},
+                "shares": {k: round(v[1] / total, 4) for k, v in kt.items()},
+                "attention_launches": n_attn, "attention_ms": ms_attn,
+                "attention_bytes_per_launch": r["attention_bytes"] / n_attn,
+                "attention_share": ms_attn / total}
+
+    def offload(self, steps, peaks):
         """KV offload: steps with every step's new K/V mirrored to pinned host memory (each
         layer's rows copied while its attention and FFN run) against the same steps without;
         then the longest request saved to the host and reloaded into its blocks (contiguous
@@ -666,9 +945,9 @@ class ContinuousWorkload:
         row = 2 * sh.n_kv_heads * sh.head_dim
         mirror = torch.empty((sh.n_layers, self.B, row), dtype=torch.int16).pin_memory()
         self.dev.set_kv_offload(mirror)
-        on = self.run(steps, peaks, nano)
+        on = self.run(steps, peaks, self.nano)
         self.dev.set_kv_offload(None)
-        off = self.run(steps, peaks, nano)
+        off = self.run(steps, peaks, self.nano)
         b = int(np.argmax(self.pos))
         n = int(self.pos[b])
         tab = self.tables[b, :int(math.ceil(n / self.bs))].copy()
@@ -701,28 +980,22 @@ class ContinuousWorkload:
                 "plain_h2d_gbs": round(nbytes / h2d_ms * 1e-6, 1),
                 "device_error": self.dev.device_error()}
 
-    def report(self, steps, peaks):
-        # a short comparison of the nano-batch splits, then the full run with the faster one
-        trial = {}
-        for nano in (None, [128, 128]):
-            trial[str(nano or [self.B])] = self.run(20, peaks, nano)["device_ms_per_step_median"]
-        best = None if trial[str([self.B])] <= trial[str([128, 128])] else [128, 128]
-        r = self.run(steps, peaks, best)
-        r["split_trial_ms_per_step"] = trial
-        # per-kind kernel time of eager steps (an event pair around each launch)
-        self.dev.set_kernel_timing(True)
-        self.run(2, peaks, best)
-        self.dev.kernel_timing()
-        self.run(3, peaks, best)
-        kt = self.dev.kernel_timing()
-        self.dev.set_kernel_timing(False)
-        r["eager_kernel_us"] = {k: round(v[1] / v[0] * 1e3, 1) for k, v in kt.items() if v[0]}
-        r["eager_kernel_launches_per_step"] = {k: v[0] // 3 for k, v in kt.items() if v[0]}
-        r["kv_offload"] = self.offload(30, peaks, best)
-        r["workload"] = ("LLaMA-3-8B-shaped 32L bf16, batch 256, ctx U[512,4096], decode lengths "
-                         "U[100,1000] with leave/join, greedy argmax fed back, graph replay")
-        r["setup_s"] = round(self.setup_s, 1)
-        return r
+    def close(self):
+        self.dev.set_token_source(None)
+        self.dev.close()
+
+
+def cfg4_table_width(bs: int = 16) -> int:
+    """Block-table width of the continuous run: the longest context plus the longest decode."""
+    return int(math.ceil((ContinuousWorkload.ctx_hi + ContinuousWorkload.dec_hi + 1) / bs))
+
+
+def cfg4_meta_bytes(B: int, mb: int) -> int:
+    """Bytes of one step's packed metadata upload (token ids, positions, lengths, slots, block
+    tables, the logits pointer and two flags), as the library lays it out."""
+    o = 12 * B
+    o = (o + 15) // 16 * 16 + 8 * B + 4 * B * mb
+    return (o + 15) // 16 * 16 + 16
 
 
 # ---------------------------------------------------------------------------------- serving run
@@ -1035,6 +1308,28 @@ def read_traffic(kind):
     return None
 
 
+def scaled_traffic(kind, algo_bytes):
+    """Per-launch DRAM bytes of a launch moving `algo_bytes` algorithmic bytes, from the ncu
+    summary of a smaller launch of the same kernel (its line gives the captured launch's
+    algorithmic bytes as a fourth field): the captured traffic scaled by the ratio, valid when
+    traffic grows in proportion to the units processed (K/V tokens read).  None when the
+    counters are stale or absent."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 4 and parts[0] == kind:
+            try:
+                dram, algo = float(parts[1]), float(parts[3])
+            except ValueError:
+                return None
+            if parts[2] != kernel_source_hash(kind) or algo <= 0:
+                return None
+            return dram * algo_bytes / algo
+    return None
+
+
 def replica_aggregate(ms_local: float, units_local: int, world: int):
     """Whole-job figures of independent replicas (the step does not shard): the slowest rank's
     time and the units every rank processed.  One collective per measurement, outside the
@@ -1064,91 +1359,84 @@ def repeat_check(ms_a: float, n_a: int, ms_b: float, n_b: int, limit: float = 0.
             "limit": limit, "flagged": spread > limit}
 
 
-def run_ours(args, rank, world):
-    import torch
-    import __graft_entry__ as ge
-    from transformer_decode_step_ns_gb300 import _lib
-    ge.build()
-    dev_idx = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(dev_idx)
-    peaks, peaks_src = load_peaks()
-    K, W = args.steps, args.warmup
-    e2e_steps = max(5, min(K, 50))
-    wl = DecodeWorkload(args.batch, total_steps=W + K + e2e_steps + 8)
-    log(f"setup {wl.setup_s:.1f}s: {wl.num_blocks} blocks, mb {wl.mb}")
+class SmallStepWorkload:
+    """The 2-layer Qwen2.5-0.5B-shaped decoder at batch 1 (the small parity case): 128 cached
+    tokens in a seeded permutation of physical blocks 0-7, this step's token at position 128 in
+    block 8, fp16 weights N(0, 0.02).  Each graph replay is timed alone after a 256 MiB write
+    that flushes L2 (the step's 60 MB of layer weights would otherwise stay in L2 between
+    replays)."""
 
-    # warm-up (captures the graph on the first step)
-    for _ in range(W):
-        warm_meta = wl.next_meta()
-        wl.step(warm_meta)
-    torch.cuda.synchronize()
-    metas = [wl.next_meta() for _ in range(K)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler()
-    clocks.start()
-    # keep the GPU busy (untimed replays of the last warm-up step) until sampling is live
-    t_wait = time.time()
-    while not clocks.has_samples() and time.time() - t_wait < 5.0:
-        for _ in range(20):
-            wl.step(warm_meta)
+    def __init__(self):
+        import torch
+        from transformer_decode_step_ns_gb300 import _lib
+        self.shape = sh = synth.qwen05b_shape(2)
+        seed = synth.config_seed(0)
+        self.w = synth.model_weights_device(sh, seed)
+        self.dev = _lib.DecodeStep(sh, self.w, 1, 9, use_graphs=True)
+        self.dev.kv_alloc(9, 16)
+        stream = torch.cuda.current_stream().cuda_stream
+        n = self.dev.kv_pool_bytes() // 2
+        for l in range(sh.n_layers):
+            k, v = self.dev.kv_layer_ptrs(l)
+            synth.fill_normal_device(k, n, seed, f"k{l}", "f16", stream=stream)
+            synth.fill_normal_device(v, n, seed, f"v{l}", "f16", stream=stream)
+        tab = np.zeros((1, 9), dtype=np.int32)
+        tab[0, :8] = synth.permutation(seed, "cfg0.blocks", 8)
+        tab[0, 8] = 8
+        tok = synth.uniform_int(seed, "cfg0.token", 1, 0, sh.vocab - 1).astype(np.int32)
+        self.meta = (tok, np.array([128], np.int32), tab, np.array([129], np.int32),
+                     np.array([8 * 16], np.int64))
+        self.logits = torch.empty((1, sh.vocab), dtype=torch.float32, device="cuda")
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def report(self, peaks, n=50, warmup=5):
+        import torch
+        for _ in range(warmup):
+            self.dev.step(*self.meta, self.logits)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            self.flush.zero_()
+            a.record()
+            self.dev.step(*self.meta, self.logits)
+            b.record()
         torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        tflops = float(peaks.get("bf16_tflops", 1900)) * 1e12
+        hbm = float(peaks["hbm_gbs"]) * 1e9
+        work = rl.decode_step_work(self.shape, self.meta[3])
+        t_roof = rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm)
+        return {"workload": "qwen2.5-0.5b-shape 2L fp16 decode, batch 1, 128 cached tokens in "
+                            "8 permuted blocks, graph replay, L2 flushed before each replay",
+                "ms_per_step_median": round(ms, 4), "tokens_per_s": round(1.0 / (ms * 1e-3), 1),
+                "replays": n, "bytes": work.total_bytes, "roofline_us": round(t_roof * 1e6, 2),
+                "frac_of_roofline": round(t_roof / (ms * 1e-3), 4),
+                "device_error": self.dev.device_error()}
+
+
+def qwen_report(args, peaks, world):
+    """The 24-layer Qwen2.5-0.5B-shaped decoder: batch 32 with its own roofline accounting (the
+    dominant kernel by eager per-launch timing), then batches 1 and 8 (graph-replayed steps)."""
+    import torch
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
+    K, W = max(args.steps, 20), args.warmup
+    wl = DecodeWorkload(args.batch, total_steps=W + K + 16)
+    for _ in range(W):
+        wl.step(wl.next_meta())
+    metas = [wl.next_meta() for _ in range(K)]
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_mid = torch.cuda.Event(enable_timing=True)
-    half = K // 2
-    clocks.mark_start()
     e0.record()
-    for i, m in enumerate(metas):
-        if i == half:
-            e_mid.record()
+    for m in metas:
         wl.step(m)
     e1.record()
     torch.cuda.synchronize()
-    clocks.mark_stop()
-    ms_total = e0.elapsed_time(e1)
-    repeat = (repeat_check(e0.elapsed_time(e_mid), half, e_mid.elapsed_time(e1), K - half)
-              if half >= 1 else None)
-    clk = clocks.stop()
-    ms_total, units = replica_aggregate(ms_total, wl.B * K, world)
-    dev_err = wl.dev.device_error()
-    info = wl.dev.info()
-    graphs = wl.dev.graph_report()
-    ms_step = ms_total / K
-    value = units / (ms_total * 1e-3)
-
-    # e2e: greedy decode through the public API.  Every step uploads its host metadata, runs,
-    # takes the argmax on the GPU into the token buffer the next step reads (device token
-    # source) and copies the ids to pinned host memory, where they are read one step late (the
-    # end-of-sequence check of asynchronous batch formation)
-    ids_dev = torch.from_numpy(wl.tokens.copy()).cuda()  # the first step's tokens
-    host_ids = [torch.empty(wl.B, dtype=torch.int32).pin_memory() for _ in range(2)]
-    evs = [torch.cuda.Event() for _ in range(2)]
-    wl.dev.set_token_source(ids_dev)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for k in range(e2e_steps):
-        m = wl.next_meta()
-        wl.dev.step(None, *m[1:], wl.logits)
-        _lib.greedy_argmax(wl.logits, ids_dev)
-        host_ids[k % 2].copy_(ids_dev, non_blocking=True)
-        evs[k % 2].record()
-        if k > 0:
-            evs[(k - 1) % 2].synchronize()
-            wl.tokens = host_ids[(k - 1) % 2].numpy().copy()
-    evs[(e2e_steps - 1) % 2].synchronize()
-    e2e_ms, e2e_units = replica_aggregate((time.perf_counter() - t0) * 1e3, wl.B * e2e_steps, world)
-    e2e_value = e2e_units / (e2e_ms * 1e-3)
-    wl.tokens = host_ids[(e2e_steps - 1) % 2].numpy().copy()
-    wl.dev.set_token_source(None)
-
-    # per-kernel timing in eager steps (same kernels, same data)
+    ms_step = e0.elapsed_time(e1) / K
     wl.dev.set_kernel_timing(True)
     for _ in range(3):
         wl.step(wl.next_meta())
-    wl.dev.kernel_timing()  # discard the first eager steps
+    wl.dev.kernel_timing()
     for _ in range(5):
         wl.step(wl.next_meta())
     kt = wl.dev.kernel_timing()
@@ -1157,132 +1445,195 @@ def run_ours(args, rank, world):
     kb = kernel_bytes(wl.shape, wl.B, metas[-1][3])
     dom = max(kt, key=lambda k: kt[k][1])
     launches, tot_ms = kt[dom]
-    avg_ms = tot_ms / launches
-    achieved = kb[dom] / (avg_ms * 1e-3) / 1e9
+    achieved = kb[dom] / (tot_ms / launches * 1e-3) / 1e9
+    work = rl.decode_step_work(wl.shape, metas[-1][3])
+    t_roof = rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm * 1e9)
+    out = {"workload": WORKLOAD_QWEN, "batch": wl.B, "ms_per_step": round(ms_step, 4),
+           "tokens_per_s": round(wl.B / (ms_step * 1e-3), 1), "steps": K,
+           "roofline_us": round(t_roof * 1e6, 1), "frac_of_roofline": round(t_roof / (ms_step * 1e-3), 4),
+           "kernels_per_step": wl.dev.info().kernels_per_step,
+           "dominant_kernel": {"kind": dom, "achieved_gbs": round(achieved, 1),
+                               "frac_of_hbm": round(achieved / hbm, 4),
+                               "traffic": read_traffic(dom), "share_of_eager_step": round(tot_ms / eager_total, 4)},
+           "kernel_avg_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in kt.items()},
+           "device_error": wl.dev.device_error()}
+    wl.dev.close()
+    del wl
+    sweep = []
+    for B in (1, 8):
+        sw = DecodeWorkload(B, total_steps=70)
+        for _ in range(5):
+            sw.step(sw.next_meta())
+        sm = [sw.next_meta() for _ in range(50)]
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for m in sm:
+            sw.step(m)
+        s1.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1) / len(sm)
+        wk = rl.decode_step_work(sw.shape, sm[-1][3])
+        tr = rl.step_roofline_time(wk.flops, wk.total_bytes, tflops, hbm * 1e9)
+        sweep.append({"batch": B, "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                      "roofline_us": round(tr * 1e6, 1), "frac_of_roofline": round(tr / (ms * 1e-3), 4)})
+        sw.dev.close()
+        del sw
+    out["batch_sweep"] = sweep
+    torch.cuda.empty_cache()
+    return out
+
+
+def oracle_leg_subprocess(threads, seconds, rows):
+    """Run the oracle leg in a child process whose BLAS uses `threads` threads (the thread count
+    is fixed when numpy loads, so it cannot change inside this process).  The child draws its
+    inputs on the host and loads no GPU code."""
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--oracle-threads",
+           str(threads), "--oracle-seconds", str(seconds), "--ref-rows", str(rows)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+    except subprocess.TimeoutExpired:
+        return {"unavailable": "oracle leg timed out"}
+    for line in reversed(r.stdout.splitlines()):
+        if line.startswith("{"):
+            return json.loads(line)
+    return {"unavailable": f"oracle leg failed (rc {r.returncode}): {r.stderr[-300:]}"}
+
+
+def run_ours(args, rank, world):
+    import torch
+    import __graft_entry__ as ge
+    from transformer_decode_step_ns_gb300 import _lib
+    ge.build()
+    dev_idx = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_idx)
+    peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
-    roof = {"kernel": f"gemm_kernel ({dom})" if dom not in ("attention", "embed_rope") else dom,
-            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": read_traffic(dom),
+    K, W = args.steps, args.warmup
+
+    # ---- headline: continuous batching of the LLaMA-3-8B shape at batch 256
+    cw = ContinuousWorkload()
+    log(f"setup {cw.setup_s:.1f}s: {cw.num_blocks} blocks, mb {cw.mb}")
+    best, trial = cw.pick_split(peaks)
+    head = cw.headline(K, W, peaks, world)
+    ms_total, units = replica_aggregate(head["ms_total"], cw.B * K, world)
+    ms_step = ms_total / K
+    value = units / (ms_total * 1e-3)
+    info = cw.dev.info()
+    graphs = cw.dev.graph_report()
+    # e2e: the continuous run through the public API, host metadata and token ids every step
+    if world > 1:
+        torch.distributed.barrier()
+    e2e_run = cw.run_async(args.continuous_steps, peaks)
+    e2e_ms, e2e_units = replica_aggregate(e2e_run["wall_s"] * 1e3, cw.B * e2e_run["steps"], world)
+    e2e_value = e2e_units / (e2e_ms * 1e-3)
+    kt = cw.kernel_times(peaks)
+    offload = cw.offload(30, peaks) if rank == 0 and not args.skip_offload else None
+    dev_err = cw.dev.device_error()
+    cw.close()
+    del cw
+    torch.cuda.empty_cache()
+
+    attn_us = kt["attention_ms"] / kt["attention_launches"] * 1e3
+    achieved = kt["attention_bytes_per_launch"] / (attn_us * 1e-6) / 1e9
+    roof = {"kernel": "attention (attn_decode_kernel)", "bound": "hbm", "achieved": achieved,
+            "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": scaled_traffic("attention_cfg4", kt["attention_bytes_per_launch"]),
             "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if peaks_src == "measured"
             else "fallback 6.8 TB/s",
-            "bytes_per_launch": kb[dom], "avg_launch_us": avg_ms * 1e3,
-            "share_of_eager_step": tot_ms / eager_total,
-            "kernel_shares": {k: round(v[1] / eager_total, 4) for k, v in kt.items()},
-            "kernel_avg_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in kt.items()}}
-
-    # whole-step roofline
-    work = rl.decode_step_work(wl.shape, metas[-1][3])
-    tflops = float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12
-    t_roof = rl.step_roofline_time(work.flops, work.total_bytes, tflops, hbm * 1e9)
+            "bytes_per_launch": kt["attention_bytes_per_launch"], "avg_launch_us": attn_us,
+            "share_of_eager_step": kt["attention_share"], "kernel_shares": kt["shares"],
+            "kernel_avg_us": kt["kernel_us"], "launches_per_step": kt["launches_per_step"]}
+    t_roof = head["roofline_s"] / K
     step_roof = {"roofline_us": t_roof * 1e6, "measured_us": ms_step * 1e3,
-                 "frac": t_roof / (ms_step * 1e-3), "bytes": work.total_bytes,
-                 "flops": work.flops,
-                 "bound": "hbm" if work.total_bytes / (hbm * 1e9) >= work.flops / tflops
-                 else "tensor"}
+                 "frac": t_roof / (ms_step * 1e-3), "bytes_per_step": head["bytes"] / K,
+                 "flops_per_step": head["flops"] / K,
+                 "bound": "hbm" if head["bytes"] / (hbm * 1e9) >= head["flops"] / (
+                     float(peaks.get("bf16_tflops_sustained", 1700)) * 1e12) else "tensor",
+                 "peaks": "measured HBM copy and sustained bf16" if peaks_src == "measured"
+                 else "fallback"}
 
-    # the same model at batch 1 and 8 (and the headline's 32): graph-replayed step time
-    sweep = []
+    # ---- the other workloads (rank 0 only)
+    extras = {}
     if rank == 0:
-        for B in (1, 8):
-            sw = DecodeWorkload(B, total_steps=70)
-            for _ in range(5):
-                sw.step(sw.next_meta())
-            sm = [sw.next_meta() for _ in range(50)]
-            torch.cuda.synchronize()
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s0.record()
-            for m in sm:
-                sw.step(m)
-            s1.record()
-            torch.cuda.synchronize()
-            ms = s0.elapsed_time(s1) / len(sm)
-            wk = rl.decode_step_work(sw.shape, sm[-1][3])
-            tr = rl.step_roofline_time(wk.flops, wk.total_bytes, tflops, hbm * 1e9)
-            sweep.append({"batch": B, "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
-                          "roofline_us": round(tr * 1e6, 1), "frac_of_roofline": round(tr / (ms * 1e-3), 4)})
+        extras["qwen_24l"] = qwen_report(args, peaks, world) if not args.skip_qwen else None
+        if not args.skip_small:
+            sw = SmallStepWorkload()
+            extras["qwen_2l_b1"] = sw.report(peaks)
             sw.dev.close()
             del sw
-        sweep.append({"batch": wl.B, "ms_per_step": round(ms_step, 4), "tokens_per_s": round(value / world, 1),
-                      "roofline_us": round(t_roof * 1e6, 1), "frac_of_roofline": round(t_roof / (ms_step * 1e-3), 4)})
+        if not args.skip_attention:
+            aw = AttentionWorkload(max_batch=max(SWEEP_BATCHES))
+            attn = aw.report(256, max(10, min(K, 50)), W, hbm)
+            attn["sweep_l2_flushed"] = aw.sweep(SWEEP_BATCHES, hbm)
+            attn["device_error"] = _lib.device_error()
+            extras["attention"] = attn
+            del aw
         torch.cuda.empty_cache()
-
-    attn = None
-    if not args.skip_attention and rank == 0:
-        aw = AttentionWorkload(max_batch=max(SWEEP_BATCHES))
-        attn = aw.report(256, max(10, min(K, 50)), W, hbm)
-        attn["sweep_l2_flushed"] = aw.sweep(SWEEP_BATCHES, hbm)
-        attn["device_error"] = _lib.device_error()
-        del aw
-        torch.cuda.empty_cache()
-
-    nano = None
-    if not args.skip_nanobatch and rank == 0:
-        nw = NanoLayerWorkload()
-        nano = nw.report(20, 3, peaks)
-        del nw
-        torch.cuda.empty_cache()
-
-    cont = None
-    if not args.skip_continuous and rank == 0 and args.continuous_steps > 0:
-        cw = ContinuousWorkload()
-        cont = cw.report(args.continuous_steps, peaks)
-        del cw
-        torch.cuda.empty_cache()
-
-    serve = None
-    if not args.skip_serving and rank == 0:
-        sw = ServingWorkload()
-        serve = sw.report()
-        del sw
-        torch.cuda.empty_cache()
+        if not args.skip_nanobatch:
+            nw = NanoLayerWorkload()
+            extras["nanobatch_layer"] = nw.report(20, 3, peaks)
+            nw.dev.close()
+            del nw
+            torch.cuda.empty_cache()
+        if not args.skip_serving:
+            sv = ServingWorkload()
+            extras["serving"] = sv.report()
+            del sv
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        import oracle
-        hw, hk, hv = host_copy_of(wl)
-        model = oracle.OracleModel.from_weights(wl.shape, hw)
-        rows = np.arange(min(args.cpu_rows, wl.B))
-        secs, reps = 0.0, 0
-        while reps < 1 or (secs < args.cpu_seconds and reps < 200):
-            secs += oracle_sample(model, hk, hv, metas[reps % len(metas)], rows, wl.bs)
-            reps += 1
-        cpu = {"value": len(rows) * reps / secs, "unit": "tokens/s", "cores": blas_threads(),
-               "kind": "oracle",
-               "sample": f"{reps} decode steps of {len(rows)} of the {wl.B} requests (24 layers "
-                         f"+ LM head each, fp64 numpy), {secs:.1f} s of CPU work"}
+        cores = len(os.sched_getaffinity(0))
+        allc = oracle_leg_subprocess(cores, args.cpu_seconds, args.ref_rows)
+        one = oracle_leg_subprocess(1, args.cpu_seconds, args.ref_rows)
+        if "value" in allc:
+            cpu = {"value": allc["value"], "unit": "tokens/s", "cores": allc["cores"],
+                   "kind": "oracle", "sample": allc["sample"],
+                   "single_thread": {"value": one.get("value"), "cores": 1,
+                                     "sample": one.get("sample", one.get("unavailable"))}}
+        else:
+            cpu = {"unavailable": allc.get("unavailable"), "kind": "oracle"}
 
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "model": "qwen2.5-0.5b-shaped (random init)",
-                   "global_batch": wl.B * world, "seq_len": "ctx U[128,1024] + decode",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "model": "llama-3-8b-shaped (random init)",
+                   "global_batch": ContinuousWorkload.B * world,
+                   "seq_len": "ctx U[512,4096] + decode U[100,1000], leave/join",
+                   "nano_split": best or [ContinuousWorkload.B],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (988 MB of weights streamed per step)"},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": wl.meta_bytes(),
-                "d2h_bytes_per_step": wl.B * 4, "steps": e2e_steps,
-                "loop": "greedy decode: host metadata upload, step, argmax into the device token "
-                        "source of the next step, ids copied to pinned host memory and read one "
-                        "step late"},
+                   "l2": "inputs larger than L2 (15 GB of weights and ~77 GB of K/V per step)"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": head["meta_bytes"],
+                "d2h_bytes_per_step": ContinuousWorkload.B * 4, "steps": e2e_run["steps"],
+                "loop": "continuous batching through the public API: every step the host slot "
+                        "mapper and join/leave bookkeeping, one packed metadata upload, graph "
+                        "replay, greedy argmax into the next step's device token source, ids "
+                        "copied to pinned host memory and read one step late",
+                "run": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e_run.items()}},
         "roofline": roof,
         "step_roofline": step_roof,
-        "batch_sweep": sweep,
-        "attention": attn,
-        "nanobatch_layer": nano,
-        "continuous": cont,
-        "serving": serve,
         "cpu_baseline": cpu,
-        "clocks": clk,
-        "repeat": repeat,
-        "gpu_launches": info.kernels_per_step * K,
-        "kernels_per_step": info.kernels_per_step,
+        "clocks": head["clocks"],
+        "repeat": head["repeat"],
+        "gpu_launches": (info.kernels_per_step + 1) * K,
+        "kernels_per_step": info.kernels_per_step + 1,
+        "split_trial_ms_per_step": trial,
+        "leaves_and_joins_in_timed_steps": head["leaves_and_joins"],
         "graph_capture_ms": info.last_capture_ms,
         "graphs": [{k: (round(v, 3) if isinstance(v, float) else v) for k, v in g.items()}
                    for g in graphs],
+        "kv_offload": offload,
         "device_error": dev_err,
     }
+    line.update(extras)
     print(json.dumps(line), flush=True)
 
 
@@ -1354,54 +1705,50 @@ def run_extra_only(args, rank, world):
                 "config": {"workload": r["workload"]}, "serving": r}
     else:
         cw = ContinuousWorkload()
-        r = cw.report(args.continuous_steps, peaks)
+        best, trial = cw.pick_split(peaks)
+        head = cw.headline(max(args.steps, 1), args.warmup, peaks, 1)
+        r = cw.run_async(args.continuous_steps, peaks)
+        r["split_trial_ms_per_step"] = trial
+        r["kernels"] = cw.kernel_times(peaks)
+        K = max(args.steps, 1)
         line = {"metric": "decode output tokens/s, continuous batching", "unit": "tokens/s",
-                "value": r["tokens_per_s_device"], "higher_is_better": True,
-                "n_gpus": world, "steps": r["steps"], "warmup": 20, "dtype": "bf16",
-                "data": "synthetic", "config": {"workload": r["workload"]}, "continuous": r}
+                "value": ContinuousWorkload.B * K / (head["ms_total"] * 1e-3),
+                "ms_per_step": head["ms_total"] / K, "higher_is_better": True,
+                "n_gpus": world, "steps": K, "warmup": args.warmup, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": WORKLOAD, "nano_split": best},
+                "frac_of_roofline": head["roofline_s"] / (head["ms_total"] * 1e-3),
+                "clocks": head["clocks"], "continuous": r}
+        cw.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
 def run_reference(args, rank, world):
-    """The oracle arm: the fp64 CPU oracle on bounded samples of the same workload."""
+    """The oracle arm: the fp64 CPU oracle on bounded samples of the headline workload, inputs
+    drawn on the host (no GPU code is loaded)."""
     if rank != 0:
         return
-    import torch
-    import __graft_entry__ as ge
-    import oracle
     K, W = args.steps, args.warmup
-    rows_per_step = max(1, args.ref_rows)
-    if not torch.cuda.is_available():
-        print(json.dumps({"impl": "reference", "unavailable":
-                          "the seeded inputs are drawn on the GPU; no CUDA device"}))
-        return
-    ge.build()
-    wl = DecodeWorkload(args.batch, total_steps=2)
-    meta = wl.next_meta()
-    hw, hk, hv = host_copy_of(wl)
-    shape, bs, B = wl.shape, wl.bs, wl.B
-    del wl
-    model = oracle.OracleModel.from_weights(shape, hw)
+    R = max(1, args.ref_rows)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", len(os.sched_getaffinity(0))))
+    smp = Cfg4OracleSample(workers=len(os.sched_getaffinity(0)))
     times = []
     for i in range(W + K):
-        rows = (np.arange(rows_per_step) + i * rows_per_step) % B
-        s = oracle_sample(model, hk, hv, meta, rows, bs)
+        s_ = smp.time_step((np.arange(R) + i * R) % ContinuousWorkload.B)
         if i >= W:
-            times.append(s)
+            times.append(s_)
     total = sum(times)
-    value = rows_per_step * K / total
+    value = R * K / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total / K * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "model": "qwen2.5-0.5b-shaped (random init)",
-                       "global_batch": B, "seq_len": "ctx U[128,1024] + decode",
+            "config": {"workload": WORKLOAD, "model": "llama-3-8b-shaped (random init)",
+                       "global_batch": ContinuousWorkload.B,
+                       "seq_len": "ctx U[512,4096] + decode U[100,1000], leave/join",
                        "parallelism": "host cores"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
-                             "kind": "oracle",
-                             "sample": f"{rows_per_step} of {B} requests per step, one full "
-                                       f"decode step each (24 layers + LM head, fp64)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": smp.describe(R, K)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -1434,14 +1781,24 @@ def main():
     ap.add_argument("--continuous-only", action="store_true",
                     help="run the continuous-batching LLaMA-3-8B workload alone")
     ap.add_argument("--cpu-rows", type=int, default=32)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="minimum CPU time of the oracle baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="minimum CPU time of each oracle baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=2)
     ap.add_argument("--attention-only", action="store_true",
                     help="time the paged attention workload alone at --attn-batch")
     ap.add_argument("--attn-batch", type=int, default=256)
     ap.add_argument("--attn-pool-blocks", type=int, default=160_000)
+    ap.add_argument("--skip-qwen", action="store_true")
+    ap.add_argument("--skip-small", action="store_true")
+    ap.add_argument("--skip-offload", action="store_true")
+    ap.add_argument("--oracle-leg", action="store_true",
+                    help="internal: time the oracle on the headline workload and print JSON")
+    ap.add_argument("--oracle-threads", type=int, default=0)
+    ap.add_argument("--oracle-seconds", type=float, default=15.0)
     args = ap.parse_args()
+    if args.oracle_leg:
+        oracle_leg(args)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -398,6 +398,58 @@ def normal_device(seed: int, name: str, shape: Sequence[int], dtype: str, std: f
     return t
 
 
+_HOST_LIB = None
+
+
+def build_host(force: bool = False) -> str:
+    """Compile synth/csrc/fill_host.c into synth/libsynth_host.so (gcc, no FP contraction)."""
+    import os
+    import shutil
+    import subprocess
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "csrc", "fill_host.c")
+    out = os.path.join(here, "libsynth_host.so")
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    cc = shutil.which("gcc") or shutil.which("cc") or "gcc"
+    cmd = [cc, "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread",
+           "-o", out, src, "-lm"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"gcc failed for fill_host.c:\n{r.stderr}")
+    return out
+
+
+def _host_lib():
+    global _HOST_LIB
+    if _HOST_LIB is None:
+        import ctypes
+        L = ctypes.CDLL(build_host())
+        L.synth_fill_normal_host.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_ulonglong,
+                                             ctypes.c_ulonglong, ctypes.c_double, ctypes.c_double,
+                                             ctypes.c_int, ctypes.c_int]
+        L.synth_fill_normal_host.restype = ctypes.c_int
+        _HOST_LIB = L
+    return _HOST_LIB
+
+
+def normal_threads(seed: int, name: str, shape: Sequence[int], dtype: str, std: float = 1.0,
+                   mean: float = 0.0, offset: int = 0, threads: int = 0) -> np.ndarray:
+    """``normal()`` computed by the C twin on ``threads`` host threads (0: every core this
+    process may use).  Same definition; both sides call their platform's own log/cos/sqrt in
+    fp64, so an element can differ only where the two round a transcendental differently in
+    the last fp64 bit and that bit decides the 16-bit rounding."""
+    import os
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.float16 if dtype == F16 else np.uint16)
+    t = threads if threads > 0 else len(os.sched_getaffinity(0))
+    r = _host_lib().synth_fill_normal_host(out.ctypes.data, n, stream_key(seed, name), offset,
+                                           float(mean), float(std), 1 if dtype == BF16 else 0, t)
+    if r != 0:
+        raise RuntimeError(f"synth_fill_normal_host failed ({r})")
+    return out.reshape(shape)
+
+
 def model_weights_device(shape: ModelShape, seed: int, std: float = 0.02,
                          gamma_std: float = 0.0) -> Dict[str, object]:
     """``model_weights`` drawn on the GPU (same values), as torch CUDA tensors."""
