@@ -237,7 +237,12 @@ def test_llama3_8b_shapes_at_truncated_depth_per_tensor(cuda_lib, depth):
         std over 0.6 (the bound is stated for logits of std ~0.6; this head's are ~1.3);
       * every K/V slot the step writes, per layer: relative L2 <= 1e-2;
       * per layer, q after RoPE, the attention output and the residuals after the attention
-        block and after the layer (ns_set_trace, eager launches): relative L2 <= 1e-2."""
+        block and after the layer (ns_set_trace, eager launches): relative L2 <= 1e-2 through
+        two layers.  Deeper, rounding the products' bf16 operands alone (the fp64 oracle with
+        only those roundings added, computed on the host for these shapes) puts the fourth
+        layer's attention output 1.1 % from the oracle, so at depth 4 the per-tensor bound is
+        1.5e-2; logits and cache slots keep 1e-2 at every depth.
+    The measured errors are printed as one JSON line (pytest -s)."""
     import torch
     from transformer_decode_step_ns_gb300 import _lib
     seed = synth.config_seed(4)
@@ -289,6 +294,8 @@ def test_llama3_8b_shapes_at_truncated_depth_per_tensor(cuda_lib, depth):
     np.testing.assert_array_equal(outs[0], outs[1])
     got = outs[0].astype(np.float64)
     abs_tol = 5e-2 * max(1.0, float(ref.std()) / 0.6)
+    measured = {"logits": round(rel_l2(got, ref), 5), "logits_max_abs": round(float(np.abs(got - ref).max()), 4),
+                "logits_std": round(float(ref.std()), 3), "max_abs_bound": round(abs_tol, 4)}
     _check_logits(got, ref, f"llama3-8b shapes, {depth} layers, logits", abs_tol=abs_tol)
     blk, off = slots // bs, slots % bs
     qd = sh.n_q_heads * sh.head_dim
@@ -303,6 +310,7 @@ def test_llama3_8b_shapes_at_truncated_depth_per_tensor(cuda_lib, depth):
         vv = _download_pool(v_ptr, pool_bytes, "bf16").reshape(shp)
         for name, pool, want in (("k", kk, tr["k"][l]), ("v", vv, tr["v"][l])):
             e = rel_l2(oracle.from_storage(pool[blk, :, off, :], "bf16"), want)
+            measured[f"L{l}.{name}"] = round(e, 5)
             assert e < 1e-2, (depth, l, name, e)
         dev.set_trace(l, q=q_t, attn=o_t, resid_mid=rm, resid_out=ro)
         dev.step(*meta, logits)
@@ -316,5 +324,8 @@ def test_llama3_8b_shapes_at_truncated_depth_per_tensor(cuda_lib, depth):
                  "resid": ro.cpu().numpy().astype(np.float64)}
         for name, g in got_t.items():
             e = rel_l2(g, tr[name][l])
-            assert e < 1e-2, (depth, l, name, e)
+            measured[f"L{l}.{name}"] = round(e, 5)
+            assert e < (1e-2 if depth <= 2 else 1.5e-2), (depth, l, name, e)
     dev.close()
+    import json
+    print(json.dumps({"depth": depth, "rel_l2": measured}))

@@ -150,6 +150,28 @@ def test_head_dim_128_over_several_token_tiles(cuda_lib, n_q, n_kv):
     _check_step(Harness(shape, 81 + n_kv, ctx))
 
 
+def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cuda_lib):
+    """300 rows, head_dim 128: unsplit every projection runs the persistent kernel (3 token
+    tiles); as 40 + 260 rows the first nano-batch runs the cluster kernel, and as 100 + 200 both
+    run persistent launches of other tile counts.  Every fused epilogue (QKV with RoPE and the
+    cache write, residual + norm, SwiGLU, the fp32 head) gives each row the same bits."""
+    shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                             ffn=768, vocab=640, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
+                             tie_embeddings=False)
+    ctx = list(synth.uniform_int(83, "ctx300", 300, 0, 70))
+    h = Harness(shape, 84, ctx)
+    got, _ = _check_step(h)
+    ks0, vs0 = h.download_pools()
+    for sizes in ([40, 260], [100, 200]):
+        h.upload_pools()
+        h.dev.set_nanobatch(sizes)
+        np.testing.assert_array_equal(h.run_gpu(), got)
+        ks, vs = h.download_pools()
+        for l in range(shape.n_layers):
+            np.testing.assert_array_equal(ks[l], ks0[l])
+            np.testing.assert_array_equal(vs[l], vs0[l])
+
+
 def test_graph_replay_equals_eager_bitwise(cuda_lib):
     shape = _tiny("bf16")
     a = Harness(shape, 41, [3, 40, 200], use_graphs=True)
@@ -438,8 +460,12 @@ def _trace_layer(h: Harness, layer: int):
     logits = h.run_gpu()
     h.dev.set_trace(-1)
     dt = sh.dtype
-    return {"q": storage_f64(from_dev(q)[:B], dt).reshape(B, sh.n_q_heads, sh.head_dim),
-            "attn": storage_f64(from_dev(o)[:B], dt).reshape(B, sh.n_q_heads, sh.head_dim),
+
+    def bits(t):  # 16-bit storage patterns in the oracle's format (float16 values or bf16 bits)
+        a = from_dev(t)[:B]
+        return a.view(np.float16) if dt == "f16" else a
+    return {"q": storage_f64(bits(q), dt).reshape(B, sh.n_q_heads, sh.head_dim),
+            "attn": storage_f64(bits(o), dt).reshape(B, sh.n_q_heads, sh.head_dim),
             "resid_attn": rm[:B].cpu().numpy().astype(np.float64),
             "resid": ro[:B].cpu().numpy().astype(np.float64)}, logits
 

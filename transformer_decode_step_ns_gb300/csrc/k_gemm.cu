@@ -61,6 +61,24 @@ __device__ __forceinline__ void set_err(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// The epilogue formulas, written once for both kernels with explicit roundings so the two give
+// a row the same bits whichever launch it is in.
+// RoPE on one (i, i + d/2) pair: (x_lo, x_hi) -> (x_lo c - x_hi s, x_hi c + x_lo s).
+__device__ __forceinline__ float rope_lo(float x_lo, float x_hi, float c, float sn) {
+  return __fmaf_rn(x_lo, c, -__fmul_rn(x_hi, sn));
+}
+__device__ __forceinline__ float rope_hi(float x_lo, float x_hi, float c, float sn) {
+  return __fmaf_rn(x_hi, c, __fmul_rn(x_lo, sn));
+}
+// silu(g) * u
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdividef(g, __fadd_rn(1.f, __expf(-g))), u);
+}
+// 1 / sqrt(mean of squares + eps) from a row's summed squares
+__device__ __forceinline__ float rms_scale(float sumsq, int n, float eps) {
+  return rsqrtf(__fadd_rn(__fdiv_rn(sumsq, static_cast<float>(n)), eps));
+}
+
 }  // namespace
 
 template <typename T>
@@ -254,8 +272,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
           const int jj = jj0 + 4 * u;
-          if (lane == 0 && jj < n_own)
-            rs_s[rank + S * jj] = rsqrtf(x / static_cast<float>(e.norm_dim) + e.eps);
+          if (lane == 0 && jj < n_own) rs_s[rank + S * jj] = rms_scale(x, e.norm_dim, e.eps);
         }
       }
     }
@@ -408,8 +425,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
               const float sc = scaled ? rs_s[j] : 1.f;
               const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
               const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
-              const float y_lo = x_lo * c - x_hi * sn;
-              const float y_hi = x_hi * c + x_lo * sn;
+              const float y_lo = rope_lo(x_lo, x_hi, c, sn);
+              const float y_hi = rope_hi(x_lo, x_hi, c, sn);
               if (n0 < e.q_dim) {
                 T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
                 dst[r_lo] = Cvt<T>::from_f(y_lo);
@@ -546,7 +563,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             const float sc = scaled ? rs_s[j] : 1.f;
             const float g = tile[j * kGemmTileN + c] * sc;
             const float u = tile[j * kGemmTileN + 64 + c] * sc;
-            const float a = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
+            const float a = silu_mul(g, u);
             ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
           }
           fence_proxy_async_global();
@@ -573,6 +590,433 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   }
 }
 
+// ------------------------------------------------------------------------------ persistent
+// Launches of more than 64 rows (the ridge point and the compute-bound dense batches of the
+// NanoFlow page) run a persistent variant: one CTA per SM loops over work units (token tile,
+// k split, 128-feature tile), token tiles fastest so CTAs running side by side share a weight
+// tile through L2.  The TMA warp streams every unit's stages through one deep ring without
+// stopping between units; the MMA warp alternates between two TMEM accumulators, so the
+// epilogue of one unit overlaps the main loop of the next.  Split-K partials go to a global
+// workspace [tile][split][BN][128] fp32; the split that arrives last (an atomic counter per
+// tile, reset by it for the next launch) sums them in split order, exactly as the cluster
+// kernel does, and runs the fused epilogue for the whole tile from registers (a thread holds one
+// feature of 16 tokens; RoPE pairs, gate/up pairs and the per-token sums of squares are
+// exchanged through a 16-token shared buffer).  Nothing waits on another CTA, so any grid size
+// is safe.  The k split of a weight, the reduction order and every epilogue formula are those
+// of the cluster kernel, so a row gets the same bits from either.
+constexpr int kXchgFloats = 16 * kGemmTileN;  // one 16-token chunk of a tile
+
+template <typename T>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap mapA,
+                           const __grid_constant__ CUtensorMap mapB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int BN = p.BN;
+  const int ns = p.nstage;
+  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(BN) * kGemmTileK * 2;
+  float* xchg = reinterpret_cast<float*>(smem + static_cast<size_t>(ns) * stage_bytes);
+  uint8_t* ctrl = reinterpret_cast<uint8_t*>(xchg + kXchgFloats);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + ns;
+  uint64_t* acc_full = empty + ns;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* issued = abort_flag + 1;
+  int* epi_flag = issued + 1;  // broadcast word of the epilogue warps
+  float* rs_s = reinterpret_cast<float*>(ctrl + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.splits, tiles_m = p.tiles_m, n_tiles = p.N / kGemmTileN;
+  const int n_units = tiles_m * S * n_tiles;
+  const int nkb_total = p.K / kGemmTileK;
+  const uint32_t ncols = BN <= 128 ? 128u : 256u;
+
+  auto stageA = [&](int st) { return smem + static_cast<size_t>(st) * stage_bytes; };
+  auto stageB = [&](int st) { return smem + static_cast<size_t>(st) * stage_bytes + kABytes; };
+  // unit u -> (token tile, split, feature tile); its k-blocks [kb0, kb0 + nkb)
+  struct Unit {
+    int tm, sp, tn, kb0, nkb;
+  };
+  auto unit_of = [&](int u) {
+    Unit w;
+    w.tm = u % tiles_m;
+    const int r = u / tiles_m;
+    w.sp = r % S;
+    w.tn = r / S;
+    w.kb0 = w.sp * p.kb_per_split;
+    w.nkb = min(p.kb_per_split, nkb_total - w.kb0);
+    return w;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < ns; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    *issued = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mapA);
+    prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = tiles_m > 1 ? policy_evict_normal() : policy_evict_first();
+      // (unit, k-block) pairs of this CTA in order; `it` counts them
+      int u = blockIdx.x, i = 0, it = 0;
+      Unit w = u < n_units ? unit_of(u) : Unit{};
+      auto next = [&]() {
+        if (++i == w.nkb) {
+          i = 0;
+          u += gridDim.x;
+          if (u < n_units) w = unit_of(u);
+        }
+      };
+      // the weights of the first ring's worth of stages go out before the dependency wait
+      const int u0 = u;
+      const Unit w0 = w;
+      int pre = 0;
+      while (pre < ns && u < n_units) {
+        mbar_arrive_expect_tx(&full[pre], stage_bytes);
+        tma_load_2d_hint(stageA(pre), &mapA, &full[pre], (w.kb0 + i) * kGemmTileK, w.tn * kGemmTileN, pol_w);
+        ++pre;
+        next();
+      }
+      griddep_wait();  // activations come from the previous kernel of the step
+      {
+        int uu = u0, ii = 0;
+        Unit ww = w0;
+        for (int t = 0; t < pre; ++t) {
+          tma_load_2d(stageB(t), &mapB, &full[t], (ww.kb0 + ii) * kGemmTileK, p.row0 + ww.tm * BN);
+          if (++ii == ww.nkb) {
+            ii = 0;
+            uu += gridDim.x;
+            if (uu < n_units) ww = unit_of(uu);
+          }
+        }
+      }
+      it = pre;
+      while (u < n_units) {
+        const int st = it % ns;
+        if (!mbar_wait(&empty[st], static_cast<uint32_t>((it / ns) - 1) & 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], stage_bytes);
+        tma_load_2d_hint(stageA(st), &mapA, &full[st], (w.kb0 + i) * kGemmTileK, w.tn * kGemmTileN, pol_w);
+        tma_load_2d(stageB(st), &mapB, &full[st], (w.kb0 + i) * kGemmTileK, p.row0 + w.tm * BN);
+        ++it;
+        next();
+      }
+      *issued = it;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, j = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
+        const Unit w = unit_of(u);
+        const int b = j & 1;
+        if (j >= 2 && !mbar_wait(&acc_empty[b], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * ncols;
+        bool ok = true;
+        for (int i = 0; i < w.nkb; ++i, ++it) {
+          const int st = it % ns;
+          if (!mbar_wait(&full[st], static_cast<uint32_t>(it / ns) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stageA(st));
+          const uint32_t b_addr = smem_u32(stageB(st));
+#pragma unroll
+          for (int k = 0; k < kGemmTileK / 16; ++k) {
+            umma_f16(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), p.idesc,
+                     (i | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        umma_commit(&acc_full[b]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue warps
+    const EpiArgs& e = p.e;
+    const int et = threadIdx.x - 64;  // 0..127
+    const int ew = warp - 2;
+    const int q = warp & 3;           // TMEM lane quarter this warp may read
+    const int f = q * 32 + lane;      // output feature within the tile
+    const bool scaled = e.sumsq_in != nullptr;
+    griddep_wait();  // the previous kernel wrote the epilogue's inputs and may read our outputs
+    int j = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
+      const Unit w = unit_of(u);
+      const int b = j & 1;
+      const int n0 = w.tn * kGemmTileN;
+      const int tok0 = p.row0 + w.tm * BN;
+      const int m_valid = min(BN, p.M - w.tm * BN);
+      const int nchunk = (m_valid + 15) >> 4;
+      // one thread waits for the accumulator (bounded) and tells the others
+      if (et == 0) {
+        const bool ok = !*abort_flag && mbar_wait(&acc_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag);
+        if (!ok) {
+          *abort_flag = 1;
+          set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+        }
+        *epi_flag = ok ? 1 : 0;
+      }
+      named_barrier_sync(1, 128);
+      if (!*epi_flag) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + static_cast<uint32_t>(b) * ncols + (static_cast<uint32_t>(q * 32) << 16);
+      const size_t tile_id = static_cast<size_t>(w.tn) * tiles_m + w.tm;
+      const size_t slot_floats = static_cast<size_t>(BN) * kGemmTileN;
+      bool run_epi = true;
+      if (S > 1) {
+        // this split's partial -> workspace; the accumulator is free again
+        float* mine = p.ws + (tile_id * S + w.sp) * slot_floats;
+        for (int c = 0; c < nchunk; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tb + static_cast<uint32_t>(c * 16), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) __stcg(&mine[(c * 16 + i) * kGemmTileN + f], __uint_as_float(r[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        __threadfence();
+        named_barrier_sync(1, 128);
+        if (et == 0) {
+          const int old = atomicAdd(&p.ws_cnt[tile_id], 1);
+          const int last = old == S - 1;
+          if (last) p.ws_cnt[tile_id] = 0;  // ready for the next launch
+          *epi_flag = last;
+        }
+        named_barrier_sync(1, 128);
+        run_epi = *epi_flag != 0;
+        if (run_epi) __threadfence();
+      }
+      if (run_epi) {
+        if (scaled) {
+          // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps), the same fixed
+          // shuffle tree as the cluster kernel (one warp per token)
+          const int n_tiles_s = e.sumsq_tiles;
+          const size_t ld = static_cast<size_t>(e.sumsq_ld);
+          for (int jj = ew; jj < m_valid; jj += 4) {
+            const float* sp = e.sumsq_in + tok0 + jj;
+            float x = 0.f;
+            if (n_tiles_s <= 64) {
+              const float x0 = lane < n_tiles_s ? sp[lane * ld] : 0.f;
+              const float x1 = lane + 32 < n_tiles_s ? sp[(lane + 32) * ld] : 0.f;
+              x = x0 + x1;
+            } else {
+              for (int t = lane; t < n_tiles_s; t += 32) x += sp[t * ld];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) rs_s[jj] = rms_scale(x, e.norm_dim, e.eps);
+          }
+          named_barrier_sync(1, 128);
+        }
+        const int d = e.head_dim, half = d >> 1;
+        const bool qk_tile = p.epi == EPI_QKV && n0 < e.q_dim + e.kv_dim;
+        for (int c = 0; c < nchunk; ++c) {
+          float v[16];
+          if (S == 1) {
+            uint32_t r[16];
+            tmem_ld16(tb + static_cast<uint32_t>(c * 16), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int rr = 0; rr < S; ++rr) {  // split order
+              const float* ps = p.ws + (tile_id * S + rr) * slot_floats + static_cast<size_t>(c * 16) * kGemmTileN + f;
+              float t[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) t[i] = __ldcg(ps + i * kGemmTileN);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += t[i];
+            }
+          }
+          if (p.epi == EPI_F32) {
+            float* out = e.out_f32;
+            if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
+            const int n_rows = e.rows_valid != nullptr ? min(m_valid, *e.rows_valid - tok0) : m_valid;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              if (jj >= n_rows) continue;
+              float val = v[i];
+              if (scaled) val *= rs_s[jj];
+              out[static_cast<size_t>(tok0 + jj) * e.ldo + n0 + f] = val;
+            }
+          } else if (p.epi == EPI_RESID) {
+            T* xo = reinterpret_cast<T*>(e.xn_out);
+            const float gam = e.gamma_next[n0 + f];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              float sq = 0.f;
+              if (jj < m_valid) {
+                const size_t gi = static_cast<size_t>(tok0 + jj) * e.resid_dim + n0 + f;
+                const float rn = e.resid[gi] + v[i];
+                e.resid[gi] = rn;
+                xo[gi] = Cvt<T>::from_f(rn * gam);
+                sq = rn * rn;
+              }
+              xchg[i * kGemmTileN + f] = sq;
+            }
+            named_barrier_sync(1, 128);
+            for (int i = ew; i < 16; i += 4) {
+              const int jj = c * 16 + i;
+              const float* tr = xchg + i * kGemmTileN;
+              float sm = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+              if (lane == 0 && jj < m_valid) e.sumsq_out[static_cast<size_t>(w.tn) * e.sumsq_ld + tok0 + jj] = sm;
+            }
+            named_barrier_sync(1, 128);
+          } else if (p.epi == EPI_SWIGLU) {
+            T* ao = reinterpret_cast<T*>(e.act_out);
+            if (q >= 2) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) xchg[i * kGemmTileN + f] = v[i];  // up rows
+            }
+            named_barrier_sync(1, 128);
+            if (q < 2) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int jj = c * 16 + i;
+                if (jj >= m_valid) continue;
+                const float sc = scaled ? rs_s[jj] : 1.f;
+                const float g = v[i] * sc;
+                const float up = xchg[i * kGemmTileN + 64 + f] * sc;
+                ao[static_cast<size_t>(tok0 + jj) * e.ffn + w.tn * 64 + f] = Cvt<T>::from_f(silu_mul(g, up));
+              }
+            }
+            named_barrier_sync(1, 128);
+          } else if (qk_tile) {
+            // q and k columns: RoPE pairs (i, i + d/2) of each head, partners exchanged
+            T* qo = reinterpret_cast<T*>(e.q_out);
+            T* kp = reinterpret_cast<T*>(e.k_pool);
+            const int hf = f % d, ip = hf % half;
+            const bool lo = hf < half;
+            const int partner = lo ? f + half : f - half;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              xchg[i * kGemmTileN + f] = jj < m_valid ? v[i] * (scaled ? rs_s[jj] : 1.f) : 0.f;
+            }
+            named_barrier_sync(1, 128);
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              if (jj >= m_valid) continue;
+              const int tok = tok0 + jj;
+              const float x = xchg[i * kGemmTileN + f], xp = xchg[i * kGemmTileN + partner];
+              const size_t o = static_cast<size_t>(tok) * half + ip;
+              const float cs = e.rope_cos[o], sn = e.rope_sin[o];
+              const float y = lo ? rope_lo(x, xp, cs, sn) : rope_hi(xp, x, cs, sn);
+              if (n0 < e.q_dim) {
+                qo[static_cast<size_t>(tok) * e.q_dim + n0 + f] = Cvt<T>::from_f(y);
+              } else {
+                const long long slot = e.slot_mapping[tok];
+                if (slot < 0 || slot >= e.pool_slots) {
+                  set_err(p.err, NS_DEV_BAD_SLOT);
+                  continue;
+                }
+                const int col = n0 - e.q_dim + f;
+                const size_t base = ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + col / d) *
+                                         e.block_size + static_cast<size_t>(slot % e.block_size)) * d;
+                const T kv = Cvt<T>::from_f(y);
+                kp[base + hf] = kv;
+                if (e.kv_stage != nullptr)
+                  reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok) * 2 * e.kv_dim + col] = kv;
+              }
+            }
+            named_barrier_sync(1, 128);
+          } else {
+            // v columns
+            T* vp = reinterpret_cast<T*>(e.v_pool);
+            const int col = n0 - e.q_dim - e.kv_dim + f;
+            const int kvh = col / d, dim = col - kvh * d;
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              if (jj >= m_valid) continue;
+              const int tok = tok0 + jj;
+              const long long slot = e.slot_mapping[tok];
+              if (slot < 0 || slot >= e.pool_slots) {
+                set_err(p.err, NS_DEV_BAD_SLOT);
+                continue;
+              }
+              const T val = Cvt<T>::from_f(v[i] * (scaled ? rs_s[jj] : 1.f));
+              vp[((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                  static_cast<size_t>(slot % e.block_size)) * d + dim] = val;
+              if (e.kv_stage != nullptr)
+                reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok) * 2 * e.kv_dim + e.kv_dim + col] = val;
+            }
+          }
+        }
+        if (p.epi == EPI_RESID || p.epi == EPI_SWIGLU) fence_proxy_async_global();
+        if (S == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
+      }
+      named_barrier_sync(1, 128);  // rs_s, xchg and the flag are reused by the next unit
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // Let this CTA's own copies in flight land before its shared memory is released.
+    const int n_issued = *issued;
+    for (int i = max(0, n_issued - ns); i < n_issued; ++i) {
+      (void)mbar_wait(&full[i % ns], static_cast<uint32_t>(i / ns) & 1u, nullptr);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * ncols);
+  }
+}
+
 // ------------------------------------------------------------------------------ host side
 
 size_t gemm_smem_bytes(int BN, int nstage) {
@@ -582,7 +1026,7 @@ size_t gemm_smem_bytes(int BN, int nstage) {
 
 namespace {
 
-// Raise the kernel's dynamic shared-memory limit once per device (threads may race to do it;
+// Raise the kernels' dynamic shared-memory limit once per device (threads may race to do it;
 // setting the attribute twice is harmless).
 template <typename T>
 cudaError_t gemm_configure() {
@@ -593,6 +1037,9 @@ cudaError_t gemm_configure() {
   if (bit == 0 || !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_persistent_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
   }
@@ -700,6 +1147,56 @@ cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const 
                         int dtype, cudaStream_t s, bool pdl) {
   if (dtype == NS_BF16) return launch_gemm_t<__nv_bfloat16>(mapA, mapB, p, s, pdl);
   return launch_gemm_t<__half>(mapA, mapB, p, s, pdl);
+}
+
+namespace {
+size_t gemm_persistent_smem(int BN, int nstage) {
+  return 1024 + static_cast<size_t>(nstage) * (kABytes + static_cast<size_t>(BN) * kGemmTileK * 2) +
+         kXchgFloats * sizeof(float) + kCtrlBytes;
+}
+}  // namespace
+
+// As many stages as fit next to the exchange buffer and the control block (at most 8).
+int gemm_persistent_stages(int BN) {
+  const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
+  const size_t room = 227 * 1024 - 1024 - kXchgFloats * sizeof(float) - kCtrlBytes;
+  return std::max(2, std::min(8, static_cast<int>(room / stage)));
+}
+
+size_t gemm_persistent_ws_floats(int tiles_m, int N, int splits, int BN) {
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(tiles_m) * (N / kGemmTileN) * splits * BN * kGemmTileN;
+}
+
+namespace {
+template <typename T>
+cudaError_t launch_gemm_persistent_t(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                                     int grid, cudaStream_t s, bool pdl) {
+  cudaError_t e = gemm_configure<T>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = gemm_persistent_smem(p.BN, p.nstage);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<T>, *mapA, *mapB, p);
+}
+}  // namespace
+
+cudaError_t launch_gemm_persistent(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
+                                   int dtype, int grid, cudaStream_t s, bool pdl) {
+  if (gemm_persistent_smem(p.BN, p.nstage) > 227 * 1024) return cudaErrorInvalidValue;
+  if (dtype == NS_BF16) return launch_gemm_persistent_t<__nv_bfloat16>(mapA, mapB, p, grid, s, pdl);
+  return launch_gemm_persistent_t<__half>(mapA, mapB, p, grid, s, pdl);
 }
 
 }  // namespace ns

@@ -119,6 +119,29 @@ int pick_bn(int m, int kb_per_split, int splits, int n_tiles, int sms) {
   return cost(narrow) * 10 <= cost(wide) * 9 ? narrow : wide;
 }
 
+// Token tile of the persistent GEMM (launches of more than 64 rows, one CTA per SM): 128 or
+// 256 tokens, whichever gives the cheaper busiest CTA, charging a unit per k-block the longer
+// of its tensor work (proportional to the tile) and its operand loads (the 16 KiB weight tile
+// plus the activation tile, both through the stage ring), plus a fixed cost per unit for the
+// pipeline's fill and the epilogue.  The tile never changes a result.
+int pick_bn_persistent(int m, int kb_per_split, int splits, int n_tiles, int sms) {
+  int best = 0;
+  double best_cost = 0.0;
+  for (int cap : {128, 256}) {
+    const int bn = pick_bn_capped(m, cap);
+    const long long units = static_cast<long long>((m + bn - 1) / bn) * splits * n_tiles;
+    const long long per_cta = (units + sms - 1) / sms;
+    const double mma = bn / 256.0 * 0.375;            // us per k-block at the SM's tensor rate
+    const double load = (16.0 + bn / 8.0) / 110.0;    // us per k-block at ~110 GB/s per SM
+    const double cost = per_cta * (kb_per_split * std::max(mma, load) + 1.5);
+    if (best == 0 || cost < best_cost * 0.97) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
 // cluster of a launch is resident at once; at least two k-blocks per split; at most one
 // portable cluster (8 CTAs) per output tile.
@@ -163,6 +186,11 @@ struct DevScratch {
   int* counters = nullptr;
   size_t n_counters = 0;
   int* err = nullptr;
+  // ns_linear's persistent-GEMM workspace and tile counters
+  float* gemm_ws = nullptr;
+  size_t gemm_ws_floats = 0;
+  int* gemm_cnt = nullptr;
+  size_t gemm_cnt_n = 0;
 };
 std::mutex g_scratch_mu;
 DevScratch g_scratch[64];
@@ -193,6 +221,27 @@ ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
     s.n_counters = n_counters;
   }
   *out = &s;
+  return NS_OK;
+}
+
+// Grow the device's ns_linear GEMM workspace (synchronises the device when it grows).
+ns_status scratch_gemm(size_t floats, size_t counters, DevScratch* s) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (s->gemm_ws_floats < floats) {
+    if (s->gemm_ws) cudaFree(s->gemm_ws);
+    s->gemm_ws = nullptr;
+    s->gemm_ws_floats = 0;
+    NS_CUDA(cudaMalloc(&s->gemm_ws, floats * sizeof(float)));
+    s->gemm_ws_floats = floats;
+  }
+  if (s->gemm_cnt_n < counters) {
+    if (s->gemm_cnt) cudaFree(s->gemm_cnt);
+    s->gemm_cnt = nullptr;
+    s->gemm_cnt_n = 0;
+    NS_CUDA(cudaMalloc(&s->gemm_cnt, counters * sizeof(int)));
+    NS_CUDA(cudaMemset(s->gemm_cnt, 0, counters * sizeof(int)));
+    s->gemm_cnt_n = counters;
+  }
   return NS_OK;
 }
 
@@ -366,6 +415,10 @@ struct ns_ctx {
   ns_block_pool pool;
   int* attn_counters = nullptr;
   float* attn_partials = nullptr;
+  // split-K workspace and tile counters of the persistent GEMM, one set per stream of the
+  // nano-batch schedule (nano-batches on the two streams run their GEMMs concurrently)
+  float* gemm_ws[2] = {nullptr, nullptr};
+  int* gemm_cnt[2] = {nullptr, nullptr};
   // metadata
   size_t meta_cap = 0;
   uint8_t* meta_host = nullptr;
@@ -495,25 +548,58 @@ ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
   return NS_OK;
 }
 
-ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
-                      int epi, const EpiArgs& e, cudaStream_t s, int kind) {
+// Launch parameters of one projection over m rows: the cluster kernel up to 64 rows, the
+// persistent kernel above (its grid in *grid, else 0).  Both take the weight's k split.
+GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int sms, int* grid) {
   GemmParams p{};
   p.M = m;
   p.row0 = row0;
   p.N = pr.N;
   p.K = pr.K;
-  p.BN = pick_bn(m, pr.kb_per, pr.splits, pr.N / kGemmTileN, h->sms);
   p.splits = pr.splits;
   p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
   p.epi = epi;
-  p.idesc = gemm_idesc(h->dtype, p.BN);
+  const int n_tiles = pr.N / kGemmTileN;
+  if (m >= kPersistentMinRows) {
+    p.BN = pick_bn_persistent(m, pr.kb_per, pr.splits, n_tiles, sms);
+    p.tiles_m = (m + p.BN - 1) / p.BN;
+    p.nstage = gemm_persistent_stages(p.BN);
+    *grid = static_cast<int>(std::min<long long>(static_cast<long long>(p.tiles_m) * pr.splits * n_tiles, sms));
+  } else {
+    p.BN = pick_bn(m, pr.kb_per, pr.splits, n_tiles, sms);
+    p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * n_tiles, p.splits);
+    *grid = 0;
+  }
+  p.idesc = gemm_idesc(dtype, p.BN);
+  return p;
+}
+
+// Workspace floats and counters the persistent GEMM needs for a projection at up to R rows.
+void proj_ws_need(const Proj& pr, int R, int sms, size_t* floats, size_t* counters) {
+  for (int m = kPersistentMinRows; m <= R; ++m) {
+    const int bn = pick_bn_persistent(m, pr.kb_per, pr.splits, pr.N / kGemmTileN, sms);
+    const int tm = (m + bn - 1) / bn;
+    *floats = std::max(*floats, gemm_persistent_ws_floats(tm, pr.N, pr.splits, bn));
+    if (pr.splits > 1) *counters = std::max(*counters, static_cast<size_t>(tm) * (pr.N / kGemmTileN));
+  }
+}
+
+ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
+                      int epi, const EpiArgs& e, cudaStream_t s, int kind, int ws_idx) {
+  int grid = 0;
+  GemmParams p = proj_params(pr, m, row0, epi, h->dtype, h->sms, &grid);
   p.err = h->err;
   p.e = e;
+  p.ws = h->gemm_ws[ws_idx];
+  p.ws_cnt = h->gemm_cnt[ws_idx];
   const CUtensorMap* mb = nullptr;
   NS_TRY(get_bmap(h, x, x_cols, p.BN, &mb));
   TimeScope ts(h, s, kind);
-  NS_CUDA(launch_gemm(&pr.mapA, mb, p, h->dtype, s, true));
+  if (grid > 0) {
+    NS_CUDA(launch_gemm_persistent(&pr.mapA, mb, p, h->dtype, grid, s, true));
+  } else {
+    NS_CUDA(launch_gemm(&pr.mapA, mb, p, h->dtype, s, true));
+  }
   h->kernels_last++;
   return NS_OK;
 }
@@ -626,7 +712,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.kv_stage = mirror ? static_cast<uint8_t*>(h->kv_stage) + static_cast<size_t>(l) * h->R * kv_row_bytes
                           : nullptr;
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
-                         st[i % 2], K_QKV));
+                         st[i % 2], K_QKV, i % 2));
       NS_CUDA(trace_copy(l, h->trace.q, h->q, q_row_bytes, nb[i].first, nb[i].second, st[i % 2]));
       if (n > 1 || mirror) NS_CUDA(cudaEventRecord(ev_qkv(l, i), st[i % 2]));
       if (mirror) {
@@ -712,13 +798,13 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       eo.sumsq_out = h->sumsq;
       eo.sumsq_ld = h->R;
       eo.resid_dim = H;
-      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O));
+      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O, i % 2));
       NS_CUDA(trace_copy(l, h->trace.resid_mid, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
 
       EpiArgs eg = norm;
       eg.act_out = h->act;
       eg.ffn = F;
-      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, s, K_GU));
+      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, s, K_GU, i % 2));
 
       EpiArgs ed{};
       ed.resid = h->resid;
@@ -727,7 +813,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ed.sumsq_out = h->sumsq;
       ed.sumsq_ld = h->R;
       ed.resid_dim = H;
-      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN));
+      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN, i % 2));
       NS_CUDA(trace_copy(l, h->trace.resid_out, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
     }
   }
@@ -737,7 +823,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     el.rows_valid = m_rows_valid;
     el.ldo = c.vocab;
     NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el,
-                       st[i % 2], K_LM));
+                       st[i % 2], K_LM, i % 2));
   }
   if (n > 1) {
     NS_CUDA(cudaEventRecord(h->events[1], h->side));
@@ -891,6 +977,10 @@ void ns_destroy(ns_handle h) {
   cudaFree(h->pools);
   cudaFree(h->attn_counters);
   cudaFree(h->attn_partials);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(h->gemm_ws[i]);
+    cudaFree(h->gemm_cnt[i]);
+  }
   cudaFreeHost(h->meta_host);
   cudaFree(h->meta_dev);
   cudaFree(h->err);
@@ -1016,6 +1106,17 @@ ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out
   CK(cuda(cudaMemset(h->xn, 0, R * H * e2), "memset"));
   CK(cuda(cudaMemset(h->o, 0, R * qd * e2), "memset"));
   CK(cuda(cudaMemset(h->act, 0, R * F * e2), "memset"));
+  {
+    size_t ws = 0, cnt = 0;
+    for (const LayerDev& L : h->layers)
+      for (const Proj* pr : {&L.qkv, &L.o, &L.gu, &L.down}) proj_ws_need(*pr, h->R, h->sms, &ws, &cnt);
+    proj_ws_need(h->lm, h->R, h->sms, &ws, &cnt);
+    for (int i = 0; i < 2 && ws > 0; ++i) {
+      CK(cuda(cudaMalloc(&h->gemm_ws[i], ws * sizeof(float)), "malloc gemm workspace"));
+      CK(cuda(cudaMalloc(&h->gemm_cnt[i], cnt * sizeof(int)), "malloc gemm counters"));
+      CK(cuda(cudaMemset(h->gemm_cnt[i], 0, cnt * sizeof(int)), "memset"));
+    }
+  }
   // metadata: pinned host staging + device copy, sized for max_batch
   h->meta_cap = meta_layout(h->R, c.max_blocks_per_seq).total;
   CK(cuda(cudaMallocHost(&h->meta_host, h->meta_cap), "pinned metadata"));
@@ -1574,27 +1675,30 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   pr.owned = false;
   pr.N = n;
   pr.K = k;
-  choose_splits(n, k, device_sms(), &pr.splits, &pr.kb_per);
+  const int sms = device_sms();
+  choose_splits(n, k, sms, &pr.splits, &pr.kb_per);
   NS_TRY(make_tmap(&pr.mapA, w, dtype, static_cast<uint64_t>(n), static_cast<uint64_t>(k), kGemmTileN));
-  GemmParams p{};
-  p.M = m;
-  p.row0 = 0;
-  p.N = n;
-  p.K = k;
-  p.BN = pick_bn(m, pr.kb_per, pr.splits, pr.N / kGemmTileN, device_sms());
-  p.splits = pr.splits;
-  p.kb_per_split = pr.kb_per;
-  p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (p.N / kGemmTileN), p.splits);
-  p.epi = EPI_F32;
-  p.idesc = gemm_idesc(dtype, p.BN);
+  int grid = 0;
+  GemmParams p = proj_params(pr, m, 0, EPI_F32, dtype, sms, &grid);
   DevScratch* sc = nullptr;
   NS_TRY(scratch_get(0, 0, &sc));
+  if (grid > 0) {
+    NS_TRY(scratch_gemm(gemm_persistent_ws_floats(p.tiles_m, n, p.splits, p.BN),
+                        pr.splits > 1 ? static_cast<size_t>(p.tiles_m) * (n / kGemmTileN) : 0, sc));
+    p.ws = sc->gemm_ws;
+    p.ws_cnt = sc->gemm_cnt;
+  }
   p.err = sc->err;
   p.e.out_f32 = y;
   p.e.ldo = n;
   CUtensorMap mb;
   NS_TRY(make_tmap(&mb, x, dtype, static_cast<uint64_t>(m), static_cast<uint64_t>(k), static_cast<uint32_t>(p.BN)));
-  NS_CUDA(launch_gemm(&pr.mapA, &mb, p, dtype, reinterpret_cast<cudaStream_t>(stream), false));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (grid > 0) {
+    NS_CUDA(launch_gemm_persistent(&pr.mapA, &mb, p, dtype, grid, st, false));
+  } else {
+    NS_CUDA(launch_gemm(&pr.mapA, &mb, p, dtype, st, false));
+  }
   return NS_OK;
 }
 

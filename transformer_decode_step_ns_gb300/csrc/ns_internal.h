@@ -71,7 +71,14 @@ struct GemmParams {
   uint32_t idesc;
   int* err;
   EpiArgs e;
+  // persistent variant (launches of more than 64 rows)
+  int tiles_m;  // token tiles of BN rows
+  float* ws;    // split-K partials [tiles_m * N/128][splits][BN][128] fp32 (splits > 1)
+  int* ws_cnt;  // [tiles_m * N/128] arrival counters, zero between launches
 };
+
+// Launches of more than this many rows take the persistent GEMM.
+constexpr int kPersistentMinRows = 65;
 
 struct AttnParams {
   const void* q;
