@@ -163,26 +163,32 @@ def test_linear_rows_do_not_depend_on_the_batch(cuda_lib):
         assert torch.equal(part, full[lo:hi])
 
 
-@pytest.mark.parametrize("n,k", [(1152, 896), (384, 512), (19456, 256)])
-def test_linear_rows_are_bitwise_the_same_in_either_gemm_kernel(cuda_lib, n, k):
-    """Up to 64 rows a projection runs the cluster kernel, above it the persistent kernel; both
-    take the weight's k split, the same split order and the same epilogue roundings, so a row's
-    result does not depend on which launch (or batch) it is in.  Shapes with split-K (3 and
-    4 splits) and without."""
+@pytest.mark.parametrize("n,k,m,parts", [
+    # 152 feature tiles: no k split; above 64 rows the persistent kernel
+    (19456, 256, 300, ((0, 40), (40, 300), (7, 71), (100, 229))),
+    # 38 feature tiles, 4 splits: persistent once there are 304 output tiles (>= 1793 rows)
+    (4864, 1024, 2048, ((0, 40), (40, 2048), (100, 1124), (1000, 2048))),
+])
+def test_linear_rows_are_bitwise_the_same_in_either_gemm_kernel(cuda_lib, n, k, m, parts):
+    """Up to 64 rows, and for split weights with few output tiles, a projection runs the
+    cluster kernel; otherwise the persistent kernel.  Both take the weight's k split, the same
+    split order and the same epilogue roundings, so a row's result does not depend on which
+    launch (or batch) it is in."""
     import torch
     from transformer_decode_step_ns_gb300 import _lib
     w = to_dev(synth.normal(12, f"w{n}", (n, k), "bf16", std=0.05))
-    x = synth.normal(12, f"x{n}", (300, k), "bf16")
-    full = torch.empty((300, n), dtype=torch.float32, device="cuda")
-    _lib.linear(w, to_dev(x), full, 300, n, k, "bf16")
-    for lo, hi in ((0, 40), (40, 300), (7, 71), (100, 229)):
+    x = synth.normal(12, f"x{n}", (m, k), "bf16")
+    full = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    _lib.linear(w, to_dev(x), full, m, n, k, "bf16")
+    for lo, hi in parts:
         part = torch.empty((hi - lo, n), dtype=torch.float32, device="cuda")
         _lib.linear(w, to_dev(x[lo:hi]), part, hi - lo, n, k, "bf16")
         torch.cuda.synchronize()
         assert torch.equal(part, full[lo:hi]), (lo, hi)
     assert _lib.device_error() == 0
-    ref = storage_f64(x, "bf16") @ storage_f64(from_dev(w), "bf16").T
-    assert rel_l2(full.cpu().numpy(), ref) < 1e-4
+    rows = np.r_[0:8, m - 8:m]
+    ref = storage_f64(x[rows], "bf16") @ storage_f64(from_dev(w), "bf16").T
+    assert rel_l2(full[rows].cpu().numpy(), ref) < 1e-4
 
 
 def test_greedy_argmax_ties_to_lowest(cuda_lib):

@@ -151,18 +151,20 @@ def test_head_dim_128_over_several_token_tiles(cuda_lib, n_q, n_kv):
 
 
 def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cuda_lib):
-    """300 rows, head_dim 128: unsplit every projection runs the persistent kernel (3 token
-    tiles); as 40 + 260 rows the first nano-batch runs the cluster kernel, and as 100 + 200 both
-    run persistent launches of other tile counts.  Every fused epilogue (QKV with RoPE and the
-    cache write, residual + norm, SwiGLU, the fp32 head) gives each row the same bits."""
-    shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
-                             ffn=768, vocab=640, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
+    """2048 rows of a model whose projections take both GEMM kernels: QKV (40 feature tiles, 3
+    splits) runs persistent at 2048 and 2008 rows and on clusters at 1024 and 40; gate/up
+    (152 tiles) and the head (152 tiles) run persistent above 64 rows; O and down (4 tiles,
+    8 splits) always on clusters.  Unsplit, 40 + 2008 and 1024 + 1024 nano-batches give every
+    row the same logits and cache bits, through every fused epilogue (QKV with RoPE and the
+    cache write, residual + norm, SwiGLU, the fp32 head); sampled rows match the oracle."""
+    shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=32, n_kv_heads=4, head_dim=128,
+                             ffn=9728, vocab=19456, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
                              tie_embeddings=False)
-    ctx = list(synth.uniform_int(83, "ctx300", 300, 0, 70))
-    h = Harness(shape, 84, ctx)
-    got, _ = _check_step(h)
+    ctx = list(synth.uniform_int(85, "ctx2048", 2048, 0, 70))
+    h = Harness(shape, 86, ctx)
+    got = h.run_gpu()
     ks0, vs0 = h.download_pools()
-    for sizes in ([40, 260], [100, 200]):
+    for sizes in ([40, 2008], [1024, 1024]):
         h.upload_pools()
         h.dev.set_nanobatch(sizes)
         np.testing.assert_array_equal(h.run_gpu(), got)
@@ -170,6 +172,15 @@ def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cud
         for l in range(shape.n_layers):
             np.testing.assert_array_equal(ks[l], ks0[l])
             np.testing.assert_array_equal(vs[l], vs0[l])
+    # rows are independent: the oracle on a sample of them, over the same initial cache
+    b = h.batch
+    rows = np.array([0, 1, 39, 40, 1023, 1024, 2047])
+    model = oracle.OracleModel.from_weights(shape, h.w)
+    kp = [a.copy() for a in h.kp]
+    vp = [a.copy() for a in h.vp]
+    ref = oracle.decode_step(model, kp, vp, b.token_ids[rows], b.positions[rows], b.block_tables[rows],
+                             b.seq_lens[rows], b.slot_mapping[rows], h.bs)
+    assert rel_l2(got[rows], ref) < 1e-2 and np.abs(got[rows] - ref).max() < 5e-2
 
 
 def test_graph_replay_equals_eager_bitwise(cuda_lib):

@@ -787,7 +787,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int tok0 = p.row0 + w.tm * BN;
       const int m_valid = min(BN, p.M - w.tm * BN);
       const int nchunk = (m_valid + 15) >> 4;
-      // one thread waits for the accumulator (bounded) and tells the others
+      if (scaled) {
+        // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps) for the unit's tokens,
+        // while the main loop runs: one warp per token, the same fixed shuffle tree as the
+        // cluster kernel, eight tokens' loads in flight at a time
+        const int n_tiles_s = e.sumsq_tiles;
+        const size_t ld = static_cast<size_t>(e.sumsq_ld);
+        for (int g0 = 0; ew + 4 * g0 < m_valid; g0 += 8) {
+          float x[8];
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+            const int jj = ew + 4 * (g0 + uu);
+            const float* sp = e.sumsq_in + tok0 + jj;
+            x[uu] = 0.f;
+            if (jj < m_valid) {
+              if (n_tiles_s <= 64) {
+                const float x0 = lane < n_tiles_s ? sp[lane * ld] : 0.f;
+                const float x1 = lane + 32 < n_tiles_s ? sp[(lane + 32) * ld] : 0.f;
+                x[uu] = x0 + x1;
+              } else {
+                for (int t = lane; t < n_tiles_s; t += 32) x[uu] += sp[t * ld];
+              }
+            }
+          }
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x[uu] += __shfl_xor_sync(0xffffffffu, x[uu], o);
+            const int jj = ew + 4 * (g0 + uu);
+            if (lane == 0 && jj < m_valid) rs_s[jj] = rms_scale(x[uu], e.norm_dim, e.eps);
+          }
+        }
+      }
+      // one thread waits for the accumulator (bounded) and tells the others; the barrier also
+      // publishes rs
       if (et == 0) {
         const bool ok = !*abort_flag && mbar_wait(&acc_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag);
         if (!ok) {
@@ -829,27 +862,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (run_epi) __threadfence();
       }
       if (run_epi) {
-        if (scaled) {
-          // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps), the same fixed
-          // shuffle tree as the cluster kernel (one warp per token)
-          const int n_tiles_s = e.sumsq_tiles;
-          const size_t ld = static_cast<size_t>(e.sumsq_ld);
-          for (int jj = ew; jj < m_valid; jj += 4) {
-            const float* sp = e.sumsq_in + tok0 + jj;
-            float x = 0.f;
-            if (n_tiles_s <= 64) {
-              const float x0 = lane < n_tiles_s ? sp[lane * ld] : 0.f;
-              const float x1 = lane + 32 < n_tiles_s ? sp[(lane + 32) * ld] : 0.f;
-              x = x0 + x1;
-            } else {
-              for (int t = lane; t < n_tiles_s; t += 32) x += sp[t * ld];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) rs_s[jj] = rms_scale(x, e.norm_dim, e.eps);
-          }
-          named_barrier_sync(1, 128);
-        }
         const int d = e.head_dim, half = d >> 1;
         const bool qk_tile = p.epi == EPI_QKV && n0 < e.q_dim + e.kv_dim;
         for (int c = 0; c < nchunk; ++c) {
@@ -863,13 +875,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int rr = 0; rr < S; ++rr) {  // split order
-              const float* ps = p.ws + (tile_id * S + rr) * slot_floats + static_cast<size_t>(c * 16) * kGemmTileN + f;
-              float t[16];
+            for (int r0 = 0; r0 < S; r0 += 4) {  // split order; four splits' loads in flight
+              float t[4][16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) t[i] = __ldcg(ps + i * kGemmTileN);
+              for (int g = 0; g < 4; ++g) {
+                if (r0 + g < S) {
+                  const float* ps = p.ws + (tile_id * S + r0 + g) * slot_floats +
+                                    static_cast<size_t>(c * 16) * kGemmTileN + f;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += t[i];
+                  for (int i = 0; i < 16; ++i) t[g][i] = __ldcg(ps + i * kGemmTileN);
+                }
+              }
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                if (r0 + g < S) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[i] += t[g][i];
+                }
+              }
             }
           }
           if (p.epi == EPI_F32) {
@@ -887,13 +910,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else if (p.epi == EPI_RESID) {
             T* xo = reinterpret_cast<T*>(e.xn_out);
             const float gam = e.gamma_next[n0 + f];
+            float old[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              old[i] = jj < m_valid ? e.resid[static_cast<size_t>(tok0 + jj) * e.resid_dim + n0 + f] : 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int jj = c * 16 + i;
               float sq = 0.f;
               if (jj < m_valid) {
                 const size_t gi = static_cast<size_t>(tok0 + jj) * e.resid_dim + n0 + f;
-                const float rn = e.resid[gi] + v[i];
+                const float rn = old[i] + v[i];
                 e.resid[gi] = rn;
                 xo[gi] = Cvt<T>::from_f(rn * gam);
                 sq = rn * rn;
@@ -936,24 +965,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int hf = f % d, ip = hf % half;
             const bool lo = hf < half;
             const int partner = lo ? f + half : f - half;
+            const bool k_tile = n0 >= e.q_dim;
+            // this chunk's angles and slots, loaded before anything is stored
+            float csv[16], snv[16];
+            long long slv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int jj = c * 16 + i;
+              const int tok = tok0 + min(jj, m_valid - 1);
+              const size_t o = static_cast<size_t>(tok) * half + ip;
+              csv[i] = e.rope_cos[o];
+              snv[i] = e.rope_sin[o];
+              slv[i] = k_tile ? e.slot_mapping[tok] : 0;
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int jj = c * 16 + i;
               xchg[i * kGemmTileN + f] = jj < m_valid ? v[i] * (scaled ? rs_s[jj] : 1.f) : 0.f;
             }
             named_barrier_sync(1, 128);
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int jj = c * 16 + i;
               if (jj >= m_valid) continue;
               const int tok = tok0 + jj;
               const float x = xchg[i * kGemmTileN + f], xp = xchg[i * kGemmTileN + partner];
-              const size_t o = static_cast<size_t>(tok) * half + ip;
-              const float cs = e.rope_cos[o], sn = e.rope_sin[o];
-              const float y = lo ? rope_lo(x, xp, cs, sn) : rope_hi(xp, x, cs, sn);
-              if (n0 < e.q_dim) {
+              const float y = lo ? rope_lo(x, xp, csv[i], snv[i]) : rope_hi(xp, x, csv[i], snv[i]);
+              if (!k_tile) {
                 qo[static_cast<size_t>(tok) * e.q_dim + n0 + f] = Cvt<T>::from_f(y);
               } else {
-                const long long slot = e.slot_mapping[tok];
+                const long long slot = slv[i];
                 if (slot < 0 || slot >= e.pool_slots) {
                   set_err(p.err, NS_DEV_BAD_SLOT);
                   continue;
@@ -973,11 +1014,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             T* vp = reinterpret_cast<T*>(e.v_pool);
             const int col = n0 - e.q_dim - e.kv_dim + f;
             const int kvh = col / d, dim = col - kvh * d;
+            long long slv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) slv[i] = e.slot_mapping[tok0 + min(c * 16 + i, m_valid - 1)];
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int jj = c * 16 + i;
               if (jj >= m_valid) continue;
               const int tok = tok0 + jj;
-              const long long slot = e.slot_mapping[tok];
+              const long long slot = slv[i];
               if (slot < 0 || slot >= e.pool_slots) {
                 set_err(p.err, NS_DEV_BAD_SLOT);
                 continue;

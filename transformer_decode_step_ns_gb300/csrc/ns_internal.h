@@ -77,7 +77,7 @@ struct GemmParams {
   int* ws_cnt;  // [tiles_m * N/128] arrival counters, zero between launches
 };
 
-// Launches of more than this many rows take the persistent GEMM.
+// Launches of fewer rows than this never take the persistent GEMM (its tiles are wide).
 constexpr int kPersistentMinRows = 65;
 
 struct AttnParams {
