@@ -165,15 +165,13 @@ def test_linear_rows_do_not_depend_on_the_batch(cuda_lib):
 
 @pytest.mark.parametrize("n,k,m,parts", [
     # 152 feature tiles: no k split; above 64 rows the persistent kernel
-    (19456, 256, 300, ((0, 40), (40, 300), (7, 71), (100, 229))),
-    # 38 feature tiles, 4 splits: persistent once there are 304 output tiles (>= 1793 rows)
-    (4864, 1024, 2048, ((0, 40), (40, 2048), (100, 1124), (1000, 2048))),
+    (19456, 256, 300, ((0, 40), (40, 300), (7, 71), (100, 229), (0, 65), (64, 128))),
+    (19456, 1024, 1100, ((0, 64), (64, 1100), (300, 812))),
 ])
 def test_linear_rows_are_bitwise_the_same_in_either_gemm_kernel(cuda_lib, n, k, m, parts):
-    """Up to 64 rows, and for split weights with few output tiles, a projection runs the
-    cluster kernel; otherwise the persistent kernel.  Both take the weight's k split, the same
-    split order and the same epilogue roundings, so a row's result does not depend on which
-    launch (or batch) it is in."""
+    """An unsplit weight runs the cluster kernel up to 64 rows and the persistent kernel above;
+    both accumulate the same k-blocks in the same order and apply the same epilogue roundings,
+    so a row's result does not depend on which launch (or batch) it is in."""
     import torch
     from transformer_decode_step_ns_gb300 import _lib
     w = to_dev(synth.normal(12, f"w{n}", (n, k), "bf16", std=0.05))

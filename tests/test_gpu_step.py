@@ -151,12 +151,12 @@ def test_head_dim_128_over_several_token_tiles(cuda_lib, n_q, n_kv):
 
 
 def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cuda_lib):
-    """2048 rows of a model whose projections take both GEMM kernels: QKV (40 feature tiles, 3
-    splits) runs persistent at 2048 and 2008 rows and on clusters at 1024 and 40; gate/up
-    (152 tiles) and the head (152 tiles) run persistent above 64 rows; O and down (4 tiles,
-    8 splits) always on clusters.  Unsplit, 40 + 2008 and 1024 + 1024 nano-batches give every
-    row the same logits and cache bits, through every fused epilogue (QKV with RoPE and the
-    cache write, residual + norm, SwiGLU, the fp32 head); sampled rows match the oracle."""
+    """2048 rows of a model whose unsplit projections (gate/up and the head: 152 feature tiles
+    each) run the persistent kernel above 64 rows and the cluster kernel below, while the split
+    ones (QKV, O, down) always run on clusters.  Unsplit, 40 + 2008 and 1024 + 1024 nano-batches
+    give every row the same logits and cache bits through every fused epilogue (QKV with RoPE and
+    the cache write, residual + norm, SwiGLU with the norm scale, the fp32 head); sampled rows
+    match the oracle."""
     shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=32, n_kv_heads=4, head_dim=128,
                              ffn=9728, vocab=19456, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
                              tie_embeddings=False)
@@ -181,6 +181,25 @@ def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cud
     ref = oracle.decode_step(model, kp, vp, b.token_ids[rows], b.positions[rows], b.block_tables[rows],
                              b.seq_lens[rows], b.slot_mapping[rows], h.bs)
     assert rel_l2(got[rows], ref) < 1e-2 and np.abs(got[rows] - ref).max() < 5e-2
+
+
+def test_wide_hidden_residual_epilogues_in_both_gemm_kernels(cuda_lib):
+    """A hidden size of 19456 (152 feature tiles) leaves the O and down projections unsplit, so
+    above 64 rows their residual + norm epilogue runs in the persistent kernel: 100 rows unsplit
+    and as 20 + 80 nano-batches (the 20 on clusters) give the same bits, and match the oracle."""
+    shape = synth.ModelShape(hidden=19456, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=128,
+                             ffn=64, vocab=256, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
+                             tie_embeddings=False)
+    ctx = list(synth.uniform_int(87, "ctx100", 100, 0, 40))
+    h = Harness(shape, 88, ctx)
+    got, _ = _check_step(h)
+    ks0, vs0 = h.download_pools()
+    h.upload_pools()
+    h.dev.set_nanobatch([20, 80])
+    np.testing.assert_array_equal(h.run_gpu(), got)
+    ks, vs = h.download_pools()
+    np.testing.assert_array_equal(ks[0], ks0[0])
+    np.testing.assert_array_equal(vs[0], vs0[0])
 
 
 def test_graph_replay_equals_eager_bitwise(cuda_lib):

@@ -591,19 +591,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 }
 
 // ------------------------------------------------------------------------------ persistent
-// Launches of more than 64 rows (the ridge point and the compute-bound dense batches of the
-// NanoFlow page) run a persistent variant: one CTA per SM loops over work units (token tile,
-// k split, 128-feature tile), token tiles fastest so CTAs running side by side share a weight
-// tile through L2.  The TMA warp streams every unit's stages through one deep ring without
-// stopping between units; the MMA warp alternates between two TMEM accumulators, so the
-// epilogue of one unit overlaps the main loop of the next.  Split-K partials go to a global
-// workspace [tile][split][BN][128] fp32; the split that arrives last (an atomic counter per
-// tile, reset by it for the next launch) sums them in split order, exactly as the cluster
-// kernel does, and runs the fused epilogue for the whole tile from registers (a thread holds one
-// feature of 16 tokens; RoPE pairs, gate/up pairs and the per-token sums of squares are
-// exchanged through a 16-token shared buffer).  Nothing waits on another CTA, so any grid size
-// is safe.  The k split of a weight, the reduction order and every epilogue formula are those
-// of the cluster kernel, so a row gets the same bits from either.
+// Launches of more than 64 rows of an unsplit weight (the ridge point and the compute-bound
+// dense batches of the NanoFlow page) run a persistent variant: one CTA per SM loops over
+// work units (token tile, 128-feature tile), token tiles fastest so CTAs running side by side
+// share a weight tile through L2.  The TMA warp streams every unit's stages through one deep
+// ring without stopping between units; the MMA warp alternates between two TMEM accumulators,
+// so the epilogue of one unit overlaps the main loop of the next.  The epilogue runs from
+// registers (a thread holds one feature of 16 tokens; RoPE pairs, gate/up pairs and the
+// per-token sums of squares are exchanged through a 16-token shared buffer) with the cluster
+// kernel's formulas and summation orders, so a row gets the same bits from either kernel.
+// Nothing waits on another CTA, so any grid size is safe.
 constexpr int kXchgFloats = 16 * kGemmTileN;  // one 16-token chunk of a tile
 
 template <typename T>
@@ -629,25 +626,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S = p.splits, tiles_m = p.tiles_m, n_tiles = p.N / kGemmTileN;
-  const int n_units = tiles_m * S * n_tiles;
+  const int tiles_m = p.tiles_m, n_tiles = p.N / kGemmTileN;
+  const int n_units = tiles_m * n_tiles;
   const int nkb_total = p.K / kGemmTileK;
   const uint32_t ncols = BN <= 128 ? 128u : 256u;
 
   auto stageA = [&](int st) { return smem + static_cast<size_t>(st) * stage_bytes; };
   auto stageB = [&](int st) { return smem + static_cast<size_t>(st) * stage_bytes + kABytes; };
-  // unit u -> (token tile, split, feature tile); its k-blocks [kb0, kb0 + nkb)
+  // unit u -> (token tile, feature tile); every unit runs all k-blocks
   struct Unit {
-    int tm, sp, tn, kb0, nkb;
+    int tm, tn, kb0, nkb;
   };
   auto unit_of = [&](int u) {
     Unit w;
     w.tm = u % tiles_m;
-    const int r = u / tiles_m;
-    w.sp = r % S;
-    w.tn = r / S;
-    w.kb0 = w.sp * p.kb_per_split;
-    w.nkb = min(p.kb_per_split, nkb_total - w.kb0);
+    w.tn = u / tiles_m;
+    w.kb0 = 0;
+    w.nkb = nkb_total;
     return w;
   };
 
@@ -789,34 +784,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int nchunk = (m_valid + 15) >> 4;
       if (scaled) {
         // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps) for the unit's tokens,
-        // while the main loop runs: one warp per token, the same fixed shuffle tree as the
-        // cluster kernel, eight tokens' loads in flight at a time
+        // while the main loop runs.  One thread per token with all its loads in flight; the sum
+        // follows the cluster kernel's shuffle tree exactly: lane l first adds partials
+        // l, l + 32, l + 64, ... in order, then the xor tree halves the lanes (lane l + o into
+        // lane l for o = 16, 8, 4, 2, 1), so the result is bitwise the same.
         const int n_tiles_s = e.sumsq_tiles;
         const size_t ld = static_cast<size_t>(e.sumsq_ld);
-        for (int g0 = 0; ew + 4 * g0 < m_valid; g0 += 8) {
-          float x[8];
+        for (int jj = et; jj < m_valid; jj += 128) {
+          const float* sp = e.sumsq_in + tok0 + jj;
+          float x[32];
+          if (n_tiles_s <= 64) {
+            float x0[32], x1[32];
 #pragma unroll
-          for (int uu = 0; uu < 8; ++uu) {
-            const int jj = ew + 4 * (g0 + uu);
-            const float* sp = e.sumsq_in + tok0 + jj;
-            x[uu] = 0.f;
-            if (jj < m_valid) {
-              if (n_tiles_s <= 64) {
-                const float x0 = lane < n_tiles_s ? sp[lane * ld] : 0.f;
-                const float x1 = lane + 32 < n_tiles_s ? sp[(lane + 32) * ld] : 0.f;
-                x[uu] = x0 + x1;
-              } else {
-                for (int t = lane; t < n_tiles_s; t += 32) x[uu] += sp[t * ld];
-              }
+            for (int l = 0; l < 32; ++l) {
+              x0[l] = l < n_tiles_s ? sp[l * ld] : 0.f;
+              x1[l] = l + 32 < n_tiles_s ? sp[(l + 32) * ld] : 0.f;
+            }
+#pragma unroll
+            for (int l = 0; l < 32; ++l) x[l] = x0[l] + x1[l];
+          } else {
+#pragma unroll
+            for (int l = 0; l < 32; ++l) {
+              x[l] = 0.f;
+              for (int t = l; t < n_tiles_s; t += 32) x[l] += sp[t * ld];
             }
           }
 #pragma unroll
-          for (int uu = 0; uu < 8; ++uu) {
+          for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x[uu] += __shfl_xor_sync(0xffffffffu, x[uu], o);
-            const int jj = ew + 4 * (g0 + uu);
-            if (lane == 0 && jj < m_valid) rs_s[jj] = rms_scale(x[uu], e.norm_dim, e.eps);
+            for (int l = 0; l < o; ++l) x[l] = x[l] + x[l + o];
           }
+          rs_s[jj] = rms_scale(x[0], e.norm_dim, e.eps);
         }
       }
       // one thread waits for the accumulator (bounded) and tells the others; the barrier also
@@ -833,67 +831,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!*epi_flag) break;
       tc_fence_after();
       const uint32_t tb = tmem + static_cast<uint32_t>(b) * ncols + (static_cast<uint32_t>(q * 32) << 16);
-      const size_t tile_id = static_cast<size_t>(w.tn) * tiles_m + w.tm;
-      const size_t slot_floats = static_cast<size_t>(BN) * kGemmTileN;
-      bool run_epi = true;
-      if (S > 1) {
-        // this split's partial -> workspace; the accumulator is free again
-        float* mine = p.ws + (tile_id * S + w.sp) * slot_floats;
-        for (int c = 0; c < nchunk; ++c) {
-          uint32_t r[16];
-          tmem_ld16(tb + static_cast<uint32_t>(c * 16), r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) __stcg(&mine[(c * 16 + i) * kGemmTileN + f], __uint_as_float(r[i]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
-        __threadfence();
-        named_barrier_sync(1, 128);
-        if (et == 0) {
-          const int old = atomicAdd(&p.ws_cnt[tile_id], 1);
-          const int last = old == S - 1;
-          if (last) p.ws_cnt[tile_id] = 0;  // ready for the next launch
-          *epi_flag = last;
-        }
-        named_barrier_sync(1, 128);
-        run_epi = *epi_flag != 0;
-        if (run_epi) __threadfence();
-      }
-      if (run_epi) {
+      {
         const int d = e.head_dim, half = d >> 1;
         const bool qk_tile = p.epi == EPI_QKV && n0 < e.q_dim + e.kv_dim;
         for (int c = 0; c < nchunk; ++c) {
           float v[16];
-          if (S == 1) {
+          {
             uint32_t r[16];
             tmem_ld16(tb + static_cast<uint32_t>(c * 16), r);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int r0 = 0; r0 < S; r0 += 4) {  // split order; four splits' loads in flight
-              float t[4][16];
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                if (r0 + g < S) {
-                  const float* ps = p.ws + (tile_id * S + r0 + g) * slot_floats +
-                                    static_cast<size_t>(c * 16) * kGemmTileN + f;
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) t[g][i] = __ldcg(ps + i * kGemmTileN);
-                }
-              }
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                if (r0 + g < S) {
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += t[g][i];
-                }
-              }
-            }
           }
           if (p.epi == EPI_F32) {
             float* out = e.out_f32;
@@ -1036,11 +984,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (p.epi == EPI_RESID || p.epi == EPI_SWIGLU) fence_proxy_async_global();
-        if (S == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[b]);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
       }
       named_barrier_sync(1, 128);  // rs_s, xchg and the flag are reused by the next unit
     }
@@ -1206,11 +1152,6 @@ int gemm_persistent_stages(int BN) {
   const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
   const size_t room = 227 * 1024 - 1024 - kXchgFloats * sizeof(float) - kCtrlBytes;
   return std::max(2, std::min(8, static_cast<int>(room / stage)));
-}
-
-size_t gemm_persistent_ws_floats(int tiles_m, int N, int splits, int BN) {
-  if (splits <= 1) return 0;
-  return static_cast<size_t>(tiles_m) * (N / kGemmTileN) * splits * BN * kGemmTileN;
 }
 
 namespace {

@@ -125,16 +125,12 @@ int pick_bn(int m, int kb_per_split, int splits, int n_tiles, int sms) {
 // 2048: 256-token tiles beat 128-token ones in every case, by up to 1.9x).
 int pick_bn_persistent(int m) { return pick_bn_capped(m, kMaxBN); }
 
-// The persistent kernel takes a launch of more than 64 rows when the weight is not split, or
-// when there are at least two output tiles per SM so the split-K reduction of one tile
-// overlaps the main loop of the next; otherwise the cluster kernel's distributed-shared-memory
-// reduction is cheaper (measured: split-K projections at 256 rows 27-48 us in the cluster
-// kernel against 50-68 us persistent).  Both give a row the same bits.
-bool use_persistent(int m, int splits, int n_tiles, int sms) {
-  if (m < kPersistentMinRows) return false;
-  const long long tiles = static_cast<long long>((m + kMaxBN - 1) / kMaxBN) * n_tiles;
-  return splits == 1 || tiles >= 2LL * sms;
-}
+// The persistent kernel takes a launch of more than 64 rows when the weight is not split.  A
+// split weight stays on the cluster kernel, whose distributed-shared-memory reduction is
+// cheaper than the persistent kernel's reduction through global memory (measured: the
+// LLaMA-3-8B split-K projections at 256 rows 27-48 us against 50-68 us, the 70B-shaped O
+// projection at 2048 rows 370 against 415 us).  Both give a row the same bits.
+bool use_persistent(int m, int splits) { return m >= kPersistentMinRows && splits == 1; }
 
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
 // cluster of a launch is resident at once; at least two k-blocks per split; at most one
@@ -180,11 +176,6 @@ struct DevScratch {
   int* counters = nullptr;
   size_t n_counters = 0;
   int* err = nullptr;
-  // ns_linear's persistent-GEMM workspace and tile counters
-  float* gemm_ws = nullptr;
-  size_t gemm_ws_floats = 0;
-  int* gemm_cnt = nullptr;
-  size_t gemm_cnt_n = 0;
 };
 std::mutex g_scratch_mu;
 DevScratch g_scratch[64];
@@ -215,27 +206,6 @@ ns_status scratch_get(size_t bytes, size_t n_counters, DevScratch** out) {
     s.n_counters = n_counters;
   }
   *out = &s;
-  return NS_OK;
-}
-
-// Grow the device's ns_linear GEMM workspace (synchronises the device when it grows).
-ns_status scratch_gemm(size_t floats, size_t counters, DevScratch* s) {
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (s->gemm_ws_floats < floats) {
-    if (s->gemm_ws) cudaFree(s->gemm_ws);
-    s->gemm_ws = nullptr;
-    s->gemm_ws_floats = 0;
-    NS_CUDA(cudaMalloc(&s->gemm_ws, floats * sizeof(float)));
-    s->gemm_ws_floats = floats;
-  }
-  if (s->gemm_cnt_n < counters) {
-    if (s->gemm_cnt) cudaFree(s->gemm_cnt);
-    s->gemm_cnt = nullptr;
-    s->gemm_cnt_n = 0;
-    NS_CUDA(cudaMalloc(&s->gemm_cnt, counters * sizeof(int)));
-    NS_CUDA(cudaMemset(s->gemm_cnt, 0, counters * sizeof(int)));
-    s->gemm_cnt_n = counters;
-  }
   return NS_OK;
 }
 
@@ -409,10 +379,6 @@ struct ns_ctx {
   ns_block_pool pool;
   int* attn_counters = nullptr;
   float* attn_partials = nullptr;
-  // split-K workspace and tile counters of the persistent GEMM, one set per stream of the
-  // nano-batch schedule (nano-batches on the two streams run their GEMMs concurrently)
-  float* gemm_ws[2] = {nullptr, nullptr};
-  int* gemm_cnt[2] = {nullptr, nullptr};
   // metadata
   size_t meta_cap = 0;
   uint8_t* meta_host = nullptr;
@@ -542,8 +508,8 @@ ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
   return NS_OK;
 }
 
-// Launch parameters of one projection over m rows: the cluster kernel up to 64 rows, the
-// persistent kernel above (its grid in *grid, else 0).  Both take the weight's k split.
+// Launch parameters of one projection over m rows: the persistent kernel for more than 64 rows
+// of an unsplit weight (its grid in *grid), else the cluster kernel (*grid = 0).
 GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int sms, int* grid) {
   GemmParams p{};
   p.M = m;
@@ -554,11 +520,11 @@ GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int 
   p.kb_per_split = pr.kb_per;
   p.epi = epi;
   const int n_tiles = pr.N / kGemmTileN;
-  if (use_persistent(m, pr.splits, n_tiles, sms)) {
+  if (use_persistent(m, pr.splits)) {
     p.BN = pick_bn_persistent(m);
     p.tiles_m = (m + p.BN - 1) / p.BN;
     p.nstage = gemm_persistent_stages(p.BN);
-    *grid = static_cast<int>(std::min<long long>(static_cast<long long>(p.tiles_m) * pr.splits * n_tiles, sms));
+    *grid = static_cast<int>(std::min<long long>(static_cast<long long>(p.tiles_m) * n_tiles, sms));
   } else {
     p.BN = pick_bn(m, pr.kb_per, pr.splits, n_tiles, sms);
     p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * n_tiles, p.splits);
@@ -568,25 +534,12 @@ GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int 
   return p;
 }
 
-// Workspace floats and counters the persistent GEMM needs for a projection at up to R rows.
-void proj_ws_need(const Proj& pr, int R, int sms, size_t* floats, size_t* counters) {
-  for (int m = kPersistentMinRows; m <= R; ++m) {
-    if (!use_persistent(m, pr.splits, pr.N / kGemmTileN, sms)) continue;
-    const int bn = pick_bn_persistent(m);
-    const int tm = (m + bn - 1) / bn;
-    *floats = std::max(*floats, gemm_persistent_ws_floats(tm, pr.N, pr.splits, bn));
-    if (pr.splits > 1) *counters = std::max(*counters, static_cast<size_t>(tm) * (pr.N / kGemmTileN));
-  }
-}
-
 ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int row0, int m,
-                      int epi, const EpiArgs& e, cudaStream_t s, int kind, int ws_idx) {
+                      int epi, const EpiArgs& e, cudaStream_t s, int kind) {
   int grid = 0;
   GemmParams p = proj_params(pr, m, row0, epi, h->dtype, h->sms, &grid);
   p.err = h->err;
   p.e = e;
-  p.ws = h->gemm_ws[ws_idx];
-  p.ws_cnt = h->gemm_cnt[ws_idx];
   const CUtensorMap* mb = nullptr;
   NS_TRY(get_bmap(h, x, x_cols, p.BN, &mb));
   TimeScope ts(h, s, kind);
@@ -707,7 +660,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       e.kv_stage = mirror ? static_cast<uint8_t*>(h->kv_stage) + static_cast<size_t>(l) * h->R * kv_row_bytes
                           : nullptr;
       NS_TRY(launch_proj(h, L.qkv, h->xn, H, nb[i].first, nb[i].second, EPI_QKV, e,
-                         st[i % 2], K_QKV, i % 2));
+                         st[i % 2], K_QKV));
       NS_CUDA(trace_copy(l, h->trace.q, h->q, q_row_bytes, nb[i].first, nb[i].second, st[i % 2]));
       if (n > 1 || mirror) NS_CUDA(cudaEventRecord(ev_qkv(l, i), st[i % 2]));
       if (mirror) {
@@ -793,13 +746,13 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       eo.sumsq_out = h->sumsq;
       eo.sumsq_ld = h->R;
       eo.resid_dim = H;
-      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O, i % 2));
+      NS_TRY(launch_proj(h, L.o, h->o, qd, nb[i].first, nb[i].second, EPI_RESID, eo, s, K_O));
       NS_CUDA(trace_copy(l, h->trace.resid_mid, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
 
       EpiArgs eg = norm;
       eg.act_out = h->act;
       eg.ffn = F;
-      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, s, K_GU, i % 2));
+      NS_TRY(launch_proj(h, L.gu, h->xn, H, nb[i].first, nb[i].second, EPI_SWIGLU, eg, s, K_GU));
 
       EpiArgs ed{};
       ed.resid = h->resid;
@@ -808,7 +761,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ed.sumsq_out = h->sumsq;
       ed.sumsq_ld = h->R;
       ed.resid_dim = H;
-      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN, i % 2));
+      NS_TRY(launch_proj(h, L.down, h->act, F, nb[i].first, nb[i].second, EPI_RESID, ed, s, K_DOWN));
       NS_CUDA(trace_copy(l, h->trace.resid_out, h->resid, r_row_bytes, r_lo, r_hi - r_lo, s));
     }
   }
@@ -818,7 +771,7 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
     el.rows_valid = m_rows_valid;
     el.ldo = c.vocab;
     NS_TRY(launch_proj(h, h->lm, h->xn, H, nb[i].first, nb[i].second, EPI_F32, el,
-                       st[i % 2], K_LM, i % 2));
+                       st[i % 2], K_LM));
   }
   if (n > 1) {
     NS_CUDA(cudaEventRecord(h->events[1], h->side));
@@ -972,10 +925,6 @@ void ns_destroy(ns_handle h) {
   cudaFree(h->pools);
   cudaFree(h->attn_counters);
   cudaFree(h->attn_partials);
-  for (int i = 0; i < 2; ++i) {
-    cudaFree(h->gemm_ws[i]);
-    cudaFree(h->gemm_cnt[i]);
-  }
   cudaFreeHost(h->meta_host);
   cudaFree(h->meta_dev);
   cudaFree(h->err);
@@ -1101,17 +1050,6 @@ ns_status ns_create(const ns_model_cfg* cfg, const ns_weights* w, ns_handle* out
   CK(cuda(cudaMemset(h->xn, 0, R * H * e2), "memset"));
   CK(cuda(cudaMemset(h->o, 0, R * qd * e2), "memset"));
   CK(cuda(cudaMemset(h->act, 0, R * F * e2), "memset"));
-  {
-    size_t ws = 0, cnt = 0;
-    for (const LayerDev& L : h->layers)
-      for (const Proj* pr : {&L.qkv, &L.o, &L.gu, &L.down}) proj_ws_need(*pr, h->R, h->sms, &ws, &cnt);
-    proj_ws_need(h->lm, h->R, h->sms, &ws, &cnt);
-    for (int i = 0; i < 2 && ws > 0; ++i) {
-      CK(cuda(cudaMalloc(&h->gemm_ws[i], ws * sizeof(float)), "malloc gemm workspace"));
-      CK(cuda(cudaMalloc(&h->gemm_cnt[i], cnt * sizeof(int)), "malloc gemm counters"));
-      CK(cuda(cudaMemset(h->gemm_cnt[i], 0, cnt * sizeof(int)), "memset"));
-    }
-  }
   // metadata: pinned host staging + device copy, sized for max_batch
   h->meta_cap = meta_layout(h->R, c.max_blocks_per_seq).total;
   CK(cuda(cudaMallocHost(&h->meta_host, h->meta_cap), "pinned metadata"));
@@ -1677,12 +1615,6 @@ ns_status ns_linear(const void* w, const void* x, float* y, int m, int n, int k,
   GemmParams p = proj_params(pr, m, 0, EPI_F32, dtype, sms, &grid);
   DevScratch* sc = nullptr;
   NS_TRY(scratch_get(0, 0, &sc));
-  if (grid > 0) {
-    NS_TRY(scratch_gemm(gemm_persistent_ws_floats(p.tiles_m, n, p.splits, p.BN),
-                        pr.splits > 1 ? static_cast<size_t>(p.tiles_m) * (n / kGemmTileN) : 0, sc));
-    p.ws = sc->gemm_ws;
-    p.ws_cnt = sc->gemm_cnt;
-  }
   p.err = sc->err;
   p.e.out_f32 = y;
   p.e.ldo = n;

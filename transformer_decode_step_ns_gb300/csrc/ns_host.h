@@ -15,10 +15,9 @@ int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits);
 uint32_t gemm_idesc(int dtype, int BN);
 cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                         int dtype, cudaStream_t s, bool pdl);
-// Persistent variant: `grid` CTAs (at most one per SM) over tiles_m * splits * N/128 units;
-// p.nstage from gemm_persistent_stages.  Workspace floats / counters a launch needs.
+// Persistent variant for unsplit weights: `grid` CTAs (at most one per SM) over
+// tiles_m * N/128 units; p.nstage from gemm_persistent_stages.
 int gemm_persistent_stages(int BN);
-size_t gemm_persistent_ws_floats(int tiles_m, int N, int splits, int BN);
 cudaError_t launch_gemm_persistent(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                                    int dtype, int grid, cudaStream_t s, bool pdl);
 

@@ -71,10 +71,7 @@ struct GemmParams {
   uint32_t idesc;
   int* err;
   EpiArgs e;
-  // persistent variant (launches of more than 64 rows)
-  int tiles_m;  // token tiles of BN rows
-  float* ws;    // split-K partials [tiles_m * N/128][splits][BN][128] fp32 (splits > 1)
-  int* ws_cnt;  // [tiles_m * N/128] arrival counters, zero between launches
+  int tiles_m;  // persistent variant: token tiles of BN rows
 };
 
 // Launches of fewer rows than this never take the persistent GEMM (its tiles are wide).
