@@ -415,10 +415,14 @@ class AttentionWorkload:
 
     n_q, n_kv, d, bs, mb = 32, 8, 128, 16, 512
 
-    def __init__(self, max_batch: int = 512, pool_blocks: int = 160_000):
+    def __init__(self, max_batch: int = 512, pool_blocks: int = 160_000, ctx_mix: str = "cfg2"):
         import torch
         seed = synth.config_seed(2)
-        self.ctx = synth.ctx_log_uniform(seed, "cfg2.ctx", max_batch, 512, 8192)
+        if ctx_mix == "cfg4":  # the continuous LLaMA-3-8B run's first-step contexts (+ this token)
+            self.ctx = synth.ctx_uniform(synth.config_seed(4), "cfg4.join.ctx", max_batch, 512, 4096) + 1
+        else:
+            self.ctx = synth.ctx_log_uniform(seed, "cfg2.ctx", max_batch, 512, 8192)
+        self.ctx_mix = ctx_mix
         need = [int(math.ceil(c / self.bs)) for c in self.ctx]
         nb = max(pool_blocks, sum(need) + 1)
         self.nb = nb
@@ -485,8 +489,10 @@ class AttentionWorkload:
     def report(self, B, steps, warmup, hbm):
         ms = self.back_to_back(B, max(steps, 10), warmup)
         nbytes = self.nbytes(B)
+        mix = ("ctx uniform[513,4097] (the continuous run's first step)" if self.ctx_mix == "cfg4"
+               else "ctx log-uniform[512,8192]")
         return {"workload": f"paged GQA decode attention, batch {B}, 32Q/8KV, d128, bf16, "
-                            f"ctx log-uniform[512,8192], {self.nb}-block pool",
+                            f"{mix}, {self.nb}-block pool",
                 "gbs": nbytes / (ms * 1e-3) / 1e9, "ms_per_launch": ms,
                 "bytes_per_launch": nbytes, "launches": max(steps, 10),
                 "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
@@ -1647,7 +1653,7 @@ def run_attention_only(args, rank, world):
     peaks, src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     B = args.attn_batch
-    aw = AttentionWorkload(max_batch=B, pool_blocks=args.attn_pool_blocks)
+    aw = AttentionWorkload(max_batch=B, pool_blocks=args.attn_pool_blocks, ctx_mix=args.attn_ctx)
     r = aw.report(B, args.steps, args.warmup, hbm)
     if rank != 0:
         return
@@ -1657,7 +1663,9 @@ def run_attention_only(args, rank, world):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": r["workload"], "l2": r["l2"]},
             "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": hbm, "unit": "GB/s",
-                         "frac": r["frac_of_hbm"], "traffic": read_traffic(f"attention_cfg2_b{B}"),
+                         "frac": r["frac_of_hbm"],
+                         "traffic": (scaled_traffic("attention_cfg4", r["bytes_per_launch"])
+                                     if args.attn_ctx == "cfg4" else read_traffic(f"attention_cfg2_b{B}")),
                          "peak_source": src},
             "device_error": _lib.device_error()}
     print(json.dumps(line), flush=True)
@@ -1788,6 +1796,9 @@ def main():
                     help="time the paged attention workload alone at --attn-batch")
     ap.add_argument("--attn-batch", type=int, default=256)
     ap.add_argument("--attn-pool-blocks", type=int, default=160_000)
+    ap.add_argument("--attn-ctx", default="cfg2", choices=["cfg2", "cfg4"],
+                    help="context mix of --attention-only: the attention workload's own, or the "
+                         "continuous LLaMA-3-8B run's")
     ap.add_argument("--skip-qwen", action="store_true")
     ap.add_argument("--skip-small", action="store_true")
     ap.add_argument("--skip-offload", action="store_true")

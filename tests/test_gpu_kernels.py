@@ -164,13 +164,13 @@ def test_linear_rows_do_not_depend_on_the_batch(cuda_lib):
 
 
 @pytest.mark.parametrize("n,k,m,parts", [
-    # 152 feature tiles: no k split; above 64 rows the persistent kernel
-    (19456, 256, 300, ((0, 40), (40, 300), (7, 71), (100, 229), (0, 65), (64, 128))),
+    # 152 feature tiles: no k split; persistent from two 256-token tiles (257 rows) on
+    (19456, 256, 600, ((0, 40), (40, 600), (7, 71), (100, 400), (0, 257), (256, 600))),
     (19456, 1024, 1100, ((0, 64), (64, 1100), (300, 812))),
 ])
 def test_linear_rows_are_bitwise_the_same_in_either_gemm_kernel(cuda_lib, n, k, m, parts):
-    """An unsplit weight runs the cluster kernel up to 64 rows and the persistent kernel above;
-    both accumulate the same k-blocks in the same order and apply the same epilogue roundings,
+    """An unsplit weight runs the cluster kernel for short launches and the persistent kernel
+    once it has two 256-token output tiles per SM; both accumulate the same k-blocks in the same order and apply the same epilogue roundings,
     so a row's result does not depend on which launch (or batch) it is in."""
     import torch
     from transformer_decode_step_ns_gb300 import _lib

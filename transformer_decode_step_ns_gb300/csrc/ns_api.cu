@@ -125,12 +125,18 @@ int pick_bn(int m, int kb_per_split, int splits, int n_tiles, int sms) {
 // 2048: 256-token tiles beat 128-token ones in every case, by up to 1.9x).
 int pick_bn_persistent(int m) { return pick_bn_capped(m, kMaxBN); }
 
-// The persistent kernel takes a launch of more than 64 rows when the weight is not split.  A
-// split weight stays on the cluster kernel, whose distributed-shared-memory reduction is
-// cheaper than the persistent kernel's reduction through global memory (measured: the
-// LLaMA-3-8B split-K projections at 256 rows 27-48 us against 50-68 us, the 70B-shaped O
-// projection at 2048 rows 370 against 415 us).  Both give a row the same bits.
-bool use_persistent(int m, int splits) { return m >= kPersistentMinRows && splits == 1; }
+// The persistent kernel takes a launch of more than 64 rows of an unsplit weight when it has at
+// least two 256-token output tiles per SM.  A split weight stays on the cluster kernel, whose
+// distributed-shared-memory reduction is cheaper than a reduction through global memory
+// (measured: the LLaMA-3-8B split-K projections at 256 rows 27-48 us against 50-68 us).  A
+// short launch stays there too: the persistent kernel's CTA fills an SM, so under programmatic
+// dependent launch it cannot start streaming its weights beside the previous kernel's CTAs
+// (measured: the 8B gate/up projection at 256 rows 75 us in the step on clusters against 98
+// persistent, though 87 against 83 alone).  Both kernels give a row the same bits.
+bool use_persistent(int m, int splits, int n_tiles, int sms) {
+  if (m < kPersistentMinRows || splits != 1) return false;
+  return static_cast<long long>((m + kMaxBN - 1) / kMaxBN) * n_tiles >= 2LL * sms;
+}
 
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
 // cluster of a launch is resident at once; at least two k-blocks per split; at most one
@@ -520,7 +526,7 @@ GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int 
   p.kb_per_split = pr.kb_per;
   p.epi = epi;
   const int n_tiles = pr.N / kGemmTileN;
-  if (use_persistent(m, pr.splits)) {
+  if (use_persistent(m, pr.splits, n_tiles, sms)) {
     p.BN = pick_bn_persistent(m);
     p.tiles_m = (m + p.BN - 1) / p.BN;
     p.nstage = gemm_persistent_stages(p.BN);
