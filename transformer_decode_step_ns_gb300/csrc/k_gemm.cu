@@ -88,10 +88,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int BN = p.BN;
-  const int nsub = p.wide ? 2 : 1;  // 128-feature sub-tiles of this CTA's tile
-  const uint32_t a_bytes = kABytes * static_cast<uint32_t>(nsub);
   const uint32_t b_bytes = static_cast<uint32_t>(BN) * kGemmTileK * 2;
-  const uint32_t stage_bytes = a_bytes + b_bytes;
+  const uint32_t stage_bytes = kABytes + b_bytes;
   uint8_t* ctrl = smem + static_cast<size_t>(p.nstage) * stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + p.nstage;
@@ -108,8 +106,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   // together and all but the first read it from L2.
   const int tile_m = blockIdx.x;
   const int split = blockIdx.y;
-  const int tile_n = blockIdx.z;  // in units of nsub * 128 features
-  const int n0 = tile_n * kGemmTileN * nsub;
+  const int tile_n = blockIdx.z;
+  const int n0 = tile_n * kGemmTileN;
   const int nkb_total = p.K / kGemmTileK;
   const int kb0 = split * p.kb_per_split;
   const int nkb = min(p.kb_per_split, nkb_total - kb0);
@@ -118,7 +116,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   const uint32_t ncols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
 
   auto stageA = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes; };
-  auto stageB = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + a_bytes; };
+  auto stageB = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kABytes; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.nstage; ++s) {
@@ -134,7 +132,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     prefetch_tmap(&mapB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, ncols * nsub);
+    tmem_alloc(tmem_slot, ncols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -150,11 +148,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   const uint32_t tmem = *tmem_slot;
   // Dependents may be scheduled once every CTA holds its TMEM (so none of them can starve us).
   if (threadIdx.x == 0) griddep_launch_dependents();
-  bool acc_ok = false;  // epilogue warps: the accumulator completed in time
-  const int q = warp & 3;             // TMEM lane quarter this warp may read
-  const int row = q * 32 + lane;      // output feature within a 128-feature sub-tile
-  float* tile = reinterpret_cast<float*>(smem);
-  const int nchunk = (m_valid + 15) >> 4;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -164,8 +157,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       const int pre = min(p.nstage, nkb);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], stage_bytes);
-        for (int h = 0; h < nsub; ++h)
-          tma_load_2d_hint(stageA(i) + h * kABytes, &mapA, &full[i], (kb0 + i) * kGemmTileK, n0 + h * kGemmTileN, pol_w);
+        tma_load_2d_hint(stageA(i), &mapA, &full[i], (kb0 + i) * kGemmTileK, n0, pol_w);
       }
       griddep_wait();  // activations come from the previous kernel of the step
       for (int i = 0; i < pre; ++i) tma_load_2d(stageB(i), &mapB, &full[i], (kb0 + i) * kGemmTileK, tok0);
@@ -179,8 +171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           break;
         }
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        for (int h = 0; h < nsub; ++h)
-          tma_load_2d_hint(stageA(s) + h * kABytes, &mapA, &full[s], (kb0 + i) * kGemmTileK, n0 + h * kGemmTileN, pol_w);
+        tma_load_2d_hint(stageA(s), &mapA, &full[s], (kb0 + i) * kGemmTileK, n0, pol_w);
         tma_load_2d(stageB(s), &mapB, &full[s], (kb0 + i) * kGemmTileK, tok0);
       }
       *issued = i;
@@ -203,9 +194,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         for (int k = 0; k < kGemmTileK / 16; ++k) {
           umma_f16(tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32),
                    p.idesc, (i | k) != 0 ? 1u : 0u);
-          if (nsub == 2)  // rows 128..255 of the weight tile into the second accumulator
-            umma_f16(tmem + ncols, sw128_kmajor_desc(a_addr + kABytes + k * 32),
-                     sw128_kmajor_desc(b_addr + k * 32), p.idesc, (i | k) != 0 ? 1u : 0u);
         }
         umma_commit(&empty[s]);
       }
@@ -288,11 +276,25 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
       }
     }
-    acc_ok = mbar_wait(accum, 0, abort_flag);
+    // TMEM -> shared tile [BN][128] fp32 (reuses the stage ring: every MMA has completed)
+    const int q = warp & 3;             // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;      // output feature within the tile
+    const bool ok = mbar_wait(accum, 0, abort_flag);
     tc_fence_after();
-    if (!acc_ok) {
+    if (!ok) {
       *abort_flag = 1;
       set_err(p.err, NS_DEV_WAIT_TIMEOUT);
+    }
+    float* tile = reinterpret_cast<float*>(smem);
+    const int nchunk = (m_valid + 15) >> 4;
+    if (ok && !*abort_flag && !two_pass) {
+      for (int c = 0; c < nchunk; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) tile[(c * 16 + i) * kGemmTileN + row] = __uint_as_float(r[i]);
+      }
     }
   }
 
@@ -306,289 +308,268 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   // A tile wider than kPassRows tokens is staged kPassRows tokens at a time (its shared-memory
   // tile is then half the size, so two CTAs fit on an SM).
   const int npass = two_pass ? (m_valid + kPassRows - 1) / kPassRows : 1;
-  for (int h = 0; h < nsub; ++h) {
-    // sub-tile h: features n0h .. n0h + 127, accumulator columns from tmh
-    const int n0h = n0 + h * kGemmTileN;
-    const int tnh = tile_n * nsub + h;
-    const uint32_t tmh = tmem + static_cast<uint32_t>(h) * ncols;
-    if (h > 0) {
-      if (S > 1) cluster_wait();  // every peer has finished reading the previous sub-tile
-      __syncthreads();            // ... and so has this CTA
-    }
-    // TMEM -> shared tile [BN][128] fp32 (reuses the stage ring: every MMA has completed)
-    if (warp >= 2 && acc_ok && !*abort_flag && !two_pass) {
-      for (int c = 0; c < nchunk; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tmh + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) tile[(c * 16 + i) * kGemmTileN + row] = __uint_as_float(r[i]);
-      }
-    }
-    __syncthreads();
-    if (S > 1 && !two_pass) {
+  __syncthreads();
+  if (S > 1 && !two_pass) {
+    cluster_sync();
+    if (warp < 2) cluster_arrive();  // these warps read no peer memory
+  }
+  if (S > 1 && two_pass && warp < 2) {
+    for (int pass = 0; pass < npass; ++pass) {  // the same phases as the epilogue warps
+      if (pass > 0) cluster_wait();
       cluster_sync();
-      if (warp < 2) cluster_arrive();  // these warps read no peer memory
+      cluster_arrive();
     }
-    if (S > 1 && two_pass && warp < 2) {
-      for (int pass = 0; pass < npass; ++pass) {  // the same phases as the epilogue warps
-        if (pass > 0) cluster_wait();
-        cluster_sync();
-        cluster_arrive();
-      }
-    }
-    if (warp >= 2) {
-      const int et = threadIdx.x - 64;  // 0..127: feature within the tile
-      const int ew = warp - 2;
-      const bool run = !*abort_flag;
-      float* const tbase = reinterpret_cast<float*>(smem);
-      // owned tokens j = rank + S * k with lo <= j < hi (rows j - lo of the staged tile)
-      auto reduce = [&](int k_lo, int k_hi, int lo) {
-        // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads
-        // are issued before they are summed (in rank order)
-        const uint32_t base = smem_u32(tbase);
-        const int fg = et & 31, slot = et >> 5;
-        for (int k = k_lo + slot; k < k_hi; k += 4) {
-          const int row = rank + S * k - lo;
-          const uint32_t off = base + static_cast<uint32_t>((row * kGemmTileN + 4 * fg) * 4);
-          float4 v[kMaxSplits];
-  #pragma unroll
-          for (int r = 0; r < kMaxSplits; ++r)
-            if (r < S) v[r] = ld_shared_cluster_f32x4(map_shared_rank(off, r));
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  #pragma unroll
-          for (int r = 0; r < kMaxSplits; ++r) {
-            if (r < S) {
-              acc.x += v[r].x;
-              acc.y += v[r].y;
-              acc.z += v[r].z;
-              acc.w += v[r].w;
-            }
-          }
-          *reinterpret_cast<float4*>(&tbase[row * kGemmTileN + 4 * fg]) = acc;
-        }
-      };
-      if (!two_pass) {
-        if (run && S > 1) reduce(0, n_own, 0);
-        named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
-        if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
-      }
-      const EpiArgs& e = p.e;
-      const bool scaled = e.sumsq_in != nullptr;
-      for (int pass = 0; pass < npass; ++pass) {
-        // token rows [lo, hi) of the CTA's tile; owned tokens k_lo <= k < k_hi among them
-        const int lo = two_pass ? pass * kPassRows : 0;
-        const int hi = two_pass ? min(lo + kPassRows, m_valid) : m_valid;
-        const int k_lo = two_pass ? max(0, (lo - rank + S - 1) / S) : 0;
-        const int k_hi = two_pass ? max(k_lo, (hi - rank + S - 1) / S) : n_own;
-        const int jn = k_hi - k_lo;
-        if (two_pass) {
-          if (pass > 0) {
-            named_barrier_sync(1, 128);  // this CTA is done with the previous pass's tile
-            if (S > 1) cluster_wait();   // ... and so are its peers
-          }
-          const int q = warp & 3, frow = q * 32 + lane;
-          if (run) {
-            for (int c = 0; c < (hi - lo + 15) >> 4; ++c) {
-              uint32_t r[16];
-              tmem_ld16(tmh + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(lo + c * 16), r);
-              tmem_ld_wait();
-  #pragma unroll
-              for (int i = 0; i < 16; ++i) tbase[(c * 16 + i) * kGemmTileN + frow] = __uint_as_float(r[i]);
-            }
-          }
-          named_barrier_sync(1, 128);
-          if (S > 1) {
-            cluster_sync();
-            if (run) reduce(k_lo, k_hi, lo);
-            named_barrier_sync(1, 128);
-            cluster_arrive();
+  }
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;  // 0..127: feature within the tile
+    const int ew = warp - 2;
+    const bool run = !*abort_flag;
+    float* const tbase = reinterpret_cast<float*>(smem);
+    // owned tokens j = rank + S * k with lo <= j < hi (rows j - lo of the staged tile)
+    auto reduce = [&](int k_lo, int k_hi, int lo) {
+      // thread -> 4 consecutive features of every 4th owned token; all ranks' float4 loads
+      // are issued before they are summed (in rank order)
+      const uint32_t base = smem_u32(tbase);
+      const int fg = et & 31, slot = et >> 5;
+      for (int k = k_lo + slot; k < k_hi; k += 4) {
+        const int row = rank + S * k - lo;
+        const uint32_t off = base + static_cast<uint32_t>((row * kGemmTileN + 4 * fg) * 4);
+        float4 v[kMaxSplits];
+#pragma unroll
+        for (int r = 0; r < kMaxSplits; ++r)
+          if (r < S) v[r] = ld_shared_cluster_f32x4(map_shared_rank(off, r));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kMaxSplits; ++r) {
+          if (r < S) {
+            acc.x += v[r].x;
+            acc.y += v[r].y;
+            acc.z += v[r].z;
+            acc.w += v[r].w;
           }
         }
+        *reinterpret_cast<float4*>(&tbase[row * kGemmTileN + 4 * fg]) = acc;
+      }
+    };
+    if (!two_pass) {
+      if (run && S > 1) reduce(0, n_own, 0);
+      named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
+      if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
+    }
+    const EpiArgs& e = p.e;
+    const bool scaled = e.sumsq_in != nullptr;
+    for (int pass = 0; pass < npass; ++pass) {
+      // token rows [lo, hi) of the CTA's tile; owned tokens k_lo <= k < k_hi among them
+      const int lo = two_pass ? pass * kPassRows : 0;
+      const int hi = two_pass ? min(lo + kPassRows, m_valid) : m_valid;
+      const int k_lo = two_pass ? max(0, (lo - rank + S - 1) / S) : 0;
+      const int k_hi = two_pass ? max(k_lo, (hi - rank + S - 1) / S) : n_own;
+      const int jn = k_hi - k_lo;
+      if (two_pass) {
+        if (pass > 0) {
+          named_barrier_sync(1, 128);  // this CTA is done with the previous pass's tile
+          if (S > 1) cluster_wait();   // ... and so are its peers
+        }
+        const int q = warp & 3, frow = q * 32 + lane;
         if (run) {
-          // tile[j * 128 + r] addresses the staged row of token j of this pass
-          float* tile = tbase - static_cast<ptrdiff_t>(lo) * kGemmTileN;
-          const bool use_pf = pass == 0 && h == 0;  // the prefetched registers hold the first chunk
-          const int start = use_pf ? et + 128 * kPf : et;
-          auto tok_of = [&](int k) { return rank + S * (k_lo + k); };  // k-th owned token of the pass
-          if (p.epi == EPI_F32) {
-            float* out = e.out_f32;
-            if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
-            // padding rows of a bucketed graph have no output row
-            const int n_rows = e.rows_valid != nullptr ? *e.rows_valid - tok0 : m_valid;
-            for (int idx = et; idx < jn * kGemmTileN; idx += 128) {
-              const int j = tok_of(idx >> 7), r = idx & 127;
-              if (j >= n_rows) continue;
-              float v = tile[j * kGemmTileN + r];
-              if (scaled) v *= rs_s[j];
-              out[static_cast<size_t>(tok0 + j) * e.ldo + n0h + r] = v;
-            }
-          } else if (p.epi == EPI_QKV) {
-            const int d = e.head_dim, half = d >> 1;
-            T* qo = reinterpret_cast<T*>(e.q_out);
-            T* kp = reinterpret_cast<T*>(e.k_pool);
-            T* vp = reinterpret_cast<T*>(e.v_pool);
-            auto kv_base = [&](long long slot, int kvh) {
-              return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
-                      static_cast<size_t>(slot % e.block_size)) * d;
-            };
-            if (n0h < e.q_dim + e.kv_dim) {
-              // q and k columns: RoPE pairs (i, i + d/2) of each head
-              auto qk = [&](int idx, float c, float sn, long long slot) {
-                const int j = tok_of(idx >> 6), pr = idx & 63;
-                const int hl = pr / half, i = pr - hl * half;
-                const int r_lo = hl * d + i, r_hi = r_lo + half;
-                const int tok = tok0 + j;
-                const float sc = scaled ? rs_s[j] : 1.f;
-                const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
-                const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
-                const float y_lo = rope_lo(x_lo, x_hi, c, sn);
-                const float y_hi = rope_hi(x_lo, x_hi, c, sn);
-                if (n0h < e.q_dim) {
-                  T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0h;
-                  dst[r_lo] = Cvt<T>::from_f(y_lo);
-                  dst[r_hi] = Cvt<T>::from_f(y_hi);
-                } else {
-                  if (slot < 0 || slot >= e.pool_slots) {
-                    set_err(p.err, NS_DEV_BAD_SLOT);
-                    return;
-                  }
-                  const size_t base = kv_base(slot, (n0h - e.q_dim + r_lo) / d);
-                  const T k_lo = Cvt<T>::from_f(y_lo), k_hi = Cvt<T>::from_f(y_hi);
-                  kp[base + i] = k_lo;
-                  kp[base + i + half] = k_hi;
-                  if (e.kv_stage != nullptr) {
-                    T* st = reinterpret_cast<T*>(e.kv_stage) + static_cast<size_t>(tok) * 2 * e.kv_dim +
-                            (n0h - e.q_dim);
-                    st[r_lo] = k_lo;
-                    st[r_hi] = k_hi;
-                  }
-                }
-              };
-              if (use_pf) {
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = et + 128 * u;
-                  if (idx < jn * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
-                }
-              }
-              // the rest in chunks of kPf, each chunk's loads issued before its stores
-              for (int b0 = start; b0 < jn * 64; b0 += 128 * kPf) {
-                float ca[kPf], cb[kPf];
-                long long cs[kPf];
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = b0 + 128 * u;
-                  if (idx < jn * 64) {
-                    const int tok = tok0 + tok_of(idx >> 6);
-                    const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
-                    ca[u] = e.rope_cos[o];
-                    cb[u] = e.rope_sin[o];
-                    cs[u] = n0h >= e.q_dim ? e.slot_mapping[tok] : 0;
-                  }
-                }
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = b0 + 128 * u;
-                  if (idx < jn * 64) qk(idx, ca[u], cb[u], cs[u]);
-                }
-              }
-            } else {
-              // v columns
-              auto vv = [&](int idx, long long slot) {
-                const int j = tok_of(idx >> 7), r = idx & 127;
-                const int col = n0h - e.q_dim - e.kv_dim + r;
-                const int kvh = col / d, dim = col - kvh * d;
+          for (int c = 0; c < (hi - lo + 15) >> 4; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(lo + c * 16), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tbase[(c * 16 + i) * kGemmTileN + frow] = __uint_as_float(r[i]);
+          }
+        }
+        named_barrier_sync(1, 128);
+        if (S > 1) {
+          cluster_sync();
+          if (run) reduce(k_lo, k_hi, lo);
+          named_barrier_sync(1, 128);
+          cluster_arrive();
+        }
+      }
+      if (run) {
+        // tile[j * 128 + r] addresses the staged row of token j of this pass
+        float* tile = tbase - static_cast<ptrdiff_t>(lo) * kGemmTileN;
+        const bool use_pf = pass == 0;  // the prefetched registers hold pass 0's first chunk
+        const int start = use_pf ? et + 128 * kPf : et;
+        auto tok_of = [&](int k) { return rank + S * (k_lo + k); };  // k-th owned token of the pass
+        if (p.epi == EPI_F32) {
+          float* out = e.out_f32;
+          if (e.out_ptr_slot != nullptr) out = reinterpret_cast<float*>(*e.out_ptr_slot);
+          // padding rows of a bucketed graph have no output row
+          const int n_rows = e.rows_valid != nullptr ? *e.rows_valid - tok0 : m_valid;
+          for (int idx = et; idx < jn * kGemmTileN; idx += 128) {
+            const int j = tok_of(idx >> 7), r = idx & 127;
+            if (j >= n_rows) continue;
+            float v = tile[j * kGemmTileN + r];
+            if (scaled) v *= rs_s[j];
+            out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
+          }
+        } else if (p.epi == EPI_QKV) {
+          const int d = e.head_dim, half = d >> 1;
+          T* qo = reinterpret_cast<T*>(e.q_out);
+          T* kp = reinterpret_cast<T*>(e.k_pool);
+          T* vp = reinterpret_cast<T*>(e.v_pool);
+          auto kv_base = [&](long long slot, int kvh) {
+            return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
+                    static_cast<size_t>(slot % e.block_size)) * d;
+          };
+          if (n0 < e.q_dim + e.kv_dim) {
+            // q and k columns: RoPE pairs (i, i + d/2) of each head
+            auto qk = [&](int idx, float c, float sn, long long slot) {
+              const int j = tok_of(idx >> 6), pr = idx & 63;
+              const int hl = pr / half, i = pr - hl * half;
+              const int r_lo = hl * d + i, r_hi = r_lo + half;
+              const int tok = tok0 + j;
+              const float sc = scaled ? rs_s[j] : 1.f;
+              const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
+              const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
+              const float y_lo = rope_lo(x_lo, x_hi, c, sn);
+              const float y_hi = rope_hi(x_lo, x_hi, c, sn);
+              if (n0 < e.q_dim) {
+                T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
+                dst[r_lo] = Cvt<T>::from_f(y_lo);
+                dst[r_hi] = Cvt<T>::from_f(y_hi);
+              } else {
                 if (slot < 0 || slot >= e.pool_slots) {
                   set_err(p.err, NS_DEV_BAD_SLOT);
                   return;
                 }
-                const T v = Cvt<T>::from_f(tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f));
-                vp[kv_base(slot, kvh) + dim] = v;
-                if (e.kv_stage != nullptr)
-                  reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok0 + j) * 2 * e.kv_dim + e.kv_dim + col] = v;
-              };
-              if (use_pf) {
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = et + 128 * u;
-                  if (idx < jn * kGemmTileN) vv(idx, pf_s[u]);
+                const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
+                const T k_lo = Cvt<T>::from_f(y_lo), k_hi = Cvt<T>::from_f(y_hi);
+                kp[base + i] = k_lo;
+                kp[base + i + half] = k_hi;
+                if (e.kv_stage != nullptr) {
+                  T* st = reinterpret_cast<T*>(e.kv_stage) + static_cast<size_t>(tok) * 2 * e.kv_dim +
+                          (n0 - e.q_dim);
+                  st[r_lo] = k_lo;
+                  st[r_hi] = k_hi;
                 }
               }
-              for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
-                long long cs[kPf];
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = b0 + 128 * u;
-                  if (idx < jn * kGemmTileN) cs[u] = e.slot_mapping[tok0 + tok_of(idx >> 7)];
-                }
-  #pragma unroll
-                for (int u = 0; u < kPf; ++u) {
-                  const int idx = b0 + 128 * u;
-                  if (idx < jn * kGemmTileN) vv(idx, cs[u]);
-                }
-              }
-            }
-            // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
-          } else if (p.epi == EPI_RESID) {
-            T* xo = reinterpret_cast<T*>(e.xn_out);
-            const float gam = h == 0 ? pf_b[0] : e.gamma_next[n0h + et];
-            auto rs_row = [&](int idx, float old) {
-              const int j = tok_of(idx >> 7), r = idx & 127;
-              const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0h + r;
-              const float rn = old + tile[j * kGemmTileN + r];
-              e.resid[gi] = rn;
-              xo[gi] = Cvt<T>::from_f(rn * gam);
-              tile[j * kGemmTileN + r] = rn * rn;
             };
             if (use_pf) {
-  #pragma unroll
+#pragma unroll
               for (int u = 0; u < kPf; ++u) {
                 const int idx = et + 128 * u;
-                if (idx < jn * kGemmTileN) rs_row(idx, pf_a[u]);
+                if (idx < jn * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
+              }
+            }
+            // the rest in chunks of kPf, each chunk's loads issued before its stores
+            for (int b0 = start; b0 < jn * 64; b0 += 128 * kPf) {
+              float ca[kPf], cb[kPf];
+              long long cs[kPf];
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * 64) {
+                  const int tok = tok0 + tok_of(idx >> 6);
+                  const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
+                  ca[u] = e.rope_cos[o];
+                  cb[u] = e.rope_sin[o];
+                  cs[u] = n0 >= e.q_dim ? e.slot_mapping[tok] : 0;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = b0 + 128 * u;
+                if (idx < jn * 64) qk(idx, ca[u], cb[u], cs[u]);
+              }
+            }
+          } else {
+            // v columns
+            auto vv = [&](int idx, long long slot) {
+              const int j = tok_of(idx >> 7), r = idx & 127;
+              const int col = n0 - e.q_dim - e.kv_dim + r;
+              const int kvh = col / d, dim = col - kvh * d;
+              if (slot < 0 || slot >= e.pool_slots) {
+                set_err(p.err, NS_DEV_BAD_SLOT);
+                return;
+              }
+              const T v = Cvt<T>::from_f(tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f));
+              vp[kv_base(slot, kvh) + dim] = v;
+              if (e.kv_stage != nullptr)
+                reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok0 + j) * 2 * e.kv_dim + e.kv_dim + col] = v;
+            };
+            if (use_pf) {
+#pragma unroll
+              for (int u = 0; u < kPf; ++u) {
+                const int idx = et + 128 * u;
+                if (idx < jn * kGemmTileN) vv(idx, pf_s[u]);
               }
             }
             for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
-              float cr[kPf];
-  #pragma unroll
+              long long cs[kPf];
+#pragma unroll
               for (int u = 0; u < kPf; ++u) {
                 const int idx = b0 + 128 * u;
-                if (idx < jn * kGemmTileN)
-                  cr[u] = e.resid[static_cast<size_t>(tok0 + tok_of(idx >> 7)) * e.resid_dim + n0h + et];
+                if (idx < jn * kGemmTileN) cs[u] = e.slot_mapping[tok0 + tok_of(idx >> 7)];
               }
-  #pragma unroll
+#pragma unroll
               for (int u = 0; u < kPf; ++u) {
                 const int idx = b0 + 128 * u;
-                if (idx < jn * kGemmTileN) rs_row(idx, cr[u]);
+                if (idx < jn * kGemmTileN) vv(idx, cs[u]);
               }
             }
-            named_barrier_sync(1, 128);
-            for (int k = ew; k < jn; k += 4) {
-              const int j = tok_of(k);
-              const float* tr = tile + j * kGemmTileN;
-              float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
-  #pragma unroll
-              for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-              if (lane == 0) e.sumsq_out[static_cast<size_t>(tnh) * e.sumsq_ld + tok0 + j] = s;
-            }
-            fence_proxy_async_global();
-          } else if (p.epi == EPI_SWIGLU) {
-            T* ao = reinterpret_cast<T*>(e.act_out);
-            const int f0 = tnh * 64;
-            for (int idx = et; idx < jn * 64; idx += 128) {
-              const int j = tok_of(idx >> 6), c = idx & 63;
-              const float sc = scaled ? rs_s[j] : 1.f;
-              const float g = tile[j * kGemmTileN + c] * sc;
-              const float u = tile[j * kGemmTileN + 64 + c] * sc;
-              const float a = silu_mul(g, u);
-              ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
-            }
-            fence_proxy_async_global();
           }
+          // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
+        } else if (p.epi == EPI_RESID) {
+          T* xo = reinterpret_cast<T*>(e.xn_out);
+          const float gam = pf_b[0];
+          auto rs_row = [&](int idx, float old) {
+            const int j = tok_of(idx >> 7), r = idx & 127;
+            const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
+            const float rn = old + tile[j * kGemmTileN + r];
+            e.resid[gi] = rn;
+            xo[gi] = Cvt<T>::from_f(rn * gam);
+            tile[j * kGemmTileN + r] = rn * rn;
+          };
+          if (use_pf) {
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = et + 128 * u;
+              if (idx < jn * kGemmTileN) rs_row(idx, pf_a[u]);
+            }
+          }
+          for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
+            float cr[kPf];
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < jn * kGemmTileN)
+                cr[u] = e.resid[static_cast<size_t>(tok0 + tok_of(idx >> 7)) * e.resid_dim + n0 + et];
+            }
+#pragma unroll
+            for (int u = 0; u < kPf; ++u) {
+              const int idx = b0 + 128 * u;
+              if (idx < jn * kGemmTileN) rs_row(idx, cr[u]);
+            }
+          }
+          named_barrier_sync(1, 128);
+          for (int k = ew; k < jn; k += 4) {
+            const int j = tok_of(k);
+            const float* tr = tile + j * kGemmTileN;
+            float s = (tr[lane] + tr[lane + 32]) + (tr[lane + 64] + tr[lane + 96]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) e.sumsq_out[static_cast<size_t>(tile_n) * e.sumsq_ld + tok0 + j] = s;
+          }
+          fence_proxy_async_global();
+        } else if (p.epi == EPI_SWIGLU) {
+          T* ao = reinterpret_cast<T*>(e.act_out);
+          const int f0 = tile_n * 64;
+          for (int idx = et; idx < jn * 64; idx += 128) {
+            const int j = tok_of(idx >> 6), c = idx & 63;
+            const float sc = scaled ? rs_s[j] : 1.f;
+            const float g = tile[j * kGemmTileN + c] * sc;
+            const float u = tile[j * kGemmTileN + 64 + c] * sc;
+            const float a = silu_mul(g, u);
+            ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
+          }
+          fence_proxy_async_global();
         }
       }
     }
-
   }
 
   // ------------------------------------------------------------------ teardown
@@ -605,7 +586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, ncols * nsub);
+    tmem_dealloc(tmem, ncols);
   }
 }
 
@@ -1029,8 +1010,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------------------ host side
 
-size_t gemm_smem_bytes(int BN, int nstage, int wide) {
-  return 1024 + static_cast<size_t>(nstage) * (kABytes * (wide ? 2 : 1) + static_cast<size_t>(BN) * kGemmTileK * 2) +
+size_t gemm_smem_bytes(int BN, int nstage) {
+  return 1024 + static_cast<size_t>(nstage) * (kABytes + static_cast<size_t>(BN) * kGemmTileK * 2) +
          kCtrlBytes;
 }
 
@@ -1092,8 +1073,8 @@ int gemm_resident_clusters(int splits, size_t smem) {
 
 }  // namespace
 
-int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits, int wide) {
-  const size_t stage = kABytes * (wide ? 2 : 1) + static_cast<size_t>(BN) * kGemmTileK * 2;
+int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits) {
+  const size_t stage = kABytes + static_cast<size_t>(BN) * kGemmTileK * 2;
   // the epilogue tile [rows][128] fp32 reuses the stage ring
   const size_t tile_rows = gemm_two_pass(BN) ? kPassRows : BN;
   const int tile_min = static_cast<int>((tile_rows * kGemmTileN * 4 + stage - 1) / stage);
@@ -1110,7 +1091,7 @@ int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits, int wid
   if (BN <= 64) return half;
   // A wider tile takes the deep ring when the whole grid is resident with it in one wave (the
   // clusters placed as the hardware places them), else two per SM.
-  return clusters <= gemm_resident_clusters(splits, gemm_smem_bytes(BN, deep, wide)) ? deep : half;
+  return clusters <= gemm_resident_clusters(splits, gemm_smem_bytes(BN, deep)) ? deep : half;
 }
 
 uint32_t gemm_idesc(int dtype, int BN) {
@@ -1125,12 +1106,11 @@ namespace {
 template <typename T>
 cudaError_t launch_gemm_t(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                           cudaStream_t s, bool pdl) {
-  const size_t smem = gemm_smem_bytes(p.BN, p.nstage, p.wide);
-  if (smem > 227 * 1024 || (p.wide && p.N % (2 * kGemmTileN) != 0)) return cudaErrorInvalidValue;
+  const size_t smem = gemm_smem_bytes(p.BN, p.nstage);
   cudaError_t e = gemm_configure<T>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.M + p.BN - 1) / p.BN, p.splits, p.N / (kGemmTileN * (p.wide ? 2 : 1)));
+  cfg.gridDim = dim3((p.M + p.BN - 1) / p.BN, p.splits, p.N / kGemmTileN);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -138,12 +138,6 @@ bool use_persistent(int m, int splits, int n_tiles, int sms) {
   return static_cast<long long>((m + kMaxBN - 1) / kMaxBN) * n_tiles >= 2LL * sms;
 }
 
-// Above 64 rows the cluster kernel gives each CTA 256 features (two accumulators that share the
-// activation tile), halving the activation bytes each weight byte brings from L2 to the SMs; the
-// decode batches keep 128-feature tiles, whose larger CTA count streams the weights faster.  The
-// tile width never changes a result (the same k-blocks in the same order per output).
-bool use_wide_tiles(int m, int N) { return m >= kPersistentMinRows && N % (2 * kGemmTileN) == 0; }
-
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
 // cluster of a launch is resident at once; at least two k-blocks per split; at most one
 // portable cluster (8 CTAs) per output tile.
@@ -539,9 +533,7 @@ GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int 
     *grid = static_cast<int>(std::min<long long>(static_cast<long long>(p.tiles_m) * n_tiles, sms));
   } else {
     p.BN = pick_bn(m, pr.kb_per, pr.splits, n_tiles, sms);
-    p.wide = use_wide_tiles(m, pr.N) ? 1 : 0;
-    p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * (n_tiles >> p.wide),
-                                p.splits, p.wide);
+    p.nstage = gemm_pick_stages(p.BN, p.kb_per_split, ((m + p.BN - 1) / p.BN) * n_tiles, p.splits);
     *grid = 0;
   }
   p.idesc = gemm_idesc(dtype, p.BN);

@@ -8,10 +8,10 @@
 namespace ns {
 
 // Kernel launchers return the launch error; `pdl` adds programmatic stream serialisation.
-size_t gemm_smem_bytes(int BN, int nstage, int wide);
+size_t gemm_smem_bytes(int BN, int nstage);
 // Stage-ring depth for a launch of `clusters` clusters of `splits` CTAs (the depth never changes
-// results); `wide`: 256-feature tiles.
-int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits, int wide);
+// results).
+int gemm_pick_stages(int BN, int kb_per_split, int clusters, int splits);
 uint32_t gemm_idesc(int dtype, int BN);
 cudaError_t launch_gemm(const CUtensorMap* mapA, const CUtensorMap* mapB, const GemmParams& p,
                         int dtype, cudaStream_t s, bool pdl);

@@ -72,8 +72,6 @@ struct GemmParams {
   int* err;
   EpiArgs e;
   int tiles_m;  // persistent variant: token tiles of BN rows
-  int wide;     // cluster kernel: 1 = each CTA computes 256 features (two accumulators sharing
-                // the activation tile), N a multiple of 256
 };
 
 // Launches of fewer rows than this never take the persistent GEMM (its tiles are wide).
