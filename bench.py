@@ -740,6 +740,7 @@ class ContinuousWorkload:
         # greedy ids of the last step: the next step's tokens (device token source)
         self.ids_dev = torch.from_numpy(self.tokens.copy()).cuda()
         self.nano = None
+        self.attn_budget = 0
         self.setup_s = time.time() - t0
 
     def join(self, b):
@@ -787,9 +788,11 @@ class ContinuousWorkload:
         self.dev.step(None, *meta, self.logits)
         _lib.greedy_argmax(self.logits, self.ids_dev)
 
-    def set_nano(self, nano):
+    def set_nano(self, nano, budget=None):
         self.nano = nano
-        self.dev.set_nanobatch(nano)
+        if budget is not None:
+            self.attn_budget = budget
+        self.dev.set_nanobatch(nano, attn_cta_budget=self.attn_budget if nano else 0)
         self.dev.set_token_source(self.ids_dev)
 
     def roofline_time(self, metas, peaks):
@@ -912,14 +915,21 @@ class ContinuousWorkload:
                 * self.shape.n_layers}
 
     def pick_split(self, peaks):
-        """A short comparison of the unsplit step and two nano-batches of 128; the faster is
-        used for the rest of the run."""
-        trial = {}
-        for nano in (None, [128, 128]):
-            trial[str(nano or [self.B])] = self.run(20, peaks, nano)["device_ms_per_step_median"]
-        best = None if trial[str([self.B])] <= trial[str([128, 128])] else [128, 128]
-        self.set_nano(best)
-        return best, trial
+        """A short comparison of the unsplit step and two nano-batches of 128 rows, the latter
+        with the attention of each nano-batch uncapped or capped at one or one half CTA per SM
+        (so that the other nano-batch's projections can run beside it on every SM: the NanoFlow
+        page's co-running of memory- and compute-heavy nano-ops); the fastest is used for the
+        rest of the run.  Returns (split, attention CTA budget, trial table)."""
+        sms = int(__import__("torch").cuda.get_device_properties(0).multi_processor_count)
+        trial, best = {}, (None, 0, float("inf"))
+        for nano, budget in ((None, 0), ([128, 128], 0), ([128, 128], sms), ([128, 128], sms // 2)):
+            self.attn_budget = budget
+            ms = self.run(20, peaks, nano)["device_ms_per_step_median"]
+            trial[f"{nano or [self.B]} attn_cta_budget={budget}"] = ms
+            if ms < best[2]:
+                best = (nano, budget, ms)
+        self.set_nano(best[0], best[1])
+        return best[0], best[1], trial
 
     def kernel_times(self, peaks):
         """Per-kind kernel times of eager steps (an event pair around each launch, on the stream
@@ -1523,7 +1533,7 @@ def run_ours(args, rank, world):
     # ---- headline: continuous batching of the LLaMA-3-8B shape at batch 256
     cw = ContinuousWorkload()
     log(f"setup {cw.setup_s:.1f}s: {cw.num_blocks} blocks, mb {cw.mb}")
-    best, trial = cw.pick_split(peaks)
+    best, budget, trial = cw.pick_split(peaks)
     head = cw.headline(K, W, peaks, world)
     ms_total, units = replica_aggregate(head["ms_total"], cw.B * K, world)
     ms_step = ms_total / K
@@ -1618,7 +1628,7 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "model": "llama-3-8b-shaped (random init)",
                    "global_batch": ContinuousWorkload.B * world,
                    "seq_len": "ctx U[512,4096] + decode U[100,1000], leave/join",
-                   "nano_split": best or [ContinuousWorkload.B],
+                   "nano_split": best or [ContinuousWorkload.B], "attn_cta_budget": budget,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (15 GB of weights and ~77 GB of K/V per step)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s",
@@ -1718,7 +1728,7 @@ def run_extra_only(args, rank, world):
                 "config": {"workload": r["workload"]}, "serving": r}
     else:
         cw = ContinuousWorkload()
-        best, trial = cw.pick_split(peaks)
+        best, budget, trial = cw.pick_split(peaks)
         head = cw.headline(max(args.steps, 1), args.warmup, peaks, 1)
         r = cw.run_async(args.continuous_steps, peaks)
         r["split_trial_ms_per_step"] = trial
@@ -1728,7 +1738,8 @@ def run_extra_only(args, rank, world):
                 "value": ContinuousWorkload.B * K / (head["ms_total"] * 1e-3),
                 "ms_per_step": head["ms_total"] / K, "higher_is_better": True,
                 "n_gpus": world, "steps": K, "warmup": args.warmup, "dtype": "bf16",
-                "data": "synthetic", "config": {"workload": WORKLOAD, "nano_split": best},
+                "data": "synthetic", "config": {"workload": WORKLOAD, "nano_split": best,
+                                                 "attn_cta_budget": budget},
                 "frac_of_roofline": head["roofline_s"] / (head["ms_total"] * 1e-3),
                 "clocks": head["clocks"], "continuous": r}
         cw.close()
