@@ -704,14 +704,19 @@ class ContinuousWorkload:
 
     B, bs, ctx_lo, ctx_hi, dec_lo, dec_hi = 256, 16, 512, 4096, 100, 1000
 
-    def __init__(self, max_joins: int = 100_000):
+    def __init__(self, max_joins: int = 100_000, n_layers: int = 32):
         import torch
         from transformer_decode_step_ns_gb300 import _lib
         self.seed = seed = synth.config_seed(4)
-        self.shape = sh = synth.llama3_8b_shape(32)
+        self.shape = sh = synth.llama3_8b_shape(n_layers)
         B, bs = self.B, self.bs
         self.mb = mb = cfg4_table_width()
-        self.num_blocks = B * mb
+        # the worst case (every row at its longest) for the full model; a truncated model (a
+        # small case for profilers) gets the first step's blocks plus room for a few hundred
+        # steps of growth and joins
+        first = int(sum(math.ceil((int(c) + 1) / bs) for c in
+                        synth.ctx_uniform(seed, "cfg4.join.ctx", B, self.ctx_lo, self.ctx_hi)))
+        self.num_blocks = B * mb if n_layers == 32 else min(B * mb, first + 16 * mb)
         t0 = time.time()
         self.w = synth.model_weights_device(sh, seed)
         self.dev = _lib.DecodeStep(sh, self.w, B, mb, use_graphs=True)
@@ -1730,7 +1735,7 @@ def run_extra_only(args, rank, world):
                 "warmup": 0, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": r["workload"]}, "serving": r}
     else:
-        cw = ContinuousWorkload()
+        cw = ContinuousWorkload(n_layers=args.layers)
         best, budget, trial = cw.pick_split(peaks)
         head = cw.headline(max(args.steps, 1), args.warmup, peaks, 1)
         r = cw.run_async(args.continuous_steps, peaks)
@@ -1818,6 +1823,9 @@ def main():
     ap.add_argument("--attn-ctx", default="cfg2", choices=["cfg2", "cfg4"],
                     help="context mix of --attention-only: the attention workload's own, or the "
                          "continuous LLaMA-3-8B run's")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="with --continuous-only: layers of the LLaMA-3-8B shape (fewer: a small "
+                         "case of the same kernels, e.g. for profilers)")
     ap.add_argument("--skip-qwen", action="store_true")
     ap.add_argument("--skip-small", action="store_true")
     ap.add_argument("--skip-offload", action="store_true")
