@@ -577,9 +577,9 @@ class NanoLayerWorkload:
         kv_write = self.B * 2 * kvd * 2
         return flops, weights + kv + kv_write
 
-    def time_variant(self, sizes, budget, steps, warmup):
+    def time_variant(self, sizes, budget, steps, warmup, gemm_budget=0):
         import torch
-        self.dev.set_nanobatch(sizes, attn_cta_budget=budget)
+        self.dev.set_nanobatch(sizes, attn_cta_budget=budget, gemm_cta_budget=gemm_budget)
         for _ in range(max(warmup, 3)):
             self.dev.step(*self.meta, None)
         torch.cuda.synchronize()
@@ -656,16 +656,23 @@ class NanoLayerWorkload:
                     "device_error": _lib.device_error()}
         prof = self.interference()
 
-        def step(sizes, budget):
-            self.dev.set_nanobatch(sizes, attn_cta_budget=budget)
+        def step(sizes, budget, gemm_budget=0):
+            self.dev.set_nanobatch(sizes, attn_cta_budget=budget, gemm_cta_budget=gemm_budget)
             self.dev.step(*self.meta, None)
 
-        found = tuner.search(step, self.B, profile=prof, reps=max(3, min(steps, 10)))
+        # projections of each nano-batch on g SMs (one persistent CTA per SM), the attention of
+        # the other on the SMs they leave (two attention CTAs per SM), or uncapped
+        import torch
+        sms = int(torch.cuda.get_device_properties(0).multi_processor_count)
+        pairs = [(g, 2 * (sms - g)) for g in (sms // 2, 2 * sms // 3, 4 * sms // 5, 9 * sms // 10)]
+        pairs += [(2 * sms // 3, 0), (4 * sms // 5, 0)]
+        found = tuner.search(step, self.B, profile=prof, reps=max(3, min(steps, 10)), gemm_pairs=pairs)
         for r in found["table"]:
             r["frac_of_roofline"] = round(t_roof / (r["ms"] * 1e-3), 4)
         rows = []
         for label, sizes in self.LABELS.items():
-            r = next(t for t in found["table"] if t["sizes"] == sizes and t["budget"] == 0)
+            r = next(t for t in found["table"] if t["sizes"] == sizes and t["budget"] == 0
+                     and t["gemm_budget"] == 0)
             rows.append({"split": label, "sizes": sizes, "attn_cta_budget": 0,
                          "us": round(r["ms"] * 1e3, 1),
                          "tflops": round(flops / (r["ms"] * 1e-3) / 1e12, 1),
@@ -673,8 +680,9 @@ class NanoLayerWorkload:
         best = found["best"]
         # the tuned configuration, timed again over the full step count
         ms = self.time_variant(None if len(best["sizes"]) == 1 else best["sizes"], best["budget"],
-                               steps, warmup)
-        tuned = {"sizes": best["sizes"], "attn_cta_budget": best["budget"], "us": round(ms * 1e3, 1),
+                               steps, warmup, best["gemm_budget"])
+        tuned = {"sizes": best["sizes"], "attn_cta_budget": best["budget"],
+                 "gemm_cta_budget": best["gemm_budget"], "us": round(ms * 1e3, 1),
                  "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                  "frac_of_roofline": round(t_roof / (ms * 1e-3), 4)}
         self.dev.set_nanobatch(None)

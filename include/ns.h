@@ -268,6 +268,15 @@ ns_status ns_kv_free_count(ns_handle h, int* n_free);
  * wave.  Sizes must sum to the batch of the following ns_decode_step calls. */
 ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_cta_budget);
 
+/* The other half of the NanoFlow page's per-nano-op thread-block budgets ("The part that is
+ * harder than it looks"): in nano-batched steps (n_split > 1), projections that run the
+ * persistent GEMM (more than 64 rows of an unsplit weight with two 256-token output tiles per
+ * SM) use at most gemm_cta_budget CTAs, one per SM, so the other nano-batch's attention can take
+ * the SMs they leave free; 0 = one per SM.  The persistent GEMM computes every output tile the
+ * same way on any grid, so results are bitwise unchanged.  gemm_cta_budget < 0 returns
+ * INVALID_ARG.  Unsplit steps ignore it. */
+ns_status ns_set_gemm_cta_budget(ns_handle h, int gemm_cta_budget);
+
 /* One decode step for `batch` rows.  Host metadata (validated, packed into one pinned buffer
  * and uploaded with a single host-to-device copy on `stream`):
  *   token_ids [batch] int32 in [0, V) (with a device token source set, NULL or entries
@@ -460,6 +469,7 @@ typedef struct {
   int kv_offload;       /* the graph mirrors K/V to the host */
   int kernels;          /* kernel nodes */
   double capture_ms;    /* host time of capture + instantiate */
+  int gemm_cta_budget;  /* 0: none (ns_set_gemm_cta_budget) */
 } ns_graph_info;
 /* *n = the number of graphs; the first min(*n, capacity) entries are written, in key order. */
 ns_status ns_get_graph_report(ns_handle h, ns_graph_info* out, int capacity, int* n);

@@ -136,7 +136,8 @@ def test_attention_batch_256_full_pool(cuda_lib):
 def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
     """One LLaMA-2-70B-shaped layer over 1024 decode rows + a 1024-token prefill chunk, run
     with the uneven 768 + 1280 nano-batch split; logits through the tied head as the probe.
-    Splits 1 and 1024 + 1024 give the same logits bitwise."""
+    Splits 1 and 1024 + 1024 (also with CTA budgets: projections on 100 SMs, attention on 104
+    CTAs) give the same logits bitwise."""
     import torch
     import bench
     nw = bench.NanoLayerWorkload()
@@ -151,8 +152,11 @@ def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
     ref = _oracle_rows(model, sh, lambda l: pools, nw.meta, rows, nw.bs)
     logits = torch.empty((nw.B, sh.vocab), dtype=torch.float32, device="cuda")
     results = {}
-    for split in ([768, 1280], None, [1024, 1024]):
-        nw.dev.set_nanobatch(split)
+    for split in ([768, 1280], None, [1024, 1024], "capped"):
+        if split == "capped":  # projections on 100 SMs, attention on the 52 they leave
+            nw.dev.set_nanobatch([1024, 1024], attn_cta_budget=104, gemm_cta_budget=100)
+        else:
+            nw.dev.set_nanobatch(split)
         nw.dev.step(*nw.meta, logits)
         torch.cuda.synchronize()
         assert nw.dev.device_error() == 0
@@ -165,6 +169,7 @@ def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
         _check_logits(got[i:i + 1], ref[i:i + 1], f"70B layer row {r}", abs_tol=abs_tol)
     np.testing.assert_array_equal(results["None"], results[str([768, 1280])])
     np.testing.assert_array_equal(results[str([1024, 1024])], results[str([768, 1280])])
+    np.testing.assert_array_equal(results["capped"], results[str([768, 1280])])
 
 
 def test_llama3_8b_32_layers_batch_256(cuda_lib):

@@ -155,8 +155,9 @@ def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cud
     each) run the persistent kernel above 64 rows and the cluster kernel below, while the split
     ones (QKV, O, down) always run on clusters.  Unsplit, 40 + 2008 and 1024 + 1024 nano-batches
     give every row the same logits and cache bits through every fused epilogue (QKV with RoPE and
-    the cache write, residual + norm, SwiGLU with the norm scale, the fp32 head); sampled rows
-    match the oracle."""
+    the cache write, residual + norm, SwiGLU with the norm scale, the fp32 head), also with the
+    persistent projections of the nano-batches capped at 40 or 7 CTAs and the attention at 50;
+    sampled rows match the oracle."""
     shape = synth.ModelShape(hidden=512, n_layers=2, n_q_heads=32, n_kv_heads=4, head_dim=128,
                              ffn=9728, vocab=19456, rms_eps=1e-5, rope_theta=5e5, dtype="bf16",
                              tie_embeddings=False)
@@ -164,9 +165,10 @@ def test_nano_batches_across_both_gemm_kernels_equal_the_whole_batch_bitwise(cud
     h = Harness(shape, 86, ctx)
     got = h.run_gpu()
     ks0, vs0 = h.download_pools()
-    for sizes in ([40, 2008], [1024, 1024]):
+    for sizes, attn_cap, gemm_cap in (([40, 2008], 0, 0), ([1024, 1024], 0, 0), ([1024, 1024], 50, 40),
+                                      ([40, 2008], 0, 7)):
         h.upload_pools()
-        h.dev.set_nanobatch(sizes)
+        h.dev.set_nanobatch(sizes, attn_cta_budget=attn_cap, gemm_cta_budget=gemm_cap)
         np.testing.assert_array_equal(h.run_gpu(), got)
         ks, vs = h.download_pools()
         for l in range(shape.n_layers):

@@ -458,6 +458,36 @@ def test_tuner_search_measures_every_split_then_budgets_and_picks_the_fastest():
     assert tuner.search(step, 2048, profile=low, timer=timer)["budgets_kept"] == [16, 48, 32, 24]
 
 
+def test_tuner_search_tries_gemm_budget_pairs_on_the_fastest_splits():
+    """(GEMM budget, attention budget) pairs are timed on the three fastest multi-batch splits,
+    after the attention budgets; a pair that helps wins, and every row records both budgets."""
+    from transformer_decode_step_ns_gb300 import tuner
+    calls = []
+
+    def cost(sizes, budget, gemm_budget):
+        base = 4.0 if sizes is None else 3.7 + 0.001 * abs(sizes[0] - 1024)
+        return base - (0.2 if (gemm_budget, budget) == (100, 104) else 0.0)
+
+    def step(sizes, budget, gemm_budget=0):
+        calls.append((None if sizes is None else tuple(sizes), budget, gemm_budget))
+
+    def timer(fn, reps):
+        calls.clear()
+        fn()
+        (sizes, budget, gb), = calls
+        return cost(None if sizes is None else list(sizes), budget, gb)
+
+    pairs = [(76, 152), (100, 104), (128, 48)]
+    out = tuner.search(step, 2048, budgets=(64,), timer=timer, gemm_pairs=pairs)
+    n1 = len(tuner.candidate_splits(2048))
+    assert len(out["table"]) == n1 + 3 * 1 + 3 * len(pairs)
+    tail = out["table"][-3 * len(pairs):]
+    assert [(r["gemm_budget"], r["budget"]) for r in tail[:3]] == pairs
+    assert all(r["gemm_budget"] == 0 for r in out["table"][:n1 + 3])
+    assert out["best"]["sizes"] == [1024, 1024]
+    assert (out["best"]["gemm_budget"], out["best"]["budget"]) == (100, 104)
+
+
 def test_async_formation_worked_example_by_hand():
     """Asynchronous formation: step 1 is formed before step 0 is committed, so its decode rows
     read their tokens from step 0's rows (-(row + 1)); B samples eos at step 0, which is seen

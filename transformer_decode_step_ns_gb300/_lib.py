@@ -39,7 +39,7 @@ SYMBOLS = (
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
     "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async", "ns_find_prompt_chunks",
-    "ns_set_trace",
+    "ns_set_trace", "ns_set_gemm_cta_budget",
 )
 
 
@@ -129,6 +129,7 @@ def lib() -> ctypes.CDLL:
             "ns_last_error_message": ([], ctypes.c_char_p),
             "ns_set_kernel_timing": ([P, I], I),
             "ns_set_trace": ([P, I, ctypes.POINTER(TraceBufs)], I),
+            "ns_set_gemm_cta_budget": ([P, I], I),
             "ns_set_token_source": ([P, P], I),
             "ns_set_graph_buckets": ([P, I, P], I),
             "ns_set_kv_offload": ([P, P, ctypes.c_size_t], I),
@@ -250,7 +251,8 @@ def _stream(stream) -> Optional[int]:
 
 class GraphInfo(ctypes.Structure):
     _fields_ = [("batch", I), ("n_split", I), ("attn_cta_budget", I), ("with_lm", I),
-                ("chunk_rows", I), ("kv_offload", I), ("kernels", I), ("capture_ms", ctypes.c_double)]
+                ("chunk_rows", I), ("kv_offload", I), ("kernels", I), ("capture_ms", ctypes.c_double),
+                ("gemm_cta_budget", I)]
 
 
 class DecodeStep:
@@ -338,7 +340,11 @@ class DecodeStep:
         check(lib().ns_kv_free_count(self.h, ctypes.byref(n)))
         return n.value
 
-    def set_nanobatch(self, sizes: Optional[Sequence[int]] = None, attn_cta_budget: int = 0):
+    def set_nanobatch(self, sizes: Optional[Sequence[int]] = None, attn_cta_budget: int = 0,
+                      gemm_cta_budget: int = 0):
+        """Nano-batch split (None: unsplit) with the attention and persistent-GEMM CTA caps of
+        its nano-ops (0: none)."""
+        check(lib().ns_set_gemm_cta_budget(self.h, gemm_cta_budget))
         if not sizes or len(sizes) == 1:
             check(lib().ns_set_nanobatch(self.h, 1, None, attn_cta_budget))
             return

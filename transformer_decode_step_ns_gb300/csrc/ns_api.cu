@@ -395,6 +395,7 @@ struct ns_ctx {
   int n_split = 1;
   std::vector<int> split_sizes;
   int attn_budget = 0;
+  int gemm_budget = 0;  // persistent-GEMM CTA cap of nano-batched steps (ns_set_gemm_cta_budget)
   std::vector<int> buckets;  // graph batch sizes (ns_set_graph_buckets), ascending
   bool graph_chunks = true;  // steps with prompt chunks replay graphs too (ns_set_graph_chunks)
   int chunk_first = 0;       // rows [chunk_first, batch) of the current step form prefill
@@ -549,6 +550,7 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   const CUtensorMap* mb = nullptr;
   NS_TRY(get_bmap(h, x, x_cols, p.BN, &mb));
   TimeScope ts(h, s, kind);
+  if (grid > 0 && h->n_split > 1 && h->gemm_budget > 0) grid = std::min(grid, h->gemm_budget);
   if (grid > 0) {
     NS_CUDA(launch_gemm_persistent(&pr.mapA, mb, p, h->dtype, grid, s, true));
   } else {
@@ -816,7 +818,7 @@ bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int
 std::vector<int> graph_key(const ns_ctx* h, int B) {
   const uint64_t src = reinterpret_cast<uint64_t>(h->tok_src);
   const uint64_t kvh = reinterpret_cast<uint64_t>(h->kv_host);
-  std::vector<int> k{B, h->n_split, h->attn_budget, h->with_lm ? 1 : 0,
+  std::vector<int> k{B, h->n_split, h->attn_budget, h->n_split > 1 ? h->gemm_budget : 0, h->with_lm ? 1 : 0,
                      static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
                      h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32),
                      static_cast<int>(h->chunk_runs.size())};
@@ -861,6 +863,7 @@ ns_status get_graph(ns_ctx* h, int B, cudaGraphExec_t* out) {
   gi.batch = B;
   gi.n_split = h->n_split;
   gi.attn_cta_budget = h->attn_budget;
+  gi.gemm_cta_budget = h->n_split > 1 ? h->gemm_budget : 0;
   gi.with_lm = h->with_lm ? 1 : 0;
   gi.chunk_rows = h->chunk_first < B ? B - h->chunk_first : 0;
   gi.kv_offload = h->kv_host != nullptr ? 1 : 0;
@@ -1235,6 +1238,13 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
   h->n_split = n_split;
   h->split_sizes = s;
   h->attn_budget = attn_cta_budget > 0 ? attn_cta_budget : 0;
+  return NS_OK;
+}
+
+ns_status ns_set_gemm_cta_budget(ns_handle h, int gemm_cta_budget) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (gemm_cta_budget < 0) return fail(NS_ERR_INVALID_ARG, "gemm_cta_budget < 0");
+  h->gemm_budget = gemm_cta_budget;
   return NS_OK;
 }
 

@@ -16,15 +16,16 @@ two-stage MILP.  Here:
   the near-even ones in every order) is timed as a captured, replayed step; the fastest
   multi-batch splits are then timed at the attention CTA budgets the profile keeps (those
   where attention retains at least ``min_p`` of its solo throughput while co-running; the four
-  best when fewer than two do), and the fastest configuration overall is returned with the
-  whole table.
+  best when fewer than two do), then at the (GEMM budget, attention budget) pairs given, where
+  the projections of each nano-batch are capped at a number of SMs and the attention takes what
+  they leave, and the fastest configuration overall is returned with the whole table.
 
 Everything here only times library calls; the step itself runs in the library's kernels.
 """
 from __future__ import annotations
 
 import itertools
-from typing import Callable, Dict, List, Optional, Sequence
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 
 def _events():
@@ -133,24 +134,31 @@ def candidate_splits(batch: int, granularity: int = 128, max_nano: int = 4) -> L
     return out
 
 
-def search(step: Callable[[Optional[List[int]], int], None], batch: int,
+def search(step: Callable[..., None], batch: int,
            profile: Optional[Dict] = None, granularity: int = 128, max_nano: int = 4,
            budgets: Sequence[int] = tuple(range(8, 129, 8)), min_p: float = 0.5, top: int = 3,
-           reps: int = 5, timer: Optional[Callable[[Callable[[], None], int], float]] = None) -> Dict:
-    """Measure the candidate splits and attention budgets of one dense batch.
+           reps: int = 5, timer: Optional[Callable[[Callable[[], None], int], float]] = None,
+           gemm_pairs: Sequence[Tuple[int, int]] = ()) -> Dict:
+    """Measure the candidate splits and CTA budgets of one dense batch.
 
     ``step(sizes, budget)`` runs one step with that nano-batch split (None: unsplit) and
-    attention CTA budget (0: none).  Budgets come from ``profile`` when given (those whose
-    co-run P_attn >= min_p, or the four best), else ``budgets``.  ``timer(fn, reps)`` returns
-    the ms per call of fn (default: CUDA events).  Returns {"best": {sizes, budget, ms},
-    "table": [{sizes, budget, ms}, ...], "budgets_kept"} in measurement order.
+    attention CTA budget (0: none); for a pair of ``gemm_pairs`` = (GEMM budget, attention
+    budget) it is called as ``step(sizes, budget, gemm_budget)``.  Attention budgets come from
+    ``profile`` when given (those whose co-run P_attn >= min_p, or the four best), else
+    ``budgets``.  ``timer(fn, reps)`` returns the ms per call of fn (default: CUDA events).
+    Returns {"best": {sizes, budget, gemm_budget, ms}, "table": [...], "budgets_kept"} in
+    measurement order.
     """
     table = []
     timer = timer or _timed
 
-    def run(sizes, budget):
-        ms = timer(lambda: step(sizes, budget), reps)
-        table.append({"sizes": sizes or [batch], "budget": budget, "ms": round(ms, 4)})
+    def run(sizes, budget, gemm_budget=0):
+        if gemm_budget:
+            ms = timer(lambda: step(sizes, budget, gemm_budget), reps)
+        else:
+            ms = timer(lambda: step(sizes, budget), reps)
+        table.append({"sizes": sizes or [batch], "budget": budget, "gemm_budget": gemm_budget,
+                      "ms": round(ms, 4)})
         return ms
 
     stage1 = [(run(s, 0), i, s) for i, s in enumerate(candidate_splits(batch, granularity, max_nano))]
@@ -163,6 +171,9 @@ def search(step: Callable[[Optional[List[int]], int], None], batch: int,
     for _, _, s in multi:
         for b in keep:
             run(s, b)
+    for _, _, s in multi:
+        for g, b in gemm_pairs:
+            run(s, b, g)
     best = min(table, key=lambda r: r["ms"])
     return {"best": best, "table": table, "budgets_kept": list(keep)}
 
