@@ -189,6 +189,28 @@ def test_linear_rows_are_bitwise_the_same_in_either_gemm_kernel(cuda_lib, n, k, 
     assert rel_l2(full[rows].cpu().numpy(), ref) < 1e-4
 
 
+def test_vocabulary_wide_head_at_decode_batches(cuda_lib):
+    """A weight with four output tiles per SM (a vocabulary-wide head) runs the persistent kernel
+    even at decode batches (1..64 rows, token tiles of 16..64): rows match fp64 and do not depend
+    on the launch they are in."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n, k, m = 4 * sms * 128, 256, 40
+    w = to_dev(synth.normal(13, "wv", (n, k), "f16", std=0.05))
+    x = synth.normal(13, "xv", (m, k), "f16")
+    full = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    _lib.linear(w, to_dev(x), full, m, n, k, "f16")
+    for lo, hi in ((0, 1), (3, 20), (20, 40)):
+        part = torch.empty((hi - lo, n), dtype=torch.float32, device="cuda")
+        _lib.linear(w, to_dev(x[lo:hi]), part, hi - lo, n, k, "f16")
+        torch.cuda.synchronize()
+        assert torch.equal(part, full[lo:hi]), (lo, hi)
+    assert _lib.device_error() == 0
+    ref = storage_f64(x, "f16") @ storage_f64(from_dev(w).view(np.float16), "f16").T
+    assert rel_l2(full.cpu().numpy(), ref) < 1e-4
+
+
 def test_greedy_argmax_ties_to_lowest(cuda_lib):
     import torch
     from transformer_decode_step_ns_gb300 import _lib

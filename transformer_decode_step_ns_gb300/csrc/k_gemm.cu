@@ -591,8 +591,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 }
 
 // ------------------------------------------------------------------------------ persistent
-// Launches of more than 64 rows of an unsplit weight (the ridge point and the compute-bound
-// dense batches of the NanoFlow page) run a persistent variant: one CTA per SM loops over
+// Long launches of an unsplit weight (more than 64 rows at the ridge point and in the
+// compute-bound dense batches of the NanoFlow page, and vocabulary-wide heads at any row count)
+// run a persistent variant: one CTA per SM loops over
 // work units (token tile, 128-feature tile), token tiles fastest so CTAs running side by side
 // share a weight tile through L2.  The TMA warp streams every unit's stages through one deep
 // ring without stopping between units; the MMA warp alternates between two TMEM accumulators,

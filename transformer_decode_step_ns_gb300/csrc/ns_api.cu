@@ -126,7 +126,8 @@ int pick_bn(int m, int kb_per_split, int splits, int n_tiles, int sms) {
 int pick_bn_persistent(int m) { return pick_bn_capped(m, kMaxBN); }
 
 // The persistent kernel takes a launch of more than 64 rows of an unsplit weight when it has at
-// least two 256-token output tiles per SM.  A split weight stays on the cluster kernel, whose
+// least two 256-token output tiles per SM, and any launch of an unsplit weight with four or more
+// tiles per SM (a vocabulary-wide head).  A split weight stays on the cluster kernel, whose
 // distributed-shared-memory reduction is cheaper than a reduction through global memory
 // (measured: the LLaMA-3-8B split-K projections at 256 rows 27-48 us against 50-68 us).  A
 // short launch stays there too: the persistent kernel's CTA fills an SM, so under programmatic
@@ -134,8 +135,11 @@ int pick_bn_persistent(int m) { return pick_bn_capped(m, kMaxBN); }
 // (measured: the 8B gate/up projection at 256 rows 75 us in the step on clusters against 98
 // persistent, though 87 against 83 alone).  Both kernels give a row the same bits.
 bool use_persistent(int m, int splits, int n_tiles, int sms) {
-  if (m < kPersistentMinRows || splits != 1) return false;
-  return static_cast<long long>((m + kMaxBN - 1) / kMaxBN) * n_tiles >= 2LL * sms;
+  if (splits != 1) return false;
+  const long long tiles = static_cast<long long>((m + kMaxBN - 1) / kMaxBN) * n_tiles;
+  // a very long launch (a vocabulary-wide head: four or more tiles per SM) streams its weights
+  // through the persistent kernel's deep ring at any row count
+  return tiles >= 4LL * sms || (m >= kPersistentMinRows && tiles >= 2LL * sms);
 }
 
 // Split-K from the weight's shape only (never the batch): about one CTA per SM, so every
@@ -515,8 +519,8 @@ ns_status copy_gain(ns_ctx* h, const void* src, float** dst) {
   return NS_OK;
 }
 
-// Launch parameters of one projection over m rows: the persistent kernel for more than 64 rows
-// of an unsplit weight (its grid in *grid), else the cluster kernel (*grid = 0).
+// Launch parameters of one projection over m rows: the persistent kernel where use_persistent
+// says so (its grid in *grid), else the cluster kernel (*grid = 0).
 GemmParams proj_params(const Proj& pr, int m, int row0, int epi, int dtype, int sms, int* grid) {
   GemmParams p{};
   p.M = m;

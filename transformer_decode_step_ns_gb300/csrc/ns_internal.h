@@ -74,7 +74,7 @@ struct GemmParams {
   int tiles_m;  // persistent variant: token tiles of BN rows
 };
 
-// Launches of fewer rows than this never take the persistent GEMM (its tiles are wide).
+// Launches of fewer rows than this take the persistent GEMM only when they are very long.
 constexpr int kPersistentMinRows = 65;
 
 struct AttnParams {
