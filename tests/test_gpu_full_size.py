@@ -43,8 +43,9 @@ def _compact_tables(tables, seq_lens, bs):
     return used, out
 
 
-def _oracle_rows(model, shape, pools, meta, rows, bs):
-    """Oracle logits of `rows` of one step.  pools(l) -> (k_ptr, v_ptr) of layer l."""
+def _oracle_rows(model, shape, pools, meta, rows, bs, trace=None):
+    """Oracle logits of `rows` of one step.  pools(l) -> (k_ptr, v_ptr) of layer l; `trace`
+    receives the oracle's per-layer tensors of those rows."""
     tok, pos, tab, sl, slots = meta
     rows = np.asarray(rows)
     used, ctab = _compact_tables(tab[rows], sl[rows], bs)
@@ -57,7 +58,8 @@ def _oracle_rows(model, shape, pools, meta, rows, bs):
         vp.append(_download_blocks(v_ptr, used, blk_bytes, shape.dtype).reshape(shp))
     index = {b: i for i, b in enumerate(used)}
     cslots = np.array([index[int(s) // bs] * bs + int(s) % bs for s in slots[rows]], np.int64)
-    return oracle.decode_step(model, kp, vp, tok[rows], pos[rows], ctab, sl[rows], cslots, bs)
+    return oracle.decode_step(model, kp, vp, tok[rows], pos[rows], ctab, sl[rows], cslots, bs,
+                              trace=trace)
 
 
 class _LazyLayers:
@@ -137,7 +139,9 @@ def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
     """One LLaMA-2-70B-shaped layer over 1024 decode rows + a 1024-token prefill chunk, run
     with the uneven 768 + 1280 nano-batch split; logits through the tied head as the probe.
     Splits 1 and 1024 + 1024 (also with CTA budgets: projections on 100 SMs, attention on 104
-    CTAs) give the same logits bitwise."""
+    CTAs) give the same logits bitwise, and the layer's q, attention output and residuals of the
+    sampled decode and chunk rows are each within relative L2 1e-2 of the oracle (per tensor,
+    no probe head involved)."""
     import torch
     import bench
     nw = bench.NanoLayerWorkload()
@@ -149,7 +153,8 @@ def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
           "layers": [{k: _host(v) for k, v in lw.items()} for lw in nw.w["layers"]]}
     model = oracle.OracleModel.from_weights(sh, hw)
     pools = nw.dev.kv_layer_ptrs(0)
-    ref = _oracle_rows(model, sh, lambda l: pools, nw.meta, rows, nw.bs)
+    tr = {}
+    ref = _oracle_rows(model, sh, lambda l: pools, nw.meta, rows, nw.bs, trace=tr)
     logits = torch.empty((nw.B, sh.vocab), dtype=torch.float32, device="cuda")
     results = {}
     for split in ([768, 1280], None, [1024, 1024], "capped"):
@@ -170,6 +175,30 @@ def test_llama2_70b_layer_2048_rows_nano_batched(cuda_lib):
     np.testing.assert_array_equal(results["None"], results[str([768, 1280])])
     np.testing.assert_array_equal(results[str([1024, 1024])], results[str([768, 1280])])
     np.testing.assert_array_equal(results["capped"], results[str([768, 1280])])
+    # the layer's own tensors for the sampled rows (no probe head involved): q after RoPE, the
+    # attention output (decode kernel and prefill-chunk kernel rows) and both residuals, each
+    # within relative L2 1e-2 of the oracle's trace
+    qd = sh.n_q_heads * sh.head_dim
+    q_t = torch.empty((nw.B, qd), dtype=torch.bfloat16, device="cuda")
+    o_t = torch.empty_like(q_t)
+    rm = torch.empty((nw.B, sh.hidden), dtype=torch.float32, device="cuda")
+    ro = torch.empty_like(rm)
+    nw.dev.set_nanobatch([768, 1280])
+    nw.dev.set_trace(0, q=q_t, attn=o_t, resid_mid=rm, resid_out=ro)
+    nw.dev.step(*nw.meta, logits)
+    torch.cuda.synchronize()
+    nw.dev.set_trace(-1)
+    assert nw.dev.device_error() == 0
+    np.testing.assert_array_equal(logits[rows].cpu().numpy(), results[str([768, 1280])])
+    idx = torch.tensor(rows, device="cuda")
+    got_t = {"q": oracle.from_storage(_host(q_t[idx]), "bf16").reshape(len(rows), sh.n_q_heads, -1),
+             "attn": oracle.from_storage(_host(o_t[idx]), "bf16").reshape(len(rows), sh.n_q_heads, -1),
+             "resid_attn": rm[idx].cpu().numpy().astype(np.float64),
+             "resid": ro[idx].cpu().numpy().astype(np.float64)}
+    for name, g in got_t.items():
+        for part, sel in (("decode rows", slice(0, len(dec_rows))), ("chunk rows", slice(len(dec_rows), None))):
+            e = rel_l2(g[sel], tr[name][0][sel])
+            assert e < 1e-2, (name, part, e)
 
 
 def test_llama3_8b_32_layers_batch_256(cuda_lib):
