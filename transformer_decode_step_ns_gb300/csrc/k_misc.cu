@@ -30,10 +30,13 @@ struct EV<__nv_bfloat16> {
 
 }  // namespace
 
-// grid = batch rows, block = 128 threads (one thread per column of each 128-column tile).
+// grid = batch rows, block = 128 threads (one thread per column of each 128-column tile).  The
+// row is read kEmbedTiles tiles at a time, all loads in flight before any result is used.
+constexpr int kEmbedTiles = 16;
+
 template <typename T>
 __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
-  __shared__ float warp_sums[4];
+  __shared__ float warp_sums[kEmbedTiles][4];
   const int row = p.row0 + blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Token ids and positions are step metadata, complete before the step: read them early.
@@ -51,19 +54,30 @@ __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
   const T* e = reinterpret_cast<const T*>(p.embed) + static_cast<size_t>(tok) * p.hidden;
   T* xn = reinterpret_cast<T*>(p.xn) + static_cast<size_t>(row) * p.hidden;
   float* resid = p.resid + static_cast<size_t>(row) * p.hidden;
-  for (int t = 0; t < p.hidden / 128; ++t) {
-    const int i = t * 128 + tid;
-    const float v = EV<T>::to_f(e[i]);
-    resid[i] = v;
-    xn[i] = EV<T>::from_f(v * p.gamma[i]);
-    float s = v * v;
+  const int n_tiles = p.hidden / 128;
+  for (int t0 = 0; t0 < n_tiles; t0 += kEmbedTiles) {
+    float v[kEmbedTiles], g[kEmbedTiles];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) warp_sums[warp] = s;
+    for (int u = 0; u < kEmbedTiles; ++u) {
+      const int i = (t0 + u) * 128 + tid;
+      v[u] = t0 + u < n_tiles ? EV<T>::to_f(e[i]) : 0.f;
+      g[u] = t0 + u < n_tiles ? p.gamma[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kEmbedTiles; ++u) {
+      if (t0 + u >= n_tiles) break;
+      const int i = (t0 + u) * 128 + tid;
+      resid[i] = v[u];
+      xn[i] = EV<T>::from_f(v[u] * g[u]);
+      float s = v[u] * v[u];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) warp_sums[u][warp] = s;
+    }
     __syncthreads();
-    if (tid == 0) {
-      p.sumsq[static_cast<size_t>(t) * p.sumsq_ld + row] =
-          (warp_sums[0] + warp_sums[1]) + (warp_sums[2] + warp_sums[3]);
+    if (tid < kEmbedTiles && t0 + tid < n_tiles) {
+      const float* w = warp_sums[tid];
+      p.sumsq[static_cast<size_t>(t0 + tid) * p.sumsq_ld + row] = (w[0] + w[1]) + (w[2] + w[3]);
     }
     __syncthreads();
   }
