@@ -1489,9 +1489,11 @@ def qwen_report(args, peaks, world):
            "device_error": wl.dev.device_error()}
     wl.dev.close()
     del wl
-    sweep = []
-    for B in (1, 8):
+    def timed(B, step_kernel):
+        """Graph-replayed steps of batch B with the given ns_set_step_kernel mode."""
         sw = DecodeWorkload(B, total_steps=70)
+        if step_kernel:
+            sw.dev.set_step_kernel(1)
         for _ in range(5):
             sw.step(sw.next_meta())
         sm = [sw.next_meta() for _ in range(50)]
@@ -1505,12 +1507,17 @@ def qwen_report(args, peaks, world):
         ms = s0.elapsed_time(s1) / len(sm)
         wk = rl.decode_step_work(sw.shape, sm[-1][3])
         tr = rl.step_roofline_time(wk.flops, wk.total_bytes, tflops, hbm * 1e9)
-        sweep.append({"batch": B, "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
-                      "roofline_us": round(tr * 1e6, 1), "frac_of_roofline": round(tr / (ms * 1e-3), 4)})
+        row = {"batch": B, "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+               "roofline_us": round(tr * 1e6, 1), "frac_of_roofline": round(tr / (ms * 1e-3), 4),
+               "kernels_per_step": sw.dev.info().kernels_per_step, "device_error": sw.dev.device_error()}
         sw.dev.close()
         del sw
-    out["batch_sweep"] = sweep
-    torch.cuda.empty_cache()
+        torch.cuda.empty_cache()
+        return row
+
+    out["batch_sweep"] = [timed(B, False) for B in (1, 8)]
+    # the persistent step kernel (ns_set_step_kernel mode 1) on the same workloads
+    out["step_kernel"] = [timed(B, True) for B in (1, 8, 32)]
     return out
 
 

@@ -277,6 +277,25 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
  * INVALID_ARG.  Unsplit steps ignore it. */
 ns_status ns_set_gemm_cta_budget(ns_handle h, int gemm_cta_budget);
 
+/* How a step is run ("The chef who calls out every order" and "The maths that matters: when the
+ * GPU is left waiting" in the nanoserve notes: at small batch a decode step is a chain of short
+ * kernels whose launch and dependency waits cost more than their own weight reads).
+ *   mode 0 (the default): one kernel per stage (embedding, per layer QKV, attention, O,
+ *     gate/up, down, then the LM head), captured in a graph when the handle uses graphs.
+ *   mode 1: steps of at most 32 decode rows, without nano-batches, prefill chunks, KV offload,
+ *     trace or per-kernel timing, run as one persistent cooperative kernel with one CTA per SM
+ *     (a grid-wide barrier between stages, each CTA streaming its share of every layer's weights
+ *     into shared memory ahead of the stages); other steps keep mode 0's kernels.
+ * The first switch to mode 1 packs a second copy of every projection weight and of the LM head
+ * (the handle's weight bytes again) into per-CTA streams and allocates small step buffers;
+ * mode 0 keeps them for a later switch back, ns_destroy frees them.  The two modes sum in
+ * different orders, so a row's bits differ between them (both are checked against the oracle);
+ * within mode 1 a row's result depends only on its own inputs, as in mode 0.  Graphs are
+ * cached per mode.  UNSUPPORTED when head_dim is not 64 or 128, a KV head serves more than 8
+ * query heads, ffn is not a multiple of 128 or hidden exceeds 4096; OUT_OF_MEMORY when the packed copy does not
+ * fit.  mode outside {0, 1}: INVALID_ARG. */
+ns_status ns_set_step_kernel(ns_handle h, int mode);
+
 /* One decode step for `batch` rows.  Host metadata (validated, packed into one pinned buffer
  * and uploaded with a single host-to-device copy on `stream`):
  *   token_ids [batch] int32 in [0, V) (with a device token source set, NULL or entries

@@ -444,3 +444,12 @@ def test_step_metadata_validation_equals_the_stated_rules(L):
 
     run()
     assert seen[0] >= 20 and seen[1] >= 20, seen  # both outcomes well exercised
+
+
+def test_handle_setters_refuse_a_null_handle_without_touching_the_device(L):
+    """ns_set_step_kernel, ns_set_nanobatch and ns_set_gemm_cta_budget return INVALID_ARG for a
+    NULL handle (checked before any CUDA call)."""
+    assert L.ns_set_step_kernel(None, 1) == 1
+    assert L.ns_set_step_kernel(None, 0) == 1
+    assert L.ns_set_gemm_cta_budget(None, 4) == 1
+    assert L.ns_set_nanobatch(None, 1, None, 0) == 1

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libns.so")
-SOURCES = ["k_gemm.cu", "k_attn.cu", "k_prefill.cu", "k_misc.cu", "ns_api.cu", "ns_noalloc.cu", "ns_sched.cpp"]
+SOURCES = ["k_gemm.cu", "k_attn.cu", "k_prefill.cu", "k_misc.cu", "k_step.cu", "ns_api.cu", "ns_noalloc.cu", "ns_sched.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -39,7 +39,7 @@ SYMBOLS = (
     "ns_sched_add", "ns_sched_next", "ns_sched_moves", "ns_sched_commit", "ns_sched_tokens",
     "ns_sched_counts", "ns_capture_graphs", "ns_get_graph_report", "ns_attn_decode_capped",
     "ns_set_graph_chunks", "ns_sched_remove", "ns_sched_set_async", "ns_find_prompt_chunks",
-    "ns_set_trace", "ns_set_gemm_cta_budget",
+    "ns_set_trace", "ns_set_gemm_cta_budget", "ns_set_step_kernel",
 )
 
 
@@ -130,6 +130,7 @@ def lib() -> ctypes.CDLL:
             "ns_set_kernel_timing": ([P, I], I),
             "ns_set_trace": ([P, I, ctypes.POINTER(TraceBufs)], I),
             "ns_set_gemm_cta_budget": ([P, I], I),
+            "ns_set_step_kernel": ([P, I], I),
             "ns_set_token_source": ([P, P], I),
             "ns_set_graph_buckets": ([P, I, P], I),
             "ns_set_kv_offload": ([P, P, ctypes.c_size_t], I),
@@ -350,6 +351,11 @@ class DecodeStep:
             return
         a = np.ascontiguousarray(sizes, dtype=np.int32)
         check(lib().ns_set_nanobatch(self.h, a.size, _ptr(a), attn_cta_budget))
+
+    def set_step_kernel(self, mode: int) -> None:
+        """0: one kernel per stage; 1: steps of at most 32 decode rows as one persistent kernel
+        (ns_set_step_kernel)."""
+        check(lib().ns_set_step_kernel(self.h, int(mode)))
 
     def step(self, token_ids, positions, block_tables, seq_lens, slot_mapping, logits,
              stream=None) -> None:

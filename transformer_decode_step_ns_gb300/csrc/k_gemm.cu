@@ -29,6 +29,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "ns_epi.cuh"
 #include "ns_internal.h"
 #include "ns_ptx.cuh"
 
@@ -59,24 +60,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void set_err(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
-}
-
-// The epilogue formulas, written once for both kernels with explicit roundings so the two give
-// a row the same bits whichever launch it is in.
-// RoPE on one (i, i + d/2) pair: (x_lo, x_hi) -> (x_lo c - x_hi s, x_hi c + x_lo s).
-__device__ __forceinline__ float rope_lo(float x_lo, float x_hi, float c, float sn) {
-  return __fmaf_rn(x_lo, c, -__fmul_rn(x_hi, sn));
-}
-__device__ __forceinline__ float rope_hi(float x_lo, float x_hi, float c, float sn) {
-  return __fmaf_rn(x_hi, c, __fmul_rn(x_lo, sn));
-}
-// silu(g) * u
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fmul_rn(__fdividef(g, __fadd_rn(1.f, __expf(-g))), u);
-}
-// 1 / sqrt(mean of squares + eps) from a row's summed squares
-__device__ __forceinline__ float rms_scale(float sumsq, int n, float eps) {
-  return rsqrtf(__fadd_rn(__fdiv_rn(sumsq, static_cast<float>(n)), eps));
 }
 
 }  // namespace

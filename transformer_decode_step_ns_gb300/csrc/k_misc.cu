@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "ns_epi.cuh"
 #include "ns_internal.h"
 #include "ns_ptx.cuh"
 
@@ -81,17 +82,11 @@ __global__ void __launch_bounds__(128) embed_rope_kernel(const EmbedParams p) {
     }
     __syncthreads();
   }
-  // RoPE table for this row: angle = pos * inv_freq_i in fp64 (inv_freq_i = theta^(-2i/d) is a
-  // host-computed fp64 table), reduced to [-pi, pi] with the two-constant Cody-Waite scheme
-  // (Cody & Waite, "Software Manual for the Elementary Functions", 1980), then fp32 sincosf.
+  // RoPE table for this row (fp64 angle, Cody-Waite reduction, fp32 sincosf)
   const int half = p.head_dim / 2;
   for (int i = tid; i < half; i += 128) {
-    const double ang = static_cast<double>(pos) * p.inv_freq[i];
-    const double k = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
-    double r = fma(-k, 6.283185307179586, ang);           // 2 pi, high part
-    r = fma(-k, 2.4492935982947064e-16, r);               // 2 pi - high part
     float sn, cs;
-    sincosf(static_cast<float>(r), &sn, &cs);
+    rope_cos_sin(pos, p.inv_freq[i], &cs, &sn);
     p.rope_cos[static_cast<size_t>(row) * half + i] = cs;
     p.rope_sin[static_cast<size_t>(row) * half + i] = sn;
   }

@@ -442,6 +442,21 @@ struct ns_ctx {
   };
   std::vector<TimedLaunch> timed;
   ns_kernel_timing timing_acc{};
+  // persistent step kernel (ns_set_step_kernel): mode and its device resources
+  int step_mode = 0;
+  struct StepDev {
+    int grid = 0, nslot = 0, max_ch = 1;
+    size_t smem = 0, wpack_bytes = 0, sync_bytes = 0;
+    StepParams shape{};            // stage tiles, chunks, splits, rotations
+    uint8_t* wpack = nullptr;
+    long long* streams = nullptr;  // stream_off [grid + 1], then stream_lm [grid]
+    float* norms = nullptr;        // attention-norm gains [n_layers][H], then FFN-norm gains
+    float* sumsq16 = nullptr;      // [kStepMaxRows][H / 16]
+    float* part = nullptr;         // attention partials
+    float* split_part = nullptr;   // split-K partial tiles
+    unsigned* sync = nullptr;      // barrier word, abort flag, attention and split-K counters
+  };
+  StepDev* step = nullptr;
 };
 
 namespace {
@@ -580,8 +595,91 @@ ns_status launch_proj(ns_ctx* h, const Proj& pr, const void* x, int x_cols, int 
   return NS_OK;
 }
 
+void free_step(ns_ctx* h) {
+  if (h->step == nullptr) return;
+  ns_ctx::StepDev* sd = h->step;
+  cudaFree(sd->wpack);
+  cudaFree(sd->streams);
+  cudaFree(sd->split_part);
+  cudaFree(sd->norms);
+  cudaFree(sd->sumsq16);
+  cudaFree(sd->part);
+  cudaFree(sd->sync);
+  delete sd;
+  h->step = nullptr;
+  h->step_mode = 0;
+}
+
+// The persistent step kernel takes a step when it is switched on and the step is plain decode
+// of at most kStepMaxRows rows on one stream with nothing else to emit.
+bool step_kernel_takes(const ns_ctx* h, int B) {
+  return h->step_mode == 1 && h->step != nullptr && B <= kStepMaxRows && h->n_split <= 1 &&
+         h->chunk_runs.empty() && h->kv_host == nullptr && h->trace_layer < 0 && !h->timing;
+}
+
+ns_status enqueue_step_persistent(ns_ctx* h, int B, cudaStream_t s) {
+  const ns_model_cfg& c = h->cfg;
+  const ns_ctx::StepDev& sd = *h->step;
+  const MetaLayout ml = meta_layout(B, c.max_blocks_per_seq);
+  StepParams p = sd.shape;
+  p.B = B;
+  p.H = c.hidden;
+  p.d = c.head_dim;
+  p.Hq = c.n_q_heads;
+  p.Hkv = c.n_kv_heads;
+  p.G = c.n_q_heads / c.n_kv_heads;
+  p.qd = c.n_q_heads * c.head_dim;
+  p.kvd = c.n_kv_heads * c.head_dim;
+  p.F = c.ffn;
+  p.vocab = c.vocab;
+  p.n_layers = c.n_layers;
+  p.eps = c.rms_eps;
+  p.scale_log2 = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.head_dim)) * 1.4426950408889634);
+  p.nslot = sd.nslot;
+  p.with_lm = h->with_lm ? 1 : 0;
+  p.wpack = sd.wpack;
+  p.stream_off = sd.streams;
+  p.stream_lm = sd.streams + sd.grid + 1;
+  p.embed = h->embed;
+  p.attn_norm = sd.norms;
+  p.ffn_norm = sd.norms + static_cast<size_t>(c.n_layers) * c.hidden;
+  p.final_norm = h->final_norm;
+  p.pools = static_cast<uint8_t*>(h->pools);
+  p.pool_bytes = static_cast<size_t>(static_cast<uint8_t*>(h->vpool[0]) - static_cast<uint8_t*>(h->kpool[0]));
+  p.num_blocks = h->num_blocks + 1;  // + padding block
+  p.mb = c.max_blocks_per_seq;
+  p.block_size = h->block_size;
+  p.pool_slots = static_cast<long long>(h->num_blocks + 1) * h->block_size;
+  p.tok = reinterpret_cast<const int*>(h->meta_dev + ml.tok);
+  p.tok_src = h->tok_src;
+  p.pos = reinterpret_cast<const int*>(h->meta_dev + ml.pos);
+  p.seq = reinterpret_cast<const int*>(h->meta_dev + ml.seq);
+  p.slot = reinterpret_cast<const long long*>(h->meta_dev + ml.slot);
+  p.tab = reinterpret_cast<const int*>(h->meta_dev + ml.tab);
+  p.logits_slot = reinterpret_cast<const unsigned long long*>(h->meta_dev + ml.logits);
+  p.rows_valid = reinterpret_cast<const int*>(h->meta_dev + ml.flags) + 1;
+  p.early_ok = reinterpret_cast<const int*>(h->meta_dev + ml.flags);
+  p.inv_freq = h->inv_freq;
+  p.resid = h->resid;
+  p.xn = h->xn;
+  p.q = h->q;
+  p.o = h->o;
+  p.act = h->act;
+  p.sumsq16 = sd.sumsq16;
+  p.split_part = sd.split_part;
+  p.attn_part = sd.part;
+  p.max_ch = sd.max_ch;
+  p.sync = sd.sync;
+  p.err = h->err;
+  NS_CUDA(cudaMemsetAsync(sd.sync, 0, sd.sync_bytes, s));
+  NS_CUDA(launch_step(p, h->dtype, sd.grid, sd.smem, s));
+  h->kernels_last = 1;
+  return NS_OK;
+}
+
 // Enqueue one step for `B` rows on `s0` (and the side stream when nano-batched).
 ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
+  if (step_kernel_takes(h, B)) return enqueue_step_persistent(h, B, s0);
   const ns_model_cfg& c = h->cfg;
   const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, F = c.ffn;
   const int qd = Hq * d, kvd = Hkv * d;
@@ -838,7 +936,7 @@ bool early_fetch_ok(ns_ctx* h, int batch, const int32_t* block_tables, const int
 std::vector<int> graph_key(const ns_ctx* h, int B) {
   const uint64_t src = reinterpret_cast<uint64_t>(h->tok_src);
   const uint64_t kvh = reinterpret_cast<uint64_t>(h->kv_host);
-  std::vector<int> k{B, h->n_split, h->attn_budget, h->n_split > 1 ? h->gemm_budget : 0, h->with_lm ? 1 : 0,
+  std::vector<int> k{B, h->step_mode, h->n_split, h->attn_budget, h->n_split > 1 ? h->gemm_budget : 0, h->with_lm ? 1 : 0,
                      static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
                      h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32),
                      static_cast<int>(h->chunk_runs.size())};
@@ -954,6 +1052,7 @@ void ns_destroy(ns_handle h) {
   cudaFree(h->pools);
   cudaFree(h->attn_counters);
   cudaFree(h->attn_partials);
+  free_step(h);
   cudaFreeHost(h->meta_host);
   cudaFree(h->meta_dev);
   cudaFree(h->err);
@@ -1258,6 +1357,153 @@ ns_status ns_set_nanobatch(ns_handle h, int n_split, const int* sizes, int attn_
   h->n_split = n_split;
   h->split_sizes = s;
   h->attn_budget = attn_cta_budget > 0 ? attn_cta_budget : 0;
+  return NS_OK;
+}
+
+ns_status ns_set_step_kernel(ns_handle h, int mode) {
+  if (h == nullptr) return fail(NS_ERR_INVALID_ARG, "null handle");
+  if (mode != 0 && mode != 1) return fail(NS_ERR_INVALID_ARG, "mode must be 0 or 1");
+  if (mode == 0 || h->step != nullptr) {
+    h->step_mode = mode;
+    return NS_OK;
+  }
+  const ns_model_cfg& c = h->cfg;
+  const int H = c.hidden, d = c.head_dim, F = c.ffn, G = c.n_q_heads / c.n_kv_heads;
+  const int qd = c.n_q_heads * d, kvd = c.n_kv_heads * d;
+  if ((d != 64 && d != 128) || G > 8 || F % 128 != 0 || H > 4096)
+    return fail(NS_ERR_UNSUPPORTED, "persistent step: head_dim 64 or 128, at most 8 query heads per KV head, ffn a multiple of 128, hidden at most 4096");
+  NS_CUDA(cudaSetDevice(h->dev));
+  int smem_max = 0;
+  NS_CUDA(cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
+  const long long room = static_cast<long long>(smem_max) - static_cast<long long>(step_smem_bytes(d, 0));
+  const int nslot = static_cast<int>(room / (kStepSlot + 16));
+  if (nslot < 4) return fail(NS_ERR_UNSUPPORTED, "persistent step: too little shared memory");
+  const size_t smem = step_smem_bytes(d, nslot);
+  int per_sm = 0;
+  NS_CUDA(step_configure(h->dtype, d, smem, &per_sm));
+  if (per_sm < 1) return fail(NS_ERR_UNSUPPORTED, "persistent step: kernel does not fit an SM");
+  const int grid = h->sms;
+  // per stage: 16-row output tiles, 128-column chunks of the reduction, K splits (reductions
+  // longer than kStepSliceChunks chunks), round-robin start of unsplit stages (each stage
+  // continues where the previous one stopped, spreading a layer's tiles over the SMs)
+  StepParams sh{};
+  sh.n_layers = c.n_layers;
+  sh.n_tiles[SS_QKV] = (qd + 2 * kvd) / 16;
+  sh.kc[SS_QKV] = H / 128;
+  sh.n_tiles[SS_O] = H / 16;
+  sh.kc[SS_O] = qd / 128;
+  sh.n_tiles[SS_GU] = F / 8;
+  sh.kc[SS_GU] = H / 128;
+  sh.n_tiles[SS_DOWN] = H / 16;
+  sh.kc[SS_DOWN] = F / 128;
+  sh.n_tiles[SS_LM] = c.vocab / 16;
+  sh.kc[SS_LM] = H / 128;
+  int rot = 0;
+  for (int k = 0; k < SS_COUNT; ++k) {
+    sh.split[k] = (sh.kc[k] + kStepSliceChunks - 1) / kStepSliceChunks;
+    sh.rot[k] = k == SS_LM ? 0 : rot % grid;
+    if (k != SS_LM && sh.split[k] == 1) rot += sh.n_tiles[k];
+    if (sh.split[k] > 1) sh.max_split_tiles = std::max(sh.max_split_tiles, sh.n_tiles[k]);
+  }
+  StepPlan plan;
+  if (!build_step_plan(grid, sh, &plan))
+    return fail(NS_ERR_UNSUPPORTED, "persistent step: a reduction needs more than 8 splits or a CTA more than 32 split tiles");
+  // the chunk stream of every CTA, in the order its compute warps consume it
+  const long long n_chunks = plan.stream_off[grid];
+  std::vector<PackDesc> desc;
+  desc.reserve(static_cast<size_t>(n_chunks));
+  const int nrope = (c.n_q_heads + c.n_kv_heads) * (d / 16);
+  auto emit = [&](int k, const StepTiles& t, int l) {
+    for (int g0 = 0; g0 < t.count; g0 += kStepGroup) {
+      const int tg = std::min(kStepGroup, t.count - g0);
+      for (int kc = t.kc0; kc < t.kc1; ++kc)
+        for (int ti = 0; ti < tg; ++ti) {
+          const int tile = t.first + (g0 + ti) * t.stride;
+          PackDesc pd{};
+          pd.kc = kc;
+          pd.tile = tile;
+          pd.kind = PK_PLAIN;
+          pd.row0 = tile * 16;
+          if (k == SS_QKV) {
+            pd.w = h->layers[l].qkv.w;
+            pd.K = H;
+            if (tile < nrope) {
+              pd.kind = PK_ROPE;
+            } else {
+              pd.row0 = qd + kvd + (tile - nrope) * 16;
+            }
+          } else if (k == SS_O) {
+            pd.w = h->layers[l].o.w;
+            pd.K = qd;
+          } else if (k == SS_GU) {
+            pd.w = h->layers[l].gu.w;
+            pd.K = H;
+            pd.kind = PK_GU;
+          } else if (k == SS_DOWN) {
+            pd.w = h->layers[l].down.w;
+            pd.K = F;
+          } else {
+            pd.w = h->lm.w;
+            pd.K = H;
+          }
+          desc.push_back(pd);
+        }
+    }
+  };
+  for (int cta = 0; cta < grid; ++cta) {
+    for (int l = 0; l < c.n_layers; ++l)
+      for (int k : {SS_QKV, SS_O, SS_GU, SS_DOWN})
+        emit(k, step_tiles(grid, cta, sh.n_tiles[k], sh.kc[k], sh.split[k], sh.rot[k]), l);
+    emit(SS_LM, step_tiles(grid, cta, sh.n_tiles[SS_LM], sh.kc[SS_LM], sh.split[SS_LM], sh.rot[SS_LM]), 0);
+  }
+  if (static_cast<long long>(desc.size()) != n_chunks)
+    return fail(NS_ERR_CUDA, "persistent step: chunk plan inconsistent");
+  auto* sd = new ns_ctx::StepDev();
+  sd->grid = grid;
+  sd->nslot = nslot;
+  sd->smem = smem;
+  sd->max_ch = (c.max_blocks_per_seq + kStepAttnBlocks - 1) / kStepAttnBlocks;
+  sd->wpack_bytes = static_cast<size_t>(n_chunks) * kStepChunk;
+  sd->shape = sh;
+  sd->sync_bytes = (2 + static_cast<size_t>(c.n_layers) * kStepMaxRows * c.n_kv_heads +
+                    (static_cast<size_t>(c.n_layers) + 1) * 4 * sh.max_split_tiles) * sizeof(unsigned);
+  h->step = sd;
+  auto cuda = [&](cudaError_t e, const char* what) -> ns_status {
+    if (e == cudaSuccess) return NS_OK;
+    free_step(h);
+    return fail(e == cudaErrorMemoryAllocation ? NS_ERR_OUT_OF_MEMORY : NS_ERR_CUDA,
+                std::string("persistent step: ") + what + ": " + cudaGetErrorString(e));
+  };
+  NS_TRY(cuda(cudaMalloc(&sd->wpack, sd->wpack_bytes), "weights"));
+  PackDesc* ddesc = nullptr;
+  NS_TRY(cuda(cudaMalloc(&ddesc, desc.size() * sizeof(PackDesc)), "pack descriptors"));
+  cudaError_t e = cudaMemcpy(ddesc, desc.data(), desc.size() * sizeof(PackDesc), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = launch_step_pack(ddesc, n_chunks, sd->wpack, d, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  cudaFree(ddesc);
+  NS_TRY(cuda(e, "pack"));
+  NS_TRY(cuda(cudaMalloc(&sd->streams, (2 * static_cast<size_t>(grid) + 1) * sizeof(long long)), "plan"));
+  NS_TRY(cuda(cudaMemcpy(sd->streams, plan.stream_off.data(), (grid + 1) * sizeof(long long), cudaMemcpyHostToDevice), "plan"));
+  NS_TRY(cuda(cudaMemcpy(sd->streams + grid + 1, plan.stream_lm.data(), grid * sizeof(long long), cudaMemcpyHostToDevice), "plan"));
+  size_t split_floats = 16;
+  for (int k = 0; k < SS_COUNT; ++k)
+    if (sh.split[k] > 1)
+      split_floats = std::max(split_floats, static_cast<size_t>(sh.n_tiles[k]) * sh.split[k] * kStepMaxRows * 16);
+  NS_TRY(cuda(cudaMalloc(&sd->split_part, split_floats * sizeof(float)), "split partials"));
+  NS_TRY(cuda(cudaMalloc(&sd->norms, 2 * static_cast<size_t>(c.n_layers) * H * sizeof(float)), "norms"));
+  for (int l = 0; l < c.n_layers; ++l) {
+    NS_TRY(cuda(cudaMemcpy(sd->norms + static_cast<size_t>(l) * H, h->layers[l].attn_norm, H * sizeof(float),
+                           cudaMemcpyDeviceToDevice), "norms"));
+    NS_TRY(cuda(cudaMemcpy(sd->norms + (static_cast<size_t>(c.n_layers) + l) * H, h->layers[l].ffn_norm,
+                           H * sizeof(float), cudaMemcpyDeviceToDevice), "norms"));
+  }
+  NS_TRY(cuda(cudaMalloc(&sd->sumsq16, static_cast<size_t>(H / 16) * kStepMaxRows * sizeof(float)), "sums"));
+  NS_TRY(cuda(cudaMemset(sd->sumsq16, 0, static_cast<size_t>(H / 16) * kStepMaxRows * sizeof(float)), "sums"));
+  const size_t part = static_cast<size_t>(kStepMaxRows) * c.n_kv_heads * sd->max_ch * G * (d + 2);
+  NS_TRY(cuda(cudaMalloc(&sd->part, part * sizeof(float)), "attention partials"));
+  NS_TRY(cuda(cudaMalloc(&sd->sync, sd->sync_bytes), "sync"));
+  NS_TRY(cuda(cudaMemset(sd->sync, 0, sd->sync_bytes), "sync"));
+  h->step_mode = 1;
   return NS_OK;
 }
 

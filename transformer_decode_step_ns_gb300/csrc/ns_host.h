@@ -3,6 +3,8 @@
 // does not depend on this file.
 #pragma once
 
+#include <vector>
+
 #include "ns_internal.h"
 
 namespace ns {
@@ -32,6 +34,20 @@ cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool p
 cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,
                           cudaStream_t s);
 cudaError_t launch_kv_copy(const KvCopyParams& p, int sms, cudaStream_t s);
+
+// Persistent step kernel (k_step.cu).
+struct StepPlan {
+  std::vector<long long> stream_off;  // [grid + 1] first chunk of each CTA's weight stream
+  std::vector<long long> stream_lm;   // [grid] first LM-head chunk of each CTA's stream
+};
+// The CTAs' weight streams for the stages of p (n_tiles, kc, split, rot, n_layers); false when
+// a split is outside 1..8 or a CTA would hold more split tiles than kStepMaxTilesPerCta.
+bool build_step_plan(int grid, const StepParams& p, StepPlan* out);
+size_t step_smem_bytes(int head_dim, int nslot);
+cudaError_t step_configure(int dtype, int head_dim, size_t smem, int* blocks_per_sm);
+cudaError_t launch_step(const StepParams& p, int dtype, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_step_pack(const PackDesc* desc, long long n, uint8_t* out, int head_dim,
+                             cudaStream_t s);
 
 // Record the text ns_last_error_message() returns on this thread.
 void set_last_error(const char* msg);

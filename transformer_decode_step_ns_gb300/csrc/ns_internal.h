@@ -166,6 +166,127 @@ __host__ __device__ inline int attn_max_chunks(int L_max) {
   return c < 1 ? 1 : (c < kAttnMaxChunks ? c : kAttnMaxChunks);
 }
 
+// ------------------------------------------------------------------ persistent step kernel
+// One cooperative launch runs a whole decode step of at most kStepMaxRows rows (k_step.cu).
+constexpr int kStepMaxRows = 32;
+// 7 compute warps + 1 weight-streaming warp: with 8 warps each of the SM's four register-file
+// partitions holds two warps, so a thread may use up to 255 registers.
+constexpr int kStepWarps = 7;                          // compute warps
+constexpr int kStepThreads = (kStepWarps + 1) * 32;    // + one weight-streaming warp
+constexpr int kStepChunk = 4096;                       // bytes of one weight chunk: 16 x 128
+// Ring slots hold kStepSlotChunks consecutive chunks, fetched by one bulk copy: measured on
+// GB300, 4 KiB TMA bulk copies stream at most ~16 GB/s per SM (their per-request cost), 16 KiB
+// copies ~47 GB/s per SM (the HBM share of an SM).
+constexpr int kStepSlotChunks = 4;
+constexpr int kStepSlot = kStepChunk * kStepSlotChunks;
+constexpr int kStepGroup = 2;                          // output tiles reduced together
+constexpr int kStepAttnBlocks = 2 * kStepWarps;        // cache blocks per attention unit
+constexpr int kStepRedStride = 24;                     // floats per token row of a reduced tile
+// A stage copies the activation columns it reduces over, for every row, into shared memory with
+// one bulk copy; at most kStepSliceChunks 128-column chunks (64 KiB at 32 rows).  Longer
+// reductions are split over teams of CTAs (split-K), the splits summed in split order.
+constexpr int kStepSliceChunks = 8;
+constexpr int kStepActBytes = kStepSliceChunks * kStepMaxRows * 256;
+constexpr int kStepMaxTilesPerCta = 32;                // tiles of one split stage per CTA
+
+enum StepStage : int { SS_QKV = 0, SS_O = 1, SS_GU = 2, SS_DOWN = 3, SS_LM = 4, SS_COUNT = 5 };
+
+// How one 16-row output tile of a projection maps to weight rows.
+enum PackKind : int {
+  PK_PLAIN = 0,  // rows row0 .. row0 + 15
+  PK_ROPE = 1,   // q/k head tile: rows 0-7 are features j*8.. of the head's first half, rows
+                 // 8-15 the same features of its second half (RoPE partners)
+  PK_GU = 2,     // rows 0-7 gate features j*8.., rows 8-15 the same up features
+};
+
+// One 4 KiB chunk of the packed weight stream: tile `tile` of matrix `w` (K columns),
+// columns kc*128 .. kc*128 + 127.
+struct PackDesc {
+  const void* w;
+  int K, kind, tile, kc, row0, pad;
+};
+
+// The output tiles one CTA computes in a stage: tiles first, first + stride, ... (count of them)
+// over columns [kc0, kc1) of the reduction (split `split` of the stage).  An unsplit stage deals
+// its tiles round-robin from CTA `rot`; a stage split S ways forms teams of S consecutive CTAs,
+// team q taking tiles q, q + teams, ... and member s the s-th column range.
+struct StepTiles {
+  int first, stride, count, split, kc0, kc1;
+};
+__host__ __device__ inline StepTiles step_tiles(int grid, int cta, int n_tiles, int kc, int S, int rot) {
+  StepTiles t{0, 1, 0, 0, 0, kc};
+  if (S <= 1) {
+    t.first = (cta - rot % grid + grid) % grid;
+    t.stride = grid;
+    t.count = t.first < n_tiles ? (n_tiles - t.first + grid - 1) / grid : 0;
+    return t;
+  }
+  const int teams = grid / S;
+  if (cta >= teams * S) return t;
+  const int q = cta / S;
+  t.split = cta - q * S;
+  t.first = q;
+  t.stride = teams;
+  t.count = q < n_tiles ? (n_tiles - q + teams - 1) / teams : 0;
+  t.kc0 = t.split * kc / S;
+  t.kc1 = (t.split + 1) * kc / S;
+  return t;
+}
+
+struct StepParams {
+  int B;  // rows of the step (<= kStepMaxRows)
+  int H, qd, kvd, F, vocab, d, G, Hq, Hkv, n_layers;
+  float eps, scale_log2;
+  int nslot;    // weight ring slots of kStepSlot bytes
+  int with_lm;  // 0: the step ends after the last layer
+  // per stage: output tiles, 128-column chunks of the reduction, K splits, round-robin start
+  int n_tiles[SS_COUNT], kc[SS_COUNT], split[SS_COUNT], rot[SS_COUNT];
+  int max_split_tiles;  // counter slots per (layer, stage) of the split stages
+  // packed weights: CTA c streams chunks stream_off[c] .. stream_off[c + 1] - 1 of wpack, its
+  // LM-head chunks from stream_lm[c]
+  const uint8_t* wpack;
+  const long long* stream_off;
+  const long long* stream_lm;
+  const void* embed;
+  const float* attn_norm;   // [n_layers][H]
+  const float* ffn_norm;    // [n_layers][H]
+  const float* final_norm;  // [H]
+  uint8_t* pools;           // K of layer l at 2l * pool_bytes, V at (2l + 1) * pool_bytes
+  size_t pool_bytes;
+  int num_blocks, mb, block_size;
+  long long pool_slots;
+  // step metadata
+  const int* tok;
+  const int* tok_src;
+  const int* pos;
+  const int* seq;
+  const long long* slot;
+  const int* tab;
+  const unsigned long long* logits_slot;
+  const int* rows_valid;
+  const int* early_ok;  // see AttnParams::early_ok
+  const double* inv_freq;
+  // activations: resid fp32 [rows][H]; xn, o, act chunk-major [width / 128][B][128] (every
+  // column slice of all rows is contiguous); q row-major [rows][qd]; per-16-column sums of
+  // squares of the residual [rows][H / 16]
+  float* resid;
+  void* xn;
+  void* q;
+  void* o;
+  void* act;
+  float* sumsq16;
+  // split-K partial tiles [tile][split][kStepMaxRows][16] fp32
+  float* split_part;
+  // attention partials [kStepMaxRows][Hkv][max_ch][G][d + 2]
+  float* attn_part;
+  int max_ch;
+  // [0] barrier arrivals, [1] abort flag, [2..] attention unit counters
+  // [n_layers][kStepMaxRows][Hkv], then split-K tile counters [n_layers + 1][4][max_split_tiles];
+  // zero at launch
+  unsigned* sync;
+  int* err;
+};
+
 // Copy between the paged pools and a contiguous buffer [n_layers][n][2][kv_dim] whose row
 // (layer, t) holds the K then V of the token at slot slots[t] (see ns_kv_reload / ns_kv_save).
 struct KvCopyParams {

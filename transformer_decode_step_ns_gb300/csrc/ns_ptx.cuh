@@ -138,6 +138,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (TMA) writes to shared memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------- PDL
 
 __device__ __forceinline__ void griddep_wait() {
