@@ -1711,7 +1711,7 @@ def run_attention_only(args, rank, world):
 
 def run_extra_only(args, rank, world):
     """One of the extra workloads alone, as its own JSON line (--nanobatch-only,
-    --continuous-only, --serving-only, --offload-only, --gemm-only)."""
+    --continuous-only, --serving-only, --offload-only, --gemm-only, --qwen-only)."""
     import torch
     import __graft_entry__ as ge
     ge.build()
@@ -1734,6 +1734,12 @@ def run_extra_only(args, rank, world):
                 "warmup": 3, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": r["workload"]}, "frac_of_roofline": round(roof / tot, 4),
                 "gemm": r}
+    elif args.qwen_only:
+        r = qwen_report(args, peaks, world)
+        line = {"metric": "decode output tokens/s, 24-layer Qwen2.5-0.5B shape", "unit": "tokens/s",
+                "value": r["tokens_per_s"], "higher_is_better": True, "n_gpus": world,
+                "steps": r["steps"], "warmup": args.warmup, "dtype": "f16", "data": "synthetic",
+                "config": {"workload": r["workload"]}, "qwen_24l": r}
     elif args.offload_only:
         r = OffloadWorkload().report()
         line = {"metric": "KV reload GB/s (contiguous H2D + scatter into pages)", "unit": "GB/s",
@@ -1842,6 +1848,9 @@ def main():
                     help="with --continuous-only: layers of the LLaMA-3-8B shape (fewer: a small "
                          "case of the same kernels, e.g. for profilers)")
     ap.add_argument("--skip-qwen", action="store_true")
+    ap.add_argument("--qwen-only", action="store_true",
+                    help="run the 24-layer Qwen2.5-0.5B-shaped workloads alone (batch --batch, 1 and 8, "
+                         "and the persistent step kernel at 1, 8 and 32)")
     ap.add_argument("--skip-small", action="store_true")
     ap.add_argument("--skip-offload", action="store_true")
     ap.add_argument("--oracle-leg", action="store_true",
@@ -1866,7 +1875,7 @@ def main():
         elif args.attention_only:
             run_attention_only(args, rank, world)
         elif (args.nanobatch_only or args.continuous_only or args.serving_only or args.offload_only
-              or args.gemm_only):
+              or args.gemm_only or args.qwen_only):
             run_extra_only(args, rank, world)
         else:
             run_ours(args, rank, world)
