@@ -436,7 +436,7 @@ ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v
  * counters, held by every GPU that loads the library until the process exits.  Requests needing
  * more -- batch * n_kv_heads slots of ceil(max_blocks_per_seq / 64) *
  * (n_q_heads / n_kv_heads) * (head_dim + 2) floats each (rounded up to 16 bytes), or
- * batch * n_kv_heads counters -- return
+ * batch * n_kv_heads + 1 counters -- return
  * NS_ERR_INVALID_ARG with a message saying so.  The first call on a device looks up the
  * buffer's device address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture.  The address is kept per device together with the id of the
@@ -489,13 +489,16 @@ typedef struct {
   int kernels;          /* kernel nodes */
   double capture_ms;    /* host time of capture + instantiate */
   int gemm_cta_budget;  /* 0: none (ns_set_gemm_cta_budget) */
+  int attn_queue;       /* decode attention hands out its units from a queue, longest rows first
+                           (chosen per step: at least 6 units per CTA) */
 } ns_graph_info;
 /* *n = the number of graphs; the first min(*n, capacity) entries are written, in key order. */
 ns_status ns_get_graph_report(ns_handle h, ns_graph_info* out, int capacity, int* n);
 
 /* Capture the decode-only graphs of these batch sizes now (start-up), with or without the LM
  * head, under the current nano-batch, token-source and offload settings, so that no step pays
- * a capture later.  Sizes in [1, max_batch]; with nano-batches only their total.  Captures are
+ * a capture later (where the rows could hold enough attention units for the unit queue, both
+ * attention variants are captured).  Sizes in [1, max_batch]; with nano-batches only their total.  Captures are
  * not replayed (no device work is run).  INVALID_ARG when the handle does not use graphs,
  * NOT_INITIALIZED before ns_kv_alloc. */
 ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with_lm);

@@ -90,6 +90,35 @@ def test_attention_cta_budget_is_bitwise_neutral(cuda_lib):
             6, 32, 8, 128, 16, tab.shape[1], nb, 0.1, 1, -1, None))  # negative budget
 
 
+@pytest.mark.parametrize("n_q,n_kv,d,dtype", [(32, 8, 128, "bf16"), (14, 2, 64, "f16")])
+def test_attention_unit_queue_and_fixed_deal_give_the_same_bits(cuda_lib, n_q, n_kv, d, dtype):
+    """From six units per CTA on, a launch hands out its later units from a global counter,
+    rows with the longest superchunks first; below that each CTA takes a fixed share.  Budgets
+    of 4 and 16 CTAs put this batch (40 rows of 1 to 2100 tokens: superchunks of fewer blocks
+    than warps next to ones of 33 to 64 blocks) in the queue, the full grid does not.  Every
+    budget gives the same bits, which match the oracle; queued launches repeated back to back
+    (the launch that takes the last ticket resets the counter) and a fixed-deal launch after
+    them change nothing."""
+    import torch
+    from transformer_decode_step_ns_gb300 import _lib
+    lens = [1, 2, 3, 5, 7, 16, 17, 33, 64, 100, 513, 1024, 1025, 2047, 2100, 300, 1200, 48, 80,
+            4] * 2
+    q, kp, vp, tab, sl, nb = attention_case(27, lens, n_q, n_kv, d, dtype)
+    base = run_attention(q, kp, vp, tab, sl, n_q, n_kv, d, dtype, nb)
+    ref = oracle_attention(q, kp, vp, tab, sl, d, dtype)
+    got = storage_f64(base, dtype)
+    for b in range(len(lens)):
+        assert rel_l2(got[b], ref[b]) < 1e-2, b
+    dq, dk, dv, dt, dl = to_dev(q), to_dev(kp), to_dev(vp), to_dev(tab), to_dev(sl)
+    for budget in (4, 4, 16, 16, 4, 0):
+        out = torch.zeros_like(dq)
+        _lib.attn_decode(dq, dk, dv, dt, dl, out, n_q, n_kv, d, 16, tab.shape[1], nb,
+                         1.0 / math.sqrt(d), dtype, cta_budget=budget)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(from_dev(out), base)
+    assert _lib.device_error() == 0
+
+
 def test_attention_bounds_checks_record_errors_and_skip_the_access(cuda_lib):
     """The kernel's own checks (each substitutes a safe value before any memory access, so no
     fault is induced): a block id outside the pool records NS_DEV_BAD_BLOCK (1) and reads block 0

@@ -367,6 +367,35 @@ def test_prefill_chunk_threshold_and_offset(cuda_lib, chunk, p0):
     _check_step(Harness(shape, 111 + chunk, ctx, shared_table_rows=shared))
 
 
+def test_attention_unit_queue_in_the_step_gives_the_same_bits(cuda_lib):
+    """With the attention capped at 8 CTAs, 24 decode rows of 1100 to 2000 tokens hold at least
+    six attention units per CTA, so the step launches the unit-queue variant (its graph reports
+    attn_queue = 1); the logits and the cache equal bitwise those of the same step on the full
+    grid, which takes the fixed deal, and match the oracle.  Graphs captured at start-up for that
+    budget include both variants, and later steps replay them."""
+    shape = _tiny("bf16")
+    ctx = [int(v) for v in synth.uniform_int(91, "ctxq", 24, 1100, 2000)]
+    full = Harness(shape, 301, ctx)
+    got, _ = _check_step(full)
+    assert [r["attn_queue"] for r in full.dev.graph_report()] == [0]
+    ks0, vs0 = full.download_pools()
+    capped = Harness(shape, 301, ctx)
+    capped.dev.set_nanobatch(None, attn_cta_budget=8)
+    capped.dev.capture_graphs([24])
+    rep = capped.dev.graph_report()
+    assert sorted(r["attn_queue"] for r in rep) == [0, 1] and all(r["batch"] == 24 for r in rep)
+    np.testing.assert_array_equal(capped.run_gpu(), got)
+    ks, vs = capped.download_pools()
+    for l in range(shape.n_layers):
+        np.testing.assert_array_equal(ks[l], ks0[l])
+        np.testing.assert_array_equal(vs[l], vs0[l])
+    assert capped.dev.info().graphs_cached == 2
+    eager = Harness(shape, 301, ctx, use_graphs=False)
+    eager.dev.set_nanobatch(None, attn_cta_budget=8)
+    np.testing.assert_array_equal(eager.run_gpu(), got)
+    assert eager.dev.device_error() == 0
+
+
 def test_startup_capture_and_capture_report(cuda_lib):
     """Graphs captured at start-up for the buckets are the ones later steps replay (no new
     capture); the report lists each with its kernel count and capture time."""

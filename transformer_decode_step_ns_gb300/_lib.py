@@ -253,7 +253,7 @@ def _stream(stream) -> Optional[int]:
 class GraphInfo(ctypes.Structure):
     _fields_ = [("batch", I), ("n_split", I), ("attn_cta_budget", I), ("with_lm", I),
                 ("chunk_rows", I), ("kv_offload", I), ("kernels", I), ("capture_ms", ctypes.c_double),
-                ("gemm_cta_budget", I)]
+                ("gemm_cta_budget", I), ("attn_queue", I)]
 
 
 class DecodeStep:
@@ -462,7 +462,7 @@ class DecodeStep:
 
     def graph_report(self) -> list:
         """One dict per captured graph: batch, n_split, attn_cta_budget, with_lm, chunk_rows,
-        kv_offload, kernels, capture_ms."""
+        kv_offload, kernels, capture_ms, gemm_cta_budget, attn_queue."""
         n = I()
         check(lib().ns_get_graph_report(self.h, None, 0, ctypes.byref(n)))
         arr = (GraphInfo * max(n.value, 1))()

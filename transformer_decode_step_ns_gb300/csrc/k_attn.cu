@@ -10,7 +10,16 @@
 //   most 64 blocks (1024 tokens); the split is a function of the row's length alone, so a row's
 //   result never depends on the rest of the batch.  A CTA takes a unit; its warps (8 at
 //   head_dim 64, else 4) take contiguous shares of the superchunk and merge through shared
-//   memory.
+//   memory (a superchunk of fewer blocks than warps gives the extra warps a copy of a block to
+//   fetch and leaves them out of the merge, so no warp's share is empty).
+// * A CTA's first unit is its index.  When the launch holds at least kAttnQueueUnits units per
+//   CTA, later units are handed out by a global counter as CTAs need them, rows with the
+//   longest superchunks first (a stable counting sort that every CTA computes alike, so a unit
+//   index names the same work everywhere): with a fixed round-robin deal the last CTA finished
+//   12-16 % after the median one.  Below that the fixed deal over the rows in their own order
+//   stays: its CTAs c and c + grid/2, which share an SM, take units c, c + grid/2, c + grid, ...
+//   so every SM gets the same number, while a queue can hand both CTAs of one SM a second unit
+//   and leave another SM with none.  Which CTA computes a unit does not change its result.
 // * Every warp streams its blocks (running ahead into its share of the CTA's next unit) through
 //   a private ring of stages; each stage holds one 16 x d K tile and one V tile, copied with
 //   16-byte cp.async by all 32 lanes (each tile is one contiguous run, so every warp request is a
@@ -29,6 +38,8 @@
 //   deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "ns_internal.h"
 #include "ns_ptx.cuh"
@@ -129,13 +140,51 @@ struct AttnShape {
   static constexpr int OFF_IDS = OFF_MRG + ((MRG_FLOATS * 4 + 15) & ~15);  // [NW][16] block ids
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G >= 1 && G <= 8, "group");
-  // then superchunk prefix [batch + 1], lengths [batch], scan scratch [NT]
+  // then the CTA's unit sequence (SEQ 64-bit entries; the next index to claim and three spare
+  // words); superchunk prefix over positions [batch + 1], lengths by row [batch], row of each
+  // position [batch]; scan scratch [NT]; sort bins [NK]
+  static constexpr int NK = kAttnSuperBlocks + 1;  // superchunk lengths 0 .. 64 (0: invalid row)
+  static constexpr int SEQ = 16;
   static size_t smem_bytes(int batch) {
-    return 1024 + OFF_IDS + NW * kAttnWarpBlocks * 4 + static_cast<size_t>(2 * batch + 1 + NT) * 4;
+    return 1024 + OFF_IDS + NW * kAttnWarpBlocks * 4 +
+           static_cast<size_t>(3 * batch + 1 + NT + NK + 2 * SEQ + 4) * 4;
   }
 };
 
-template <typename T, int D, int G>
+// Entry k of a CTA's unit sequence when it is not set yet (one lane; out of line, since it runs
+// once per unit and the streaming loop around it is hot).  The first warp to get here claims the
+// entry and takes the next ticket from the launch's counter; the others wait for it (bounded; a
+// wait that runs out records NS_DEV_WAIT_TIMEOUT and ends the sequence).  Every CTA with a first
+// unit takes exactly one ticket past the last unit, so the launch takes `total` tickets in all;
+// the one that takes the last resets the counter (no CTA of this launch takes another, and the
+// next launch reads it only after its dependency wait, when this grid has finished).
+__device__ __noinline__ int queue_claim(unsigned long long* entry, int* claim, unsigned* sched,
+                                        int total, int k, int* err) {
+  volatile unsigned long long* e = entry;
+  const unsigned long long tag = static_cast<unsigned long long>(k + 1) << 32;
+  unsigned long long x;
+  if (atomicCAS(claim, k, k + 1) == k) {
+    const unsigned c = atomicAdd(sched, 1u);
+    if (c == static_cast<unsigned>(total) - 1u) atomicExch(sched, 0u);
+    x = tag | (gridDim.x + c);
+    *e = x;
+  } else {
+    const unsigned long long t0 = global_timer_ns();
+    while (((x = *e) >> 32) != static_cast<unsigned long long>(k + 1)) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        set_err(err, NS_DEV_WAIT_TIMEOUT);
+        x = tag | 0x7fffffffu;
+        break;
+      }
+    }
+  }
+  return static_cast<int>(x & 0x7fffffffu);
+}
+
+// Q: the launch may hand out units from the global queue (it does when it holds at least
+// kAttnQueueUnits units per CTA).  Without Q the fixed deal is compiled alone: the queue's code
+// in the same kernel slows the streaming loop even when it does not run.
+template <typename T, int D, int G, bool Q>
 __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 ? 1 : 2)
     attn_decode_kernel(const AttnParams p) {
   using S = AttnShape<D, G>;
@@ -145,42 +194,141 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   float* m_ml = m_acc + S::NW * G * D;                           // [NW][G][2]
   float* m_w = m_ml + S::NW * G * 2;                             // [2][G][kAttnMaxChunks]
   int* ids_all = reinterpret_cast<int*>(smem + S::OFF_IDS);      // [NW][kAttnWarpBlocks]
-  int* pre = ids_all + S::NW * kAttnWarpBlocks;                  // superchunk prefix [batch + 1]
+  // [SEQ] unit k of the CTA's sequence in entry k % SEQ, tagged (k + 1) << 32 | unit: one 64-bit
+  // word, so a reader that sees the tag sees the unit without a fence
+  unsigned long long* seq = reinterpret_cast<unsigned long long*>(ids_all + S::NW * kAttnWarpBlocks);
+  int* seq_claim = reinterpret_cast<int*>(seq + S::SEQ);         // next sequence index to claim
+  int* pre = seq_claim + 4;                                      // superchunk prefix [batch + 1]
   int* lens = pre + p.batch + 1;                                 // validated seq_lens [batch]
-  int* tot = lens + p.batch;                                     // per-thread scan scratch [NT]
+  int* order = lens + p.batch;                                   // row of each position [batch]
+  int* tot = order + p.batch;                                    // warp totals of the scan [NT]
+  int* bins = tot + S::NT;                                       // [NK]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads, batch = p.batch;
   uint8_t* ring = smem + warp * S::RING;
-  // Superchunk prefix over the rows.  seq_lens are step metadata, final before the step starts,
-  // so under programmatic dependent launch this overlaps the previous kernel.
-  {
-    const int per = (batch + S::NT - 1) / S::NT;
-    const int lo = tid * per, hi = min(batch, lo + per);
-    int run = 0;
-    for (int b = lo; b < hi; ++b) {
-      const int L = p.seq_lens[p.row0 + b];
-      const bool ok = L >= 1 && L <= p.mb * p.block_size;
-      if (!ok) set_err(p.err, NS_DEV_BAD_LENGTH);
-      lens[b] = ok ? L : 0;
-      run += ok ? attn_num_chunks(L) : 0;
+  if (Q && tid == 0) {
+    for (int i = 1; i < S::SEQ; ++i) seq[i] = 0;
+    // the first unit is fixed: it may be fetched before the dependency wait
+    seq[0] = (1ull << 32) | blockIdx.x;
+    *seq_claim = 1;
+  }
+  // Rows, their superchunk counts and the scheduling order.  seq_lens are step metadata, final
+  // before the step starts, so under programmatic dependent launch this overlaps the previous
+  // kernel.  Thread t validates rows [t * per, (t + 1) * per); a block-wide scan (warp shuffles,
+  // then the warps' totals) counts the superchunks.  Without the queue the rows keep their order
+  // and that scan is the prefix.  With it the rows are ordered longest superchunk first, ties by
+  // row index (a stable counting sort): warp w ranks rows [w * wper, (w + 1) * wper), 32 at a
+  // time; lanes holding the same length find each other with a match, and the warp's running
+  // count per length (kept in the stage rings, free until the first copy) ranks them after its
+  // earlier rows.  lens stays indexed by row; order maps a position to its row.
+  static_assert(S::NW * S::NK * 4 <= S::NW * S::RING && S::NK <= 96, "sort scratch");
+  int* cnt = reinterpret_cast<int*>(smem);  // [NW][NK] a warp's rows per length (queue only)
+  if (Q)
+    for (int i = tid; i < S::NW * S::NK; i += S::NT) cnt[i] = 0;
+  auto block_scan = [&](int v) {  // inclusive over the warp; lane 31 leaves the warp's total
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
     }
-    tot[tid] = run;
+    if (lane == 31) tot[warp] = inc;
+    return inc;
+  };
+  const int per = (batch + S::NT - 1) / S::NT;
+  const int lo_t = tid * per, hi_t = min(batch, lo_t + per);
+  int run = 0;
+  for (int b = lo_t; b < hi_t; ++b) {
+    const int L0 = p.seq_lens[p.row0 + b];
+    const bool ok = L0 >= 1 && L0 <= p.mb * p.block_size;
+    if (!ok) set_err(p.err, NS_DEV_BAD_LENGTH);
+    lens[b] = ok ? L0 : 0;
+    run += ok ? attn_num_chunks(L0) : 0;
+  }
+  int inc = block_scan(run);
+  __syncthreads();
+  int before_warp = 0, n_chunks = 0;
+  for (int w = 0; w < S::NW; ++w) {
+    const int t = tot[w];
+    before_warp += w < warp ? t : 0;
+    n_chunks += t;
+  }
+  const bool queue = Q && static_cast<long long>(n_chunks) * Hkv >=
+                              static_cast<long long>(kAttnQueueUnits) * gridDim.x;  // block-uniform
+  if (queue) {
+    const int wper = (batch + S::NW - 1) / S::NW;
+    const int lo = warp * wper, hi = min(batch, lo + wper);
+    int* wc = cnt + warp * S::NK;
+    for (int b0 = lo; b0 < hi; b0 += 32) {
+      const int b = b0 + lane;
+      const unsigned act = __ballot_sync(0xffffffffu, b < hi);
+      if (b < hi) {
+        const int key = attn_chunk_blocks(lens[b]);
+        const unsigned same = __match_any_sync(act, key);
+        const int before = __popc(same & ((1u << lane) - 1u));
+        pre[b] = wc[key] + before;  // rank among this warp's rows of the same length
+        __syncwarp(act);
+        if (before == 0) wc[key] += __popc(same);
+      }
+      __syncwarp();
+    }
     __syncthreads();
-    if (tid == 0) {
+    if (tid < S::NK) {  // per length: the warps' offsets, and the length's total
       int acc = 0;
-      for (int i = 0; i < S::NT; ++i) {
-        const int v = tot[i];
-        tot[i] = acc;
+      for (int w = 0; w < S::NW; ++w) {
+        const int v = cnt[w * S::NK + tid];
+        cnt[w * S::NK + tid] = acc;
         acc += v;
       }
-      pre[batch] = acc;
+      bins[tid] = acc;
     }
     __syncthreads();
-    int acc = tot[tid];
-    for (int b = lo; b < hi; ++b) {
-      pre[b] = acc;
-      acc += attn_num_chunks(lens[b]);
+    if (warp == 0) {  // where each length starts, longest first (lane l: the 3l-th to 3l+2-th)
+      int v[3], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int k = S::NK - 1 - (3 * lane + j);
+        v[j] = k >= 0 ? bins[k] : 0;
+        sum += v[j];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int acc = incl - sum;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int k = S::NK - 1 - (3 * lane + j);
+        if (k >= 0) bins[k] = acc;
+        acc += v[j];
+      }
     }
+    __syncthreads();
+    for (int b0 = lo; b0 < hi; b0 += 32) {
+      const int b = b0 + lane;
+      if (b < hi) {
+        const int key = attn_chunk_blocks(lens[b]);
+        order[bins[key] + wc[key] + pre[b]] = b;
+      }
+    }
+    __syncthreads();
+    // the superchunk counts again, now over positions
+    run = 0;
+    for (int i = lo_t; i < hi_t; ++i) run += attn_num_chunks(lens[order[i]]);
+    inc = block_scan(run);
+    __syncthreads();
+    before_warp = 0;
+    for (int w = 0; w < warp; ++w) before_warp += tot[w];
+  }
+  {
+    int acc = before_warp + inc - run;
+    for (int i = lo_t; i < hi_t; ++i) {
+      pre[i] = acc;
+      acc += attn_num_chunks(lens[queue ? order[i] : i]);
+    }
+    if (tid == S::NT - 1) pre[batch] = acc;
     __syncthreads();
   }
   const int total = pre[batch] * Hkv;
@@ -199,15 +347,19 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
       const int mid = (lo + hi + 1) >> 1;
       if (pre[mid] <= cg) lo = mid; else hi = mid - 1;
     }
-    x.b = lo;
+    x.b = queue ? order[lo] : lo;
     x.sc = cg - pre[lo];
-    x.L = lens[lo];
+    x.L = lens[x.b];
     x.nchunks = attn_num_chunks(x.L);
     const int cb = attn_chunk_blocks(x.L);
     x.blk0 = x.sc * cb;
     const int nb = min(cb, (x.L + S::BS - 1) / S::BS - x.blk0);
     x.w0 = x.blk0 + (nb * warp) / S::NW;
     x.w1 = x.blk0 + (nb * (warp + 1)) / S::NW;
+    // With the queue a warp whose share would be empty (fewer blocks than warps) fetches one
+    // block of another warp's share and merges the empty share's state instead, so every warp
+    // streams every unit.  The fixed deal skips such units.
+    if constexpr (Q) x.w1 = max(x.w1, x.w0 + 1);
     return x;
   };
 
@@ -220,7 +372,24 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   const uint64_t pol = policy_evict_first();  // K/V are streamed once
   const T* kpool = reinterpret_cast<const T*>(p.k_pool);
   const T* vpool = reinterpret_cast<const T*>(p.v_pool);
-  int pu = blockIdx.x, pi = 0;
+  // Unit k of this CTA's sequence (warp-collective).  The first warp that needs an entry not yet
+  // set claims it and takes the next unit from the global counter; the others wait for it
+  // (bounded).  Every warp has blocks in every unit and the warps merge each unit before the
+  // next, so a producer leads the slowest consumer by at most NST + 1 units and an entry is not
+  // reused (SEQ units later) while any warp still needs it.
+  auto unit_at = [&](int k) -> int {
+    if (!queue) return blockIdx.x + k * gridDim.x;
+    int v = 0;
+    if (lane == 0) {
+      const unsigned long long x = *(volatile unsigned long long*)(seq + k % S::SEQ);
+      v = (x >> 32) == static_cast<unsigned long long>(k + 1)
+              ? static_cast<int>(x & 0x7fffffffu)
+              : queue_claim(seq + k % S::SEQ, seq_claim, p.sched, total, k, p.err);
+    }
+    return __shfl_sync(0xffffffffu, v, 0);
+  };
+  int pk = 0, pu = blockIdx.x, pi = 0, nxt = 0x7fffffff;
+  bool lookahead = !queue;  // later units may be named (with the queue: after the dependency wait)
   Unit pun{}, nun{};
   int nid = 0;
   auto load_ids = [&](int unit) {  // register <- this warp's block ids of `unit` (non-blocking)
@@ -228,7 +397,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
     const int* src = p.block_tables + static_cast<size_t>(p.row0 + nun.b) * p.mb;
     nid = lane < nun.w1 - nun.w0 ? src[nun.w0 + lane] : 0;
   };
-  auto enter = [&]() {  // the producer moves to unit pu; skip units where this warp has no blocks
+  auto enter = [&]() {  // the producer moves to unit pu (decoded in nun)
     for (;;) {
       __syncwarp();
       if (pu >= total) break;
@@ -241,10 +410,19 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
         }
         ids[lane] = blk;
       }
-      if (pu + static_cast<int>(gridDim.x) < total) load_ids(pu + gridDim.x);
-      __syncwarp();
-      if (pun.w1 > pun.w0) break;
-      pu += gridDim.x;
+      if constexpr (Q) {  // every share is non-empty
+        if (lookahead) {
+          nxt = unit_at(pk + 1);
+          if (nxt < total) load_ids(nxt);
+        }
+        __syncwarp();
+        break;
+      } else {  // units where this warp has no blocks are skipped
+        if (pu + static_cast<int>(gridDim.x) < total) load_ids(pu + gridDim.x);
+        __syncwarp();
+        if (pun.w1 > pun.w0) break;
+        pu += gridDim.x;
+      }
     }
   };
   auto issue = [&](int stage) {  // warp-collective: one cp.async group per call
@@ -265,7 +443,12 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
       }
       if (++pi >= pun.w1 - pun.w0) {
         pi = 0;
-        pu += gridDim.x;
+        if constexpr (Q) {
+          pk += 1;
+          pu = nxt;
+        } else {
+          pu += gridDim.x;
+        }
         enter();
       }
     }
@@ -276,11 +459,20 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   // Blocks without a token of this step may be fetched before the previous kernel (which writes
   // this step's K/V and q) has finished.  In a decode-only batch only the last block of a row
   // holds this step's token; rows of a prefill chunk read blocks other rows write now, and the
-  // host then clears early_ok.
+  // host then clears early_ok.  With the queue the early fetches stay inside the first unit:
+  // the counter that hands out later units may still be in use by the previous launch until the
+  // dependency wait.
   const bool early = p.early_ok == nullptr || *p.early_ok != 0;
   int s0 = 0;
-  while (early && s0 < S::NST && pu < total && pun.w0 + pi != (pun.L - 1) / S::BS) issue(s0++);
+  while (early && s0 < S::NST && pu < total && pun.w0 + pi != (pun.L - 1) / S::BS &&
+         (!queue || pi + 1 < pun.w1 - pun.w0))
+    issue(s0++);
   griddep_wait();
+  lookahead = true;
+  if (queue && pu < total) {  // the early fetches stayed in the first unit
+    nxt = unit_at(1);
+    if (nxt < total) load_ids(nxt);
+  }
   for (int s = s0; s < S::NST; ++s) issue(s);
 
   const int gq = lane >> 2, tq = lane & 3;
@@ -291,14 +483,16 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   const int h_e = 2 * tq, h_o = 2 * tq + 1;
 
   int ci = 0;
-  for (int u = blockIdx.x; u < total; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int u = unit_at(k);
+    if (u >= total) break;
     const Unit x = decode(u);
     const size_t row = static_cast<size_t>(p.row0 + x.b);
     float m_run = -INFINITY, l_run = 0.f;
     float acc[S::KS][4];
 #pragma unroll
     for (int mt = 0; mt < S::KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    if (x.w1 > x.w0) {
+    if (Q || x.w1 > x.w0) {
       // q of the group as the A operand: rows = heads (G of 16 used), k = dims
       uint32_t qa[S::KS][2];
       {
@@ -393,6 +587,14 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
 
     // ---- merge the warps' shares of the superchunk through shared memory, in warp order
     {
+      // a warp that streamed a copy (its own share was empty) gives the empty share's state
+      const int nb = min(attn_chunk_blocks(x.L), (x.L + S::BS - 1) / S::BS - x.blk0);
+      if (Q && (nb * (warp + 1)) / S::NW == (nb * warp) / S::NW) {
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < S::KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      }
       float* wacc = m_acc + warp * G * D;
 #pragma unroll
       for (int mt = 0; mt < S::KS; ++mt) {
@@ -435,19 +637,23 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
       }
     }
     if (x.nchunks > 1) {
-      // superchunks of one (row, kv head) are merged by the CTA that finishes last
-      __threadfence();
+      // Superchunks of one (row, kv head) are merged by the CTA that finishes last.  The barrier
+      // orders every thread's partial stores before thread 0's increment, which releases them
+      // at GPU scope and acquires the other CTAs' (acq_rel); the second barrier passes that on
+      // to the threads that read them.  No thread fences while its copies are in flight.
       named_barrier_sync(1, S::NT);
       int* last_flag = reinterpret_cast<int*>(m_w + 2 * G * kAttnMaxChunks);
       if (tid == 0) {
         int* cnt = p.counters + row * Hkv + x.g;
-        const int last = (atomicAdd(cnt, 1) == x.nchunks - 1) ? 1 : 0;
+        int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(prev) : "l"(cnt) : "memory");
+        const int last = prev == x.nchunks - 1 ? 1 : 0;
         if (last) *cnt = 0;  // ready for the next launch
         last_flag[0] = last;
       }
       named_barrier_sync(1, S::NT);
       if (last_flag[0]) {
-        __threadfence();
         // weight_c = 2^(m_c - M) / sum_c' l_c' 2^(m_c' - M), summed in superchunk order
         float* wm = m_w;                          // [G][kAttnMaxChunks]: m, then the weight
         float* wl = m_w + G * kAttnMaxChunks;     // [G][kAttnMaxChunks]: l
@@ -508,14 +714,14 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
 
 namespace {
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool Q>
 cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pdl) {
   using S = AttnShape<D, G>;
   static int configured_mask = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 31 && !(configured_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T, D, G>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T, D, G, Q>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     configured_mask |= 1 << dev;
@@ -530,19 +736,26 @@ cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t s, bool pd
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G>, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, D, G, Q>, p);
+}
+
+template <typename T, int D, bool Q>
+cudaError_t dispatch_g(const AttnParams& p, int group, int grid, cudaStream_t s, bool pdl) {
+  switch (group) {
+    case 1: return launch_attn_t<T, D, 1, Q>(p, grid, s, pdl);
+    case 2: return launch_attn_t<T, D, 2, Q>(p, grid, s, pdl);
+    case 4: return launch_attn_t<T, D, 4, Q>(p, grid, s, pdl);
+    case 7: return launch_attn_t<T, D, 7, Q>(p, grid, s, pdl);
+    case 8: return launch_attn_t<T, D, 8, Q>(p, grid, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <typename T, int D>
-cudaError_t dispatch_g(const AttnParams& p, int group, int grid, cudaStream_t s, bool pdl) {
-  switch (group) {
-    case 1: return launch_attn_t<T, D, 1>(p, grid, s, pdl);
-    case 2: return launch_attn_t<T, D, 2>(p, grid, s, pdl);
-    case 4: return launch_attn_t<T, D, 4>(p, grid, s, pdl);
-    case 7: return launch_attn_t<T, D, 7>(p, grid, s, pdl);
-    case 8: return launch_attn_t<T, D, 8>(p, grid, s, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t dispatch_q(const AttnParams& p, int group, int grid, cudaStream_t s, bool pdl,
+                       bool queue) {
+  return queue ? dispatch_g<T, D, true>(p, group, grid, s, pdl)
+               : dispatch_g<T, D, false>(p, group, grid, s, pdl);
 }
 
 template <typename T, int D, int G>
@@ -551,12 +764,18 @@ int max_grid_t(int batch) {
   int dev = 0, sms = 1, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaFuncSetAttribute(attn_decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       227 * 1024);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<T, D, G>, S::NT,
-                                                    S::smem_bytes(batch)) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  // both variants: the same block size, shared memory and register bound
+  int per_sm_q = 0;
+  cudaFuncSetAttribute(attn_decode_kernel<T, D, G, false>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaFuncSetAttribute(attn_decode_kernel<T, D, G, true>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<T, D, G, false>,
+                                                    S::NT, S::smem_bytes(batch)) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_q, attn_decode_kernel<T, D, G, true>,
+                                                    S::NT, S::smem_bytes(batch)) != cudaSuccess)
+    per_sm = per_sm_q = 1;
+  per_sm = std::max(1, std::min(per_sm, per_sm_q));
   return sms * per_sm;
 }
 
@@ -587,14 +806,14 @@ int attn_max_grid(int dtype, int head_dim, int group, int batch) {
 }
 
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
-                        cudaStream_t s, bool pdl) {
+                        cudaStream_t s, bool pdl, bool queue) {
   if (grid < 1) grid = 1;
   if (dtype == NS_BF16) {
-    return head_dim == 64 ? dispatch_g<__nv_bfloat16, 64>(p, group, grid, s, pdl)
-                          : dispatch_g<__nv_bfloat16, 128>(p, group, grid, s, pdl);
+    return head_dim == 64 ? dispatch_q<__nv_bfloat16, 64>(p, group, grid, s, pdl, queue)
+                          : dispatch_q<__nv_bfloat16, 128>(p, group, grid, s, pdl, queue);
   }
-  return head_dim == 64 ? dispatch_g<__half, 64>(p, group, grid, s, pdl)
-                        : dispatch_g<__half, 128>(p, group, grid, s, pdl);
+  return head_dim == 64 ? dispatch_q<__half, 64>(p, group, grid, s, pdl, queue)
+                        : dispatch_q<__half, 128>(p, group, grid, s, pdl, queue);
 }
 
 }  // namespace ns

@@ -401,6 +401,10 @@ struct ns_ctx {
   std::vector<int> split_sizes;
   int attn_budget = 0;
   int gemm_budget = 0;  // persistent-GEMM CTA cap of nano-batched steps (ns_set_gemm_cta_budget)
+  // the decode attention launches of the step being enqueued use the unit-queue variant (set
+  // from the step's sequence lengths; part of the graph key)
+  bool attn_queue = false;
+  std::vector<int> attn_grid_memo;  // attn_max_grid per row count (0: not yet asked)
   std::vector<int> buckets;  // graph batch sizes (ns_set_graph_buckets), ascending
   bool graph_chunks = true;  // steps with prompt chunks replay graphs too (ns_set_graph_chunks)
   int chunk_first = 0;       // rows [chunk_first, batch) of the current step form prefill
@@ -677,6 +681,41 @@ ns_status enqueue_step_persistent(ns_ctx* h, int B, cudaStream_t s) {
   return NS_OK;
 }
 
+// Grid of a decode attention launch over `rows` rows: one full wave (memoised per row count),
+// at most one CTA per unit, within the attention CTA budget.
+int attn_grid(ns_ctx* h, int rows) {
+  const ns_model_cfg& c = h->cfg;
+  if (static_cast<int>(h->attn_grid_memo.size()) <= rows) h->attn_grid_memo.resize(rows + 1, 0);
+  int& wave = h->attn_grid_memo[rows];
+  if (wave == 0) wave = attn_max_grid(h->dtype, c.head_dim, c.n_q_heads / c.n_kv_heads, rows);
+  int grid = std::min(wave, rows * c.n_kv_heads * h->max_chunks);
+  if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
+  return std::max(grid, 1);
+}
+
+// Whether a step over B rows launches the unit-queue variant of decode attention: when the
+// decode rows of some nano-batch hold at least kAttnQueueUnits (row, kv head, superchunk) units
+// per CTA of its launch.  seq: the step's host sequence lengths (B of them); null takes the
+// most any row could hold.
+bool attn_queue_for(ns_ctx* h, int B, const int32_t* seq) {
+  const int Hkv = h->cfg.n_kv_heads;
+  int r = 0;
+  const int n = h->n_split <= 1 ? 1 : h->n_split;
+  for (int i = 0; i < n; ++i) {
+    const int rows = h->n_split <= 1 ? B : h->split_sizes[i];
+    const int r_lo = r, r_hi = r + rows;
+    r = r_hi;
+    const int d_hi = std::min(r_hi, std::max(r_lo, h->chunk_first));
+    if (d_hi <= r_lo) continue;
+    long long chunks = 0;
+    for (int b = r_lo; b < d_hi; ++b)
+      chunks += seq != nullptr ? attn_num_chunks(seq[b]) : h->max_chunks;
+    if (chunks * Hkv >= static_cast<long long>(kAttnQueueUnits) * attn_grid(h, d_hi - r_lo))
+      return true;
+  }
+  return false;
+}
+
 // Enqueue one step for `B` rows on `s0` (and the side stream when nano-batched).
 ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
   if (step_kernel_takes(h, B)) return enqueue_step_persistent(h, B, s0);
@@ -822,6 +861,8 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       ap.max_chunks = h->max_chunks;
       ap.partials = h->attn_partials;
       ap.counters = h->attn_counters;
+      ap.sched = reinterpret_cast<unsigned*>(h->attn_counters + static_cast<size_t>(h->R) * Hkv) +
+                 nb[i].first;
       ap.err = h->err;
       ap.early_ok = reinterpret_cast<const int*>(h->meta_dev + ml.flags);
       // decode rows of the nano-batch, then the prefill-chunk rows it holds (chunks come last)
@@ -829,10 +870,9 @@ ns_status enqueue_step(ns_ctx* h, int B, cudaStream_t s0) {
       const int d_hi = std::min(r_hi, std::max(r_lo, h->chunk_first));
       if (d_hi > r_lo) {
         ap.batch = d_hi - r_lo;
-        int grid = std::min(attn_max_grid(h->dtype, d, G, ap.batch), ap.batch * Hkv * h->max_chunks);
-        if (h->attn_budget > 0) grid = std::min(grid, h->attn_budget);
+        const int grid = attn_grid(h, ap.batch);
         TimeScope ts(h, s, K_ATTN);
-        NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true));
+        NS_CUDA(launch_attn(ap, h->dtype, d, G, grid, s, true, h->attn_queue));
         h->kernels_last++;
       }
       for (size_t ci = 0; ci < h->chunk_runs.size(); ++ci) {
@@ -939,7 +979,7 @@ std::vector<int> graph_key(const ns_ctx* h, int B) {
   std::vector<int> k{B, h->step_mode, h->n_split, h->attn_budget, h->n_split > 1 ? h->gemm_budget : 0, h->with_lm ? 1 : 0,
                      static_cast<int>(src & 0xffffffffu), static_cast<int>(src >> 32),
                      h->chunk_first, static_cast<int>(kvh & 0xffffffffu), static_cast<int>(kvh >> 32),
-                     static_cast<int>(h->chunk_runs.size())};
+                     static_cast<int>(h->chunk_runs.size()), h->attn_queue ? 1 : 0};
   for (int v : h->chunk_runs) k.push_back(v);
   for (int v : h->split_sizes) k.push_back(v);
   return k;
@@ -982,6 +1022,7 @@ ns_status get_graph(ns_ctx* h, int B, cudaGraphExec_t* out) {
   gi.n_split = h->n_split;
   gi.attn_cta_budget = h->attn_budget;
   gi.gemm_cta_budget = h->n_split > 1 ? h->gemm_budget : 0;
+  gi.attn_queue = h->attn_queue ? 1 : 0;
   gi.with_lm = h->with_lm ? 1 : 0;
   gi.chunk_rows = h->chunk_first < B ? B - h->chunk_first : 0;
   gi.kv_offload = h->kv_host != nullptr ? 1 : 0;
@@ -1220,8 +1261,10 @@ ns_status ns_kv_alloc(ns_handle h, int num_blocks, int block_size) {
   h->max_chunks = attn_max_chunks(c.max_blocks_per_seq * block_size);
   const int G = c.n_q_heads / c.n_kv_heads;
   const size_t rows_heads = static_cast<size_t>(h->R) * c.n_kv_heads;
-  NS_CUDA(cudaMalloc(&h->attn_counters, rows_heads * sizeof(int)));
-  NS_CUDA(cudaMemset(h->attn_counters, 0, rows_heads * sizeof(int)));
+  // superchunk counters [R][n_kv_heads], then a unit-queue counter per possible first row of an
+  // attention launch (nano-batches on two streams run concurrently)
+  NS_CUDA(cudaMalloc(&h->attn_counters, (rows_heads + h->R) * sizeof(int)));
+  NS_CUDA(cudaMemset(h->attn_counters, 0, (rows_heads + h->R) * sizeof(int)));
   NS_CUDA(cudaMalloc(&h->attn_partials,
                      rows_heads * attn_slot_floats(h->max_chunks, G, c.head_dim) * sizeof(float)));
   h->pool.block_size = block_size;
@@ -1583,6 +1626,7 @@ ns_status ns_decode_step(ns_handle h, int batch, const int32_t* token_ids, const
   NS_CUDA(cudaEventRecord(h->meta_done, s));
   h->meta_pending = true;
   h->with_lm = logits_out != nullptr;
+  h->attn_queue = attn_queue_for(h, graphed ? Bg : batch, reinterpret_cast<const int32_t*>(mh + ml.seq));
   if (graphed) {
     cudaGraphExec_t ex = nullptr;
     NS_TRY(get_graph(h, Bg, &ex));
@@ -1624,7 +1668,13 @@ ns_status ns_capture_graphs(ns_handle h, int n, const int* batch_sizes, int with
     h->chunk_first = batch_sizes[i];  // decode-only layout
     h->chunk_runs.clear();
     cudaGraphExec_t ex = nullptr;
+    // the fixed-deal attention, and the unit-queue one where the rows could need it
+    h->attn_queue = false;
     NS_TRY(get_graph(h, batch_sizes[i], &ex));
+    if (attn_queue_for(h, batch_sizes[i], nullptr)) {
+      h->attn_queue = true;
+      NS_TRY(get_graph(h, batch_sizes[i], &ex));
+    }
   }
   return NS_OK;
 }
@@ -1850,7 +1900,7 @@ ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v
   if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1ll << 31))
     return fail(NS_ERR_UNSUPPORTED, "num_blocks * n_kv_heads * block_size must fit in int32");
   DevScratch* sc = nullptr;
-  NS_TRY(scratch_get(rows_heads * attn_slot_floats(max_chunks, G, head_dim) * sizeof(float), rows_heads, &sc));
+  NS_TRY(scratch_get(rows_heads * attn_slot_floats(max_chunks, G, head_dim) * sizeof(float), rows_heads + 1, &sc));
   AttnParams ap{};
   ap.q = q;
   ap.q_row_stride = static_cast<long long>(n_q_heads) * head_dim;
@@ -1870,12 +1920,17 @@ ns_status ns_attn_decode_capped(const void* q, const void* k_pool, const void* v
   ap.max_chunks = max_chunks;
   ap.partials = static_cast<float*>(sc->buf);
   ap.counters = sc->counters;
+  ap.sched = reinterpret_cast<unsigned*>(sc->counters + rows_heads);
   ap.err = sc->err;
   const int cap = attn_max_grid(dtype, head_dim, G, batch);
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   int grid = static_cast<int>(std::min<long long>(cap, units));
   if (cta_budget > 0) grid = std::min(grid, cta_budget);
-  NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false));
+  // seq_lens are on the device: the queue variant whenever the rows could hold enough units
+  // (it falls back to the fixed deal itself when they do not)
+  const bool queue = units >= static_cast<long long>(kAttnQueueUnits) * grid;
+  NS_CUDA(launch_attn(ap, dtype, head_dim, G, grid, reinterpret_cast<cudaStream_t>(stream), false,
+                      queue));
   return NS_OK;
 }
 

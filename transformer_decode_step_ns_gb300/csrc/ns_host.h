@@ -27,8 +27,11 @@ bool attn_supported(int head_dim, int group, int block_size);
 int attn_max_grid(int dtype, int head_dim, int group, int batch);  // one full wave
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, int group,
                            cudaStream_t s, bool pdl);
+// queue: launch the variant that may hand out units from p.sched (it does so when the rows hold
+// at least kAttnQueueUnits units per CTA); false compiles the fixed deal alone.  Both give the
+// same bits.
 cudaError_t launch_attn(const AttnParams& p, int dtype, int head_dim, int group, int grid,
-                        cudaStream_t s, bool pdl);
+                        cudaStream_t s, bool pdl, bool queue);
 
 cudaError_t launch_embed(const EmbedParams& p, int dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* out,

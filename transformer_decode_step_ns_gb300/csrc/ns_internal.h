@@ -19,6 +19,11 @@ constexpr int kAttnSuperBlocks = 64;  // decode attention: rows split into super
 constexpr int kAttnMaxChunks = 64;    // superchunks per row (seq_len <= 65536 with 16-token blocks)
 constexpr int kAttnWarpBlocks = 16;   // block ids one warp holds per superchunk (64 / 4 warps at
                                       // most; 8 at head_dim 64)
+// Decode attention units (row, kv head, superchunk) per CTA from which a launch hands out its
+// later units from a global queue, longest superchunks first, instead of a fixed deal (measured
+// on the paged attention benchmark: at 4-6 units per CTA the two tie, at 1-3 the fixed deal is
+// 8-14 % faster, from 10 the queue is 4-7 % faster).
+constexpr int kAttnQueueUnits = 6;
 constexpr int kMaxRows = 4096;
 
 enum EpiMode : int {
@@ -93,6 +98,9 @@ struct AttnParams {
   float* partials;         // per (row, kv head), attn_slot_floats apart (16-byte aligned):
                            // [max_chunks][G][head_dim] accumulators, then [max_chunks][G][2] (m, l)
   int* counters;           // [rows][n_kv_heads], zero between launches
+  // the attention unit queue's ticket counter: zero at launch, and zero again when the launch
+  // has taken its last ticket.  Launches that may run at the same time use different words.
+  unsigned* sched;
   int* err;
   // Device word, read before the dependency wait: nonzero when no block a row reads, other than
   // its last, receives a token in this step, so those blocks may be fetched while the previous

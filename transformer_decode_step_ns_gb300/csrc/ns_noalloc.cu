@@ -123,9 +123,9 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
   const int max_chunks = attn_max_chunks(max_blocks_per_seq * block_size);
   const size_t rows_heads = static_cast<size_t>(batch) * n_kv_heads;
   const size_t partial_bytes = rows_heads * attn_slot_floats(max_chunks, G, head_dim) * sizeof(float);
-  if (partial_bytes > kNoAllocPartialBytes || rows_heads > kNoAllocCounters) {
+  if (partial_bytes > kNoAllocPartialBytes || rows_heads + 1 > kNoAllocCounters) {
     set_last_error(("ns_attn_decode_noalloc: request needs " + std::to_string(partial_bytes) +
-                    " bytes of partials and " + std::to_string(rows_heads) +
+                    " bytes of partials and " + std::to_string(rows_heads + 1) +
                     " counters; the fixed scratch holds " + std::to_string(kNoAllocPartialBytes) +
                     " bytes and " + std::to_string(kNoAllocCounters) +
                     " counters (reduce batch, kv heads or max_blocks_per_seq)").c_str());
@@ -140,8 +140,9 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
   if (st != NS_OK) return st;
   int* counters = reinterpret_cast<int*>(base + kNoAllocPartialBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The counters must start at zero; a call that ended early could have left them dirty.
-  cudaError_t e = cudaMemsetAsync(counters, 0, rows_heads * sizeof(int), s);
+  // The counters (per (row, kv head), then the unit queue's) must start at zero; a call that
+  // ended early could have left them dirty.
+  cudaError_t e = cudaMemsetAsync(counters, 0, (rows_heads + 1) * sizeof(int), s);
   if (e != cudaSuccess) {
     set_last_error((std::string("ns_attn_decode_noalloc: ") + cudaGetErrorString(e)).c_str());
     return NS_ERR_CUDA;
@@ -165,11 +166,14 @@ extern "C" ns_status ns_attn_decode_noalloc(const void* q, const void* k_pool, c
   ap.max_chunks = max_chunks;
   ap.partials = reinterpret_cast<float*>(base);
   ap.counters = counters;
+  ap.sched = reinterpret_cast<unsigned*>(counters + rows_heads);
   ap.err = dev_err;
   const long long units = static_cast<long long>(batch) * n_kv_heads * max_chunks;
   const int grid =
       static_cast<int>(std::min<long long>(attn_max_grid(dtype, head_dim, G, batch), units));
-  e = launch_attn(ap, dtype, head_dim, G, grid, s, false);
+  // seq_lens are on the device: the queue variant whenever the rows could hold enough units
+  e = launch_attn(ap, dtype, head_dim, G, grid, s, false,
+                  units >= static_cast<long long>(kAttnQueueUnits) * grid);
   if (e != cudaSuccess) {
     set_last_error((std::string("ns_attn_decode_noalloc: launch: ") + cudaGetErrorString(e)).c_str());
     return NS_ERR_CUDA;
