@@ -141,13 +141,15 @@ struct AttnShape {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G >= 1 && G <= 8, "group");
   // then the CTA's unit sequence (SEQ 64-bit entries; the next index to claim and three spare
-  // words); superchunk prefix over positions [batch + 1], lengths by row [batch], row of each
-  // position [batch]; scan scratch [NT]; sort bins [NK]
+  // words); superchunk prefix over positions [batch + 1], row of each position [batch], the
+  // warps' scan totals [NW], sort bins [NK].  The rows' lengths are read from seq_lens (it stays
+  // in L1) rather than kept here: at head_dim 128 and a group of 4, two CTAs then share an SM up
+  // to 665 rows.
   static constexpr int NK = kAttnSuperBlocks + 1;  // superchunk lengths 0 .. 64 (0: invalid row)
   static constexpr int SEQ = 16;
   static size_t smem_bytes(int batch) {
     return 1024 + OFF_IDS + NW * kAttnWarpBlocks * 4 +
-           static_cast<size_t>(3 * batch + 1 + NT + NK + 2 * SEQ + 4) * 4;
+           static_cast<size_t>(2 * batch + 1 + NW + NK + 2 * SEQ + 4) * 4;
   }
 };
 
@@ -199,10 +201,9 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   unsigned long long* seq = reinterpret_cast<unsigned long long*>(ids_all + S::NW * kAttnWarpBlocks);
   int* seq_claim = reinterpret_cast<int*>(seq + S::SEQ);         // next sequence index to claim
   int* pre = seq_claim + 4;                                      // superchunk prefix [batch + 1]
-  int* lens = pre + p.batch + 1;                                 // validated seq_lens [batch]
-  int* order = lens + p.batch;                                   // row of each position [batch]
-  int* tot = order + p.batch;                                    // warp totals of the scan [NT]
-  int* bins = tot + S::NT;                                       // [NK]
+  int* order = pre + p.batch + 1;                                // row of each position [batch]
+  int* tot = order + p.batch;                                    // warp totals of the scan [NW]
+  int* bins = tot + S::NW;                                       // [NK]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads, batch = p.batch;
   uint8_t* ring = smem + warp * S::RING;
@@ -220,11 +221,15 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   // row index (a stable counting sort): warp w ranks rows [w * wper, (w + 1) * wper), 32 at a
   // time; lanes holding the same length find each other with a match, and the warp's running
   // count per length (kept in the stage rings, free until the first copy) ranks them after its
-  // earlier rows.  lens stays indexed by row; order maps a position to its row.
+  // earlier rows; order maps a position to its row.
   static_assert(S::NW * S::NK * 4 <= S::NW * S::RING && S::NK <= 96, "sort scratch");
   int* cnt = reinterpret_cast<int*>(smem);  // [NW][NK] a warp's rows per length (queue only)
   if (Q)
     for (int i = tid; i < S::NW * S::NK; i += S::NT) cnt[i] = 0;
+  auto row_len = [&](int b) {  // the row's length, 0 when outside [1, mb * block_size]
+    const int L = __ldg(p.seq_lens + p.row0 + b);
+    return L >= 1 && L <= p.mb * p.block_size ? L : 0;
+  };
   auto block_scan = [&](int v) {  // inclusive over the warp; lane 31 leaves the warp's total
     int inc = v;
 #pragma unroll
@@ -239,11 +244,9 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
   const int lo_t = tid * per, hi_t = min(batch, lo_t + per);
   int run = 0;
   for (int b = lo_t; b < hi_t; ++b) {
-    const int L0 = p.seq_lens[p.row0 + b];
-    const bool ok = L0 >= 1 && L0 <= p.mb * p.block_size;
-    if (!ok) set_err(p.err, NS_DEV_BAD_LENGTH);
-    lens[b] = ok ? L0 : 0;
-    run += ok ? attn_num_chunks(L0) : 0;
+    const int L0 = row_len(b);
+    if (L0 == 0) set_err(p.err, NS_DEV_BAD_LENGTH);
+    run += L0 > 0 ? attn_num_chunks(L0) : 0;
   }
   int inc = block_scan(run);
   __syncthreads();
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
       const int b = b0 + lane;
       const unsigned act = __ballot_sync(0xffffffffu, b < hi);
       if (b < hi) {
-        const int key = attn_chunk_blocks(lens[b]);
+        const int key = attn_chunk_blocks(row_len(b));
         const unsigned same = __match_any_sync(act, key);
         const int before = __popc(same & ((1u << lane) - 1u));
         pre[b] = wc[key] + before;  // rank among this warp's rows of the same length
@@ -309,14 +312,14 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
     for (int b0 = lo; b0 < hi; b0 += 32) {
       const int b = b0 + lane;
       if (b < hi) {
-        const int key = attn_chunk_blocks(lens[b]);
+        const int key = attn_chunk_blocks(row_len(b));
         order[bins[key] + wc[key] + pre[b]] = b;
       }
     }
     __syncthreads();
     // the superchunk counts again, now over positions
     run = 0;
-    for (int i = lo_t; i < hi_t; ++i) run += attn_num_chunks(lens[order[i]]);
+    for (int i = lo_t; i < hi_t; ++i) run += attn_num_chunks(row_len(order[i]));
     inc = block_scan(run);
     __syncthreads();
     before_warp = 0;
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
     int acc = before_warp + inc - run;
     for (int i = lo_t; i < hi_t; ++i) {
       pre[i] = acc;
-      acc += attn_num_chunks(lens[queue ? order[i] : i]);
+      acc += attn_num_chunks(row_len(queue ? order[i] : i));
     }
     if (tid == S::NT - 1) pre[batch] = acc;
     __syncthreads();
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
     }
     x.b = queue ? order[lo] : lo;
     x.sc = cg - pre[lo];
-    x.L = lens[x.b];
+    x.L = row_len(x.b);
     x.nchunks = attn_num_chunks(x.L);
     const int cb = attn_chunk_blocks(x.L);
     x.blk0 = x.sc * cb;
