@@ -464,7 +464,10 @@ ns_status ns_greedy_argmax(const float* logits, int batch, int vocab, int32_t* o
                            ns_stream_t stream);
 
 /* Read and clear the device error word of the handle (NULL handle = the word used by the
- * handle-free calls on the current device).  Synchronises the device. */
+ * handle-free calls on the current device).  Synchronises the device.  After
+ * NS_DEV_WAIT_TIMEOUT it also clears the attention kernel's counters (split-K arrivals and the
+ * unit queue's tickets) of the handle or of the handle-free calls, which a kernel that gave up
+ * a wait may have left set; the allocation-free call clears its own before every launch. */
 ns_status ns_get_device_error(ns_handle h, int* code);
 
 /* Step statistics: kernels launched per step and per graph, graph count, last capture ms. */

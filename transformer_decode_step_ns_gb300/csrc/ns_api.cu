@@ -1860,17 +1860,29 @@ ns_status ns_get_step_info(ns_handle h, ns_step_info* out) {
 ns_status ns_get_device_error(ns_handle h, int* code) {
   if (code == nullptr) return fail(NS_ERR_INVALID_ARG, "null argument");
   int* word = nullptr;
+  int* counters = nullptr;  // attention counters a wait that ran out may have left set
+  size_t n_counters = 0;
   if (h != nullptr) {
     NS_CUDA(cudaSetDevice(h->dev));
     word = h->err;
+    if (h->attn_counters != nullptr) {
+      counters = h->attn_counters;
+      n_counters = static_cast<size_t>(h->R) * h->cfg.n_kv_heads + h->R;
+    }
   } else {
     DevScratch* sc = nullptr;
     NS_TRY(scratch_get(0, 0, &sc));
     word = sc->err;
+    counters = sc->counters;
+    n_counters = sc->n_counters;
   }
   NS_CUDA(cudaDeviceSynchronize());
   NS_CUDA(cudaMemcpy(code, word, sizeof(int), cudaMemcpyDeviceToHost));
   NS_CUDA(cudaMemset(word, 0, sizeof(int)));
+  // a kernel that gave up a wait may not have brought its split-K arrival counters or its unit
+  // queue's ticket counter back to zero; no kernel runs now, so clear them for the next launch
+  if (*code == NS_DEV_WAIT_TIMEOUT && counters != nullptr && n_counters > 0)
+    NS_CUDA(cudaMemset(counters, 0, n_counters * sizeof(int)));
   return NS_OK;
 }
 
