@@ -715,6 +715,14 @@ __global__ void __launch_bounds__(AttnShape<D, G>::NT, AttnShape<D, G>::NW == 8 
 
 // ------------------------------------------------------------------------------ host side
 
+}  // namespace ns
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+namespace ns {
+
 namespace {
 
 template <typename T, int D, int G, bool Q>
@@ -761,11 +769,22 @@ cudaError_t dispatch_q(const AttnParams& p, int group, int grid, cudaStream_t s,
                : dispatch_g<T, D, false>(p, group, grid, s, pdl);
 }
 
+// One full wave of the kernel for `batch` rows on the current device: SMs x resident CTAs per
+// SM, asked of the occupancy API once per (device, shared memory size) and kept.
 template <typename T, int D, int G>
 int max_grid_t(int batch) {
   using S = AttnShape<D, G>;
-  int dev = 0, sms = 1, per_sm = 0;
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, int> cache;
+  int dev = 0;
   cudaGetDevice(&dev);
+  const auto key = std::make_pair(dev, S::smem_bytes(batch));
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int sms = 1, per_sm = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // both variants: the same block size, shared memory and register bound
   int per_sm_q = 0;
@@ -779,6 +798,8 @@ int max_grid_t(int batch) {
                                                     S::NT, S::smem_bytes(batch)) != cudaSuccess)
     per_sm = per_sm_q = 1;
   per_sm = std::max(1, std::min(per_sm, per_sm_q));
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = sms * per_sm;
   return sms * per_sm;
 }
 
