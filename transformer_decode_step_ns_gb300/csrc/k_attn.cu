@@ -10,16 +10,19 @@
 //   most 64 blocks (1024 tokens); the split is a function of the row's length alone, so a row's
 //   result never depends on the rest of the batch.  A CTA takes a unit; its warps (8 at
 //   head_dim 64, else 4) take contiguous shares of the superchunk and merge through shared
-//   memory (a superchunk of fewer blocks than warps gives the extra warps a copy of a block to
-//   fetch and leaves them out of the merge, so no warp's share is empty).
+//   memory.
 // * A CTA's first unit is its index.  When the launch holds at least kAttnQueueUnits units per
 //   CTA, later units are handed out by a global counter as CTAs need them, rows with the
 //   longest superchunks first (a stable counting sort that every CTA computes alike, so a unit
 //   index names the same work everywhere): with a fixed round-robin deal the last CTA finished
 //   12-16 % after the median one.  Below that the fixed deal over the rows in their own order
-//   stays: its CTAs c and c + grid/2, which share an SM, take units c, c + grid/2, c + grid, ...
-//   so every SM gets the same number, while a queue can hand both CTAs of one SM a second unit
-//   and leave another SM with none.  Which CTA computes a unit does not change its result.
+//   stays: CTA c takes units c, c + grid, c + 2 grid, ..., and since CTAs c and c + grid/2
+//   share an SM, every SM gets the same number of units, while a queue can hand both CTAs of
+//   one SM a second unit and leave another SM with none.  The two schedules are two compiled
+//   variants (the queue's code slows the fixed deal's loop even unused); the host picks one.
+//   Which CTA computes a unit does not change its result.  In the queue variant a superchunk of
+//   fewer blocks than warps gives the extra warps a copy of a block to fetch and the empty
+//   share's state to merge, so every warp streams every unit; the fixed deal skips such units.
 // * Every warp streams its blocks (running ahead into its share of the CTA's next unit) through
 //   a private ring of stages; each stage holds one 16 x d K tile and one V tile, copied with
 //   16-byte cp.async by all 32 lanes (each tile is one contiguous run, so every warp request is a
