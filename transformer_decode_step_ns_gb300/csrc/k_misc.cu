@@ -106,19 +106,38 @@ __device__ __forceinline__ void argmax_merge(float& best, int& bi, float ov, int
   }
 }
 
-__global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int vocab,
-                                                      int32_t* out) {
-  __shared__ float sv[32];
-  __shared__ int si[32];
+constexpr int kArgmaxThreads = 256;
+
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_kernel(const float* logits, int vocab,
+                                                                int32_t* out) {
+  __shared__ float sv[kArgmaxThreads / 32];
+  __shared__ int si[kArgmaxThreads / 32];
   const int row = blockIdx.y;
   const int rank = static_cast<int>(cluster_ctarank());
-  const int per = (vocab + kArgmaxSplit - 1) / kArgmaxSplit;
-  const int lo = rank * per, hi = min(vocab, lo + per);
   const float* r = logits + static_cast<size_t>(row) * vocab;
   float best = -INFINITY;
   int bi = 0x7fffffff;
+  if ((vocab & 3) == 0) {
+    // rows start on 16 bytes: 16-byte loads over slices of whole float4s
+    const int n4 = vocab >> 2;
+    const int per4 = (n4 + kArgmaxSplit - 1) / kArgmaxSplit;
+    const int lo4 = rank * per4, hi4 = min(n4, lo4 + per4);
+    const float4* r4 = reinterpret_cast<const float4*>(r);
 #pragma unroll 4
-  for (int i = lo + static_cast<int>(threadIdx.x); i < hi; i += blockDim.x) argmax_merge(best, bi, r[i], i);
+    for (int i = lo4 + static_cast<int>(threadIdx.x); i < hi4; i += blockDim.x) {
+      const float4 v = __ldg(r4 + i);
+      argmax_merge(best, bi, v.x, 4 * i);
+      argmax_merge(best, bi, v.y, 4 * i + 1);
+      argmax_merge(best, bi, v.z, 4 * i + 2);
+      argmax_merge(best, bi, v.w, 4 * i + 3);
+    }
+  } else {
+    const int per = (vocab + kArgmaxSplit - 1) / kArgmaxSplit;
+    const int lo = rank * per, hi = min(vocab, lo + per);
+#pragma unroll 4
+    for (int i = lo + static_cast<int>(threadIdx.x); i < hi; i += blockDim.x)
+      argmax_merge(best, bi, r[i], i);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
     argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
@@ -235,7 +254,7 @@ cudaError_t launch_argmax(const float* logits, int batch, int vocab, int32_t* ou
                           cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kArgmaxSplit, batch, 1);
-  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
