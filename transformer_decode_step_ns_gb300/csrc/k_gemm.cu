@@ -42,13 +42,31 @@ struct Cvt;
 template <>
 struct Cvt<__half> {
   static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+  static __device__ __forceinline__ uint32_t bits(float x) { return __half_as_ushort(from_f(x)); }
 };
 template <>
 struct Cvt<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from_f(float x) {
     return __float2bfloat16_rn(x);
   }
+  static __device__ __forceinline__ uint32_t bits(float x) {
+    return __bfloat16_as_ushort(from_f(x));
+  }
 };
+
+// four values rounded to the storage type, in memory order, for one 8-byte store
+template <typename T>
+__device__ __forceinline__ uint2 pack4(float4 v) {
+  return make_uint2(Cvt<T>::bits(v.x) | (Cvt<T>::bits(v.y) << 16),
+                    Cvt<T>::bits(v.z) | (Cvt<T>::bits(v.w) << 16));
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 
 constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
 constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
@@ -125,9 +143,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
   const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int n_own = m_valid > rank ? (m_valid - rank + S - 1) / S : 0;  // owned tokens
   const bool two_pass = gemm_two_pass(BN);
+  // the QKV epilogue stages its q/k columns' RoPE rows in the ring when they fit behind the tile
+  const bool qkv_staged =
+      p.epi == EPI_QKV && !two_pass && n0 < p.e.q_dim + p.e.kv_dim &&
+      static_cast<size_t>(n_own) * 8 * (p.e.head_dim >> 1) + static_cast<size_t>(BN) * kGemmTileN * 4 <=
+          static_cast<size_t>(p.nstage) * stage_bytes;
   // epilogue prefetch registers (first kPf iterations of each epilogue thread)
   float pf_a[kPf] = {}, pf_b[kPf] = {};
-  long long pf_s[kPf] = {};
   const uint32_t tmem = *tmem_slot;
   // Dependents may be scheduled once every CTA holds its TMEM (so none of them can starve us).
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -187,39 +209,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // ------------------------------------------------------------------ epilogue warps
     // Everything the epilogue reads besides the accumulator is loaded while the main loop
     // runs: the RMSNorm scale of each owned token, and (for the first kPf iterations of each
-    // thread) the RoPE cos/sin and cache slots or the residual values.  Loads are issued
-    // before any of their results is used, so they cost one memory round trip.
+    // thread) the residual values.  Loads are issued before any of their results is used, so
+    // they cost one memory round trip.  The QKV epilogue copies its RoPE rows into the ring as
+    // soon as the accumulator is complete (below).
     const EpiArgs& e = p.e;
     const int et = threadIdx.x - 64;  // 0..127
     const int ew = warp - 2;
-    const bool qk_cols = n0 < e.q_dim + e.kv_dim;
     // inputs fixed before the step starts (metadata, weights)
-    if (p.epi == EPI_QKV) {
-#pragma unroll
-      for (int u = 0; u < kPf; ++u) {
-        const int idx = et + 128 * u;
-        if (qk_cols) {
-          if (idx < n_own * 64 && n0 >= e.q_dim) pf_s[u] = e.slot_mapping[tok0 + rank + S * (idx >> 6)];
-        } else if (idx < n_own * kGemmTileN) {
-          pf_s[u] = e.slot_mapping[tok0 + rank + S * (idx >> 7)];
-        }
-      }
-    } else if (p.epi == EPI_RESID) {
-      pf_b[0] = e.gamma_next[n0 + et];
-    }
+    if (p.epi == EPI_RESID) pf_b[0] = e.gamma_next[n0 + et];
     griddep_wait();  // the previous kernel wrote the rest and may still read our outputs
-    if (p.epi == EPI_QKV && qk_cols) {
-      const int half = e.head_dim >> 1;
-#pragma unroll
-      for (int u = 0; u < kPf; ++u) {
-        const int idx = et + 128 * u;
-        if (idx < n_own * 64) {
-          const size_t o = static_cast<size_t>(tok0 + rank + S * (idx >> 6)) * half + (idx & 63) % half;
-          pf_a[u] = e.rope_cos[o];
-          pf_b[u] = e.rope_sin[o];
-        }
-      }
-    } else if (p.epi == EPI_RESID) {
+    if (p.epi == EPI_RESID) {
 #pragma unroll
       for (int u = 0; u < kPf; ++u) {
         const int idx = et + 128 * u;
@@ -269,6 +268,21 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       set_err(p.err, NS_DEV_WAIT_TIMEOUT);
     }
     float* tile = reinterpret_cast<float*>(smem);
+    // The RoPE cos/sin rows of the owned tokens go into the ring behind the staged tile (every
+    // MMA has completed, so the ring is free); they land while the tile is read out of TMEM and
+    // reduced across the cluster.  [owned token][cos half | sin half] fp32.
+    if (ok && !*abort_flag && qkv_staged) {
+      const int half = e.head_dim >> 1, pieces = half >> 1;  // 16-byte pieces per token
+      const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(BN) * kGemmTileN * 4;
+      for (int idx = et; idx < n_own * pieces; idx += 128) {
+        const int k = idx / pieces, pc = idx - k * pieces;
+        const bool is_cos = pc < (pieces >> 1);
+        const float* src = (is_cos ? e.rope_cos : e.rope_sin) +
+                           static_cast<size_t>(tok0 + rank + S * k) * half +
+                           4 * (is_cos ? pc : pc - (pieces >> 1));
+        cp_async_16(base + static_cast<uint32_t>((k * 2 * half + 4 * pc) * 4), src);
+      }
+    }
     const int nchunk = (m_valid + 15) >> 4;
     if (ok && !*abort_flag && !two_pass) {
       for (int c = 0; c < nchunk; ++c) {
@@ -336,7 +350,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     };
     if (!two_pass) {
       if (run && S > 1) reduce(0, n_own, 0);
-      named_barrier_sync(1, 128);  // reduced rows and the RMSNorm scales are in shared memory
+      if (qkv_staged) cp_async_commit_wait_all();  // this thread's RoPE rows have landed
+      named_barrier_sync(1, 128);  // reduced rows, RMSNorm scales and RoPE rows are in shared memory
       if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
     }
     const EpiArgs& e = p.e;
@@ -390,108 +405,80 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             out[static_cast<size_t>(tok0 + j) * e.ldo + n0 + r] = v;
           }
         } else if (p.epi == EPI_QKV) {
+          // A warp takes whole owned tokens (the pass's k = ew, ew + 4, ...); lane l holds
+          // features 4l .. 4l + 3 of the tile.  The RoPE partners (i, i + d/2) of a head sit
+          // half/4 lanes apart and swap values by shuffles; a token costs one 16-byte read of
+          // the tile, of cos and of sin, one 8-byte store, and one cache address per lane.
+          // Each element gets the formulas of the persistent kernel's epilogue.
           const int d = e.head_dim, half = d >> 1;
-          T* qo = reinterpret_cast<T*>(e.q_out);
-          T* kp = reinterpret_cast<T*>(e.k_pool);
-          T* vp = reinterpret_cast<T*>(e.v_pool);
-          auto kv_base = [&](long long slot, int kvh) {
-            return ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) * e.block_size +
-                    static_cast<size_t>(slot % e.block_size)) * d;
-          };
-          if (n0 < e.q_dim + e.kv_dim) {
-            // q and k columns: RoPE pairs (i, i + d/2) of each head
-            auto qk = [&](int idx, float c, float sn, long long slot) {
-              const int j = tok_of(idx >> 6), pr = idx & 63;
-              const int hl = pr / half, i = pr - hl * half;
-              const int r_lo = hl * d + i, r_hi = r_lo + half;
-              const int tok = tok0 + j;
-              const float sc = scaled ? rs_s[j] : 1.f;
-              const float x_lo = tile[j * kGemmTileN + r_lo] * sc;
-              const float x_hi = tile[j * kGemmTileN + r_hi] * sc;
-              const float y_lo = rope_lo(x_lo, x_hi, c, sn);
-              const float y_hi = rope_hi(x_lo, x_hi, c, sn);
-              if (n0 < e.q_dim) {
-                T* dst = qo + static_cast<size_t>(tok) * e.q_dim + n0;
-                dst[r_lo] = Cvt<T>::from_f(y_lo);
-                dst[r_hi] = Cvt<T>::from_f(y_hi);
+          const bool is_q = n0 < e.q_dim;
+          const bool is_k = !is_q && n0 < e.q_dim + e.kv_dim;
+          const bool rope = is_q || is_k;
+          const int f0 = 4 * lane;
+          const int fd = f0 % d;  // feature within its head
+          const bool low = fd < half;
+          const int i0 = low ? fd : fd - half;  // RoPE pair of the lane's first feature
+          const int plane = half >> 2;          // lanes between partners
+          const int col = n0 - e.q_dim - (is_k || is_q ? 0 : e.kv_dim) + f0;  // within K or V
+          const int kvh = col / d, dim = col - kvh * d;
+          const float* staged = reinterpret_cast<const float*>(smem + static_cast<size_t>(BN) * kGemmTileN * 4);
+          for (int kk0 = ew; kk0 < jn; kk0 += 128) {
+            // lane t holds the cache slot of the warp's token kk0 + 4t
+            long long my_slot = 0;
+            if (!is_q && kk0 + 4 * lane < jn) my_slot = e.slot_mapping[tok0 + tok_of(kk0 + 4 * lane)];
+            for (int t = 0; t < 32; ++t) {
+              const int kk = kk0 + 4 * t;
+              if (kk >= jn) break;
+              const int j = tok_of(kk), tok = tok0 + j;
+              float4 x = *reinterpret_cast<const float4*>(&tile[j * kGemmTileN + f0]);
+              if (scaled) {
+                const float sc = rs_s[j];
+                x.x *= sc;
+                x.y *= sc;
+                x.z *= sc;
+                x.w *= sc;
+              }
+              if (rope) {
+                float4 c, sn;
+                if (qkv_staged) {
+                  const float* row = staged + static_cast<size_t>(k_lo + kk) * 2 * half;
+                  c = *reinterpret_cast<const float4*>(row + i0);
+                  sn = *reinterpret_cast<const float4*>(row + half + i0);
+                } else {
+                  const size_t o = static_cast<size_t>(tok) * half + i0;
+                  c = *reinterpret_cast<const float4*>(e.rope_cos + o);
+                  sn = *reinterpret_cast<const float4*>(e.rope_sin + o);
+                }
+                const float4 xp = make_float4(__shfl_xor_sync(0xffffffffu, x.x, plane),
+                                              __shfl_xor_sync(0xffffffffu, x.y, plane),
+                                              __shfl_xor_sync(0xffffffffu, x.z, plane),
+                                              __shfl_xor_sync(0xffffffffu, x.w, plane));
+                if (low) {
+                  x = make_float4(rope_lo(x.x, xp.x, c.x, sn.x), rope_lo(x.y, xp.y, c.y, sn.y),
+                                  rope_lo(x.z, xp.z, c.z, sn.z), rope_lo(x.w, xp.w, c.w, sn.w));
+                } else {
+                  x = make_float4(rope_hi(xp.x, x.x, c.x, sn.x), rope_hi(xp.y, x.y, c.y, sn.y),
+                                  rope_hi(xp.z, x.z, c.z, sn.z), rope_hi(xp.w, x.w, c.w, sn.w));
+                }
+              }
+              const uint2 v4 = pack4<T>(x);
+              if (is_q) {
+                *reinterpret_cast<uint2*>(reinterpret_cast<T*>(e.q_out) +
+                                          static_cast<size_t>(tok) * e.q_dim + n0 + f0) = v4;
               } else {
+                const long long slot = __shfl_sync(0xffffffffu, my_slot, t);
                 if (slot < 0 || slot >= e.pool_slots) {
-                  set_err(p.err, NS_DEV_BAD_SLOT);
-                  return;
+                  if (lane == 0) set_err(p.err, NS_DEV_BAD_SLOT);
+                  continue;
                 }
-                const size_t base = kv_base(slot, (n0 - e.q_dim + r_lo) / d);
-                const T k_lo = Cvt<T>::from_f(y_lo), k_hi = Cvt<T>::from_f(y_hi);
-                kp[base + i] = k_lo;
-                kp[base + i + half] = k_hi;
-                if (e.kv_stage != nullptr) {
-                  T* st = reinterpret_cast<T*>(e.kv_stage) + static_cast<size_t>(tok) * 2 * e.kv_dim +
-                          (n0 - e.q_dim);
-                  st[r_lo] = k_lo;
-                  st[r_hi] = k_hi;
-                }
-              }
-            };
-            if (use_pf) {
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = et + 128 * u;
-                if (idx < jn * 64) qk(idx, pf_a[u], pf_b[u], pf_s[u]);
-              }
-            }
-            // the rest in chunks of kPf, each chunk's loads issued before its stores
-            for (int b0 = start; b0 < jn * 64; b0 += 128 * kPf) {
-              float ca[kPf], cb[kPf];
-              long long cs[kPf];
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = b0 + 128 * u;
-                if (idx < jn * 64) {
-                  const int tok = tok0 + tok_of(idx >> 6);
-                  const size_t o = static_cast<size_t>(tok) * half + (idx & 63) % half;
-                  ca[u] = e.rope_cos[o];
-                  cb[u] = e.rope_sin[o];
-                  cs[u] = n0 >= e.q_dim ? e.slot_mapping[tok] : 0;
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = b0 + 128 * u;
-                if (idx < jn * 64) qk(idx, ca[u], cb[u], cs[u]);
-              }
-            }
-          } else {
-            // v columns
-            auto vv = [&](int idx, long long slot) {
-              const int j = tok_of(idx >> 7), r = idx & 127;
-              const int col = n0 - e.q_dim - e.kv_dim + r;
-              const int kvh = col / d, dim = col - kvh * d;
-              if (slot < 0 || slot >= e.pool_slots) {
-                set_err(p.err, NS_DEV_BAD_SLOT);
-                return;
-              }
-              const T v = Cvt<T>::from_f(tile[j * kGemmTileN + r] * (scaled ? rs_s[j] : 1.f));
-              vp[kv_base(slot, kvh) + dim] = v;
-              if (e.kv_stage != nullptr)
-                reinterpret_cast<T*>(e.kv_stage)[static_cast<size_t>(tok0 + j) * 2 * e.kv_dim + e.kv_dim + col] = v;
-            };
-            if (use_pf) {
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = et + 128 * u;
-                if (idx < jn * kGemmTileN) vv(idx, pf_s[u]);
-              }
-            }
-            for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
-              long long cs[kPf];
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = b0 + 128 * u;
-                if (idx < jn * kGemmTileN) cs[u] = e.slot_mapping[tok0 + tok_of(idx >> 7)];
-              }
-#pragma unroll
-              for (int u = 0; u < kPf; ++u) {
-                const int idx = b0 + 128 * u;
-                if (idx < jn * kGemmTileN) vv(idx, cs[u]);
+                T* pool = reinterpret_cast<T*>(is_k ? e.k_pool : e.v_pool);
+                const size_t base = ((static_cast<size_t>(slot / e.block_size) * e.n_kv_heads + kvh) *
+                                         e.block_size + static_cast<size_t>(slot % e.block_size)) * d;
+                *reinterpret_cast<uint2*>(pool + base + dim) = v4;
+                if (e.kv_stage != nullptr)
+                  *reinterpret_cast<uint2*>(reinterpret_cast<T*>(e.kv_stage) +
+                                            static_cast<size_t>(tok) * 2 * e.kv_dim +
+                                            (is_k ? 0 : e.kv_dim) + col) = v4;
               }
             }
           }
