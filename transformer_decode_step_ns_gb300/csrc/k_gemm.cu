@@ -70,7 +70,6 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 
 constexpr uint32_t kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KiB weight tile per stage
 constexpr int kCtrlBytes = 2048;                            // barriers, flags, rs[256]
-constexpr int kPf = 6;  // epilogue iterations per thread whose inputs are loaded early
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -148,8 +147,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       p.epi == EPI_QKV && !two_pass && n0 < p.e.q_dim + p.e.kv_dim &&
       static_cast<size_t>(n_own) * 8 * (p.e.head_dim >> 1) + static_cast<size_t>(BN) * kGemmTileN * 4 <=
           static_cast<size_t>(p.nstage) * stage_bytes;
-  // epilogue prefetch registers (first kPf iterations of each epilogue thread)
-  float pf_a[kPf] = {}, pf_b[kPf] = {};
+  // the residual epilogue stages the old residual rows of its owned tokens the same way
+  const size_t tile_bytes = static_cast<size_t>(two_pass ? kPassRows : BN) * kGemmTileN * 4;
+  const bool resid_staged =
+      p.epi == EPI_RESID && static_cast<size_t>(n_own) * kGemmTileN * 4 + tile_bytes <=
+                                static_cast<size_t>(p.nstage) * stage_bytes;
+  // the residual epilogue's next-norm gains for the lane's four features (loaded early)
+  float4 gam4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint32_t tmem = *tmem_slot;
   // Dependents may be scheduled once every CTA holds its TMEM (so none of them can starve us).
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -207,25 +211,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue warps
-    // Everything the epilogue reads besides the accumulator is loaded while the main loop
-    // runs: the RMSNorm scale of each owned token, and (for the first kPf iterations of each
-    // thread) the residual values.  Loads are issued before any of their results is used, so
-    // they cost one memory round trip.  The QKV epilogue copies its RoPE rows into the ring as
-    // soon as the accumulator is complete (below).
+    // What the epilogue reads besides the accumulator is loaded while the main loop runs (the
+    // RMSNorm scale of each owned token, the next norm's gains) or copied into the ring as soon
+    // as the accumulator is complete (the QKV epilogue's RoPE rows, the residual epilogue's old
+    // residual rows), where it lands during the TMEM read-out and the split-K reduction.
     const EpiArgs& e = p.e;
     const int et = threadIdx.x - 64;  // 0..127
     const int ew = warp - 2;
     // inputs fixed before the step starts (metadata, weights)
-    if (p.epi == EPI_RESID) pf_b[0] = e.gamma_next[n0 + et];
+    if (p.epi == EPI_RESID) gam4 = *reinterpret_cast<const float4*>(e.gamma_next + n0 + 4 * lane);
     griddep_wait();  // the previous kernel wrote the rest and may still read our outputs
-    if (p.epi == EPI_RESID) {
-#pragma unroll
-      for (int u = 0; u < kPf; ++u) {
-        const int idx = et + 128 * u;
-        if (idx < n_own * kGemmTileN)
-          pf_a[u] = e.resid[static_cast<size_t>(tok0 + rank + S * (idx >> 7)) * e.resid_dim + n0 + et];
-      }
-    }
     if (e.sumsq_in != nullptr) {
       // rs[j] = rsqrt(sum of the row's per-tile partial sums / H + eps): one warp per token,
       // lanes over the partials, a fixed shuffle tree (the order depends on H only)
@@ -271,6 +266,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // The RoPE cos/sin rows of the owned tokens go into the ring behind the staged tile (every
     // MMA has completed, so the ring is free); they land while the tile is read out of TMEM and
     // reduced across the cluster.  [owned token][cos half | sin half] fp32.
+    if (ok && !*abort_flag && resid_staged) {
+      const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(tile_bytes);
+      for (int idx = et; idx < n_own * (kGemmTileN / 4); idx += 128) {
+        const int k = idx >> 5, pc = idx & 31;
+        cp_async_16(base + static_cast<uint32_t>((k * kGemmTileN + 4 * pc) * 4),
+                    e.resid + static_cast<size_t>(tok0 + rank + S * k) * e.resid_dim + n0 + 4 * pc);
+      }
+    }
     if (ok && !*abort_flag && qkv_staged) {
       const int half = e.head_dim >> 1, pieces = half >> 1;  // 16-byte pieces per token
       const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(BN) * kGemmTileN * 4;
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     };
     if (!two_pass) {
       if (run && S > 1) reduce(0, n_own, 0);
-      if (qkv_staged) cp_async_commit_wait_all();  // this thread's RoPE rows have landed
+      if (qkv_staged || resid_staged) cp_async_commit_wait_all();  // this thread's rows landed
       named_barrier_sync(1, 128);  // reduced rows, RMSNorm scales and RoPE rows are in shared memory
       if (S > 1) cluster_arrive();  // this CTA's remote reads are complete
     }
@@ -378,6 +381,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             for (int i = 0; i < 16; ++i) tbase[(c * 16 + i) * kGemmTileN + frow] = __uint_as_float(r[i]);
           }
         }
+        if (resid_staged && pass == 0) cp_async_commit_wait_all();  // this thread's rows landed
         named_barrier_sync(1, 128);
         if (S > 1) {
           cluster_sync();
@@ -389,8 +393,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       if (run) {
         // tile[j * 128 + r] addresses the staged row of token j of this pass
         float* tile = tbase - static_cast<ptrdiff_t>(lo) * kGemmTileN;
-        const bool use_pf = pass == 0;  // the prefetched registers hold pass 0's first chunk
-        const int start = use_pf ? et + 128 * kPf : et;
         auto tok_of = [&](int k) { return rank + S * (k_lo + k); };  // k-th owned token of the pass
         if (p.epi == EPI_F32) {
           float* out = e.out_f32;
@@ -484,36 +486,24 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           }
           // q and the cache are read by ordinary loads and cp.async (no async-proxy fence)
         } else if (p.epi == EPI_RESID) {
+          // A warp takes whole owned tokens; lane l holds features 4l .. 4l + 3: the new
+          // residual, the next norm's input and the square that the per-token sum below reads.
           T* xo = reinterpret_cast<T*>(e.xn_out);
-          const float gam = pf_b[0];
-          auto rs_row = [&](int idx, float old) {
-            const int j = tok_of(idx >> 7), r = idx & 127;
-            const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + r;
-            const float rn = old + tile[j * kGemmTileN + r];
-            e.resid[gi] = rn;
-            xo[gi] = Cvt<T>::from_f(rn * gam);
-            tile[j * kGemmTileN + r] = rn * rn;
-          };
-          if (use_pf) {
-#pragma unroll
-            for (int u = 0; u < kPf; ++u) {
-              const int idx = et + 128 * u;
-              if (idx < jn * kGemmTileN) rs_row(idx, pf_a[u]);
-            }
-          }
-          for (int b0 = start; b0 < jn * kGemmTileN; b0 += 128 * kPf) {
-            float cr[kPf];
-#pragma unroll
-            for (int u = 0; u < kPf; ++u) {
-              const int idx = b0 + 128 * u;
-              if (idx < jn * kGemmTileN)
-                cr[u] = e.resid[static_cast<size_t>(tok0 + tok_of(idx >> 7)) * e.resid_dim + n0 + et];
-            }
-#pragma unroll
-            for (int u = 0; u < kPf; ++u) {
-              const int idx = b0 + 128 * u;
-              if (idx < jn * kGemmTileN) rs_row(idx, cr[u]);
-            }
+          const int f0 = 4 * lane;
+          const float* staged = reinterpret_cast<const float*>(smem + tile_bytes);
+          for (int kk = ew; kk < jn; kk += 4) {
+            const int j = tok_of(kk);
+            const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + f0;
+            float4* tp = reinterpret_cast<float4*>(&tile[j * kGemmTileN + f0]);
+            const float4 x = *tp;
+            const float4 old =
+                resid_staged ? *reinterpret_cast<const float4*>(staged + static_cast<size_t>(k_lo + kk) * kGemmTileN + f0)
+                             : *reinterpret_cast<const float4*>(e.resid + gi);
+            const float4 rn = make_float4(old.x + x.x, old.y + x.y, old.z + x.z, old.w + x.w);
+            *reinterpret_cast<float4*>(e.resid + gi) = rn;
+            *reinterpret_cast<uint2*>(xo + gi) =
+                pack4<T>(make_float4(rn.x * gam4.x, rn.y * gam4.y, rn.z * gam4.z, rn.w * gam4.w));
+            *tp = make_float4(rn.x * rn.x, rn.y * rn.y, rn.z * rn.z, rn.w * rn.w);
           }
           named_barrier_sync(1, 128);
           for (int k = ew; k < jn; k += 4) {
@@ -526,15 +516,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           }
           fence_proxy_async_global();
         } else if (p.epi == EPI_SWIGLU) {
+          // a warp takes whole owned tokens; lane l makes outputs 2l and 2l + 1 of the tile's 64
+          // (gate rows 0-63, up rows 64-127)
           T* ao = reinterpret_cast<T*>(e.act_out);
           const int f0 = tile_n * 64;
-          for (int idx = et; idx < jn * 64; idx += 128) {
-            const int j = tok_of(idx >> 6), c = idx & 63;
+          for (int kk = ew; kk < jn; kk += 4) {
+            const int j = tok_of(kk);
             const float sc = scaled ? rs_s[j] : 1.f;
-            const float g = tile[j * kGemmTileN + c] * sc;
-            const float u = tile[j * kGemmTileN + 64 + c] * sc;
-            const float a = silu_mul(g, u);
-            ao[static_cast<size_t>(tok0 + j) * e.ffn + f0 + c] = Cvt<T>::from_f(a);
+            const float2 g = *reinterpret_cast<const float2*>(&tile[j * kGemmTileN + 2 * lane]);
+            const float2 u = *reinterpret_cast<const float2*>(&tile[j * kGemmTileN + 64 + 2 * lane]);
+            const float a0 = silu_mul(g.x * sc, u.x * sc), a1 = silu_mul(g.y * sc, u.y * sc);
+            *reinterpret_cast<uint32_t*>(ao + static_cast<size_t>(tok0 + j) * e.ffn + f0 + 2 * lane) =
+                Cvt<T>::bits(a0) | (Cvt<T>::bits(a1) << 16);
           }
           fence_proxy_async_global();
         }
