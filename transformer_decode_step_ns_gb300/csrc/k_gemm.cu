@@ -428,9 +428,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             // lane t holds the cache slot of the warp's token kk0 + 4t
             long long my_slot = 0;
             if (!is_q && kk0 + 4 * lane < jn) my_slot = e.slot_mapping[tok0 + tok_of(kk0 + 4 * lane)];
-            for (int t = 0; t < 32; ++t) {
+            const int nt = min(32, (jn - kk0 + 3) >> 2);  // the warp's tokens in this batch
+#pragma unroll 2
+            for (int t = 0; t < nt; ++t) {
               const int kk = kk0 + 4 * t;
-              if (kk >= jn) break;
               const int j = tok_of(kk), tok = tok0 + j;
               float4 x = *reinterpret_cast<const float4*>(&tile[j * kGemmTileN + f0]);
               if (scaled) {
@@ -491,6 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           T* xo = reinterpret_cast<T*>(e.xn_out);
           const int f0 = 4 * lane;
           const float* staged = reinterpret_cast<const float*>(smem + tile_bytes);
+#pragma unroll 4
           for (int kk = ew; kk < jn; kk += 4) {
             const int j = tok_of(kk);
             const size_t gi = static_cast<size_t>(tok0 + j) * e.resid_dim + n0 + f0;
@@ -520,6 +522,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           // (gate rows 0-63, up rows 64-127)
           T* ao = reinterpret_cast<T*>(e.act_out);
           const int f0 = tile_n * 64;
+#pragma unroll 4
           for (int kk = ew; kk < jn; kk += 4) {
             const int j = tok_of(kk);
             const float sc = scaled ? rs_s[j] : 1.f;
