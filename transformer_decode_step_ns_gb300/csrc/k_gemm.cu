@@ -924,7 +924,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
             named_barrier_sync(1, 128);
-          } else {
+          } else if (p.epi == EPI_QKV) {
             // v columns
             T* vp = reinterpret_cast<T*>(e.v_pool);
             const int col = n0 - e.q_dim - e.kv_dim + f;
